@@ -1,0 +1,456 @@
+"""Pins of the CPU oracle against what the pages and the mathematics fix.
+
+Each test ties an oracle function to something other than itself: the page's
+worked example, a closed form, a library routine on a special case, brute
+force on a tiny input, or an invariant of the method. They run without a GPU.
+"""
+import dataclasses
+import math
+import os
+
+import numpy as np
+import pytest
+
+import dflash_inputs as di
+from oracle import dflash_oracle as O
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+# ------------------------------------------------------------------ four-bit matrices
+
+def _pack(q: np.ndarray) -> np.ndarray:
+    """Codes -7..7 [rows][cols] -> interchange bytes (test-side packer, by the format's text)."""
+    u = (q + 8).astype(np.uint8)
+    return (u[:, 0::2] | (u[:, 1::2] << 4)).astype(np.uint8)
+
+
+def test_dequant_hand_group():
+    # byte 0x19: low nibble 9 -> +1 at the even column, high nibble 1 -> -7 at the odd one
+    codes = np.array([[0x19, 0x8F]], dtype=np.uint8)
+    scales = np.array([[0.5]], dtype=np.float16)
+    w = O.dequant_int4(codes, scales, 4)
+    assert w.tolist() == [[0.5, -3.5, 3.5, 0.0]]
+
+
+def test_dequant_roundtrip_exact():
+    rng = np.random.default_rng(1)
+    rows, cols, group = 37, 256, 32
+    q = rng.integers(-7, 8, size=(rows, cols))
+    # every group holds a code of magnitude 7, so its scale is recovered exactly
+    for r in range(rows):
+        for g0 in range(0, cols, group):
+            q[r, g0 + rng.integers(0, group)] = 7 * (1 if rng.random() < 0.5 else -1)
+    scales = (rng.random((rows, cols // group)) * 0.1 + 1e-3).astype(np.float16)
+    codes = _pack(q)
+    w = O.dequant_int4(codes, scales, group)
+    c2, s2 = di.quantize_int4(w.astype(np.float32), group)
+    assert np.array_equal(c2, codes)
+    assert np.array_equal(s2.view(np.uint16), scales.view(np.uint16))
+
+
+def test_dequant_zero_group():
+    codes, scales = di.quantize_int4(np.zeros((2, 64), np.float32), 32)
+    assert np.all(O.dequant_int4(codes, scales, 32) == 0.0)
+    assert np.all(codes == 0x88)
+
+
+def test_int4_matmul_brute_force():
+    rng = np.random.default_rng(2)
+    rows, cols, group, n = 5, 64, 16, 3
+    q = rng.integers(-7, 8, size=(rows, cols))
+    scales = (rng.random((rows, cols // group)) + 0.1).astype(np.float16)
+    m = di.Int4(codes=_pack(q), scales=scales, rows=rows, cols=cols, group=group)
+    x = rng.standard_normal((n, cols))
+    y = O.int4_matmul(m, x)
+    for i in range(n):
+        for r in range(rows):
+            acc = 0.0
+            for c in range(cols):
+                acc += float(q[r, c]) * float(scales[r, c // group]) * x[i, c]
+            assert abs(y[i, r] - acc) <= 1e-12 * max(1.0, abs(acc))
+    # a slab of rows
+    assert np.allclose(O.int4_matmul(m, x, 1, 4), y[:, 1:4], rtol=0, atol=1e-13)
+
+
+def test_int4_single_code_gives_scale_times_x():
+    q = np.zeros((3, 32), dtype=np.int64)
+    q[1, 5] = 1
+    scales = np.full((3, 1), 0.375, dtype=np.float16)
+    m = di.Int4(codes=_pack(q), scales=scales, rows=3, cols=32, group=32)
+    x = np.arange(32, dtype=np.float64)[None, :] * 0.25
+    y = O.int4_matmul(m, x)
+    assert y.tolist() == [[0.0, 0.375 * 5 * 0.25, 0.0]]
+
+
+def test_f16_matmul_rounds_activations_to_f16():
+    w = np.array([[1.0, 1.0]], dtype=np.float16)
+    x = np.array([[1.0 + 2.0 ** -12, 3.0]])          # 1 + 2^-12 rounds to 1 in f16
+    assert O.f16_matmul(w, x).tolist() == [[4.0]]
+    rng = np.random.default_rng(3)
+    w = rng.standard_normal((4, 24)).astype(np.float16)
+    x = rng.standard_normal((2, 24))
+    ref = [[sum(float(np.float16(x[i, c])) * float(w[r, c]) for c in range(24)) for r in range(4)] for i in range(2)]
+    assert np.allclose(O.f16_matmul(w, x), ref, rtol=0, atol=1e-12)
+
+
+# ------------------------------------------------------------------ norms and rotation
+
+def test_rms_constant_row_closed_form():
+    w = np.array([1.0, 2.0, -0.5, 3.0])
+    for c, eps in [(2.0, 0.0), (-0.3, 1e-6), (1e-4, 1e-6)]:
+        y = O.rms(np.full(4, c), w, eps)
+        assert np.allclose(y, c / math.sqrt(c * c + eps) * w, rtol=1e-14, atol=0)
+
+
+def test_rms_unit_mean_square_and_scale_invariance():
+    rng = np.random.default_rng(4)
+    x = rng.standard_normal((3, 64))
+    y = O.rms(x, np.ones(64), 0.0)
+    assert np.allclose((y * y).mean(axis=1), 1.0, rtol=1e-13)
+    assert np.allclose(O.rms(-7.5 * x, np.ones(64), 0.0), -y, rtol=1e-13)
+    # per head: a [rows][heads*hd] input normalises each run of hd alone
+    z = O.rms(x.reshape(3, 64), np.ones(16), 0.0).reshape(3, 4, 16)
+    assert np.allclose((z * z).mean(axis=2), 1.0, rtol=1e-13)
+
+
+def test_inv_freq_closed_form():
+    inv = O.inv_freq(128, 1e6)
+    assert inv.dtype == np.float32 and len(inv) == 64
+    assert inv[0] == 1.0
+    assert inv[32] == np.float32(1e-3)          # theta^(-64/128) = 1e6^-0.5
+    assert inv[16] == np.float32(10 ** -1.5)
+
+
+def test_rotate_is_complex_multiplication_on_half_split_pairs():
+    inv = np.array([1.0, 0.25], dtype=np.float32)     # head_dim 4
+    x = np.array([[1.0, 2.0, 3.0, -1.0]])
+    p = 3
+    y = O.rotate(x, 1, [p], inv)
+    for i, f in enumerate(inv):
+        ang = float(np.float32(p) * f)
+        z = complex(x[0, i], x[0, i + 2]) * complex(math.cos(ang), math.sin(ang))
+        assert abs(y[0, i] - z.real) < 1e-14 and abs(y[0, i + 2] - z.imag) < 1e-14
+    # the pair is (i, i + hd/2): a unit vector in slot 0 turns into slot 2, not slot 1
+    e = O.rotate(np.array([[1.0, 0.0, 0.0, 0.0]]), 1, [p], inv)
+    assert abs(e[0, 1]) == 0.0 and abs(e[0, 2] - math.sin(3.0)) < 1e-15
+
+
+def test_rotate_position_zero_identity_norms_and_relative_position():
+    rng = np.random.default_rng(5)
+    inv = O.inv_freq(64, 1e6)
+    x = rng.standard_normal((2, 3 * 64))
+    assert np.array_equal(O.rotate(x, 3, [0, 0], inv), x)
+    y = O.rotate(x, 3, [7, 1000], inv)
+    pairs = lambda v: v.reshape(2, 3, 2, 32)
+    assert np.allclose((pairs(y) ** 2).sum(2), (pairs(x) ** 2).sum(2), rtol=1e-13)
+    q, k = rng.standard_normal((1, 64)), rng.standard_normal((1, 64))
+    d0 = (O.rotate(q, 1, [10], inv) * O.rotate(k, 1, [3], inv)).sum()
+    d1 = (O.rotate(q, 1, [110], inv) * O.rotate(k, 1, [103], inv)).sum()
+    assert abs(d0 - d1) < 1e-5 * (np.abs(q).sum() * np.abs(k).sum()) ** 0.5
+
+
+# ------------------------------------------------------------------ row convolution
+
+def _base(kn, hs, rng):
+    return rng.standard_normal((2, kn, hs))
+
+
+def test_conv_identity_kernel():
+    rng = np.random.default_rng(6)
+    x = rng.standard_normal((5, 8))
+    base = np.zeros((2, 1, 8)); base[:, 0, :] = 1.0
+    d = np.zeros((5, 2 * 1 * 2))
+    for stage in (0, 1):
+        assert np.array_equal(O.conv(base, d, x, stage, 1, 4), x)
+
+
+def test_conv_static_kernel_is_causal_fir():
+    rng = np.random.default_rng(7)
+    rows, hs, kn = 9, 12, 4
+    x = rng.standard_normal((rows, hs))
+    base = _base(kn, hs, rng)
+    d = np.zeros((rows, 2 * kn * (hs // 3)))
+    for stage in (0, 1):
+        y = O.conv(base, d, x, stage, kn, 3)
+        for i in range(hs):
+            ref = np.convolve(x[:, i], base[stage, :, i])[:rows]
+            assert np.allclose(y[:, i], ref, rtol=0, atol=1e-13)
+
+
+def test_conv_dynamic_term_reaches_only_its_group_row_and_offset():
+    rng = np.random.default_rng(8)
+    rows, hs, kn, gs = 6, 8, 3, 2
+    groups = hs // gs
+    x = rng.standard_normal((rows, hs))
+    base = np.zeros((2, kn, hs))
+    d = np.zeros((rows, 2, kn, groups))
+    r, stage, o, g = 4, 1, 2, 3
+    d[r, stage, o, g] = 0.5
+    y = O.conv(base, d.reshape(rows, -1), x, stage, kn, gs)
+    want = np.zeros((rows, hs))
+    want[r, g * gs:(g + 1) * gs] = 0.5 * x[r - o, g * gs:(g + 1) * gs]
+    assert np.array_equal(y, want)
+    # the other stage does not see it
+    assert np.all(O.conv(base, d.reshape(rows, -1), x, 0, kn, gs) == 0)
+
+
+def test_conv_row_zero_sees_only_itself():
+    rng = np.random.default_rng(9)
+    x = rng.standard_normal((4, 6)); x2 = x.copy(); x2[1:] = rng.standard_normal((3, 6))
+    base = _base(4, 6, rng); d = rng.standard_normal((4, 2 * 4 * 3))
+    assert np.array_equal(O.conv(base, d, x, 0, 4, 2)[0], O.conv(base, d, x2, 0, 4, 2)[0])
+
+
+# ------------------------------------------------------------------ attention
+
+def _softmax_attention_brute(q, keys, vals, scale):
+    out = []
+    for qi in q:
+        s = [scale * sum(a * b for a, b in zip(qi, k)) for k in keys]
+        m = max(s)
+        e = [math.exp(v - m) for v in s]
+        z = sum(e)
+        out.append([sum(e[j] * vals[j][c] for j in range(len(keys))) / z for c in range(len(vals[0]))])
+    return np.array(out)
+
+
+def test_attention_without_context_is_plain_softmax_attention():
+    rng = np.random.default_rng(10)
+    rows, hd = 4, 6
+    q, k, v = (rng.standard_normal((rows, hd)) for _ in range(3))
+    empty = np.zeros((0, 1, hd))
+    y = O.attention(q, k, v, empty, empty, 0, 0, 0, 1, 1, hd, 0.4)
+    assert np.allclose(y, _softmax_attention_brute(q, k, v, 0.4), rtol=0, atol=1e-13)
+
+
+def test_attention_one_key_returns_its_value():
+    rng = np.random.default_rng(11)
+    v = rng.standard_normal((1, 8))
+    empty = np.zeros((0, 1, 8))
+    y = O.attention(rng.standard_normal((1, 8)), rng.standard_normal((1, 8)), v, empty, empty, 0, 5, 0, 1, 1, 8, 1.0)
+    assert np.allclose(y, v, rtol=0, atol=1e-15)
+
+
+def test_attention_gqa_maps_contiguous_heads():
+    rows, hd, nh, kv = 2, 4, 4, 2
+    q = np.zeros((rows, nh * hd))
+    k = np.zeros((rows, kv * hd))
+    v = np.concatenate([np.zeros((rows, hd)), np.ones((rows, hd))], axis=1)
+    empty = np.zeros((0, kv, hd))
+    y = O.attention(q, k, v, empty, empty, 0, 0, 0, nh, kv, hd, 1.0).reshape(rows, nh, hd)
+    assert np.all(y[:, :2] == 0.0) and np.all(y[:, 2:] == 1.0)
+
+
+def test_attention_window_mask_uniform_weights_closed_form():
+    # zero queries: every visible key weighs the same, so y is the mean of the visible values
+    hd, rows, n, lo, anchor, window = 2, 3, 10, 20, 30, 6
+    ck = np.zeros((n, 1, hd))
+    cv = np.zeros((n, 1, hd))
+    for j in range(n):
+        cv[j, 0, :] = lo + j                # value = its position
+    blk_v = np.full((rows, hd), 100.0)
+    y = O.attention(np.zeros((rows, hd)), np.zeros((rows, hd)), blk_v, ck, cv, lo, anchor, window, 1, 1, hd, 1.0)
+    for r in range(rows):
+        first = anchor + r + 1 - window     # the row sees context positions >= first
+        vis = [p for p in range(lo, lo + n) if p >= first]
+        want = (sum(vis) + 100.0 * rows) / (len(vis) + rows)
+        assert np.allclose(y[r], want, rtol=1e-14)
+
+
+def test_attention_window_zero_equals_a_covering_window():
+    rng = np.random.default_rng(12)
+    rows, hd, n, anchor = 3, 4, 7, 7
+    args = [rng.standard_normal((rows, 2 * hd)), rng.standard_normal((rows, hd)), rng.standard_normal((rows, hd)),
+            rng.standard_normal((n, 1, hd)), rng.standard_normal((n, 1, hd))]
+    y0 = O.attention(*args, 0, anchor, 0, 2, 1, hd, 0.5)
+    y1 = O.attention(*args, 0, anchor, anchor + rows, 2, 1, hd, 0.5)
+    assert np.array_equal(y0, y1)
+
+
+def test_attention_block_rows_permutation_equivariant():
+    rng = np.random.default_rng(13)
+    rows, hd, n = 6, 4, 5
+    q, k, v = rng.standard_normal((rows, 2 * hd)), rng.standard_normal((rows, hd)), rng.standard_normal((rows, hd))
+    ck, cv = rng.standard_normal((n, 1, hd)), rng.standard_normal((n, 1, hd))
+    perm = np.concatenate([[0], 1 + rng.permutation(rows - 1)])
+    y = O.attention(q, k, v, ck, cv, 0, n, 0, 2, 1, hd, 0.5)
+    yp = O.attention(q[perm], k[perm], v[perm], ck, cv, 0, n, 0, 2, 1, hd, 0.5)
+    assert np.allclose(yp, y[perm], rtol=0, atol=1e-14)
+
+
+def test_context_range_cases():
+    assert O.context_range(0, 100, 100, 0) == (0, 100)
+    assert O.context_range(0, 100, 100, 10) == (91, 100)          # row 0 sees 91..99
+    assert O.context_range(0, 100, 60, 0) == (0, 60)              # nothing at or after the anchor
+    assert O.context_range(50, 10, 55, 100) == (50, 55)
+    assert O.context_range(50, 10, 40, 0) == (50, 50)             # anchor before the context: empty
+    assert O.context_range(0, 5, 5, 2) == (4, 5)
+
+
+# ------------------------------------------------------------------ top-k and the selector
+
+def _golden_top_k():
+    lines = [l.split() for l in open(os.path.join(GOLDEN, "top_k_worked_example.txt")) if l.strip() and not l.startswith("#")]
+    x = np.array([float(v) for v in lines[0][1:]])
+    cases = []
+    for l in lines[1:]:
+        k = int(l[1])
+        exp = [(float(p.split(":")[0]), int(p.split(":")[1])) for p in l[3:]]
+        cases.append((k, exp))
+    return x, cases
+
+
+def test_top_k_worked_example_of_the_page():
+    x, cases = _golden_top_k()
+    for k, exp in cases:
+        assert [(float(v), i) for v, i in O.top_k(x, k)] == exp
+
+
+def _top_k_insertion(x, k):
+    """Insertion into a sorted list, as the page's top_k describes it in words."""
+    best = []
+    for i, v in enumerate(x):
+        if len(best) == k and v <= best[-1][0]:
+            continue
+        at = 0
+        while at < len(best) and best[at][0] >= v:
+            at += 1
+        best.insert(at, (v, i))
+        del best[k:]
+    return best
+
+
+def test_top_k_brute_force_with_ties():
+    rng = np.random.default_rng(14)
+    for trial in range(200):
+        n = int(rng.integers(1, 40))
+        x = rng.integers(-3, 4, size=n).astype(np.float64) * 0.5
+        k = int(rng.integers(1, n + 1))
+        got = [(float(v), i) for v, i in O.top_k(x, k)]
+        assert got == [(float(v), i) for v, i in _top_k_insertion(list(x), k)]
+
+
+def _books(V, rank, rng, zero=False):
+    if zero:
+        return np.zeros((V, rank), np.float16), np.zeros((V, rank), np.float16)
+    return rng.standard_normal((V, rank)).astype(np.float16), rng.standard_normal((V, rank)).astype(np.float16)
+
+
+def test_select_without_codebooks_picks_the_plain_token():
+    rng = np.random.default_rng(15)
+    logits = rng.standard_normal((5, 50))
+    hp = rng.standard_normal((5, 8))
+    P, C = _books(50, 8, rng, zero=True)
+    chosen, plain = O.select_with(hp, logits, 3, P, C, 6)
+    assert chosen == plain == [int(np.argmax(r)) for r in logits]
+    P, C = _books(50, 8, rng)
+    chosen, plain = O.select_with(hp, logits, 3, P, C, 1)
+    assert chosen == plain
+
+
+def test_select_brute_force_over_the_vocabulary():
+    rng = np.random.default_rng(16)
+    V, rank, top, n = 30, 4, 5, 6
+    for trial in range(20):
+        logits = rng.standard_normal((n, V))
+        hp = rng.standard_normal((n, rank))
+        P, C = _books(V, rank, rng)
+        anchor = int(rng.integers(0, V))
+        chosen, _ = O.select_with(hp, logits, anchor, P, C, top)
+        prev = anchor
+        for j in range(n):
+            allscores = logits[j] + (P[prev].astype(np.float64) * hp[j]) @ C.astype(np.float64).T
+            order = sorted(range(V), key=lambda t: (-logits[j][t], t))[:top]
+            best = max(order, key=lambda t: (allscores[t], -order.index(t)))
+            assert chosen[j] == best
+            prev = best
+
+
+# ------------------------------------------------------------------ whole-pass invariants (tiny shapes)
+
+def _tiny(**over):
+    g = dataclasses.replace(di.workload("tiny").geometry, **over)
+    return g, di.make_weights(g, 0)
+
+
+def test_block_mask_rows_enter_identical():
+    g, w = _tiny()
+    o = O.Oracle(g, w)
+    o.settle(0, di.make_taps(g, 0, 20))
+    tr = {}
+    o.block(20, di.block_rows(g, 0, 5), tr)
+    L0 = tr["layers"][0]
+    assert np.array_equal(L0["x"][1], L0["x"][7]) and np.array_equal(L0["ad"][2], L0["ad"][15])
+    assert not np.array_equal(L0["xc"][1], L0["xc"][7]) or g.conv_kernel == 1
+
+
+def test_block_window_zero_equals_covering_window():
+    g, w = _tiny(windows=(0,))
+    g2 = dataclasses.replace(g, windows=(64,))
+    taps = di.make_taps(g, 0, 40)
+    h = di.block_rows(g, 0, 9)
+    a, b = O.Oracle(g, w), O.Oracle(g2, w)
+    a.settle(0, taps); b.settle(0, taps)
+    assert np.array_equal(a.block(40, h), b.block(40, h))
+    # a window shorter than the context changes the result
+    c = O.Oracle(dataclasses.replace(g, windows=(8,)), w)
+    c.settle(0, taps)
+    assert not np.allclose(a.block(40, h), c.block(40, h))
+
+
+def test_block_no_rope_layer_is_position_invariant():
+    g, w = _tiny(no_rope=(0,))
+    taps = di.make_taps(g, 0, 24)
+    h = di.block_rows(g, 0, 11)
+    a, b = O.Oracle(g, w), O.Oracle(g, w)
+    a.settle(0, taps)
+    b.reset(first=1000); b.settle(1000, taps)
+    assert np.allclose(a.block(24, h), b.block(1024, h), rtol=0, atol=1e-12)
+    # with rotation the positions matter
+    g2, _ = _tiny()
+    c, d = O.Oracle(g2, w), O.Oracle(g2, w)
+    c.settle(0, taps); d.reset(first=1000); d.settle(1000, taps)
+    assert not np.allclose(c.block(24, h), d.block(1024, h), rtol=0, atol=1e-6)
+
+
+def test_block_with_empty_context():
+    g, w = _tiny()
+    o = O.Oracle(g, w)
+    hn = o.block(0, di.block_rows(g, 0, 3))
+    assert hn.shape == (g.block, g.hidden) and np.all(np.isfinite(hn))
+
+
+def test_settle_rows_are_independent_and_values_position_free():
+    g, w = _tiny()
+    taps = di.make_taps(g, 0, 12)
+    a = O.Oracle(g, w)
+    a.settle(0, taps)
+    b = O.Oracle(g, w)
+    b.settle(0, taps[:5]); b.settle(5, taps[5:])
+    assert np.allclose(a.ctx_k[0], b.ctx_k[0], rtol=0, atol=1e-13)
+    _, kv0 = a.settle_rows(0, taps[:3])
+    _, kv9 = a.settle_rows(100, taps[:3])
+    assert np.array_equal(kv0[0][1], kv9[0][1])                      # V has no position
+    inv = O.inv_freq(g.head_dim, g.rope_theta)
+    # row 0 sits at position 0, where the rotation is the identity
+    k_at_100 = O.rotate(kv0[0][0][:1].reshape(1, -1), g.kv_heads, [100], inv)
+    assert np.allclose(kv9[0][0][:1].reshape(1, -1), k_at_100, rtol=0, atol=1e-13)
+
+
+def test_settle_replaces_rows_from_pos_on():
+    g, w = _tiny()
+    taps = di.make_taps(g, 0, 10)
+    other = di.make_taps(g, 1, 4)
+    a = O.Oracle(g, w)
+    a.settle(0, taps)
+    a.settle(6, other)
+    b = O.Oracle(g, w)
+    b.settle(0, np.concatenate([taps[:6], other]))
+    assert a.len == 10 and np.allclose(a.ctx_k[0], b.ctx_k[0], rtol=0, atol=1e-13)
+
+
+def test_inputs_are_seeded():
+    g = di.workload("tiny").geometry
+    assert np.array_equal(di.make_taps(g, 3, 70)[64:], di.make_taps(g, 3, 6, start=64))
+    assert not np.array_equal(di.make_taps(g, 3, 4), di.make_taps(g, 4, 4))
