@@ -1,0 +1,449 @@
+#!/usr/bin/env python
+"""Throughput of the DFlash 2 drafter pass on GB300.
+
+One step = one pass of the whole hot path over one batch of synthetic input:
+reset, settle of the workload's context (256-row calls), the block, and the
+selector (for the batched workload the contexts are settled once before the
+timed region and a step is one block per sequence plus the selector).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl gb300|reference]
+
+Prints one JSON line (rank 0). Under torchrun every rank runs its own replica
+on its own GPU (no data-path collective); the value is the sum over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import dflash_inputs as di  # noqa: E402
+
+METRIC = "DFlash2 draft blocks/s and settle rows/s on 1 GB300; % of HBM roofline"
+DEFAULT_WORKLOAD = "qwen3-0.6b"
+L2_FLUSH_BYTES = 256 << 20
+REJECT = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown")
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=100)
+    p.add_argument("--warmup", type=int, default=10)
+    p.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(di.WORKLOADS))
+    p.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    p.add_argument("--no-graph", action="store_true", help="direct calls instead of a CUDA graph replay")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    return p.parse_args()
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            m = json.load(f)
+        return float(m["hbm_gbs"]), float(m["bf16_tflops"]), "measured"
+    except Exception:
+        return 6800.0, 1900.0, "fallback"
+
+
+# ------------------------------------------------------------------ clocks
+class Clocks:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu: int):
+        self.gpu = gpu
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-f", self.path], stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = []
+        try:
+            for line in open(self.path):
+                f = [x.strip() for x in line.split(",")]
+                if len(f) >= 9:
+                    rows.append(f)
+            os.unlink(self.path)
+        except Exception:
+            pass
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        sm, smax, power = [], [], []
+        for f in rows:
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+                power.append(float(f[3]))
+            except ValueError:
+                continue
+            for i, n in enumerate(names):
+                if f[5 + i].lower() == "active":
+                    reasons.add(n)
+        loaded = [s for s, p in zip(sm, power) if p > 0.3 * max(power)] if power else []
+        return {"sm_mhz": float(np.median(loaded or sm)) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ the GB300 arm
+class Bench:
+    def __init__(self, wl, device):
+        import torch
+        from speculative_block_drafter_gb300 import _lib
+        from speculative_block_drafter_gb300.drafter import Drafter, PackedMatrix
+        self.torch = torch
+        self.L = _lib
+        self.wl = wl
+        g = self.g = wl.geometry
+        self.dev = device
+        self.k = g.block - 1
+        self.width = wl.head_width
+        self.w = di.make_weights(g, wl.seed)
+        self.d = Drafter(g, self.w, max_batch=wl.batch, ctx_cap=wl.context + g.block)
+        B = wl.batch
+        self.taps_host = [di.make_taps(g, wl.seed + s, wl.context) for s in range(B)]
+        self.anchor_tok = [di.anchor_token(g, wl.seed + s) for s in range(B)]
+        self.h_host = np.stack([di.block_rows(g, wl.seed + s, self.anchor_tok[s]) for s in range(B)]).astype(np.float32)
+        self.taps = [torch.from_numpy(t).to(device) for t in self.taps_host]
+        self.h = torch.from_numpy(self.h_host).to(device).contiguous()
+        self.at = torch.tensor(self.anchor_tok, dtype=torch.int32, device=device)
+        self.anchors = [wl.context] * B
+        self.logits = torch.empty(B, self.k, self.width, dtype=torch.float32, device=device)
+        self.hp = torch.empty(B, self.k, g.selector_rank, dtype=torch.float32, device=device)
+        self.chosen = torch.empty(B, self.k, dtype=torch.int32, device=device)
+        self.plain = torch.empty(B, self.k, dtype=torch.int32, device=device)
+        self.flush_buf = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
+        self.settle_in_step = wl.batch == 1
+        if not self.settle_in_step:
+            self._settle_all()
+        self.head = PackedMatrix(self.w["head"], device=str(device))
+
+    def _settle_all(self):
+        for s in range(self.wl.batch):
+            self.d.reset(s, 0)
+            self.d.settle(s, 0, self.taps[s])
+
+    def step(self):
+        if self.settle_in_step:
+            self._settle_all()
+        self.d.block(self.anchors, self.h, self.k, self.width, out=(self.logits, self.hp))
+        self.d.select(self.logits, self.hp, self.at, out=(self.chosen, self.plain))
+
+    def flush(self):
+        self.flush_buf.zero_()
+
+    def timed(self, fn, steps, graph=None):
+        torch = self.torch
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        for i in range(steps):
+            self.flush()
+            evs[i][0].record()
+            if graph is not None:
+                graph.replay()
+            else:
+                fn()
+            evs[i][1].record()
+        torch.cuda.synchronize()
+        return [a.elapsed_time(b) for a, b in evs]
+
+    def capture(self):
+        torch = self.torch
+        c0 = self.L.dflash_launch_count()
+        self.step()
+        torch.cuda.synchronize()
+        per_step = self.L.dflash_launch_count() - c0
+        try:
+            graph = torch.cuda.CUDAGraph()
+            s = torch.cuda.Stream()
+            s.wait_stream(torch.cuda.current_stream())
+            with torch.cuda.stream(s):
+                with torch.cuda.graph(graph, stream=s):
+                    self.step()
+            torch.cuda.current_stream().wait_stream(s)
+            torch.cuda.synchronize()
+            return graph, per_step
+        except Exception as e:  # capture unsupported: time direct calls
+            sys.stderr.write(f"graph capture failed ({e}); timing direct calls\n")
+            return None, per_step
+
+    def roofline(self, steps, hbm_peak):
+        """The head GEMM (the int4 weight-streaming kernel at its largest shape), timed alone."""
+        torch = self.torch
+        g = self.g
+        x = torch.randn(self.wl.batch * self.k, g.hidden, device=self.dev, dtype=torch.float32)
+        self.head.matmul(x)
+        torch.cuda.synchronize()
+        ms = self.timed(lambda: self.head.matmul(x), steps)
+        t = float(np.mean(ms)) * 1e-3
+        rows = self.width
+        nbytes = (rows * g.hidden // 2 + rows * (g.hidden // g.quant_group) * 2
+                  + x.numel() * 4 + x.shape[0] * rows * 4)
+        achieved = nbytes / t / 1e9
+        traffic = None
+        try:
+            with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+                traffic = json.load(f).get(f"gemm_int4_head@{self.wl.name}")
+        except Exception:
+            pass
+        return {"kernel": "k_gemm<int4> (head, %d x %d, %d rows)" % (rows, g.hidden, x.shape[0]),
+                "bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
+                "frac": round(achieved / hbm_peak, 4), "traffic": traffic,
+                "algorithmic_bytes": int(nbytes), "ms_per_launch": round(t * 1e3, 5)}
+
+    def phases(self, steps):
+        torch = self.torch
+        out = {}
+        if self.settle_in_step:
+            ms = self.timed(self._settle_all, steps)
+            out["settle_rows_per_s"] = self.wl.context * self.wl.batch / (np.mean(ms) * 1e-3)
+            out["settle_ms"] = float(np.mean(ms))
+        ms = self.timed(lambda: self.d.block(self.anchors, self.h, self.k, self.width, out=(self.logits, self.hp)),
+                        steps)
+        out["block_ms"] = float(np.mean(ms))
+        out["blocks_per_s_block_only"] = self.wl.batch / (np.mean(ms) * 1e-3)
+        ms = self.timed(lambda: self.d.select(self.logits, self.hp, self.at, out=(self.chosen, self.plain)), steps)
+        out["select_ms"] = float(np.mean(ms))
+        return {k: (round(v, 4) if isinstance(v, float) else v) for k, v in out.items()}
+
+    def e2e(self, steps):
+        """Through the public API from pinned host memory: inputs in, tokens out, every step."""
+        torch = self.torch
+        taps_pin = [torch.from_numpy(t).pin_memory() for t in self.taps_host]
+        h_pin = torch.from_numpy(self.h_host).pin_memory()
+        at_pin = torch.tensor(self.anchor_tok, dtype=torch.int32).pin_memory()
+        out_pin = torch.empty(self.wl.batch, self.k, dtype=torch.int32).pin_memory()
+        taps_dev = [torch.empty_like(t, device=self.dev) for t in taps_pin]
+        h_dev = torch.empty_like(h_pin, device=self.dev)
+        at_dev = torch.empty_like(at_pin, device=self.dev)
+        h2d = (sum(t.numel() * 4 for t in taps_pin) if self.settle_in_step else 0) + h_pin.numel() * 4 + at_pin.numel() * 4
+        d2h = out_pin.numel() * 4
+
+        def one():
+            if self.settle_in_step:
+                for s in range(self.wl.batch):
+                    taps_dev[s].copy_(taps_pin[s], non_blocking=True)
+                    self.d.reset(s, 0)
+                    self.d.settle(s, 0, taps_dev[s])
+            h_dev.copy_(h_pin, non_blocking=True)
+            at_dev.copy_(at_pin, non_blocking=True)
+            self.d.block(self.anchors, h_dev, self.k, self.width, out=(self.logits, self.hp))
+            self.d.select(self.logits, self.hp, at_dev, out=(self.chosen, self.plain))
+            out_pin.copy_(self.chosen, non_blocking=True)
+            torch.cuda.current_stream().synchronize()
+
+        one()
+        times = []
+        for _ in range(steps):
+            self.flush()
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            one()
+            times.append(time.perf_counter() - t0)
+        return float(np.mean(times)), h2d, d2h
+
+
+def cpu_baseline(wl):
+    """The oracle as it stands on this host's cores, on a bounded sample of the workload."""
+    from oracle import dflash_oracle as O
+    g = wl.geometry
+    w = di.make_weights(g, wl.seed)
+    orc = O.Oracle(g, w)
+    a = di.anchor_token(g, wl.seed)
+    h = di.block_rows(g, wl.seed, a)
+    chunk = min(wl.context, 256)
+    taps = di.make_taps(g, wl.seed, chunk)
+    t0 = time.perf_counter()
+    orc.settle(0, taps)
+    t_chunk = time.perf_counter() - t0
+    # the block over a context of `chunk` rows stands in for the full context's (the
+    # context's attention is a small part of the oracle's block time)
+    t0 = time.perf_counter()
+    orc.draft(chunk, h, a)
+    t_block = time.perf_counter() - t0
+    nchunks = (wl.context + 255) // 256 if wl.batch == 1 else 0
+    step = nchunks * t_chunk + t_block * wl.batch
+    threads = os.cpu_count()
+    try:
+        from threadpoolctl import threadpool_info
+        threads = max([i.get("num_threads", 0) for i in threadpool_info()] + [1])
+    except Exception:
+        pass
+    sample = (f"one {chunk}-row settle chunk ({t_chunk:.2f} s) and one block + selector over {chunk} context rows "
+              f"({t_block:.2f} s), scaled to {nchunks} chunks + {wl.batch} block(s) per step")
+    return {"value": wl.batch / step, "unit": "blocks/s", "cores": threads, "kind": "oracle", "sample": sample}
+
+
+def run_gb300(args):
+    import torch
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    from speculative_block_drafter_gb300 import build, _lib
+    if rank == 0:
+        build.build()
+    if world > 1:
+        torch.distributed.barrier()
+    _lib.lib()
+    dev = torch.device("cuda", torch.cuda.current_device())
+    wl = di.workload(args.workload)
+    hbm_peak, _, peak_kind = peaks()
+    b = Bench(wl, dev)
+    for _ in range(args.warmup):
+        b.step()
+    torch.cuda.synchronize()
+    graph, launches = (None, None)
+    if args.no_graph:
+        c0 = _lib.dflash_launch_count()
+        b.step()
+        torch.cuda.synchronize()
+        launches = _lib.dflash_launch_count() - c0
+    else:
+        graph, launches = b.capture()
+        for _ in range(2):
+            graph.replay() if graph is not None else b.step()
+        torch.cuda.synchronize()
+
+    def measure():
+        clocks = Clocks(local)
+        clocks.start()
+        time.sleep(0.3)
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+        ms = b.timed(b.step, args.steps, graph)
+        torch.cuda.synchronize()
+        if world > 1:
+            torch.distributed.barrier()
+        return ms, clocks.stop()
+
+    ms, clocks = measure()
+    if any(r in clocks["reasons"] for r in REJECT):
+        ms, clocks = measure()
+        clocks["remeasured"] = True
+    step_ms = float(np.mean(ms))
+    if world > 1:
+        t = torch.tensor([step_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        step_ms = float(t.item())
+    units = wl.batch * world
+    value = units / (step_ms * 1e-3)
+    roof = b.roofline(max(5, min(args.steps, 50)), hbm_peak)
+    roof["peak_kind"] = f"{peak_kind} (HBM copy, MEASURED_PEAKS.json)" if peak_kind == "measured" else "fallback"
+    phases = b.phases(max(5, min(args.steps, 50)))
+    e2e_s, h2d, d2h = b.e2e(max(3, min(args.steps, 30)))
+    e2e_value = units / e2e_s
+    if world > 1:
+        t = torch.tensor([e2e_s], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_value = units / float(t.item())
+    out = {
+        "metric": METRIC, "value": round(value, 2), "unit": "blocks/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(step_ms, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": wl.name, "description": wl.description, "context": wl.context, "batch": wl.batch,
+                   "block": wl.geometry.block, "head_width": wl.head_width,
+                   "step": ("reset + settle(%d rows) + block + select" % wl.context) if b.settle_in_step
+                   else "one block per sequence + select (contexts settled before)",
+                   "l2": "flushed between steps (256 MiB write)", "graph": graph is not None,
+                   "parallelism": "replicas" if world > 1 else "single"},
+        "roofline": roof,
+        "phases": phases,
+        "e2e": {"value": round(e2e_value, 2), "unit": "blocks/s", "h2d_bytes_per_step": int(h2d),
+                "d2h_bytes_per_step": int(d2h)},
+        "gpu_launches": int(launches) * args.steps if launches is not None else None,
+        "clocks": clocks,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(wl)
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def run_reference(args):
+    """The oracle as it stands, timed on the host cores on the same workload and unit."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    wl = di.workload(args.workload)
+    from oracle import dflash_oracle as O
+    g = wl.geometry
+    w = di.make_weights(g, wl.seed)
+    a = di.anchor_token(g, wl.seed)
+    h = di.block_rows(g, wl.seed, a)
+    chunk = min(wl.context, 256)
+    taps = di.make_taps(g, wl.seed, chunk)
+    nchunks = (wl.context + 255) // 256 if wl.batch == 1 else 0
+
+    def sample():
+        orc = O.Oracle(g, w)
+        t0 = time.perf_counter()
+        orc.settle(0, taps)
+        t1 = time.perf_counter()
+        orc.draft(chunk, h, a)
+        t2 = time.perf_counter()
+        return nchunks * (t1 - t0) + wl.batch * (t2 - t1)
+
+    for _ in range(args.warmup):
+        sample()
+    times = [sample() for _ in range(args.steps)]
+    step = float(np.mean(times))
+    value = wl.batch / step
+    threads = os.cpu_count()
+    s = (f"per step: one {chunk}-row settle chunk scaled to {nchunks} chunks and {wl.batch} block(s) + selector "
+         f"over {chunk} context rows")
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "blocks/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": step * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": wl.name, "description": wl.description, "context": wl.context, "batch": wl.batch},
+        "cpu_baseline": {"value": value, "unit": "blocks/s", "cores": threads, "kind": "oracle", "sample": s},
+        "e2e": {"value": value, "unit": "blocks/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gb300(args)
+
+
+if __name__ == "__main__":
+    main()

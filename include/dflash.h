@@ -1,0 +1,187 @@
+/*
+ * dflash.h - C ABI of the GB300 (sm_103a) DFlash 2 drafter pass.
+ *
+ * The pass, as the cortiq-engine pages define it (src/cortiq_engine/dflash.rs,
+ * module doc and `Drafter`; src/gpu_cuda/hyb/dflash.rs, `Dev`):
+ *
+ *   settle   t   = rms(FC . f16(taps), hidden_norm)              per context row
+ *            K_l = rot(rms_head(Wk_l . t, k_norm_l)),  V_l = Wv_l . t   into the cache
+ *   block    rows [anchor, MASK, ...] at positions a, a+1, ...:
+ *            x = rms(h); d = Pr . f16(x); x = conv(stage 0, x, d); q, k, v = W . x;
+ *            per-head q/k norms and rotation; attention over the layer's windowed
+ *            context and the block's own rows (not causal); h += conv(stage 1, Wo . y, d);
+ *            the SwiGLU MLP wrapped the same way; hn = rms(h, norm)
+ *   head     logits[j] = Head[0:width] . hn[j],  hp[j] = S . f16(hn[j])   for rows j = 1..k
+ *   select   per row: top candidates re-scored in order, score = logit + (P[prev] * hp) . C[cand]
+ *
+ * Conventions for every call:
+ *  - Device pointers are plain CUDA device addresses; the caller owns all
+ *    device memory (weights, caches, workspace, inputs, outputs). The library
+ *    allocates no device memory and keeps only small host state.
+ *  - Calls that take a stream only enqueue work on it (no host synchronisation,
+ *    no device-to-host copy); they can be captured in a CUDA graph.
+ *  - Every call that can fail returns 0 on success or a DFLASH_E_* code, with a
+ *    thread-local message in dflash_last_error(). On failure nothing is enqueued
+ *    unless the code is DFLASH_E_CUDA (a launch failed after earlier launches).
+ *  - The library fails loudly: there is no host fallback of any step.
+ */
+#ifndef DFLASH_H
+#define DFLASH_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define DFLASH_MAX_LAYERS 64
+#define DFLASH_SETTLE_MAX 256     /* rows per settle call (gpu_cuda/hyb/dflash.rs, SETTLE_MAX) */
+#define DFLASH_MAX_BLOCK 16       /* rows of a block this build takes */
+
+enum {
+  DFLASH_OK = 0,
+  DFLASH_E_GEOMETRY = 1,   /* the geometry breaks a rule of Geometry::of or a limit of this build */
+  DFLASH_E_ARG = 2,        /* a bad argument: null or misaligned pointer, size out of range */
+  DFLASH_E_CAPACITY = 3,   /* the context cache or the workspace is too small */
+  DFLASH_E_CUDA = 4,       /* a CUDA call failed */
+  DFLASH_E_NOMEM = 5       /* a host allocation failed */
+};
+
+/* What a DFlash 2 checkpoint fixes (dflash.rs, `Geometry`). `windows[l]` is the
+ * positions a block row of layer l sees back, 0 = all; `no_rope[l]` = 1 for a
+ * layer without rotary position. `quant_group` is the four-bit group along the
+ * input dimension (32, 64 or 128). `conv_group` is channels per group of the
+ * row convolution (groups = hidden / conv_group). */
+typedef struct dflash_geometry {
+  int32_t hidden, intermediate, layers, heads, kv_heads, head_dim, vocab, block;
+  uint32_t mask_token;
+  int32_t conv_group, conv_kernel, selector_rank, selector_top, taps, quant_group;
+  int32_t windows[DFLASH_MAX_LAYERS];
+  uint8_t no_rope[DFLASH_MAX_LAYERS];
+  double rope_theta, eps;
+} dflash_geometry;
+
+/* A matrix in the library's packed layout (dflash_pack_int4 / dflash_pack_f16). */
+typedef struct dflash_matrix {
+  const void *data;      /* device; int4: tiles of codes; f16: tiles of values */
+  const void *scales;    /* device; int4 only: packed f16 scales; NULL for f16 */
+} dflash_matrix;
+
+/* One layer (dflash.rs `Layer`): f32 device vectors, packed matrices. */
+typedef struct dflash_layer_weights {
+  const float *in_norm, *post_norm;        /* [hidden] */
+  const float *q_norm, *k_norm;            /* [head_dim] */
+  const float *attn_base, *mlp_base;       /* [2][conv_kernel][hidden] */
+  dflash_matrix attn_proj, mlp_proj;       /* f16 [2*conv_kernel*groups][hidden] */
+  dflash_matrix q, k, v, o, gate, up, down;/* int4 [rows][cols] as in Drafter::new */
+} dflash_layer_weights;
+
+typedef struct dflash_weights {
+  dflash_matrix fc;                /* f16 [hidden][taps*hidden] */
+  const float *hidden_norm, *norm; /* [hidden] */
+  dflash_matrix sel;               /* f16 [selector_rank][hidden] */
+  const uint16_t *pred_book;       /* f16 [vocab][selector_rank], row-major, unpacked */
+  const uint16_t *succ_book;       /* f16 [vocab][selector_rank], row-major, unpacked */
+  dflash_matrix head;              /* int4 [vocab][hidden] (the target's head) */
+  const dflash_layer_weights *layers; /* host array of `layers` entries */
+} dflash_weights;
+
+typedef struct dflash_t dflash_t;
+
+/* ---- packing (the library's matrix layouts) -------------------------------- */
+
+/* Bytes of the packed codes and of the packed scales of a four-bit matrix
+ * [rows][cols]; rows % 16 == 0, cols % 64 == 0, group in {32, 64, 128}.
+ * Returns 0 for a shape the library does not take. */
+size_t dflash_int4_packed_bytes(int64_t rows, int64_t cols, int32_t group);
+size_t dflash_int4_scale_bytes(int64_t rows, int64_t cols, int32_t group);
+
+/* Repack a four-bit matrix from the interchange format (codes u8 [rows][cols/2],
+ * q+8 offset-binary, the even column in the low nibble; scales f16
+ * [rows][cols/group]) into the library's tile layout. All pointers are device
+ * pointers, 16-byte aligned; dst_codes/dst_scales hold the sizes above.
+ * Enqueued on `stream`. Errors: DFLASH_E_ARG. */
+int dflash_pack_int4(const uint8_t *codes, const uint16_t *scales, int64_t rows, int64_t cols,
+                     int32_t group, void *dst_codes, void *dst_scales, void *stream);
+
+/* The f16 matrices' tile layout: bytes, and the repack from row-major f16. */
+size_t dflash_f16_packed_bytes(int64_t rows, int64_t cols);
+int dflash_pack_f16(const uint16_t *src, int64_t rows, int64_t cols, void *dst, void *stream);
+
+/* The exact values of a packed four-bit matrix, f32 [rows][cols] (q * scale):
+ * the drafter's own dequantisation, exposed for checking. */
+int dflash_dequant_int4(const void *codes, const void *scales, int64_t rows, int64_t cols,
+                        int32_t group, float *out, void *stream);
+
+/* The drafter's product of a packed matrix W [rows][cols] with T rows of X:
+ * Y[t][r] = sum_c X[t][c] W[r][c], f32 X [T][cols] and Y [T][rows] (device,
+ * row-major). `kind` 4: a four-bit matrix (group `group`; X enters at full f32
+ * precision as f16 hi + lo planes); `kind` 16: an f16 matrix (X rounded to f16,
+ * as the card arm's `to_half` before its f16 GEMM). Exposed for checking the
+ * kernels the pass uses. Errors: ARG, CUDA. */
+int dflash_gemm(const dflash_matrix *w, int32_t kind, int64_t rows, int64_t cols, int32_t group, const float *x,
+                int32_t T, float *y, void *stream);
+
+/* ---- the drafter ----------------------------------------------------------- */
+
+/* Workspace bytes for up to `max_batch` sequences in one block call. */
+size_t dflash_workspace_bytes(const dflash_geometry *g, int32_t max_batch);
+
+/* Check the geometry (Geometry::of's rules and this build's limits: hidden % 64,
+ * heads*head_dim % 64, intermediate % 64, head_dim in {64, 128}, block <= 16,
+ * selector_top <= 32, vocab % 16) and bind the weights, the per-sequence
+ * context caches and the workspace. `ctx_k` / `ctx_v` are host arrays of
+ * max_batch*layers device pointers, indexed [seq*layers + layer], each an f32
+ * cache [ctx_cap][kv_heads][head_dim] (the card arm's layout,
+ * `[position - first][kv][hd]`). Every sequence starts empty at first = 0.
+ * Nothing is enqueued. Errors: GEOMETRY, ARG, CAPACITY (workspace), NOMEM. */
+int dflash_create(dflash_t **out, const dflash_geometry *g, const dflash_weights *w,
+                  int32_t max_batch, float *const *ctx_k, float *const *ctx_v, int64_t ctx_cap,
+                  void *workspace, size_t workspace_bytes);
+
+/* Context of sequence `seq` = empty, starting at position `first`. Host only. */
+int dflash_reset(dflash_t *d, int32_t seq, int64_t first);
+
+/* The settled context of `seq`: first position and row count. Host only. */
+int dflash_context(const dflash_t *d, int32_t seq, int64_t *first, int64_t *len);
+
+/* Settle `n` (1..256) tap rows of sequence `seq` at positions pos..pos+n-1
+ * (gpu_cuda/hyb/dflash.rs `Dev::settle`; dflash.rs `settle_rows`). `taps` is a
+ * device f32 [n][taps*hidden], joined in tap order. first <= pos <= first+len:
+ * rows at held positions replace them and what follows (len = pos-first+n).
+ * Errors: ARG (n, pos), CAPACITY (pos-first+n > ctx_cap), CUDA. */
+int dflash_settle(dflash_t *d, int32_t seq, int64_t pos, const float *taps, int32_t n, void *stream);
+
+/* One block of `batch` sequences 0..batch-1 (dflash.rs `Drafter::block` +
+ * the head and selector GEMMs of `Dev::block`). `anchor_pos` is a host array
+ * [batch]; `h` a device f32 [batch][block][hidden] of the rows' embeddings
+ * (read only). Writes logits f32 [batch][k][width] (rows 1..k over the head's
+ * first `width` rows) and hp f32 [batch][k][selector_rank]. 0 < k < block,
+ * selector_top <= width <= vocab. Layer l of sequence s reads its context
+ * range by `Drafter::block`'s rule. Errors: ARG, CUDA. */
+int dflash_block(dflash_t *d, int32_t batch, const int64_t *anchor_pos, const float *h, int32_t k,
+                 int32_t width, float *logits, float *hp, void *stream);
+
+/* The selector (dflash.rs `Drafter::select_with`, `top_k`) for `batch`
+ * sequences: logits f32 [batch][k][width], hp f32 [batch][k][rank],
+ * anchor_tok u32 [batch] (device). Writes chosen u32 [batch][k] and
+ * plain u32 [batch][k] (each row's own top token). An anchor token >= vocab
+ * (device data, so not checked on the host) makes every output of its
+ * sequence 0xFFFFFFFF. Errors: ARG, CUDA. */
+int dflash_select(dflash_t *d, int32_t batch, const float *logits, const float *hp,
+                  const uint32_t *anchor_tok, int32_t k, int32_t width, uint32_t *chosen,
+                  uint32_t *plain, void *stream);
+
+void dflash_destroy(dflash_t *d);
+
+/* The message of the calling thread's last failure ("" if none). */
+const char *dflash_last_error(void);
+
+/* Kernels the library has enqueued in this process so far (launch accounting). */
+uint64_t dflash_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* DFLASH_H */

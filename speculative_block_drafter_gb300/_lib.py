@@ -1,0 +1,185 @@
+"""ctypes binding of libdflash.so (include/dflash.h): argument marshalling only.
+
+Every function here forwards to the C entry point of the same name. The
+library must have been built (``speculative_block_drafter_gb300.build``); a
+missing library raises, there is no other path.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "libdflash.so")
+
+MAX_LAYERS = 64
+SETTLE_MAX = 256
+
+E_NAMES = {0: "OK", 1: "E_GEOMETRY", 2: "E_ARG", 3: "E_CAPACITY", 4: "E_CUDA", 5: "E_NOMEM"}
+
+
+class DflashError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"{E_NAMES.get(code, code)}: {msg}")
+        self.code = code
+
+
+class Geometry(C.Structure):
+    _fields_ = [
+        ("hidden", C.c_int32), ("intermediate", C.c_int32), ("layers", C.c_int32), ("heads", C.c_int32),
+        ("kv_heads", C.c_int32), ("head_dim", C.c_int32), ("vocab", C.c_int32), ("block", C.c_int32),
+        ("mask_token", C.c_uint32),
+        ("conv_group", C.c_int32), ("conv_kernel", C.c_int32), ("selector_rank", C.c_int32),
+        ("selector_top", C.c_int32), ("taps", C.c_int32), ("quant_group", C.c_int32),
+        ("windows", C.c_int32 * MAX_LAYERS), ("no_rope", C.c_uint8 * MAX_LAYERS),
+        ("rope_theta", C.c_double), ("eps", C.c_double),
+    ]
+
+
+class Matrix(C.Structure):
+    _fields_ = [("data", C.c_void_p), ("scales", C.c_void_p)]
+
+
+class LayerWeights(C.Structure):
+    _fields_ = [
+        ("in_norm", C.c_void_p), ("post_norm", C.c_void_p), ("q_norm", C.c_void_p), ("k_norm", C.c_void_p),
+        ("attn_base", C.c_void_p), ("mlp_base", C.c_void_p),
+        ("attn_proj", Matrix), ("mlp_proj", Matrix),
+        ("q", Matrix), ("k", Matrix), ("v", Matrix), ("o", Matrix), ("gate", Matrix), ("up", Matrix), ("down", Matrix),
+    ]
+
+
+class Weights(C.Structure):
+    _fields_ = [
+        ("fc", Matrix), ("hidden_norm", C.c_void_p), ("norm", C.c_void_p), ("sel", Matrix),
+        ("pred_book", C.c_void_p), ("succ_book", C.c_void_p), ("head", Matrix),
+        ("layers", C.POINTER(LayerWeights)),
+    ]
+
+
+_lib = None
+
+EXPORTS = {
+    "dflash_int4_packed_bytes": (C.c_size_t, [C.c_int64, C.c_int64, C.c_int32]),
+    "dflash_int4_scale_bytes": (C.c_size_t, [C.c_int64, C.c_int64, C.c_int32]),
+    "dflash_pack_int4": (C.c_int, [C.c_void_p, C.c_void_p, C.c_int64, C.c_int64, C.c_int32, C.c_void_p,
+                                   C.c_void_p, C.c_void_p]),
+    "dflash_f16_packed_bytes": (C.c_size_t, [C.c_int64, C.c_int64]),
+    "dflash_pack_f16": (C.c_int, [C.c_void_p, C.c_int64, C.c_int64, C.c_void_p, C.c_void_p]),
+    "dflash_dequant_int4": (C.c_int, [C.c_void_p, C.c_void_p, C.c_int64, C.c_int64, C.c_int32, C.c_void_p,
+                                      C.c_void_p]),
+    "dflash_gemm": (C.c_int, [C.POINTER(Matrix), C.c_int32, C.c_int64, C.c_int64, C.c_int32, C.c_void_p, C.c_int32,
+                              C.c_void_p, C.c_void_p]),
+    "dflash_workspace_bytes": (C.c_size_t, [C.POINTER(Geometry), C.c_int32]),
+    "dflash_create": (C.c_int, [C.POINTER(C.c_void_p), C.POINTER(Geometry), C.POINTER(Weights), C.c_int32,
+                                C.POINTER(C.c_void_p), C.POINTER(C.c_void_p), C.c_int64, C.c_void_p, C.c_size_t]),
+    "dflash_reset": (C.c_int, [C.c_void_p, C.c_int32, C.c_int64]),
+    "dflash_context": (C.c_int, [C.c_void_p, C.c_int32, C.POINTER(C.c_int64), C.POINTER(C.c_int64)]),
+    "dflash_settle": (C.c_int, [C.c_void_p, C.c_int32, C.c_int64, C.c_void_p, C.c_int32, C.c_void_p]),
+    "dflash_block": (C.c_int, [C.c_void_p, C.c_int32, C.POINTER(C.c_int64), C.c_void_p, C.c_int32, C.c_int32,
+                               C.c_void_p, C.c_void_p, C.c_void_p]),
+    "dflash_select": (C.c_int, [C.c_void_p, C.c_int32, C.c_void_p, C.c_void_p, C.c_void_p, C.c_int32, C.c_int32,
+                                C.c_void_p, C.c_void_p, C.c_void_p]),
+    "dflash_destroy": (None, [C.c_void_p]),
+    "dflash_last_error": (C.c_char_p, []),
+    "dflash_launch_count": (C.c_uint64, []),
+}
+
+
+def lib():
+    """The loaded library; raises if it was not built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build the CUDA library first "
+                               "(python -m speculative_block_drafter_gb300.build)")
+        L = C.CDLL(LIB_PATH)
+        for name, (res, args) in EXPORTS.items():
+            f = getattr(L, name)
+            f.restype = res
+            f.argtypes = args
+        _lib = L
+    return _lib
+
+
+def _check(code: int):
+    if code != 0:
+        raise DflashError(code, lib().dflash_last_error().decode())
+
+
+def last_error() -> str:
+    return lib().dflash_last_error().decode()
+
+
+# --- one wrapper per entry point (same names, marshalling only) -------------------
+
+def dflash_int4_packed_bytes(rows, cols, group):
+    return lib().dflash_int4_packed_bytes(rows, cols, group)
+
+
+def dflash_int4_scale_bytes(rows, cols, group):
+    return lib().dflash_int4_scale_bytes(rows, cols, group)
+
+
+def dflash_f16_packed_bytes(rows, cols):
+    return lib().dflash_f16_packed_bytes(rows, cols)
+
+
+def dflash_pack_int4(codes, scales, rows, cols, group, dst, dst_scales, stream):
+    _check(lib().dflash_pack_int4(codes, scales, rows, cols, group, dst, dst_scales, stream))
+
+
+def dflash_pack_f16(src, rows, cols, dst, stream):
+    _check(lib().dflash_pack_f16(src, rows, cols, dst, stream))
+
+
+def dflash_dequant_int4(codes, scales, rows, cols, group, out, stream):
+    _check(lib().dflash_dequant_int4(codes, scales, rows, cols, group, out, stream))
+
+
+def dflash_gemm(w: Matrix, kind, rows, cols, group, x, T, y, stream):
+    _check(lib().dflash_gemm(C.byref(w), kind, rows, cols, group, x, T, y, stream))
+
+
+def dflash_workspace_bytes(geom: Geometry, max_batch: int) -> int:
+    return lib().dflash_workspace_bytes(C.byref(geom), max_batch)
+
+
+def dflash_create(geom: Geometry, weights: Weights, max_batch, ctx_k, ctx_v, ctx_cap, workspace, ws_bytes):
+    h = C.c_void_p()
+    ks = (C.c_void_p * len(ctx_k))(*ctx_k)
+    vs = (C.c_void_p * len(ctx_v))(*ctx_v)
+    _check(lib().dflash_create(C.byref(h), C.byref(geom), C.byref(weights), max_batch, ks, vs, ctx_cap,
+                               workspace, ws_bytes))
+    return h
+
+
+def dflash_reset(h, seq, first):
+    _check(lib().dflash_reset(h, seq, first))
+
+
+def dflash_context(h, seq):
+    f, n = C.c_int64(), C.c_int64()
+    _check(lib().dflash_context(h, seq, C.byref(f), C.byref(n)))
+    return f.value, n.value
+
+
+def dflash_settle(h, seq, pos, taps, n, stream):
+    _check(lib().dflash_settle(h, seq, pos, taps, n, stream))
+
+
+def dflash_block(h, batch, anchor_pos, hrows, k, width, logits, hp, stream):
+    ap = (C.c_int64 * batch)(*[int(a) for a in anchor_pos])
+    _check(lib().dflash_block(h, batch, ap, hrows, k, width, logits, hp, stream))
+
+
+def dflash_select(h, batch, logits, hp, anchor_tok, k, width, chosen, plain, stream):
+    _check(lib().dflash_select(h, batch, logits, hp, anchor_tok, k, width, chosen, plain, stream))
+
+
+def dflash_destroy(h):
+    lib().dflash_destroy(h)
+
+
+def dflash_launch_count() -> int:
+    return lib().dflash_launch_count()

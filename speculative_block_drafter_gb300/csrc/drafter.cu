@@ -1,0 +1,406 @@
+// The C ABI of the drafter (include/dflash.h) and the host driver that
+// enqueues a settle, a block and a selection. The pass follows cortiq-engine
+// src/gpu_cuda/hyb/dflash.rs (`Dev::settle`, `Dev::block`) and
+// src/cortiq_engine/dflash.rs (`Drafter::block`, `Drafter::select_with`).
+// The host keeps only each sequence's (first, len); the device memory is the
+// caller's.
+#include <algorithm>
+#include <cmath>
+#include <climits>
+#include <cstring>
+#include <new>
+#include <string>
+#include <vector>
+
+#include "dflash.h"
+#include "kernels.h"
+
+namespace dfl {
+std::atomic<unsigned long long> g_launches{0};
+}
+
+namespace {
+
+thread_local std::string g_err;
+
+int fail(int code, const std::string &msg) {
+  g_err = msg;
+  return code;
+}
+
+#define DF_CUDA(call)                                                                            \
+  do {                                                                                           \
+    cudaError_t e_ = (call);                                                                     \
+    if (e_ != cudaSuccess) return fail(DFLASH_E_CUDA, std::string(#call) + ": " + cudaGetErrorString(e_)); \
+  } while (0)
+
+constexpr size_t ALIGN = 256;
+size_t up(size_t n) { return (n + ALIGN - 1) / ALIGN * ALIGN; }
+
+bool aligned16(const void *p) { return ((uintptr_t)p & 15) == 0; }
+
+struct Seq {
+  int64_t first = 0, len = 0;
+};
+
+// Workspace carve; sizes in bytes.
+struct Carve {
+  size_t h, x, xc, d, q, k, v, y, o, gt, up, part, sel, total;
+};
+
+Carve carve_of(const dflash_geometry &g, int max_batch) {
+  const int R = g.block;
+  const size_t T = (size_t)std::max(max_batch * R, DFLASH_SETTLE_MAX);
+  const size_t G = (size_t)g.hidden / g.conv_group;
+  const size_t pr = 2 * (size_t)g.conv_kernel * G;
+  const size_t f = sizeof(float);
+  Carve c{};
+  c.h = up(T * g.hidden * f);
+  c.x = up(T * g.hidden * f);
+  c.xc = up(T * g.hidden * f);
+  c.d = up(T * pr * f);
+  c.q = up(T * (size_t)g.heads * g.head_dim * f);
+  c.k = up(T * (size_t)g.kv_heads * g.head_dim * f);
+  c.v = c.k;
+  c.y = c.q;
+  c.o = up(T * g.hidden * f);
+  c.gt = up(T * (size_t)g.intermediate * f);
+  c.up = c.gt;
+  c.part = up(dfl::attn_partial_bytes(max_batch, g.kv_heads, g.heads, R, g.head_dim));
+  c.sel = up(dfl::select_scratch_bytes(max_batch * (R - 1), g.vocab, g.selector_top));
+  c.total = c.h + c.x + c.xc + c.d + c.q + c.k + c.v + c.y + c.o + c.gt + c.up + c.part + c.sel;
+  return c;
+}
+
+std::string check_geometry(const dflash_geometry &g) {
+  // Geometry::of's rules (src/cortiq_engine/dflash.rs)
+  if (g.layers < 1 || g.layers > DFLASH_MAX_LAYERS) return "layers must be 1..64";
+  if (g.block < 2) return "block must be at least 2";
+  if (g.taps < 1) return "no taps";
+  if (g.kv_heads < 1) return "kv_heads must be at least 1";
+  if (g.heads % g.kv_heads != 0) return "heads must be a multiple of kv_heads";
+  if (g.head_dim % 2 != 0) return "head_dim must be even";
+  if (g.conv_group < 1) return "conv_group must be at least 1";
+  if (g.hidden % g.conv_group != 0) return "hidden must be a multiple of conv_group";
+  for (int l = 0; l < g.layers; ++l)
+    if (g.windows[l] < 0) return "a negative window";
+  // this build's limits
+  if (g.block > DFLASH_MAX_BLOCK) return "block must be at most 16";
+  if (g.head_dim != 64 && g.head_dim != 128) return "head_dim must be 64 or 128";
+  if (g.hidden % 64 || g.intermediate % 64 || (g.heads * g.head_dim) % 64)
+    return "hidden, intermediate and heads*head_dim must be multiples of 64";
+  if ((g.kv_heads * g.head_dim) % 16) return "kv_heads*head_dim must be a multiple of 16";
+  if (g.vocab < 16 || g.vocab % 16) return "vocab must be a positive multiple of 16";
+  if ((2 * g.conv_kernel * (g.hidden / g.conv_group)) % 16) return "2*conv_kernel*groups must be a multiple of 16";
+  if (g.conv_kernel < 1 || g.conv_kernel > DFLASH_MAX_BLOCK) return "conv_kernel must be 1..16";
+  if (g.selector_rank < 16 || g.selector_rank > 256 || g.selector_rank % 16) return "selector_rank must be 16..256, a multiple of 16";
+  if (g.selector_top < 1 || g.selector_top > 32 || g.selector_top > g.vocab) return "selector_top must be 1..32";
+  if (g.quant_group != 32 && g.quant_group != 64 && g.quant_group != 128) return "quant_group must be 32, 64 or 128";
+  if (g.hidden % g.quant_group || g.intermediate % g.quant_group || (g.heads * g.head_dim) % g.quant_group)
+    return "every four-bit matrix's columns must be a multiple of quant_group";
+  if (g.heads / g.kv_heads * g.block > 64) return "heads/kv_heads * block must be at most 64";
+  if (!(g.eps >= 0.0) || !(g.rope_theta > 0.0)) return "eps must be >= 0 and rope_theta > 0";
+  return "";
+}
+
+bool int4_ok(const dflash_matrix &m) { return m.data && m.scales && aligned16(m.data) && aligned16(m.scales); }
+bool f16_ok(const dflash_matrix &m) { return m.data && aligned16(m.data); }
+
+}  // namespace
+
+struct dflash_t {
+  dflash_geometry g;
+  dflash_weights w;
+  std::vector<dflash_layer_weights> layers;
+  int max_batch = 0;
+  std::vector<float *> ck, cv;
+  int64_t cap = 0;
+  char *ws = nullptr;
+  Carve c{};
+  float *h, *x, *xc, *d, *q, *k, *v, *y, *o, *gt, *up, *part;
+  void *sel;
+  std::vector<Seq> seqs;
+  std::vector<float> inv;
+  int num_sms = 148;
+};
+
+extern "C" {
+
+const char *dflash_last_error(void) { return g_err.c_str(); }
+
+uint64_t dflash_launch_count(void) { return dfl::g_launches.load(); }
+
+size_t dflash_int4_packed_bytes(int64_t rows, int64_t cols, int32_t group) {
+  if (rows <= 0 || cols <= 0 || rows % 16 || cols % 64 || (group != 32 && group != 64 && group != 128) || cols % group)
+    return 0;
+  return dfl::int4_packed_bytes(rows, cols);
+}
+
+size_t dflash_int4_scale_bytes(int64_t rows, int64_t cols, int32_t group) {
+  if (dflash_int4_packed_bytes(rows, cols, group) == 0) return 0;
+  return dfl::int4_scale_bytes(rows, cols, group);
+}
+
+size_t dflash_f16_packed_bytes(int64_t rows, int64_t cols) {
+  if (rows <= 0 || cols <= 0 || rows % 16 || cols % 64) return 0;
+  return dfl::f16_packed_bytes(rows, cols);
+}
+
+int dflash_pack_int4(const uint8_t *codes, const uint16_t *scales, int64_t rows, int64_t cols, int32_t group,
+                     void *dst_codes, void *dst_scales, void *stream) {
+  if (dflash_int4_packed_bytes(rows, cols, group) == 0) return fail(DFLASH_E_ARG, "pack_int4: unsupported shape");
+  if (!codes || !scales || !dst_codes || !dst_scales) return fail(DFLASH_E_ARG, "pack_int4: null pointer");
+  if (!aligned16(dst_codes) || !aligned16(dst_scales)) return fail(DFLASH_E_ARG, "pack_int4: misaligned output");
+  DF_CUDA(dfl::pack_int4(codes, scales, rows, cols, group, dst_codes, dst_scales, (cudaStream_t)stream));
+  return DFLASH_OK;
+}
+
+int dflash_pack_f16(const uint16_t *src, int64_t rows, int64_t cols, void *dst, void *stream) {
+  if (dflash_f16_packed_bytes(rows, cols) == 0) return fail(DFLASH_E_ARG, "pack_f16: unsupported shape");
+  if (!src || !dst) return fail(DFLASH_E_ARG, "pack_f16: null pointer");
+  if (!aligned16(dst)) return fail(DFLASH_E_ARG, "pack_f16: misaligned output");
+  DF_CUDA(dfl::pack_f16(src, rows, cols, dst, (cudaStream_t)stream));
+  return DFLASH_OK;
+}
+
+int dflash_dequant_int4(const void *codes, const void *scales, int64_t rows, int64_t cols, int32_t group, float *out,
+                        void *stream) {
+  if (dflash_int4_packed_bytes(rows, cols, group) == 0) return fail(DFLASH_E_ARG, "dequant_int4: unsupported shape");
+  if (!codes || !scales || !out) return fail(DFLASH_E_ARG, "dequant_int4: null pointer");
+  if (!aligned16(codes) || !aligned16(scales)) return fail(DFLASH_E_ARG, "dequant_int4: misaligned input");
+  DF_CUDA(dfl::dequant_int4(codes, scales, rows, cols, group, out, (cudaStream_t)stream));
+  return DFLASH_OK;
+}
+
+int dflash_gemm(const dflash_matrix *w, int32_t kind, int64_t rows, int64_t cols, int32_t group, const float *x,
+                int32_t T, float *y, void *stream) {
+  if (!w || !x || !y || T < 1) return fail(DFLASH_E_ARG, "gemm: null pointer or no rows");
+  if (((uintptr_t)x & 7) || ((uintptr_t)y & 3)) return fail(DFLASH_E_ARG, "gemm: misaligned x or y");
+  if (rows > INT32_MAX || cols > INT32_MAX) return fail(DFLASH_E_ARG, "gemm: matrix too large");
+  int sms = 148, dev = 0;
+  if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (kind == 4) {
+    if (dflash_int4_packed_bytes(rows, cols, group) == 0) return fail(DFLASH_E_ARG, "gemm: unsupported int4 shape");
+    if (!int4_ok(*w)) return fail(DFLASH_E_ARG, "gemm: null or misaligned matrix");
+    DF_CUDA(dfl::gemm_int4(dfl::Gemm{w->data, w->scales, group, (int)rows, (int)cols, x, (int)cols, y, (int)rows, T, false},
+                           sms, (cudaStream_t)stream));
+  } else if (kind == 16) {
+    if (dflash_f16_packed_bytes(rows, cols) == 0) return fail(DFLASH_E_ARG, "gemm: unsupported f16 shape");
+    if (!f16_ok(*w)) return fail(DFLASH_E_ARG, "gemm: null or misaligned matrix");
+    DF_CUDA(dfl::gemm_f16(dfl::Gemm{w->data, nullptr, 64, (int)rows, (int)cols, x, (int)cols, y, (int)rows, T, false},
+                          sms, (cudaStream_t)stream));
+  } else {
+    return fail(DFLASH_E_ARG, "gemm: kind must be 4 or 16");
+  }
+  return DFLASH_OK;
+}
+
+size_t dflash_workspace_bytes(const dflash_geometry *g, int32_t max_batch) {
+  if (!g || max_batch < 1 || max_batch > dfl::MAX_BATCH || !check_geometry(*g).empty()) return 0;
+  return carve_of(*g, max_batch).total;
+}
+
+int dflash_create(dflash_t **out, const dflash_geometry *g, const dflash_weights *w, int32_t max_batch,
+                  float *const *ctx_k, float *const *ctx_v, int64_t ctx_cap, void *workspace,
+                  size_t workspace_bytes) {
+  if (!out || !g || !w) return fail(DFLASH_E_ARG, "create: null argument");
+  *out = nullptr;
+  const std::string why = check_geometry(*g);
+  if (!why.empty()) return fail(DFLASH_E_GEOMETRY, "unsupported DFlash geometry: " + why);
+  if (max_batch < 1 || max_batch > dfl::MAX_BATCH) return fail(DFLASH_E_ARG, "create: max_batch must be 1..64");
+  if (!ctx_k || !ctx_v || ctx_cap < 1) return fail(DFLASH_E_ARG, "create: context caches");
+  if (!workspace || !aligned16(workspace)) return fail(DFLASH_E_ARG, "create: null or misaligned workspace");
+  const Carve c = carve_of(*g, max_batch);
+  if (workspace_bytes < c.total) return fail(DFLASH_E_CAPACITY, "create: workspace smaller than dflash_workspace_bytes");
+  if (!w->layers) return fail(DFLASH_E_ARG, "create: no layers");
+  if (!f16_ok(w->fc) || !f16_ok(w->sel) || !int4_ok(w->head) || !w->hidden_norm || !w->norm || !w->pred_book ||
+      !w->succ_book)
+    return fail(DFLASH_E_ARG, "create: a null or misaligned weight");
+  for (int l = 0; l < g->layers; ++l) {
+    const dflash_layer_weights &L = w->layers[l];
+    if (!L.in_norm || !L.post_norm || !L.q_norm || !L.k_norm || !L.attn_base || !L.mlp_base ||
+        !f16_ok(L.attn_proj) || !f16_ok(L.mlp_proj) || !int4_ok(L.q) || !int4_ok(L.k) || !int4_ok(L.v) ||
+        !int4_ok(L.o) || !int4_ok(L.gate) || !int4_ok(L.up) || !int4_ok(L.down))
+      return fail(DFLASH_E_ARG, "create: a null or misaligned weight of layer " + std::to_string(l));
+  }
+  for (int i = 0; i < max_batch * g->layers; ++i)
+    if (!ctx_k[i] || !ctx_v[i] || !aligned16(ctx_k[i]) || !aligned16(ctx_v[i]))
+      return fail(DFLASH_E_ARG, "create: a null or misaligned context cache");
+
+  dflash_t *d = new (std::nothrow) dflash_t;
+  if (!d) return fail(DFLASH_E_NOMEM, "create: out of host memory");
+  d->g = *g;
+  d->w = *w;
+  d->layers.assign(w->layers, w->layers + g->layers);
+  d->w.layers = d->layers.data();
+  d->max_batch = max_batch;
+  d->ck.assign(ctx_k, ctx_k + (size_t)max_batch * g->layers);
+  d->cv.assign(ctx_v, ctx_v + (size_t)max_batch * g->layers);
+  d->cap = ctx_cap;
+  d->ws = (char *)workspace;
+  d->c = c;
+  char *p = d->ws;
+  auto take = [&](size_t n) {
+    char *r = p;
+    p += n;
+    return r;
+  };
+  d->h = (float *)take(c.h);
+  d->x = (float *)take(c.x);
+  d->xc = (float *)take(c.xc);
+  d->d = (float *)take(c.d);
+  d->q = (float *)take(c.q);
+  d->k = (float *)take(c.k);
+  d->v = (float *)take(c.v);
+  d->y = (float *)take(c.y);
+  d->o = (float *)take(c.o);
+  d->gt = (float *)take(c.gt);
+  d->up = (float *)take(c.up);
+  d->part = (float *)take(c.part);
+  d->sel = take(c.sel);
+  d->seqs.assign(max_batch, Seq{});
+  // inv_freq = f32(theta^(-2i/hd)) (src/cortiq_engine/dflash.rs, Drafter::new)
+  d->inv.resize(g->head_dim / 2);
+  for (int i = 0; i < g->head_dim / 2; ++i)
+    d->inv[i] = (float)std::pow(g->rope_theta, -(2.0 * i) / (double)g->head_dim);
+  int dev = 0;
+  if (cudaGetDevice(&dev) == cudaSuccess) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && n > 0) d->num_sms = n;
+  }
+  *out = d;
+  return DFLASH_OK;
+}
+
+void dflash_destroy(dflash_t *d) { delete d; }
+
+int dflash_reset(dflash_t *d, int32_t seq, int64_t first) {
+  if (!d || seq < 0 || seq >= d->max_batch || first < 0) return fail(DFLASH_E_ARG, "reset: bad sequence or position");
+  d->seqs[seq].first = first;
+  d->seqs[seq].len = 0;
+  return DFLASH_OK;
+}
+
+int dflash_context(const dflash_t *d, int32_t seq, int64_t *first, int64_t *len) {
+  if (!d || seq < 0 || seq >= d->max_batch) return fail(DFLASH_E_ARG, "context: bad sequence");
+  if (first) *first = d->seqs[seq].first;
+  if (len) *len = d->seqs[seq].len;
+  return DFLASH_OK;
+}
+
+int dflash_settle(dflash_t *d, int32_t seq, int64_t pos, const float *taps, int32_t n, void *stream) {
+  if (!d) return fail(DFLASH_E_ARG, "settle: null drafter");
+  if (seq < 0 || seq >= d->max_batch) return fail(DFLASH_E_ARG, "settle: bad sequence");
+  if (n < 1 || n > DFLASH_SETTLE_MAX) return fail(DFLASH_E_ARG, "settle: a settle of 1 to 256 tap rows");
+  if (!taps || ((uintptr_t)taps & 7)) return fail(DFLASH_E_ARG, "settle: null or misaligned taps");
+  Seq &s = d->seqs[seq];
+  if (pos < s.first || pos > s.first + s.len)
+    return fail(DFLASH_E_ARG, "settle: pos must lie in [first, first + len] (reset the sequence for a gap)");
+  const int64_t at = pos - s.first;
+  if (at + n > d->cap) return fail(DFLASH_E_CAPACITY, "settle: context rows do not fit the cache");
+  const dflash_geometry &g = d->g;
+  cudaStream_t st = (cudaStream_t)stream;
+  const int hs = g.hidden, tw = g.taps * g.hidden, kvd = g.kv_heads * g.head_dim;
+  // t = rms(fc . f16(taps), hidden_norm)
+  dfl::Gemm fc{d->w.fc.data, nullptr, 64, hs, tw, taps, tw, d->x, hs, n, false};
+  DF_CUDA(dfl::gemm_f16(fc, d->num_sms, st));
+  DF_CUDA(dfl::rmsnorm(d->x, d->w.hidden_norm, d->x, n, hs, (float)g.eps, 1, -1, -1, st));
+  for (int l = 0; l < g.layers; ++l) {
+    const dflash_layer_weights &L = d->layers[l];
+    float *kc = d->ck[(size_t)seq * g.layers + l] + at * kvd;
+    float *vc = d->cv[(size_t)seq * g.layers + l] + at * kvd;
+    dfl::Gemm gk{L.k.data, L.k.scales, g.quant_group, kvd, hs, d->x, hs, kc, kvd, n, false};
+    dfl::Gemm gv{L.v.data, L.v.scales, g.quant_group, kvd, hs, d->x, hs, vc, kvd, n, false};
+    DF_CUDA(dfl::gemm_int4(gk, d->num_sms, st));
+    DF_CUDA(dfl::gemm_int4(gv, d->num_sms, st));
+    DF_CUDA(dfl::head_norm_rope(kc, kvd, L.k_norm, d->inv.data(), n, g.kv_heads, g.head_dim, (float)g.eps,
+                                g.no_rope[l] == 0, nullptr, 0, 1, pos, st));
+  }
+  s.len = at + n;
+  return DFLASH_OK;
+}
+
+int dflash_block(dflash_t *d, int32_t batch, const int64_t *anchor_pos, const float *h, int32_t k, int32_t width,
+                 float *logits, float *hp, void *stream) {
+  if (!d) return fail(DFLASH_E_ARG, "block: null drafter");
+  const dflash_geometry &g = d->g;
+  const int R = g.block;
+  if (batch < 1 || batch > d->max_batch) return fail(DFLASH_E_ARG, "block: batch must be 1..max_batch");
+  if (!anchor_pos || !h || !logits || !hp || ((uintptr_t)h & 15)) return fail(DFLASH_E_ARG, "block: null or misaligned pointer");
+  if (k < 1 || k >= R) return fail(DFLASH_E_ARG, "block: k must be 1..block-1");
+  if (width < g.selector_top || width > g.vocab) return fail(DFLASH_E_ARG, "block: width must be selector_top..vocab");
+  for (int b = 0; b < batch; ++b)
+    if (anchor_pos[b] < 0) return fail(DFLASH_E_ARG, "block: a negative anchor position");
+  cudaStream_t st = (cudaStream_t)stream;
+  const int T = batch * R;
+  const int hs = g.hidden, nh = g.heads, kv = g.kv_heads, hd = g.head_dim, ffn = g.intermediate;
+  const int qd = nh * hd, kvd = kv * hd, kn = g.conv_kernel, gs = g.conv_group;
+  const int pr = 2 * kn * (hs / gs);
+  const float eps = (float)g.eps;
+  const float scale = std::pow((float)hd, -0.5f);
+  const int grp = g.quant_group;
+  const int sms = d->num_sms;
+  DF_CUDA(cudaMemcpyAsync(d->h, h, (size_t)T * hs * sizeof(float), cudaMemcpyDeviceToDevice, st));
+  std::vector<dfl::AttnSeq> seqs(batch);
+  for (int l = 0; l < g.layers; ++l) {
+    const dflash_layer_weights &L = d->layers[l];
+    const int W = g.windows[l];
+    const bool rot = g.no_rope[l] == 0;
+    // attention: x = norm(h); x, d = conv_in(x); q, k, v
+    DF_CUDA(dfl::rmsnorm(d->h, L.in_norm, d->x, T, hs, eps, R, -1, -1, st));
+    DF_CUDA(dfl::gemm_f16(dfl::Gemm{L.attn_proj.data, nullptr, 64, pr, hs, d->x, hs, d->d, pr, T, false}, sms, st));
+    DF_CUDA(dfl::conv_stage0(d->x, d->d, L.attn_base, d->xc, T, hs, kn, gs, R, st));
+    DF_CUDA(dfl::gemm_int4(dfl::Gemm{L.q.data, L.q.scales, grp, qd, hs, d->xc, hs, d->q, qd, T, false}, sms, st));
+    DF_CUDA(dfl::gemm_int4(dfl::Gemm{L.k.data, L.k.scales, grp, kvd, hs, d->xc, hs, d->k, kvd, T, false}, sms, st));
+    DF_CUDA(dfl::gemm_int4(dfl::Gemm{L.v.data, L.v.scales, grp, kvd, hs, d->xc, hs, d->v, kvd, T, false}, sms, st));
+    DF_CUDA(dfl::head_norm_rope(d->q, qd, L.q_norm, d->inv.data(), T, nh, hd, eps, rot, anchor_pos, batch, R, 0, st));
+    DF_CUDA(dfl::head_norm_rope(d->k, kvd, L.k_norm, d->inv.data(), T, kv, hd, eps, rot, anchor_pos, batch, R, 0, st));
+    // the layer's context range (src/cortiq_engine/dflash.rs, Drafter::block; no rows dropped)
+    for (int b = 0; b < batch; ++b) {
+      const Seq &s = d->seqs[b];
+      const int64_t a = anchor_pos[b];
+      const int64_t base = s.first;
+      const int64_t hi = std::max(std::min(a, s.first + s.len), base);
+      int64_t lo = base;
+      if (W > 0) lo = std::min(std::max(std::max<int64_t>(a + 1 - W, 0), base), hi);
+      seqs[b].ck = d->ck[(size_t)b * g.layers + l] + (lo - s.first) * kvd;
+      seqs[b].cv = d->cv[(size_t)b * g.layers + l] + (lo - s.first) * kvd;
+      seqs[b].n = (int)(hi - lo);
+      seqs[b].lo = lo;
+      seqs[b].anchor = a;
+    }
+    DF_CUDA(dfl::attention(d->q, d->k, d->v, seqs.data(), batch, 0, nh, kv, hd, R, W, scale, d->part, d->y, st));
+    DF_CUDA(dfl::gemm_int4(dfl::Gemm{L.o.data, L.o.scales, grp, hs, qd, d->y, qd, d->o, hs, T, false}, sms, st));
+    DF_CUDA(dfl::conv_stage1_residual(d->o, d->d, L.attn_base, d->h, T, hs, kn, gs, R, st));
+    // the MLP the same way
+    DF_CUDA(dfl::rmsnorm(d->h, L.post_norm, d->x, T, hs, eps, R, -1, -1, st));
+    DF_CUDA(dfl::gemm_f16(dfl::Gemm{L.mlp_proj.data, nullptr, 64, pr, hs, d->x, hs, d->d, pr, T, false}, sms, st));
+    DF_CUDA(dfl::conv_stage0(d->x, d->d, L.mlp_base, d->xc, T, hs, kn, gs, R, st));
+    DF_CUDA(dfl::gemm_int4(dfl::Gemm{L.gate.data, L.gate.scales, grp, ffn, hs, d->xc, hs, d->gt, ffn, T, false}, sms, st));
+    DF_CUDA(dfl::gemm_int4(dfl::Gemm{L.up.data, L.up.scales, grp, ffn, hs, d->xc, hs, d->up, ffn, T, false}, sms, st));
+    DF_CUDA(dfl::silu_mul(d->gt, d->up, d->gt, (int64_t)T * ffn, st));
+    DF_CUDA(dfl::gemm_int4(dfl::Gemm{L.down.data, L.down.scales, grp, hs, ffn, d->gt, ffn, d->o, hs, T, false}, sms, st));
+    DF_CUDA(dfl::conv_stage1_residual(d->o, d->d, L.mlp_base, d->h, T, hs, kn, gs, R, st));
+  }
+  // the last norm; the head and the selector's projection over rows 1..k
+  const int Tk = batch * k;
+  DF_CUDA(dfl::rmsnorm(d->h, d->w.norm, d->x, T, hs, eps, R, 1, k, st));
+  DF_CUDA(dfl::gemm_int4(dfl::Gemm{d->w.head.data, d->w.head.scales, grp, width, hs, d->x, hs, logits, width, Tk, false}, sms, st));
+  DF_CUDA(dfl::gemm_f16(dfl::Gemm{d->w.sel.data, nullptr, 64, g.selector_rank, hs, d->x, hs, hp, g.selector_rank, Tk, false}, sms, st));
+  return DFLASH_OK;
+}
+
+int dflash_select(dflash_t *d, int32_t batch, const float *logits, const float *hp, const uint32_t *anchor_tok,
+                  int32_t k, int32_t width, uint32_t *chosen, uint32_t *plain, void *stream) {
+  if (!d) return fail(DFLASH_E_ARG, "select: null drafter");
+  const dflash_geometry &g = d->g;
+  if (batch < 1 || batch > d->max_batch) return fail(DFLASH_E_ARG, "select: batch must be 1..max_batch");
+  if (k < 1 || k >= g.block) return fail(DFLASH_E_ARG, "select: k must be 1..block-1");
+  if (width < g.selector_top || width > g.vocab) return fail(DFLASH_E_ARG, "select: width must be selector_top..vocab");
+  if (!logits || !hp || !anchor_tok || !chosen || !plain) return fail(DFLASH_E_ARG, "select: null pointer");
+  DF_CUDA(dfl::select_tokens(logits, hp, anchor_tok, d->w.pred_book, d->w.succ_book, batch, k, width, g.selector_rank,
+                             g.selector_top, g.vocab, d->sel, chosen, plain, (cudaStream_t)stream));
+  return DFLASH_OK;
+}
+
+}  // extern "C"

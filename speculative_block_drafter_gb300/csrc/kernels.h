@@ -1,0 +1,86 @@
+// Host-side launchers of the drafter's kernels (internal to the library).
+#pragma once
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <atomic>
+
+namespace dfl {
+
+// Kernel launches enqueued by the library in this process.
+extern std::atomic<unsigned long long> g_launches;
+inline void count_launch(int n = 1) { g_launches.fetch_add((unsigned long long)n, std::memory_order_relaxed); }
+
+// -------------------------------------------------------------- packing (gemm.cu)
+size_t int4_packed_bytes(int64_t rows, int64_t cols);
+size_t int4_scale_bytes(int64_t rows, int64_t cols, int group);
+size_t f16_packed_bytes(int64_t rows, int64_t cols);
+cudaError_t pack_int4(const uint8_t *codes, const uint16_t *scales, int64_t rows, int64_t cols, int group,
+                      void *dst, void *dst_scales, cudaStream_t st);
+cudaError_t pack_f16(const uint16_t *src, int64_t rows, int64_t cols, void *dst, cudaStream_t st);
+cudaError_t dequant_int4(const void *codes, const void *scales, int64_t rows, int64_t cols, int group,
+                         float *out, cudaStream_t st);
+
+// -------------------------------------------------------------- weight-streaming GEMM (gemm.cu)
+// Y[t][n] (= or +=) sum_k X[t][k] W[n][k] for t < T, n < N.
+// int4: X enters as f16 hi+lo planes (full f32 precision); f16: X rounded to f16.
+// `zero_first`: the launcher clears Y[0..T)[0..N) itself when it splits K.
+// `accumulate`: add into Y (never cleared) instead of storing.
+struct Gemm {
+  const void *w;        // packed matrix
+  const void *scales;   // int4 scales (null for f16)
+  int group;            // int4 group
+  int N, K;             // rows, cols of W
+  const float *X;       // [T][ldx]
+  int ldx;
+  float *Y;             // [T][ldy]
+  int ldy;
+  int T;
+  bool accumulate;
+};
+cudaError_t gemm_int4(const Gemm &g, int num_sms, cudaStream_t st);
+cudaError_t gemm_f16(const Gemm &g, int num_sms, cudaStream_t st);
+
+// -------------------------------------------------------------- row kernels (rows.cu)
+// out[map(t)] = x[t] * rsqrt(mean(x[t]^2) + eps) * w for rows t < T. If
+// `keep_from/keep_to` are set (>= 0), only rows whose position in their block
+// (t % block) lies in [keep_from, keep_to] are written, packed per sequence.
+cudaError_t rmsnorm(const float *x, const float *w, float *out, int T, int hs, float eps, int block,
+                    int keep_from, int keep_to, cudaStream_t st);
+// Stage 0 of the row convolution: y[t] = sum_o (base[0][o] + d[t][0][o][g]) * x[t-o], o <= t % block.
+cudaError_t conv_stage0(const float *x, const float *d, const float *base, float *y, int T, int hs, int kn,
+                        int gs, int block, cudaStream_t st);
+// Stage 1 with the residual: h[t] += sum_o (base[1][o] + d[t][1][o][g]) * x[t-o].
+cudaError_t conv_stage1_residual(const float *x, const float *d, const float *base, float *h, int T, int hs,
+                                 int kn, int gs, int block, cudaStream_t st);
+constexpr int MAX_BATCH = 64;
+// Per head rms norm (weight [hd]) and, if rotary, the half-split rotation of
+// row t to position pos0[t / block] + t % block (pos0: host array of `nseq`
+// positions, passed by value) or, when pos0 is null, to `pos_base + t`.
+// `inv_freq` is a host array of hd/2 f32 values, passed by value.
+cudaError_t head_norm_rope(float *x, int ld, const float *w, const float *inv_freq, int T, int heads, int hd,
+                           float eps, bool rotary, const int64_t *pos0, int nseq, int block, int64_t pos_base,
+                           cudaStream_t st);
+// m = silu(g) * u, elementwise over n values.
+cudaError_t silu_mul(const float *g, const float *u, float *m, int64_t n, cudaStream_t st);
+
+// -------------------------------------------------------------- attention (attention.cu)
+struct AttnSeq {        // per sequence and layer, on the device
+  const float *ck, *cv; // cache rows of positions lo.. (already offset)
+  int n;                // context rows read
+  int64_t lo;           // position of the first
+  int64_t anchor;       // position of block row 0
+};
+size_t attn_partial_bytes(int max_batch, int kv_heads, int heads, int block, int hd);
+// `seqs` is a host array of `batch` entries (passed by value).
+cudaError_t attention(const float *q, const float *k, const float *v, const AttnSeq *seqs, int batch,
+                      int max_ctx, int heads, int kv_heads, int hd, int block, int window, float scale,
+                      float *partials, float *y, cudaStream_t st);
+
+// -------------------------------------------------------------- selector (select.cu)
+size_t select_scratch_bytes(int max_rows, int width, int top);
+cudaError_t select_tokens(const float *logits, const float *hp, const uint32_t *anchor_tok,
+                          const uint16_t *pred, const uint16_t *succ, int batch, int k, int width, int rank,
+                          int top, int vocab, void *scratch, uint32_t *chosen, uint32_t *plain, cudaStream_t st);
+
+}  // namespace dfl

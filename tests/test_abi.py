@@ -1,0 +1,151 @@
+"""The C ABI without a GPU: the library loads, exports every declared entry point,
+and its host-side checks reject bad geometry and arguments before any launch."""
+import ctypes as C
+import dataclasses
+import os
+import re
+
+import pytest
+
+import dflash_inputs as di
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    from speculative_block_drafter_gb300 import build, _lib
+    if not os.path.exists(_lib.LIB_PATH):
+        build.build()
+    _lib.lib()
+    return _lib
+
+
+def _declared():
+    names = set()
+    for f in os.listdir(os.path.join(ROOT, "include")):
+        if f.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", f)).read()
+            src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+            names |= set(re.findall(r"\b(dflash_[a-z0-9_]+)\s*\(", src))
+    return names
+
+
+def test_every_declared_symbol_is_exported(L):
+    names = _declared()
+    assert "dflash_create" in names and "dflash_block" in names
+    lib = L.lib()
+    for n in sorted(names):
+        assert hasattr(lib, n), n
+    assert names <= set(L.EXPORTS), names - set(L.EXPORTS)
+
+
+def _geom(L, **over):
+    from speculative_block_drafter_gb300.drafter import geometry_struct
+    g = dataclasses.replace(di.workload("tiny").geometry, **over)
+    return geometry_struct(g)
+
+
+def test_workspace_bytes_for_every_workload(L):
+    from speculative_block_drafter_gb300.drafter import geometry_struct
+    for name, wl in di.WORKLOADS.items():
+        n = L.dflash_workspace_bytes(geometry_struct(wl.geometry), wl.batch)
+        assert n > 0, name
+
+
+@pytest.mark.parametrize("over", [dict(layers=0), dict(block=1), dict(taps=0), dict(kv_heads=0), dict(heads=3),
+                                  dict(conv_group=0), dict(conv_group=7), dict(head_dim=96), dict(block=17),
+                                  dict(quant_group=48), dict(selector_top=33), dict(hidden=200, conv_group=8),
+                                  dict(vocab=4100), dict(selector_rank=8)])
+def test_geometry_rules(L, over):
+    g = _geom(L, **over)
+    if "layers" in over and over["layers"] == 0:
+        pass
+    assert L.dflash_workspace_bytes(g, 1) == 0
+    h = C.c_void_p()
+    w = L.Weights()
+    one = (C.c_void_p * 1)(C.c_void_p(4096))
+    code = L.lib().dflash_create(C.byref(h), C.byref(g), C.byref(w), 1, one, one, 16, C.c_void_p(4096), 1 << 30)
+    assert code == 1, L.last_error()
+    assert "geometry" in L.last_error()
+
+
+def _fake_create(L, max_batch=1, cap=64):
+    """A drafter bound to aligned fake addresses: valid for host-only calls, never for launches."""
+    g = _geom(L)
+    addr = [1 << 20]
+
+    def nxt():
+        addr[0] += 4096
+        return addr[0]
+
+    layers = (L.LayerWeights * g.layers)()
+    for i in range(g.layers):
+        x = layers[i]
+        for f in ("in_norm", "post_norm", "q_norm", "k_norm", "attn_base", "mlp_base"):
+            setattr(x, f, nxt())
+        x.attn_proj = L.Matrix(nxt(), None)
+        x.mlp_proj = L.Matrix(nxt(), None)
+        for f in ("q", "k", "v", "o", "gate", "up", "down"):
+            setattr(x, f, L.Matrix(nxt(), nxt()))
+    w = L.Weights()
+    w.fc, w.sel, w.head = L.Matrix(nxt(), None), L.Matrix(nxt(), None), L.Matrix(nxt(), nxt())
+    w.hidden_norm, w.norm, w.pred_book, w.succ_book = nxt(), nxt(), nxt(), nxt()
+    w.layers = C.cast(layers, C.POINTER(L.LayerWeights))
+    caches = [nxt() for _ in range(max_batch * g.layers)]
+    ws = L.dflash_workspace_bytes(g, max_batch)
+    return L.dflash_create(g, w, max_batch, caches, caches, cap, nxt(), ws), (g, w, layers)
+
+
+def test_create_and_host_state(L):
+    h, keep = _fake_create(L, max_batch=2)
+    assert L.dflash_context(h, 0) == (0, 0)
+    L.dflash_reset(h, 1, 500)
+    assert L.dflash_context(h, 1) == (500, 0)
+    with pytest.raises(L.DflashError):
+        L.dflash_reset(h, 2, 0)
+    L.dflash_destroy(h)
+
+
+def test_settle_and_block_argument_errors_before_any_launch(L):
+    h, keep = _fake_create(L, max_batch=1, cap=64)
+    taps = 1 << 24
+    for n in (0, 257):
+        with pytest.raises(L.DflashError) as e:
+            L.dflash_settle(h, 0, 0, taps, n, None)
+        assert e.value.code == 2
+    with pytest.raises(L.DflashError) as e:               # a gap: the caller resets the sequence
+        L.dflash_settle(h, 0, 5, taps, 1, None)
+    assert e.value.code == 2
+    with pytest.raises(L.DflashError) as e:               # the cache holds 64 rows
+        L.dflash_settle(h, 0, 0, taps, 65, None)
+    assert e.value.code == 3
+    out = 1 << 25
+    for k, width in ((0, 4096), (16, 4096), (15, 7), (15, 4097)):
+        with pytest.raises(L.DflashError) as e:
+            L.dflash_block(h, 1, [0], taps, k, width, out, out, None)
+        assert e.value.code == 2
+    with pytest.raises(L.DflashError) as e:
+        L.dflash_block(h, 2, [0, 0], taps, 15, 4096, out, out, None)
+    assert e.value.code == 2
+    L.dflash_destroy(h)
+
+
+def test_create_rejects_small_workspace_and_null_weights(L):
+    g = _geom(L)
+    h = C.c_void_p()
+    w = L.Weights()
+    one = (C.c_void_p * 1)(C.c_void_p(4096))
+    code = L.lib().dflash_create(C.byref(h), C.byref(g), C.byref(w), 1, one, one, 16, C.c_void_p(4096), 1024)
+    assert code == 3
+    ws = L.dflash_workspace_bytes(g, 1)
+    code = L.lib().dflash_create(C.byref(h), C.byref(g), C.byref(w), 1, one, one, 16, C.c_void_p(4096), ws)
+    assert code == 2
+
+
+def test_packed_sizes(L):
+    assert L.dflash_int4_packed_bytes(32, 128, 64) == 32 * 64
+    assert L.dflash_int4_scale_bytes(32, 128, 64) == 2 * 2 * 8 * 4
+    assert L.dflash_int4_packed_bytes(30, 128, 64) == 0
+    assert L.dflash_int4_packed_bytes(32, 96, 32) == 0
+    assert L.dflash_f16_packed_bytes(16, 64) == 2048

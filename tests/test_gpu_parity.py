@@ -1,0 +1,235 @@
+"""Parity of the CUDA path (through the C ABI) with the CPU oracle, on seeded synthetic inputs."""
+import dataclasses
+
+import numpy as np
+import pytest
+
+import dflash_inputs as di
+from oracle import dflash_oracle as O
+from parity import LOGIT_REL, check_close, check_tokens, rel_err
+
+torch = pytest.importorskip("torch")
+pytestmark = [pytest.mark.gpu,
+              pytest.mark.skipif(not torch.cuda.is_available(), reason="needs a CUDA GPU")]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from speculative_block_drafter_gb300 import build
+    build.build()
+
+
+def _drafter():
+    from speculative_block_drafter_gb300 import drafter
+    return drafter
+
+
+def _rand_int4(rng, rows, cols, group, zero_groups=False):
+    q = rng.integers(-7, 8, size=(rows, cols))
+    scales = (rng.random((rows, cols // group)) * 0.05 + 1e-3).astype(np.float16)
+    if zero_groups:
+        scales[::3, ::2] = 0
+        q.reshape(rows, cols // group, group)[::3, ::2, :] = 0
+    u = (q + 8).astype(np.uint8)
+    codes = (u[:, 0::2] | (u[:, 1::2] << 4)).astype(np.uint8)
+    return di.Int4(codes=codes, scales=scales, rows=rows, cols=cols, group=group)
+
+
+# ------------------------------------------------------------------ dequant and GEMMs
+
+@pytest.mark.parametrize("rows,cols,group", [(16, 64, 32), (48, 256, 64), (32, 384, 128), (160, 1024, 64)])
+def test_dequant_bit_exact(rows, cols, group):
+    rng = np.random.default_rng(rows + cols)
+    m = _rand_int4(rng, rows, cols, group, zero_groups=True)
+    got = _drafter().dequant_int4(m)
+    ref = O.dequant_int4(m.codes, m.scales, group).astype(np.float32)
+    assert np.array_equal(got.view(np.uint32), ref.view(np.uint32))
+
+
+def test_dequant_bit_exact_generated_head():
+    g = di.workload("tiny").geometry
+    w = di.make_weights(g, 0)
+    m = w["head"]
+    got = _drafter().dequant_int4(m)
+    ref = O.dequant_int4(m.codes, m.scales, m.group).astype(np.float32)
+    assert np.array_equal(got.view(np.uint32), ref.view(np.uint32))
+
+
+def _bound(wabs: np.ndarray, x: np.ndarray) -> float:
+    return float((np.abs(x) @ wabs.T).max())
+
+
+@pytest.mark.parametrize("rows,cols,group,T", [(16, 64, 32, 1), (64, 256, 64, 5), (48, 512, 128, 16),
+                                               (96, 1024, 64, 17), (32, 2048, 64, 40), (2048, 5120, 64, 16)])
+def test_gemm_int4_matches_oracle(rows, cols, group, T):
+    rng = np.random.default_rng(rows * 7 + T)
+    m = _rand_int4(rng, rows, cols, group)
+    x = rng.standard_normal((T, cols)).astype(np.float32)
+    pm = _drafter().PackedMatrix(m)
+    y = pm.matmul(torch.from_numpy(x).cuda()).cpu().numpy()
+    ref = O.int4_matmul(m, x)
+    wabs = np.abs(O.dequant_int4(m.codes, m.scales, group))
+    err = np.abs(y - ref).max()
+    assert err <= 2e-6 * _bound(wabs, x), (err, _bound(wabs, x))
+
+
+@pytest.mark.parametrize("rows,cols,T", [(16, 64, 1), (64, 512, 16), (1280, 5120, 16), (128, 3072, 256), (64, 256, 33)])
+def test_gemm_f16_matches_oracle(rows, cols, T):
+    rng = np.random.default_rng(rows + cols + T)
+    w = (rng.standard_normal((rows, cols)) / np.sqrt(cols)).astype(np.float16)
+    x = rng.standard_normal((T, cols)).astype(np.float32)
+    pm = _drafter().PackedMatrix(w)
+    y = pm.matmul(torch.from_numpy(x).cuda()).cpu().numpy()
+    ref = O.f16_matmul(w, x)
+    err = np.abs(y - ref).max()
+    assert err <= 2e-6 * _bound(np.abs(w.astype(np.float64)), x.astype(np.float16).astype(np.float64)), err
+
+
+# ------------------------------------------------------------------ the pass
+
+class Pair:
+    """The GPU drafter and the oracle on the same weights."""
+
+    def __init__(self, g, seed=0, max_batch=1, ctx_cap=4096):
+        self.g = g
+        self.w = di.make_weights(g, seed)
+        self.gpu = _drafter().Drafter(g, self.w, max_batch=max_batch, ctx_cap=ctx_cap)
+        self.orc = [O.Oracle(g, self.w) for _ in range(max_batch)]
+
+    def settle(self, seq, pos, taps):
+        self.gpu.settle(seq, pos, torch.from_numpy(taps).cuda())
+        self.orc[seq].settle(pos, taps)
+
+    def reset(self, seq, first):
+        self.gpu.reset(seq, first)
+        self.orc[seq].reset(first)
+
+    def check_cache(self, seq=0):
+        torch.cuda.synchronize()
+        o = self.orc[seq]
+        f, n = self.gpu.context(seq)
+        assert (f, n) == (o.first, o.len)
+        worst = 0.0
+        for l in range(self.g.layers):
+            k = self.gpu.ctx_k[seq][l][:n].cpu().numpy()
+            v = self.gpu.ctx_v[seq][l][:n].cpu().numpy()
+            worst = max(worst, check_close(f"K layer {l}", k, o.ctx_k[l]), check_close(f"V layer {l}", v, o.ctx_v[l]))
+        return worst
+
+    def draft(self, anchors, hs_rows, anchor_toks, k=None, width=None):
+        g = self.g
+        k = g.block - 1 if k is None else k
+        width = g.vocab if width is None else width
+        h = torch.from_numpy(np.stack(hs_rows).astype(np.float32)).cuda().contiguous()
+        logits, hp = self.gpu.block(anchors, h, k, width)
+        at = torch.tensor(anchor_toks, dtype=torch.int32, device="cuda")
+        chosen, plain = self.gpu.select(logits, hp, at)
+        torch.cuda.synchronize()
+        res = []
+        for b in range(len(anchors)):
+            _, lo, hpo, ch, pl = self.orc[b].draft(anchors[b], hs_rows[b], anchor_toks[b], k, width)
+            lg = logits[b].cpu().numpy()
+            hg = hp[b].cpu().numpy()
+            el = check_close(f"logits seq {b}", lg, lo)
+            eh = check_close(f"hp seq {b}", hg, hpo)
+            ties = check_tokens(chosen[b].cpu().numpy(), plain[b].cpu().numpy(), hpo, lo, anchor_toks[b],
+                                self.w["pred_book"], self.w["succ_book"], g.selector_top)
+            res.append(dict(logit_err=el, hp_err=eh, ties=ties, chosen=chosen[b].cpu().numpy(),
+                            oracle_chosen=np.array(ch)))
+        return res
+
+
+def _tiny(**over):
+    return dataclasses.replace(di.workload("tiny").geometry, **over)
+
+
+def test_settle_tiny_matches_oracle_with_ragged_chunks():
+    g = _tiny()
+    p = Pair(g, ctx_cap=512)
+    taps = di.make_taps(g, 0, 301)
+    p.settle(0, 0, taps[:1])            # one row
+    p.settle(0, 1, taps[1:300])         # 256 + 43 rows, two calls
+    p.settle(0, 300, taps[300:301])
+    assert p.check_cache() < 1e-4
+    # rows at held positions replace them and what follows
+    other = di.make_taps(g, 5, 40)
+    p.settle(0, 200, other)
+    assert p.check_cache() < 1e-4
+
+
+def test_block_tiny_matches_oracle():
+    wl = di.workload("tiny")
+    g = wl.geometry
+    p = Pair(g)
+    p.settle(0, 0, di.make_taps(g, 0, wl.context))
+    a = di.anchor_token(g, 0)
+    r = p.draft([wl.context], [di.block_rows(g, 0, a)], [a])[0]
+    assert r["logit_err"] < 1e-4 and r["hp_err"] < 1e-4
+
+
+def test_select_alone_on_identical_inputs():
+    """The selector on the oracle's own logits and hp (f32): isolates it from the block."""
+    g = _tiny()
+    rng = np.random.default_rng(3)
+    w = di.make_weights(g, 0)
+    d = _drafter().Drafter(g, w, max_batch=2, ctx_cap=64)
+    k, width = g.block - 1, g.vocab
+    logits = rng.standard_normal((2, k, width)).astype(np.float32)
+    logits[0, 3, 10] = logits[0, 3, 20] = 9.0         # an exact tie: the lower index comes first
+    hp = rng.standard_normal((2, k, g.selector_rank)).astype(np.float32)
+    anchors = [5, 4000]
+    ch, pl = d.select(torch.from_numpy(logits).cuda(), torch.from_numpy(hp).cuda(),
+                      torch.tensor(anchors, dtype=torch.int32, device="cuda"))
+    ch, pl = ch.cpu().numpy(), pl.cpu().numpy()
+    for b in range(2):
+        och, opl = O.select_with(hp[b], logits[b], anchors[b], w["pred_book"], w["succ_book"], g.selector_top)
+        assert list(pl[b]) == opl
+        check_tokens(ch[b], pl[b], hp[b].astype(np.float64), logits[b].astype(np.float64), anchors[b],
+                     w["pred_book"], w["succ_book"], g.selector_top)
+    assert pl[0, 3] == 10
+
+
+@pytest.mark.parametrize("case", ["empty_context", "windowed", "short_k_shortlist", "no_rope_first_1000",
+                                  "batch3"])
+def test_block_edge_cases(case):
+    g = _tiny()
+    seeds = [0]
+    if case == "windowed":
+        g = _tiny(windows=(40,))
+    if case == "no_rope_first_1000":
+        g = _tiny(no_rope=(0,))
+    batch = 3 if case == "batch3" else 1
+    p = Pair(g, max_batch=batch, ctx_cap=512)
+    anchors, rows, toks, k, width = [], [], [], None, None
+    for b in range(batch):
+        first, n = 0, 100 + 37 * b
+        if case == "no_rope_first_1000":
+            first = 1000
+        p.reset(b, first)
+        if case != "empty_context":
+            p.settle(b, first, di.make_taps(g, b, n))
+        else:
+            n = 0
+        a = first + n
+        if case == "windowed":
+            a = 90                       # anchored inside the context: rows at and after it are excluded
+        tok = di.anchor_token(g, b + 1)
+        anchors.append(a)
+        rows.append(di.block_rows(g, b, tok))
+        toks.append(tok)
+    if case == "short_k_shortlist":
+        k, width = 3, 1024
+    for r in p.draft(anchors, rows, toks, k, width):
+        assert r["logit_err"] < 1e-4
+
+
+def test_full_qwen3_0p6b_workload():
+    """The bench's workload: 1024 positions settled in four chunks, then one block and the selector."""
+    wl = di.workload("qwen3-0.6b")
+    g = wl.geometry
+    p = Pair(g, ctx_cap=wl.context + 256)
+    p.settle(0, 0, di.make_taps(g, 0, wl.context))
+    assert p.check_cache() < 1e-4
+    a = di.anchor_token(g, 0)
+    r = p.draft([wl.context], [di.block_rows(g, 0, a)], [a])[0]
+    assert r["logit_err"] < 1e-4, r
