@@ -20,6 +20,7 @@ constexpr int ATT_THREADS = 256;
 constexpr int KEYS = 32;        // keys per step
 constexpr int QMAX = 64;        // queries per CTA (rep * block)
 constexpr int SPLIT_CTAS = 1024;
+constexpr int MIN_SPLIT_KEYS = 128;  // keys a split takes at least
 
 struct AttnArgs {
   AttnSeq seq[MAX_BATCH];
@@ -29,7 +30,7 @@ static int splits_for(int batch, int kv, int max_n) {
   if (max_n <= 0) return 0;
   int s = SPLIT_CTAS / std::max(1, batch * kv);
   s = std::max(1, std::min(s, 128));
-  s = std::min(s, (max_n + KEYS - 1) / KEYS);
+  s = std::min(s, (max_n + MIN_SPLIT_KEYS - 1) / MIN_SPLIT_KEYS);
   return s;
 }
 

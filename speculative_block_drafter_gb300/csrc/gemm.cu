@@ -196,7 +196,7 @@ __device__ __forceinline__ uint4 ldg_stream(const uint4 *p) {
 
 // out_mode: 0 store, 1 atomic add, 2 plain add (each element owned by one thread)
 template <bool INT4, int NB, int PF>
-__global__ void __launch_bounds__(GW * 32) k_gemm(const uint4 *__restrict__ W, const uint32_t *__restrict__ S,
+__global__ void __launch_bounds__(GW * 32, INT4 ? 2 : 1) k_gemm(const uint4 *__restrict__ W, const uint32_t *__restrict__ S,
                                                   int group, int N, int K, const float *__restrict__ X, int ldx,
                                                   float *__restrict__ Y, int ldy, int T, int kc, int out_mode) {
   extern __shared__ uint4 sm[];
@@ -205,14 +205,36 @@ __global__ void __launch_bounds__(GW * 32) k_gemm(const uint4 *__restrict__ W, c
   const int tok0 = blockIdx.x * 16;
   const int kt0 = blockIdx.z * kc, kt1 = min(KT, kt0 + kc);
   if (kt0 >= kt1) return;
-  stage_x<INT4>(sm, X, ldx, T, tok0, kt0 * 64, (kt1 - kt0) * 4);
-  __syncthreads();
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, c = lane & 3;
   const int RB = (N + 15) / 16;
   const int rb0 = (blockIdx.y * GW + warp) * NB;
-  if (rb0 >= RB) return;
+  const bool active = rb0 < RB;
   const int NG = INT4 ? K / group : 0;
+
+  const uint4 *wp[NB];
+  bool live[NB];
+#pragma unroll
+  for (int i = 0; i < NB; ++i) {
+    live[i] = rb0 + i < RB;
+    const int rb = live[i] ? rb0 + i : (active ? rb0 : 0);
+    wp[i] = W + ((int64_t)rb * KT) * (32 * WV) + lane;
+  }
+
+  // the first weight tiles are in flight while the activations are staged
+  uint4 buf[PF][NB][WV];
+#pragma unroll
+  for (int p = 0; p < PF; ++p)
+#pragma unroll
+    for (int i = 0; i < NB; ++i)
+#pragma unroll
+      for (int v = 0; v < WV; ++v)
+        buf[p][i][v] = (active && kt0 + p < kt1) ? ldg_stream(wp[i] + (int64_t)(kt0 + p) * (32 * WV) + v * 32)
+                                                 : make_uint4(0, 0, 0, 0);
+
+  stage_x<INT4>(sm, X, ldx, T, tok0, kt0 * 64, (kt1 - kt0) * 4);
+  __syncthreads();
+  if (!active) return;
 
   float acc[NB][2][4];
 #pragma unroll
@@ -221,25 +243,6 @@ __global__ void __launch_bounds__(GW * 32) k_gemm(const uint4 *__restrict__ W, c
     for (int t = 0; t < 2; ++t)
 #pragma unroll
       for (int e = 0; e < 4; ++e) acc[i][t][e] = 0.f;
-
-  const uint4 *wp[NB];
-  bool live[NB];
-#pragma unroll
-  for (int i = 0; i < NB; ++i) {
-    live[i] = rb0 + i < RB;
-    const int rb = live[i] ? rb0 + i : rb0;
-    wp[i] = W + ((int64_t)rb * KT) * (32 * WV) + lane;
-  }
-
-  uint4 buf[PF][NB][WV];
-#pragma unroll
-  for (int p = 0; p < PF; ++p)
-#pragma unroll
-    for (int i = 0; i < NB; ++i)
-#pragma unroll
-      for (int v = 0; v < WV; ++v)
-        buf[p][i][v] = (kt0 + p < kt1) ? ldg_stream(wp[i] + (int64_t)(kt0 + p) * (32 * WV) + v * 32)
-                                       : make_uint4(0, 0, 0, 0);
 
   for (int kt = kt0; kt < kt1; kt += PF) {
 #pragma unroll

@@ -4,156 +4,218 @@
 // token chosen before: score = logit + (P[prev] * hp) . C[cand], the first
 // strictly greater score winning, the chain starting at the anchor token.
 //
-// Stage 1 (many CTAs): each chunk of a row's logits yields its own top `top`.
-// Stage 2 (one CTA per sequence): per row, the chunks' candidates merge into the
-// row's top `top`, then the row's choice, which the next row needs.
+// Stage 1 (chunks x rows CTAs): each chunk of 2048 logits yields its own top `top`.
+// Stage 2 (one CTA per row): the chunks' candidates merge into the row's top `top`.
+// Stage 3 (one CTA per sequence): the chain. Row j's predecessor is the anchor
+// (j = 0) or one of row j-1's candidates, so every score the chain can ask for is
+// computed first, in parallel; the chain itself then only compares numbers.
 #include "common.cuh"
 #include "kernels.h"
 
 namespace dfl {
 
 constexpr int SEL_THREADS = 256;
-constexpr int SEL_PER = 8;                       // logits per thread in stage 1
-constexpr int SEL_CHUNK = SEL_THREADS * SEL_PER;  // logits per chunk
-constexpr int MERGE_PER = 16;                    // candidates per thread in stage 2
+constexpr int SEL_PER = 8;                         // logits per thread in stage 1
+constexpr int SEL_CHUNK = SEL_THREADS * SEL_PER;   // logits per chunk
+constexpr int MERGE_PER = 16;                      // candidates per thread in stage 2
 constexpr int TOP_MAX = 32;
 constexpr int RANK_MAX = 256;
+constexpr int CHAIN_THREADS = 512;
+constexpr int KMAX = 15;
 
 static inline int sel_chunks(int width) { return (width + SEL_CHUNK - 1) / SEL_CHUNK; }
 
 size_t select_scratch_bytes(int max_rows, int width, int top) {
-  return (size_t)max_rows * sel_chunks(width) * top * sizeof(unsigned long long);
+  return (size_t)max_rows * (sel_chunks(width) + 1) * top * sizeof(unsigned long long);
 }
 
-// Block-wide maximum of one key per thread; every thread gets it.
-__device__ __forceinline__ unsigned long long block_max_u64(unsigned long long v, unsigned long long *red) {
-  v = warp_max_u64(v);
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (lane == 0) red[warp] = v;
-  __syncthreads();
-  unsigned long long m = 0;
-  if (threadIdx.x < 32) {
-    m = threadIdx.x < (blockDim.x >> 5) ? red[threadIdx.x] : 0ull;
-    m = warp_max_u64(m);
-    if (threadIdx.x == 0) red[32] = m;
+// The `top` largest keys of a warp (N keys per lane in `keys`), largest first,
+// written by lane 0 to out[0..top). Keys are unique except 0 (= none).
+template <int N>
+__device__ __forceinline__ void warp_top(unsigned long long (&keys)[N], int top, unsigned long long *out) {
+  const int lane = threadIdx.x & 31;
+  for (int t = 0; t < top; ++t) {
+    unsigned long long mine = 0;
+#pragma unroll
+    for (int i = 0; i < N; ++i) mine = keys[i] > mine ? keys[i] : mine;
+    const unsigned long long best = warp_max_u64(mine);
+    if (best != 0ull && mine == best) {
+#pragma unroll
+      for (int i = 0; i < N; ++i)
+        if (keys[i] == best) keys[i] = 0ull;
+    }
+    if (lane == 0) out[t] = best;
   }
-  __syncthreads();
-  m = red[32];
-  __syncthreads();
-  return m;
 }
 
+// One CTA per (chunk, row): every warp takes 256 logits and keeps its top; one
+// warp then takes the top of the warps' lists.
 __global__ void __launch_bounds__(SEL_THREADS) k_topk_chunks(const float *__restrict__ logits, int width, int top,
                                                              unsigned long long *__restrict__ cand) {
-  __shared__ unsigned long long red[33];
+  __shared__ unsigned long long wl[SEL_THREADS / 32][TOP_MAX];
   const int chunk = blockIdx.x, row = blockIdx.y;
   const int nchunks = gridDim.x;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const float *lr = logits + (int64_t)row * width;
   unsigned long long keys[SEL_PER];
 #pragma unroll
   for (int i = 0; i < SEL_PER; ++i) {
-    const int idx = chunk * SEL_CHUNK + i * SEL_THREADS + threadIdx.x;
+    const int idx = chunk * SEL_CHUNK + warp * 256 + i * 32 + lane;
     keys[i] = idx < width ? cand_key(lr[idx], (uint32_t)idx) : 0ull;
   }
-  unsigned long long* out = cand + ((int64_t)row * nchunks + chunk) * top;
-  for (int t = 0; t < top; ++t) {
-    unsigned long long mine = 0;
+  warp_top<SEL_PER>(keys, top, wl[warp]);
+  __syncthreads();
+  if (warp == 0) {
+    constexpr int M = SEL_THREADS / 32 * TOP_MAX / 32;  // keys per lane in the final round
+    unsigned long long k2[M];
 #pragma unroll
-    for (int i = 0; i < SEL_PER; ++i) mine = keys[i] > mine ? keys[i] : mine;
-    const unsigned long long best = block_max_u64(mine, red);
-    if (best != 0ull && mine == best) {
-#pragma unroll
-      for (int i = 0; i < SEL_PER; ++i)
-        if (keys[i] == best) keys[i] = 0ull;
+    for (int i = 0; i < M; ++i) {
+      const int idx = i * 32 + lane;  // over [warps][top]
+      const int w = idx / TOP_MAX, t = idx % TOP_MAX;
+      k2[i] = t < top ? wl[w][t] : 0ull;
     }
-    if (threadIdx.x == 0) out[t] = best;
+    warp_top<M>(k2, top, cand + ((int64_t)row * nchunks + chunk) * top);
   }
 }
 
-__global__ void __launch_bounds__(SEL_THREADS) k_select(const float *__restrict__ logits, const float *__restrict__ hp,
-                                                        const uint32_t *__restrict__ anchor_tok,
-                                                        const uint16_t *__restrict__ pred,
-                                                        const uint16_t *__restrict__ succ, int k, int width, int rank,
-                                                        int top, int nchunks, int vocab,
-                                                        const unsigned long long *__restrict__ cand,
-                                                        uint32_t *__restrict__ chosen, uint32_t *__restrict__ plain) {
-  __shared__ unsigned long long red[33];
-  __shared__ uint32_t ctok[TOP_MAX];
-  __shared__ float cscore[TOP_MAX];
-  __shared__ float pc[RANK_MAX];
-  __shared__ uint32_t prev_s;
-  const int b = blockIdx.x;
+// One CTA per row: merge the chunks' lists into the row's top `top`.
+__global__ void __launch_bounds__(SEL_THREADS) k_topk_merge(const unsigned long long *__restrict__ cand, int nchunks,
+                                                            int top, unsigned long long *__restrict__ best) {
+  __shared__ unsigned long long wl[SEL_THREADS / 32][TOP_MAX];
+  const int row = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int ncand = nchunks * top;
-  if (threadIdx.x == 0) prev_s = anchor_tok[b];
+  const unsigned long long *cr = cand + (int64_t)row * ncand;
+  unsigned long long keys[MERGE_PER];
+#pragma unroll
+  for (int i = 0; i < MERGE_PER; ++i) {
+    const int idx = (warp * MERGE_PER + i) * 32 + lane;
+    keys[i] = idx < ncand ? cr[idx] : 0ull;
+  }
+  warp_top<MERGE_PER>(keys, top, wl[warp]);
   __syncthreads();
-  if (prev_s >= (uint32_t)vocab) {  // not a token: the sequence's outputs say so
-    for (int j = threadIdx.x; j < k; j += SEL_THREADS) chosen[b * k + j] = plain[b * k + j] = 0xFFFFFFFFu;
+  if (warp == 0) {
+    constexpr int M = SEL_THREADS / 32 * TOP_MAX / 32;
+    unsigned long long k2[M];
+#pragma unroll
+    for (int i = 0; i < M; ++i) {
+      const int idx = i * 32 + lane;
+      const int w = idx / TOP_MAX, t = idx % TOP_MAX;
+      k2[i] = t < top ? wl[w][t] : 0ull;
+    }
+    warp_top<M>(k2, top, best + (int64_t)row * top);
+  }
+}
+
+// One CTA per sequence: the score of every (row, predecessor, candidate) the
+// chain can meet, then the chain. The codebook rows involved (P of every
+// possible predecessor, C of every candidate) and hp are read into shared
+// memory once, in parallel; rows are taken in slabs of `slab` when they do not
+// all fit.
+__global__ void __launch_bounds__(CHAIN_THREADS) k_select_chain(
+    const float *__restrict__ logits, const float *__restrict__ hp, const uint32_t *__restrict__ anchor_tok,
+    const uint16_t *__restrict__ pred, const uint16_t *__restrict__ succ, int k, int width, int rank, int top,
+    int vocab, int slab, const unsigned long long *__restrict__ best, uint32_t *__restrict__ chosen,
+    uint32_t *__restrict__ plain) {
+  __shared__ uint32_t ctok[KMAX][TOP_MAX];
+  __shared__ float clogit[KMAX][TOP_MAX];
+  extern __shared__ float dyn[];
+  float *score = dyn;                                        // [k][top][top]
+  float *hps = score + k * top * top;                        // [slab][rank]
+  uint16_t *Ps = (uint16_t *)(hps + slab * rank);            // [slab][top][rank]
+  uint16_t *Cs = Ps + (size_t)slab * top * rank;             // [slab][top][rank]
+  const int b = blockIdx.x;
+  const uint32_t anchor = anchor_tok[b];
+  if (anchor >= (uint32_t)vocab) {  // not a token: the sequence's outputs say so
+    for (int j = threadIdx.x; j < k; j += CHAIN_THREADS) chosen[b * k + j] = plain[b * k + j] = 0xFFFFFFFFu;
     return;
   }
-  for (int j = 0; j < k; ++j) {
-    const int row = b * k + j;
-    const unsigned long long *cr = cand + (int64_t)row * ncand;
-    unsigned long long keys[MERGE_PER];
-#pragma unroll
-    for (int i = 0; i < MERGE_PER; ++i) {
-      const int idx = i * SEL_THREADS + threadIdx.x;
-      keys[i] = idx < ncand ? cr[idx] : 0ull;
+  for (int i = threadIdx.x; i < k * top; i += CHAIN_THREADS) {
+    const int j = i / top, c = i % top;
+    const uint32_t tok = cand_index(best[((int64_t)b * k + j) * top + c]);
+    ctok[j][c] = tok;
+    clogit[j][c] = logits[((int64_t)b * k + j) * width + tok];
+  }
+  __syncthreads();
+  const int r2 = rank / 2;  // u32 pairs per codebook row
+  for (int j0 = 0; j0 < k; j0 += slab) {
+    const int nj = min(slab, k - j0);
+    // rows of this slab: P of each predecessor (the anchor for row 0), C of each candidate, hp
+    for (int i = threadIdx.x; i < nj * top * r2; i += CHAIN_THREADS) {
+      const int jj = i / (top * r2), p = (i / r2) % top, e = i % r2;
+      const int j = j0 + jj;
+      const uint32_t prev = j == 0 ? anchor : ctok[j - 1][p];
+      ((uint32_t *)Ps)[(jj * top + p) * r2 + e] = ((const uint32_t *)(pred + (int64_t)prev * rank))[e];
+      ((uint32_t *)Cs)[(jj * top + p) * r2 + e] = ((const uint32_t *)(succ + (int64_t)ctok[j][p] * rank))[e];
     }
-    for (int t = 0; t < top; ++t) {
-      unsigned long long mine = 0;
-#pragma unroll
-      for (int i = 0; i < MERGE_PER; ++i) mine = keys[i] > mine ? keys[i] : mine;
-      const unsigned long long best = block_max_u64(mine, red);
-      if (best != 0ull && mine == best) {
-#pragma unroll
-        for (int i = 0; i < MERGE_PER; ++i)
-          if (keys[i] == best) keys[i] = 0ull;
-      }
-      if (threadIdx.x == 0) ctok[t] = cand_index(best);
-    }
-    const uint32_t prev = prev_s;
-    for (int i = threadIdx.x; i < rank; i += SEL_THREADS)
-      pc[i] = __half2float(__ushort_as_half(pred[(int64_t)prev * rank + i])) * hp[(int64_t)row * rank + i];
+    for (int i = threadIdx.x; i < nj * rank; i += CHAIN_THREADS)
+      hps[i] = hp[((int64_t)b * k + j0) * rank + i];
     __syncthreads();
-    for (int c = warp; c < top; c += SEL_THREADS / 32) {
-      const uint32_t tok = ctok[c];
+    // score[j][p][c] = logit[j][c] + sum_i (P[prev_p][i] * hp[j][i]) * C[cand_c][i]
+    for (int it = threadIdx.x; it < nj * top * top; it += CHAIN_THREADS) {
+      const int jj = it / (top * top), p = (it / top) % top, c = it % top;
+      const int j = j0 + jj;
+      if (j == 0 && p > 0) continue;
+      const __half2 *pr = (const __half2 *)(Ps + (jj * top + p) * rank);
+      const __half2 *cr = (const __half2 *)(Cs + (jj * top + c) * rank);
+      const float *hr = hps + jj * rank;
       float acc = 0.f;
-      for (int i = lane; i < rank; i += 32)
-        acc = fmaf(pc[i], __half2float(__ushort_as_half(succ[(int64_t)tok * rank + i])), acc);
-      acc = warp_sum(acc);
-      if (lane == 0) cscore[c] = logits[(int64_t)row * width + tok] + acc;
-    }
-    __syncthreads();
-    if (threadIdx.x == 0) {
-      float best = -INFINITY;
-      uint32_t bt = ctok[0];
-      for (int c = 0; c < top; ++c) {
-        if (cscore[c] > best) {
-          best = cscore[c];
-          bt = ctok[c];
-        }
+      for (int e = 0; e < r2; ++e) {
+        const float2 pv = __half22float2(pr[e]);
+        const float2 cv = __half22float2(cr[e]);
+        acc = fmaf(pv.x * hr[2 * e], cv.x, acc);
+        acc = fmaf(pv.y * hr[2 * e + 1], cv.y, acc);
       }
-      chosen[row] = bt;
-      plain[row] = ctok[0];
-      prev_s = bt;
+      score[(j * top + p) * top + c] = clogit[j][c] + acc;
     }
     __syncthreads();
   }
+  if (threadIdx.x == 0) {
+    int slot = 0;  // the predecessor's slot among the previous row's candidates
+    for (int j = 0; j < k; ++j) {
+      float bs = -INFINITY;
+      int bc = 0;
+      for (int c = 0; c < top; ++c) {
+        const float sc = score[(j * top + slot) * top + c];
+        if (sc > bs) {
+          bs = sc;
+          bc = c;
+        }
+      }
+      chosen[b * k + j] = ctok[j][bc];
+      plain[b * k + j] = ctok[j][0];
+      slot = bc;
+    }
+  }
+}
+
+static size_t chain_smem(int k, int top, int rank, int slab) {
+  return (size_t)k * top * top * 4 + (size_t)slab * rank * 4 + 2 * (size_t)slab * top * rank * 2;
 }
 
 cudaError_t select_tokens(const float *logits, const float *hp, const uint32_t *anchor_tok, const uint16_t *pred,
                           const uint16_t *succ, int batch, int k, int width, int rank, int top, int vocab, void *scratch,
                           uint32_t *chosen, uint32_t *plain, cudaStream_t st) {
-  if (top > TOP_MAX || rank > RANK_MAX || top < 1) return cudaErrorInvalidValue;
+  if (top > TOP_MAX || rank > RANK_MAX || top < 1 || k > KMAX) return cudaErrorInvalidValue;
   const int nchunks = sel_chunks(width);
   if (nchunks * top > MERGE_PER * SEL_THREADS) return cudaErrorInvalidValue;
   unsigned long long *cand = (unsigned long long *)scratch;
+  unsigned long long *best = cand + (size_t)batch * k * nchunks * top;
   dim3 g1(nchunks, batch * k);
   k_topk_chunks<<<g1, SEL_THREADS, 0, st>>>(logits, width, top, cand);
-  k_select<<<batch, SEL_THREADS, 0, st>>>(logits, hp, anchor_tok, pred, succ, k, width, rank, top, nchunks, vocab, cand,
-                                          chosen, plain);
-  count_launch(2);
+  k_topk_merge<<<batch * k, SEL_THREADS, 0, st>>>(cand, nchunks, top, best);
+  constexpr size_t SMEM_MAX = 200 * 1024;
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(k_select_chain, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_MAX);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  int slab = k;
+  while (slab > 1 && chain_smem(k, top, rank, slab) > SMEM_MAX) --slab;
+  k_select_chain<<<batch, CHAIN_THREADS, chain_smem(k, top, rank, slab), st>>>(
+      logits, hp, anchor_tok, pred, succ, k, width, rank, top, vocab, slab, best, chosen, plain);
+  count_launch(3);
   return cudaGetLastError();
 }
 

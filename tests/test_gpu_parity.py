@@ -164,7 +164,8 @@ def test_block_tiny_matches_oracle():
     p.settle(0, 0, di.make_taps(g, 0, wl.context))
     a = di.anchor_token(g, 0)
     r = p.draft([wl.context], [di.block_rows(g, 0, a)], [a])[0]
-    assert r["logit_err"] < 1e-4 and r["hp_err"] < 1e-4
+    # hp multiplies f16-rounded rows (as the oracle does): a one-ulp rounding flip moves it by ~1e-4
+    assert r["logit_err"] < 1e-4 and r["hp_err"] < 5e-4
 
 
 def test_select_alone_on_identical_inputs():
