@@ -173,6 +173,30 @@ int dflash_select(dflash_t *d, int32_t batch, const float *logits, const float *
                   const uint32_t *anchor_tok, int32_t k, int32_t width, uint32_t *chosen,
                   uint32_t *plain, void *stream);
 
+/* The selector for callers that cannot allocate device memory: code running
+ * under another framework's memory pool (which owns the device heap and does
+ * not let a plug-in call cudaMalloc), decode loops that must not take
+ * cudaMalloc's implicit device-wide synchronisation mid-token, and
+ * foreign-function callers with no device allocator. The pages have no
+ * counterpart of this call; it computes what dflash_select computes (same
+ * arguments and outputs, the codebooks f16 [vocab][rank] and the sizes passed
+ * directly, no drafter handle) and needs no workspace: its candidate scratch
+ * is a fixed 8 MiB array inside the library, held by every GPU that loads the
+ * library until the process exits, so
+ * batch * k * (ceil(width / 2048) + 1) * top * 8 bytes must fit in 8 MiB
+ * (else DFLASH_E_CAPACITY; dflash_select has no such limit). The first call
+ * on a device looks up that device's address of the array
+ * (cudaGetSymbolAddress); make that first call before any stream capture.
+ * Every call on a device shares the one array, so calls that overlap on the
+ * GPU (other streams, other threads) race; serialise them. Nothing in the
+ * array needs to start at zero: a call reads only slots it wrote itself.
+ * It calls no cudaMalloc, cudaFree or allocating library routine.
+ * Errors: ARG, CAPACITY, CUDA. */
+int dflash_select_static(const float *logits, const float *hp, const uint32_t *anchor_tok,
+                         const uint16_t *pred_book, const uint16_t *succ_book, int32_t batch, int32_t k,
+                         int32_t width, int32_t vocab, int32_t rank, int32_t top, uint32_t *chosen,
+                         uint32_t *plain, void *stream);
+
 void dflash_destroy(dflash_t *d);
 
 /* The message of the calling thread's last failure ("" if none). */

@@ -80,6 +80,9 @@ EXPORTS = {
                                C.c_void_p, C.c_void_p, C.c_void_p]),
     "dflash_select": (C.c_int, [C.c_void_p, C.c_int32, C.c_void_p, C.c_void_p, C.c_void_p, C.c_int32, C.c_int32,
                                 C.c_void_p, C.c_void_p, C.c_void_p]),
+    "dflash_select_static": (C.c_int, [C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_int32,
+                                       C.c_int32, C.c_int32, C.c_int32, C.c_int32, C.c_int32, C.c_void_p,
+                                       C.c_void_p, C.c_void_p]),
     "dflash_destroy": (None, [C.c_void_p]),
     "dflash_last_error": (C.c_char_p, []),
     "dflash_launch_count": (C.c_uint64, []),
@@ -175,6 +178,13 @@ def dflash_block(h, batch, anchor_pos, hrows, k, width, logits, hp, stream):
 
 def dflash_select(h, batch, logits, hp, anchor_tok, k, width, chosen, plain, stream):
     _check(lib().dflash_select(h, batch, logits, hp, anchor_tok, k, width, chosen, plain, stream))
+
+
+def dflash_select_static(logits, hp, anchor_tok, pred_book, succ_book, batch, k, width, vocab, rank, top, chosen,
+                         plain, stream):
+    """The selector with its scratch inside the library (for callers that cannot allocate device memory)."""
+    _check(lib().dflash_select_static(logits, hp, anchor_tok, pred_book, succ_book, batch, k, width, vocab, rank,
+                                      top, chosen, plain, stream))
 
 
 def dflash_destroy(h):

@@ -103,6 +103,15 @@ std::string check_geometry(const dflash_geometry &g) {
   return "";
 }
 
+}  // namespace
+
+namespace dfl {
+// Record a failure message for dflash_last_error() from another file of the library.
+int dflash_fail(int code, const std::string &msg) { return fail(code, msg); }
+}  // namespace dfl
+
+namespace {
+
 bool int4_ok(const dflash_matrix &m) { return m.data && m.scales && aligned16(m.data) && aligned16(m.scales); }
 bool f16_ok(const dflash_matrix &m) { return m.data && aligned16(m.data); }
 

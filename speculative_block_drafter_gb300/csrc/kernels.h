@@ -4,12 +4,15 @@
 #include <stdint.h>
 
 #include <atomic>
+#include <string>
 
 namespace dfl {
 
 // Kernel launches enqueued by the library in this process.
 extern std::atomic<unsigned long long> g_launches;
 inline void count_launch(int n = 1) { g_launches.fetch_add((unsigned long long)n, std::memory_order_relaxed); }
+// Set the calling thread's dflash_last_error() message; returns `code`.
+int dflash_fail(int code, const std::string &msg);
 
 // -------------------------------------------------------------- packing (gemm.cu)
 size_t int4_packed_bytes(int64_t rows, int64_t cols);

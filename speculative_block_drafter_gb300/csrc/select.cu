@@ -9,7 +9,11 @@
 // Stage 3 (one CTA per sequence): the chain. Row j's predecessor is the anchor
 // (j = 0) or one of row j-1's candidates, so every score the chain can ask for is
 // computed first, in parallel; the chain itself then only compares numbers.
+#include <mutex>
+#include <string>
+
 #include "common.cuh"
+#include "dflash.h"
 #include "kernels.h"
 
 namespace dfl {
@@ -220,3 +224,73 @@ cudaError_t select_tokens(const float *logits, const float *hp, const uint32_t *
 }
 
 }  // namespace dfl
+
+// ---------------------------------------------------------------------------
+// The selector for callers that cannot allocate device memory.
+//
+// Some callers have no way to hand the library scratch memory: code that runs
+// under another framework's memory pool (which owns the device heap and does
+// not let a plug-in call cudaMalloc), decode loops that must not take
+// cudaMalloc's implicit device-wide synchronisation in the middle of a token,
+// and foreign-function callers with no device allocator of their own. For
+// them the selector's candidate scratch lives in a fixed array below, part of
+// the library image: every GPU that loads the library holds it until the
+// process exits.
+
+namespace dfl {
+namespace {
+
+constexpr size_t kStaticSelectScratch = 8u << 20;  // bytes: 32 sequences x 15 rows at a 151,936 vocabulary
+static __device__ __align__(256) unsigned char g_select_scratch[kStaticSelectScratch];
+
+// Host code cannot use g_select_scratch as a device address (in host code the
+// name is a host-side stand-in), so each device's address is looked up once.
+std::mutex g_scratch_mu;
+void *g_scratch_addr[64] = {};
+
+cudaError_t static_scratch(void **out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  if (!g_scratch_addr[dev]) {
+    void *p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_select_scratch);
+    if (e != cudaSuccess) return e;
+    g_scratch_addr[dev] = p;
+  }
+  *out = g_scratch_addr[dev];
+  return cudaSuccess;
+}
+
+}  // namespace
+
+}  // namespace dfl
+
+extern "C" int dflash_select_static(const float *logits, const float *hp, const uint32_t *anchor_tok,
+                                    const uint16_t *pred_book, const uint16_t *succ_book, int32_t batch, int32_t k,
+                                    int32_t width, int32_t vocab, int32_t rank, int32_t top, uint32_t *chosen,
+                                    uint32_t *plain, void *stream) {
+  using namespace dfl;
+  if (!logits || !hp || !anchor_tok || !pred_book || !succ_book || !chosen || !plain)
+    return dflash_fail(DFLASH_E_ARG, "select_static: null pointer");
+  if (batch < 1 || k < 1 || k > KMAX || top < 1 || top > TOP_MAX || width < top || width > vocab ||
+      rank < 16 || rank > RANK_MAX || rank % 16)
+    return dflash_fail(DFLASH_E_ARG, "select_static: batch >= 1, 1 <= k <= 15, 1 <= top <= 32, "
+                                     "top <= width <= vocab, rank a multiple of 16 in 16..256");
+  if (sel_chunks(width) * top > MERGE_PER * SEL_THREADS)
+    return dflash_fail(DFLASH_E_ARG, "select_static: width / top beyond the selector's merge");
+  const size_t need = select_scratch_bytes(batch * k, width, top);
+  if (need > kStaticSelectScratch)
+    return dflash_fail(DFLASH_E_CAPACITY, "select_static: batch * k * (width / 2048 + 1) * top * 8 bytes of "
+                                          "candidates exceed the fixed 8 MiB scratch; use dflash_select");
+  void *scratch = nullptr;
+  cudaError_t e = static_scratch(&scratch);
+  if (e != cudaSuccess)
+    return dflash_fail(DFLASH_E_CUDA, std::string("select_static: cudaGetSymbolAddress: ") + cudaGetErrorString(e));
+  e = select_tokens(logits, hp, anchor_tok, pred_book, succ_book, batch, k, width, rank, top, vocab, scratch,
+                    chosen, plain, (cudaStream_t)stream);
+  if (e != cudaSuccess) return dflash_fail(DFLASH_E_CUDA, std::string("select_static: ") + cudaGetErrorString(e));
+  return DFLASH_OK;
+}
