@@ -92,7 +92,7 @@ typedef struct dflash_t dflash_t;
 /* ---- packing (the library's matrix layouts) -------------------------------- */
 
 /* Bytes of the packed codes and of the packed scales of a four-bit matrix
- * [rows][cols]; rows % 16 == 0, cols % 64 == 0, group in {32, 64, 128}.
+ * [rows][cols]; cols % 64 == 0, group in {32, 64, 128}, rows padded to 128.
  * Returns 0 for a shape the library does not take. */
 size_t dflash_int4_packed_bytes(int64_t rows, int64_t cols, int32_t group);
 size_t dflash_int4_scale_bytes(int64_t rows, int64_t cols, int32_t group);
@@ -118,10 +118,18 @@ int dflash_dequant_int4(const void *codes, const void *scales, int64_t rows, int
  * Y[t][r] = sum_c X[t][c] W[r][c], f32 X [T][cols] and Y [T][rows] (device,
  * row-major). `kind` 4: a four-bit matrix (group `group`; X enters at full f32
  * precision as f16 hi + lo planes); `kind` 16: an f16 matrix (X rounded to f16,
- * as the card arm's `to_half` before its f16 GEMM). Exposed for checking the
- * kernels the pass uses. Errors: ARG, CUDA. */
+ * as the card arm's `to_half` before its f16 GEMM). `workspace` (device,
+ * 16-byte aligned) receives the packed rows of X: at least
+ * dflash_gemm_workspace_bytes(kind, cols, T) bytes. Exposed for checking the
+ * kernels the pass uses. Errors: ARG, CAPACITY, CUDA. */
+size_t dflash_gemm_workspace_bytes(int32_t kind, int64_t cols, int32_t T);
 int dflash_gemm(const dflash_matrix *w, int32_t kind, int64_t rows, int64_t cols, int32_t group, const float *x,
-                int32_t T, float *y, void *stream);
+                int32_t T, float *y, void *workspace, size_t workspace_bytes, void *stream);
+
+/* The library's device error word: bit 0 is set when one of its kernels gave
+ * up a bounded wait (the kernel then stopped early and its outputs are not to
+ * be trusted). Reads it (synchronising the device) and clears it if `reset`. */
+int dflash_device_error(uint32_t *error, int32_t reset);
 
 /* ---- the drafter ----------------------------------------------------------- */
 
@@ -182,14 +190,16 @@ int dflash_select(dflash_t *d, int32_t batch, const float *logits, const float *
  * arguments and outputs, the codebooks f16 [vocab][rank] and the sizes passed
  * directly, no drafter handle) and needs no workspace: its candidate scratch
  * is a fixed 8 MiB array inside the library, held by every GPU that loads the
- * library until the process exits, so
- * batch * k * (ceil(width / 2048) + 1) * top * 8 bytes must fit in 8 MiB
- * (else DFLASH_E_CAPACITY; dflash_select has no such limit). The first call
+ * library until the process exits, so a call's candidates and score tables,
+ * batch * k * (ceil(width / 2048) * top * 8 + top * 4 + top * top * 4 + 4) + 256
+ * bytes, must fit in 8 MiB (else DFLASH_E_CAPACITY; dflash_select has no such
+ * limit). The first call
  * on a device looks up that device's address of the array
  * (cudaGetSymbolAddress); make that first call before any stream capture.
  * Every call on a device shares the one array, so calls that overlap on the
- * GPU (other streams, other threads) race; serialise them. Nothing in the
- * array needs to start at zero: a call reads only slots it wrote itself.
+ * GPU (other streams, other threads) race; serialise them. The one part that
+ * must start at zero (a per-sequence counter) is cleared by each call itself;
+ * everything else a call reads it wrote itself.
  * It calls no cudaMalloc, cudaFree or allocating library routine.
  * Errors: ARG, CAPACITY, CUDA. */
 int dflash_select_static(const float *logits, const float *hp, const uint32_t *anchor_tok,

@@ -68,8 +68,10 @@ EXPORTS = {
     "dflash_pack_f16": (C.c_int, [C.c_void_p, C.c_int64, C.c_int64, C.c_void_p, C.c_void_p]),
     "dflash_dequant_int4": (C.c_int, [C.c_void_p, C.c_void_p, C.c_int64, C.c_int64, C.c_int32, C.c_void_p,
                                       C.c_void_p]),
+    "dflash_gemm_workspace_bytes": (C.c_size_t, [C.c_int32, C.c_int64, C.c_int32]),
     "dflash_gemm": (C.c_int, [C.POINTER(Matrix), C.c_int32, C.c_int64, C.c_int64, C.c_int32, C.c_void_p, C.c_int32,
-                              C.c_void_p, C.c_void_p]),
+                              C.c_void_p, C.c_void_p, C.c_size_t, C.c_void_p]),
+    "dflash_device_error": (C.c_int, [C.POINTER(C.c_uint32), C.c_int32]),
     "dflash_workspace_bytes": (C.c_size_t, [C.POINTER(Geometry), C.c_int32]),
     "dflash_create": (C.c_int, [C.POINTER(C.c_void_p), C.POINTER(Geometry), C.POINTER(Weights), C.c_int32,
                                 C.POINTER(C.c_void_p), C.POINTER(C.c_void_p), C.c_int64, C.c_void_p, C.c_size_t]),
@@ -140,8 +142,18 @@ def dflash_dequant_int4(codes, scales, rows, cols, group, out, stream):
     _check(lib().dflash_dequant_int4(codes, scales, rows, cols, group, out, stream))
 
 
-def dflash_gemm(w: Matrix, kind, rows, cols, group, x, T, y, stream):
-    _check(lib().dflash_gemm(C.byref(w), kind, rows, cols, group, x, T, y, stream))
+def dflash_gemm_workspace_bytes(kind, cols, T):
+    return lib().dflash_gemm_workspace_bytes(kind, cols, T)
+
+
+def dflash_gemm(w: Matrix, kind, rows, cols, group, x, T, y, workspace, ws_bytes, stream):
+    _check(lib().dflash_gemm(C.byref(w), kind, rows, cols, group, x, T, y, workspace, ws_bytes, stream))
+
+
+def dflash_device_error(reset: bool = True) -> int:
+    v = C.c_uint32()
+    _check(lib().dflash_device_error(C.byref(v), 1 if reset else 0))
+    return v.value
 
 
 def dflash_workspace_bytes(geom: Geometry, max_batch: int) -> int:

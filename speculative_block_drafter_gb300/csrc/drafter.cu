@@ -45,7 +45,7 @@ struct Seq {
 
 // Workspace carve; sizes in bytes.
 struct Carve {
-  size_t h, x, xc, d, q, k, v, y, o, gt, up, part, sel, total;
+  size_t h, x, xc, d, q, k, v, y, o, gt, up, part, sel, act, total;
 };
 
 Carve carve_of(const dflash_geometry &g, int max_batch) {
@@ -68,7 +68,13 @@ Carve carve_of(const dflash_geometry &g, int max_batch) {
   c.up = c.gt;
   c.part = up(dfl::attn_partial_bytes(max_batch, g.kv_heads, g.heads, R, g.head_dim));
   c.sel = up(dfl::select_scratch_bytes(max_batch * (R - 1), g.vocab, g.selector_top));
-  c.total = c.h + c.x + c.xc + c.d + c.q + c.k + c.v + c.y + c.o + c.gt + c.up + c.part + c.sel;
+  // packed token tiles of the largest GEMM (block rows, a settle chunk, the fc's taps)
+  const int Tb = max_batch * R;
+  const int kmax = std::max(std::max(g.hidden, g.intermediate), g.heads * g.head_dim);
+  c.act = up(std::max({dfl::tc_act_bytes(Tb, kmax, true), dfl::tc_act_bytes(DFLASH_SETTLE_MAX, g.hidden, true),
+                       dfl::tc_act_bytes(DFLASH_SETTLE_MAX, g.taps * g.hidden, false),
+                       dfl::tc_act_bytes(Tb, g.hidden, false)}));
+  c.total = c.h + c.x + c.xc + c.d + c.q + c.k + c.v + c.y + c.o + c.gt + c.up + c.part + c.sel + c.act;
   return c;
 }
 
@@ -127,7 +133,7 @@ struct dflash_t {
   char *ws = nullptr;
   Carve c{};
   float *h, *x, *xc, *d, *q, *k, *v, *y, *o, *gt, *up, *part;
-  void *sel;
+  void *sel, *act;
   std::vector<Seq> seqs;
   std::vector<float> inv;
   int num_sms = 148;
@@ -140,19 +146,19 @@ const char *dflash_last_error(void) { return g_err.c_str(); }
 uint64_t dflash_launch_count(void) { return dfl::g_launches.load(); }
 
 size_t dflash_int4_packed_bytes(int64_t rows, int64_t cols, int32_t group) {
-  if (rows <= 0 || cols <= 0 || rows % 16 || cols % 64 || (group != 32 && group != 64 && group != 128) || cols % group)
+  if (rows <= 0 || cols <= 0 || cols % 64 || (group != 32 && group != 64 && group != 128) || cols % group)
     return 0;
-  return dfl::int4_packed_bytes(rows, cols);
+  return dfl::tc_int4_codes_bytes(rows, cols);
 }
 
 size_t dflash_int4_scale_bytes(int64_t rows, int64_t cols, int32_t group) {
   if (dflash_int4_packed_bytes(rows, cols, group) == 0) return 0;
-  return dfl::int4_scale_bytes(rows, cols, group);
+  return dfl::tc_int4_scale_bytes(rows, cols, group);
 }
 
 size_t dflash_f16_packed_bytes(int64_t rows, int64_t cols) {
-  if (rows <= 0 || cols <= 0 || rows % 16 || cols % 64) return 0;
-  return dfl::f16_packed_bytes(rows, cols);
+  if (rows <= 0 || cols <= 0 || cols % 64) return 0;
+  return dfl::tc_f16_bytes(rows, cols);
 }
 
 int dflash_pack_int4(const uint8_t *codes, const uint16_t *scales, int64_t rows, int64_t cols, int32_t group,
@@ -160,7 +166,7 @@ int dflash_pack_int4(const uint8_t *codes, const uint16_t *scales, int64_t rows,
   if (dflash_int4_packed_bytes(rows, cols, group) == 0) return fail(DFLASH_E_ARG, "pack_int4: unsupported shape");
   if (!codes || !scales || !dst_codes || !dst_scales) return fail(DFLASH_E_ARG, "pack_int4: null pointer");
   if (!aligned16(dst_codes) || !aligned16(dst_scales)) return fail(DFLASH_E_ARG, "pack_int4: misaligned output");
-  DF_CUDA(dfl::pack_int4(codes, scales, rows, cols, group, dst_codes, dst_scales, (cudaStream_t)stream));
+  DF_CUDA(dfl::tc_pack_int4(codes, scales, rows, cols, group, dst_codes, dst_scales, (cudaStream_t)stream));
   return DFLASH_OK;
 }
 
@@ -168,7 +174,7 @@ int dflash_pack_f16(const uint16_t *src, int64_t rows, int64_t cols, void *dst, 
   if (dflash_f16_packed_bytes(rows, cols) == 0) return fail(DFLASH_E_ARG, "pack_f16: unsupported shape");
   if (!src || !dst) return fail(DFLASH_E_ARG, "pack_f16: null pointer");
   if (!aligned16(dst)) return fail(DFLASH_E_ARG, "pack_f16: misaligned output");
-  DF_CUDA(dfl::pack_f16(src, rows, cols, dst, (cudaStream_t)stream));
+  DF_CUDA(dfl::tc_pack_f16(src, rows, cols, dst, (cudaStream_t)stream));
   return DFLASH_OK;
 }
 
@@ -177,30 +183,43 @@ int dflash_dequant_int4(const void *codes, const void *scales, int64_t rows, int
   if (dflash_int4_packed_bytes(rows, cols, group) == 0) return fail(DFLASH_E_ARG, "dequant_int4: unsupported shape");
   if (!codes || !scales || !out) return fail(DFLASH_E_ARG, "dequant_int4: null pointer");
   if (!aligned16(codes) || !aligned16(scales)) return fail(DFLASH_E_ARG, "dequant_int4: misaligned input");
-  DF_CUDA(dfl::dequant_int4(codes, scales, rows, cols, group, out, (cudaStream_t)stream));
+  DF_CUDA(dfl::tc_dequant_int4(codes, scales, rows, cols, group, out, (cudaStream_t)stream));
   return DFLASH_OK;
 }
 
+size_t dflash_gemm_workspace_bytes(int32_t kind, int64_t cols, int32_t T) {
+  if ((kind != 4 && kind != 16) || cols <= 0 || cols % 64 || cols > INT32_MAX || T < 1) return 0;
+  return dfl::tc_act_bytes(T, (int)cols, kind == 4);
+}
+
 int dflash_gemm(const dflash_matrix *w, int32_t kind, int64_t rows, int64_t cols, int32_t group, const float *x,
-                int32_t T, float *y, void *stream) {
+                int32_t T, float *y, void *workspace, size_t workspace_bytes, void *stream) {
   if (!w || !x || !y || T < 1) return fail(DFLASH_E_ARG, "gemm: null pointer or no rows");
-  if (((uintptr_t)x & 7) || ((uintptr_t)y & 3)) return fail(DFLASH_E_ARG, "gemm: misaligned x or y");
+  if (((uintptr_t)x & 3) || ((uintptr_t)y & 3)) return fail(DFLASH_E_ARG, "gemm: misaligned x or y");
   if (rows > INT32_MAX || cols > INT32_MAX) return fail(DFLASH_E_ARG, "gemm: matrix too large");
+  const size_t need = dflash_gemm_workspace_bytes(kind, cols, T);
+  if (need == 0) return fail(DFLASH_E_ARG, "gemm: kind must be 4 or 16, cols a multiple of 64");
+  if (!workspace || ((uintptr_t)workspace & 15)) return fail(DFLASH_E_ARG, "gemm: null or misaligned workspace");
+  if (workspace_bytes < need) return fail(DFLASH_E_CAPACITY, "gemm: workspace smaller than dflash_gemm_workspace_bytes");
   int sms = 148, dev = 0;
   if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  dfl::TcJob job{w->data, w->scales, y, (int)rows, (int)rows};
   if (kind == 4) {
     if (dflash_int4_packed_bytes(rows, cols, group) == 0) return fail(DFLASH_E_ARG, "gemm: unsupported int4 shape");
     if (!int4_ok(*w)) return fail(DFLASH_E_ARG, "gemm: null or misaligned matrix");
-    DF_CUDA(dfl::gemm_int4(dfl::Gemm{w->data, w->scales, group, (int)rows, (int)cols, x, (int)cols, y, (int)rows, T, false},
-                           sms, (cudaStream_t)stream));
-  } else if (kind == 16) {
-    if (dflash_f16_packed_bytes(rows, cols) == 0) return fail(DFLASH_E_ARG, "gemm: unsupported f16 shape");
-    if (!f16_ok(*w)) return fail(DFLASH_E_ARG, "gemm: null or misaligned matrix");
-    DF_CUDA(dfl::gemm_f16(dfl::Gemm{w->data, nullptr, 64, (int)rows, (int)cols, x, (int)cols, y, (int)rows, T, false},
-                          sms, (cudaStream_t)stream));
+    DF_CUDA(dfl::tc_gemm_int4(&job, 1, group, x, (int)cols, T, (int)cols, workspace, sms, (cudaStream_t)stream));
   } else {
-    return fail(DFLASH_E_ARG, "gemm: kind must be 4 or 16");
+    if (!f16_ok(*w)) return fail(DFLASH_E_ARG, "gemm: null or misaligned matrix");
+    DF_CUDA(dfl::tc_gemm_f16(&job, 1, x, (int)cols, T, (int)cols, workspace, sms, (cudaStream_t)stream));
   }
+  return DFLASH_OK;
+}
+
+int dflash_device_error(uint32_t *error, int32_t reset) {
+  if (!error) return fail(DFLASH_E_ARG, "device_error: null pointer");
+  unsigned v = 0;
+  DF_CUDA(dfl::read_device_error(&v, reset != 0));
+  *error = v;
   return DFLASH_OK;
 }
 
@@ -267,6 +286,7 @@ int dflash_create(dflash_t **out, const dflash_geometry *g, const dflash_weights
   d->up = (float *)take(c.up);
   d->part = (float *)take(c.part);
   d->sel = take(c.sel);
+  d->act = take(c.act);
   d->seqs.assign(max_batch, Seq{});
   // inv_freq = f32(theta^(-2i/hd)) (src/cortiq_engine/dflash.rs, Drafter::new)
   d->inv.resize(g->head_dim / 2);
@@ -311,17 +331,15 @@ int dflash_settle(dflash_t *d, int32_t seq, int64_t pos, const float *taps, int3
   cudaStream_t st = (cudaStream_t)stream;
   const int hs = g.hidden, tw = g.taps * g.hidden, kvd = g.kv_heads * g.head_dim;
   // t = rms(fc . f16(taps), hidden_norm)
-  dfl::Gemm fc{d->w.fc.data, nullptr, 64, hs, tw, taps, tw, d->x, hs, n, false};
-  DF_CUDA(dfl::gemm_f16(fc, d->num_sms, st));
+  const dfl::TcJob fc{d->w.fc.data, nullptr, d->x, hs, hs};
+  DF_CUDA(dfl::tc_gemm_f16(&fc, 1, taps, tw, n, tw, d->act, d->num_sms, st));
   DF_CUDA(dfl::rmsnorm(d->x, d->w.hidden_norm, d->x, n, hs, (float)g.eps, 1, -1, -1, st));
   for (int l = 0; l < g.layers; ++l) {
     const dflash_layer_weights &L = d->layers[l];
     float *kc = d->ck[(size_t)seq * g.layers + l] + at * kvd;
     float *vc = d->cv[(size_t)seq * g.layers + l] + at * kvd;
-    dfl::Gemm gk{L.k.data, L.k.scales, g.quant_group, kvd, hs, d->x, hs, kc, kvd, n, false};
-    dfl::Gemm gv{L.v.data, L.v.scales, g.quant_group, kvd, hs, d->x, hs, vc, kvd, n, false};
-    DF_CUDA(dfl::gemm_int4(gk, d->num_sms, st));
-    DF_CUDA(dfl::gemm_int4(gv, d->num_sms, st));
+    const dfl::TcJob kv[2] = {{L.k.data, L.k.scales, kc, kvd, kvd}, {L.v.data, L.v.scales, vc, kvd, kvd}};
+    DF_CUDA(dfl::tc_gemm_int4(kv, 2, g.quant_group, d->x, hs, n, hs, d->act, d->num_sms, st));
     DF_CUDA(dfl::head_norm_rope(kc, kvd, L.k_norm, d->inv.data(), n, g.kv_heads, g.head_dim, (float)g.eps,
                                 g.no_rope[l] == 0, nullptr, 0, 1, pos, st));
   }
@@ -357,11 +375,12 @@ int dflash_block(dflash_t *d, int32_t batch, const int64_t *anchor_pos, const fl
     const bool rot = g.no_rope[l] == 0;
     // attention: x = norm(h); x, d = conv_in(x); q, k, v
     DF_CUDA(dfl::rmsnorm(d->h, L.in_norm, d->x, T, hs, eps, R, -1, -1, st));
-    DF_CUDA(dfl::gemm_f16(dfl::Gemm{L.attn_proj.data, nullptr, 64, pr, hs, d->x, hs, d->d, pr, T, false}, sms, st));
+    const dfl::TcJob ap{L.attn_proj.data, nullptr, d->d, pr, pr};
+    DF_CUDA(dfl::tc_gemm_f16(&ap, 1, d->x, hs, T, hs, d->act, sms, st));
     DF_CUDA(dfl::conv_stage0(d->x, d->d, L.attn_base, d->xc, T, hs, kn, gs, R, st));
-    DF_CUDA(dfl::gemm_int4(dfl::Gemm{L.q.data, L.q.scales, grp, qd, hs, d->xc, hs, d->q, qd, T, false}, sms, st));
-    DF_CUDA(dfl::gemm_int4(dfl::Gemm{L.k.data, L.k.scales, grp, kvd, hs, d->xc, hs, d->k, kvd, T, false}, sms, st));
-    DF_CUDA(dfl::gemm_int4(dfl::Gemm{L.v.data, L.v.scales, grp, kvd, hs, d->xc, hs, d->v, kvd, T, false}, sms, st));
+    const dfl::TcJob qkv[3] = {{L.q.data, L.q.scales, d->q, qd, qd}, {L.k.data, L.k.scales, d->k, kvd, kvd},
+                               {L.v.data, L.v.scales, d->v, kvd, kvd}};
+    DF_CUDA(dfl::tc_gemm_int4(qkv, 3, grp, d->xc, hs, T, hs, d->act, sms, st));
     DF_CUDA(dfl::head_norm_rope(d->q, qd, L.q_norm, d->inv.data(), T, nh, hd, eps, rot, anchor_pos, batch, R, 0, st));
     DF_CUDA(dfl::head_norm_rope(d->k, kvd, L.k_norm, d->inv.data(), T, kv, hd, eps, rot, anchor_pos, batch, R, 0, st));
     // the layer's context range (src/cortiq_engine/dflash.rs, Drafter::block; no rows dropped)
@@ -379,23 +398,28 @@ int dflash_block(dflash_t *d, int32_t batch, const int64_t *anchor_pos, const fl
       seqs[b].anchor = a;
     }
     DF_CUDA(dfl::attention(d->q, d->k, d->v, seqs.data(), batch, 0, nh, kv, hd, R, W, scale, d->part, d->y, st));
-    DF_CUDA(dfl::gemm_int4(dfl::Gemm{L.o.data, L.o.scales, grp, hs, qd, d->y, qd, d->o, hs, T, false}, sms, st));
+    const dfl::TcJob oj{L.o.data, L.o.scales, d->o, hs, hs};
+    DF_CUDA(dfl::tc_gemm_int4(&oj, 1, grp, d->y, qd, T, qd, d->act, sms, st));
     DF_CUDA(dfl::conv_stage1_residual(d->o, d->d, L.attn_base, d->h, T, hs, kn, gs, R, st));
     // the MLP the same way
     DF_CUDA(dfl::rmsnorm(d->h, L.post_norm, d->x, T, hs, eps, R, -1, -1, st));
-    DF_CUDA(dfl::gemm_f16(dfl::Gemm{L.mlp_proj.data, nullptr, 64, pr, hs, d->x, hs, d->d, pr, T, false}, sms, st));
+    const dfl::TcJob mp{L.mlp_proj.data, nullptr, d->d, pr, pr};
+    DF_CUDA(dfl::tc_gemm_f16(&mp, 1, d->x, hs, T, hs, d->act, sms, st));
     DF_CUDA(dfl::conv_stage0(d->x, d->d, L.mlp_base, d->xc, T, hs, kn, gs, R, st));
-    DF_CUDA(dfl::gemm_int4(dfl::Gemm{L.gate.data, L.gate.scales, grp, ffn, hs, d->xc, hs, d->gt, ffn, T, false}, sms, st));
-    DF_CUDA(dfl::gemm_int4(dfl::Gemm{L.up.data, L.up.scales, grp, ffn, hs, d->xc, hs, d->up, ffn, T, false}, sms, st));
+    const dfl::TcJob gu[2] = {{L.gate.data, L.gate.scales, d->gt, ffn, ffn}, {L.up.data, L.up.scales, d->up, ffn, ffn}};
+    DF_CUDA(dfl::tc_gemm_int4(gu, 2, grp, d->xc, hs, T, hs, d->act, sms, st));
     DF_CUDA(dfl::silu_mul(d->gt, d->up, d->gt, (int64_t)T * ffn, st));
-    DF_CUDA(dfl::gemm_int4(dfl::Gemm{L.down.data, L.down.scales, grp, hs, ffn, d->gt, ffn, d->o, hs, T, false}, sms, st));
+    const dfl::TcJob dn{L.down.data, L.down.scales, d->o, hs, hs};
+    DF_CUDA(dfl::tc_gemm_int4(&dn, 1, grp, d->gt, ffn, T, ffn, d->act, sms, st));
     DF_CUDA(dfl::conv_stage1_residual(d->o, d->d, L.mlp_base, d->h, T, hs, kn, gs, R, st));
   }
   // the last norm; the head and the selector's projection over rows 1..k
   const int Tk = batch * k;
   DF_CUDA(dfl::rmsnorm(d->h, d->w.norm, d->x, T, hs, eps, R, 1, k, st));
-  DF_CUDA(dfl::gemm_int4(dfl::Gemm{d->w.head.data, d->w.head.scales, grp, width, hs, d->x, hs, logits, width, Tk, false}, sms, st));
-  DF_CUDA(dfl::gemm_f16(dfl::Gemm{d->w.sel.data, nullptr, 64, g.selector_rank, hs, d->x, hs, hp, g.selector_rank, Tk, false}, sms, st));
+  const dfl::TcJob hj{d->w.head.data, d->w.head.scales, logits, width, width};
+  DF_CUDA(dfl::tc_gemm_int4(&hj, 1, grp, d->x, hs, Tk, hs, d->act, sms, st));
+  const dfl::TcJob sj{d->w.sel.data, nullptr, hp, g.selector_rank, g.selector_rank};
+  DF_CUDA(dfl::tc_gemm_f16(&sj, 1, d->x, hs, Tk, hs, d->act, sms, st));
   return DFLASH_OK;
 }
 

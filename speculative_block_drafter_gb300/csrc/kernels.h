@@ -14,35 +14,38 @@ inline void count_launch(int n = 1) { g_launches.fetch_add((unsigned long long)n
 // Set the calling thread's dflash_last_error() message; returns `code`.
 int dflash_fail(int code, const std::string &msg);
 
-// -------------------------------------------------------------- packing (gemm.cu)
-size_t int4_packed_bytes(int64_t rows, int64_t cols);
-size_t int4_scale_bytes(int64_t rows, int64_t cols, int group);
-size_t f16_packed_bytes(int64_t rows, int64_t cols);
-cudaError_t pack_int4(const uint8_t *codes, const uint16_t *scales, int64_t rows, int64_t cols, int group,
-                      void *dst, void *dst_scales, cudaStream_t st);
-cudaError_t pack_f16(const uint16_t *src, int64_t rows, int64_t cols, void *dst, cudaStream_t st);
-cudaError_t dequant_int4(const void *codes, const void *scales, int64_t rows, int64_t cols, int group,
-                         float *out, cudaStream_t st);
+// -------------------------------------------------------------- tensor-core GEMMs (tc_gemm.cu)
+// Packed layouts: four-bit codes in 4 KiB tiles of 128 rows x 64 columns plus
+// per-row f16 scales per 32-or-64-column unit; f16 matrices in 16 KiB tiles of
+// 128 rows x 64 columns, 128-byte swizzled. Rows are padded to 128.
+size_t tc_int4_codes_bytes(int64_t rows, int64_t cols);
+size_t tc_int4_scale_bytes(int64_t rows, int64_t cols, int group);
+size_t tc_f16_bytes(int64_t rows, int64_t cols);
+cudaError_t tc_pack_int4(const uint8_t *codes, const uint16_t *scales, int64_t rows, int64_t cols, int group,
+                         void *dst, void *dst_scales, cudaStream_t st);
+cudaError_t tc_pack_f16(const uint16_t *src, int64_t rows, int64_t cols, void *dst, cudaStream_t st);
+cudaError_t tc_dequant_int4(const void *codes, const void *scales, int64_t rows, int64_t cols, int group, float *out,
+                            cudaStream_t st);
 
-// -------------------------------------------------------------- weight-streaming GEMM (gemm.cu)
-// Y[t][n] (= or +=) sum_k X[t][k] W[n][k] for t < T, n < N.
-// int4: X enters as f16 hi+lo planes (full f32 precision); f16: X rounded to f16.
-// `zero_first`: the launcher clears Y[0..T)[0..N) itself when it splits K.
-// `accumulate`: add into Y (never cleared) instead of storing.
-struct Gemm {
-  const void *w;        // packed matrix
-  const void *scales;   // int4 scales (null for f16)
-  int group;            // int4 group
-  int N, K;             // rows, cols of W
-  const float *X;       // [T][ldx]
-  int ldx;
-  float *Y;             // [T][ldy]
+// One matrix of a GEMM launch: Y[t][r] (r < n) = sum_k X[t][k] W[r][k].
+struct TcJob {
+  const void *w;        // packed codes or f16 tiles
+  const void *scales;   // packed scales (four-bit), else null
+  float *y;             // [T][ldy]
+  int n;                // rows
   int ldy;
-  int T;
-  bool accumulate;
 };
-cudaError_t gemm_int4(const Gemm &g, int num_sms, cudaStream_t st);
-cudaError_t gemm_f16(const Gemm &g, int num_sms, cudaStream_t st);
+// Bytes of the packed token tiles a GEMM of T rows over K columns needs.
+size_t tc_act_bytes(int T, int K, bool int4);
+// Up to 4 matrices over the same X [T][ldx] (K columns) in one launch. `act`
+// receives the packed token tiles (tc_act_bytes). When the k-range is split,
+// the outputs are cleared and accumulated with atomics.
+cudaError_t tc_gemm_int4(const TcJob *jobs, int njobs, int group, const float *X, int ldx, int T, int K, void *act,
+                         int num_sms, cudaStream_t st);
+cudaError_t tc_gemm_f16(const TcJob *jobs, int njobs, const float *X, int ldx, int T, int K, void *act, int num_sms,
+                        cudaStream_t st);
+// The device error word (a bounded wait that gave up sets bit 0).
+cudaError_t read_device_error(unsigned *out, bool reset);
 
 // -------------------------------------------------------------- row kernels (rows.cu)
 // out[map(t)] = x[t] * rsqrt(mean(x[t]^2) + eps) * w for rows t < T. If

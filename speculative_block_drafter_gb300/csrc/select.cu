@@ -29,8 +29,11 @@ constexpr int KMAX = 15;
 
 static inline int sel_chunks(int width) { return (width + SEL_CHUNK - 1) / SEL_CHUNK; }
 
+// Scratch of one call: per row the chunks' candidates (u64), the row's
+// candidates (u32) and its score table (f32 [top][top]); one counter per row
+// (sequences <= rows).
 size_t select_scratch_bytes(int max_rows, int width, int top) {
-  return (size_t)max_rows * (sel_chunks(width) + 1) * top * sizeof(unsigned long long);
+  return (size_t)max_rows * ((size_t)sel_chunks(width) * top * 8 + (size_t)top * 4 + (size_t)top * top * 4 + 4) + 256;
 }
 
 // The `top` largest keys of a warp (N keys per lane in `keys`), largest first,
@@ -82,14 +85,10 @@ __global__ void __launch_bounds__(SEL_THREADS) k_topk_chunks(const float *__rest
   }
 }
 
-// One CTA per row: merge the chunks' lists into the row's top `top`.
-__global__ void __launch_bounds__(SEL_THREADS) k_topk_merge(const unsigned long long *__restrict__ cand, int nchunks,
-                                                            int top, unsigned long long *__restrict__ best) {
-  __shared__ unsigned long long wl[SEL_THREADS / 32][TOP_MAX];
-  const int row = blockIdx.x;
+// The row's top `top` from the chunks' lists, largest first, into ctok (smem).
+__device__ void merge_row(const unsigned long long *__restrict__ cr, int ncand, int top, unsigned long long (*wl)[TOP_MAX],
+                          uint32_t *ctok) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int ncand = nchunks * top;
-  const unsigned long long *cr = cand + (int64_t)row * ncand;
   unsigned long long keys[MERGE_PER];
 #pragma unroll
   for (int i = 0; i < MERGE_PER; ++i) {
@@ -107,119 +106,114 @@ __global__ void __launch_bounds__(SEL_THREADS) k_topk_merge(const unsigned long 
       const int w = idx / TOP_MAX, t = idx % TOP_MAX;
       k2[i] = t < top ? wl[w][t] : 0ull;
     }
-    warp_top<M>(k2, top, best + (int64_t)row * top);
-  }
-}
-
-// One CTA per sequence: the score of every (row, predecessor, candidate) the
-// chain can meet, then the chain. The codebook rows involved (P of every
-// possible predecessor, C of every candidate) and hp are read into shared
-// memory once, in parallel; rows are taken in slabs of `slab` when they do not
-// all fit.
-__global__ void __launch_bounds__(CHAIN_THREADS) k_select_chain(
-    const float *__restrict__ logits, const float *__restrict__ hp, const uint32_t *__restrict__ anchor_tok,
-    const uint16_t *__restrict__ pred, const uint16_t *__restrict__ succ, int k, int width, int rank, int top,
-    int vocab, int slab, const unsigned long long *__restrict__ best, uint32_t *__restrict__ chosen,
-    uint32_t *__restrict__ plain) {
-  __shared__ uint32_t ctok[KMAX][TOP_MAX];
-  __shared__ float clogit[KMAX][TOP_MAX];
-  extern __shared__ float dyn[];
-  float *score = dyn;                                        // [k][top][top]
-  float *hps = score + k * top * top;                        // [slab][rank]
-  uint16_t *Ps = (uint16_t *)(hps + slab * rank);            // [slab][top][rank]
-  uint16_t *Cs = Ps + (size_t)slab * top * rank;             // [slab][top][rank]
-  const int b = blockIdx.x;
-  const uint32_t anchor = anchor_tok[b];
-  if (anchor >= (uint32_t)vocab) {  // not a token: the sequence's outputs say so
-    for (int j = threadIdx.x; j < k; j += CHAIN_THREADS) chosen[b * k + j] = plain[b * k + j] = 0xFFFFFFFFu;
-    return;
-  }
-  for (int i = threadIdx.x; i < k * top; i += CHAIN_THREADS) {
-    const int j = i / top, c = i % top;
-    const uint32_t tok = cand_index(best[((int64_t)b * k + j) * top + c]);
-    ctok[j][c] = tok;
-    clogit[j][c] = logits[((int64_t)b * k + j) * width + tok];
+    __shared__ unsigned long long fin[TOP_MAX];
+    warp_top<M>(k2, top, fin);
+    __syncwarp();
+    for (int t = lane; t < top; t += 32) ctok[t] = cand_index(fin[t]);
   }
   __syncthreads();
-  const int r2 = rank / 2;  // u32 pairs per codebook row
-  for (int j0 = 0; j0 < k; j0 += slab) {
-    const int nj = min(slab, k - j0);
-    // rows of this slab: P of each predecessor (the anchor for row 0), C of each candidate, hp
-    for (int i = threadIdx.x; i < nj * top * r2; i += CHAIN_THREADS) {
-      const int jj = i / (top * r2), p = (i / r2) % top, e = i % r2;
-      const int j = j0 + jj;
-      const uint32_t prev = j == 0 ? anchor : ctok[j - 1][p];
-      ((uint32_t *)Ps)[(jj * top + p) * r2 + e] = ((const uint32_t *)(pred + (int64_t)prev * rank))[e];
-      ((uint32_t *)Cs)[(jj * top + p) * r2 + e] = ((const uint32_t *)(succ + (int64_t)ctok[j][p] * rank))[e];
-    }
-    for (int i = threadIdx.x; i < nj * rank; i += CHAIN_THREADS)
-      hps[i] = hp[((int64_t)b * k + j0) * rank + i];
+}
+
+// One CTA per (sequence, row j): row j's candidates, the predecessors it can
+// have (the anchor for row 0, else row j-1's candidates, merged again here),
+// and every score[p][c] = logit[c] + sum_i (P[prev_p][i] * hp[i]) * C[cand_c][i].
+// The CTA that finishes a sequence last runs its chain: the first strictly
+// greater score in candidate order wins, its token is the next predecessor.
+__global__ void __launch_bounds__(SEL_THREADS) k_row_scores(
+    const float *__restrict__ logits, const float *__restrict__ hp, const uint32_t *__restrict__ anchor_tok,
+    const uint16_t *__restrict__ pred, const uint16_t *__restrict__ succ, int k, int width, int rank, int top,
+    int vocab, int nchunks, const unsigned long long *__restrict__ cand, uint32_t *__restrict__ ctok_g,
+    float *__restrict__ score_g, unsigned int *__restrict__ done, uint32_t *__restrict__ chosen,
+    uint32_t *__restrict__ plain) {
+  __shared__ unsigned long long wl[SEL_THREADS / 32][TOP_MAX];
+  __shared__ uint32_t cur[TOP_MAX], prv[TOP_MAX];
+  __shared__ float clog[TOP_MAX];
+  __shared__ __align__(16) uint16_t Ps[TOP_MAX * RANK_MAX];
+  __shared__ __align__(16) uint16_t Cs[TOP_MAX * RANK_MAX];
+  __shared__ float hs[RANK_MAX];
+  __shared__ bool last;
+  const int row = blockIdx.x, b = row / k, j = row % k;
+  const uint32_t anchor = anchor_tok[b];
+  const bool bad = anchor >= (uint32_t)vocab;
+  const int ncand = nchunks * top;
+  if (!bad) {
+    merge_row(cand + (int64_t)row * ncand, ncand, top, wl, cur);
+    if (j > 0) merge_row(cand + (int64_t)(row - 1) * ncand, ncand, top, wl, prv);
+    const int np = j > 0 ? top : 1;
+    if (j == 0 && threadIdx.x == 0) prv[0] = anchor;
     __syncthreads();
-    // score[j][p][c] = logit[j][c] + sum_i (P[prev_p][i] * hp[j][i]) * C[cand_c][i]
-    for (int it = threadIdx.x; it < nj * top * top; it += CHAIN_THREADS) {
-      const int jj = it / (top * top), p = (it / top) % top, c = it % top;
-      const int j = j0 + jj;
-      if (j == 0 && p > 0) continue;
-      const __half2 *pr = (const __half2 *)(Ps + (jj * top + p) * rank);
-      const __half2 *cr = (const __half2 *)(Cs + (jj * top + c) * rank);
-      const float *hr = hps + jj * rank;
+    const int r2 = rank / 2;
+    for (int i = threadIdx.x; i < top * r2; i += SEL_THREADS) {
+      const int c = i / r2, e = i % r2;
+      ((uint32_t *)Cs)[c * r2 + e] = ((const uint32_t *)(succ + (int64_t)cur[c] * rank))[e];
+      if (c < np) ((uint32_t *)Ps)[c * r2 + e] = ((const uint32_t *)(pred + (int64_t)prv[c] * rank))[e];
+    }
+    for (int i = threadIdx.x; i < rank; i += SEL_THREADS) hs[i] = hp[(int64_t)row * rank + i];
+    for (int c = threadIdx.x; c < top; c += SEL_THREADS) clog[c] = logits[(int64_t)row * width + cur[c]];
+    __syncthreads();
+    for (int it = threadIdx.x; it < np * top; it += SEL_THREADS) {
+      const int p = it / top, c = it % top;
+      const __half2 *pr = (const __half2 *)(Ps + p * rank);
+      const __half2 *cr = (const __half2 *)(Cs + c * rank);
       float acc = 0.f;
       for (int e = 0; e < r2; ++e) {
         const float2 pv = __half22float2(pr[e]);
         const float2 cv = __half22float2(cr[e]);
-        acc = fmaf(pv.x * hr[2 * e], cv.x, acc);
-        acc = fmaf(pv.y * hr[2 * e + 1], cv.y, acc);
+        acc = fmaf(pv.x * hs[2 * e], cv.x, acc);
+        acc = fmaf(pv.y * hs[2 * e + 1], cv.y, acc);
       }
-      score[(j * top + p) * top + c] = clogit[j][c] + acc;
+      score_g[((int64_t)row * top + p) * top + c] = clog[c] + acc;
     }
-    __syncthreads();
+    for (int c = threadIdx.x; c < top; c += SEL_THREADS) ctok_g[(int64_t)row * top + c] = cur[c];
   }
-  if (threadIdx.x == 0) {
-    int slot = 0;  // the predecessor's slot among the previous row's candidates
-    for (int j = 0; j < k; ++j) {
-      float bs = -INFINITY;
-      int bc = 0;
-      for (int c = 0; c < top; ++c) {
-        const float sc = score[(j * top + slot) * top + c];
-        if (sc > bs) {
-          bs = sc;
-          bc = c;
-        }
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) last = atomicAdd(done + b, 1u) == (unsigned)(k - 1);
+  __syncthreads();
+  if (!last || threadIdx.x != 0) return;
+  __threadfence();
+  done[b] = 0;  // ready for the next call
+  if (bad) {
+    for (int jj = 0; jj < k; ++jj) chosen[b * k + jj] = plain[b * k + jj] = 0xFFFFFFFFu;
+    return;
+  }
+  int slot = 0;  // the predecessor's slot among the previous row's candidates
+  for (int jj = 0; jj < k; ++jj) {
+    const int rr = b * k + jj;
+    const float *sr = score_g + ((int64_t)rr * top + slot) * top;
+    float bs = -INFINITY;
+    int bc = 0;
+    for (int c = 0; c < top; ++c) {
+      const float sc = __ldcg(sr + c);
+      if (sc > bs) {
+        bs = sc;
+        bc = c;
       }
-      chosen[b * k + j] = ctok[j][bc];
-      plain[b * k + j] = ctok[j][0];
-      slot = bc;
     }
+    chosen[rr] = __ldcg(ctok_g + (int64_t)rr * top + bc);
+    plain[rr] = __ldcg(ctok_g + (int64_t)rr * top);
+    slot = bc;
   }
-}
-
-static size_t chain_smem(int k, int top, int rank, int slab) {
-  return (size_t)k * top * top * 4 + (size_t)slab * rank * 4 + 2 * (size_t)slab * top * rank * 2;
 }
 
 cudaError_t select_tokens(const float *logits, const float *hp, const uint32_t *anchor_tok, const uint16_t *pred,
                           const uint16_t *succ, int batch, int k, int width, int rank, int top, int vocab, void *scratch,
                           uint32_t *chosen, uint32_t *plain, cudaStream_t st) {
-  if (top > TOP_MAX || rank > RANK_MAX || top < 1 || k > KMAX) return cudaErrorInvalidValue;
+  if (top > TOP_MAX || rank > RANK_MAX || top < 1 || k > KMAX || rank % 2) return cudaErrorInvalidValue;
   const int nchunks = sel_chunks(width);
   if (nchunks * top > MERGE_PER * SEL_THREADS) return cudaErrorInvalidValue;
+  const int rows = batch * k;
   unsigned long long *cand = (unsigned long long *)scratch;
-  unsigned long long *best = cand + (size_t)batch * k * nchunks * top;
-  dim3 g1(nchunks, batch * k);
+  uint32_t *ctok = (uint32_t *)(cand + (size_t)rows * nchunks * top);
+  float *score = (float *)(ctok + (size_t)rows * top);
+  unsigned int *done = (unsigned int *)(score + (size_t)rows * top * top);
+  cudaError_t e = cudaMemsetAsync(done, 0, (size_t)batch * sizeof(unsigned int), st);
+  if (e != cudaSuccess) return e;
+  dim3 g1(nchunks, rows);
   k_topk_chunks<<<g1, SEL_THREADS, 0, st>>>(logits, width, top, cand);
-  k_topk_merge<<<batch * k, SEL_THREADS, 0, st>>>(cand, nchunks, top, best);
-  constexpr size_t SMEM_MAX = 200 * 1024;
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(k_select_chain, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_MAX);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
-  int slab = k;
-  while (slab > 1 && chain_smem(k, top, rank, slab) > SMEM_MAX) --slab;
-  k_select_chain<<<batch, CHAIN_THREADS, chain_smem(k, top, rank, slab), st>>>(
-      logits, hp, anchor_tok, pred, succ, k, width, rank, top, vocab, slab, best, chosen, plain);
-  count_launch(3);
+  k_row_scores<<<rows, SEL_THREADS, 0, st>>>(logits, hp, anchor_tok, pred, succ, k, width, rank, top, vocab, nchunks,
+                                             cand, ctok, score, done, chosen, plain);
+  count_launch(2);
   return cudaGetLastError();
 }
 
@@ -283,8 +277,8 @@ extern "C" int dflash_select_static(const float *logits, const float *hp, const 
     return dflash_fail(DFLASH_E_ARG, "select_static: width / top beyond the selector's merge");
   const size_t need = select_scratch_bytes(batch * k, width, top);
   if (need > kStaticSelectScratch)
-    return dflash_fail(DFLASH_E_CAPACITY, "select_static: batch * k * (width / 2048 + 1) * top * 8 bytes of "
-                                          "candidates exceed the fixed 8 MiB scratch; use dflash_select");
+    return dflash_fail(DFLASH_E_CAPACITY, "select_static: the call's candidates and score tables exceed the fixed "
+                                          "8 MiB scratch; use dflash_select");
   void *scratch = nullptr;
   cudaError_t e = static_scratch(&scratch);
   if (e != cudaSuccess)

@@ -1,0 +1,670 @@
+// Weight GEMMs of the drafter on the 5th-generation tensor cores (tcgen05):
+// Y[t][n] = sum_k X[t][k] W[n][k] for the four-bit matrices (q, k, v, o, gate,
+// up, down, head) and the f16 ones (fc, the kernel projections, the selector's
+// projection); cortiq-engine src/gpu_cuda/hyb/dflash.rs (`Dev::settle`,
+// `Dev::block`) names which is which.
+//
+// One CTA owns a 128-row tile of one matrix, a tile of TT tokens and a range of
+// 64-column k-tiles. Warp 4 streams the k-tiles into a shared-memory ring with
+// bulk copies; warp 5 issues tcgen05.mma (M = 128 weight rows, N = TT tokens,
+// K = 16) into tensor memory.
+//
+// Four-bit matrices: warps 0-3 own one weight row each. They turn the row's
+// codes into exact f16 integers (-7..7) and store them in tensor memory, where
+// the MMA reads its A operand; the tokens enter as two f16 planes, hi = f16(x)
+// and lo = f16(x - hi), both accumulated into the same tensor-memory columns.
+// Each quantisation group has its own accumulator, which the same warps read
+// back, multiply by the group's f16 scale in f32 and add up in registers: the
+// dequantisation is exact and no shared-memory bandwidth is spent on A.
+//
+// f16 matrices: the weight tiles go to shared memory by bulk copy as they are
+// (pre-swizzled by the packer) and the tokens enter rounded to f16 (the card
+// arm's `to_half`); one accumulator spans the CTA's k-range.
+#include <algorithm>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "tc.cuh"
+
+namespace dfl {
+
+constexpr int TC_THREADS = 192;  // warps 0-3 rows / epilogue, 4 producer, 5 MMA
+constexpr int TC_PRODUCER = 4;
+constexpr int TC_MMA = 5;
+constexpr int TC_STAGES = 4;
+constexpr uint32_t TC_TMEM_COLS = 256;
+
+// ---------------------------------------------------------------- packed layouts
+
+size_t tc_int4_codes_bytes(int64_t rows, int64_t cols) { return (size_t)((rows + 127) / 128) * 128 * cols / 2; }
+static int drain_units(int group) { return group >= 64 ? 1 : 2; }
+size_t tc_int4_scale_bytes(int64_t rows, int64_t cols, int group) {
+  return (size_t)((rows + 127) / 128) * (cols / 64) * drain_units(group) * 256;
+}
+size_t tc_f16_bytes(int64_t rows, int64_t cols) { return (size_t)((rows + 127) / 128) * 128 * cols * 2; }
+
+// Codes: per (row tile m, k-tile kt) 4 KiB = [half h][row r][16 B]; the 16 B of
+// (r, h) hold columns 32h .. 32h+31 as four u32 of eight nibbles (q + 8) in the
+// order c0 c2 c4 c6 c1 c3 c5 c7 of their eight columns, so that two lop3 give
+// the f16 pairs (c0,c1), (c2,c3), ... Rows past the matrix are code 8 (q = 0).
+__global__ void k_tc_pack_int4(const uint8_t *__restrict__ codes, int64_t rows, int64_t cols,
+                               uint32_t *__restrict__ dst) {
+  const int64_t KT = cols / 64;
+  const int64_t MT = (rows + 127) / 128;
+  const int64_t total = MT * KT * 2 * 128 * 4;  // u32 words
+  int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (t >= total) return;
+  const int j = (int)(t & 3);
+  const int r = (int)((t >> 2) & 127);
+  const int h = (int)((t >> 9) & 1);
+  const int64_t tile = t >> 10;
+  const int64_t m = tile / KT, kt = tile % KT;
+  const int64_t row = m * 128 + r;
+  uint32_t w = 0;
+  for (int i = 0; i < 8; ++i) {
+    const int e = (i < 4) ? 2 * i : 2 * (i - 4) + 1;  // nibble i holds column e of the eight
+    const int64_t col = kt * 64 + 32 * h + 8 * j + e;
+    uint32_t nib = 8;
+    if (row < rows) {
+      const uint8_t byte = codes[row * (cols / 2) + col / 2];
+      nib = (col & 1) ? (byte >> 4) : (byte & 15);
+    }
+    w |= nib << (4 * i);
+  }
+  dst[t] = w;
+}
+
+// Scales: per (m, kt) [drain unit u][row r] f16; unit u covers columns
+// kt*64 + 32u .. (both units share the group's scale when the group is >= 64).
+__global__ void k_tc_pack_scales(const uint16_t *__restrict__ scales, int64_t rows, int64_t cols, int group,
+                                 uint16_t *__restrict__ dst) {
+  const int64_t KT = cols / 64;
+  const int64_t MT = (rows + 127) / 128;
+  const int DU = group >= 64 ? 1 : 2;
+  const int64_t total = MT * KT * DU * 128;
+  int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (t >= total) return;
+  const int r = (int)(t & 127);
+  const int u = (int)((t >> 7) % DU);
+  const int64_t tile = (t >> 7) / DU;
+  const int64_t m = tile / KT, kt = tile % KT;
+  const int64_t row = m * 128 + r;
+  const int64_t col = kt * 64 + 32 * u;
+  dst[t] = row < rows ? scales[row * (cols / group) + col / group] : (uint16_t)0;
+}
+
+// f16 matrix: per (m, kt) 16 KiB, 128 rows x 64 columns, K-major with the
+// 128-byte swizzle; rows past the matrix are zero.
+__global__ void k_tc_pack_f16(const uint16_t *__restrict__ src, int64_t rows, int64_t cols, uint4 *__restrict__ dst) {
+  const int64_t KT = cols / 64;
+  const int64_t MT = (rows + 127) / 128;
+  const int64_t total = MT * KT * 128 * 8;  // 16-byte chunks
+  int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (t >= total) return;
+  const int c = (int)(t & 7);
+  const int r = (int)((t >> 3) & 127);
+  const int64_t tile = t >> 10;
+  const int64_t m = tile / KT, kt = tile % KT;
+  const int64_t row = m * 128 + r;
+  uint32_t v[4] = {0, 0, 0, 0};
+  if (row < rows) {
+    const uint16_t *p = src + row * cols + kt * 64 + c * 8;
+    for (int i = 0; i < 4; ++i) v[i] = (uint32_t)p[2 * i] | ((uint32_t)p[2 * i + 1] << 16);
+  }
+  dst[tile * 1024 + sw128_off(r, c) / 16] = make_uint4(v[0], v[1], v[2], v[3]);
+}
+
+// Tokens: per (token tile tt, k-tile kt, plane p) TT rows x 64 columns f16,
+// K-major with the 128-byte swizzle. Plane 0 = f16(x); plane 1 = f16(x - f16(x)).
+template <int PLANES>
+__global__ void k_tc_pack_act(const float *__restrict__ X, int ldx, int T, int K, int TT, uint4 *__restrict__ dst) {
+  const int KT = K / 64;
+  const int64_t total = (int64_t)((T + TT - 1) / TT) * KT * TT * 8;
+  int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (t >= total) return;
+  const int c = (int)(t & 7);
+  const int r = (int)((t >> 3) % TT);
+  const int64_t rest = (t >> 3) / TT;
+  const int kt = (int)(rest % KT);
+  const int tt = (int)(rest / KT);
+  const int tok = tt * TT + r;
+  float x[8];
+  if (tok < T) {
+    const float *p = X + (int64_t)tok * ldx + kt * 64 + c * 8;
+    for (int i = 0; i < 8; ++i) x[i] = p[i];
+  } else {
+    for (int i = 0; i < 8; ++i) x[i] = 0.f;
+  }
+  uint32_t hi[4], lo[4];
+  for (int i = 0; i < 4; ++i) {
+    if (PLANES == 2) {
+      split2(x[2 * i], x[2 * i + 1], hi[i], lo[i]);
+    } else {
+      hi[i] = pack_half2(__float2half_rn(x[2 * i]), __float2half_rn(x[2 * i + 1]));
+    }
+  }
+  const int64_t base = (((int64_t)tt * KT + kt) * PLANES) * TT * 8;  // in 16-byte chunks
+  dst[base + sw128_off(r, c) / 16] = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+  if (PLANES == 2) dst[base + TT * 8 + sw128_off(r, c) / 16] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+}
+
+// ---------------------------------------------------------------- jobs
+constexpr int MAX_JOBS = 4;
+struct TcJobs {
+  const void *w[MAX_JOBS];        // packed codes / f16 tiles
+  const uint16_t *s[MAX_JOBS];    // packed scales (four-bit)
+  float *y[MAX_JOBS];
+  int n[MAX_JOBS];                // rows
+  int ldy[MAX_JOBS];
+  int tile0[MAX_JOBS + 1];        // first row tile of each job in the grid's y
+  int njobs;
+};
+
+__device__ __forceinline__ int job_of(const TcJobs &J, int mt) {
+  int j = 0;
+#pragma unroll
+  for (int i = 1; i < MAX_JOBS; ++i)
+    if (i < J.njobs && mt >= J.tile0[i]) j = i;
+  return j;
+}
+
+// ---------------------------------------------------------------- four-bit kernel
+template <int TT, int DU>
+struct Int4Cfg {
+  static constexpr int B_BYTES = 2 * TT * 128;        // hi + lo planes of one k-tile
+  static constexpr int CODE_OFF = B_BYTES;
+  static constexpr int SCALE_OFF = B_BYTES + 4096;
+  static constexpr int STAGE = ((SCALE_OFF + DU * 256) + 1023) / 1024 * 1024;
+  static constexpr int NDU = TT <= 32 ? 4 : 2;        // accumulators in flight
+  static constexpr int DCOL = TC_STAGES * 32;         // tensor-memory columns of the accumulators
+  static_assert(DCOL + NDU * TT <= (int)TC_TMEM_COLS, "tensor memory");
+  static constexpr int SMEM = TC_STAGES * STAGE + 1024 + 256;
+};
+
+template <int TT, int DU>
+__global__ void __launch_bounds__(TC_THREADS) k_tc_int4(TcJobs J, const uint8_t *__restrict__ bpack, int K, int T,
+                                                        int kc, int atomic_out) {
+  using C = Int4Cfg<TT, DU>;
+  extern __shared__ __align__(1024) uint8_t smraw[];
+  uint8_t *sm = smraw + ((1024 - (smem_u32(smraw) & 1023)) & 1023);
+  uint64_t *bars = (uint64_t *)(sm + TC_STAGES * C::STAGE);
+  uint32_t *tslot = (uint32_t *)(bars + 3 * TC_STAGES + 2 * C::NDU);
+  const uint32_t full0 = smem_u32(bars), empty0 = full0 + 8 * TC_STAGES, afull0 = empty0 + 8 * TC_STAGES;
+  const uint32_t dfull0 = afull0 + 8 * TC_STAGES, dfree0 = dfull0 + 8 * C::NDU;
+
+  const int KT = K / 64;
+  const int tt = blockIdx.x, mt = blockIdx.y;
+  const int kt0 = blockIdx.z * kc, kt1 = min(KT, kt0 + kc);
+  const int n = kt1 - kt0;
+  if (n <= 0) return;
+  const int job = job_of(J, mt);
+  const int m = mt - J.tile0[job];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < TC_STAGES; ++i) {
+      mbar_init(full0 + 8 * i, 1);
+      mbar_init(empty0 + 8 * i, 1);
+      mbar_init(afull0 + 8 * i, 128);
+    }
+    for (int i = 0; i < C::NDU; ++i) {
+      mbar_init(dfull0 + 8 * i, 1);
+      mbar_init(dfree0 + 8 * i, 128);
+    }
+    mbar_fence_init();
+  }
+  if (warp == 0) tmem_alloc(smem_u32(tslot), TC_TMEM_COLS);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tslot;
+
+  if (warp == TC_PRODUCER) {
+    if (lane == 0) {
+      const uint8_t *wc = (const uint8_t *)J.w[job] + ((int64_t)m * KT) * 4096;
+      const uint8_t *ws = (const uint8_t *)J.s[job] + ((int64_t)m * KT) * DU * 256;
+      const uint8_t *bp = bpack + ((int64_t)tt * KT) * C::B_BYTES;
+      for (int i = 0; i < n; ++i) {
+        const int s = i % TC_STAGES, kt = kt0 + i;
+        if (i >= TC_STAGES && !mbar_wait(empty0 + 8 * s, ((i / TC_STAGES) - 1) & 1)) break;
+        const uint32_t st = smem_u32(sm + s * C::STAGE);
+        mbar_expect_tx(full0 + 8 * s, C::B_BYTES + 4096 + DU * 256);
+        bulk_g2s(st, bp + (int64_t)kt * C::B_BYTES, C::B_BYTES, full0 + 8 * s);
+        bulk_g2s(st + C::CODE_OFF, wc + (int64_t)kt * 4096, 4096, full0 + 8 * s);
+        bulk_g2s(st + C::SCALE_OFF, ws + (int64_t)kt * DU * 256, DU * 256, full0 + 8 * s);
+      }
+    }
+  } else if (warp == TC_MMA) {
+    if (lane == 0) {
+      constexpr uint32_t idesc = f16_idesc(128, TT);
+      constexpr int KSU = 4 / DU;  // k-steps of 16 per drain unit
+      bool ok = true;
+      for (int i = 0; i < n && ok; ++i) {
+        const int s = i % TC_STAGES;
+        if (!mbar_wait(afull0 + 8 * s, (i / TC_STAGES) & 1)) break;
+        tc_fence_after();
+        const uint32_t st = smem_u32(sm + s * C::STAGE);
+        for (int du = 0; du < DU; ++du) {
+          const int u = i * DU + du, d = u % C::NDU;
+          if (u >= C::NDU && !mbar_wait(dfree0 + 8 * d, ((u / C::NDU) - 1) & 1)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t dcol = tbase + C::DCOL + d * TT;
+          for (int ks = 0; ks < KSU; ++ks) {
+            const int kstep = du * KSU + ks;
+            const uint32_t a = tbase + s * 32 + kstep * 8;
+            mma_ts(dcol, a, sw128_desc(st + kstep * 32), idesc, ks > 0);
+            mma_ts(dcol, a, sw128_desc(st + TT * 128 + kstep * 32), idesc, 1);
+          }
+          mma_commit(dfull0 + 8 * d);
+        }
+        mma_commit(empty0 + 8 * s);
+      }
+    }
+  } else {
+    // warps 0-3: the row's codes into tensor memory; each accumulator back, scaled
+    const int r = warp * 32 + lane;
+    const uint32_t lrow = (uint32_t)(warp * 32) << 16;
+    float acc[TT];
+#pragma unroll
+    for (int t = 0; t < TT; ++t) acc[t] = 0.f;
+    float sc_prev[DU], sc_cur[DU];
+#pragma unroll
+    for (int u = 0; u < DU; ++u) sc_prev[u] = sc_cur[u] = 0.f;
+    bool ok = true;
+    for (int i = 0; i <= n && ok; ++i) {
+      if (i < n) {
+        const int s = i % TC_STAGES;
+        if (!__all_sync(0xffffffffu, mbar_wait(full0 + 8 * s, (i / TC_STAGES) & 1))) break;
+        const uint8_t *st = sm + s * C::STAGE;
+        const uint4 c0 = *(const uint4 *)(st + C::CODE_OFF + r * 16);
+        const uint4 c1 = *(const uint4 *)(st + C::CODE_OFF + 2048 + r * 16);
+#pragma unroll
+        for (int u = 0; u < DU; ++u)
+          sc_cur[u] = __half2float(__ushort_as_half(*(const uint16_t *)(st + C::SCALE_OFF + u * 256 + r * 2)));
+        uint32_t v[32];
+        const uint32_t words[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          uint32_t a4[4];
+          dequant8(words[j], a4);
+          v[4 * j + 0] = a4[0];
+          v[4 * j + 1] = a4[1];
+          v[4 * j + 2] = a4[2];
+          v[4 * j + 3] = a4[3];
+        }
+        if (i >= TC_STAGES && !__all_sync(0xffffffffu, mbar_wait(empty0 + 8 * s, ((i / TC_STAGES) - 1) & 1))) break;
+        tc_fence_after();
+        tmem_st32(tbase + lrow + s * 32, v);
+        tc_wait_st();
+        tc_fence_before();
+        mbar_arrive(afull0 + 8 * s);
+      }
+      const int j = i - 1;  // drain the previous k-tile's accumulators
+      if (j >= 0) {
+#pragma unroll
+        for (int du = 0; du < DU; ++du) {
+          const int u = j * DU + du, d = u % C::NDU;
+          if (!__all_sync(0xffffffffu, mbar_wait(dfull0 + 8 * d, (u / C::NDU) & 1))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+#pragma unroll
+          for (int c0 = 0; c0 < TT; c0 += 16) {
+            uint32_t w16[16];
+            tmem_ld16(tbase + lrow + C::DCOL + d * TT + c0, w16);
+            tc_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 16; ++e) acc[c0 + e] = fmaf(sc_prev[du], __uint_as_float(w16[e]), acc[c0 + e]);
+          }
+          tc_fence_before();
+          mbar_arrive(dfree0 + 8 * d);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < DU; ++u) sc_prev[u] = sc_cur[u];
+    }
+    const int row = m * 128 + r;
+    if (ok && row < J.n[job]) {
+      float *y = J.y[job];
+      const int ldy = J.ldy[job];
+#pragma unroll
+      for (int t = 0; t < TT; ++t) {
+        const int tok = tt * TT + t;
+        if (tok < T) {
+          if (atomic_out) atomicAdd(y + (int64_t)tok * ldy + row, acc[t]);
+          else y[(int64_t)tok * ldy + row] = acc[t];
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tbase, TC_TMEM_COLS);
+  }
+}
+
+// ---------------------------------------------------------------- f16 kernel
+template <int TT>
+struct F16Cfg {
+  static constexpr int B_BYTES = TT * 128;
+  static constexpr int A_OFF = B_BYTES;
+  static constexpr int STAGE = B_BYTES + 16384;
+  static constexpr int STAGES = TT >= 128 ? 4 : 6;
+  static constexpr int SMEM = STAGES * STAGE + 1024 + 256;
+  static constexpr uint32_t COLS = TT <= 32 ? 32 : TT;
+};
+
+template <int TT>
+__global__ void __launch_bounds__(TC_THREADS) k_tc_f16(TcJobs J, const uint8_t *__restrict__ bpack, int K, int T,
+                                                       int kc, int atomic_out) {
+  using C = F16Cfg<TT>;
+  constexpr int S = C::STAGES;
+  extern __shared__ __align__(1024) uint8_t smraw[];
+  uint8_t *sm = smraw + ((1024 - (smem_u32(smraw) & 1023)) & 1023);
+  uint64_t *bars = (uint64_t *)(sm + S * C::STAGE);
+  uint32_t *tslot = (uint32_t *)(bars + 2 * S + 1);
+  const uint32_t full0 = smem_u32(bars), empty0 = full0 + 8 * S, done = empty0 + 8 * S;
+
+  const int KT = K / 64;
+  const int tt = blockIdx.x, mt = blockIdx.y;
+  const int kt0 = blockIdx.z * kc, kt1 = min(KT, kt0 + kc);
+  const int n = kt1 - kt0;
+  if (n <= 0) return;
+  const int job = job_of(J, mt);
+  const int m = mt - J.tile0[job];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < S; ++i) {
+      mbar_init(full0 + 8 * i, 1);
+      mbar_init(empty0 + 8 * i, 1);
+    }
+    mbar_init(done, 1);
+    mbar_fence_init();
+  }
+  if (warp == 0) tmem_alloc(smem_u32(tslot), C::COLS);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tslot;
+
+  if (warp == TC_PRODUCER) {
+    if (lane == 0) {
+      const uint8_t *wa = (const uint8_t *)J.w[job] + ((int64_t)m * KT) * 16384;
+      const uint8_t *bp = bpack + ((int64_t)tt * KT) * C::B_BYTES;
+      for (int i = 0; i < n; ++i) {
+        const int s = i % S, kt = kt0 + i;
+        if (i >= S && !mbar_wait(empty0 + 8 * s, ((i / S) - 1) & 1)) break;
+        const uint32_t st = smem_u32(sm + s * C::STAGE);
+        mbar_expect_tx(full0 + 8 * s, C::B_BYTES + 16384);
+        bulk_g2s(st, bp + (int64_t)kt * C::B_BYTES, C::B_BYTES, full0 + 8 * s);
+        bulk_g2s(st + C::A_OFF, wa + (int64_t)kt * 16384, 16384, full0 + 8 * s);
+      }
+    }
+  } else if (warp == TC_MMA) {
+    if (lane == 0) {
+      constexpr uint32_t idesc = f16_idesc(128, TT);
+      for (int i = 0; i < n; ++i) {
+        const int s = i % S;
+        if (!mbar_wait(full0 + 8 * s, (i / S) & 1)) break;
+        tc_fence_after();
+        const uint32_t st = smem_u32(sm + s * C::STAGE);
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks)
+          mma_ss(tbase, sw128_desc(st + C::A_OFF + ks * 32), sw128_desc(st + ks * 32), idesc, (i > 0 || ks > 0));
+        mma_commit(empty0 + 8 * s);
+      }
+      mma_commit(done);
+    }
+  } else {
+    const int r = warp * 32 + lane;
+    const uint32_t lrow = (uint32_t)(warp * 32) << 16;
+    const bool ok = __all_sync(0xffffffffu, mbar_wait(done, 0));
+    tc_fence_after();
+    const int row = m * 128 + r;
+    if (ok) {
+      float *y = J.y[job];
+      const int ldy = J.ldy[job];
+      const bool live = row < J.n[job];
+#pragma unroll 1
+      for (int c0 = 0; c0 < TT; c0 += 16) {
+        uint32_t w16[16];
+        tmem_ld16(tbase + lrow + c0, w16);
+        tc_wait_ld();
+        if (live) {
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const int tok = tt * TT + c0 + e;
+            if (tok < T) {
+              if (atomic_out) atomicAdd(y + (int64_t)tok * ldy + row, __uint_as_float(w16[e]));
+              else y[(int64_t)tok * ldy + row] = __uint_as_float(w16[e]);
+            }
+          }
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tbase, C::COLS);
+  }
+}
+
+// The exact values of packed four-bit codes, f32 [rows][cols]: the kernels'
+// own dequantisation (dequant8) and scale layout, exposed for checking.
+__global__ void k_tc_dequant(const uint4 *__restrict__ codes, const uint16_t *__restrict__ scales, int64_t rows,
+                             int64_t cols, int DU, float *__restrict__ out) {
+  const int64_t KT = cols / 64;
+  const int64_t MT = (rows + 127) / 128;
+  const int64_t total = MT * KT * 2 * 128;  // (tile, half, row)
+  int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (t >= total) return;
+  const int r = (int)(t & 127);
+  const int h = (int)((t >> 7) & 1);
+  const int64_t tile = t >> 8;
+  const int64_t m = tile / KT, kt = tile % KT;
+  const int64_t row = m * 128 + r;
+  if (row >= rows) return;
+  const uint4 v = codes[tile * 256 + h * 128 + r];
+  const uint32_t words[4] = {v.x, v.y, v.z, v.w};
+  const int u = DU == 2 ? h : 0;
+  const float sc = __half2float(__ushort_as_half(scales[(tile * DU + u) * 128 + r]));
+  for (int j = 0; j < 4; ++j) {
+    uint32_t a[4];
+    dequant8(words[j], a);
+    for (int p = 0; p < 4; ++p) {
+      const int64_t col = kt * 64 + 32 * h + 8 * j + 2 * p;
+      const float q0 = __half2float(__ushort_as_half((uint16_t)(a[p] & 0xFFFF)));
+      const float q1 = __half2float(__ushort_as_half((uint16_t)(a[p] >> 16)));
+      out[row * cols + col] = __fmul_rn(q0, sc);
+      out[row * cols + col + 1] = __fmul_rn(q1, sc);
+    }
+  }
+}
+
+// ---------------------------------------------------------------- launchers
+
+static unsigned blocks_for(int64_t n, int b) { return (unsigned)((n + b - 1) / b); }
+
+cudaError_t tc_pack_int4(const uint8_t *codes, const uint16_t *scales, int64_t rows, int64_t cols, int group,
+                         void *dst, void *dst_scales, cudaStream_t st) {
+  const int64_t MT = (rows + 127) / 128, KT = cols / 64;
+  k_tc_pack_int4<<<blocks_for(MT * KT * 1024, 256), 256, 0, st>>>(codes, rows, cols, (uint32_t *)dst);
+  k_tc_pack_scales<<<blocks_for(MT * KT * drain_units(group) * 128, 256), 256, 0, st>>>(scales, rows, cols, group,
+                                                                                       (uint16_t *)dst_scales);
+  count_launch(2);
+  return cudaGetLastError();
+}
+
+cudaError_t tc_dequant_int4(const void *codes, const void *scales, int64_t rows, int64_t cols, int group, float *out,
+                            cudaStream_t st) {
+  const int64_t MT = (rows + 127) / 128, KT = cols / 64;
+  k_tc_dequant<<<blocks_for(MT * KT * 256, 256), 256, 0, st>>>((const uint4 *)codes, (const uint16_t *)scales, rows,
+                                                              cols, drain_units(group), out);
+  count_launch(1);
+  return cudaGetLastError();
+}
+
+cudaError_t tc_pack_f16(const uint16_t *src, int64_t rows, int64_t cols, void *dst, cudaStream_t st) {
+  const int64_t MT = (rows + 127) / 128, KT = cols / 64;
+  k_tc_pack_f16<<<blocks_for(MT * KT * 1024, 256), 256, 0, st>>>(src, rows, cols, (uint4 *)dst);
+  count_launch(1);
+  return cudaGetLastError();
+}
+
+static int tt_int4(int T) { return T <= 16 ? 16 : T <= 32 ? 32 : 64; }
+static int tt_f16(int T) { return T <= 16 ? 16 : T <= 32 ? 32 : T <= 64 ? 64 : T <= 128 ? 128 : 256; }
+
+size_t tc_act_bytes(int T, int K, bool int4) {
+  const int TT = int4 ? tt_int4(T) : tt_f16(T);
+  return (size_t)((T + TT - 1) / TT) * TT * K * 2 * (int4 ? 2 : 1);
+}
+
+template <typename KERN>
+static cudaError_t set_smem(KERN kern, int bytes, bool &done) {
+  if (done) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) done = true;
+  return e;
+}
+
+// Grid over (token tiles, row tiles of all jobs, k splits): splits fill the
+// GPU, but a CTA keeps at least `kc_min` k-tiles so that its set-up and its
+// output atomics stay small beside its stream.
+static void plan(int ntt, int mtiles, int KT, int num_sms, int kc_min, int &kc, int &splits) {
+  const int64_t base = (int64_t)ntt * mtiles;
+  const int64_t want = 2 * (int64_t)num_sms;
+  splits = 1;
+  if (base < want) splits = (int)std::min<int64_t>(KT, (want + base - 1) / base);
+  kc = (KT + splits - 1) / splits;
+  kc = std::max(kc, std::min(kc_min, KT));
+  splits = (KT + kc - 1) / kc;
+}
+
+static cudaError_t zero_outputs(const TcJob *jobs, int njobs, int T, cudaStream_t st) {
+  for (int j = 0; j < njobs; ++j) {
+    cudaError_t e = cudaMemset2DAsync(jobs[j].y, (size_t)jobs[j].ldy * 4, 0, (size_t)jobs[j].n * 4, T, st);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+static cudaError_t fill_jobs(const TcJob *jobs, int njobs, TcJobs &J, int &mtiles) {
+  if (njobs < 1 || njobs > MAX_JOBS) return cudaErrorInvalidValue;
+  J = TcJobs{};
+  J.njobs = njobs;
+  mtiles = 0;
+  for (int j = 0; j < njobs; ++j) {
+    J.w[j] = jobs[j].w;
+    J.s[j] = (const uint16_t *)jobs[j].scales;
+    J.y[j] = jobs[j].y;
+    J.n[j] = jobs[j].n;
+    J.ldy[j] = jobs[j].ldy;
+    J.tile0[j] = mtiles;
+    mtiles += (jobs[j].n + 127) / 128;
+  }
+  J.tile0[njobs] = mtiles;
+  return cudaSuccess;
+}
+
+template <int TT, int DU>
+static cudaError_t launch_int4(const TcJobs &J, int mtiles, const uint8_t *bp, int K, int T, int ntt, int num_sms,
+                               bool zero, const TcJob *jobs, int njobs, cudaStream_t st) {
+  using C = Int4Cfg<TT, DU>;
+  static bool configured = false;
+  cudaError_t e = set_smem(k_tc_int4<TT, DU>, C::SMEM, configured);
+  if (e != cudaSuccess) return e;
+  int kc, splits;
+  plan(ntt, mtiles, K / 64, num_sms, 8, kc, splits);
+  if (splits > 1 && zero) {
+    e = zero_outputs(jobs, njobs, T, st);
+    if (e != cudaSuccess) return e;
+  }
+  dim3 grid(ntt, mtiles, splits);
+  k_tc_int4<TT, DU><<<grid, TC_THREADS, C::SMEM, st>>>(J, bp, K, T, kc, splits > 1);
+  count_launch(1);
+  return cudaGetLastError();
+}
+
+cudaError_t tc_gemm_int4(const TcJob *jobs, int njobs, int group, const float *X, int ldx, int T, int K, void *act,
+                         int num_sms, cudaStream_t st) {
+  TcJobs J;
+  int mtiles;
+  cudaError_t e = fill_jobs(jobs, njobs, J, mtiles);
+  if (e != cudaSuccess) return e;
+  const int TT = tt_int4(T);
+  const int ntt = (T + TT - 1) / TT;
+  const int KT = K / 64;
+  const int64_t chunks = (int64_t)ntt * KT * TT * 8;
+  k_tc_pack_act<2><<<blocks_for(chunks, 256), 256, 0, st>>>(X, ldx, T, K, TT, (uint4 *)act);
+  count_launch(1);
+  const uint8_t *bp = (const uint8_t *)act;
+  const int DU = drain_units(group);
+  if (TT == 16) return DU == 1 ? launch_int4<16, 1>(J, mtiles, bp, K, T, ntt, num_sms, true, jobs, njobs, st)
+                               : launch_int4<16, 2>(J, mtiles, bp, K, T, ntt, num_sms, true, jobs, njobs, st);
+  if (TT == 32) return DU == 1 ? launch_int4<32, 1>(J, mtiles, bp, K, T, ntt, num_sms, true, jobs, njobs, st)
+                               : launch_int4<32, 2>(J, mtiles, bp, K, T, ntt, num_sms, true, jobs, njobs, st);
+  return DU == 1 ? launch_int4<64, 1>(J, mtiles, bp, K, T, ntt, num_sms, true, jobs, njobs, st)
+                 : launch_int4<64, 2>(J, mtiles, bp, K, T, ntt, num_sms, true, jobs, njobs, st);
+}
+
+template <int TT>
+static cudaError_t launch_f16(const TcJobs &J, int mtiles, const uint8_t *bp, int K, int T, int ntt, int num_sms,
+                              const TcJob *jobs, int njobs, cudaStream_t st) {
+  using C = F16Cfg<TT>;
+  static bool configured = false;
+  cudaError_t e = set_smem(k_tc_f16<TT>, C::SMEM, configured);
+  if (e != cudaSuccess) return e;
+  int kc, splits;
+  plan(ntt, mtiles, K / 64, num_sms, TT >= 64 ? 16 : 8, kc, splits);
+  if (splits > 1) {
+    e = zero_outputs(jobs, njobs, T, st);
+    if (e != cudaSuccess) return e;
+  }
+  dim3 grid(ntt, mtiles, splits);
+  k_tc_f16<TT><<<grid, TC_THREADS, C::SMEM, st>>>(J, bp, K, T, kc, splits > 1);
+  count_launch(1);
+  return cudaGetLastError();
+}
+
+cudaError_t tc_gemm_f16(const TcJob *jobs, int njobs, const float *X, int ldx, int T, int K, void *act, int num_sms,
+                        cudaStream_t st) {
+  TcJobs J;
+  int mtiles;
+  cudaError_t e = fill_jobs(jobs, njobs, J, mtiles);
+  if (e != cudaSuccess) return e;
+  const int TT = tt_f16(T);
+  const int ntt = (T + TT - 1) / TT;
+  const int KT = K / 64;
+  const int64_t chunks = (int64_t)ntt * KT * TT * 8;
+  k_tc_pack_act<1><<<blocks_for(chunks, 256), 256, 0, st>>>(X, ldx, T, K, TT, (uint4 *)act);
+  count_launch(1);
+  const uint8_t *bp = (const uint8_t *)act;
+  switch (TT) {
+    case 16: return launch_f16<16>(J, mtiles, bp, K, T, ntt, num_sms, jobs, njobs, st);
+    case 32: return launch_f16<32>(J, mtiles, bp, K, T, ntt, num_sms, jobs, njobs, st);
+    case 64: return launch_f16<64>(J, mtiles, bp, K, T, ntt, num_sms, jobs, njobs, st);
+    case 128: return launch_f16<128>(J, mtiles, bp, K, T, ntt, num_sms, jobs, njobs, st);
+    default: return launch_f16<256>(J, mtiles, bp, K, T, ntt, num_sms, jobs, njobs, st);
+  }
+}
+
+cudaError_t read_device_error(unsigned *out, bool reset) {
+  cudaError_t e = cudaMemcpyFromSymbol(out, g_dev_error, sizeof(unsigned));
+  if (e != cudaSuccess) return e;
+  if (reset) {
+    const unsigned zero = 0;
+    e = cudaMemcpyToSymbol(g_dev_error, &zero, sizeof(unsigned));
+  }
+  return e;
+}
+
+}  // namespace dfl

@@ -210,6 +210,9 @@ class PackedMatrix:
         """Y [T][rows] = X [T][cols] . W^T on the GPU."""
         assert x.dtype == torch.float32 and x.is_cuda and x.is_contiguous() and x.shape[1] == self.cols
         y = torch.empty(x.shape[0], self.rows, dtype=torch.float32, device=x.device)
+        nb = L.dflash_gemm_workspace_bytes(self.kind, self.cols, x.shape[0])
+        if getattr(self, "_ws", None) is None or self._ws.numel() < nb:
+            self._ws = torch.empty(nb, dtype=torch.uint8, device=x.device)
         L.dflash_gemm(self.mat, self.kind, self.rows, self.cols, self.group, x.data_ptr(), x.shape[0], y.data_ptr(),
-                      _stream())
+                      self._ws.data_ptr(), self._ws.numel(), _stream())
         return y

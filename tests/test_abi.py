@@ -144,8 +144,14 @@ def test_create_rejects_small_workspace_and_null_weights(L):
 
 
 def test_packed_sizes(L):
-    assert L.dflash_int4_packed_bytes(32, 128, 64) == 32 * 64
-    assert L.dflash_int4_scale_bytes(32, 128, 64) == 2 * 2 * 8 * 4
-    assert L.dflash_int4_packed_bytes(30, 128, 64) == 0
+    # rows pad to tiles of 128; codes are half a byte, scales one f16 per row and 64 (or 32) columns
+    assert L.dflash_int4_packed_bytes(32, 128, 64) == 128 * 64
+    assert L.dflash_int4_packed_bytes(256, 128, 64) == 256 * 64
+    assert L.dflash_int4_scale_bytes(256, 128, 64) == 2 * 2 * 256
+    assert L.dflash_int4_scale_bytes(256, 128, 32) == 2 * 2 * 2 * 256
     assert L.dflash_int4_packed_bytes(32, 96, 32) == 0
-    assert L.dflash_f16_packed_bytes(16, 64) == 2048
+    assert L.dflash_int4_packed_bytes(32, 128, 48) == 0
+    assert L.dflash_f16_packed_bytes(16, 64) == 128 * 64 * 2
+    assert L.dflash_gemm_workspace_bytes(4, 1024, 16) == 16 * 1024 * 4
+    assert L.dflash_gemm_workspace_bytes(16, 1024, 200) == 256 * 1024 * 2
+    assert L.dflash_gemm_workspace_bytes(5, 1024, 16) == 0

@@ -19,6 +19,15 @@ def built():
     build.build()
 
 
+@pytest.fixture(autouse=True)
+def no_device_error():
+    """No kernel of the library may give up a bounded wait."""
+    from speculative_block_drafter_gb300 import _lib as L
+    yield
+    torch.cuda.synchronize()
+    assert L.dflash_device_error(reset=True) == 0
+
+
 def _drafter():
     from speculative_block_drafter_gb300 import drafter
     return drafter
@@ -191,19 +200,21 @@ def test_select_alone_on_identical_inputs():
 
 
 @pytest.mark.parametrize("case", ["empty_context", "windowed", "short_k_shortlist", "no_rope_first_1000",
-                                  "batch3"])
+                                  "batch3", "rep4_long"])
 def test_block_edge_cases(case):
     g = _tiny()
     seeds = [0]
     if case == "windowed":
         g = _tiny(windows=(40,))
+    if case == "rep4_long":              # 4 query heads per KV head (64 queries a CTA), a longer context
+        g = _tiny(heads=8, kv_heads=2, windows=(300,))
     if case == "no_rope_first_1000":
         g = _tiny(no_rope=(0,))
     batch = 3 if case == "batch3" else 1
-    p = Pair(g, max_batch=batch, ctx_cap=512)
+    p = Pair(g, max_batch=batch, ctx_cap=1024)
     anchors, rows, toks, k, width = [], [], [], None, None
     for b in range(batch):
-        first, n = 0, 100 + 37 * b
+        first, n = 0, (700 if case == "rep4_long" else 100 + 37 * b)
         if case == "no_rope_first_1000":
             first = 1000
         p.reset(b, first)
