@@ -65,7 +65,7 @@ def build(verbose: bool = False, ptxas_info: bool = False) -> str:
                     raise RuntimeError(f"nvcc failed on {os.path.basename(src)}")
     objs = [os.path.join(BUILD, os.path.basename(s)[:-3] + ".o") for s in sources]
     if jobs or not os.path.exists(LIB):
-        cmd = [nvcc, *ARCH, "-shared", "-o", LIB, *objs]
+        cmd = [nvcc, *ARCH, "-shared", "-Xlinker", "--no-undefined", "-o", LIB, *objs]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             sys.stderr.write(r.stdout + r.stderr)

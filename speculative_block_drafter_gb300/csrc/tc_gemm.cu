@@ -169,46 +169,88 @@ __device__ __forceinline__ int job_of(const TcJobs &J, int mt) {
 }
 
 // ---------------------------------------------------------------- four-bit kernel
-template <int TT, int DU>
-struct Int4Cfg {
-  static constexpr int B_BYTES = 2 * TT * 128;        // hi + lo planes of one k-tile
-  static constexpr int CODE_OFF = B_BYTES;
-  static constexpr int SCALE_OFF = B_BYTES + 4096;
-  static constexpr int STAGE = ((SCALE_OFF + DU * 256) + 1023) / 1024 * 1024;
-  static constexpr int NDU = TT <= 32 ? 4 : 2;        // accumulators in flight
-  static constexpr int DCOL = TC_STAGES * 32;         // tensor-memory columns of the accumulators
-  static_assert(DCOL + NDU * TT <= (int)TC_TMEM_COLS, "tensor memory");
-  static constexpr int SMEM = TC_STAGES * STAGE + 1024 + 256;
+//
+// Persistent CTAs walk a list of items (MT row tiles of one matrix, a token
+// tile, a k-range); the k-tiles of consecutive items flow through one pipeline:
+//   warp 8        bulk-copies each k-tile (tokens hi/lo, the MT tiles' codes and scales)
+//   warps 0-3     dequantise their row of each tile into a tensor-memory A slot
+//   warps 9..     one per row tile: the MMAs of each quantisation unit, N = 2 TT
+//                 (the hi and lo planes are one 2TT-row B operand)
+//   warps 4-7     read each accumulator back (hi + lo halves), scale it and add
+//                 it up; at the end of an item they write the item's rows
+// A small-N MMA is cheap to run but not to issue (about 50 cycles from one
+// thread), so each row tile has its own issuing warp and each instruction
+// carries both planes. The drain warps release a shared-memory stage (they read
+// its scales last).
+constexpr int I4_PRODUCER = 8;
+constexpr int I4_MMA0 = 9;
+constexpr int I4_MAX_THREADS = 32 * (I4_MMA0 + 2);
+
+template <int TT, int DU, int MT>
+struct I4 {
+  static constexpr int THREADS = 32 * (I4_MMA0 + MT);
+  static constexpr int B_BYTES = 2 * TT * 128;                 // hi + lo planes of a k-tile
+  static constexpr int CODE_OFF = B_BYTES;                     // MT x 4 KiB
+  static constexpr int SCALE_OFF = B_BYTES + MT * 4096;        // MT x DU x 256 B
+  static constexpr int STAGE = ((SCALE_OFF + MT * DU * 256) + 1023) / 1024 * 1024;
+  static constexpr int S = 6;                                  // shared-memory stages
+  static constexpr int SA = 2;                                 // tensor-memory A slots
+  static constexpr int AW = MT * 32;                           // A columns of a slot
+  static constexpr int DW = MT * 2 * TT;                       // accumulator columns of a unit
+  static constexpr int DCOL = SA * AW;
+  static constexpr int NDU = ((int)TC_TMEM_COLS - DCOL) / DW;  // accumulators in flight
+  static_assert(NDU >= 2, "tensor memory");
+  static constexpr int NBAR = 2 * S + 2 * SA + 2 * NDU;
+  static constexpr int SMEM = S * STAGE + 1024 + 512;
 };
 
-template <int TT, int DU>
-__global__ void __launch_bounds__(TC_THREADS) k_tc_int4(TcJobs J, const uint8_t *__restrict__ bpack, int K, int T,
-                                                        int kc, int atomic_out) {
-  using C = Int4Cfg<TT, DU>;
+struct I4Items {
+  int groups;       // row-tile groups over all jobs
+  int gtile0[MAX_JOBS + 1];
+  int splits, kc, ntt, items;
+};
+
+__device__ __forceinline__ void i4_item(const TcJobs &J, const I4Items &P, int MT, int KT, int it, int &job, int &m0,
+                                        int &mtv, int &tt, int &kt0, int &kt1) {
+  const int sp = it % P.splits;
+  const int rest = it / P.splits;
+  const int mg = rest % P.groups;
+  tt = rest / P.groups;
+  job = 0;
+#pragma unroll
+  for (int i = 1; i < MAX_JOBS; ++i)
+    if (i < J.njobs && mg >= P.gtile0[i]) job = i;
+  m0 = (mg - P.gtile0[job]) * MT;
+  const int tiles = J.tile0[job + 1] - J.tile0[job];
+  mtv = min(MT, tiles - m0);
+  kt0 = sp * P.kc;
+  kt1 = min(KT, kt0 + P.kc);
+}
+
+template <int TT, int DU, int MT>
+__global__ void __launch_bounds__(I4_MAX_THREADS, 2) k_tc_int4(TcJobs J, I4Items P, const uint8_t *__restrict__ bpack,
+                                                               int K, int T, int atomic_out) {
+  using C = I4<TT, DU, MT>;
   extern __shared__ __align__(1024) uint8_t smraw[];
   uint8_t *sm = smraw + ((1024 - (smem_u32(smraw) & 1023)) & 1023);
-  uint64_t *bars = (uint64_t *)(sm + TC_STAGES * C::STAGE);
-  uint32_t *tslot = (uint32_t *)(bars + 3 * TC_STAGES + 2 * C::NDU);
-  const uint32_t full0 = smem_u32(bars), empty0 = full0 + 8 * TC_STAGES, afull0 = empty0 + 8 * TC_STAGES;
-  const uint32_t dfull0 = afull0 + 8 * TC_STAGES, dfree0 = dfull0 + 8 * C::NDU;
-
+  uint64_t *bars = (uint64_t *)(sm + C::S * C::STAGE);
+  uint32_t *tslot = (uint32_t *)(bars + C::NBAR);
+  const uint32_t full0 = smem_u32(bars), empty0 = full0 + 8 * C::S, afull0 = empty0 + 8 * C::S;
+  const uint32_t afree0 = afull0 + 8 * C::SA, dfull0 = afree0 + 8 * C::SA, dfree0 = dfull0 + 8 * C::NDU;
   const int KT = K / 64;
-  const int tt = blockIdx.x, mt = blockIdx.y;
-  const int kt0 = blockIdx.z * kc, kt1 = min(KT, kt0 + kc);
-  const int n = kt1 - kt0;
-  if (n <= 0) return;
-  const int job = job_of(J, mt);
-  const int m = mt - J.tile0[job];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < TC_STAGES; ++i) {
+    for (int i = 0; i < C::S; ++i) {
       mbar_init(full0 + 8 * i, 1);
-      mbar_init(empty0 + 8 * i, 1);
+      mbar_init(empty0 + 8 * i, 128);
+    }
+    for (int i = 0; i < C::SA; ++i) {
       mbar_init(afull0 + 8 * i, 128);
+      mbar_init(afree0 + 8 * i, MT);
     }
     for (int i = 0; i < C::NDU; ++i) {
-      mbar_init(dfull0 + 8 * i, 1);
+      mbar_init(dfull0 + 8 * i, MT);
       mbar_init(dfree0 + 8 * i, 128);
     }
     mbar_fence_init();
@@ -219,125 +261,196 @@ __global__ void __launch_bounds__(TC_THREADS) k_tc_int4(TcJobs J, const uint8_t 
   tc_fence_after();
   const uint32_t tbase = *tslot;
 
-  if (warp == TC_PRODUCER) {
+  if (warp == I4_PRODUCER) {
     if (lane == 0) {
-      const uint8_t *wc = (const uint8_t *)J.w[job] + ((int64_t)m * KT) * 4096;
-      const uint8_t *ws = (const uint8_t *)J.s[job] + ((int64_t)m * KT) * DU * 256;
-      const uint8_t *bp = bpack + ((int64_t)tt * KT) * C::B_BYTES;
-      for (int i = 0; i < n; ++i) {
-        const int s = i % TC_STAGES, kt = kt0 + i;
-        if (i >= TC_STAGES && !mbar_wait(empty0 + 8 * s, ((i / TC_STAGES) - 1) & 1)) break;
-        const uint32_t st = smem_u32(sm + s * C::STAGE);
-        mbar_expect_tx(full0 + 8 * s, C::B_BYTES + 4096 + DU * 256);
-        bulk_g2s(st, bp + (int64_t)kt * C::B_BYTES, C::B_BYTES, full0 + 8 * s);
-        bulk_g2s(st + C::CODE_OFF, wc + (int64_t)kt * 4096, 4096, full0 + 8 * s);
-        bulk_g2s(st + C::SCALE_OFF, ws + (int64_t)kt * DU * 256, DU * 256, full0 + 8 * s);
+      int i = 0;
+      bool ok = true;
+      for (int it = blockIdx.x; it < P.items && ok; it += gridDim.x) {
+        int job, m0, mtv, tt, kt0, kt1;
+        i4_item(J, P, MT, KT, it, job, m0, mtv, tt, kt0, kt1);
+        const uint8_t *wc = (const uint8_t *)J.w[job] + (int64_t)m0 * KT * 4096;
+        const uint8_t *ws = (const uint8_t *)J.s[job] + (int64_t)m0 * KT * DU * 256;
+        const uint8_t *bp = bpack + (int64_t)tt * KT * C::B_BYTES;
+        for (int kt = kt0; kt < kt1; ++kt, ++i) {
+          const int s = i % C::S;
+          if (i >= C::S && !mbar_wait(empty0 + 8 * s, ((i / C::S) - 1) & 1)) {
+            ok = false;
+            break;
+          }
+          const uint32_t st = smem_u32(sm + s * C::STAGE);
+          mbar_expect_tx(full0 + 8 * s, C::B_BYTES + mtv * (4096 + DU * 256));
+          bulk_g2s(st, bp + (int64_t)kt * C::B_BYTES, C::B_BYTES, full0 + 8 * s);
+          for (int jj = 0; jj < mtv; ++jj) {
+            bulk_g2s(st + C::CODE_OFF + jj * 4096, wc + ((int64_t)jj * KT + kt) * 4096, 4096, full0 + 8 * s);
+            bulk_g2s(st + C::SCALE_OFF + jj * DU * 256, ws + ((int64_t)jj * KT + kt) * DU * 256, DU * 256,
+                     full0 + 8 * s);
+          }
+        }
       }
     }
-  } else if (warp == TC_MMA) {
+  } else if (warp >= I4_MMA0 && warp < I4_MMA0 + MT) {
     if (lane == 0) {
-      constexpr uint32_t idesc = f16_idesc(128, TT);
-      constexpr int KSU = 4 / DU;  // k-steps of 16 per drain unit
+      const int jj = warp - I4_MMA0;  // this warp's row tile of the item
+      constexpr uint32_t idesc = f16_idesc(128, 2 * TT);
+      constexpr int KSU = 4 / DU;
+      int i = 0, u = 0;
       bool ok = true;
-      for (int i = 0; i < n && ok; ++i) {
-        const int s = i % TC_STAGES;
-        if (!mbar_wait(afull0 + 8 * s, (i / TC_STAGES) & 1)) break;
-        tc_fence_after();
-        const uint32_t st = smem_u32(sm + s * C::STAGE);
-        for (int du = 0; du < DU; ++du) {
-          const int u = i * DU + du, d = u % C::NDU;
-          if (u >= C::NDU && !mbar_wait(dfree0 + 8 * d, ((u / C::NDU) - 1) & 1)) {
+      for (int it = blockIdx.x; it < P.items && ok; it += gridDim.x) {
+        int job, m0, mtv, tt, kt0, kt1;
+        i4_item(J, P, MT, KT, it, job, m0, mtv, tt, kt0, kt1);
+        const bool live = jj < mtv;
+        for (int kt = kt0; kt < kt1 && ok; ++kt, ++i) {
+          const int s = i % C::S, a = i % C::SA;
+          if (!mbar_wait(full0 + 8 * s, (i / C::S) & 1) || !mbar_wait(afull0 + 8 * a, (i / C::SA) & 1)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t dcol = tbase + C::DCOL + d * TT;
-          for (int ks = 0; ks < KSU; ++ks) {
-            const int kstep = du * KSU + ks;
-            const uint32_t a = tbase + s * 32 + kstep * 8;
-            mma_ts(dcol, a, sw128_desc(st + kstep * 32), idesc, ks > 0);
-            mma_ts(dcol, a, sw128_desc(st + TT * 128 + kstep * 32), idesc, 1);
+          const uint32_t st = smem_u32(sm + s * C::STAGE);
+          for (int du = 0; du < DU; ++du, ++u) {
+            const int d = u % C::NDU;
+            if (u >= C::NDU && !mbar_wait(dfree0 + 8 * d, ((u / C::NDU) - 1) & 1)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            if (live) {
+              const uint32_t dcol = tbase + C::DCOL + d * C::DW + jj * 2 * TT;
+#pragma unroll
+              for (int ks = 0; ks < KSU; ++ks) {
+                const int kstep = du * KSU + ks;
+                mma_ts(dcol, tbase + a * C::AW + jj * 32 + kstep * 8, sw128_desc(st + kstep * 32), idesc, ks > 0);
+              }
+            }
+            mma_commit(dfull0 + 8 * d);
           }
-          mma_commit(dfull0 + 8 * d);
+          mma_commit(afree0 + 8 * a);
         }
-        mma_commit(empty0 + 8 * s);
       }
     }
-  } else {
-    // warps 0-3: the row's codes into tensor memory; each accumulator back, scaled
+  } else if (warp < 4) {
+    // dequantise: thread r owns row r of each of the item's tiles
     const int r = warp * 32 + lane;
     const uint32_t lrow = (uint32_t)(warp * 32) << 16;
-    float acc[TT];
-#pragma unroll
-    for (int t = 0; t < TT; ++t) acc[t] = 0.f;
-    float sc_prev[DU], sc_cur[DU];
-#pragma unroll
-    for (int u = 0; u < DU; ++u) sc_prev[u] = sc_cur[u] = 0.f;
+    int i = 0;
     bool ok = true;
-    for (int i = 0; i <= n && ok; ++i) {
-      if (i < n) {
-        const int s = i % TC_STAGES;
-        if (!__all_sync(0xffffffffu, mbar_wait(full0 + 8 * s, (i / TC_STAGES) & 1))) break;
-        const uint8_t *st = sm + s * C::STAGE;
-        const uint4 c0 = *(const uint4 *)(st + C::CODE_OFF + r * 16);
-        const uint4 c1 = *(const uint4 *)(st + C::CODE_OFF + 2048 + r * 16);
-#pragma unroll
-        for (int u = 0; u < DU; ++u)
-          sc_cur[u] = __half2float(__ushort_as_half(*(const uint16_t *)(st + C::SCALE_OFF + u * 256 + r * 2)));
-        uint32_t v[32];
-        const uint32_t words[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          uint32_t a4[4];
-          dequant8(words[j], a4);
-          v[4 * j + 0] = a4[0];
-          v[4 * j + 1] = a4[1];
-          v[4 * j + 2] = a4[2];
-          v[4 * j + 3] = a4[3];
+    for (int it = blockIdx.x; it < P.items && ok; it += gridDim.x) {
+      int job, m0, mtv, tt, kt0, kt1;
+      i4_item(J, P, MT, KT, it, job, m0, mtv, tt, kt0, kt1);
+      for (int kt = kt0; kt < kt1; ++kt, ++i) {
+        const int s = i % C::S, a = i % C::SA;
+        if (!__all_sync(0xffffffffu, mbar_wait(full0 + 8 * s, (i / C::S) & 1))) {
+          ok = false;
+          break;
         }
-        if (i >= TC_STAGES && !__all_sync(0xffffffffu, mbar_wait(empty0 + 8 * s, ((i / TC_STAGES) - 1) & 1))) break;
+        const uint8_t *st = sm + s * C::STAGE;
+        if (i >= C::SA && !__all_sync(0xffffffffu, mbar_wait(afree0 + 8 * a, ((i / C::SA) - 1) & 1))) {
+          ok = false;
+          break;
+        }
         tc_fence_after();
-        tmem_st32(tbase + lrow + s * 32, v);
+#pragma unroll
+        for (int jj = 0; jj < MT; ++jj) {
+          if (jj < mtv) {
+            const uint4 c0 = *(const uint4 *)(st + C::CODE_OFF + jj * 4096 + r * 16);
+            const uint4 c1 = *(const uint4 *)(st + C::CODE_OFF + jj * 4096 + 2048 + r * 16);
+            const uint32_t words[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+            uint32_t v[32];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              uint32_t a4[4];
+              dequant8(words[j], a4);
+              v[4 * j + 0] = a4[0];
+              v[4 * j + 1] = a4[1];
+              v[4 * j + 2] = a4[2];
+              v[4 * j + 3] = a4[3];
+            }
+            tmem_st32(tbase + lrow + a * C::AW + jj * 32, v);
+          }
+        }
         tc_wait_st();
         tc_fence_before();
-        mbar_arrive(afull0 + 8 * s);
+        mbar_arrive(afull0 + 8 * a);
       }
-      const int j = i - 1;  // drain the previous k-tile's accumulators
-      if (j >= 0) {
+    }
+  } else if (warp < 8) {
+    // drain: warps 4-7 read the accumulators of their lanes (rows 32(warp-4) ..)
+    const int r = (warp - 4) * 32 + lane;
+    const uint32_t lrow = (uint32_t)((warp - 4) * 32) << 16;
+    float acc[MT][TT];
 #pragma unroll
-        for (int du = 0; du < DU; ++du) {
-          const int u = j * DU + du, d = u % C::NDU;
+    for (int jj = 0; jj < MT; ++jj)
+#pragma unroll
+      for (int t = 0; t < TT; ++t) acc[jj][t] = 0.f;
+    int i = 0, u = 0;
+    bool ok = true;
+    for (int it = blockIdx.x; it < P.items && ok; it += gridDim.x) {
+      int job, m0, mtv, tt, kt0, kt1;
+      i4_item(J, P, MT, KT, it, job, m0, mtv, tt, kt0, kt1);
+      for (int kt = kt0; kt < kt1 && ok; ++kt, ++i) {
+        const int s = i % C::S;
+        if (!__all_sync(0xffffffffu, mbar_wait(full0 + 8 * s, (i / C::S) & 1))) {
+          ok = false;
+          break;
+        }
+        const uint8_t *st = sm + s * C::STAGE;
+        float sc[MT][DU];
+#pragma unroll
+        for (int jj = 0; jj < MT; ++jj)
+#pragma unroll
+          for (int du = 0; du < DU; ++du)
+            sc[jj][du] = jj < mtv ? __half2float(__ushort_as_half(
+                                        *(const uint16_t *)(st + C::SCALE_OFF + (jj * DU + du) * 256 + r * 2)))
+                                  : 0.f;
+#pragma unroll
+        for (int du = 0; du < DU; ++du, ++u) {
+          const int d = u % C::NDU;
           if (!__all_sync(0xffffffffu, mbar_wait(dfull0 + 8 * d, (u / C::NDU) & 1))) {
             ok = false;
             break;
           }
           tc_fence_after();
 #pragma unroll
-          for (int c0 = 0; c0 < TT; c0 += 16) {
-            uint32_t w16[16];
-            tmem_ld16(tbase + lrow + C::DCOL + d * TT + c0, w16);
-            tc_wait_ld();
+          for (int jj = 0; jj < MT; ++jj) {
+            if (jj < mtv) {
 #pragma unroll
-            for (int e = 0; e < 16; ++e) acc[c0 + e] = fmaf(sc_prev[du], __uint_as_float(w16[e]), acc[c0 + e]);
+              for (int c0 = 0; c0 < TT; c0 += 16) {
+                uint32_t wh[16], wl[16];
+                const uint32_t col = tbase + lrow + C::DCOL + d * C::DW + jj * 2 * TT + c0;
+                tmem_ld16(col, wh);
+                tmem_ld16(col + TT, wl);
+                tc_wait_ld();
+#pragma unroll
+                for (int e = 0; e < 16; ++e)
+                  acc[jj][c0 + e] =
+                      fmaf(sc[jj][du], __uint_as_float(wh[e]) + __uint_as_float(wl[e]), acc[jj][c0 + e]);
+              }
+            }
           }
           tc_fence_before();
           mbar_arrive(dfree0 + 8 * d);
         }
+        mbar_arrive(empty0 + 8 * s);
       }
-#pragma unroll
-      for (int u = 0; u < DU; ++u) sc_prev[u] = sc_cur[u];
-    }
-    const int row = m * 128 + r;
-    if (ok && row < J.n[job]) {
+      if (!ok) break;
+      // the item's rows
       float *y = J.y[job];
-      const int ldy = J.ldy[job];
+      const int ldy = J.ldy[job], n = J.n[job];
 #pragma unroll
-      for (int t = 0; t < TT; ++t) {
-        const int tok = tt * TT + t;
-        if (tok < T) {
-          if (atomic_out) atomicAdd(y + (int64_t)tok * ldy + row, acc[t]);
-          else y[(int64_t)tok * ldy + row] = acc[t];
+      for (int jj = 0; jj < MT; ++jj) {
+        const int row = (m0 + jj) * 128 + r;
+        if (jj < mtv && row < n) {
+#pragma unroll
+          for (int t = 0; t < TT; ++t) {
+            const int tok = tt * TT + t;
+            if (tok < T) {
+              if (atomic_out) atomicAdd(y + (int64_t)tok * ldy + row, acc[jj][t]);
+              else y[(int64_t)tok * ldy + row] = acc[jj][t];
+            }
+          }
         }
+#pragma unroll
+        for (int t = 0; t < TT; ++t) acc[jj][t] = 0.f;
       }
     }
   }
@@ -520,8 +633,8 @@ cudaError_t tc_pack_f16(const uint16_t *src, int64_t rows, int64_t cols, void *d
   return cudaGetLastError();
 }
 
-static int tt_int4(int T) { return T <= 16 ? 16 : T <= 32 ? 32 : 64; }
-static int tt_f16(int T) { return T <= 16 ? 16 : T <= 32 ? 32 : T <= 64 ? 64 : T <= 128 ? 128 : 256; }
+static int tt_int4(int T) { return T <= 16 ? 16 : 32; }
+static int tt_f16(int T) { return T <= 16 ? 16 : T <= 32 ? 32 : T <= 64 ? 64 : 128; }
 
 size_t tc_act_bytes(int T, int K, bool int4) {
   const int TT = int4 ? tt_int4(T) : tt_f16(T);
@@ -575,21 +688,31 @@ static cudaError_t fill_jobs(const TcJob *jobs, int njobs, TcJobs &J, int &mtile
   return cudaSuccess;
 }
 
-template <int TT, int DU>
-static cudaError_t launch_int4(const TcJobs &J, int mtiles, const uint8_t *bp, int K, int T, int ntt, int num_sms,
-                               bool zero, const TcJob *jobs, int njobs, cudaStream_t st) {
-  using C = Int4Cfg<TT, DU>;
+template <int TT, int DU, int MT>
+static cudaError_t launch_int4(const TcJobs &J, int njobs, const uint8_t *bp, int K, int T, int ntt, int num_sms,
+                               const TcJob *jobs, cudaStream_t st) {
+  using C = I4<TT, DU, MT>;
   static bool configured = false;
-  cudaError_t e = set_smem(k_tc_int4<TT, DU>, C::SMEM, configured);
+  cudaError_t e = set_smem(k_tc_int4<TT, DU, MT>, C::SMEM, configured);
   if (e != cudaSuccess) return e;
-  int kc, splits;
-  plan(ntt, mtiles, K / 64, num_sms, 8, kc, splits);
-  if (splits > 1 && zero) {
+  I4Items P{};
+  P.groups = 0;
+  for (int j = 0; j < njobs; ++j) {
+    P.gtile0[j] = P.groups;
+    P.groups += (J.tile0[j + 1] - J.tile0[j] + MT - 1) / MT;
+  }
+  P.gtile0[njobs] = P.groups;
+  P.ntt = ntt;
+  const int KT = K / 64;
+  // enough items for two CTAs an SM, each at least 8 k-tiles long
+  plan(ntt, P.groups, KT, num_sms, 8, P.kc, P.splits);
+  P.items = ntt * P.groups * P.splits;
+  if (P.splits > 1) {
     e = zero_outputs(jobs, njobs, T, st);
     if (e != cudaSuccess) return e;
   }
-  dim3 grid(ntt, mtiles, splits);
-  k_tc_int4<TT, DU><<<grid, TC_THREADS, C::SMEM, st>>>(J, bp, K, T, kc, splits > 1);
+  const int grid = std::min(P.items, 2 * num_sms);
+  k_tc_int4<TT, DU, MT><<<grid, C::THREADS, C::SMEM, st>>>(J, P, bp, K, T, P.splits > 1);
   count_launch(1);
   return cudaGetLastError();
 }
@@ -608,12 +731,10 @@ cudaError_t tc_gemm_int4(const TcJob *jobs, int njobs, int group, const float *X
   count_launch(1);
   const uint8_t *bp = (const uint8_t *)act;
   const int DU = drain_units(group);
-  if (TT == 16) return DU == 1 ? launch_int4<16, 1>(J, mtiles, bp, K, T, ntt, num_sms, true, jobs, njobs, st)
-                               : launch_int4<16, 2>(J, mtiles, bp, K, T, ntt, num_sms, true, jobs, njobs, st);
-  if (TT == 32) return DU == 1 ? launch_int4<32, 1>(J, mtiles, bp, K, T, ntt, num_sms, true, jobs, njobs, st)
-                               : launch_int4<32, 2>(J, mtiles, bp, K, T, ntt, num_sms, true, jobs, njobs, st);
-  return DU == 1 ? launch_int4<64, 1>(J, mtiles, bp, K, T, ntt, num_sms, true, jobs, njobs, st)
-                 : launch_int4<64, 2>(J, mtiles, bp, K, T, ntt, num_sms, true, jobs, njobs, st);
+  if (TT == 16) return DU == 1 ? launch_int4<16, 1, 2>(J, njobs, bp, K, T, ntt, num_sms, jobs, st)
+                               : launch_int4<16, 2, 2>(J, njobs, bp, K, T, ntt, num_sms, jobs, st);
+  return DU == 1 ? launch_int4<32, 1, 1>(J, njobs, bp, K, T, ntt, num_sms, jobs, st)
+                 : launch_int4<32, 2, 1>(J, njobs, bp, K, T, ntt, num_sms, jobs, st);
 }
 
 template <int TT>
@@ -652,8 +773,7 @@ cudaError_t tc_gemm_f16(const TcJob *jobs, int njobs, const float *X, int ldx, i
     case 16: return launch_f16<16>(J, mtiles, bp, K, T, ntt, num_sms, jobs, njobs, st);
     case 32: return launch_f16<32>(J, mtiles, bp, K, T, ntt, num_sms, jobs, njobs, st);
     case 64: return launch_f16<64>(J, mtiles, bp, K, T, ntt, num_sms, jobs, njobs, st);
-    case 128: return launch_f16<128>(J, mtiles, bp, K, T, ntt, num_sms, jobs, njobs, st);
-    default: return launch_f16<256>(J, mtiles, bp, K, T, ntt, num_sms, jobs, njobs, st);
+    default: return launch_f16<128>(J, mtiles, bp, K, T, ntt, num_sms, jobs, njobs, st);
   }
 }
 

@@ -1,0 +1,76 @@
+"""Time one of the drafter's kernels alone through the C ABI (for tuning and profiling).
+
+    python -m speculative_block_drafter_gb300.microbench gemm --rows 151936 --cols 1024 --tokens 15 --kind 4
+    python -m speculative_block_drafter_gb300.microbench gemm --rows 5120 --cols 25600 --tokens 256 --kind 16
+
+Random codes / values of the given shape; the L2 cache is flushed between
+launches; prints the mean time and the algorithmic bandwidth of one launch
+(weights, activations in, outputs out).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+
+import numpy as np
+import torch
+
+import dflash_inputs as di
+from . import build
+from .drafter import PackedMatrix
+
+
+def _int4(rows, cols, group, seed=0):
+    rng = np.random.default_rng(seed)
+    codes = rng.integers(0, 256, size=(rows, cols // 2), dtype=np.uint8)
+    scales = (rng.random((rows, cols // group)) * 0.01 + 1e-3).astype(np.float16)
+    return di.Int4(codes=codes, scales=scales, rows=rows, cols=cols, group=group)
+
+
+def gemm(args):
+    build.build()
+    if args.kind == 4:
+        m = _int4(args.rows, args.cols, args.group)
+        wbytes = args.rows * args.cols // 2 + args.rows * (args.cols // args.group) * 2
+    else:
+        m = (np.random.default_rng(0).standard_normal((args.rows, args.cols)) * 0.01).astype(np.float16)
+        wbytes = args.rows * args.cols * 2
+    pm = PackedMatrix(m)
+    x = torch.randn(args.tokens, args.cols, device="cuda")
+    flush = torch.empty(256 << 18, device="cuda")
+    for _ in range(3):
+        pm.matmul(x)
+    torch.cuda.synchronize()
+    ts = []
+    for _ in range(args.iters):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        pm.matmul(x)
+        b.record()
+        torch.cuda.synchronize()
+        ts.append(a.elapsed_time(b))
+    ms = float(np.mean(ts))
+    nbytes = wbytes + x.numel() * 4 + args.tokens * args.rows * 4
+    print(json.dumps({"kernel": f"gemm kind {args.kind}", "rows": args.rows, "cols": args.cols, "tokens": args.tokens,
+                      "ms": round(ms, 5), "GB/s": round(nbytes / ms / 1e6, 1),
+                      "TFLOP/s": round(2 * args.rows * args.cols * args.tokens / ms / 1e9, 1)}))
+
+
+def main():
+    p = argparse.ArgumentParser()
+    sub = p.add_subparsers(dest="cmd", required=True)
+    g = sub.add_parser("gemm")
+    g.add_argument("--rows", type=int, default=151936)
+    g.add_argument("--cols", type=int, default=1024)
+    g.add_argument("--tokens", type=int, default=15)
+    g.add_argument("--kind", type=int, default=4, choices=[4, 16])
+    g.add_argument("--group", type=int, default=64)
+    g.add_argument("--iters", type=int, default=20)
+    args = p.parse_args()
+    if args.cmd == "gemm":
+        gemm(args)
+
+
+if __name__ == "__main__":
+    main()
