@@ -34,10 +34,23 @@ __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
-// Wait for the phase of parity `parity` to complete; false after the limit.
+// try_wait that lets the hardware suspend the thread up to `ns` nanoseconds
+// while the phase is incomplete (it resumes as soon as the phase completes), so
+// that waiting warps leave the issue slots to the working ones.
+__device__ __forceinline__ bool mbar_try_sleep(uint32_t bar, uint32_t parity, uint32_t ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(ns)
+      : "memory");
+  return ok != 0;
+}
+// Wait for the phase of parity `parity` to complete; false after the limit
+// (at most 2^18 suspensions of up to 4 us each).
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
-  for (int i = 0; i < (1 << 21); ++i)
-    if (mbar_try(bar, parity)) return true;
+  for (int i = 0; i < (1 << 18); ++i)
+    if (mbar_try_sleep(bar, parity, 4000)) return true;
   atomicOr(&g_dev_error, DFL_ERR_TIMEOUT);
   return false;
 }
