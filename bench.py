@@ -113,6 +113,25 @@ class Clocks:
                 "sm_max_mhz": max(smax) if smax else None, "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def head_traffic(workload: str):
+    """DRAM bytes of one head-GEMM launch from the committed ncu capture, or None
+    when there is none for this workload or the kernel sources changed since."""
+    import hashlib
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            doc = json.load(f)
+        h = hashlib.sha256()
+        for s in ("tc_gemm.cu", "tc.cuh", "common.cuh", "kernels.h"):
+            with open(os.path.join(ROOT, "speculative_block_drafter_gb300", "csrc", s), "rb") as f:
+                h.update(f.read())
+        if h.hexdigest()[:16] != doc.get("sources_sha256_16"):
+            return None
+        entry = doc.get(f"gemm_int4_head@{workload}")
+        return int(entry["bytes"]) if entry else None
+    except (OSError, ValueError, KeyError):
+        return None
+
+
 # ------------------------------------------------------------------ the GB300 arm
 class Bench:
     def __init__(self, wl, device):
@@ -207,12 +226,7 @@ class Bench:
         nbytes = (rows * g.hidden // 2 + rows * (g.hidden // g.quant_group) * 2
                   + x.numel() * 4 + x.shape[0] * rows * 4)
         achieved = nbytes / t / 1e9
-        traffic = None
-        try:
-            with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
-                traffic = json.load(f).get(f"gemm_int4_head@{self.wl.name}")
-        except Exception:
-            pass
+        traffic = head_traffic(self.wl.name)
         return {"kernel": "k_gemm<int4> (head, %d x %d, %d rows)" % (rows, g.hidden, x.shape[0]),
                 "bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
                 "frac": round(achieved / hbm_peak, 4), "traffic": traffic,
