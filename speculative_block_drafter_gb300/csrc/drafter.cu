@@ -334,15 +334,24 @@ int dflash_settle(dflash_t *d, int32_t seq, int64_t pos, const float *taps, int3
   const dfl::TcJob fc{d->w.fc.data, nullptr, d->x, hs, hs};
   DF_CUDA(dfl::tc_gemm_f16(&fc, 1, taps, tw, n, tw, d->act, d->num_sms, st));
   DF_CUDA(dfl::rmsnorm(d->x, d->w.hidden_norm, d->x, n, hs, (float)g.eps, 1, -1, -1, st));
+  // k = Wk t, v = Wv t of every layer in one GEMM, straight into the caches at rows at..at+n-1
+  dfl::WideJob kv[dfl::WIDE_MAX_JOBS];
+  float *kc[DFLASH_MAX_LAYERS];
+  const float *kn[DFLASH_MAX_LAYERS];
+  int rot[DFLASH_MAX_LAYERS];
   for (int l = 0; l < g.layers; ++l) {
     const dflash_layer_weights &L = d->layers[l];
-    float *kc = d->ck[(size_t)seq * g.layers + l] + at * kvd;
-    float *vc = d->cv[(size_t)seq * g.layers + l] + at * kvd;
-    const dfl::TcJob kv[2] = {{L.k.data, L.k.scales, kc, kvd, kvd}, {L.v.data, L.v.scales, vc, kvd, kvd}};
-    DF_CUDA(dfl::tc_gemm_int4(kv, 2, g.quant_group, d->x, hs, n, hs, d->act, d->num_sms, st));
-    DF_CUDA(dfl::head_norm_rope(kc, kvd, L.k_norm, d->inv.data(), n, g.kv_heads, g.head_dim, (float)g.eps,
-                                g.no_rope[l] == 0, nullptr, 0, 1, pos, st));
+    kc[l] = d->ck[(size_t)seq * g.layers + l] + at * kvd;
+    kn[l] = L.k_norm;
+    rot[l] = g.no_rope[l] == 0;
+    kv[2 * l] = dfl::WideJob{L.k.data, L.k.scales, kc[l], kvd, kvd, 0};
+    kv[2 * l + 1] = dfl::WideJob{L.v.data, L.v.scales, d->cv[(size_t)seq * g.layers + l] + at * kvd, kvd, kvd, 0};
   }
+  DF_CUDA(dfl::wide_zero(kv, 2 * g.layers, 0, n, st));
+  DF_CUDA(dfl::wide_pack(d->x, hs, n, hs, true, d->act, st));
+  DF_CUDA(dfl::wide_gemm(kv, 2 * g.layers, 0, true, g.quant_group, d->act, n, hs, d->num_sms, st));
+  // k = rot(rms_head(k, k_norm)) at positions pos..pos+n-1 (rotary layers)
+  DF_CUDA(dfl::ctx_norm_rope(kc, kn, rot, g.layers, n, g.kv_heads, g.head_dim, (float)g.eps, d->inv.data(), pos, st));
   s.len = at + n;
   return DFLASH_OK;
 }

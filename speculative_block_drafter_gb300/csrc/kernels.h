@@ -44,6 +44,42 @@ cudaError_t tc_gemm_int4(const TcJob *jobs, int njobs, int group, const float *X
                          int num_sms, cudaStream_t st);
 cudaError_t tc_gemm_f16(const TcJob *jobs, int njobs, const float *X, int ldx, int T, int K, void *act, int num_sms,
                         cudaStream_t st);
+// Pack X [T][ldx] (K columns) into token tiles of TT rows: per (tile, k-tile)
+// `planes` f16 planes (hi = f16(x), lo = f16(x - hi)) of TT x 64, 128-byte swizzled.
+cudaError_t pack_act(const float *X, int ldx, int T, int K, int TT, int planes, void *act, cudaStream_t st);
+
+// -------------------------------------------------------------- wide GEMMs (tc_wide.cu)
+// Many tokens (T > 32): the (token tile, row tile, k-tile) units of all jobs
+// are split evenly over the SMs and every output is accumulated with atomics
+// (the caller clears Y first). Jobs share K; `tile0` is a job's first row tile
+// in the concatenation of all jobs' 128-row tiles (in job order). The jobs
+// travel by value in the launch (K and V of up to 64 layers).
+constexpr int WIDE_MAX_N = 256;      // token rows of one MMA
+constexpr int WIDE_MAX_JOBS = 128;
+struct WideJob {
+  const void *w;   // packed codes or f16 tiles
+  const void *s;   // packed scales (four-bit), else null
+  float *y;        // [T][ldy] (y_off added)
+  int n;           // rows
+  int ldy;
+  int tile0;
+};
+struct WideArgs {
+  int njobs, mtiles;
+  int64_t y_off;
+  const uint8_t *bpack;
+  int K, KT, T, N, ntt;
+  int64_t units;
+  WideJob job[WIDE_MAX_JOBS];
+};
+void wide_tiles(int T, int &ntt, int &N);
+size_t wide_act_bytes(int T, int K, bool int4);
+cudaError_t wide_pack(const float *X, int ldx, int T, int K, bool int4, void *act, cudaStream_t st);
+cudaError_t wide_gemm(const WideJob *jobs, int njobs, int64_t y_off, bool int4, int group, const void *act, int T,
+                      int K, int num_sms, cudaStream_t st);
+// Clear rows [0, T) after y_off of each job's output.
+cudaError_t wide_zero(const WideJob *jobs, int njobs, int64_t y_off, int T, cudaStream_t st);
+
 // The device error word (a bounded wait that gave up sets bit 0).
 cudaError_t read_device_error(unsigned *out, bool reset);
 
@@ -67,6 +103,11 @@ constexpr int MAX_BATCH = 64;
 cudaError_t head_norm_rope(float *x, int ld, const float *w, const float *inv_freq, int T, int heads, int hd,
                            float eps, bool rotary, const int64_t *pos0, int nseq, int block, int64_t pos_base,
                            cudaStream_t st);
+// The context K of every layer of one settle: the per-head norm and rotation of
+// rows [0, T) of k[l] (ld = heads * hd) to positions pos_base + t, with layer
+// l's norm weight w[l] and rotary flag (host arrays of `nlayers`, passed by value).
+cudaError_t ctx_norm_rope(float *const *k, const float *const *w, const int *rotary, int nlayers, int T, int heads,
+                          int hd, float eps, const float *inv_freq, int64_t pos_base, cudaStream_t st);
 // m = silu(g) * u, elementwise over n values.
 cudaError_t silu_mul(const float *g, const float *u, float *m, int64_t n, cudaStream_t st);
 

@@ -85,18 +85,13 @@ struct PosArgs {
   float inv[64];  // inv_freq, head_dim <= 128
 };
 
-// One warp per (row, head). HD/32 values per lane: lane owns i = lane + 32m
+// One warp normalises one head of HD values at p (weight w) and, if rotary,
+// rotates it to `pos`. HD/32 values per lane: lane owns i = lane + 32m
 // (m < HD/64) of the low half and its partner i + HD/2.
 template <int HD>
-__global__ void k_head_norm_rope(float *__restrict__ x, int ld, const float *__restrict__ w, int T, int heads,
-                                 float eps, int rotary, PosArgs pa,
-                                 int use_pos0, int block, int64_t pos_base) {
+__device__ __forceinline__ void norm_rope_head(float *__restrict__ p, const float *__restrict__ w, float eps,
+                                               bool rotary, int64_t pos, const float *inv, int lane) {
   constexpr int M = HD / 64;  // pairs per lane
-  const int wid = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const int lane = threadIdx.x & 31;
-  if (wid >= T * heads) return;
-  const int t = wid / heads, h = wid % heads;
-  float *p = x + (int64_t)t * ld + h * HD;
   float lo[M], hi[M];
   float ss = 0.f;
 #pragma unroll
@@ -114,11 +109,10 @@ __global__ void k_head_norm_rope(float *__restrict__ x, int ld, const float *__r
     hi[m] = hi[m] * s * w[lane + 32 * m + HD / 2];
   }
   if (rotary) {
-    const int64_t pos = use_pos0 ? pa.pos0[t / block] + (t % block) : pos_base + t;
     const float fp = (float)pos;
 #pragma unroll
     for (int m = 0; m < M; ++m) {
-      const float ang = __fmul_rn(fp, pa.inv[lane + 32 * m]);
+      const float ang = __fmul_rn(fp, inv[lane + 32 * m]);
       float sn, cs;
       sincosf(ang, &sn, &cs);
       const float a = lo[m], b = hi[m];
@@ -131,6 +125,57 @@ __global__ void k_head_norm_rope(float *__restrict__ x, int ld, const float *__r
     p[lane + 32 * m] = lo[m];
     p[lane + 32 * m + HD / 2] = hi[m];
   }
+}
+
+// One warp per (row, head).
+template <int HD>
+__global__ void k_head_norm_rope(float *__restrict__ x, int ld, const float *__restrict__ w, int T, int heads,
+                                 float eps, int rotary, PosArgs pa,
+                                 int use_pos0, int block, int64_t pos_base) {
+  const int wid = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (wid >= T * heads) return;
+  const int t = wid / heads, h = wid % heads;
+  const int64_t pos = use_pos0 ? pa.pos0[t / block] + (t % block) : pos_base + t;
+  norm_rope_head<HD>(x + (int64_t)t * ld + h * HD, w, eps, rotary != 0, pos, pa.inv, lane);
+}
+
+struct CtxRope {
+  float *k[64];
+  const float *w[64];
+  int rotary[64];
+  float inv[64];
+};
+
+// One warp per (row, head) of layer blockIdx.y's context K.
+template <int HD>
+__global__ void k_ctx_norm_rope(CtxRope R, int T, int heads, float eps, int64_t pos_base) {
+  const int wid = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (wid >= T * heads) return;
+  const int l = blockIdx.y;
+  const int t = wid / heads, h = wid % heads;
+  norm_rope_head<HD>(R.k[l] + ((int64_t)t * heads + h) * HD, R.w[l], eps, R.rotary[l] != 0, pos_base + t, R.inv, lane);
+}
+
+cudaError_t ctx_norm_rope(float *const *k, const float *const *w, const int *rotary, int nlayers, int T, int heads,
+                          int hd, float eps, const float *inv_freq, int64_t pos_base, cudaStream_t st) {
+  if (T <= 0) return cudaSuccess;
+  if (nlayers < 1 || nlayers > 64) return cudaErrorInvalidValue;
+  CtxRope R{};
+  for (int l = 0; l < nlayers; ++l) {
+    R.k[l] = k[l];
+    R.w[l] = w[l];
+    R.rotary[l] = rotary[l];
+  }
+  for (int i = 0; i < 64; ++i) R.inv[i] = i < hd / 2 ? inv_freq[i] : 0.f;
+  const int warps = T * heads;
+  dim3 grid((unsigned)((warps * 32 + 255) / 256), nlayers);
+  if (hd == 128) k_ctx_norm_rope<128><<<grid, 256, 0, st>>>(R, T, heads, eps, pos_base);
+  else if (hd == 64) k_ctx_norm_rope<64><<<grid, 256, 0, st>>>(R, T, heads, eps, pos_base);
+  else return cudaErrorInvalidValue;
+  count_launch(1);
+  return cudaGetLastError();
 }
 
 cudaError_t head_norm_rope(float *x, int ld, const float *w, const float *inv_freq, int T, int heads, int hd,

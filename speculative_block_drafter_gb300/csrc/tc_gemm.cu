@@ -633,12 +633,38 @@ cudaError_t tc_pack_f16(const uint16_t *src, int64_t rows, int64_t cols, void *d
   return cudaGetLastError();
 }
 
+static cudaError_t zero_outputs(const TcJob *jobs, int njobs, int T, cudaStream_t st);
+
+// Up to 32 tokens: the kernels of this file; more: the wide GEMMs (tc_wide.cu).
+constexpr int NARROW_MAX_T = 32;
 static int tt_int4(int T) { return T <= 16 ? 16 : 32; }
-static int tt_f16(int T) { return T <= 16 ? 16 : T <= 32 ? 32 : T <= 64 ? 64 : 128; }
+static int tt_f16(int T) { return T <= 16 ? 16 : 32; }
 
 size_t tc_act_bytes(int T, int K, bool int4) {
+  if (T > NARROW_MAX_T) return wide_act_bytes(T, K, int4);
   const int TT = int4 ? tt_int4(T) : tt_f16(T);
   return (size_t)((T + TT - 1) / TT) * TT * K * 2 * (int4 ? 2 : 1);
+}
+
+cudaError_t pack_act(const float *X, int ldx, int T, int K, int TT, int planes, void *act, cudaStream_t st) {
+  const int64_t chunks = (int64_t)((T + TT - 1) / TT) * (K / 64) * TT * 8;
+  if (planes == 2) k_tc_pack_act<2><<<blocks_for(chunks, 256), 256, 0, st>>>(X, ldx, T, K, TT, (uint4 *)act);
+  else k_tc_pack_act<1><<<blocks_for(chunks, 256), 256, 0, st>>>(X, ldx, T, K, TT, (uint4 *)act);
+  count_launch(1);
+  return cudaGetLastError();
+}
+
+// The wide path for up to 4 matrices given as TcJobs.
+static cudaError_t wide_jobs(const TcJob *jobs, int njobs, bool int4, int group, const float *X, int ldx, int T,
+                             int K, void *act, int num_sms, cudaStream_t st) {
+  if (njobs < 1 || njobs > MAX_JOBS) return cudaErrorInvalidValue;
+  WideJob w[MAX_JOBS];
+  for (int j = 0; j < njobs; ++j) w[j] = WideJob{jobs[j].w, jobs[j].scales, jobs[j].y, jobs[j].n, jobs[j].ldy, 0};
+  cudaError_t e = zero_outputs(jobs, njobs, T, st);
+  if (e != cudaSuccess) return e;
+  e = wide_pack(X, ldx, T, K, int4, act, st);
+  if (e != cudaSuccess) return e;
+  return wide_gemm(w, njobs, 0, int4, group, act, T, K, num_sms, st);
 }
 
 template <typename KERN>
@@ -719,6 +745,7 @@ static cudaError_t launch_int4(const TcJobs &J, int njobs, const uint8_t *bp, in
 
 cudaError_t tc_gemm_int4(const TcJob *jobs, int njobs, int group, const float *X, int ldx, int T, int K, void *act,
                          int num_sms, cudaStream_t st) {
+  if (T > NARROW_MAX_T) return wide_jobs(jobs, njobs, true, group, X, ldx, T, K, act, num_sms, st);
   TcJobs J;
   int mtiles;
   cudaError_t e = fill_jobs(jobs, njobs, J, mtiles);
@@ -745,7 +772,7 @@ static cudaError_t launch_f16(const TcJobs &J, int mtiles, const uint8_t *bp, in
   cudaError_t e = set_smem(k_tc_f16<TT>, C::SMEM, configured);
   if (e != cudaSuccess) return e;
   int kc, splits;
-  plan(ntt, mtiles, K / 64, num_sms, TT >= 64 ? 16 : 8, kc, splits);
+  plan(ntt, mtiles, K / 64, num_sms, 8, kc, splits);
   if (splits > 1) {
     e = zero_outputs(jobs, njobs, T, st);
     if (e != cudaSuccess) return e;
@@ -758,6 +785,7 @@ static cudaError_t launch_f16(const TcJobs &J, int mtiles, const uint8_t *bp, in
 
 cudaError_t tc_gemm_f16(const TcJob *jobs, int njobs, const float *X, int ldx, int T, int K, void *act, int num_sms,
                         cudaStream_t st) {
+  if (T > NARROW_MAX_T) return wide_jobs(jobs, njobs, false, 0, X, ldx, T, K, act, num_sms, st);
   TcJobs J;
   int mtiles;
   cudaError_t e = fill_jobs(jobs, njobs, J, mtiles);
@@ -769,12 +797,8 @@ cudaError_t tc_gemm_f16(const TcJob *jobs, int njobs, const float *X, int ldx, i
   k_tc_pack_act<1><<<blocks_for(chunks, 256), 256, 0, st>>>(X, ldx, T, K, TT, (uint4 *)act);
   count_launch(1);
   const uint8_t *bp = (const uint8_t *)act;
-  switch (TT) {
-    case 16: return launch_f16<16>(J, mtiles, bp, K, T, ntt, num_sms, jobs, njobs, st);
-    case 32: return launch_f16<32>(J, mtiles, bp, K, T, ntt, num_sms, jobs, njobs, st);
-    case 64: return launch_f16<64>(J, mtiles, bp, K, T, ntt, num_sms, jobs, njobs, st);
-    default: return launch_f16<128>(J, mtiles, bp, K, T, ntt, num_sms, jobs, njobs, st);
-  }
+  return TT == 16 ? launch_f16<16>(J, mtiles, bp, K, T, ntt, num_sms, jobs, njobs, st)
+                  : launch_f16<32>(J, mtiles, bp, K, T, ntt, num_sms, jobs, njobs, st);
 }
 
 cudaError_t read_device_error(unsigned *out, bool reset) {

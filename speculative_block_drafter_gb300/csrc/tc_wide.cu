@@ -1,0 +1,481 @@
+// Weight GEMMs over many tokens (a settle chunk of up to 256 rows, a batch of
+// blocks) on the tcgen05 tensor cores: Y[t][r] = sum_k X[t][k] W[r][k].
+//
+// At these sizes a 128-row weight tile meets up to 256 tokens in one MMA
+// (M = 128, N = tokens, K = 16), so the weights are no longer the whole cost:
+// the work is split evenly over the SMs ("stream-K"). The (token tile, row
+// tile, 64-column k-tile) units of all matrices are laid end to end and each
+// CTA takes one contiguous run. Wherever the run crosses a row tile, the CTA
+// adds its partial sums into Y with atomics (Y is cleared first).
+//
+//   warp 4      bulk-copies each unit's operands into a shared-memory ring
+//   warp 5      issues the MMAs (one thread)
+//   warps 0-3   four-bit matrices: turn the unit's codes into the A operand in
+//               tensor memory; at the end of a run: read the accumulator back
+//               and add it to Y
+//
+// f16 matrices (fc, the kernel projections, the selector's projection): the
+// weight tiles go to shared memory as packed and the tokens enter rounded to
+// f16, as the card arm does (`to_half`, cortiq-engine
+// src/gpu_cuda/hyb/dflash.rs, `Dev::settle`).
+//
+// Four-bit matrices: every weight q * s is written exactly as hi + lo, two
+// f16 values, after scaling the row by a power of two 2^p chosen from its
+// largest scale in the run (so that lo stays a normal f16); the tokens enter
+// as f16 planes x = xh + xl. One accumulator spans the whole run:
+//   D = Wh xh + Wh xl + Wl xh   (three MMAs a k-step; Wl xl is below 2^-22)
+// and the run's partial sums are multiplied by 2^-p when added to Y.
+#include <algorithm>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "tc.cuh"
+
+namespace dfl {
+
+constexpr int W_THREADS = 192;
+constexpr int W_PRODUCER = 4;
+constexpr int W_MMA = 5;
+constexpr int W_KIND_F16 = 0;
+constexpr int W_KIND_I4 = 1;
+
+template <int KIND, int DU>
+struct WCfg {
+  // shared-memory stage: B (token planes, N x 128 B each) first, then
+  // f16: the weight tile (16 KiB); four-bit: codes (4 KiB) and scales (DU x 256 B)
+  static constexpr int PLANES = KIND == W_KIND_F16 ? 1 : 2;
+  static constexpr int A_BYTES = KIND == W_KIND_F16 ? 16384 : 4096 + DU * 256;
+  static constexpr int STAGE_MAX = (PLANES * WIDE_MAX_N * 128 + A_BYTES + 1023) / 1024 * 1024;
+  static constexpr int STAGES = KIND == W_KIND_F16 ? 4 : 3;
+  static constexpr int SA = 2;                     // tensor-memory A slots (four-bit)
+  static constexpr int NBUF = KIND == W_KIND_F16 ? 2 : 1;
+  static constexpr int A_COL = 256;                // A slots after the accumulator (four-bit)
+  static constexpr int NBAR = 2 * STAGES + 2 * SA + 2 * NBUF;
+  static constexpr int SMEM = STAGES * STAGE_MAX + 1024 + 8 * NBAR + 64;
+};
+
+__device__ __forceinline__ WideJob wjob(const WideArgs &A, int j) { return A.job[j]; }
+
+// The job holding global row tile mt (jobs in order of tile0).
+__device__ __forceinline__ int wjob_of(const WideArgs &A, int mt) {
+  int lo = 0, hi = A.njobs - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (wjob(A, mid).tile0 <= mt) lo = mid;
+    else hi = mid - 1;
+  }
+  return lo;
+}
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// Bulk copy into the same offset of the shared memory of every CTA in `mask`,
+// signalling each one's barrier at offset `bar`.
+__device__ __forceinline__ void bulk_g2s_mc(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar,
+                                            uint16_t mask) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster [%0], [%1], %2, [%3], %4;" ::
+          "r"(dst),
+      "l"(src), "r"(bytes), "r"(bar), "h"(mask)
+      : "memory");
+}
+// Arrive on the barrier at offset `bar` of every CTA in `mask` once this thread's MMAs so far are done.
+__device__ __forceinline__ void mma_commit_mc(uint32_t bar, uint16_t mask) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::
+                   "r"(bar),
+               "h"(mask)
+               : "memory");
+}
+
+// A unit: token tile, group of CL row tiles (this CTA's tile = group * CL + rank), k-tile.
+struct WUnit {
+  int tt, mt, kt;
+  bool ghost;  // past the last row tile: the CTA only helps its cluster load B
+};
+template <int CL>
+__device__ __forceinline__ WUnit wunit(const WideArgs &A, int64_t u, int rank) {
+  const int groups = (A.mtiles + CL - 1) / CL;
+  const int64_t per_tt = (int64_t)groups * A.KT;
+  WUnit r;
+  r.tt = (int)(u / per_tt);
+  const int64_t rest = u - (int64_t)r.tt * per_tt;
+  const int g = (int)(rest / A.KT);
+  r.kt = (int)(rest - (int64_t)g * A.KT);
+  r.mt = g * CL + rank;
+  r.ghost = r.mt >= A.mtiles;
+  if (r.ghost) r.mt = A.mtiles - 1;
+  return r;
+}
+
+// the end (exclusive) of the run that starts at unit u: the end of its k-range or of the cluster's range
+__device__ __forceinline__ int64_t wrun_end(const WideArgs &A, int64_t u, int64_t u1) {
+  const int64_t tile_end = (u / A.KT + 1) * A.KT;
+  return tile_end < u1 ? tile_end : u1;
+}
+
+template <int KIND, int DU, int CL>
+__global__ void __launch_bounds__(W_THREADS, 1) k_wide(WideArgs A) {
+  using C = WCfg<KIND, DU>;
+  constexpr int S = C::STAGES;
+  extern __shared__ __align__(1024) uint8_t smraw[];
+  uint8_t *sm = smraw + ((1024 - (smem_u32(smraw) & 1023)) & 1023);
+  const int N = A.N;
+  const int b_bytes = C::PLANES * N * 128;
+  const int stage = (b_bytes + C::A_BYTES + 1023) & ~1023;
+  uint64_t *bars = (uint64_t *)(sm + S * stage);
+  uint32_t *tslot = (uint32_t *)(bars + C::NBAR);
+  const uint32_t full0 = smem_u32(bars), empty0 = full0 + 8 * S, afull0 = empty0 + 8 * S;
+  const uint32_t afree0 = afull0 + 8 * C::SA, dfull0 = afree0 + 8 * C::SA, dfree0 = dfull0 + 8 * C::NBUF;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int rank = CL > 1 ? (int)cluster_rank() : 0;
+  const uint16_t everyone = (uint16_t)((1u << CL) - 1);
+
+  // this cluster's units
+  const int64_t q = blockIdx.x / CL, Q = gridDim.x / CL;
+  const int64_t u0 = q * A.units / Q;
+  const int64_t u1 = (q + 1) * A.units / Q;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < S; ++i) {
+      mbar_init(full0 + 8 * i, 1);
+      // released by every cluster CTA's MMAs (their B) and, four-bit, this CTA's dequantisers (codes)
+      mbar_init(empty0 + 8 * i, KIND == W_KIND_F16 ? CL : CL + 128);
+    }
+    for (int i = 0; i < C::SA; ++i) {
+      mbar_init(afull0 + 8 * i, 128);
+      mbar_init(afree0 + 8 * i, 1);
+    }
+    for (int i = 0; i < C::NBUF; ++i) {
+      mbar_init(dfull0 + 8 * i, 1);
+      mbar_init(dfree0 + 8 * i, 128);
+    }
+    mbar_fence_init();
+  }
+  if (warp == 0) tmem_alloc(smem_u32(tslot), 512);
+  tc_fence_before();
+  __syncthreads();
+  if (CL > 1) cluster_sync();  // every barrier of the cluster exists before the first multicast
+  tc_fence_after();
+  const uint32_t tbase = *tslot;
+
+  if (warp == W_PRODUCER) {
+    if (lane == 0) {
+      const int slice = b_bytes / CL;
+      int i = 0;
+      bool ok = true;
+      for (int64_t u = u0; u < u1; ++u, ++i) {
+        const WUnit w = wunit<CL>(A, u, rank);
+        const int s = i % S;
+        if (i >= S && !mbar_wait(empty0 + 8 * s, ((i / S) - 1) & 1)) {
+          ok = false;
+          break;
+        }
+        const WideJob J = wjob(A, wjob_of(A, w.mt));
+        const int64_t tile = (int64_t)(w.mt - J.tile0) * A.KT + w.kt;
+        const uint32_t st = smem_u32(sm + s * stage);
+        const uint8_t *bp = A.bpack + ((int64_t)w.tt * A.KT + w.kt) * b_bytes;
+        mbar_expect_tx(full0 + 8 * s, b_bytes + C::A_BYTES);
+        if (CL > 1) bulk_g2s_mc(st + rank * slice, bp + rank * slice, slice, full0 + 8 * s, everyone);
+        else bulk_g2s(st, bp, b_bytes, full0 + 8 * s);
+        if (KIND == W_KIND_F16) {
+          bulk_g2s(st + b_bytes, (const uint8_t *)J.w + tile * 16384, 16384, full0 + 8 * s);
+        } else {
+          bulk_g2s(st + b_bytes, (const uint8_t *)J.w + tile * 4096, 4096, full0 + 8 * s);
+          bulk_g2s(st + b_bytes + 4096, (const uint8_t *)J.s + tile * DU * 256, DU * 256, full0 + 8 * s);
+        }
+      }
+      // every stage released by every consumer (no copy or remote arrive still bound for this CTA)
+      if (ok)
+        for (int k = (i > S ? i - S : 0); k < i; ++k)
+          if (!mbar_wait(empty0 + 8 * (k % S), (k / S) & 1)) break;
+    }
+  } else if (warp == W_MMA) {
+    if (lane == 0) {
+      const uint32_t idesc = f16_idesc(128, N);
+      int i = 0, run = 0;
+      bool ok = true;
+      for (int64_t u = u0; u < u1 && ok; ++run) {
+        const int64_t ue = wrun_end(A, u, u1);
+        const int d = run % C::NBUF;
+        if (run >= C::NBUF && !mbar_wait(dfree0 + 8 * d, ((run / C::NBUF) - 1) & 1)) break;
+        tc_fence_after();
+        const uint32_t dcol = tbase + d * 256;
+        for (int64_t v = u; v < ue; ++v, ++i) {
+          const int s = i % S;
+          if (!mbar_wait(full0 + 8 * s, (i / S) & 1)) {
+            ok = false;
+            break;
+          }
+          const uint32_t st = smem_u32(sm + s * stage);
+          if (KIND == W_KIND_F16) {
+            tc_fence_after();
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks)
+              mma_ss(dcol, sw128_desc(st + b_bytes + ks * 32), sw128_desc(st + ks * 32), idesc, (v > u || ks > 0));
+          } else {
+            const int a = i % C::SA;
+            if (!mbar_wait(afull0 + 8 * a, (i / C::SA) & 1)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t ah = tbase + C::A_COL + a * 64, al = ah + 32;
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks) {
+              const uint64_t bh = sw128_desc(st + ks * 32), bl = sw128_desc(st + N * 128 + ks * 32);
+              mma_ts(dcol, ah + ks * 8, bh, idesc, (v > u || ks > 0));
+              mma_ts(dcol, ah + ks * 8, bl, idesc, 1);
+              mma_ts(dcol, al + ks * 8, bh, idesc, 1);
+            }
+            mma_commit(afree0 + 8 * a);
+          }
+          if (CL > 1) mma_commit_mc(empty0 + 8 * s, everyone);
+          else mma_commit(empty0 + 8 * s);
+        }
+        mma_commit(dfull0 + 8 * d);
+        u = ue;
+      }
+    }
+  } else if (warp < 4) {
+    const int r = warp * 32 + lane;
+    const uint32_t lrow = (uint32_t)(warp * 32) << 16;
+    int i = 0, run = 0;
+    bool ok = true;
+    for (int64_t u = u0; u < u1 && ok; ++run) {
+      const int64_t ue = wrun_end(A, u, u1);
+      const WUnit w0 = wunit<CL>(A, u, rank);
+      const WideJob J = wjob(A, wjob_of(A, w0.mt));
+      const int m = w0.mt - J.tile0;
+      // four-bit: the row's power-of-two scaling for this run
+      float unscale = 1.f;
+      if (KIND == W_KIND_I4) {
+        const uint16_t *sc = (const uint16_t *)J.s + ((int64_t)m * A.KT) * DU * 128 + r;
+        float smax = 0.f;
+        for (int kt = w0.kt; kt < w0.kt + (int)(ue - u); ++kt)
+#pragma unroll
+          for (int du = 0; du < DU; ++du)
+            smax = fmaxf(smax, fabsf(__half2float(__ushort_as_half(sc[((int64_t)kt * DU + du) * 128]))));
+        int p = 0;
+        if (smax > 0.f) {
+          int e;
+          frexpf(smax, &e);          // smax in [2^(e-1), 2^e)
+          p = max(-100, min(100, 12 - e));  // smax * 2^p < 2^12: |q| * s * 2^p < 2^15
+        }
+        unscale = ldexpf(1.f, -p);
+        for (int64_t v = u; v < ue && ok; ++v, ++i) {
+          const int s = i % S, a = i % C::SA;
+          if (!__all_sync(0xffffffffu, mbar_wait(full0 + 8 * s, (i / S) & 1))) {
+            ok = false;
+            break;
+          }
+          if (i >= C::SA && !__all_sync(0xffffffffu, mbar_wait(afree0 + 8 * a, ((i / C::SA) - 1) & 1))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint8_t *st = sm + s * stage;
+          const uint4 c0 = *(const uint4 *)(st + b_bytes + r * 16);
+          const uint4 c1 = *(const uint4 *)(st + b_bytes + 2048 + r * 16);
+          __half2 s2[DU];
+#pragma unroll
+          for (int du = 0; du < DU; ++du) {
+            const float sv = __half2float(__ushort_as_half(*(const uint16_t *)(st + b_bytes + 4096 + du * 256 + r * 2)));
+            s2[du] = __float2half2_rn(ldexpf(sv, p));
+          }
+          mbar_arrive(empty0 + 8 * s);
+          const uint32_t words[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+          uint32_t vh[32], vl[32];
+#pragma unroll
+          for (int jw = 0; jw < 8; ++jw) {
+            uint32_t q4[4];
+            dequant8(words[jw], q4);
+            const __half2 sc2 = s2[DU == 2 ? jw / 4 : 0];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const __half2 qv = *(const __half2 *)&q4[e];
+              const __half2 h = __hmul2(qv, sc2);
+              const __half2 l = __hfma2(qv, sc2, __hneg2(h));
+              vh[4 * jw + e] = *(const uint32_t *)&h;
+              vl[4 * jw + e] = *(const uint32_t *)&l;
+            }
+          }
+          tmem_st32(tbase + lrow + C::A_COL + a * 64, vh);
+          tmem_st32(tbase + lrow + C::A_COL + a * 64 + 32, vl);
+          tc_wait_st();
+          tc_fence_before();
+          mbar_arrive(afull0 + 8 * a);
+        }
+        if (!ok) break;
+      }
+      // the run's partial sums into Y
+      const int d = run % C::NBUF;
+      if (!__all_sync(0xffffffffu, mbar_wait(dfull0 + 8 * d, (run / C::NBUF) & 1))) break;
+      tc_fence_after();
+      const int row = m * 128 + r;
+      const bool live = !w0.ghost && row < J.n;
+      float *y = J.y + A.y_off + row;
+      const int tok0 = w0.tt * N;
+      for (int c0 = 0; c0 < N; c0 += 16) {
+        uint32_t v16[16];
+        tmem_ld16(tbase + lrow + d * 256 + c0, v16);
+        tc_wait_ld();
+        if (live) {
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const int tok = tok0 + c0 + e;
+            if (tok < A.T) atomicAdd(y + (int64_t)tok * J.ldy, __uint_as_float(v16[e]) * unscale);
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(dfree0 + 8 * d);
+      u = ue;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tbase, 512);
+  }
+  if (CL > 1) cluster_sync();  // no CTA leaves while its peers may still reach its shared memory
+}
+
+// ---------------------------------------------------------------- launch
+
+// Token tiles of a wide GEMM: as few as fit 256 rows, of equal height (a multiple of 16).
+void wide_tiles(int T, int &ntt, int &N) {
+  ntt = (T + WIDE_MAX_N - 1) / WIDE_MAX_N;
+  const int per = (T + ntt - 1) / ntt;
+  N = (per + 15) / 16 * 16;
+}
+
+size_t wide_act_bytes(int T, int K, bool int4) {
+  int ntt, N;
+  wide_tiles(T, ntt, N);
+  return (size_t)ntt * N * K * 2 * (int4 ? 2 : 1);
+}
+
+// CTAs sharing each token tile (multicast); 1 = no cluster.
+#ifndef W_CLUSTER
+#define W_CLUSTER 2
+#endif
+
+// Runs of at least this many units: a run ends with a read-back of its accumulator.
+constexpr int W_MIN_RUN = 4;
+
+template <int KIND, int DU, int CL>
+static cudaError_t launch_wide(WideArgs &A, int num_sms, cudaStream_t st) {
+  using C = WCfg<KIND, DU>;
+  static int max_clusters = 0;
+  auto kern = k_wide<KIND, DU, CL>;
+  if (max_clusters == 0) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (e != cudaSuccess) return e;
+    if (CL > 1) {
+      e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 0);
+      cudaLaunchConfig_t cfg = {};
+      cudaLaunchAttribute at[1];
+      at[0].id = cudaLaunchAttributeClusterDimension;
+      at[0].val.clusterDim.x = CL;
+      at[0].val.clusterDim.y = 1;
+      at[0].val.clusterDim.z = 1;
+      cfg.gridDim = dim3(CL * num_sms);
+      cfg.blockDim = dim3(W_THREADS);
+      cfg.dynamicSmemBytes = C::SMEM;
+      cfg.attrs = at;
+      cfg.numAttrs = 1;
+      int n = 0;
+      e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
+      if (e != cudaSuccess) return e;
+      max_clusters = std::max(1, n);
+    } else {
+      max_clusters = num_sms;
+    }
+  }
+  const int groups = (A.mtiles + CL - 1) / CL;
+  A.units = (int64_t)A.ntt * groups * A.KT;
+  const int64_t clusters = std::max<int64_t>(1, std::min<int64_t>(max_clusters, A.units / W_MIN_RUN));
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = CL;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  cfg.gridDim = dim3((unsigned)(clusters * CL));
+  cfg.blockDim = dim3(W_THREADS);
+  cfg.dynamicSmemBytes = C::SMEM;
+  cfg.stream = st;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, A);
+  count_launch(1);
+  return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+// Pack X into token tiles of N rows (f16 planes, 128-byte swizzled k-tiles).
+cudaError_t wide_pack(const float *X, int ldx, int T, int K, bool int4, void *act, cudaStream_t st) {
+  int ntt, N;
+  wide_tiles(T, ntt, N);
+  return pack_act(X, ldx, T, K, N, int4 ? 2 : 1, act, st);
+}
+
+cudaError_t wide_gemm(const WideJob *jobs, int njobs, int64_t y_off, bool int4, int group, const void *act, int T,
+                      int K, int num_sms, cudaStream_t st) {
+  if (njobs < 1 || njobs > WIDE_MAX_JOBS || T < 1 || K % 64) return cudaErrorInvalidValue;
+  WideArgs A{};
+  A.njobs = njobs;
+  A.mtiles = 0;
+  for (int j = 0; j < njobs; ++j) {
+    A.job[j] = jobs[j];
+    A.job[j].tile0 = A.mtiles;
+    A.mtiles += (jobs[j].n + 127) / 128;
+  }
+  A.y_off = y_off;
+  A.bpack = (const uint8_t *)act;
+  A.K = K;
+  A.KT = K / 64;
+  A.T = T;
+  wide_tiles(T, A.ntt, A.N);
+  if (!int4) return launch_wide<W_KIND_F16, 1, W_CLUSTER>(A, num_sms, st);
+  return group >= 64 ? launch_wide<W_KIND_I4, 1, W_CLUSTER>(A, num_sms, st)
+                     : launch_wide<W_KIND_I4, 2, W_CLUSTER>(A, num_sms, st);
+}
+
+// ---------------------------------------------------------------- clearing the outputs
+
+struct ZeroArgs {
+  float *y[WIDE_MAX_JOBS];
+  int ld[WIDE_MAX_JOBS];
+};
+
+// Clear rows [0, T) of output blockIdx.y.
+__global__ void k_wide_zero(ZeroArgs Z, int T) {
+  float *y = Z.y[blockIdx.y];
+  const int64_t n = (int64_t)T * Z.ld[blockIdx.y];
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
+    y[i] = 0.f;
+}
+
+cudaError_t wide_zero(const WideJob *jobs, int njobs, int64_t y_off, int T, cudaStream_t st) {
+  if (njobs < 1 || njobs > WIDE_MAX_JOBS) return cudaErrorInvalidValue;
+  ZeroArgs Z{};
+  int64_t most = 0;
+  for (int j = 0; j < njobs; ++j) {
+    Z.y[j] = jobs[j].y + y_off;
+    Z.ld[j] = jobs[j].ldy;
+    most = std::max<int64_t>(most, (int64_t)T * jobs[j].ldy);
+  }
+  dim3 grid((unsigned)std::min<int64_t>((most + 255) / 256, 64), njobs);
+  k_wide_zero<<<grid, 256, 0, st>>>(Z, T);
+  count_launch(1);
+  return cudaGetLastError();
+}
+
+}  // namespace dfl

@@ -153,5 +153,7 @@ def test_packed_sizes(L):
     assert L.dflash_int4_packed_bytes(32, 128, 48) == 0
     assert L.dflash_f16_packed_bytes(16, 64) == 128 * 64 * 2
     assert L.dflash_gemm_workspace_bytes(4, 1024, 16) == 16 * 1024 * 4
-    assert L.dflash_gemm_workspace_bytes(16, 1024, 200) == 256 * 1024 * 2
+    # more than 32 rows: token tiles of at most 256 rows, equal heights rounded up to 16
+    assert L.dflash_gemm_workspace_bytes(16, 1024, 200) == 208 * 1024 * 2
+    assert L.dflash_gemm_workspace_bytes(4, 1024, 480) == 2 * 240 * 1024 * 2 * 2
     assert L.dflash_gemm_workspace_bytes(5, 1024, 16) == 0

@@ -69,7 +69,10 @@ def _bound(wabs: np.ndarray, x: np.ndarray) -> float:
 
 
 @pytest.mark.parametrize("rows,cols,group,T", [(16, 64, 32, 1), (64, 256, 64, 5), (48, 512, 128, 16),
-                                               (96, 1024, 64, 17), (32, 2048, 64, 40), (2048, 5120, 64, 16)])
+                                               (96, 1024, 64, 17), (32, 2048, 64, 40), (2048, 5120, 64, 16),
+                                               # many tokens: the split-weight kernel, one and two token tiles
+                                               (300, 1024, 64, 256), (130, 512, 32, 100), (256, 768, 64, 480),
+                                               (1024, 5120, 64, 256)])
 def test_gemm_int4_matches_oracle(rows, cols, group, T):
     rng = np.random.default_rng(rows * 7 + T)
     m = _rand_int4(rng, rows, cols, group)
@@ -82,7 +85,8 @@ def test_gemm_int4_matches_oracle(rows, cols, group, T):
     assert err <= 2e-6 * _bound(wabs, x), (err, _bound(wabs, x))
 
 
-@pytest.mark.parametrize("rows,cols,T", [(16, 64, 1), (64, 512, 16), (1280, 5120, 16), (128, 3072, 256), (64, 256, 33)])
+@pytest.mark.parametrize("rows,cols,T", [(16, 64, 1), (64, 512, 16), (1280, 5120, 16), (128, 3072, 256), (64, 256, 33),
+                                         (1024, 3072, 256), (200, 1024, 300), (5120, 2560, 256)])
 def test_gemm_f16_matches_oracle(rows, cols, T):
     rng = np.random.default_rng(rows + cols + T)
     w = (rng.standard_normal((rows, cols)) / np.sqrt(cols)).astype(np.float16)
@@ -244,4 +248,6 @@ def test_full_qwen3_0p6b_workload():
     assert p.check_cache() < 1e-4
     a = di.anchor_token(g, 0)
     r = p.draft([wl.context], [di.block_rows(g, 0, a)], [a])[0]
-    assert r["logit_err"] < 1e-4, r
+    # both sides round the kernel projections' inputs to f16, so a 1e-6 difference in the
+    # cache can flip one of them by an ulp (~5e-4 of that element); the contract is LOGIT_REL
+    assert r["logit_err"] < 5e-4, r
