@@ -97,6 +97,7 @@ std::string check_geometry(const dflash_geometry &g) {
     return "hidden, intermediate and heads*head_dim must be multiples of 64";
   if ((g.kv_heads * g.head_dim) % 16) return "kv_heads*head_dim must be a multiple of 16";
   if (g.vocab < 16 || g.vocab % 16) return "vocab must be a positive multiple of 16";
+  if (g.vocab > (1 << 21)) return "vocab must be at most 2,097,152";
   if ((2 * g.conv_kernel * (g.hidden / g.conv_group)) % 16) return "2*conv_kernel*groups must be a multiple of 16";
   if (g.conv_kernel < 1 || g.conv_kernel > DFLASH_MAX_BLOCK) return "conv_kernel must be 1..16";
   if (g.selector_rank < 16 || g.selector_rank > 256 || g.selector_rank % 16) return "selector_rank must be 16..256, a multiple of 16";

@@ -4,11 +4,18 @@
 // token chosen before: score = logit + (P[prev] * hp) . C[cand], the first
 // strictly greater score winning, the chain starting at the anchor token.
 //
-// Stage 1 (chunks x rows CTAs): each chunk of 2048 logits yields its own top `top`.
-// Stage 2 (one CTA per row): the chunks' candidates merge into the row's top `top`.
-// Stage 3 (one CTA per sequence): the chain. Row j's predecessor is the anchor
-// (j = 0) or one of row j-1's candidates, so every score the chain can ask for is
-// computed first, in parallel; the chain itself then only compares numbers.
+// Stage 1 (chunks x rows CTAs): the largest key (value, then lower index) of
+// each chunk of 2048 logits.
+// Stage 2 (one CTA per row): tau = the top-th largest of the chunk maxima. The
+// top chunk maxima are `top` distinct logits of the row, so the row's top-th
+// largest key is at least tau, and every key >= tau is a candidate: one pass
+// collects them (typically a few dozen) and their ranks give the row's top
+// `top` in order. More than the CTA can hold (many equal logits) falls back to
+// `top` exact passes over the row.
+// Stage 2 also computes every score the chain can ask of the row (row j's
+// predecessors are the anchor for j = 0, else row j-1's candidates, which the
+// CTA finds again). Stage 3 (one CTA per sequence): the chain itself, over the
+// tables copied into shared memory.
 #include <mutex>
 #include <string>
 
@@ -19,9 +26,10 @@
 namespace dfl {
 
 constexpr int SEL_THREADS = 256;
-constexpr int SEL_PER = 8;                         // logits per thread in stage 1
-constexpr int SEL_CHUNK = SEL_THREADS * SEL_PER;   // logits per chunk
-constexpr int MERGE_PER = 16;                      // candidates per thread in stage 2
+constexpr int SEL_CHUNK = 2048;                    // logits per chunk of stage 1
+constexpr int ROW_THREADS = 512;
+constexpr int CAND_CAP = 1024;                     // candidates (and chunk maxima) a row CTA holds
+constexpr int MAX_CHUNKS = CAND_CAP;               // width <= 2 M
 constexpr int TOP_MAX = 32;
 constexpr int RANK_MAX = 256;
 constexpr int CHAIN_THREADS = 512;
@@ -29,170 +37,207 @@ constexpr int KMAX = 15;
 
 static inline int sel_chunks(int width) { return (width + SEL_CHUNK - 1) / SEL_CHUNK; }
 
-// Scratch of one call: per row the chunks' candidates (u64), the row's
-// candidates (u32) and its score table (f32 [top][top]); one counter per row
-// (sequences <= rows).
+// Scratch of one call: per row the chunk maxima (u64), the row's candidates
+// (u32) and its score table (f32 [top][top]).
 size_t select_scratch_bytes(int max_rows, int width, int top) {
-  return (size_t)max_rows * ((size_t)sel_chunks(width) * top * 8 + (size_t)top * 4 + (size_t)top * top * 4 + 4) + 256;
+  return (size_t)max_rows * ((size_t)sel_chunks(width) * 8 + (size_t)top * 4 + (size_t)top * top * 4) + 256;
 }
 
-// The `top` largest keys of a warp (N keys per lane in `keys`), largest first,
-// written by lane 0 to out[0..top). Keys are unique except 0 (= none).
-template <int N>
-__device__ __forceinline__ void warp_top(unsigned long long (&keys)[N], int top, unsigned long long *out) {
-  const int lane = threadIdx.x & 31;
-  for (int t = 0; t < top; ++t) {
-    unsigned long long mine = 0;
-#pragma unroll
-    for (int i = 0; i < N; ++i) mine = keys[i] > mine ? keys[i] : mine;
-    const unsigned long long best = warp_max_u64(mine);
-    if (best != 0ull && mine == best) {
-#pragma unroll
-      for (int i = 0; i < N; ++i)
-        if (keys[i] == best) keys[i] = 0ull;
-    }
-    if (lane == 0) out[t] = best;
-  }
-}
+__device__ __forceinline__ unsigned long long umax64(unsigned long long a, unsigned long long b) { return a > b ? a : b; }
 
-// One CTA per (chunk, row): every warp takes 256 logits and keeps its top; one
-// warp then takes the top of the warps' lists.
-__global__ void __launch_bounds__(SEL_THREADS) k_topk_chunks(const float *__restrict__ logits, int width, int top,
-                                                             unsigned long long *__restrict__ cand) {
-  __shared__ unsigned long long wl[SEL_THREADS / 32][TOP_MAX];
+// Stage 1: one CTA per (chunk, row), eight logits a thread.
+__global__ void __launch_bounds__(SEL_THREADS) k_chunk_max(const float *__restrict__ logits, int width,
+                                                           unsigned long long *__restrict__ cmax) {
+  __shared__ unsigned long long red[SEL_THREADS / 32];
   const int chunk = blockIdx.x, row = blockIdx.y;
-  const int nchunks = gridDim.x;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const float *lr = logits + (int64_t)row * width;
-  unsigned long long keys[SEL_PER];
+  unsigned long long best = 0ull;
 #pragma unroll
-  for (int i = 0; i < SEL_PER; ++i) {
-    const int idx = chunk * SEL_CHUNK + warp * 256 + i * 32 + lane;
-    keys[i] = idx < width ? cand_key(lr[idx], (uint32_t)idx) : 0ull;
+  for (int i = 0; i < SEL_CHUNK / SEL_THREADS; ++i) {
+    const int idx = chunk * SEL_CHUNK + i * SEL_THREADS + threadIdx.x;
+    if (idx < width) best = umax64(best, cand_key(__ldg(lr + idx), (uint32_t)idx));
   }
-  warp_top<SEL_PER>(keys, top, wl[warp]);
+  best = warp_max_u64(best);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = best;
   __syncthreads();
-  if (warp == 0) {
-    constexpr int M = SEL_THREADS / 32 * TOP_MAX / 32;  // keys per lane in the final round
-    unsigned long long k2[M];
-#pragma unroll
-    for (int i = 0; i < M; ++i) {
-      const int idx = i * 32 + lane;  // over [warps][top]
-      const int w = idx / TOP_MAX, t = idx % TOP_MAX;
-      k2[i] = t < top ? wl[w][t] : 0ull;
-    }
-    warp_top<M>(k2, top, cand + ((int64_t)row * nchunks + chunk) * top);
+  if (threadIdx.x < 32) {
+    unsigned long long v = threadIdx.x < SEL_THREADS / 32 ? red[threadIdx.x] : 0ull;
+    v = warp_max_u64(v);
+    if (threadIdx.x == 0) cmax[(int64_t)row * gridDim.x + chunk] = v;
   }
 }
 
-// The row's top `top` from the chunks' lists, largest first, into ctok (smem).
-__device__ void merge_row(const unsigned long long *__restrict__ cr, int ncand, int top, unsigned long long (*wl)[TOP_MAX],
-                          uint32_t *ctok) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  unsigned long long keys[MERGE_PER];
-#pragma unroll
-  for (int i = 0; i < MERGE_PER; ++i) {
-    const int idx = (warp * MERGE_PER + i) * 32 + lane;
-    keys[i] = idx < ncand ? cr[idx] : 0ull;
+// The largest key below `below` in the row (block-wide), for the exact fallback.
+__device__ unsigned long long row_max_below(const float *__restrict__ lr, int width, unsigned long long below,
+                                            unsigned long long *red) {
+  unsigned long long best = 0ull;
+  for (int idx = threadIdx.x; idx < width; idx += ROW_THREADS) {
+    const unsigned long long k = cand_key(lr[idx], (uint32_t)idx);
+    if (k < below) best = umax64(best, k);
   }
-  warp_top<MERGE_PER>(keys, top, wl[warp]);
+  best = warp_max_u64(best);
   __syncthreads();
-  if (warp == 0) {
-    constexpr int M = SEL_THREADS / 32 * TOP_MAX / 32;
-    unsigned long long k2[M];
-#pragma unroll
-    for (int i = 0; i < M; ++i) {
-      const int idx = i * 32 + lane;
-      const int w = idx / TOP_MAX, t = idx % TOP_MAX;
-      k2[i] = t < top ? wl[w][t] : 0ull;
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = best;
+  __syncthreads();
+  unsigned long long v = 0ull;
+  for (int w = 0; w < ROW_THREADS / 32; ++w) v = umax64(v, red[w]);
+  return v;
+}
+
+// The row's top `top` keys' indices, in order, into out (shared memory):
+// candidates >= tau (the top-th largest chunk maximum) ranked among themselves.
+__device__ void row_top(const float *__restrict__ lr, int width, int top, int nchunks,
+                        const unsigned long long *__restrict__ cm, unsigned long long *keys, unsigned long long *red,
+                        uint32_t *out) {
+  __shared__ unsigned long long tau;
+  __shared__ int cnt;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    tau = 0ull;  // fewer chunks than `top`: every logit is a candidate
+    cnt = 0;
+  }
+  for (int i = threadIdx.x; i < nchunks; i += ROW_THREADS) keys[i] = cm[i];
+  __syncthreads();
+  if (nchunks >= top) {
+    for (int i = threadIdx.x; i < nchunks; i += ROW_THREADS) {
+      const unsigned long long k = keys[i];
+      int above = 0;
+      for (int m = 0; m < nchunks; ++m) above += keys[m] > k;
+      if (above == top - 1) tau = k;  // keys are unique: exactly one thread
     }
-    __shared__ unsigned long long fin[TOP_MAX];
-    warp_top<M>(k2, top, fin);
-    __syncwarp();
-    for (int t = lane; t < top; t += 32) ctok[t] = cand_index(fin[t]);
+  }
+  __syncthreads();
+  const unsigned long long t = tau;
+  const int n4 = (width & 3) == 0 ? width / 4 : 0;
+  for (int i = threadIdx.x; i < n4; i += ROW_THREADS) {
+    const float4 v = __ldg((const float4 *)lr + i);
+    const float vv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const unsigned long long k = cand_key(vv[e], (uint32_t)(4 * i + e));
+      if (k >= t) {
+        const int at = atomicAdd(&cnt, 1);
+        if (at < CAND_CAP) keys[at] = k;
+      }
+    }
+  }
+  for (int idx = 4 * n4 + threadIdx.x; idx < width; idx += ROW_THREADS) {
+    const unsigned long long k = cand_key(lr[idx], (uint32_t)idx);
+    if (k >= t) {
+      const int at = atomicAdd(&cnt, 1);
+      if (at < CAND_CAP) keys[at] = k;
+    }
+  }
+  __syncthreads();
+  const int n = cnt;
+  if (n <= CAND_CAP) {
+    for (int i = threadIdx.x; i < n; i += ROW_THREADS) {
+      const unsigned long long k = keys[i];
+      int above = 0;
+      for (int m = 0; m < n; ++m) above += keys[m] > k;
+      if (above < top) out[above] = cand_index(k);
+    }
+  } else {
+    // many equal logits: `top` exact passes, each the largest key below the last
+    unsigned long long below = ~0ull;
+    for (int r = 0; r < top; ++r) {
+      below = row_max_below(lr, width, below, red);
+      if (threadIdx.x == 0) out[r] = cand_index(below);
+    }
   }
   __syncthreads();
 }
 
-// One CTA per (sequence, row j): row j's candidates, the predecessors it can
-// have (the anchor for row 0, else row j-1's candidates, merged again here),
-// and every score[p][c] = logit[c] + sum_i (P[prev_p][i] * hp[i]) * C[cand_c][i].
-// The CTA that finishes a sequence last runs its chain: the first strictly
-// greater score in candidate order wins, its token is the next predecessor.
-__global__ void __launch_bounds__(SEL_THREADS) k_row_scores(
+// Stage 2: one CTA per row j of a sequence: its candidates, its possible
+// predecessors (the anchor, or row j-1's candidates, found again here) and the
+// score table score[p][c] = logit[cand_c] + sum_i (P[prev_p][i] * hp[i]) * C[cand_c][i].
+__global__ void __launch_bounds__(ROW_THREADS) k_row_select(
     const float *__restrict__ logits, const float *__restrict__ hp, const uint32_t *__restrict__ anchor_tok,
     const uint16_t *__restrict__ pred, const uint16_t *__restrict__ succ, int k, int width, int rank, int top,
-    int vocab, int nchunks, const unsigned long long *__restrict__ cand, uint32_t *__restrict__ ctok_g,
-    float *__restrict__ score_g, unsigned int *__restrict__ done, uint32_t *__restrict__ chosen,
-    uint32_t *__restrict__ plain) {
-  __shared__ unsigned long long wl[SEL_THREADS / 32][TOP_MAX];
+    int vocab, int nchunks, const unsigned long long *__restrict__ cmax, uint32_t *__restrict__ ctok,
+    float *__restrict__ score) {
+  __shared__ unsigned long long keys[CAND_CAP];
+  __shared__ unsigned long long red[ROW_THREADS / 32];
   __shared__ uint32_t cur[TOP_MAX], prv[TOP_MAX];
-  __shared__ float clog[TOP_MAX];
   __shared__ __align__(16) uint16_t Ps[TOP_MAX * RANK_MAX];
   __shared__ __align__(16) uint16_t Cs[TOP_MAX * RANK_MAX];
   __shared__ float hs[RANK_MAX];
-  __shared__ bool last;
+  __shared__ float clog[TOP_MAX];
   const int row = blockIdx.x, b = row / k, j = row % k;
   const uint32_t anchor = anchor_tok[b];
-  const bool bad = anchor >= (uint32_t)vocab;
-  const int ncand = nchunks * top;
-  if (!bad) {
-    merge_row(cand + (int64_t)row * ncand, ncand, top, wl, cur);
-    if (j > 0) merge_row(cand + (int64_t)(row - 1) * ncand, ncand, top, wl, prv);
-    const int np = j > 0 ? top : 1;
-    if (j == 0 && threadIdx.x == 0) prv[0] = anchor;
-    __syncthreads();
-    const int r2 = rank / 2;
-    for (int i = threadIdx.x; i < top * r2; i += SEL_THREADS) {
-      const int c = i / r2, e = i % r2;
-      ((uint32_t *)Cs)[c * r2 + e] = ((const uint32_t *)(succ + (int64_t)cur[c] * rank))[e];
-      if (c < np) ((uint32_t *)Ps)[c * r2 + e] = ((const uint32_t *)(pred + (int64_t)prv[c] * rank))[e];
-    }
-    for (int i = threadIdx.x; i < rank; i += SEL_THREADS) hs[i] = hp[(int64_t)row * rank + i];
-    for (int c = threadIdx.x; c < top; c += SEL_THREADS) clog[c] = logits[(int64_t)row * width + cur[c]];
-    __syncthreads();
-    for (int it = threadIdx.x; it < np * top; it += SEL_THREADS) {
-      const int p = it / top, c = it % top;
-      const __half2 *pr = (const __half2 *)(Ps + p * rank);
-      const __half2 *cr = (const __half2 *)(Cs + c * rank);
-      float acc = 0.f;
-      for (int e = 0; e < r2; ++e) {
-        const float2 pv = __half22float2(pr[e]);
-        const float2 cv = __half22float2(cr[e]);
-        acc = fmaf(pv.x * hs[2 * e], cv.x, acc);
-        acc = fmaf(pv.y * hs[2 * e + 1], cv.y, acc);
-      }
-      score_g[((int64_t)row * top + p) * top + c] = clog[c] + acc;
-    }
-    for (int c = threadIdx.x; c < top; c += SEL_THREADS) ctok_g[(int64_t)row * top + c] = cur[c];
+  if (anchor >= (uint32_t)vocab) return;  // the chain reports it
+  row_top(logits + (int64_t)row * width, width, top, nchunks, cmax + (int64_t)row * nchunks, keys, red, cur);
+  if (j > 0)
+    row_top(logits + (int64_t)(row - 1) * width, width, top, nchunks, cmax + (int64_t)(row - 1) * nchunks, keys, red,
+            prv);
+  else if (threadIdx.x == 0)
+    prv[0] = anchor;
+  __syncthreads();
+  const int np = j > 0 ? top : 1;
+  const int r2 = rank / 2;
+  for (int i = threadIdx.x; i < top * r2; i += ROW_THREADS) {
+    const int c = i / r2, e = i % r2;
+    ((uint32_t *)Cs)[c * r2 + e] = __ldg((const uint32_t *)(succ + (int64_t)cur[c] * rank) + e);
+    if (c < np) ((uint32_t *)Ps)[c * r2 + e] = __ldg((const uint32_t *)(pred + (int64_t)prv[c] * rank) + e);
   }
-  __threadfence();
+  for (int i = threadIdx.x; i < rank; i += ROW_THREADS) hs[i] = hp[(int64_t)row * rank + i];
+  for (int c = threadIdx.x; c < top; c += ROW_THREADS) {
+    clog[c] = logits[(int64_t)row * width + cur[c]];
+    ctok[(int64_t)row * top + c] = cur[c];
+  }
   __syncthreads();
-  if (threadIdx.x == 0) last = atomicAdd(done + b, 1u) == (unsigned)(k - 1);
-  __syncthreads();
-  if (!last || threadIdx.x != 0) return;
-  __threadfence();
-  done[b] = 0;  // ready for the next call
-  if (bad) {
-    for (int jj = 0; jj < k; ++jj) chosen[b * k + jj] = plain[b * k + jj] = 0xFFFFFFFFu;
+  for (int it = threadIdx.x; it < np * top; it += ROW_THREADS) {
+    const int p = it / top, c = it % top;
+    const __half2 *pr = (const __half2 *)(Ps + p * rank);
+    const __half2 *cr = (const __half2 *)(Cs + c * rank);
+    float acc = 0.f;
+    for (int e = 0; e < r2; ++e) {
+      const float2 pv = __half22float2(pr[e]);
+      const float2 cv = __half22float2(cr[e]);
+      acc = fmaf(pv.x * hs[2 * e], cv.x, acc);
+      acc = fmaf(pv.y * hs[2 * e + 1], cv.y, acc);
+    }
+    score[((int64_t)row * top + p) * top + c] = clog[c] + acc;
+  }
+}
+
+// Stage 3: one CTA per sequence runs the chain over the rows' tables: the first
+// strictly greater score in candidate order wins and is the next predecessor.
+__global__ void __launch_bounds__(CHAIN_THREADS) k_chain(const uint32_t *__restrict__ anchor_tok, int k, int top,
+                                                         int vocab, const uint32_t *__restrict__ ctok,
+                                                         const float *__restrict__ score, uint32_t *__restrict__ chosen,
+                                                         uint32_t *__restrict__ plain) {
+  extern __shared__ __align__(16) uint8_t chain_sm[];
+  float *sc = (float *)chain_sm;                    // [k][top][top]
+  uint32_t *cand = (uint32_t *)(sc + k * top * top);  // [k][top]
+  const int b = blockIdx.x;
+  if (anchor_tok[b] >= (uint32_t)vocab) {
+    for (int j = threadIdx.x; j < k; j += CHAIN_THREADS) chosen[b * k + j] = plain[b * k + j] = 0xFFFFFFFFu;
     return;
   }
-  int slot = 0;  // the predecessor's slot among the previous row's candidates
-  for (int jj = 0; jj < k; ++jj) {
-    const int rr = b * k + jj;
-    const float *sr = score_g + ((int64_t)rr * top + slot) * top;
-    float bs = -INFINITY;
-    int bc = 0;
-    for (int c = 0; c < top; ++c) {
-      const float sc = __ldcg(sr + c);
-      if (sc > bs) {
-        bs = sc;
-        bc = c;
-      }
+  const float *sg = score + (int64_t)b * k * top * top;
+  for (int i = threadIdx.x; i < k * top * top; i += CHAIN_THREADS) {
+    const int j = i / (top * top);
+    const int p = (i / top) % top;
+    if (j > 0 || p == 0) sc[i] = sg[i];  // row 0 has one predecessor, the anchor
+  }
+  for (int i = threadIdx.x; i < k * top; i += CHAIN_THREADS) cand[i] = ctok[(int64_t)b * k * top + i];
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int slot = 0;  // the predecessor's place among the previous row's candidates
+    for (int j = 0; j < k; ++j) {
+      const float *r = sc + (j * top + slot) * top;
+      float bs = -INFINITY;
+      int bc = 0;
+      for (int c = 0; c < top; ++c)
+        if (r[c] > bs) {
+          bs = r[c];
+          bc = c;
+        }
+      chosen[b * k + j] = cand[j * top + bc];
+      plain[b * k + j] = cand[j * top];
+      slot = bc;
     }
-    chosen[rr] = __ldcg(ctok_g + (int64_t)rr * top + bc);
-    plain[rr] = __ldcg(ctok_g + (int64_t)rr * top);
-    slot = bc;
   }
 }
 
@@ -201,19 +246,24 @@ cudaError_t select_tokens(const float *logits, const float *hp, const uint32_t *
                           uint32_t *chosen, uint32_t *plain, cudaStream_t st) {
   if (top > TOP_MAX || rank > RANK_MAX || top < 1 || k > KMAX || rank % 2) return cudaErrorInvalidValue;
   const int nchunks = sel_chunks(width);
-  if (nchunks * top > MERGE_PER * SEL_THREADS) return cudaErrorInvalidValue;
+  if (nchunks > MAX_CHUNKS) return cudaErrorInvalidValue;
   const int rows = batch * k;
-  unsigned long long *cand = (unsigned long long *)scratch;
-  uint32_t *ctok = (uint32_t *)(cand + (size_t)rows * nchunks * top);
+  unsigned long long *cmax = (unsigned long long *)scratch;
+  uint32_t *ctok = (uint32_t *)(cmax + (size_t)rows * nchunks);
   float *score = (float *)(ctok + (size_t)rows * top);
-  unsigned int *done = (unsigned int *)(score + (size_t)rows * top * top);
-  cudaError_t e = cudaMemsetAsync(done, 0, (size_t)batch * sizeof(unsigned int), st);
-  if (e != cudaSuccess) return e;
-  dim3 g1(nchunks, rows);
-  k_topk_chunks<<<g1, SEL_THREADS, 0, st>>>(logits, width, top, cand);
-  k_row_scores<<<rows, SEL_THREADS, 0, st>>>(logits, hp, anchor_tok, pred, succ, k, width, rank, top, vocab, nchunks,
-                                             cand, ctok, score, done, chosen, plain);
-  count_launch(2);
+  static bool configured = false;
+  const size_t smem = (size_t)k * top * top * 4 + (size_t)k * top * 4;
+  if (!configured) {
+    const size_t most = (size_t)KMAX * TOP_MAX * TOP_MAX * 4 + (size_t)KMAX * TOP_MAX * 4;
+    cudaError_t e = cudaFuncSetAttribute(k_chain, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)most);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  k_chunk_max<<<dim3(nchunks, rows), SEL_THREADS, 0, st>>>(logits, width, cmax);
+  k_row_select<<<rows, ROW_THREADS, 0, st>>>(logits, hp, anchor_tok, pred, succ, k, width, rank, top, vocab, nchunks,
+                                             cmax, ctok, score);
+  k_chain<<<batch, CHAIN_THREADS, smem, st>>>(anchor_tok, k, top, vocab, ctok, score, chosen, plain);
+  count_launch(3);
   return cudaGetLastError();
 }
 
@@ -234,7 +284,7 @@ cudaError_t select_tokens(const float *logits, const float *hp, const uint32_t *
 namespace dfl {
 namespace {
 
-constexpr size_t kStaticSelectScratch = 8u << 20;  // bytes: 32 sequences x 15 rows at a 151,936 vocabulary
+constexpr size_t kStaticSelectScratch = 8u << 20;  // bytes: 1,688 a row at a 151,936 vocabulary and top 16
 static __device__ __align__(256) unsigned char g_select_scratch[kStaticSelectScratch];
 
 // Host code cannot use g_select_scratch as a device address (in host code the
@@ -273,8 +323,7 @@ extern "C" int dflash_select_static(const float *logits, const float *hp, const 
       rank < 16 || rank > RANK_MAX || rank % 16)
     return dflash_fail(DFLASH_E_ARG, "select_static: batch >= 1, 1 <= k <= 15, 1 <= top <= 32, "
                                      "top <= width <= vocab, rank a multiple of 16 in 16..256");
-  if (sel_chunks(width) * top > MERGE_PER * SEL_THREADS)
-    return dflash_fail(DFLASH_E_ARG, "select_static: width / top beyond the selector's merge");
+  if (sel_chunks(width) > MAX_CHUNKS) return dflash_fail(DFLASH_E_ARG, "select_static: width beyond 2 M");
   const size_t need = select_scratch_bytes(batch * k, width, top);
   if (need > kStaticSelectScratch)
     return dflash_fail(DFLASH_E_CAPACITY, "select_static: the call's candidates and score tables exceed the fixed "

@@ -181,15 +181,19 @@ def test_block_tiny_matches_oracle():
     assert r["logit_err"] < 1e-4 and r["hp_err"] < 5e-4
 
 
-def test_select_alone_on_identical_inputs():
-    """The selector on the oracle's own logits and hp (f32): isolates it from the block."""
-    g = _tiny()
+@pytest.mark.parametrize("vocab", [4096, 151936])
+def test_select_alone_on_identical_inputs(vocab):
+    """The selector on the oracle's own logits and hp (f32): isolates it from the block.
+    Rows of equal logits take the exact fallback (more candidates than a CTA holds)."""
+    g = _tiny(vocab=vocab)
     rng = np.random.default_rng(3)
     w = di.make_weights(g, 0)
     d = _drafter().Drafter(g, w, max_batch=2, ctx_cap=64)
     k, width = g.block - 1, g.vocab
     logits = rng.standard_normal((2, k, width)).astype(np.float32)
     logits[0, 3, 10] = logits[0, 3, 20] = 9.0         # an exact tie: the lower index comes first
+    logits[1, 5, :] = 0.5                              # a row of equal logits
+    logits[0, 7, 100:3100] = 20.0                      # 3000 equal maxima
     hp = rng.standard_normal((2, k, g.selector_rank)).astype(np.float32)
     anchors = [5, 4000]
     ch, pl = d.select(torch.from_numpy(logits).cuda(), torch.from_numpy(hp).cuda(),
@@ -200,7 +204,8 @@ def test_select_alone_on_identical_inputs():
         assert list(pl[b]) == opl
         check_tokens(ch[b], pl[b], hp[b].astype(np.float64), logits[b].astype(np.float64), anchors[b],
                      w["pred_book"], w["succ_book"], g.selector_top)
-    assert pl[0, 3] == 10
+    assert pl[0, 3] == 10 and pl[1, 5] == 0 and pl[0, 7] == 100
+    d.close()
 
 
 @pytest.mark.parametrize("case", ["empty_context", "windowed", "short_k_shortlist", "no_rope_first_1000",

@@ -62,6 +62,6 @@ def test_select_static_equals_select_on_consecutive_calls(vocab, rank, top, batc
 def test_select_static_rejects_what_does_not_fit():
     from speculative_block_drafter_gb300 import _lib as L
     with pytest.raises(L.DflashError) as e:
-        # 64 sequences x 15 rows at a 151,936 vocabulary need more than the fixed scratch
-        L.dflash_select_static(16, 16, 16, 16, 16, 64, 15, 151936, 151936, 64, 16, 16, 16, None)
+        # 1024 sequences x 15 rows at a 151,936 vocabulary need more than the fixed scratch
+        L.dflash_select_static(16, 16, 16, 16, 16, 1024, 15, 151936, 151936, 64, 16, 16, 16, None)
     assert e.value.code == 3 and "8 MiB" in str(e.value)
