@@ -35,7 +35,7 @@ L2_FLUSH_BYTES = 256 << 20
 REJECT = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown")
 
 
-def parse():
+def parse(argv=None):
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
     p.add_argument("--steps", type=int, default=100)
@@ -44,7 +44,7 @@ def parse():
     p.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     p.add_argument("--no-graph", action="store_true", help="direct calls instead of a CUDA graph replay")
     p.add_argument("--no-cpu-baseline", action="store_true")
-    return p.parse_args()
+    return p.parse_args(argv)
 
 
 def peaks():
@@ -111,6 +111,23 @@ class Clocks:
         loaded = [s for s, p in zip(sm, power) if p > 0.3 * max(power)] if power else []
         return {"sm_mhz": float(np.median(loaded or sm)) if sm else None,
                 "sm_max_mhz": max(smax) if smax else None, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def max_over_ranks(x: float, device=None) -> float:
+    """The largest `x` over the ranks of the default process group (x itself alone)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_rank: int, world: int, seconds_max: float) -> float:
+    """Units all ranks processed over the slowest rank's time (weak scaling: each rank
+    runs its own replica of the workload)."""
+    return units_per_rank * world / seconds_max
 
 
 def head_traffic(workload: str):
@@ -368,22 +385,13 @@ def run_gb300(args):
     if any(r in clocks["reasons"] for r in REJECT):
         ms, clocks = measure()
         clocks["remeasured"] = True
-    step_ms = float(np.mean(ms))
-    if world > 1:
-        t = torch.tensor([step_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        step_ms = float(t.item())
-    units = wl.batch * world
-    value = units / (step_ms * 1e-3)
+    step_ms = max_over_ranks(float(np.mean(ms)), dev)
+    value = whole_job_rate(wl.batch, world, step_ms * 1e-3)
     roof = b.roofline(max(5, min(args.steps, 50)), hbm_peak)
     roof["peak_kind"] = f"{peak_kind} (HBM copy, MEASURED_PEAKS.json)" if peak_kind == "measured" else "fallback"
     phases = b.phases(max(5, min(args.steps, 50)))
     e2e_s, h2d, d2h = b.e2e(max(3, min(args.steps, 30)))
-    e2e_value = units / e2e_s
-    if world > 1:
-        t = torch.tensor([e2e_s], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_value = units / float(t.item())
+    e2e_value = whole_job_rate(wl.batch, world, max_over_ranks(e2e_s, dev))
     out = {
         "metric": METRIC, "value": round(value, 2), "unit": "blocks/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(step_ms, 5), "higher_is_better": True, "scaling": "weak",
