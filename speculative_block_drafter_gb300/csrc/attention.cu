@@ -84,6 +84,7 @@ __global__ void __launch_bounds__(ATT_THREADS) k_attn(const float *__restrict__ 
                                                       const float *__restrict__ v, AttnArgs args, int heads, int kv,
                                                       int R, int window, float scale, int nsplit, int cps,
                                                       float *__restrict__ part) {
+  pdl_wait();
   using SM = AttnSmem<HD>;
   constexpr int KW = CH / KG;      // keys per warp per chunk
   constexpr int NT = KW / 8;       // n8 tiles of scores
@@ -295,6 +296,7 @@ __global__ void __launch_bounds__(ATT_THREADS) k_attn(const float *__restrict__ 
 template <int HD>
 __global__ void k_attn_merge(const float *__restrict__ part, int heads, int kv, int R, int nsplit,
                              float *__restrict__ y) {
+  pdl_wait();
   const int qi_all = blockIdx.x;  // over kv * Q
   const int b = blockIdx.y;
   const int rep = heads / kv, Q = rep * R;
@@ -330,12 +332,12 @@ static cudaError_t launch_attn(const float *q, const float *k, const float *v, c
   const int cps = chunks_per_split(batch, kv, max_n);
   const int ns = max_n > 0 ? ((max_n + CH - 1) / CH + cps - 1) / cps : 0;
   dim3 grid(ns + 1, kv, batch);
-  k_attn<HD, KG><<<grid, ATT_THREADS, smem, st>>>(q, k, v, args, heads, kv, R, window, scale, ns, cps, part);
+  cudaError_t e = launch_pdl(k_attn<HD, KG>, grid, dim3(ATT_THREADS), smem, st, 1, q, k, v, args, heads, kv, R, window,
+                             scale, ns, cps, part);
+  if (e != cudaSuccess) return e;
   const int Q = heads / kv * R;
   dim3 g2(kv * Q, batch);
-  k_attn_merge<HD><<<g2, HD, 0, st>>>(part, heads, kv, R, ns, y);
-  count_launch(2);
-  return cudaGetLastError();
+  return launch_pdl(k_attn_merge<HD>, g2, dim3(HD), 0, st, 1, part, heads, kv, R, ns, y);
 }
 
 template <int HD>

@@ -22,6 +22,21 @@ namespace dfl {
 constexpr int TILE_ROWS = 16;
 constexpr int TILE_COLS = 64;
 
+// ---------------------------------------------------------------- programmatic dependent launch
+// Every kernel of the pass is launched so that it may start while the kernel
+// before it in the stream finishes (launch_pdl). Such a kernel calls pdl_wait()
+// before it touches any buffer an earlier kernel reads or writes (weights are
+// never written during a pass and may be read before), in every thread and
+// before any early return, so that the chain of waits orders the whole stream.
+// pdl_trigger() lets the next kernel start before this one ends. Only the
+// kernels that pack a GEMM's token tiles call it early (the GEMM then fetches
+// its first weight tiles meanwhile); the GEMMs call it when their own work is
+// done; the others not at all (the next kernel starts as they exit). A kernel
+// started early shares the SMs with the one still running: a few heavy CTAs
+// would be packed onto the SMs that happen to be free.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ---------------------------------------------------------------- small math
 __device__ __forceinline__ uint32_t lop3_and_or(uint32_t a, uint32_t b, uint32_t c) {
   uint32_t r;

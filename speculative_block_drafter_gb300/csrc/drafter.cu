@@ -348,9 +348,7 @@ int dflash_settle(dflash_t *d, int32_t seq, int64_t pos, const float *taps, int3
     kv[2 * l] = dfl::WideJob{L.k.data, L.k.scales, kc[l], kvd, kvd, 0};
     kv[2 * l + 1] = dfl::WideJob{L.v.data, L.v.scales, d->cv[(size_t)seq * g.layers + l] + at * kvd, kvd, kvd, 0};
   }
-  DF_CUDA(dfl::wide_zero(kv, 2 * g.layers, 0, n, st));
-  DF_CUDA(dfl::wide_pack(d->x, hs, n, hs, true, d->act, st));
-  DF_CUDA(dfl::wide_gemm(kv, 2 * g.layers, 0, true, g.quant_group, d->act, n, hs, d->num_sms, st));
+  DF_CUDA(dfl::wide_gemm(kv, 2 * g.layers, 0, true, g.quant_group, d->x, hs, n, hs, d->act, d->num_sms, st));
   // k = rot(rms_head(k, k_norm)) at positions pos..pos+n-1 (rotary layers)
   DF_CUDA(dfl::ctx_norm_rope(kc, kn, rot, g.layers, n, g.kv_heads, g.head_dim, (float)g.eps, d->inv.data(), pos, st));
   s.len = at + n;

@@ -5,6 +5,7 @@
 
 #include <atomic>
 #include <string>
+#include <utility>
 
 namespace dfl {
 
@@ -13,6 +14,36 @@ extern std::atomic<unsigned long long> g_launches;
 inline void count_launch(int n = 1) { g_launches.fetch_add((unsigned long long)n, std::memory_order_relaxed); }
 // Set the calling thread's dflash_last_error() message; returns `code`.
 int dflash_fail(int code, const std::string &msg);
+
+// Launch `kern` so that it may start while the previous kernel of the stream
+// finishes (programmatic dependent launch); the kernel orders itself with
+// pdl_wait() (common.cuh). cluster > 1 launches thread-block clusters of that
+// many CTAs along x.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st, int cluster,
+                       Args &&...args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute at[2];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  int n = 1;
+  if (cluster > 1) {
+    at[1].id = cudaLaunchAttributeClusterDimension;
+    at[1].val.clusterDim.x = (unsigned)cluster;
+    at[1].val.clusterDim.y = 1;
+    at[1].val.clusterDim.z = 1;
+    n = 2;
+  }
+  cfg.attrs = at;
+  cfg.numAttrs = n;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+  count_launch(1);
+  return e != cudaSuccess ? e : cudaGetLastError();
+}
 
 // -------------------------------------------------------------- tensor-core GEMMs (tc_gemm.cu)
 // Packed layouts: four-bit codes in 4 KiB tiles of 128 rows x 64 columns plus
@@ -44,16 +75,15 @@ cudaError_t tc_gemm_int4(const TcJob *jobs, int njobs, int group, const float *X
                          int num_sms, cudaStream_t st);
 cudaError_t tc_gemm_f16(const TcJob *jobs, int njobs, const float *X, int ldx, int T, int K, void *act, int num_sms,
                         cudaStream_t st);
-// Pack X [T][ldx] (K columns) into token tiles of TT rows: per (tile, k-tile)
-// `planes` f16 planes (hi = f16(x), lo = f16(x - hi)) of TT x 64, 128-byte swizzled.
-cudaError_t pack_act(const float *X, int ldx, int T, int K, int TT, int planes, void *act, cudaStream_t st);
 
 // -------------------------------------------------------------- wide GEMMs (tc_wide.cu)
-// Many tokens (T > 32): the (token tile, row tile, k-tile) units of all jobs
-// are split evenly over the SMs and every output is accumulated with atomics
-// (the caller clears Y first). Jobs share K; `tile0` is a job's first row tile
-// in the concatenation of all jobs' 128-row tiles (in job order). The jobs
-// travel by value in the launch (K and V of up to 64 layers).
+// Many tokens (T > 32): X [T][ldx] is packed into token tiles of up to 256
+// rows (`act`, wide_act_bytes) and the (token tile, row tile, k-tile) units of
+// all jobs are split evenly over the SMs. A run of units over a row tile's
+// whole k-range stores its outputs; the row tiles split between two runs are
+// cleared first and accumulated with atomics. Jobs share K; `tile0` (set
+// here) is a job's first row tile in the concatenation of all jobs' 128-row
+// tiles. The jobs travel by value in the launch (K and V of up to 64 layers).
 constexpr int WIDE_MAX_N = 256;      // token rows of one MMA
 constexpr int WIDE_MAX_JOBS = 128;
 struct WideJob {
@@ -74,11 +104,8 @@ struct WideArgs {
 };
 void wide_tiles(int T, int &ntt, int &N);
 size_t wide_act_bytes(int T, int K, bool int4);
-cudaError_t wide_pack(const float *X, int ldx, int T, int K, bool int4, void *act, cudaStream_t st);
-cudaError_t wide_gemm(const WideJob *jobs, int njobs, int64_t y_off, bool int4, int group, const void *act, int T,
-                      int K, int num_sms, cudaStream_t st);
-// Clear rows [0, T) after y_off of each job's output.
-cudaError_t wide_zero(const WideJob *jobs, int njobs, int64_t y_off, int T, cudaStream_t st);
+cudaError_t wide_gemm(const WideJob *jobs, int njobs, int64_t y_off, bool int4, int group, const float *X, int ldx,
+                      int T, int K, void *act, int num_sms, cudaStream_t st);
 
 // The device error word (a bounded wait that gave up sets bit 0).
 cudaError_t read_device_error(unsigned *out, bool reset);

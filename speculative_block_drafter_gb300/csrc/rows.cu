@@ -8,9 +8,30 @@
 namespace dfl {
 
 // ---------------------------------------------------------------- rms
-// x * (mean(x^2) + eps)^-1/2 * w, one CTA per row.
-__global__ void k_rmsnorm(const float *__restrict__ x, const float *__restrict__ w, float *__restrict__ out, int hs,
-                          float eps, int block, int keep_from, int keep_to) {
+// x * (mean(x^2) + eps)^-1/2 * w, one CTA per row. V4: rows, weight and output
+// 16-byte aligned and hs a multiple of 4 (float4 accesses, the row kept in
+// registers between the two passes when it fits).
+constexpr int RMS_THREADS = 256;
+constexpr int RMS_KEEP = 8;  // float4 a thread keeps: rows up to 8192
+
+__device__ __forceinline__ float block_sum(float v, float *red) {
+  v = warp_sum(v);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    float t = threadIdx.x < (blockDim.x >> 5) ? red[threadIdx.x] : 0.f;
+    t = warp_sum(t);
+    if (threadIdx.x == 0) red[0] = t;
+  }
+  __syncthreads();
+  return red[0];
+}
+
+template <bool V4>
+__global__ void __launch_bounds__(RMS_THREADS) k_rmsnorm(const float *__restrict__ x, const float *__restrict__ w,
+                                                         float *__restrict__ out, int hs, float eps, int block,
+                                                         int keep_from, int keep_to) {
+  pdl_wait();
   const int t = blockIdx.x;
   int orow = t;
   if (keep_from >= 0) {
@@ -18,30 +39,56 @@ __global__ void k_rmsnorm(const float *__restrict__ x, const float *__restrict__
     if (r < keep_from || r > keep_to) return;
     orow = s * (keep_to - keep_from + 1) + (r - keep_from);
   }
-  const float *xr = x + (int64_t)t * hs;
-  float ss = 0.f;
-  for (int i = threadIdx.x; i < hs; i += blockDim.x) ss = fmaf(xr[i], xr[i], ss);
   __shared__ float red[32];
-  ss = warp_sum(ss);
-  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
-  __syncthreads();
-  if (threadIdx.x < 32) {
-    float v = threadIdx.x < (blockDim.x >> 5) ? red[threadIdx.x] : 0.f;
-    v = warp_sum(v);
-    if (threadIdx.x == 0) red[0] = v;
-  }
-  __syncthreads();
-  const float s = 1.0f / sqrtf(red[0] / (float)hs + eps);
+  const float *xr = x + (int64_t)t * hs;
   float *o = out + (int64_t)orow * hs;
-  for (int i = threadIdx.x; i < hs; i += blockDim.x) o[i] = xr[i] * s * w[i];
+  if (V4) {
+    const int n4 = hs / 4;
+    const float4 *x4 = (const float4 *)xr;
+    float4 keep[RMS_KEEP];
+    float ss = 0.f;
+#pragma unroll
+    for (int m = 0; m < RMS_KEEP; ++m) {
+      const int i = threadIdx.x + m * RMS_THREADS;
+      keep[m] = i < n4 ? x4[i] : make_float4(0.f, 0.f, 0.f, 0.f);
+      ss = fmaf(keep[m].x, keep[m].x, fmaf(keep[m].y, keep[m].y, fmaf(keep[m].z, keep[m].z, fmaf(keep[m].w, keep[m].w, ss))));
+    }
+    for (int i = threadIdx.x + RMS_KEEP * RMS_THREADS; i < n4; i += RMS_THREADS) {
+      const float4 v = x4[i];
+      ss = fmaf(v.x, v.x, fmaf(v.y, v.y, fmaf(v.z, v.z, fmaf(v.w, v.w, ss))));
+    }
+    const float sc = 1.0f / sqrtf(block_sum(ss, red) / (float)hs + eps);
+    const float4 *w4 = (const float4 *)w;
+    float4 *o4 = (float4 *)o;
+#pragma unroll
+    for (int m = 0; m < RMS_KEEP; ++m) {
+      const int i = threadIdx.x + m * RMS_THREADS;
+      if (i < n4) {
+        const float4 g = w4[i];
+        o4[i] = make_float4(keep[m].x * sc * g.x, keep[m].y * sc * g.y, keep[m].z * sc * g.z, keep[m].w * sc * g.w);
+      }
+    }
+    for (int i = threadIdx.x + RMS_KEEP * RMS_THREADS; i < n4; i += RMS_THREADS) {
+      const float4 v = x4[i], g = w4[i];
+      o4[i] = make_float4(v.x * sc * g.x, v.y * sc * g.y, v.z * sc * g.z, v.w * sc * g.w);
+    }
+  } else {
+    float ss = 0.f;
+    for (int i = threadIdx.x; i < hs; i += RMS_THREADS) ss = fmaf(xr[i], xr[i], ss);
+    const float sc = 1.0f / sqrtf(block_sum(ss, red) / (float)hs + eps);
+    for (int i = threadIdx.x; i < hs; i += RMS_THREADS) o[i] = xr[i] * sc * w[i];
+  }
 }
 
 cudaError_t rmsnorm(const float *x, const float *w, float *out, int T, int hs, float eps, int block, int keep_from,
                     int keep_to, cudaStream_t st) {
   if (T <= 0) return cudaSuccess;
-  k_rmsnorm<<<T, 256, 0, st>>>(x, w, out, hs, eps, block, keep_from, keep_to);
-  count_launch(1);
-  return cudaGetLastError();
+  const bool v4 = (hs % 4 == 0) && ((((uintptr_t)x) | ((uintptr_t)w) | ((uintptr_t)out)) & 15) == 0;
+  if (v4)
+    return launch_pdl(k_rmsnorm<true>, dim3(T), dim3(RMS_THREADS), 0, st, 1, x, w, out, hs, eps, block, keep_from,
+                      keep_to);
+  return launch_pdl(k_rmsnorm<false>, dim3(T), dim3(RMS_THREADS), 0, st, 1, x, w, out, hs, eps, block, keep_from,
+                    keep_to);
 }
 
 // ---------------------------------------------------------------- row convolution
@@ -49,6 +96,7 @@ cudaError_t rmsnorm(const float *x, const float *w, float *out, int T, int hs, f
 template <int STAGE>
 __global__ void k_conv(const float *__restrict__ x, const float *__restrict__ d, const float *__restrict__ base,
                        float *__restrict__ y, int hs, int kn, int gs, int block) {
+  pdl_wait();
   const int t = blockIdx.y;
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= hs) return;
@@ -66,17 +114,13 @@ __global__ void k_conv(const float *__restrict__ x, const float *__restrict__ d,
 cudaError_t conv_stage0(const float *x, const float *d, const float *base, float *y, int T, int hs, int kn, int gs,
                         int block, cudaStream_t st) {
   dim3 grid((hs + 255) / 256, T);
-  k_conv<0><<<grid, 256, 0, st>>>(x, d, base, y, hs, kn, gs, block);
-  count_launch(1);
-  return cudaGetLastError();
+  return launch_pdl(k_conv<0>, grid, dim3(256), 0, st, 1, x, d, base, y, hs, kn, gs, block);
 }
 
 cudaError_t conv_stage1_residual(const float *x, const float *d, const float *base, float *h, int T, int hs, int kn,
                                  int gs, int block, cudaStream_t st) {
   dim3 grid((hs + 255) / 256, T);
-  k_conv<1><<<grid, 256, 0, st>>>(x, d, base, h, hs, kn, gs, block);
-  count_launch(1);
-  return cudaGetLastError();
+  return launch_pdl(k_conv<1>, grid, dim3(256), 0, st, 1, x, d, base, h, hs, kn, gs, block);
 }
 
 // ---------------------------------------------------------------- head norm + rotation
@@ -132,6 +176,7 @@ template <int HD>
 __global__ void k_head_norm_rope(float *__restrict__ x, int ld, const float *__restrict__ w, int T, int heads,
                                  float eps, int rotary, PosArgs pa,
                                  int use_pos0, int block, int64_t pos_base) {
+  pdl_wait();
   const int wid = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (wid >= T * heads) return;
@@ -150,6 +195,7 @@ struct CtxRope {
 // One warp per (row, head) of layer blockIdx.y's context K.
 template <int HD>
 __global__ void k_ctx_norm_rope(CtxRope R, int T, int heads, float eps, int64_t pos_base) {
+  pdl_wait();
   const int wid = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (wid >= T * heads) return;
@@ -171,11 +217,9 @@ cudaError_t ctx_norm_rope(float *const *k, const float *const *w, const int *rot
   for (int i = 0; i < 64; ++i) R.inv[i] = i < hd / 2 ? inv_freq[i] : 0.f;
   const int warps = T * heads;
   dim3 grid((unsigned)((warps * 32 + 255) / 256), nlayers);
-  if (hd == 128) k_ctx_norm_rope<128><<<grid, 256, 0, st>>>(R, T, heads, eps, pos_base);
-  else if (hd == 64) k_ctx_norm_rope<64><<<grid, 256, 0, st>>>(R, T, heads, eps, pos_base);
-  else return cudaErrorInvalidValue;
-  count_launch(1);
-  return cudaGetLastError();
+  if (hd == 128) return launch_pdl(k_ctx_norm_rope<128>, grid, dim3(256), 0, st, 1, R, T, heads, eps, pos_base);
+  if (hd == 64) return launch_pdl(k_ctx_norm_rope<64>, grid, dim3(256), 0, st, 1, R, T, heads, eps, pos_base);
+  return cudaErrorInvalidValue;
 }
 
 cudaError_t head_norm_rope(float *x, int ld, const float *w, const float *inv_freq, int T, int heads, int hd,
@@ -188,20 +232,19 @@ cudaError_t head_norm_rope(float *x, int ld, const float *w, const float *inv_fr
   for (int i = 0; i < 64; ++i) pa.inv[i] = i < hd / 2 ? inv_freq[i] : 0.f;
   const int warps = T * heads;
   const unsigned grid = (unsigned)((warps * 32 + 255) / 256);
+  const int up0 = pos0 != nullptr;
   if (hd == 128)
-    k_head_norm_rope<128><<<grid, 256, 0, st>>>(x, ld, w, T, heads, eps, rotary, pa, pos0 != nullptr,
-                                                block, pos_base);
-  else if (hd == 64)
-    k_head_norm_rope<64><<<grid, 256, 0, st>>>(x, ld, w, T, heads, eps, rotary, pa, pos0 != nullptr,
-                                               block, pos_base);
-  else
-    return cudaErrorInvalidValue;
-  count_launch(1);
-  return cudaGetLastError();
+    return launch_pdl(k_head_norm_rope<128>, dim3(grid), dim3(256), 0, st, 1, x, ld, w, T, heads, eps, (int)rotary, pa,
+                      up0, block, pos_base);
+  if (hd == 64)
+    return launch_pdl(k_head_norm_rope<64>, dim3(grid), dim3(256), 0, st, 1, x, ld, w, T, heads, eps, (int)rotary, pa,
+                      up0, block, pos_base);
+  return cudaErrorInvalidValue;
 }
 
 // ---------------------------------------------------------------- SiLU gate
 __global__ void k_silu_mul(const float *__restrict__ g, const float *__restrict__ u, float *__restrict__ m, int64_t n) {
+  pdl_wait();
   int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= n) return;
   const float a = g[i];
@@ -209,9 +252,7 @@ __global__ void k_silu_mul(const float *__restrict__ g, const float *__restrict_
 }
 
 cudaError_t silu_mul(const float *g, const float *u, float *m, int64_t n, cudaStream_t st) {
-  k_silu_mul<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(g, u, m, n);
-  count_launch(1);
-  return cudaGetLastError();
+  return launch_pdl(k_silu_mul, dim3((unsigned)((n + 255) / 256)), dim3(256), 0, st, 1, g, u, m, n);
 }
 
 }  // namespace dfl

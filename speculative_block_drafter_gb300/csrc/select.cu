@@ -48,6 +48,7 @@ __device__ __forceinline__ unsigned long long umax64(unsigned long long a, unsig
 // Stage 1: one CTA per (chunk, row), eight logits a thread.
 __global__ void __launch_bounds__(SEL_THREADS) k_chunk_max(const float *__restrict__ logits, int width,
                                                            unsigned long long *__restrict__ cmax) {
+  pdl_wait();
   __shared__ unsigned long long red[SEL_THREADS / 32];
   const int chunk = blockIdx.x, row = blockIdx.y;
   const float *lr = logits + (int64_t)row * width;
@@ -156,6 +157,7 @@ __global__ void __launch_bounds__(ROW_THREADS) k_row_select(
     const uint16_t *__restrict__ pred, const uint16_t *__restrict__ succ, int k, int width, int rank, int top,
     int vocab, int nchunks, const unsigned long long *__restrict__ cmax, uint32_t *__restrict__ ctok,
     float *__restrict__ score) {
+  pdl_wait();
   __shared__ unsigned long long keys[CAND_CAP];
   __shared__ unsigned long long red[ROW_THREADS / 32];
   __shared__ uint32_t cur[TOP_MAX], prv[TOP_MAX];
@@ -207,6 +209,7 @@ __global__ void __launch_bounds__(CHAIN_THREADS) k_chain(const uint32_t *__restr
                                                          int vocab, const uint32_t *__restrict__ ctok,
                                                          const float *__restrict__ score, uint32_t *__restrict__ chosen,
                                                          uint32_t *__restrict__ plain) {
+  pdl_wait();
   extern __shared__ __align__(16) uint8_t chain_sm[];
   float *sc = (float *)chain_sm;                    // [k][top][top]
   uint32_t *cand = (uint32_t *)(sc + k * top * top);  // [k][top]
@@ -259,12 +262,13 @@ cudaError_t select_tokens(const float *logits, const float *hp, const uint32_t *
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  k_chunk_max<<<dim3(nchunks, rows), SEL_THREADS, 0, st>>>(logits, width, cmax);
-  k_row_select<<<rows, ROW_THREADS, 0, st>>>(logits, hp, anchor_tok, pred, succ, k, width, rank, top, vocab, nchunks,
-                                             cmax, ctok, score);
-  k_chain<<<batch, CHAIN_THREADS, smem, st>>>(anchor_tok, k, top, vocab, ctok, score, chosen, plain);
-  count_launch(3);
-  return cudaGetLastError();
+  cudaError_t e = launch_pdl(k_chunk_max, dim3(nchunks, rows), dim3(SEL_THREADS), 0, st, 1, logits, width, cmax);
+  if (e != cudaSuccess) return e;
+  e = launch_pdl(k_row_select, dim3(rows), dim3(ROW_THREADS), 0, st, 1, logits, hp, anchor_tok, pred, succ, k, width,
+                 rank, top, vocab, nchunks, cmax, ctok, score);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(k_chain, dim3(batch), dim3(CHAIN_THREADS), smem, st, 1, anchor_tok, k, top, vocab, ctok, score,
+                    chosen, plain);
 }
 
 }  // namespace dfl

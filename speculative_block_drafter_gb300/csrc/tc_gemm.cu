@@ -114,42 +114,47 @@ __global__ void k_tc_pack_f16(const uint16_t *__restrict__ src, int64_t rows, in
   dst[tile * 1024 + sw128_off(r, c) / 16] = make_uint4(v[0], v[1], v[2], v[3]);
 }
 
-// Tokens: per (token tile tt, k-tile kt, plane p) TT rows x 64 columns f16,
-// K-major with the 128-byte swizzle. Plane 0 = f16(x); plane 1 = f16(x - f16(x)).
+// Outputs a split-K launch accumulates into, cleared first: T rows of n floats.
+constexpr int MAX_JOBS = 4;
+struct ZeroJobs {
+  float *y[MAX_JOBS];
+  int ldy[MAX_JOBS];
+  int n[MAX_JOBS];
+  int njobs;
+};
+
+// The token tiles of a GEMM (blocks < pack_blocks) and the clearing of its
+// outputs (the other blocks).
 template <int PLANES>
-__global__ void k_tc_pack_act(const float *__restrict__ X, int ldx, int T, int K, int TT, uint4 *__restrict__ dst) {
-  const int KT = K / 64;
-  const int64_t total = (int64_t)((T + TT - 1) / TT) * KT * TT * 8;
-  int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (t >= total) return;
-  const int c = (int)(t & 7);
-  const int r = (int)((t >> 3) % TT);
-  const int64_t rest = (t >> 3) / TT;
-  const int kt = (int)(rest % KT);
-  const int tt = (int)(rest / KT);
-  const int tok = tt * TT + r;
-  float x[8];
-  if (tok < T) {
-    const float *p = X + (int64_t)tok * ldx + kt * 64 + c * 8;
-    for (int i = 0; i < 8; ++i) x[i] = p[i];
-  } else {
-    for (int i = 0; i < 8; ++i) x[i] = 0.f;
-  }
-  uint32_t hi[4], lo[4];
-  for (int i = 0; i < 4; ++i) {
-    if (PLANES == 2) {
-      split2(x[2 * i], x[2 * i + 1], hi[i], lo[i]);
-    } else {
-      hi[i] = pack_half2(__float2half_rn(x[2 * i]), __float2half_rn(x[2 * i + 1]));
+__global__ void k_tc_pack_act(const float *__restrict__ X, int ldx, int T, int K, int TT, uint4 *__restrict__ dst,
+                              ZeroJobs Z, int pack_blocks) {
+  pdl_wait();
+  pdl_trigger();
+  if ((int)blockIdx.x >= pack_blocks) {
+    // segments of 2048 outputs of one token row, round robin over the clearing blocks
+    const int zb = blockIdx.x - pack_blocks, nzb = gridDim.x - pack_blocks;
+    int seg0 = 0;
+    for (int j = 0; j < Z.njobs; ++j) {
+      const int per_row = (Z.n[j] + 2047) / 2048;
+      const int segs = T * per_row;
+      int first = zb - seg0 % nzb;
+      if (first < 0) first += nzb;
+      for (int sg = first; sg < segs; sg += nzb) {
+        const int t = sg / per_row, c0 = (sg - t * per_row) * 2048;
+        float *y = Z.y[j] + (int64_t)t * Z.ldy[j];
+        const int c1 = min(Z.n[j], c0 + 2048);
+        for (int c = c0 + threadIdx.x; c < c1; c += blockDim.x) y[c] = 0.f;
+      }
+      seg0 += segs;
     }
+    return;
   }
-  const int64_t base = (((int64_t)tt * KT + kt) * PLANES) * TT * 8;  // in 16-byte chunks
-  dst[base + sw128_off(r, c) / 16] = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-  if (PLANES == 2) dst[base + TT * 8 + sw128_off(r, c) / 16] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+  const int64_t total = (int64_t)((T + TT - 1) / TT) * (K / 64) * TT * 8;
+  const int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (t < total) pack_act_chunk<PLANES>(X, ldx, T, K, TT, dst, t);
 }
 
 // ---------------------------------------------------------------- jobs
-constexpr int MAX_JOBS = 4;
 struct TcJobs {
   const void *w[MAX_JOBS];        // packed codes / f16 tiles
   const uint16_t *s[MAX_JOBS];    // packed scales (four-bit)
@@ -186,15 +191,15 @@ constexpr int I4_PRODUCER = 8;
 constexpr int I4_MMA0 = 9;
 constexpr int I4_MAX_THREADS = 32 * (I4_MMA0 + 2);
 
-template <int TT, int DU, int MT>
+template <int TT, int DU, int MT, int SA_>
 struct I4 {
   static constexpr int THREADS = 32 * (I4_MMA0 + MT);
   static constexpr int B_BYTES = 2 * TT * 128;                 // hi + lo planes of a k-tile
   static constexpr int CODE_OFF = B_BYTES;                     // MT x 4 KiB
   static constexpr int SCALE_OFF = B_BYTES + MT * 4096;        // MT x DU x 256 B
   static constexpr int STAGE = ((SCALE_OFF + MT * DU * 256) + 1023) / 1024 * 1024;
-  static constexpr int S = 6;                                  // shared-memory stages
-  static constexpr int SA = 2;                                 // tensor-memory A slots
+  static constexpr int S = (96 * 1024 / STAGE) < 12 ? (96 * 1024 / STAGE) : 12;  // shared-memory stages
+  static constexpr int SA = SA_;                               // tensor-memory A slots
   static constexpr int AW = MT * 32;                           // A columns of a slot
   static constexpr int DW = MT * 2 * TT;                       // accumulator columns of a unit
   static constexpr int DCOL = SA * AW;
@@ -227,10 +232,10 @@ __device__ __forceinline__ void i4_item(const TcJobs &J, const I4Items &P, int M
   kt1 = min(KT, kt0 + P.kc);
 }
 
-template <int TT, int DU, int MT>
+template <int TT, int DU, int MT, int SA>
 __global__ void __launch_bounds__(I4_MAX_THREADS, 2) k_tc_int4(TcJobs J, I4Items P, const uint8_t *__restrict__ bpack,
                                                                int K, int T, int atomic_out) {
-  using C = I4<TT, DU, MT>;
+  using C = I4<TT, DU, MT, SA>;
   extern __shared__ __align__(1024) uint8_t smraw[];
   uint8_t *sm = smraw + ((1024 - (smem_u32(smraw) & 1023)) & 1023);
   uint64_t *bars = (uint64_t *)(sm + C::S * C::STAGE);
@@ -255,6 +260,28 @@ __global__ void __launch_bounds__(I4_MAX_THREADS, 2) k_tc_int4(TcJobs J, I4Items
     }
     mbar_fence_init();
   }
+  __syncthreads();
+  // The weights do not depend on the kernels before this one: the first stages'
+  // codes and scales are fetched before waiting for them.
+  int npre = 0;
+  if (warp == I4_PRODUCER && lane == 0) {
+    for (int it = blockIdx.x; it < P.items && npre < C::S; it += gridDim.x) {
+      int job, m0, mtv, tt, kt0, kt1;
+      i4_item(J, P, MT, KT, it, job, m0, mtv, tt, kt0, kt1);
+      const uint8_t *wc = (const uint8_t *)J.w[job] + (int64_t)m0 * KT * 4096;
+      const uint8_t *ws = (const uint8_t *)J.s[job] + (int64_t)m0 * KT * DU * 256;
+      for (int kt = kt0; kt < kt1 && npre < C::S; ++kt, ++npre) {
+        const uint32_t st = smem_u32(sm + npre * C::STAGE);
+        mbar_expect_tx(full0 + 8 * npre, C::B_BYTES + mtv * (4096 + DU * 256));
+        for (int jj = 0; jj < mtv; ++jj) {
+          bulk_g2s(st + C::CODE_OFF + jj * 4096, wc + ((int64_t)jj * KT + kt) * 4096, 4096, full0 + 8 * npre);
+          bulk_g2s(st + C::SCALE_OFF + jj * DU * 256, ws + ((int64_t)jj * KT + kt) * DU * 256, DU * 256,
+                   full0 + 8 * npre);
+        }
+      }
+    }
+  }
+  pdl_wait();
   if (warp == 0) tmem_alloc(smem_u32(tslot), TC_TMEM_COLS);
   tc_fence_before();
   __syncthreads();
@@ -273,18 +300,20 @@ __global__ void __launch_bounds__(I4_MAX_THREADS, 2) k_tc_int4(TcJobs J, I4Items
         const uint8_t *bp = bpack + (int64_t)tt * KT * C::B_BYTES;
         for (int kt = kt0; kt < kt1; ++kt, ++i) {
           const int s = i % C::S;
-          if (i >= C::S && !mbar_wait(empty0 + 8 * s, ((i / C::S) - 1) & 1)) {
-            ok = false;
-            break;
-          }
           const uint32_t st = smem_u32(sm + s * C::STAGE);
-          mbar_expect_tx(full0 + 8 * s, C::B_BYTES + mtv * (4096 + DU * 256));
-          bulk_g2s(st, bp + (int64_t)kt * C::B_BYTES, C::B_BYTES, full0 + 8 * s);
-          for (int jj = 0; jj < mtv; ++jj) {
-            bulk_g2s(st + C::CODE_OFF + jj * 4096, wc + ((int64_t)jj * KT + kt) * 4096, 4096, full0 + 8 * s);
-            bulk_g2s(st + C::SCALE_OFF + jj * DU * 256, ws + ((int64_t)jj * KT + kt) * DU * 256, DU * 256,
-                     full0 + 8 * s);
+          if (i >= npre) {
+            if (i >= C::S && !mbar_wait(empty0 + 8 * s, ((i / C::S) - 1) & 1)) {
+              ok = false;
+              break;
+            }
+            mbar_expect_tx(full0 + 8 * s, C::B_BYTES + mtv * (4096 + DU * 256));
+            for (int jj = 0; jj < mtv; ++jj) {
+              bulk_g2s(st + C::CODE_OFF + jj * 4096, wc + ((int64_t)jj * KT + kt) * 4096, 4096, full0 + 8 * s);
+              bulk_g2s(st + C::SCALE_OFF + jj * DU * 256, ws + ((int64_t)jj * KT + kt) * DU * 256, DU * 256,
+                       full0 + 8 * s);
+            }
           }
+          bulk_g2s(st, bp + (int64_t)kt * C::B_BYTES, C::B_BYTES, full0 + 8 * s);
         }
       }
     }
@@ -454,6 +483,7 @@ __global__ void __launch_bounds__(I4_MAX_THREADS, 2) k_tc_int4(TcJobs J, I4Items
       }
     }
   }
+  pdl_trigger();  // this CTA's work is done
   tc_fence_before();
   __syncthreads();
   if (warp == 0) {
@@ -488,7 +518,11 @@ __global__ void __launch_bounds__(TC_THREADS) k_tc_f16(TcJobs J, const uint8_t *
   const int tt = blockIdx.x, mt = blockIdx.y;
   const int kt0 = blockIdx.z * kc, kt1 = min(KT, kt0 + kc);
   const int n = kt1 - kt0;
-  if (n <= 0) return;
+  if (n <= 0) {
+    pdl_wait();
+    pdl_trigger();
+    return;
+  }
   const int job = job_of(J, mt);
   const int m = mt - J.tile0[job];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -501,6 +535,16 @@ __global__ void __launch_bounds__(TC_THREADS) k_tc_f16(TcJobs J, const uint8_t *
     mbar_init(done, 1);
     mbar_fence_init();
   }
+  __syncthreads();
+  // the first stages' weight tiles before waiting for the kernels this one follows
+  const uint8_t *wa = (const uint8_t *)J.w[job] + ((int64_t)m * KT) * 16384;
+  const int npre = n < S ? n : S;
+  if (warp == TC_PRODUCER && lane == 0)
+    for (int i = 0; i < npre; ++i) {
+      mbar_expect_tx(full0 + 8 * i, C::B_BYTES + 16384);
+      bulk_g2s(smem_u32(sm + i * C::STAGE) + C::A_OFF, wa + (int64_t)(kt0 + i) * 16384, 16384, full0 + 8 * i);
+    }
+  pdl_wait();
   if (warp == 0) tmem_alloc(smem_u32(tslot), C::COLS);
   tc_fence_before();
   __syncthreads();
@@ -509,15 +553,16 @@ __global__ void __launch_bounds__(TC_THREADS) k_tc_f16(TcJobs J, const uint8_t *
 
   if (warp == TC_PRODUCER) {
     if (lane == 0) {
-      const uint8_t *wa = (const uint8_t *)J.w[job] + ((int64_t)m * KT) * 16384;
       const uint8_t *bp = bpack + ((int64_t)tt * KT) * C::B_BYTES;
       for (int i = 0; i < n; ++i) {
         const int s = i % S, kt = kt0 + i;
-        if (i >= S && !mbar_wait(empty0 + 8 * s, ((i / S) - 1) & 1)) break;
         const uint32_t st = smem_u32(sm + s * C::STAGE);
-        mbar_expect_tx(full0 + 8 * s, C::B_BYTES + 16384);
+        if (i >= npre) {
+          if (i >= S && !mbar_wait(empty0 + 8 * s, ((i / S) - 1) & 1)) break;
+          mbar_expect_tx(full0 + 8 * s, C::B_BYTES + 16384);
+          bulk_g2s(st + C::A_OFF, wa + (int64_t)kt * 16384, 16384, full0 + 8 * s);
+        }
         bulk_g2s(st, bp + (int64_t)kt * C::B_BYTES, C::B_BYTES, full0 + 8 * s);
-        bulk_g2s(st + C::A_OFF, wa + (int64_t)kt * 16384, 16384, full0 + 8 * s);
       }
     }
   } else if (warp == TC_MMA) {
@@ -563,6 +608,7 @@ __global__ void __launch_bounds__(TC_THREADS) k_tc_f16(TcJobs J, const uint8_t *
       }
     }
   }
+  pdl_trigger();  // this CTA's work is done
   tc_fence_before();
   __syncthreads();
   if (warp == 0) {
@@ -633,8 +679,6 @@ cudaError_t tc_pack_f16(const uint16_t *src, int64_t rows, int64_t cols, void *d
   return cudaGetLastError();
 }
 
-static cudaError_t zero_outputs(const TcJob *jobs, int njobs, int T, cudaStream_t st);
-
 // Up to 32 tokens: the kernels of this file; more: the wide GEMMs (tc_wide.cu).
 constexpr int NARROW_MAX_T = 32;
 static int tt_int4(int T) { return T <= 16 ? 16 : 32; }
@@ -646,12 +690,29 @@ size_t tc_act_bytes(int T, int K, bool int4) {
   return (size_t)((T + TT - 1) / TT) * TT * K * 2 * (int4 ? 2 : 1);
 }
 
-cudaError_t pack_act(const float *X, int ldx, int T, int K, int TT, int planes, void *act, cudaStream_t st) {
+// Pack X into token tiles of TT rows and, for a split-K launch, clear its outputs.
+static cudaError_t launch_pack(const float *X, int ldx, int T, int K, int TT, int planes, void *act,
+                               const TcJob *jobs, int njobs, bool clear, cudaStream_t st) {
   const int64_t chunks = (int64_t)((T + TT - 1) / TT) * (K / 64) * TT * 8;
-  if (planes == 2) k_tc_pack_act<2><<<blocks_for(chunks, 256), 256, 0, st>>>(X, ldx, T, K, TT, (uint4 *)act);
-  else k_tc_pack_act<1><<<blocks_for(chunks, 256), 256, 0, st>>>(X, ldx, T, K, TT, (uint4 *)act);
-  count_launch(1);
-  return cudaGetLastError();
+  const int pack_blocks = (int)blocks_for(chunks, 256);
+  ZeroJobs Z{};
+  int zero_blocks = 0;
+  if (clear) {
+    Z.njobs = njobs;
+    int64_t most = 0;
+    for (int j = 0; j < njobs; ++j) {
+      Z.y[j] = jobs[j].y;
+      Z.ldy[j] = jobs[j].ldy;
+      Z.n[j] = jobs[j].n;
+      most = std::max<int64_t>(most, (int64_t)T * jobs[j].n);
+    }
+    zero_blocks = (int)std::min<int64_t>(blocks_for(most, 2048), 256);
+  }
+  if (planes == 2)
+    return launch_pdl(k_tc_pack_act<2>, dim3(pack_blocks + zero_blocks), dim3(256), 0, st, 1, X, ldx, T, K, TT,
+                      (uint4 *)act, Z, pack_blocks);
+  return launch_pdl(k_tc_pack_act<1>, dim3(pack_blocks + zero_blocks), dim3(256), 0, st, 1, X, ldx, T, K, TT,
+                    (uint4 *)act, Z, pack_blocks);
 }
 
 // The wide path for up to 4 matrices given as TcJobs.
@@ -660,11 +721,7 @@ static cudaError_t wide_jobs(const TcJob *jobs, int njobs, bool int4, int group,
   if (njobs < 1 || njobs > MAX_JOBS) return cudaErrorInvalidValue;
   WideJob w[MAX_JOBS];
   for (int j = 0; j < njobs; ++j) w[j] = WideJob{jobs[j].w, jobs[j].scales, jobs[j].y, jobs[j].n, jobs[j].ldy, 0};
-  cudaError_t e = zero_outputs(jobs, njobs, T, st);
-  if (e != cudaSuccess) return e;
-  e = wide_pack(X, ldx, T, K, int4, act, st);
-  if (e != cudaSuccess) return e;
-  return wide_gemm(w, njobs, 0, int4, group, act, T, K, num_sms, st);
+  return wide_gemm(w, njobs, 0, int4, group, X, ldx, T, K, act, num_sms, st);
 }
 
 template <typename KERN>
@@ -688,14 +745,6 @@ static void plan(int ntt, int mtiles, int KT, int num_sms, int kc_min, int &kc, 
   splits = (KT + kc - 1) / kc;
 }
 
-static cudaError_t zero_outputs(const TcJob *jobs, int njobs, int T, cudaStream_t st) {
-  for (int j = 0; j < njobs; ++j) {
-    cudaError_t e = cudaMemset2DAsync(jobs[j].y, (size_t)jobs[j].ldy * 4, 0, (size_t)jobs[j].n * 4, T, st);
-    if (e != cudaSuccess) return e;
-  }
-  return cudaSuccess;
-}
-
 static cudaError_t fill_jobs(const TcJob *jobs, int njobs, TcJobs &J, int &mtiles) {
   if (njobs < 1 || njobs > MAX_JOBS) return cudaErrorInvalidValue;
   J = TcJobs{};
@@ -714,12 +763,12 @@ static cudaError_t fill_jobs(const TcJob *jobs, int njobs, TcJobs &J, int &mtile
   return cudaSuccess;
 }
 
-template <int TT, int DU, int MT>
-static cudaError_t launch_int4(const TcJobs &J, int njobs, const uint8_t *bp, int K, int T, int ntt, int num_sms,
-                               const TcJob *jobs, cudaStream_t st) {
-  using C = I4<TT, DU, MT>;
+template <int TT, int DU, int MT, int SA>
+static cudaError_t launch_int4(const TcJobs &J, int njobs, const float *X, int ldx, void *act, int K, int T, int ntt,
+                               int num_sms, const TcJob *jobs, cudaStream_t st) {
+  using C = I4<TT, DU, MT, SA>;
   static bool configured = false;
-  cudaError_t e = set_smem(k_tc_int4<TT, DU, MT>, C::SMEM, configured);
+  cudaError_t e = set_smem(k_tc_int4<TT, DU, MT, SA>, C::SMEM, configured);
   if (e != cudaSuccess) return e;
   I4Items P{};
   P.groups = 0;
@@ -733,14 +782,11 @@ static cudaError_t launch_int4(const TcJobs &J, int njobs, const uint8_t *bp, in
   // enough items for two CTAs an SM, each at least 8 k-tiles long
   plan(ntt, P.groups, KT, num_sms, 8, P.kc, P.splits);
   P.items = ntt * P.groups * P.splits;
-  if (P.splits > 1) {
-    e = zero_outputs(jobs, njobs, T, st);
-    if (e != cudaSuccess) return e;
-  }
+  e = launch_pack(X, ldx, T, K, TT, 2, act, jobs, njobs, P.splits > 1, st);
+  if (e != cudaSuccess) return e;
   const int grid = std::min(P.items, 2 * num_sms);
-  k_tc_int4<TT, DU, MT><<<grid, C::THREADS, C::SMEM, st>>>(J, P, bp, K, T, P.splits > 1);
-  count_launch(1);
-  return cudaGetLastError();
+  return launch_pdl(k_tc_int4<TT, DU, MT, SA>, dim3(grid), dim3(C::THREADS), C::SMEM, st, 1, J, P,
+                    (const uint8_t *)act, K, T, (int)(P.splits > 1));
 }
 
 cudaError_t tc_gemm_int4(const TcJob *jobs, int njobs, int group, const float *X, int ldx, int T, int K, void *act,
@@ -752,35 +798,28 @@ cudaError_t tc_gemm_int4(const TcJob *jobs, int njobs, int group, const float *X
   if (e != cudaSuccess) return e;
   const int TT = tt_int4(T);
   const int ntt = (T + TT - 1) / TT;
-  const int KT = K / 64;
-  const int64_t chunks = (int64_t)ntt * KT * TT * 8;
-  k_tc_pack_act<2><<<blocks_for(chunks, 256), 256, 0, st>>>(X, ldx, T, K, TT, (uint4 *)act);
-  count_launch(1);
-  const uint8_t *bp = (const uint8_t *)act;
   const int DU = drain_units(group);
-  if (TT == 16) return DU == 1 ? launch_int4<16, 1, 2>(J, njobs, bp, K, T, ntt, num_sms, jobs, st)
-                               : launch_int4<16, 2, 2>(J, njobs, bp, K, T, ntt, num_sms, jobs, st);
-  return DU == 1 ? launch_int4<32, 1, 1>(J, njobs, bp, K, T, ntt, num_sms, jobs, st)
-                 : launch_int4<32, 2, 1>(J, njobs, bp, K, T, ntt, num_sms, jobs, st);
+  // (token tile, quantisation units a k-tile, 128-row tiles an item, tensor-memory A slots)
+  if (TT == 16) return DU == 1 ? launch_int4<16, 1, 2, 2>(J, njobs, X, ldx, act, K, T, ntt, num_sms, jobs, st)
+                               : launch_int4<16, 2, 2, 2>(J, njobs, X, ldx, act, K, T, ntt, num_sms, jobs, st);
+  return DU == 1 ? launch_int4<32, 1, 1, 2>(J, njobs, X, ldx, act, K, T, ntt, num_sms, jobs, st)
+                 : launch_int4<32, 2, 1, 2>(J, njobs, X, ldx, act, K, T, ntt, num_sms, jobs, st);
 }
 
 template <int TT>
-static cudaError_t launch_f16(const TcJobs &J, int mtiles, const uint8_t *bp, int K, int T, int ntt, int num_sms,
-                              const TcJob *jobs, int njobs, cudaStream_t st) {
+static cudaError_t launch_f16(const TcJobs &J, int mtiles, const float *X, int ldx, void *act, int K, int T, int ntt,
+                              int num_sms, const TcJob *jobs, int njobs, cudaStream_t st) {
   using C = F16Cfg<TT>;
   static bool configured = false;
   cudaError_t e = set_smem(k_tc_f16<TT>, C::SMEM, configured);
   if (e != cudaSuccess) return e;
   int kc, splits;
   plan(ntt, mtiles, K / 64, num_sms, 8, kc, splits);
-  if (splits > 1) {
-    e = zero_outputs(jobs, njobs, T, st);
-    if (e != cudaSuccess) return e;
-  }
+  e = launch_pack(X, ldx, T, K, TT, 1, act, jobs, njobs, splits > 1, st);
+  if (e != cudaSuccess) return e;
   dim3 grid(ntt, mtiles, splits);
-  k_tc_f16<TT><<<grid, TC_THREADS, C::SMEM, st>>>(J, bp, K, T, kc, splits > 1);
-  count_launch(1);
-  return cudaGetLastError();
+  return launch_pdl(k_tc_f16<TT>, grid, dim3(TC_THREADS), C::SMEM, st, 1, J, (const uint8_t *)act, K, T, kc,
+                    (int)(splits > 1));
 }
 
 cudaError_t tc_gemm_f16(const TcJob *jobs, int njobs, const float *X, int ldx, int T, int K, void *act, int num_sms,
@@ -792,13 +831,8 @@ cudaError_t tc_gemm_f16(const TcJob *jobs, int njobs, const float *X, int ldx, i
   if (e != cudaSuccess) return e;
   const int TT = tt_f16(T);
   const int ntt = (T + TT - 1) / TT;
-  const int KT = K / 64;
-  const int64_t chunks = (int64_t)ntt * KT * TT * 8;
-  k_tc_pack_act<1><<<blocks_for(chunks, 256), 256, 0, st>>>(X, ldx, T, K, TT, (uint4 *)act);
-  count_launch(1);
-  const uint8_t *bp = (const uint8_t *)act;
-  return TT == 16 ? launch_f16<16>(J, mtiles, bp, K, T, ntt, num_sms, jobs, njobs, st)
-                  : launch_f16<32>(J, mtiles, bp, K, T, ntt, num_sms, jobs, njobs, st);
+  return TT == 16 ? launch_f16<16>(J, mtiles, X, ldx, act, K, T, ntt, num_sms, jobs, njobs, st)
+                  : launch_f16<32>(J, mtiles, X, ldx, act, K, T, ntt, num_sms, jobs, njobs, st);
 }
 
 cudaError_t read_device_error(unsigned *out, bool reset) {

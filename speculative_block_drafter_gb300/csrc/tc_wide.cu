@@ -50,9 +50,21 @@ struct WCfg {
   static constexpr int SA = 2;                     // tensor-memory A slots (four-bit)
   static constexpr int NBUF = KIND == W_KIND_F16 ? 2 : 1;
   static constexpr int A_COL = 256;                // A slots after the accumulator (four-bit)
-  static constexpr int NBAR = 2 * STAGES + 2 * SA + 2 * NBUF;
-  static constexpr int SMEM = STAGES * STAGE_MAX + 1024 + 8 * NBAR + 64;
+  static constexpr int NBAR = 2 * STAGES + 2 * SA + 2 * NBUF + 1;  // + the epilogue's 128-thread barrier
+  static constexpr int STAGING = 2 * 16 * 128 * 4;  // two slices of 16 tokens x 128 rows f32 (the epilogue)
+  static constexpr int SMEM = STAGES * STAGE_MAX + STAGING + 1024 + 8 * NBAR + 64;
 };
+
+// ---------------------------------------------------------------- epilogue helpers
+// The epilogue's warps 0-3 meet on an mbarrier of count 128 (a bounded wait, so
+// that a warp that gave up elsewhere cannot stall the others for ever).
+__device__ __forceinline__ bool drain_bar(uint32_t bar, int &phase) {
+  mbar_arrive(bar);
+  const bool ok = mbar_wait(bar, (uint32_t)phase);
+  phase ^= 1;
+  return ok;
+}
+
 
 __device__ __forceinline__ WideJob wjob(const WideArgs &A, int j) { return A.job[j]; }
 
@@ -119,6 +131,50 @@ __device__ __forceinline__ int64_t wrun_end(const WideArgs &A, int64_t u, int64_
   return tile_end < u1 ? tile_end : u1;
 }
 
+// A walk over consecutive units of one CTA: the token tile, the k-tile and the
+// address of the CTA's weight tile, advanced without divisions.
+template <int CL>
+struct WCursor {
+  int tt, g, kt, groups;
+  int64_t tile0;              // the row tile's first k-tile in its matrix's packed tiles
+  const uint8_t *w, *s;       // the matrix's codes (or f16 tiles) and scales
+  __device__ __forceinline__ void locate(const WideArgs &A, int rank) {
+    int mt = g * CL + rank;
+    if (mt >= A.mtiles) mt = A.mtiles - 1;  // a ghost CTA loads a real tile it will not write
+    const WideJob J = wjob(A, wjob_of(A, mt));
+    tile0 = (int64_t)(mt - J.tile0) * A.KT;
+    w = (const uint8_t *)J.w;
+    s = (const uint8_t *)J.s;
+  }
+  __device__ __forceinline__ void start(const WideArgs &A, int64_t u, int rank) {
+    groups = (A.mtiles + CL - 1) / CL;
+    const int64_t tg = u / A.KT;
+    kt = (int)(u - tg * A.KT);
+    g = (int)(tg % groups);
+    tt = (int)(tg / groups);
+    locate(A, rank);
+  }
+  __device__ __forceinline__ void next(const WideArgs &A, int rank) {
+    if (++kt == A.KT) {
+      kt = 0;
+      if (++g == groups) {
+        g = 0;
+        ++tt;
+      }
+      locate(A, rank);
+    }
+  }
+  template <int KIND, int DU>
+  __device__ __forceinline__ void load_a(const WideArgs &A, uint32_t dst, uint32_t bar) const {
+    if (KIND == W_KIND_F16) {
+      bulk_g2s(dst, w + (tile0 + kt) * 16384, 16384, bar);
+    } else {
+      bulk_g2s(dst, w + (tile0 + kt) * 4096, 4096, bar);
+      bulk_g2s(dst + 4096, s + (tile0 + kt) * DU * 256, DU * 256, bar);
+    }
+  }
+};
+
 template <int KIND, int DU, int CL>
 __global__ void __launch_bounds__(W_THREADS, 1) k_wide(WideArgs A) {
   using C = WCfg<KIND, DU>;
@@ -128,10 +184,12 @@ __global__ void __launch_bounds__(W_THREADS, 1) k_wide(WideArgs A) {
   const int N = A.N;
   const int b_bytes = C::PLANES * N * 128;
   const int stage = (b_bytes + C::A_BYTES + 1023) & ~1023;
-  uint64_t *bars = (uint64_t *)(sm + S * stage);
+  float *staging = (float *)(sm + S * stage);
+  uint64_t *bars = (uint64_t *)(sm + S * stage + C::STAGING);
   uint32_t *tslot = (uint32_t *)(bars + C::NBAR);
   const uint32_t full0 = smem_u32(bars), empty0 = full0 + 8 * S, afull0 = empty0 + 8 * S;
   const uint32_t afree0 = afull0 + 8 * C::SA, dfull0 = afree0 + 8 * C::SA, dfree0 = dfull0 + 8 * C::NBUF;
+  const uint32_t ebar = dfree0 + 8 * C::NBUF;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int rank = CL > 1 ? (int)cluster_rank() : 0;
   const uint16_t everyone = (uint16_t)((1u << CL) - 1);
@@ -155,40 +213,53 @@ __global__ void __launch_bounds__(W_THREADS, 1) k_wide(WideArgs A) {
       mbar_init(dfull0 + 8 * i, 1);
       mbar_init(dfree0 + 8 * i, 128);
     }
+    mbar_init(ebar, 128);
     mbar_fence_init();
   }
+  __syncthreads();
+  if (CL > 1) cluster_sync();  // every barrier of the cluster exists before the first multicast
+  // The weights do not depend on the kernels before this one: the first stages'
+  // weight tiles are fetched before waiting for them. The producer walks its
+  // units with counters (a division per unit would slow the one thread that
+  // feeds the pipeline).
+  WCursor<CL> cur;
+  int npre = 0;
+  if (warp == W_PRODUCER && lane == 0) {
+    cur.start(A, u0, rank);
+    for (; npre < S && u0 + npre < u1; ++npre, cur.next(A, rank)) {
+      mbar_expect_tx(full0 + 8 * npre, b_bytes + C::A_BYTES);
+      cur.load_a<KIND, DU>(A, smem_u32(sm + npre * stage) + b_bytes, full0 + 8 * npre);
+    }
+  }
+  pdl_wait();
   if (warp == 0) tmem_alloc(smem_u32(tslot), 512);
   tc_fence_before();
   __syncthreads();
-  if (CL > 1) cluster_sync();  // every barrier of the cluster exists before the first multicast
   tc_fence_after();
   const uint32_t tbase = *tslot;
 
   if (warp == W_PRODUCER) {
     if (lane == 0) {
       const int slice = b_bytes / CL;
+      WCursor<CL> bc;  // the units' token tiles
+      bc.start(A, u0, rank);
       int i = 0;
       bool ok = true;
-      for (int64_t u = u0; u < u1; ++u, ++i) {
-        const WUnit w = wunit<CL>(A, u, rank);
+      for (int64_t u = u0; u < u1; ++u, ++i, bc.next(A, rank)) {
         const int s = i % S;
-        if (i >= S && !mbar_wait(empty0 + 8 * s, ((i / S) - 1) & 1)) {
-          ok = false;
-          break;
-        }
-        const WideJob J = wjob(A, wjob_of(A, w.mt));
-        const int64_t tile = (int64_t)(w.mt - J.tile0) * A.KT + w.kt;
         const uint32_t st = smem_u32(sm + s * stage);
-        const uint8_t *bp = A.bpack + ((int64_t)w.tt * A.KT + w.kt) * b_bytes;
-        mbar_expect_tx(full0 + 8 * s, b_bytes + C::A_BYTES);
+        if (i >= npre) {
+          if (i >= S && !mbar_wait(empty0 + 8 * s, ((i / S) - 1) & 1)) {
+            ok = false;
+            break;
+          }
+          mbar_expect_tx(full0 + 8 * s, b_bytes + C::A_BYTES);
+          cur.load_a<KIND, DU>(A, st + b_bytes, full0 + 8 * s);
+          cur.next(A, rank);
+        }
+        const uint8_t *bp = A.bpack + ((int64_t)bc.tt * A.KT + bc.kt) * b_bytes;
         if (CL > 1) bulk_g2s_mc(st + rank * slice, bp + rank * slice, slice, full0 + 8 * s, everyone);
         else bulk_g2s(st, bp, b_bytes, full0 + 8 * s);
-        if (KIND == W_KIND_F16) {
-          bulk_g2s(st + b_bytes, (const uint8_t *)J.w + tile * 16384, 16384, full0 + 8 * s);
-        } else {
-          bulk_g2s(st + b_bytes, (const uint8_t *)J.w + tile * 4096, 4096, full0 + 8 * s);
-          bulk_g2s(st + b_bytes + 4096, (const uint8_t *)J.s + tile * DU * 256, DU * 256, full0 + 8 * s);
-        }
       }
       // every stage released by every consumer (no copy or remote arrive still bound for this CTA)
       if (ok)
@@ -245,7 +316,7 @@ __global__ void __launch_bounds__(W_THREADS, 1) k_wide(WideArgs A) {
   } else if (warp < 4) {
     const int r = warp * 32 + lane;
     const uint32_t lrow = (uint32_t)(warp * 32) << 16;
-    int i = 0, run = 0;
+    int i = 0, run = 0, ephase = 0;
     bool ok = true;
     for (int64_t u = u0; u < u1 && ok; ++run) {
       const int64_t ue = wrun_end(A, u, u1);
@@ -317,20 +388,55 @@ __global__ void __launch_bounds__(W_THREADS, 1) k_wide(WideArgs A) {
       const int d = run % C::NBUF;
       if (!__all_sync(0xffffffffu, mbar_wait(dfull0 + 8 * d, (run / C::NBUF) & 1))) break;
       tc_fence_after();
-      const int row = m * 128 + r;
-      const bool live = !w0.ghost && row < J.n;
-      float *y = J.y + A.y_off + row;
+      // a run over the whole k-range owns its outputs; the others add into cleared ones
+      const bool whole = (ue - u) == A.KT;
+      const int row0 = m * 128;
+      const int rows = min(128, J.n - row0);
+      float *ybase = J.y + A.y_off + row0;
       const int tok0 = w0.tt * N;
-      for (int c0 = 0; c0 < N; c0 += 16) {
-        uint32_t v16[16];
-        tmem_ld16(tbase + lrow + d * 256 + c0, v16);
-        tc_wait_ld();
-        if (live) {
+      const int ntok = min(N, A.T - tok0);
+      const bool bulk = (rows & 3) == 0 && (J.ldy & 3) == 0 && (((uintptr_t)ybase) & 15) == 0;
+      if (w0.ghost) {
+        // nothing to write
+      } else if (bulk) {
+        // 16 tokens at a time: TMEM -> registers -> a [token][row] slice in shared
+        // memory; then each warp writes 4 whole token rows, 16 bytes a lane
+        // (vector stores, or vector atomic adds for a split tile)
+        for (int c0 = 0, ci = 0; c0 < N && ok; c0 += 16, ++ci) {
+          float *stg = staging + (ci & 1) * 16 * 128;
+          uint32_t v16[16];
+          tmem_ld16(tbase + lrow + d * 256 + c0, v16);
+          tc_wait_ld();
 #pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            const int tok = tok0 + c0 + e;
-            if (tok < A.T) atomicAdd(y + (int64_t)tok * J.ldy, __uint_as_float(v16[e]) * unscale);
+          for (int e = 0; e < 16; ++e) stg[e * 128 + r] = __uint_as_float(v16[e]) * unscale;
+          ok = drain_bar(ebar, ephase);
+          if (4 * lane < rows) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const int e = warp * 4 + q;
+              if (c0 + e < ntok) {
+                const float4 v = *(const float4 *)(stg + e * 128 + 4 * lane);
+                float4 *dst = (float4 *)(ybase + (int64_t)(tok0 + c0 + e) * J.ldy) + lane;
+                if (whole) *dst = v;
+                else atomicAdd(dst, v);
+              }
+            }
           }
+        }
+        ok = __all_sync(0xffffffffu, ok);
+      } else {
+        const bool live = r < rows;
+        float *y = ybase + r;
+        for (int c0 = 0; c0 < N; c0 += 16) {
+          uint32_t v16[16];
+          tmem_ld16(tbase + lrow + d * 256 + c0, v16);
+          tc_wait_ld();
+          if (live)
+            for (int e = 0; e < 16 && c0 + e < ntok; ++e) {
+              const float v = __uint_as_float(v16[e]) * unscale;
+              if (whole) y[(int64_t)(tok0 + c0 + e) * J.ldy] = v;
+              else atomicAdd(y + (int64_t)(tok0 + c0 + e) * J.ldy, v);
+            }
         }
       }
       tc_fence_before();
@@ -338,6 +444,7 @@ __global__ void __launch_bounds__(W_THREADS, 1) k_wide(WideArgs A) {
       u = ue;
     }
   }
+  pdl_trigger();  // this CTA's work is done
   tc_fence_before();
   __syncthreads();
   if (warp == 0) {
@@ -362,72 +469,102 @@ size_t wide_act_bytes(int T, int K, bool int4) {
   return (size_t)ntt * N * K * 2 * (int4 ? 2 : 1);
 }
 
-// CTAs sharing each token tile (multicast); 1 = no cluster.
-#ifndef W_CLUSTER
-#define W_CLUSTER 2
-#endif
+// The token tiles (blocks < pack_blocks) and the clearing of the row tiles
+// that a boundary between two clusters' ranges splits (their runs add into the
+// outputs; runs over a whole k-range store). Clearing block b takes boundary
+// b / (CL * WZ_PARTS), row tile (b / WZ_PARTS) % CL of its group and a part
+// of the tile's token rows.
+constexpr int WZ_PARTS = 8;
+
+template <int PLANES>
+__global__ void k_wide_pack(const float *__restrict__ X, int ldx, WideArgs A, int Q, int CL, uint4 *__restrict__ dst,
+                            int pack_blocks) {
+  pdl_wait();
+  pdl_trigger();
+  if ((int)blockIdx.x < pack_blocks) {
+    const int64_t total = (int64_t)A.ntt * A.KT * A.N * 8;
+    const int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (t < total) pack_act_chunk<PLANES>(X, ldx, A.T, A.K, A.N, dst, t);
+    return;
+  }
+  const int zb = blockIdx.x - pack_blocks;
+  const int part = zb % WZ_PARTS, c = (zb / WZ_PARTS) % CL, q = zb / (WZ_PARTS * CL) + 1;
+  const int64_t u = (int64_t)q * A.units / Q;
+  if (u % A.KT == 0) return;
+  // the tile group was cleared for the boundary before if that one split it too
+  const int64_t up = (int64_t)(q - 1) * A.units / Q;
+  if (q > 1 && up % A.KT != 0 && up / A.KT == u / A.KT) return;
+  const int groups = (A.mtiles + CL - 1) / CL;
+  const int64_t tg = u / A.KT;
+  const int tt = (int)(tg / groups), g = (int)(tg % groups);
+  const int mt = g * CL + c;
+  if (mt >= A.mtiles) return;
+  int lo = 0, hi = A.njobs - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (A.job[mid].tile0 <= mt) lo = mid;
+    else hi = mid - 1;
+  }
+  const WideJob J = A.job[lo];
+  const int row0 = (mt - J.tile0) * 128;
+  const int rows = min(128, J.n - row0);
+  const int toks = min(A.N, A.T - tt * A.N);
+  const int per = (toks + WZ_PARTS - 1) / WZ_PARTS;
+  const int t0 = part * per, t1 = min(toks, t0 + per);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+  float *base = J.y + A.y_off + (int64_t)(tt * A.N) * J.ldy + row0;
+  const bool v4 = rows == 128 && (J.ldy & 3) == 0 && (((uintptr_t)base) & 15) == 0;
+  for (int t = t0 + warp; t < t1; t += nw) {
+    float *y = base + (int64_t)t * J.ldy;
+    if (v4) ((float4 *)y)[lane] = make_float4(0.f, 0.f, 0.f, 0.f);
+    else
+      for (int r = lane; r < rows; r += 32) y[r] = 0.f;
+  }
+}
 
 // Runs of at least this many units: a run ends with a read-back of its accumulator.
 constexpr int W_MIN_RUN = 4;
+// CTAs sharing each token tile (multicast).
+constexpr int W_CLUSTER = 2;
 
 template <int KIND, int DU, int CL>
-static cudaError_t launch_wide(WideArgs &A, int num_sms, cudaStream_t st) {
+static cudaError_t launch_wide(WideArgs &A, const float *X, int ldx, void *act, int num_sms, cudaStream_t st) {
   using C = WCfg<KIND, DU>;
   static int max_clusters = 0;
   auto kern = k_wide<KIND, DU, CL>;
   if (max_clusters == 0) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
-    if (CL > 1) {
-      e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 0);
-      cudaLaunchConfig_t cfg = {};
-      cudaLaunchAttribute at[1];
-      at[0].id = cudaLaunchAttributeClusterDimension;
-      at[0].val.clusterDim.x = CL;
-      at[0].val.clusterDim.y = 1;
-      at[0].val.clusterDim.z = 1;
-      cfg.gridDim = dim3(CL * num_sms);
-      cfg.blockDim = dim3(W_THREADS);
-      cfg.dynamicSmemBytes = C::SMEM;
-      cfg.attrs = at;
-      cfg.numAttrs = 1;
-      int n = 0;
-      e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
-      if (e != cudaSuccess) return e;
-      max_clusters = std::max(1, n);
-    } else {
-      max_clusters = num_sms;
-    }
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = CL;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3(CL * num_sms);
+    cfg.blockDim = dim3(W_THREADS);
+    cfg.dynamicSmemBytes = C::SMEM;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    int n = 0;
+    e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
+    if (e != cudaSuccess) return e;
+    max_clusters = std::max(1, n);
   }
   const int groups = (A.mtiles + CL - 1) / CL;
   A.units = (int64_t)A.ntt * groups * A.KT;
-  const int64_t clusters = std::max<int64_t>(1, std::min<int64_t>(max_clusters, A.units / W_MIN_RUN));
-  cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute at[1];
-  at[0].id = cudaLaunchAttributeClusterDimension;
-  at[0].val.clusterDim.x = CL;
-  at[0].val.clusterDim.y = 1;
-  at[0].val.clusterDim.z = 1;
-  cfg.gridDim = dim3((unsigned)(clusters * CL));
-  cfg.blockDim = dim3(W_THREADS);
-  cfg.dynamicSmemBytes = C::SMEM;
-  cfg.stream = st;
-  cfg.attrs = at;
-  cfg.numAttrs = 1;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, A);
-  count_launch(1);
-  return e != cudaSuccess ? e : cudaGetLastError();
+  const int Q = (int)std::max<int64_t>(1, std::min<int64_t>(max_clusters, A.units / W_MIN_RUN));
+  const int64_t chunks = (int64_t)A.ntt * A.KT * A.N * 8;
+  const int pack_blocks = (int)((chunks + 255) / 256);
+  const int zero_blocks = (Q - 1) * CL * WZ_PARTS;
+  cudaError_t e = launch_pdl(k_wide_pack<C::PLANES>, dim3(pack_blocks + zero_blocks), dim3(256), 0, st, 1, X, ldx, A, Q,
+                             CL, (uint4 *)act, pack_blocks);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(kern, dim3((unsigned)(Q * CL)), dim3(W_THREADS), C::SMEM, st, CL, A);
 }
 
-// Pack X into token tiles of N rows (f16 planes, 128-byte swizzled k-tiles).
-cudaError_t wide_pack(const float *X, int ldx, int T, int K, bool int4, void *act, cudaStream_t st) {
-  int ntt, N;
-  wide_tiles(T, ntt, N);
-  return pack_act(X, ldx, T, K, N, int4 ? 2 : 1, act, st);
-}
-
-cudaError_t wide_gemm(const WideJob *jobs, int njobs, int64_t y_off, bool int4, int group, const void *act, int T,
-                      int K, int num_sms, cudaStream_t st) {
+cudaError_t wide_gemm(const WideJob *jobs, int njobs, int64_t y_off, bool int4, int group, const float *X, int ldx,
+                      int T, int K, void *act, int num_sms, cudaStream_t st) {
   if (njobs < 1 || njobs > WIDE_MAX_JOBS || T < 1 || K % 64) return cudaErrorInvalidValue;
   WideArgs A{};
   A.njobs = njobs;
@@ -443,39 +580,9 @@ cudaError_t wide_gemm(const WideJob *jobs, int njobs, int64_t y_off, bool int4, 
   A.KT = K / 64;
   A.T = T;
   wide_tiles(T, A.ntt, A.N);
-  if (!int4) return launch_wide<W_KIND_F16, 1, W_CLUSTER>(A, num_sms, st);
-  return group >= 64 ? launch_wide<W_KIND_I4, 1, W_CLUSTER>(A, num_sms, st)
-                     : launch_wide<W_KIND_I4, 2, W_CLUSTER>(A, num_sms, st);
-}
-
-// ---------------------------------------------------------------- clearing the outputs
-
-struct ZeroArgs {
-  float *y[WIDE_MAX_JOBS];
-  int ld[WIDE_MAX_JOBS];
-};
-
-// Clear rows [0, T) of output blockIdx.y.
-__global__ void k_wide_zero(ZeroArgs Z, int T) {
-  float *y = Z.y[blockIdx.y];
-  const int64_t n = (int64_t)T * Z.ld[blockIdx.y];
-  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
-    y[i] = 0.f;
-}
-
-cudaError_t wide_zero(const WideJob *jobs, int njobs, int64_t y_off, int T, cudaStream_t st) {
-  if (njobs < 1 || njobs > WIDE_MAX_JOBS) return cudaErrorInvalidValue;
-  ZeroArgs Z{};
-  int64_t most = 0;
-  for (int j = 0; j < njobs; ++j) {
-    Z.y[j] = jobs[j].y + y_off;
-    Z.ld[j] = jobs[j].ldy;
-    most = std::max<int64_t>(most, (int64_t)T * jobs[j].ldy);
-  }
-  dim3 grid((unsigned)std::min<int64_t>((most + 255) / 256, 64), njobs);
-  k_wide_zero<<<grid, 256, 0, st>>>(Z, T);
-  count_launch(1);
-  return cudaGetLastError();
+  if (!int4) return launch_wide<W_KIND_F16, 1, W_CLUSTER>(A, X, ldx, act, num_sms, st);
+  return group >= 64 ? launch_wide<W_KIND_I4, 1, W_CLUSTER>(A, X, ldx, act, num_sms, st)
+                     : launch_wide<W_KIND_I4, 2, W_CLUSTER>(A, X, ldx, act, num_sms, st);
 }
 
 }  // namespace dfl
