@@ -19,23 +19,26 @@ namespace dfl {
 constexpr int ATT_THREADS = 256;
 constexpr int CH = 64;              // keys per chunk
 constexpr int QMAX = 64;            // queries per CTA (rep * block)
-constexpr int TARGET_CTAS = 320;    // split-K aims at about this many CTAs
+// Split-K aims at one wave: a CTA (about 170 KB of shared memory) per SM.
 
 struct AttnArgs {
   AttnSeq seq[MAX_BATCH];
 };
 
-// Chunks a split takes: enough splits for ~TARGET_CTAS CTAs over all (sequence, KV head).
-static int chunks_per_split(int batch, int kv, int max_n) {
+// Chunks a split takes: one wave of the context's CTAs over the SMs that the
+// block's own CTAs (one per sequence and KV head) leave free.
+static int chunks_per_split(int batch, int kv, int max_n, int num_sms) {
   const int chunks = (max_n + CH - 1) / CH;
   const int units = batch * kv * chunks;
-  return std::max(1, (units + TARGET_CTAS - 1) / TARGET_CTAS);
+  const int ctas = std::max(num_sms - batch * kv, batch * kv);
+  return std::max(1, (units + ctas - 1) / ctas);
 }
 
 size_t attn_partial_bytes(int max_batch, int kv_heads, int heads, int block, int hd) {
   const int Q = heads / kv_heads * block;
-  // splits per (sequence, KV head) <= TARGET_CTAS / (batch * kv) + 1, plus the block's own
-  const size_t worst = (size_t)TARGET_CTAS + 2 * (size_t)max_batch * kv_heads;
+  // per (sequence, KV head): at most ceil(units / ctas) + 1 context splits (ctas >= batch * kv), plus
+  // the block's own; bounded for any SM count up to 1024
+  const size_t worst = (size_t)1024 + 3 * (size_t)max_batch * kv_heads;
   return worst * Q * (hd + 2) * sizeof(float);
 }
 
@@ -122,17 +125,30 @@ __global__ void __launch_bounds__(ATT_THREADS) k_attn(const float *__restrict__ 
   };
   if (kbeg < kend) stage(kbeg);
 
-  // the queries, hi/lo
-  for (int i = tid; i < QMAX * HD; i += ATT_THREADS) {
-    const int qi = i / HD, d = i % HD;
-    float x = 0.f;
-    if (qi < Q) {
-      const int hrep = qi / R, r = qi % R;
-      x = q[((int64_t)b * R + r) * heads * HD + (g * rep + hrep) * HD + d];
+  // the queries, hi/lo: every load of the thread first, then the conversions
+  {
+    constexpr int PER = QMAX * HD / 4 / ATT_THREADS;  // float4 a thread
+    float4 xv[PER];
+#pragma unroll
+    for (int m = 0; m < PER; ++m) {
+      const int i = tid + m * ATT_THREADS;
+      const int qi = i / (HD / 4), d4 = i % (HD / 4);
+      xv[m] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (qi < Q) {
+        const int hrep = qi / R, r = qi - hrep * R;
+        xv[m] = *(const float4 *)(q + ((int64_t)b * R + r) * heads * HD + (g * rep + hrep) * HD + 4 * d4);
+      }
     }
-    const __half h = __float2half_rn(x);
-    Qh[qi * SM::LD + d] = h;
-    Ql[qi * SM::LD + d] = __float2half_rn(x - __half2float(h));
+#pragma unroll
+    for (int m = 0; m < PER; ++m) {
+      const int i = tid + m * ATT_THREADS;
+      const int qi = i / (HD / 4), d4 = i % (HD / 4);
+      uint32_t h0, l0, h1, l1;
+      split2(xv[m].x, xv[m].y, h0, l0);
+      split2(xv[m].z, xv[m].w, h1, l1);
+      *(uint2 *)(Qh + qi * SM::LD + 4 * d4) = make_uint2(h0, h1);
+      *(uint2 *)(Ql + qi * SM::LD + 4 * d4) = make_uint2(l0, l1);
+    }
   }
 
   float o[OT][4];
@@ -273,22 +289,30 @@ __global__ void __launch_bounds__(ATT_THREADS) k_attn(const float *__restrict__ 
   }
   __syncthreads();
   float *out = part + ((int64_t)(b * kv + g) * (nsplit + 1) + sp) * Q * (HD + 2);
-  for (int i = tid; i < Q * (HD + 2); i += ATT_THREADS) {
-    const int qi = i / (HD + 2), c = i % (HD + 2);
+  // one warp per query row at a time: the key groups' weights once, then the row
+  for (int qi = warp; qi < Q; qi += ATT_THREADS / 32) {
     const int qbk = qi / 16, rr = qi % 16;
     float M = -INFINITY;
+#pragma unroll
     for (int kg = 0; kg < KG; ++kg) M = fmaxf(M, scr[(kg * QW + qbk) * 16 * (HD + 2) + rr * (HD + 2) + HD]);
-    float acc = 0.f;
-    if (c == HD) {
-      acc = M;
-    } else {
-      for (int kg = 0; kg < KG; ++kg) {
-        const float *w = scr + (kg * QW + qbk) * 16 * (HD + 2) + rr * (HD + 2);
-        if (w[HD] == -INFINITY) continue;
-        acc = fmaf(w[c], expf(w[HD] - M), acc);  // c < HD: o; c == HD + 1: l
-      }
+    float wt[KG];
+#pragma unroll
+    for (int kg = 0; kg < KG; ++kg) {
+      const float mk = scr[(kg * QW + qbk) * 16 * (HD + 2) + rr * (HD + 2) + HD];
+      wt[kg] = mk == -INFINITY ? 0.f : expf(mk - M);
     }
-    out[i] = acc;
+    float *orow = out + (int64_t)qi * (HD + 2);
+    for (int c = lane; c < HD + 2; c += 32) {
+      float acc = 0.f;
+      if (c == HD) {
+        acc = M;
+      } else {
+#pragma unroll
+        for (int kg = 0; kg < KG; ++kg)
+          acc = fmaf(scr[(kg * QW + qbk) * 16 * (HD + 2) + rr * (HD + 2) + c], wt[kg], acc);  // o, or l at HD + 1
+      }
+      orow[c] = acc;
+    }
   }
 }
 
@@ -321,7 +345,7 @@ __global__ void k_attn_merge(const float *__restrict__ part, int heads, int kv, 
 template <int HD, int KG>
 static cudaError_t launch_attn(const float *q, const float *k, const float *v, const AttnArgs &args, int batch,
                                int max_n, int heads, int kv, int R, int window, float scale, float *part, float *y,
-                               cudaStream_t st) {
+                               int num_sms, cudaStream_t st) {
   const size_t smem = AttnSmem<HD>::BYTES;
   static bool configured = false;
   if (!configured) {
@@ -329,7 +353,7 @@ static cudaError_t launch_attn(const float *q, const float *k, const float *v, c
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  const int cps = chunks_per_split(batch, kv, max_n);
+  const int cps = chunks_per_split(batch, kv, max_n, num_sms);
   const int ns = max_n > 0 ? ((max_n + CH - 1) / CH + cps - 1) / cps : 0;
   dim3 grid(ns + 1, kv, batch);
   cudaError_t e = launch_pdl(k_attn<HD, KG>, grid, dim3(ATT_THREADS), smem, st, 1, q, k, v, args, heads, kv, R, window,
@@ -343,15 +367,16 @@ static cudaError_t launch_attn(const float *q, const float *k, const float *v, c
 template <int HD>
 static cudaError_t launch_attn_hd(const float *q, const float *k, const float *v, const AttnArgs &args, int batch,
                                   int max_n, int heads, int kv, int R, int window, float scale, float *part, float *y,
-                                  cudaStream_t st) {
+                                  int num_sms, cudaStream_t st) {
   const int QW = (heads / kv * R + 15) / 16;
-  if (QW >= 3) return launch_attn<HD, 2>(q, k, v, args, batch, max_n, heads, kv, R, window, scale, part, y, st);
-  return launch_attn<HD, 4>(q, k, v, args, batch, max_n, heads, kv, R, window, scale, part, y, st);
+  if (QW >= 3)
+    return launch_attn<HD, 2>(q, k, v, args, batch, max_n, heads, kv, R, window, scale, part, y, num_sms, st);
+  return launch_attn<HD, 4>(q, k, v, args, batch, max_n, heads, kv, R, window, scale, part, y, num_sms, st);
 }
 
 cudaError_t attention(const float *q, const float *k, const float *v, const AttnSeq *seqs, int batch, int max_ctx,
                       int heads, int kv_heads, int hd, int block, int window, float scale, float *partials, float *y,
-                      cudaStream_t st) {
+                      int num_sms, cudaStream_t st) {
   (void)max_ctx;
   if (batch > MAX_BATCH || heads / kv_heads * block > QMAX) return cudaErrorInvalidValue;
   AttnArgs args;
@@ -364,8 +389,13 @@ cudaError_t attention(const float *q, const float *k, const float *v, const Attn
       args.seq[i] = AttnSeq{nullptr, nullptr, 0, 0, 0};
     }
   }
-  if (hd == 128) return launch_attn_hd<128>(q, k, v, args, batch, max_n, heads, kv_heads, block, window, scale, partials, y, st);
-  if (hd == 64) return launch_attn_hd<64>(q, k, v, args, batch, max_n, heads, kv_heads, block, window, scale, partials, y, st);
+  num_sms = std::max(1, std::min(num_sms, 1024));
+  if (hd == 128)
+    return launch_attn_hd<128>(q, k, v, args, batch, max_n, heads, kv_heads, block, window, scale, partials, y, num_sms,
+                               st);
+  if (hd == 64)
+    return launch_attn_hd<64>(q, k, v, args, batch, max_n, heads, kv_heads, block, window, scale, partials, y, num_sms,
+                              st);
   return cudaErrorInvalidValue;
 }
 

@@ -405,7 +405,8 @@ int dflash_block(dflash_t *d, int32_t batch, const int64_t *anchor_pos, const fl
       seqs[b].lo = lo;
       seqs[b].anchor = a;
     }
-    DF_CUDA(dfl::attention(d->q, d->k, d->v, seqs.data(), batch, 0, nh, kv, hd, R, W, scale, d->part, d->y, st));
+    DF_CUDA(dfl::attention(d->q, d->k, d->v, seqs.data(), batch, 0, nh, kv, hd, R, W, scale, d->part, d->y,
+                           d->num_sms, st));
     const dfl::TcJob oj{L.o.data, L.o.scales, d->o, hs, hs};
     DF_CUDA(dfl::tc_gemm_int4(&oj, 1, grp, d->y, qd, T, qd, d->act, sms, st));
     DF_CUDA(dfl::conv_stage1_residual(d->o, d->d, L.attn_base, d->h, T, hs, kn, gs, R, st));

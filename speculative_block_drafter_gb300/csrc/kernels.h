@@ -149,7 +149,7 @@ size_t attn_partial_bytes(int max_batch, int kv_heads, int heads, int block, int
 // `seqs` is a host array of `batch` entries (passed by value).
 cudaError_t attention(const float *q, const float *k, const float *v, const AttnSeq *seqs, int batch,
                       int max_ctx, int heads, int kv_heads, int hd, int block, int window, float scale,
-                      float *partials, float *y, cudaStream_t st);
+                      float *partials, float *y, int num_sms, cudaStream_t st);
 
 // -------------------------------------------------------------- selector (select.cu)
 size_t select_scratch_bytes(int max_rows, int width, int top);
