@@ -21,6 +21,7 @@
 // (pre-swizzled by the packer) and the tokens enter rounded to f16 (the card
 // arm's `to_half`); one accumulator spans the CTA's k-range.
 #include <algorithm>
+#include <climits>
 
 #include "common.cuh"
 #include "kernels.h"
@@ -209,18 +210,26 @@ struct I4 {
   static constexpr int SMEM = S * STAGE + 1024 + 512;
 };
 
+// The units of a launch, (token tile, group of MT row tiles, k-tile), laid end
+// to end; CTA b takes units [b U / grid, (b + 1) U / grid) ("stream-K"), as runs
+// that each stay inside one group's k-range. A run over the whole k-range
+// stores its rows; a shorter one adds them into outputs cleared beforehand.
 struct I4Items {
   int groups;       // row-tile groups over all jobs
   int gtile0[MAX_JOBS + 1];
-  int splits, kc, ntt, items;
+  int ntt;
+  int units;        // < 2^31 (checked at launch)
+  int whole;        // CTA ranges at group boundaries (when there are as many groups as CTAs)
 };
 
-__device__ __forceinline__ void i4_item(const TcJobs &J, const I4Items &P, int MT, int KT, int it, int &job, int &m0,
-                                        int &mtv, int &tt, int &kt0, int &kt1) {
-  const int sp = it % P.splits;
-  const int rest = it / P.splits;
-  const int mg = rest % P.groups;
-  tt = rest / P.groups;
+// The run that starts at unit u and ends at the group's last k-tile or at u1.
+__device__ __forceinline__ void i4_run(const TcJobs &J, const I4Items &P, int MT, int KT, int u, int u1, int &job,
+                                       int &m0, int &mtv, int &tt, int &kt0, int &kt1) {
+  const int tg = u / KT;
+  kt0 = u - tg * KT;
+  const int mg = tg % P.groups;
+  tt = tg / P.groups;
+  kt1 = min(KT, kt0 + (u1 - u));
   job = 0;
 #pragma unroll
   for (int i = 1; i < MAX_JOBS; ++i)
@@ -228,13 +237,11 @@ __device__ __forceinline__ void i4_item(const TcJobs &J, const I4Items &P, int M
   m0 = (mg - P.gtile0[job]) * MT;
   const int tiles = J.tile0[job + 1] - J.tile0[job];
   mtv = min(MT, tiles - m0);
-  kt0 = sp * P.kc;
-  kt1 = min(KT, kt0 + P.kc);
 }
 
 template <int TT, int DU, int MT, int SA>
 __global__ void __launch_bounds__(I4_MAX_THREADS, 2) k_tc_int4(TcJobs J, I4Items P, const uint8_t *__restrict__ bpack,
-                                                               int K, int T, int atomic_out) {
+                                                               int K, int T) {
   using C = I4<TT, DU, MT, SA>;
   extern __shared__ __align__(1024) uint8_t smraw[];
   uint8_t *sm = smraw + ((1024 - (smem_u32(smraw) & 1023)) & 1023);
@@ -244,6 +251,15 @@ __global__ void __launch_bounds__(I4_MAX_THREADS, 2) k_tc_int4(TcJobs J, I4Items
   const uint32_t afree0 = afull0 + 8 * C::SA, dfull0 = afree0 + 8 * C::SA, dfree0 = dfull0 + 8 * C::NDU;
   const int KT = K / 64;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  int ru0, ru1;
+  if (P.whole) {
+    const int ng = P.units / KT;
+    ru0 = (int)((int64_t)blockIdx.x * ng / gridDim.x) * KT;
+    ru1 = (int)((int64_t)(blockIdx.x + 1) * ng / gridDim.x) * KT;
+  } else {
+    ru0 = (int)((int64_t)blockIdx.x * P.units / gridDim.x);
+    ru1 = (int)((int64_t)(blockIdx.x + 1) * P.units / gridDim.x);
+  }
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::S; ++i) {
@@ -265,9 +281,9 @@ __global__ void __launch_bounds__(I4_MAX_THREADS, 2) k_tc_int4(TcJobs J, I4Items
   // codes and scales are fetched before waiting for them.
   int npre = 0;
   if (warp == I4_PRODUCER && lane == 0) {
-    for (int it = blockIdx.x; it < P.items && npre < C::S; it += gridDim.x) {
-      int job, m0, mtv, tt, kt0, kt1;
-      i4_item(J, P, MT, KT, it, job, m0, mtv, tt, kt0, kt1);
+    int job, m0, mtv, tt, kt0, kt1;
+    for (int pu = ru0; pu < ru1 && npre < C::S; pu += kt1 - kt0) {
+      i4_run(J, P, MT, KT, pu, ru1, job, m0, mtv, tt, kt0, kt1);
       const uint8_t *wc = (const uint8_t *)J.w[job] + (int64_t)m0 * KT * 4096;
       const uint8_t *ws = (const uint8_t *)J.s[job] + (int64_t)m0 * KT * DU * 256;
       for (int kt = kt0; kt < kt1 && npre < C::S; ++kt, ++npre) {
@@ -292,9 +308,9 @@ __global__ void __launch_bounds__(I4_MAX_THREADS, 2) k_tc_int4(TcJobs J, I4Items
     if (lane == 0) {
       int i = 0;
       bool ok = true;
-      for (int it = blockIdx.x; it < P.items && ok; it += gridDim.x) {
-        int job, m0, mtv, tt, kt0, kt1;
-        i4_item(J, P, MT, KT, it, job, m0, mtv, tt, kt0, kt1);
+      int job, m0, mtv, tt, kt0, kt1;
+      for (int pu = ru0; pu < ru1 && ok; pu += kt1 - kt0) {
+        i4_run(J, P, MT, KT, pu, ru1, job, m0, mtv, tt, kt0, kt1);
         const uint8_t *wc = (const uint8_t *)J.w[job] + (int64_t)m0 * KT * 4096;
         const uint8_t *ws = (const uint8_t *)J.s[job] + (int64_t)m0 * KT * DU * 256;
         const uint8_t *bp = bpack + (int64_t)tt * KT * C::B_BYTES;
@@ -324,9 +340,9 @@ __global__ void __launch_bounds__(I4_MAX_THREADS, 2) k_tc_int4(TcJobs J, I4Items
       constexpr int KSU = 4 / DU;
       int i = 0, u = 0;
       bool ok = true;
-      for (int it = blockIdx.x; it < P.items && ok; it += gridDim.x) {
-        int job, m0, mtv, tt, kt0, kt1;
-        i4_item(J, P, MT, KT, it, job, m0, mtv, tt, kt0, kt1);
+      int job, m0, mtv, tt, kt0, kt1;
+      for (int pu = ru0; pu < ru1 && ok; pu += kt1 - kt0) {
+        i4_run(J, P, MT, KT, pu, ru1, job, m0, mtv, tt, kt0, kt1);
         const bool live = jj < mtv;
         for (int kt = kt0; kt < kt1 && ok; ++kt, ++i) {
           const int s = i % C::S, a = i % C::SA;
@@ -363,9 +379,9 @@ __global__ void __launch_bounds__(I4_MAX_THREADS, 2) k_tc_int4(TcJobs J, I4Items
     const uint32_t lrow = (uint32_t)(warp * 32) << 16;
     int i = 0;
     bool ok = true;
-    for (int it = blockIdx.x; it < P.items && ok; it += gridDim.x) {
-      int job, m0, mtv, tt, kt0, kt1;
-      i4_item(J, P, MT, KT, it, job, m0, mtv, tt, kt0, kt1);
+    int job, m0, mtv, tt, kt0, kt1;
+    for (int pu = ru0; pu < ru1 && ok; pu += kt1 - kt0) {
+      i4_run(J, P, MT, KT, pu, ru1, job, m0, mtv, tt, kt0, kt1);
       for (int kt = kt0; kt < kt1; ++kt, ++i) {
         const int s = i % C::S, a = i % C::SA;
         if (!__all_sync(0xffffffffu, mbar_wait(full0 + 8 * s, (i / C::S) & 1))) {
@@ -413,9 +429,9 @@ __global__ void __launch_bounds__(I4_MAX_THREADS, 2) k_tc_int4(TcJobs J, I4Items
       for (int t = 0; t < TT; ++t) acc[jj][t] = 0.f;
     int i = 0, u = 0;
     bool ok = true;
-    for (int it = blockIdx.x; it < P.items && ok; it += gridDim.x) {
-      int job, m0, mtv, tt, kt0, kt1;
-      i4_item(J, P, MT, KT, it, job, m0, mtv, tt, kt0, kt1);
+    int job, m0, mtv, tt, kt0, kt1;
+    for (int pu = ru0; pu < ru1 && ok; pu += kt1 - kt0) {
+      i4_run(J, P, MT, KT, pu, ru1, job, m0, mtv, tt, kt0, kt1);
       for (int kt = kt0; kt < kt1 && ok; ++kt, ++i) {
         const int s = i % C::S;
         if (!__all_sync(0xffffffffu, mbar_wait(full0 + 8 * s, (i / C::S) & 1))) {
@@ -473,7 +489,7 @@ __global__ void __launch_bounds__(I4_MAX_THREADS, 2) k_tc_int4(TcJobs J, I4Items
           for (int t = 0; t < TT; ++t) {
             const int tok = tt * TT + t;
             if (tok < T) {
-              if (atomic_out) atomicAdd(y + (int64_t)tok * ldy + row, acc[jj][t]);
+              if (kt1 - kt0 < KT) atomicAdd(y + (int64_t)tok * ldy + row, acc[jj][t]);
               else y[(int64_t)tok * ldy + row] = acc[jj][t];
             }
           }
@@ -779,14 +795,25 @@ static cudaError_t launch_int4(const TcJobs &J, int njobs, const float *X, int l
   P.gtile0[njobs] = P.groups;
   P.ntt = ntt;
   const int KT = K / 64;
-  // enough items for two CTAs an SM, each at least 8 k-tiles long
-  plan(ntt, P.groups, KT, num_sms, 8, P.kc, P.splits);
-  P.items = ntt * P.groups * P.splits;
-  e = launch_pack(X, ldx, T, K, TT, 2, act, jobs, njobs, P.splits > 1, st);
+  const int64_t units = (int64_t)ntt * P.groups * KT;
+  if (units >= INT32_MAX) return cudaErrorInvalidValue;
+  P.units = (int)units;
+  // two CTAs an SM, each at least 8 units long; whole groups a CTA when there are enough of them
+  const int ngroups = ntt * P.groups;
+  int grid;
+  bool split = false;
+  if (ngroups >= 2 * num_sms) {
+    P.whole = 1;
+    grid = 2 * num_sms;
+  } else {
+    P.whole = 0;
+    grid = (int)std::max<int64_t>(1, std::min<int64_t>(2 * num_sms, P.units / 8));
+    for (int b = 1; b < grid && !split; ++b) split = ((int64_t)b * P.units / grid) % KT != 0;
+  }
+  e = launch_pack(X, ldx, T, K, TT, 2, act, jobs, njobs, split, st);
   if (e != cudaSuccess) return e;
-  const int grid = std::min(P.items, 2 * num_sms);
   return launch_pdl(k_tc_int4<TT, DU, MT, SA>, dim3(grid), dim3(C::THREADS), C::SMEM, st, 1, J, P,
-                    (const uint8_t *)act, K, T, (int)(P.splits > 1));
+                    (const uint8_t *)act, K, T);
 }
 
 cudaError_t tc_gemm_int4(const TcJob *jobs, int njobs, int group, const float *X, int ldx, int T, int K, void *act,
