@@ -190,10 +190,10 @@ int dflash_select(dflash_t *d, int32_t batch, const float *logits, const float *
  * arguments and outputs, the codebooks f16 [vocab][rank] and the sizes passed
  * directly, no drafter handle) and needs no workspace: its candidate scratch
  * is a fixed 8 MiB array inside the library, held by every GPU that loads the
- * library until the process exits, so a call's chunk maxima, candidates and
- * score tables, batch * k * (ceil(width / 2048) * 8 + top * 4 + top * top * 4)
- * + 256 bytes, must fit in 8 MiB (else DFLASH_E_CAPACITY; dflash_select has no
- * such limit). The first call
+ * library until the process exits, so a call's chunk maxima, candidate lists
+ * and score tables, batch * k * (ceil(width / 2048) * 8 + 8200 + top * 4 +
+ * top * top * 4) + 256 bytes, must fit in 8 MiB (else DFLASH_E_CAPACITY;
+ * dflash_select has no such limit). The first call
  * on a device looks up that device's address of the array
  * (cudaGetSymbolAddress); make that first call before any stream capture.
  * Every call on a device shares the one array, so calls that overlap on the

@@ -441,7 +441,7 @@ int dflash_select(dflash_t *d, int32_t batch, const float *logits, const float *
   if (width < g.selector_top || width > g.vocab) return fail(DFLASH_E_ARG, "select: width must be selector_top..vocab");
   if (!logits || !hp || !anchor_tok || !chosen || !plain) return fail(DFLASH_E_ARG, "select: null pointer");
   DF_CUDA(dfl::select_tokens(logits, hp, anchor_tok, d->w.pred_book, d->w.succ_book, batch, k, width, g.selector_rank,
-                             g.selector_top, g.vocab, d->sel, chosen, plain, (cudaStream_t)stream));
+                             g.selector_top, g.vocab, d->sel, chosen, plain, d->num_sms, (cudaStream_t)stream));
   return DFLASH_OK;
 }
 

@@ -155,6 +155,7 @@ cudaError_t attention(const float *q, const float *k, const float *v, const Attn
 size_t select_scratch_bytes(int max_rows, int width, int top);
 cudaError_t select_tokens(const float *logits, const float *hp, const uint32_t *anchor_tok,
                           const uint16_t *pred, const uint16_t *succ, int batch, int k, int width, int rank,
-                          int top, int vocab, void *scratch, uint32_t *chosen, uint32_t *plain, cudaStream_t st);
+                          int top, int vocab, void *scratch, uint32_t *chosen, uint32_t *plain, int num_sms,
+                          cudaStream_t st);
 
 }  // namespace dfl

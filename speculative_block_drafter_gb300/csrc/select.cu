@@ -6,16 +6,18 @@
 //
 // Stage 1 (chunks x rows CTAs): the largest key (value, then lower index) of
 // each chunk of 2048 logits.
-// Stage 2 (one CTA per row): tau = the top-th largest of the chunk maxima. The
-// top chunk maxima are `top` distinct logits of the row, so the row's top-th
-// largest key is at least tau, and every key >= tau is a candidate: one pass
-// collects them (typically a few dozen) and their ranks give the row's top
-// `top` in order. More than the CTA can hold (many equal logits) falls back to
-// `top` exact passes over the row.
-// Stage 2 also computes every score the chain can ask of the row (row j's
-// predecessors are the anchor for j = 0, else row j-1's candidates, which the
-// CTA finds again). Stage 3 (one CTA per sequence): the chain itself, over the
-// tables copied into shared memory.
+// Stage 2 (chunks x rows CTAs): tau = the top-th largest of the row's chunk
+// maxima. The top chunk maxima are `top` distinct logits of the row, so the
+// row's top-th largest key is at least tau, and every key >= tau is a
+// candidate: the chunks append theirs to the row's list (typically a few
+// dozen entries).
+// Stage 3 (one CTA per row): the list ranked among itself gives the row's top
+// `top` in order (a list past its capacity, from many equal logits, falls back
+// to `top` exact passes over the row); the CTA also ranks the previous row's
+// list and computes every score the chain can ask of the row (row j's
+// predecessors are the anchor for j = 0, else row j-1's candidates).
+// Stage 4 (one CTA per sequence): the chain itself, over the tables copied
+// into shared memory.
 #include <mutex>
 #include <string>
 
@@ -37,34 +39,85 @@ constexpr int KMAX = 15;
 
 static inline int sel_chunks(int width) { return (width + SEL_CHUNK - 1) / SEL_CHUNK; }
 
-// Scratch of one call: per row the chunk maxima (u64), the row's candidates
-// (u32) and its score table (f32 [top][top]).
-size_t select_scratch_bytes(int max_rows, int width, int top) {
-  return (size_t)max_rows * ((size_t)sel_chunks(width) * 8 + (size_t)top * 4 + (size_t)top * top * 4) + 256;
+// Scratch of one call, per row: the chunk maxima (u64), the candidate count and
+// list (u64, CAND_CAP), the row's top (u32) and its score table (f32 [top][top]).
+static size_t row_scratch(int width, int top) {
+  return (size_t)sel_chunks(width) * 8 + 8 + (size_t)CAND_CAP * 8 + (size_t)top * 4 + (size_t)top * top * 4;
 }
+size_t select_scratch_bytes(int max_rows, int width, int top) { return (size_t)max_rows * row_scratch(width, top) + 256; }
 
 __device__ __forceinline__ unsigned long long umax64(unsigned long long a, unsigned long long b) { return a > b ? a : b; }
 
-// Stage 1: one CTA per (chunk, row), eight logits a thread.
-__global__ void __launch_bounds__(SEL_THREADS) k_chunk_max(const float *__restrict__ logits, int width,
-                                                           unsigned long long *__restrict__ cmax) {
+// Stage 1: a CTA per (group of cpb chunks, row), eight logits a thread per chunk.
+__global__ void __launch_bounds__(SEL_THREADS) k_chunk_max(const float *__restrict__ logits, int width, int nchunks,
+                                                           int cpb, unsigned long long *__restrict__ cmax,
+                                                           int *__restrict__ cnt) {
   pdl_wait();
   __shared__ unsigned long long red[SEL_THREADS / 32];
-  const int chunk = blockIdx.x, row = blockIdx.y;
+  const int row = blockIdx.y;
   const float *lr = logits + (int64_t)row * width;
-  unsigned long long best = 0ull;
+  const int c0 = blockIdx.x * cpb, c1 = min(nchunks, c0 + cpb);
+  for (int chunk = c0; chunk < c1; ++chunk) {
+    unsigned long long best = 0ull;
 #pragma unroll
-  for (int i = 0; i < SEL_CHUNK / SEL_THREADS; ++i) {
-    const int idx = chunk * SEL_CHUNK + i * SEL_THREADS + threadIdx.x;
-    if (idx < width) best = umax64(best, cand_key(__ldg(lr + idx), (uint32_t)idx));
+    for (int i = 0; i < SEL_CHUNK / SEL_THREADS; ++i) {
+      const int idx = chunk * SEL_CHUNK + i * SEL_THREADS + threadIdx.x;
+      if (idx < width) best = umax64(best, cand_key(__ldg(lr + idx), (uint32_t)idx));
+    }
+    best = warp_max_u64(best);
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = best;
+    __syncthreads();
+    if (threadIdx.x < 32) {
+      unsigned long long v = threadIdx.x < SEL_THREADS / 32 ? red[threadIdx.x] : 0ull;
+      v = warp_max_u64(v);
+      if (threadIdx.x == 0) cmax[(int64_t)row * nchunks + chunk] = v;
+    }
+    __syncthreads();
   }
-  best = warp_max_u64(best);
-  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = best;
+  if (blockIdx.x == 0 && threadIdx.x == 0) cnt[row] = 0;
+}
+
+// Stage 2: a CTA per (group of cpb chunks, row): tau = the row's top-th
+// largest chunk maximum (the top chunk maxima are `top` distinct logits of the
+// row, so the row's top-th key is at least tau); the chunks' keys >= tau join
+// the row's candidate list.
+__global__ void __launch_bounds__(SEL_THREADS) k_chunk_filter(const float *__restrict__ logits, int width, int top,
+                                                              int nchunks, int cpb,
+                                                              const unsigned long long *__restrict__ cmax,
+                                                              int *__restrict__ cnt,
+                                                              unsigned long long *__restrict__ cands) {
+  pdl_wait();
+  __shared__ unsigned long long cm[MAX_CHUNKS];
+  __shared__ unsigned long long tau;
+  const int row = blockIdx.y;
+  for (int i = threadIdx.x; i < nchunks; i += SEL_THREADS) cm[i] = cmax[(int64_t)row * nchunks + i];
+  if (threadIdx.x == 0) tau = 0ull;  // fewer chunks than `top`: every logit is a candidate
   __syncthreads();
-  if (threadIdx.x < 32) {
-    unsigned long long v = threadIdx.x < SEL_THREADS / 32 ? red[threadIdx.x] : 0ull;
-    v = warp_max_u64(v);
-    if (threadIdx.x == 0) cmax[(int64_t)row * gridDim.x + chunk] = v;
+  if (nchunks >= top)
+    for (int i = threadIdx.x; i < nchunks; i += SEL_THREADS) {
+      const unsigned long long k = cm[i];
+      int above = 0;
+      for (int m = 0; m < nchunks; ++m) above += cm[m] > k;
+      if (above == top - 1) tau = k;  // keys are unique: exactly one thread
+    }
+  __syncthreads();
+  const unsigned long long t = tau;
+  const float *lr = logits + (int64_t)row * width;
+  unsigned long long *out = cands + (int64_t)row * CAND_CAP;
+  const int c0 = blockIdx.x * cpb, c1 = min(nchunks, c0 + cpb);
+  for (int chunk = c0; chunk < c1; ++chunk) {
+    if (cm[chunk] < t) continue;  // nothing in this chunk reaches tau
+#pragma unroll
+    for (int i = 0; i < SEL_CHUNK / SEL_THREADS; ++i) {
+      const int idx = chunk * SEL_CHUNK + i * SEL_THREADS + threadIdx.x;
+      if (idx < width) {
+        const unsigned long long k = cand_key(__ldg(lr + idx), (uint32_t)idx);
+        if (k >= t) {
+          const int at = atomicAdd(cnt + row, 1);
+          if (at < CAND_CAP) out[at] = k;
+        }
+      }
+    }
   }
 }
 
@@ -85,53 +138,16 @@ __device__ unsigned long long row_max_below(const float *__restrict__ lr, int wi
   return v;
 }
 
-// The row's top `top` keys' indices, in order, into out (shared memory):
-// candidates >= tau (the top-th largest chunk maximum) ranked among themselves.
-__device__ void row_top(const float *__restrict__ lr, int width, int top, int nchunks,
-                        const unsigned long long *__restrict__ cm, unsigned long long *keys, unsigned long long *red,
+// The row's top `top` keys' indices, in order, into out (shared memory): its
+// candidate list ranked among itself, or, when the list overflowed (many equal
+// logits), `top` exact passes over the row.
+__device__ void row_top(const float *__restrict__ lr, int width, int top, int n,
+                        const unsigned long long *__restrict__ list, unsigned long long *keys, unsigned long long *red,
                         uint32_t *out) {
-  __shared__ unsigned long long tau;
-  __shared__ int cnt;
   __syncthreads();
-  if (threadIdx.x == 0) {
-    tau = 0ull;  // fewer chunks than `top`: every logit is a candidate
-    cnt = 0;
-  }
-  for (int i = threadIdx.x; i < nchunks; i += ROW_THREADS) keys[i] = cm[i];
-  __syncthreads();
-  if (nchunks >= top) {
-    for (int i = threadIdx.x; i < nchunks; i += ROW_THREADS) {
-      const unsigned long long k = keys[i];
-      int above = 0;
-      for (int m = 0; m < nchunks; ++m) above += keys[m] > k;
-      if (above == top - 1) tau = k;  // keys are unique: exactly one thread
-    }
-  }
-  __syncthreads();
-  const unsigned long long t = tau;
-  const int n4 = (width & 3) == 0 ? width / 4 : 0;
-  for (int i = threadIdx.x; i < n4; i += ROW_THREADS) {
-    const float4 v = __ldg((const float4 *)lr + i);
-    const float vv[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const unsigned long long k = cand_key(vv[e], (uint32_t)(4 * i + e));
-      if (k >= t) {
-        const int at = atomicAdd(&cnt, 1);
-        if (at < CAND_CAP) keys[at] = k;
-      }
-    }
-  }
-  for (int idx = 4 * n4 + threadIdx.x; idx < width; idx += ROW_THREADS) {
-    const unsigned long long k = cand_key(lr[idx], (uint32_t)idx);
-    if (k >= t) {
-      const int at = atomicAdd(&cnt, 1);
-      if (at < CAND_CAP) keys[at] = k;
-    }
-  }
-  __syncthreads();
-  const int n = cnt;
   if (n <= CAND_CAP) {
+    for (int i = threadIdx.x; i < n; i += ROW_THREADS) keys[i] = list[i];
+    __syncthreads();
     for (int i = threadIdx.x; i < n; i += ROW_THREADS) {
       const unsigned long long k = keys[i];
       int above = 0;
@@ -139,7 +155,6 @@ __device__ void row_top(const float *__restrict__ lr, int width, int top, int nc
       if (above < top) out[above] = cand_index(k);
     }
   } else {
-    // many equal logits: `top` exact passes, each the largest key below the last
     unsigned long long below = ~0ull;
     for (int r = 0; r < top; ++r) {
       below = row_max_below(lr, width, below, red);
@@ -149,13 +164,13 @@ __device__ void row_top(const float *__restrict__ lr, int width, int top, int nc
   __syncthreads();
 }
 
-// Stage 2: one CTA per row j of a sequence: its candidates, its possible
-// predecessors (the anchor, or row j-1's candidates, found again here) and the
+// Stage 3: one CTA per row j of a sequence: its candidates, its possible
+// predecessors (the anchor, or row j-1's candidates, ranked again here) and the
 // score table score[p][c] = logit[cand_c] + sum_i (P[prev_p][i] * hp[i]) * C[cand_c][i].
 __global__ void __launch_bounds__(ROW_THREADS) k_row_select(
     const float *__restrict__ logits, const float *__restrict__ hp, const uint32_t *__restrict__ anchor_tok,
     const uint16_t *__restrict__ pred, const uint16_t *__restrict__ succ, int k, int width, int rank, int top,
-    int vocab, int nchunks, const unsigned long long *__restrict__ cmax, uint32_t *__restrict__ ctok,
+    int vocab, const int *__restrict__ cnt, const unsigned long long *__restrict__ cands, uint32_t *__restrict__ ctok,
     float *__restrict__ score) {
   pdl_wait();
   __shared__ unsigned long long keys[CAND_CAP];
@@ -168,10 +183,10 @@ __global__ void __launch_bounds__(ROW_THREADS) k_row_select(
   const int row = blockIdx.x, b = row / k, j = row % k;
   const uint32_t anchor = anchor_tok[b];
   if (anchor >= (uint32_t)vocab) return;  // the chain reports it
-  row_top(logits + (int64_t)row * width, width, top, nchunks, cmax + (int64_t)row * nchunks, keys, red, cur);
+  row_top(logits + (int64_t)row * width, width, top, cnt[row], cands + (int64_t)row * CAND_CAP, keys, red, cur);
   if (j > 0)
-    row_top(logits + (int64_t)(row - 1) * width, width, top, nchunks, cmax + (int64_t)(row - 1) * nchunks, keys, red,
-            prv);
+    row_top(logits + (int64_t)(row - 1) * width, width, top, cnt[row - 1], cands + (int64_t)(row - 1) * CAND_CAP,
+            keys, red, prv);
   else if (threadIdx.x == 0)
     prv[0] = anchor;
   __syncthreads();
@@ -203,7 +218,7 @@ __global__ void __launch_bounds__(ROW_THREADS) k_row_select(
   }
 }
 
-// Stage 3: one CTA per sequence runs the chain over the rows' tables: the first
+// Stage 4: one CTA per sequence runs the chain over the rows' tables: the first
 // strictly greater score in candidate order wins and is the next predecessor.
 __global__ void __launch_bounds__(CHAIN_THREADS) k_chain(const uint32_t *__restrict__ anchor_tok, int k, int top,
                                                          int vocab, const uint32_t *__restrict__ ctok,
@@ -246,13 +261,15 @@ __global__ void __launch_bounds__(CHAIN_THREADS) k_chain(const uint32_t *__restr
 
 cudaError_t select_tokens(const float *logits, const float *hp, const uint32_t *anchor_tok, const uint16_t *pred,
                           const uint16_t *succ, int batch, int k, int width, int rank, int top, int vocab, void *scratch,
-                          uint32_t *chosen, uint32_t *plain, cudaStream_t st) {
+                          uint32_t *chosen, uint32_t *plain, int num_sms, cudaStream_t st) {
   if (top > TOP_MAX || rank > RANK_MAX || top < 1 || k > KMAX || rank % 2) return cudaErrorInvalidValue;
   const int nchunks = sel_chunks(width);
   if (nchunks > MAX_CHUNKS) return cudaErrorInvalidValue;
   const int rows = batch * k;
   unsigned long long *cmax = (unsigned long long *)scratch;
-  uint32_t *ctok = (uint32_t *)(cmax + (size_t)rows * nchunks);
+  unsigned long long *cands = cmax + (size_t)rows * nchunks;
+  int *cnt = (int *)(cands + (size_t)rows * CAND_CAP);
+  uint32_t *ctok = (uint32_t *)(cnt + ((rows + 1) & ~1));
   float *score = (float *)(ctok + (size_t)rows * top);
   static bool configured = false;
   const size_t smem = (size_t)k * top * top * 4 + (size_t)k * top * 4;
@@ -262,10 +279,16 @@ cudaError_t select_tokens(const float *logits, const float *hp, const uint32_t *
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  cudaError_t e = launch_pdl(k_chunk_max, dim3(nchunks, rows), dim3(SEL_THREADS), 0, st, 1, logits, width, cmax);
+  // chunks a CTA so that stages 1 and 2 are about one wave (8 CTAs an SM)
+  const int cpb = std::max(1, (int)(((int64_t)nchunks * rows + 8 * num_sms - 1) / (8 * num_sms)));
+  const dim3 g12((nchunks + cpb - 1) / cpb, rows);
+  cudaError_t e = launch_pdl(k_chunk_max, g12, dim3(SEL_THREADS), 0, st, 1, logits, width, nchunks, cpb, cmax, cnt);
+  if (e != cudaSuccess) return e;
+  e = launch_pdl(k_chunk_filter, g12, dim3(SEL_THREADS), 0, st, 1, logits, width, top, nchunks, cpb, cmax, cnt,
+                 cands);
   if (e != cudaSuccess) return e;
   e = launch_pdl(k_row_select, dim3(rows), dim3(ROW_THREADS), 0, st, 1, logits, hp, anchor_tok, pred, succ, k, width,
-                 rank, top, vocab, nchunks, cmax, ctok, score);
+                 rank, top, vocab, cnt, cands, ctok, score);
   if (e != cudaSuccess) return e;
   return launch_pdl(k_chain, dim3(batch), dim3(CHAIN_THREADS), smem, st, 1, anchor_tok, k, top, vocab, ctok, score,
                     chosen, plain);
@@ -288,7 +311,7 @@ cudaError_t select_tokens(const float *logits, const float *hp, const uint32_t *
 namespace dfl {
 namespace {
 
-constexpr size_t kStaticSelectScratch = 8u << 20;  // bytes: 1,688 a row at a 151,936 vocabulary and top 16
+constexpr size_t kStaticSelectScratch = 8u << 20;  // bytes: 9,888 a row at a 151,936 vocabulary and top 16
 static __device__ __align__(256) unsigned char g_select_scratch[kStaticSelectScratch];
 
 // Host code cannot use g_select_scratch as a device address (in host code the
@@ -336,8 +359,10 @@ extern "C" int dflash_select_static(const float *logits, const float *hp, const 
   cudaError_t e = static_scratch(&scratch);
   if (e != cudaSuccess)
     return dflash_fail(DFLASH_E_CUDA, std::string("select_static: cudaGetSymbolAddress: ") + cudaGetErrorString(e));
+  int sms = 148, dev = 0;
+  if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   e = select_tokens(logits, hp, anchor_tok, pred_book, succ_book, batch, k, width, rank, top, vocab, scratch,
-                    chosen, plain, (cudaStream_t)stream);
+                    chosen, plain, sms, (cudaStream_t)stream);
   if (e != cudaSuccess) return dflash_fail(DFLASH_E_CUDA, std::string("select_static: ") + cudaGetErrorString(e));
   return DFLASH_OK;
 }
