@@ -342,10 +342,49 @@ __global__ void k_attn_merge(const float *__restrict__ part, int heads, int kv, 
   y[((int64_t)b * R + r) * heads * HD + (g * rep + hrep) * HD + d] = acc / L;
 }
 
+// The same merge written straight into the token tiles of the output
+// projection (hi/lo planes; a thread per 8 columns of a query row), with the
+// projection's outputs cleared by the blocks past the work grid when it splits.
+template <int HD>
+__global__ void __launch_bounds__(256) k_attn_merge_pack(const float *__restrict__ part, int heads, int kv, int R,
+                                                         int nsplit, int work_blocks, PackDst P, ZeroSet Z) {
+  pdl_wait();
+  pdl_trigger();  // the GEMM this feeds may fetch its weights meanwhile
+  if ((int)blockIdx.x >= work_blocks) {
+    if (blockIdx.y == 0) zero_set_clear(Z, blockIdx.x - work_blocks, gridDim.x - work_blocks);
+    return;
+  }
+  constexpr int D8 = HD / 8;
+  const int b = blockIdx.y;
+  const int rep = heads / kv, Q = rep * R;
+  const int id = blockIdx.x * 256 + threadIdx.x;
+  if (id >= kv * Q * D8) return;
+  const int qa = id / D8, d8 = id - qa * D8;
+  const int g = qa / Q, qi = qa - g * Q;
+  const int hrep = qi / R, r = qi - hrep * R;
+  const float *base = part + (int64_t)(b * kv + g) * (nsplit + 1) * Q * (HD + 2) + (int64_t)qi * (HD + 2);
+  const int64_t sstride = (int64_t)Q * (HD + 2);
+  float M = -INFINITY;
+  for (int s = 0; s <= nsplit; ++s) M = fmaxf(M, base[s * sstride + HD]);
+  float L = 0.f, acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  for (int s = 0; s <= nsplit; ++s) {
+    const float *ps = base + s * sstride;
+    const float m = ps[HD];
+    if (m == -INFINITY) continue;
+    const float e = expf(m - M);
+    L = fmaf(ps[HD + 1], e, L);
+#pragma unroll
+    for (int c = 0; c < 8; ++c) acc[c] = fmaf(ps[8 * d8 + c], e, acc[c]);
+  }
+#pragma unroll
+  for (int c = 0; c < 8; ++c) acc[c] = acc[c] / L;
+  pack_store8(P, b * R + r, (g * rep + hrep) * HD + 8 * d8, acc);
+}
+
 template <int HD, int KG>
 static cudaError_t launch_attn(const float *q, const float *k, const float *v, const AttnArgs &args, int batch,
                                int max_n, int heads, int kv, int R, int window, float scale, float *part, float *y,
-                               int num_sms, cudaStream_t st) {
+                               int num_sms, const PackDst *pack, const ZeroSet *zero, cudaStream_t st) {
   const size_t smem = AttnSmem<HD>::BYTES;
   static bool configured = false;
   if (!configured) {
@@ -360,6 +399,14 @@ static cudaError_t launch_attn(const float *q, const float *k, const float *v, c
                              scale, ns, cps, part);
   if (e != cudaSuccess) return e;
   const int Q = heads / kv * R;
+  if (pack) {
+    const int work = (kv * Q * (HD / 8) + 255) / 256;
+    int64_t most = 0;
+    for (int j = 0; j < zero->count; ++j) most = std::max<int64_t>(most, zero->n[j]);
+    const int zb = zero->count ? (int)std::min<int64_t>((most + 1023) / 1024, 128) : 0;
+    return launch_pdl(k_attn_merge_pack<HD>, dim3(work + zb, batch), dim3(256), 0, st, 1, part, heads, kv, R, ns, work,
+                      *pack, *zero);
+  }
   dim3 g2(kv * Q, batch);
   return launch_pdl(k_attn_merge<HD>, g2, dim3(HD), 0, st, 1, part, heads, kv, R, ns, y);
 }
@@ -367,16 +414,18 @@ static cudaError_t launch_attn(const float *q, const float *k, const float *v, c
 template <int HD>
 static cudaError_t launch_attn_hd(const float *q, const float *k, const float *v, const AttnArgs &args, int batch,
                                   int max_n, int heads, int kv, int R, int window, float scale, float *part, float *y,
-                                  int num_sms, cudaStream_t st) {
+                                  int num_sms, const PackDst *pack, const ZeroSet *zero, cudaStream_t st) {
   const int QW = (heads / kv * R + 15) / 16;
   if (QW >= 3)
-    return launch_attn<HD, 2>(q, k, v, args, batch, max_n, heads, kv, R, window, scale, part, y, num_sms, st);
-  return launch_attn<HD, 4>(q, k, v, args, batch, max_n, heads, kv, R, window, scale, part, y, num_sms, st);
+    return launch_attn<HD, 2>(q, k, v, args, batch, max_n, heads, kv, R, window, scale, part, y, num_sms, pack, zero,
+                              st);
+  return launch_attn<HD, 4>(q, k, v, args, batch, max_n, heads, kv, R, window, scale, part, y, num_sms, pack, zero,
+                            st);
 }
 
 cudaError_t attention(const float *q, const float *k, const float *v, const AttnSeq *seqs, int batch, int max_ctx,
                       int heads, int kv_heads, int hd, int block, int window, float scale, float *partials, float *y,
-                      int num_sms, cudaStream_t st) {
+                      int num_sms, const PackDst *pack, const ZeroSet *zero, cudaStream_t st) {
   (void)max_ctx;
   if (batch > MAX_BATCH || heads / kv_heads * block > QMAX) return cudaErrorInvalidValue;
   AttnArgs args;
@@ -392,10 +441,10 @@ cudaError_t attention(const float *q, const float *k, const float *v, const Attn
   num_sms = std::max(1, std::min(num_sms, 1024));
   if (hd == 128)
     return launch_attn_hd<128>(q, k, v, args, batch, max_n, heads, kv_heads, block, window, scale, partials, y, num_sms,
-                               st);
+                               pack, zero, st);
   if (hd == 64)
     return launch_attn_hd<64>(q, k, v, args, batch, max_n, heads, kv_heads, block, window, scale, partials, y, num_sms,
-                              st);
+                              pack, zero, st);
   return cudaErrorInvalidValue;
 }
 

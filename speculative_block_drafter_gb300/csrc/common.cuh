@@ -6,22 +6,6 @@
 
 namespace dfl {
 
-// ---------------------------------------------------------------- packed layouts
-//
-// Four-bit matrices [rows][cols]: tiles of 16 rows x 64 columns, 512 bytes,
-// ordered [row block][column tile]. Inside a tile, lane l (0..31) owns 16 bytes:
-// u32 j (0..3) is the mma.m16n8k16 A fragment of the lane for columns
-// 16j..16j+15, eight nibbles (q + 8) in the order a0 a2 a4 a6 a1 a3 a5 a7, where
-// with g = l/4, c = l%4:  a0 (g, 2c)  a1 (g, 2c+1)  a2 (g+8, 2c)  a3 (g+8, 2c+1)
-//                         a4 (g, 2c+8) a5 (g, 2c+9) a6 (g+8, 2c+8) a7 (g+8, 2c+9).
-// Scales: u32 [row block][group][g] = f16 scale of row g | f16 of row g+8 << 16.
-//
-// f16 matrices: the same tiles, 2 KiB each; lane l owns 64 bytes, u32 4j+m is
-// the pair (a_{2m}, a_{2m+1}) of column step j, laid out [tile][j][lane][4 u32]
-// so that one step of one tile is 512 contiguous bytes.
-constexpr int TILE_ROWS = 16;
-constexpr int TILE_COLS = 64;
-
 // ---------------------------------------------------------------- programmatic dependent launch
 // Every kernel of the pass is launched so that it may start while the kernel
 // before it in the stream finishes (launch_pdl). Such a kernel calls pdl_wait()
@@ -126,6 +110,99 @@ __device__ __forceinline__ unsigned long long warp_max_u64(unsigned long long v)
     v = w > v ? w : v;
   }
   return v;
+}
+
+// ---------------------------------------------------------------- packed token tiles
+// Byte offset of (row r, 16-byte chunk c) in a K-major tile of 64 f16 per row, 128-byte swizzle.
+__host__ __device__ __forceinline__ uint32_t sw128_off(int r, int c) {
+  return (uint32_t)((r >> 3) * 1024 + (r & 7) * 128 + ((c ^ (r & 7)) << 4));
+}
+
+// ---------------------------------------------------------------- token tiles
+// One 16-byte chunk (8 columns of one token row) of the packed token tiles:
+// per (token tile tt, k-tile kt, plane p) TT rows x 64 columns f16, K-major
+// with the 128-byte swizzle. Plane 0 = f16(x); plane 1 = f16(x - f16(x)).
+// Chunk t < ceil(T/TT) * (K/64) * TT * 8; rows past T are zero.
+template <int PLANES>
+__device__ __forceinline__ void pack_act_chunk(const float *__restrict__ X, int ldx, int T, int K, int TT,
+                                               uint4 *__restrict__ dst, int64_t t) {
+  const int KT = K / 64;
+  const int c = (int)(t & 7);
+  const int r = (int)((t >> 3) % TT);
+  const int64_t rest = (t >> 3) / TT;
+  const int kt = (int)(rest % KT);
+  const int tt = (int)(rest / KT);
+  const int tok = tt * TT + r;
+  float x[8];
+  if (tok < T) {
+    const float *src = X + (int64_t)tok * ldx + kt * 64 + c * 8;
+    if ((((uintptr_t)src) & 15) == 0) {
+      const float4 a = ((const float4 *)src)[0], b = ((const float4 *)src)[1];
+      x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
+      x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+    } else {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) x[i] = src[i];
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) x[i] = 0.f;
+  }
+  uint32_t hi[4], lo[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    if (PLANES == 2) {
+      split2(x[2 * i], x[2 * i + 1], hi[i], lo[i]);
+    } else {
+      hi[i] = pack_half2(__float2half_rn(x[2 * i]), __float2half_rn(x[2 * i + 1]));
+    }
+  }
+  const int64_t base = (((int64_t)tt * KT + kt) * PLANES) * TT * 8;  // in 16-byte chunks
+  dst[base + sw128_off(r, c) / 16] = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+  if (PLANES == 2) dst[base + TT * 8 + sw128_off(r, c) / 16] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+}
+
+// A GEMM's packed token tiles as a producer kernel writes them: 8 consecutive
+// columns of one token row at a time (the layout of pack_act_chunk).
+struct PackDst {
+  uint4 *dst;
+  int TT;      // token rows a tile
+  int planes;  // 1: f16(x); 2: hi and lo
+  int KT;      // 64-column k-tiles
+};
+__device__ __forceinline__ void pack_store8(const PackDst &P, int tok, int col, const float (&x)[8]) {
+  const int tt = tok / P.TT, r = tok - tt * P.TT, kt = col >> 6, c = (col & 63) >> 3;
+  const int64_t base = ((int64_t)tt * P.KT + kt) * P.planes * P.TT * 8;
+  uint32_t hi[4], lo[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    if (P.planes == 2) split2(x[2 * i], x[2 * i + 1], hi[i], lo[i]);
+    else hi[i] = pack_half2(__float2half_rn(x[2 * i]), __float2half_rn(x[2 * i + 1]));
+  }
+  P.dst[base + sw128_off(r, c) / 16] = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+  if (P.planes == 2) P.dst[base + P.TT * 8 + sw128_off(r, c) / 16] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+}
+
+// Outputs that the GEMM fed by a producer accumulates into when its k-range is
+// split: the producer clears T rows of n floats of each (grid-stride over blocks).
+constexpr int ZERO_MAX = 4;
+struct ZeroSet {
+  float *y[ZERO_MAX];
+  int ldy[ZERO_MAX];
+  int n[ZERO_MAX];
+  int count;
+  int T;
+};
+__device__ __forceinline__ void zero_set_clear(const ZeroSet &Z, int block, int nblocks) {
+  for (int j = 0; j < Z.count; ++j)
+    for (int t = 0; t < Z.T; ++t) {
+      float *y = Z.y[j] + (int64_t)t * Z.ldy[j];
+      for (int c = (block * blockDim.x + threadIdx.x) * 4; c < Z.n[j]; c += nblocks * blockDim.x * 4) {
+        if (c + 3 < Z.n[j] && (((uintptr_t)(y + c)) & 15) == 0) *(float4 *)(y + c) = make_float4(0.f, 0.f, 0.f, 0.f);
+        else
+          for (int e = 0; e < 4 && c + e < Z.n[j]; ++e) y[c + e] = 0.f;
+      }
+    }
 }
 
 }  // namespace dfl

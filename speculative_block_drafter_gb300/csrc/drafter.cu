@@ -45,7 +45,7 @@ struct Seq {
 
 // Workspace carve; sizes in bytes.
 struct Carve {
-  size_t h, x, xc, d, q, k, v, y, o, gt, up, part, sel, act, total;
+  size_t h, x, xc, d, d2, q, k, v, y, o, gt, up, part, sel, act, total;
 };
 
 Carve carve_of(const dflash_geometry &g, int max_batch) {
@@ -59,6 +59,7 @@ Carve carve_of(const dflash_geometry &g, int max_batch) {
   c.x = up(T * g.hidden * f);
   c.xc = up(T * g.hidden * f);
   c.d = up(T * pr * f);
+  c.d2 = c.d;  // the MLP's kernel projection (the attention's d is still read when it is written)
   c.q = up(T * (size_t)g.heads * g.head_dim * f);
   c.k = up(T * (size_t)g.kv_heads * g.head_dim * f);
   c.v = c.k;
@@ -74,7 +75,7 @@ Carve carve_of(const dflash_geometry &g, int max_batch) {
   c.act = up(std::max({dfl::tc_act_bytes(Tb, kmax, true), dfl::tc_act_bytes(DFLASH_SETTLE_MAX, g.hidden, true),
                        dfl::tc_act_bytes(DFLASH_SETTLE_MAX, g.taps * g.hidden, false),
                        dfl::tc_act_bytes(Tb, g.hidden, false)}));
-  c.total = c.h + c.x + c.xc + c.d + c.q + c.k + c.v + c.y + c.o + c.gt + c.up + c.part + c.sel + c.act;
+  c.total = c.h + c.x + c.xc + c.d + c.d2 + c.q + c.k + c.v + c.y + c.o + c.gt + c.up + c.part + c.sel + c.act;
   return c;
 }
 
@@ -133,7 +134,7 @@ struct dflash_t {
   int64_t cap = 0;
   char *ws = nullptr;
   Carve c{};
-  float *h, *x, *xc, *d, *q, *k, *v, *y, *o, *gt, *up, *part;
+  float *h, *x, *xc, *d, *d2, *q, *k, *v, *y, *o, *gt, *up, *part;
   void *sel, *act;
   std::vector<Seq> seqs;
   std::vector<float> inv;
@@ -278,6 +279,7 @@ int dflash_create(dflash_t **out, const dflash_geometry *g, const dflash_weights
   d->x = (float *)take(c.x);
   d->xc = (float *)take(c.xc);
   d->d = (float *)take(c.d);
+  d->d2 = (float *)take(c.d2);
   d->q = (float *)take(c.q);
   d->k = (float *)take(c.k);
   d->v = (float *)take(c.v);
@@ -377,20 +379,7 @@ int dflash_block(dflash_t *d, int32_t batch, const int64_t *anchor_pos, const fl
   const int sms = d->num_sms;
   DF_CUDA(cudaMemcpyAsync(d->h, h, (size_t)T * hs * sizeof(float), cudaMemcpyDeviceToDevice, st));
   std::vector<dfl::AttnSeq> seqs(batch);
-  for (int l = 0; l < g.layers; ++l) {
-    const dflash_layer_weights &L = d->layers[l];
-    const int W = g.windows[l];
-    const bool rot = g.no_rope[l] == 0;
-    // attention: x = norm(h); x, d = conv_in(x); q, k, v
-    DF_CUDA(dfl::rmsnorm(d->h, L.in_norm, d->x, T, hs, eps, R, -1, -1, st));
-    const dfl::TcJob ap{L.attn_proj.data, nullptr, d->d, pr, pr};
-    DF_CUDA(dfl::tc_gemm_f16(&ap, 1, d->x, hs, T, hs, d->act, sms, st));
-    DF_CUDA(dfl::conv_stage0(d->x, d->d, L.attn_base, d->xc, T, hs, kn, gs, R, st));
-    const dfl::TcJob qkv[3] = {{L.q.data, L.q.scales, d->q, qd, qd}, {L.k.data, L.k.scales, d->k, kvd, kvd},
-                               {L.v.data, L.v.scales, d->v, kvd, kvd}};
-    DF_CUDA(dfl::tc_gemm_int4(qkv, 3, grp, d->xc, hs, T, hs, d->act, sms, st));
-    DF_CUDA(dfl::head_norm_rope(d->q, qd, L.q_norm, d->inv.data(), T, nh, hd, eps, rot, anchor_pos, batch, R, 0, st));
-    DF_CUDA(dfl::head_norm_rope(d->k, kvd, L.k_norm, d->inv.data(), T, kv, hd, eps, rot, anchor_pos, batch, R, 0, st));
+  auto ranges = [&](int l, int W) {
     // the layer's context range (src/cortiq_engine/dflash.rs, Drafter::block; no rows dropped)
     for (int b = 0; b < batch; ++b) {
       const Seq &s = d->seqs[b];
@@ -405,8 +394,108 @@ int dflash_block(dflash_t *d, int32_t batch, const int64_t *anchor_pos, const fl
       seqs[b].lo = lo;
       seqs[b].anchor = a;
     }
-    DF_CUDA(dfl::attention(d->q, d->k, d->v, seqs.data(), batch, 0, nh, kv, hd, R, W, scale, d->part, d->y,
-                           d->num_sms, st));
+  };
+  const int Tk = batch * k;
+
+  if (T <= 32) {
+    // Up to 32 rows: every GEMM reads token tiles that the kernel before it
+    // wrote (norm, convolution, SiLU or the attention merge), which also clears
+    // the GEMM's outputs when the GEMM splits its k-range.
+    const int tf = dfl::tc_tile_rows(T, false), ti = dfl::tc_tile_rows(T, true);
+    auto pack_for = [&](int planes, int tt, int K) { return dfl::PackDst{(uint4 *)d->act, tt, planes, K / 64}; };
+    auto zero_for = [&](const dfl::TcJob *jobs, int n, bool split, int rows) {
+      dfl::ZeroSet z{};
+      if (split) {
+        z.count = n;
+        z.T = rows;
+        for (int j = 0; j < n; ++j) {
+          z.y[j] = jobs[j].y;
+          z.ldy[j] = jobs[j].ldy;
+          z.n[j] = jobs[j].n;
+        }
+      }
+      return z;
+    };
+    for (int l = 0; l < g.layers; ++l) {
+      const dflash_layer_weights &L = d->layers[l];
+      const int W = g.windows[l];
+      const bool rot = g.no_rope[l] == 0;
+      const dfl::TcJob ap{L.attn_proj.data, nullptr, d->d, pr, pr};
+      const dfl::TcJob qkv[3] = {{L.q.data, L.q.scales, d->q, qd, qd}, {L.k.data, L.k.scales, d->k, kvd, kvd},
+                                 {L.v.data, L.v.scales, d->v, kvd, kvd}};
+      const dfl::TcJob oj{L.o.data, L.o.scales, d->o, hs, hs};
+      const dfl::TcJob mp{L.mlp_proj.data, nullptr, d->d2, pr, pr};
+      const dfl::TcJob gu[2] = {{L.gate.data, L.gate.scales, d->gt, ffn, ffn},
+                                {L.up.data, L.up.scales, d->up, ffn, ffn}};
+      const dfl::TcJob dn{L.down.data, L.down.scales, d->o, hs, hs};
+      // attention: x = norm(h) (for layers after the first, the previous layer's
+      // last convolution already did it); d = Pr_attn . f16(x); xc = conv_in(x, d); q, k, v
+      if (l == 0)
+        DF_CUDA(dfl::rms_pack(d->h, nullptr, nullptr, nullptr, kn, gs, L.in_norm, d->x, T, hs, eps, R, -1, -1,
+                              pack_for(1, tf, hs), zero_for(&ap, 1, dfl::tc_splits_f16(&ap, 1, T, hs, sms), T), st));
+      DF_CUDA(dfl::tc_gemm_f16_packed(&ap, 1, d->act, tf * 128, T, hs, sms, st));
+      DF_CUDA(dfl::conv0_pack(d->x, d->d, L.attn_base, T, hs, kn, gs, R, pack_for(2, ti, hs),
+                              zero_for(qkv, 3, dfl::tc_splits_int4(qkv, 3, T, hs, sms), T), st));
+      DF_CUDA(dfl::tc_gemm_int4_packed(qkv, 3, grp, d->act, T, hs, sms, st));
+      DF_CUDA(dfl::qk_norm_rope(d->q, qd, L.q_norm, nh, d->k, kvd, L.k_norm, kv, d->inv.data(), T, hd, eps, rot,
+                                anchor_pos, batch, R, st));
+      ranges(l, W);
+      const dfl::PackDst po = pack_for(2, ti, qd);
+      const dfl::ZeroSet zo = zero_for(&oj, 1, dfl::tc_splits_int4(&oj, 1, T, qd, sms), T);
+      DF_CUDA(dfl::attention(d->q, d->k, d->v, seqs.data(), batch, 0, nh, kv, hd, R, W, scale, d->part, d->y, sms, &po,
+                             &zo, st));
+      DF_CUDA(dfl::tc_gemm_int4_packed(&oj, 1, grp, d->act, T, qd, sms, st));
+      // h += conv_out(o, d); x = norm(h); the MLP the same way
+      DF_CUDA(dfl::rms_pack(d->h, d->o, d->d, L.attn_base, kn, gs, L.post_norm, d->x, T, hs, eps, R, -1, -1,
+                            pack_for(1, tf, hs), zero_for(&mp, 1, dfl::tc_splits_f16(&mp, 1, T, hs, sms), T), st));
+      DF_CUDA(dfl::tc_gemm_f16_packed(&mp, 1, d->act, tf * 128, T, hs, sms, st));
+      DF_CUDA(dfl::conv0_pack(d->x, d->d2, L.mlp_base, T, hs, kn, gs, R, pack_for(2, ti, hs),
+                              zero_for(gu, 2, dfl::tc_splits_int4(gu, 2, T, hs, sms), T), st));
+      DF_CUDA(dfl::tc_gemm_int4_packed(gu, 2, grp, d->act, T, hs, sms, st));
+      DF_CUDA(dfl::silu_pack(d->gt, d->up, T, ffn, pack_for(2, ti, ffn),
+                             zero_for(&dn, 1, dfl::tc_splits_int4(&dn, 1, T, ffn, sms), T), st));
+      DF_CUDA(dfl::tc_gemm_int4_packed(&dn, 1, grp, d->act, T, ffn, sms, st));
+      // h += conv_out(down, d) and the next norm: the next layer's input norm, or the last norm (rows 1..k)
+      if (l + 1 < g.layers) {
+        const dflash_layer_weights &N = d->layers[l + 1];
+        const dfl::TcJob ap2{N.attn_proj.data, nullptr, d->d, pr, pr};
+        DF_CUDA(dfl::rms_pack(d->h, d->o, d->d2, L.mlp_base, kn, gs, N.in_norm, d->x, T, hs, eps, R, -1, -1,
+                              pack_for(1, tf, hs), zero_for(&ap2, 1, dfl::tc_splits_f16(&ap2, 1, T, hs, sms), T),
+                              st));
+      } else {
+        const dfl::TcJob ends[2] = {{d->w.head.data, d->w.head.scales, logits, width, width},
+                                    {d->w.sel.data, nullptr, hp, g.selector_rank, g.selector_rank}};
+        const bool split = dfl::tc_splits_int4(&ends[0], 1, Tk, hs, sms) || dfl::tc_splits_f16(&ends[1], 1, Tk, hs, sms);
+        DF_CUDA(dfl::rms_pack(d->h, d->o, d->d2, L.mlp_base, kn, gs, d->w.norm, nullptr, T, hs, eps, R, 1, k,
+                              pack_for(2, dfl::tc_tile_rows(Tk, true), hs), zero_for(ends, 2, split, Tk), st));
+      }
+    }
+    // the head and the selector's projection over rows 1..k (the selector reads the hi plane)
+    const int th = dfl::tc_tile_rows(Tk, true);
+    const dfl::TcJob hj{d->w.head.data, d->w.head.scales, logits, width, width};
+    DF_CUDA(dfl::tc_gemm_int4_packed(&hj, 1, grp, d->act, Tk, hs, sms, st));
+    const dfl::TcJob sj{d->w.sel.data, nullptr, hp, g.selector_rank, g.selector_rank};
+    DF_CUDA(dfl::tc_gemm_f16_packed(&sj, 1, d->act, 2 * th * 128, Tk, hs, sms, st));
+    return DFLASH_OK;
+  }
+
+  for (int l = 0; l < g.layers; ++l) {
+    const dflash_layer_weights &L = d->layers[l];
+    const int W = g.windows[l];
+    const bool rot = g.no_rope[l] == 0;
+    // attention: x = norm(h); x, d = conv_in(x); q, k, v
+    DF_CUDA(dfl::rmsnorm(d->h, L.in_norm, d->x, T, hs, eps, R, -1, -1, st));
+    const dfl::TcJob ap{L.attn_proj.data, nullptr, d->d, pr, pr};
+    DF_CUDA(dfl::tc_gemm_f16(&ap, 1, d->x, hs, T, hs, d->act, sms, st));
+    DF_CUDA(dfl::conv_stage0(d->x, d->d, L.attn_base, d->xc, T, hs, kn, gs, R, st));
+    const dfl::TcJob qkv[3] = {{L.q.data, L.q.scales, d->q, qd, qd}, {L.k.data, L.k.scales, d->k, kvd, kvd},
+                               {L.v.data, L.v.scales, d->v, kvd, kvd}};
+    DF_CUDA(dfl::tc_gemm_int4(qkv, 3, grp, d->xc, hs, T, hs, d->act, sms, st));
+    DF_CUDA(dfl::qk_norm_rope(d->q, qd, L.q_norm, nh, d->k, kvd, L.k_norm, kv, d->inv.data(), T, hd, eps, rot,
+                              anchor_pos, batch, R, st));
+    ranges(l, W);
+    DF_CUDA(dfl::attention(d->q, d->k, d->v, seqs.data(), batch, 0, nh, kv, hd, R, W, scale, d->part, d->y, sms,
+                           nullptr, nullptr, st));
     const dfl::TcJob oj{L.o.data, L.o.scales, d->o, hs, hs};
     DF_CUDA(dfl::tc_gemm_int4(&oj, 1, grp, d->y, qd, T, qd, d->act, sms, st));
     DF_CUDA(dfl::conv_stage1_residual(d->o, d->d, L.attn_base, d->h, T, hs, kn, gs, R, st));
@@ -423,7 +512,6 @@ int dflash_block(dflash_t *d, int32_t batch, const int64_t *anchor_pos, const fl
     DF_CUDA(dfl::conv_stage1_residual(d->o, d->d, L.mlp_base, d->h, T, hs, kn, gs, R, st));
   }
   // the last norm; the head and the selector's projection over rows 1..k
-  const int Tk = batch * k;
   DF_CUDA(dfl::rmsnorm(d->h, d->w.norm, d->x, T, hs, eps, R, 1, k, st));
   const dfl::TcJob hj{d->w.head.data, d->w.head.scales, logits, width, width};
   DF_CUDA(dfl::tc_gemm_int4(&hj, 1, grp, d->x, hs, Tk, hs, d->act, sms, st));

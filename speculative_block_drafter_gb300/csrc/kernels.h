@@ -7,6 +7,8 @@
 #include <string>
 #include <utility>
 
+#include "common.cuh"
+
 namespace dfl {
 
 // Kernel launches enqueued by the library in this process.
@@ -107,6 +109,19 @@ size_t wide_act_bytes(int T, int K, bool int4);
 cudaError_t wide_gemm(const WideJob *jobs, int njobs, int64_t y_off, bool int4, int group, const float *X, int ldx,
                       int T, int K, void *act, int num_sms, cudaStream_t st);
 
+// Narrow GEMMs (T <= 32) on token tiles a producer kernel has packed: the
+// tiles' rows, whether the launch will split its k-range (its outputs must then
+// be cleared by the producer), and the launches. `bstride` is the bytes from
+// one k-tile of the f16 GEMM's tiles to the next (TT * 128, or twice that to
+// read the hi plane of a two-plane pack).
+int tc_tile_rows(int T, bool int4);
+bool tc_splits_int4(const TcJob *jobs, int njobs, int T, int K, int num_sms);
+bool tc_splits_f16(const TcJob *jobs, int njobs, int T, int K, int num_sms);
+cudaError_t tc_gemm_int4_packed(const TcJob *jobs, int njobs, int group, const void *act, int T, int K, int num_sms,
+                                cudaStream_t st);
+cudaError_t tc_gemm_f16_packed(const TcJob *jobs, int njobs, const void *act, int bstride, int T, int K, int num_sms,
+                               cudaStream_t st);
+
 // The device error word (a bounded wait that gave up sets bit 0).
 cudaError_t read_device_error(unsigned *out, bool reset);
 
@@ -135,6 +150,23 @@ cudaError_t head_norm_rope(float *x, int ld, const float *w, const float *inv_fr
 // l's norm weight w[l] and rotary flag (host arrays of `nlayers`, passed by value).
 cudaError_t ctx_norm_rope(float *const *k, const float *const *w, const int *rotary, int nlayers, int T, int heads,
                           int hd, float eps, const float *inv_freq, int64_t pos_base, cudaStream_t st);
+// Fused producers of a GEMM's packed token tiles (rows.cu). Each writes its
+// result into P (the following GEMM's token tiles) and clears Z (that GEMM's
+// outputs, when it splits its k-range).
+// rms_pack: optionally h[t] += the stage-1 convolution of (cx, cd, cbase)
+// first; then x = rms(h[t], w) into xout (may be null) and P, rows outside
+// [keep_from, keep_to] of their block left out when keep_from >= 0.
+cudaError_t rms_pack(float *h, const float *cx, const float *cd, const float *cbase, int kn, int gs, const float *w,
+                     float *xout, int T, int hs, float eps, int block, int keep_from, int keep_to, const PackDst &P,
+                     const ZeroSet &Z, cudaStream_t st);
+cudaError_t conv0_pack(const float *x, const float *d, const float *base, int T, int hs, int kn, int gs, int block,
+                       const PackDst &P, const ZeroSet &Z, cudaStream_t st);
+cudaError_t silu_pack(const float *g, const float *u, int T, int n, const PackDst &P, const ZeroSet &Z,
+                      cudaStream_t st);
+// q and k of the block: per head norm and rotation to pos0[t / block] + t % block, one launch.
+cudaError_t qk_norm_rope(float *q, int ldq, const float *wq, int hq, float *k, int ldk, const float *wk, int hk,
+                         const float *inv_freq, int T, int hd, float eps, bool rotary, const int64_t *pos0, int nseq,
+                         int block, cudaStream_t st);
 // m = silu(g) * u, elementwise over n values.
 cudaError_t silu_mul(const float *g, const float *u, float *m, int64_t n, cudaStream_t st);
 
@@ -147,9 +179,12 @@ struct AttnSeq {        // per sequence and layer, on the device
 };
 size_t attn_partial_bytes(int max_batch, int kv_heads, int heads, int block, int hd);
 // `seqs` is a host array of `batch` entries (passed by value).
+// With `pack` set, the merged rows go straight into those token tiles (for the
+// output projection; `zero` its outputs to clear) instead of y.
 cudaError_t attention(const float *q, const float *k, const float *v, const AttnSeq *seqs, int batch,
                       int max_ctx, int heads, int kv_heads, int hd, int block, int window, float scale,
-                      float *partials, float *y, int num_sms, cudaStream_t st);
+                      float *partials, float *y, int num_sms, const PackDst *pack, const ZeroSet *zero,
+                      cudaStream_t st);
 
 // -------------------------------------------------------------- selector (select.cu)
 size_t select_scratch_bytes(int max_rows, int width, int top);

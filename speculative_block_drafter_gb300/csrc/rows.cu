@@ -2,6 +2,8 @@
 // convolution (both stages), the per-head q/k norm with the rotation, SiLU.
 // Cited passages: cortiq-engine src/cortiq_engine/dflash.rs, `rms`,
 // `Drafter::conv`, `Drafter::rotate`, `Drafter::mlp`, `Drafter::block`.
+#include <algorithm>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -253,6 +255,239 @@ __global__ void k_silu_mul(const float *__restrict__ g, const float *__restrict_
 
 cudaError_t silu_mul(const float *g, const float *u, float *m, int64_t n, cudaStream_t st) {
   return launch_pdl(k_silu_mul, dim3((unsigned)((n + 255) / 256)), dim3(256), 0, st, 1, g, u, m, n);
+}
+
+
+// ---------------------------------------------------------------- fused producers of a GEMM's token tiles
+// Each writes its result straight into the packed token tiles of the GEMM that
+// follows (PackDst) and, when that GEMM will split its k-range, clears the
+// GEMM's outputs (ZeroSet) with its blocks past the work grid. Threads own 8
+// consecutive columns of a row.
+
+constexpr int FP_THREADS = 256;
+constexpr int FP_KEEP = 4;  // 8-column groups a thread keeps between the two passes of a row (hs <= 8192)
+
+__device__ __forceinline__ void load8(const float *p, float (&v)[8]) {
+  const float4 a = ((const float4 *)p)[0], b = ((const float4 *)p)[1];
+  v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+}
+__device__ __forceinline__ void store8(float *p, const float (&v)[8]) {
+  ((float4 *)p)[0] = make_float4(v[0], v[1], v[2], v[3]);
+  ((float4 *)p)[1] = make_float4(v[4], v[5], v[6], v[7]);
+}
+
+// Stage 1 of the row convolution with the residual for 8 channels i0.. of row t:
+// h[t][i] += sum_{o <= min(kn-1, t % block)} (base[1][o][i] + d[t][1][o][i/gs]) * x[t-o][i].
+__device__ __forceinline__ void conv1_8(const float *__restrict__ x, const float *__restrict__ d,
+                                        const float *__restrict__ base, float (&h)[8], int t, int i0, int hs, int kn,
+                                        int gs, int block) {
+  const int groups = hs / gs, r = t % block;
+  const float *dr = d + (int64_t)t * (2 * kn * groups) + kn * groups;
+  const float *br = base + (int64_t)kn * hs;
+  const int nmax = min(kn, r + 1);
+  for (int o = 0; o < nmax; ++o) {
+    float xv[8], bv[8];
+    load8(x + (int64_t)(t - o) * hs + i0, xv);
+    load8(br + (int64_t)o * hs + i0, bv);
+    if (gs % 8 == 0) {
+      const float dv = dr[o * groups + i0 / gs];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) h[e] = fmaf(bv[e] + dv, xv[e], h[e]);
+    } else {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) h[e] = fmaf(bv[e] + dr[o * groups + (i0 + e) / gs], xv[e], h[e]);
+    }
+  }
+}
+
+// One CTA per row t (blocks >= T clear). If `conv` is set, first h[t] += the
+// stage-1 convolution of (cx, cd, cbase) (the residual); then x = rms(h[t], w)
+// into xout (if set) and into the token tiles at the row's packed index
+// (rows outside [keep_from, keep_to] of their block are left out, packed per
+// sequence, when keep_from >= 0).
+__global__ void __launch_bounds__(1024) k_rms_pack(float *__restrict__ h, const float *__restrict__ cx,
+                                                         const float *__restrict__ cd, const float *__restrict__ cbase,
+                                                         int kn, int gs, const float *__restrict__ w,
+                                                         float *__restrict__ xout, int T, int hs, float eps, int block,
+                                                         int keep_from, int keep_to, PackDst P, ZeroSet Z) {
+  pdl_wait();
+  pdl_trigger();  // the GEMM this feeds may fetch its weights meanwhile
+  if ((int)blockIdx.x >= T) {
+    zero_set_clear(Z, blockIdx.x - T, gridDim.x - T);
+    return;
+  }
+  const int t = blockIdx.x;
+  const int ng = hs / 8, nt = blockDim.x;
+  float v[FP_KEEP][8];
+  float ss = 0.f;
+  float *hr = h + (int64_t)t * hs;
+#pragma unroll
+  for (int m = 0; m < FP_KEEP; ++m) {
+    const int gi = threadIdx.x + m * nt;
+    if (gi < ng) {
+      load8(hr + 8 * gi, v[m]);
+      if (cx) {
+        conv1_8(cx, cd, cbase, v[m], t, 8 * gi, hs, kn, gs, block);
+        store8(hr + 8 * gi, v[m]);
+      }
+#pragma unroll
+      for (int e = 0; e < 8; ++e) ss = fmaf(v[m][e], v[m][e], ss);
+    }
+  }
+  __shared__ float red[32];
+  ss = warp_sum(ss);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    float q = threadIdx.x < (nt >> 5) ? red[threadIdx.x] : 0.f;
+    q = warp_sum(q);
+    if (threadIdx.x == 0) red[0] = q;
+  }
+  __syncthreads();
+  const float sc = 1.0f / sqrtf(red[0] / (float)hs + eps);
+  int orow = t;
+  bool keep = true;
+  if (keep_from >= 0) {
+    const int sq = t / block, r = t % block;
+    keep = r >= keep_from && r <= keep_to;
+    orow = sq * (keep_to - keep_from + 1) + (r - keep_from);
+  }
+  if (!keep) return;
+#pragma unroll
+  for (int m = 0; m < FP_KEEP; ++m) {
+    const int gi = threadIdx.x + m * nt;
+    if (gi < ng) {
+      float wv[8], o[8];
+      load8(w + 8 * gi, wv);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) o[e] = v[m][e] * sc * wv[e];
+      if (xout) store8(xout + (int64_t)orow * hs + 8 * gi, o);
+      pack_store8(P, orow, 8 * gi, o);
+    }
+  }
+}
+
+// Stage 0 of the row convolution into the token tiles: one thread per 8 channels of a row.
+__global__ void __launch_bounds__(FP_THREADS) k_conv0_pack(const float *__restrict__ x, const float *__restrict__ d,
+                                                           const float *__restrict__ base, int T, int hs, int kn,
+                                                           int gs, int block, int work_blocks, PackDst P, ZeroSet Z) {
+  pdl_wait();
+  pdl_trigger();  // the GEMM this feeds may fetch its weights meanwhile
+  if ((int)blockIdx.x >= work_blocks) {
+    zero_set_clear(Z, blockIdx.x - work_blocks, gridDim.x - work_blocks);
+    return;
+  }
+  const int ng = hs / 8;
+  const int id = blockIdx.x * FP_THREADS + threadIdx.x;
+  if (id >= T * ng) return;
+  const int t = id / ng, i0 = 8 * (id - t * ng);
+  const int groups = hs / gs, r = t % block;
+  const float *dr = d + (int64_t)t * (2 * kn * groups);
+  const int nmax = min(kn, r + 1);
+  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  for (int o = 0; o < nmax; ++o) {
+    float xv[8], bv[8];
+    load8(x + (int64_t)(t - o) * hs + i0, xv);
+    load8(base + (int64_t)o * hs + i0, bv);
+    if (gs % 8 == 0) {
+      const float dv = dr[o * groups + i0 / gs];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) acc[e] = fmaf(bv[e] + dv, xv[e], acc[e]);
+    } else {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) acc[e] = fmaf(bv[e] + dr[o * groups + (i0 + e) / gs], xv[e], acc[e]);
+    }
+  }
+  pack_store8(P, t, i0, acc);
+}
+
+// m = silu(g) * u into the token tiles: one thread per 8 columns of a row.
+__global__ void __launch_bounds__(FP_THREADS) k_silu_pack(const float *__restrict__ g, const float *__restrict__ u,
+                                                          int T, int n, int work_blocks, PackDst P, ZeroSet Z) {
+  pdl_wait();
+  pdl_trigger();  // the GEMM this feeds may fetch its weights meanwhile
+  if ((int)blockIdx.x >= work_blocks) {
+    zero_set_clear(Z, blockIdx.x - work_blocks, gridDim.x - work_blocks);
+    return;
+  }
+  const int ng = n / 8;
+  const int id = blockIdx.x * FP_THREADS + threadIdx.x;
+  if (id >= T * ng) return;
+  const int t = id / ng, i0 = 8 * (id - t * ng);
+  float gv[8], uv[8], m[8];
+  load8(g + (int64_t)t * n + i0, gv);
+  load8(u + (int64_t)t * n + i0, uv);
+#pragma unroll
+  for (int e = 0; e < 8; ++e) m[e] = gv[e] / (1.0f + expf(-gv[e])) * uv[e];
+  pack_store8(P, t, i0, m);
+}
+
+// The per-head norm and rotation of the block's q and k in one launch.
+template <int HD>
+__global__ void k_qk_norm_rope(float *__restrict__ q, int ldq, const float *__restrict__ wq, int hq,
+                               float *__restrict__ k, int ldk, const float *__restrict__ wk, int hk, int T, float eps,
+                               int rotary, PosArgs pa, int block) {
+  pdl_wait();
+  const int wid = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  const int nq = T * hq;
+  if (wid >= nq + T * hk) return;
+  const bool isq = wid < nq;
+  const int w2 = isq ? wid : wid - nq, heads = isq ? hq : hk;
+  const int t = w2 / heads, h = w2 % heads;
+  const int64_t pos = pa.pos0[t / block] + (t % block);
+  float *p = isq ? q + (int64_t)t * ldq + h * HD : k + (int64_t)t * ldk + h * HD;
+  norm_rope_head<HD>(p, isq ? wq : wk, eps, rotary != 0, pos, pa.inv, lane);
+}
+
+static unsigned zero_blocks_for(const ZeroSet &Z) {
+  int64_t most = 0;
+  for (int j = 0; j < Z.count; ++j) most = std::max<int64_t>(most, (int64_t)Z.n[j]);
+  return Z.count ? (unsigned)std::min<int64_t>((most + 1023) / 1024, 128) : 0u;
+}
+
+cudaError_t rms_pack(float *h, const float *cx, const float *cd, const float *cbase, int kn, int gs, const float *w,
+                     float *xout, int T, int hs, float eps, int block, int keep_from, int keep_to, const PackDst &P,
+                     const ZeroSet &Z, cudaStream_t st) {
+  // a thread per 8-column group of the row (at most FP_KEEP groups a thread)
+  const int ng = hs / 8;
+  const int nt = std::min(1024, std::max(32, (ng + 31) / 32 * 32));
+  if (hs % 8 || ng > nt * FP_KEEP) return cudaErrorInvalidValue;
+  return launch_pdl(k_rms_pack, dim3(T + zero_blocks_for(Z)), dim3(nt), 0, st, 1, h, cx, cd, cbase, kn, gs, w, xout, T,
+                    hs, eps, block, keep_from, keep_to, P, Z);
+}
+
+cudaError_t conv0_pack(const float *x, const float *d, const float *base, int T, int hs, int kn, int gs, int block,
+                       const PackDst &P, const ZeroSet &Z, cudaStream_t st) {
+  if (hs % 8) return cudaErrorInvalidValue;
+  const int work = (T * (hs / 8) + FP_THREADS - 1) / FP_THREADS;
+  return launch_pdl(k_conv0_pack, dim3(work + zero_blocks_for(Z)), dim3(FP_THREADS), 0, st, 1, x, d, base, T, hs, kn,
+                    gs, block, work, P, Z);
+}
+
+cudaError_t silu_pack(const float *g, const float *u, int T, int n, const PackDst &P, const ZeroSet &Z,
+                      cudaStream_t st) {
+  if (n % 8) return cudaErrorInvalidValue;
+  const int work = (T * (n / 8) + FP_THREADS - 1) / FP_THREADS;
+  return launch_pdl(k_silu_pack, dim3(work + zero_blocks_for(Z)), dim3(FP_THREADS), 0, st, 1, g, u, T, n, work, P, Z);
+}
+
+cudaError_t qk_norm_rope(float *q, int ldq, const float *wq, int hq, float *k, int ldk, const float *wk, int hk,
+                         const float *inv_freq, int T, int hd, float eps, bool rotary, const int64_t *pos0, int nseq,
+                         int block, cudaStream_t st) {
+  if (T <= 0) return cudaSuccess;
+  PosArgs pa;
+  for (int i = 0; i < MAX_BATCH; ++i) pa.pos0[i] = (pos0 && i < nseq) ? pos0[i] : 0;
+  for (int i = 0; i < 64; ++i) pa.inv[i] = i < hd / 2 ? inv_freq[i] : 0.f;
+  const int warps = T * (hq + hk);
+  const unsigned grid = (unsigned)((warps * 32 + 255) / 256);
+  if (hd == 128)
+    return launch_pdl(k_qk_norm_rope<128>, dim3(grid), dim3(256), 0, st, 1, q, ldq, wq, hq, k, ldk, wk, hk, T, eps,
+                      (int)rotary, pa, block);
+  if (hd == 64)
+    return launch_pdl(k_qk_norm_rope<64>, dim3(grid), dim3(256), 0, st, 1, q, ldq, wq, hq, k, ldk, wk, hk, T, eps,
+                      (int)rotary, pa, block);
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace dfl

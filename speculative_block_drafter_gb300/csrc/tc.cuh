@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "common.cuh"
+
 namespace dfl {
 
 constexpr unsigned DFL_ERR_TIMEOUT = 1u;
@@ -133,55 +135,6 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
 // Arrive on `bar` once every tcgen05.mma issued so far by this thread has completed.
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
-}
-
-// Byte offset of (row r, 16-byte chunk c) in a K-major tile of 64 f16 per row, 128-byte swizzle.
-__host__ __device__ __forceinline__ uint32_t sw128_off(int r, int c) {
-  return (uint32_t)((r >> 3) * 1024 + (r & 7) * 128 + ((c ^ (r & 7)) << 4));
-}
-
-// ---------------------------------------------------------------- token tiles
-// One 16-byte chunk (8 columns of one token row) of the packed token tiles:
-// per (token tile tt, k-tile kt, plane p) TT rows x 64 columns f16, K-major
-// with the 128-byte swizzle. Plane 0 = f16(x); plane 1 = f16(x - f16(x)).
-// Chunk t < ceil(T/TT) * (K/64) * TT * 8; rows past T are zero.
-template <int PLANES>
-__device__ __forceinline__ void pack_act_chunk(const float *__restrict__ X, int ldx, int T, int K, int TT,
-                                               uint4 *__restrict__ dst, int64_t t) {
-  const int KT = K / 64;
-  const int c = (int)(t & 7);
-  const int r = (int)((t >> 3) % TT);
-  const int64_t rest = (t >> 3) / TT;
-  const int kt = (int)(rest % KT);
-  const int tt = (int)(rest / KT);
-  const int tok = tt * TT + r;
-  float x[8];
-  if (tok < T) {
-    const float *src = X + (int64_t)tok * ldx + kt * 64 + c * 8;
-    if ((((uintptr_t)src) & 15) == 0) {
-      const float4 a = ((const float4 *)src)[0], b = ((const float4 *)src)[1];
-      x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
-      x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
-    } else {
-#pragma unroll
-      for (int i = 0; i < 8; ++i) x[i] = src[i];
-    }
-  } else {
-#pragma unroll
-    for (int i = 0; i < 8; ++i) x[i] = 0.f;
-  }
-  uint32_t hi[4], lo[4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    if (PLANES == 2) {
-      split2(x[2 * i], x[2 * i + 1], hi[i], lo[i]);
-    } else {
-      hi[i] = pack_half2(__float2half_rn(x[2 * i]), __float2half_rn(x[2 * i + 1]));
-    }
-  }
-  const int64_t base = (((int64_t)tt * KT + kt) * PLANES) * TT * 8;  // in 16-byte chunks
-  dst[base + sw128_off(r, c) / 16] = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-  if (PLANES == 2) dst[base + TT * 8 + sw128_off(r, c) / 16] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
 }
 
 }  // namespace dfl

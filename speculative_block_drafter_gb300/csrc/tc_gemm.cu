@@ -520,8 +520,8 @@ struct F16Cfg {
 };
 
 template <int TT>
-__global__ void __launch_bounds__(TC_THREADS) k_tc_f16(TcJobs J, const uint8_t *__restrict__ bpack, int K, int T,
-                                                       int kc, int atomic_out) {
+__global__ void __launch_bounds__(TC_THREADS) k_tc_f16(TcJobs J, const uint8_t *__restrict__ bpack, int bstride, int K,
+                                                       int T, int kc, int atomic_out) {
   using C = F16Cfg<TT>;
   constexpr int S = C::STAGES;
   extern __shared__ __align__(1024) uint8_t smraw[];
@@ -569,7 +569,7 @@ __global__ void __launch_bounds__(TC_THREADS) k_tc_f16(TcJobs J, const uint8_t *
 
   if (warp == TC_PRODUCER) {
     if (lane == 0) {
-      const uint8_t *bp = bpack + ((int64_t)tt * KT) * C::B_BYTES;
+      const uint8_t *bp = bpack + ((int64_t)tt * KT) * bstride;
       for (int i = 0; i < n; ++i) {
         const int s = i % S, kt = kt0 + i;
         const uint32_t st = smem_u32(sm + s * C::STAGE);
@@ -578,7 +578,7 @@ __global__ void __launch_bounds__(TC_THREADS) k_tc_f16(TcJobs J, const uint8_t *
           mbar_expect_tx(full0 + 8 * s, C::B_BYTES + 16384);
           bulk_g2s(st + C::A_OFF, wa + (int64_t)kt * 16384, 16384, full0 + 8 * s);
         }
-        bulk_g2s(st, bp + (int64_t)kt * C::B_BYTES, C::B_BYTES, full0 + 8 * s);
+        bulk_g2s(st, bp + (int64_t)kt * bstride, C::B_BYTES, full0 + 8 * s);
       }
     }
   } else if (warp == TC_MMA) {
@@ -779,14 +779,10 @@ static cudaError_t fill_jobs(const TcJob *jobs, int njobs, TcJobs &J, int &mtile
   return cudaSuccess;
 }
 
-template <int TT, int DU, int MT, int SA>
-static cudaError_t launch_int4(const TcJobs &J, int njobs, const float *X, int ldx, void *act, int K, int T, int ntt,
-                               int num_sms, const TcJob *jobs, cudaStream_t st) {
-  using C = I4<TT, DU, MT, SA>;
-  static bool configured = false;
-  cudaError_t e = set_smem(k_tc_int4<TT, DU, MT, SA>, C::SMEM, configured);
-  if (e != cudaSuccess) return e;
-  I4Items P{};
+// ---- four-bit: the partition of a launch
+template <int MT>
+static void plan_int4(const TcJobs &J, int njobs, int ntt, int K, int num_sms, I4Items &P, int &grid, bool &split) {
+  P = I4Items{};
   P.groups = 0;
   for (int j = 0; j < njobs; ++j) {
     P.gtile0[j] = P.groups;
@@ -795,13 +791,10 @@ static cudaError_t launch_int4(const TcJobs &J, int njobs, const float *X, int l
   P.gtile0[njobs] = P.groups;
   P.ntt = ntt;
   const int KT = K / 64;
-  const int64_t units = (int64_t)ntt * P.groups * KT;
-  if (units >= INT32_MAX) return cudaErrorInvalidValue;
-  P.units = (int)units;
+  P.units = (int)std::min<int64_t>((int64_t)ntt * P.groups * KT, INT32_MAX - 1);
   // two CTAs an SM, each at least 8 units long; whole groups a CTA when there are enough of them
   const int ngroups = ntt * P.groups;
-  int grid;
-  bool split = false;
+  split = false;
   if (ngroups >= 2 * num_sms) {
     P.whole = 1;
     grid = 2 * num_sms;
@@ -810,10 +803,68 @@ static cudaError_t launch_int4(const TcJobs &J, int njobs, const float *X, int l
     grid = (int)std::max<int64_t>(1, std::min<int64_t>(2 * num_sms, P.units / 8));
     for (int b = 1; b < grid && !split; ++b) split = ((int64_t)b * P.units / grid) % KT != 0;
   }
-  e = launch_pack(X, ldx, T, K, TT, 2, act, jobs, njobs, split, st);
+}
+
+template <int TT, int DU, int MT, int SA>
+static cudaError_t launch_int4(const TcJobs &J, int njobs, const void *act, int K, int T, int ntt, int num_sms,
+                               cudaStream_t st) {
+  using C = I4<TT, DU, MT, SA>;
+  static bool configured = false;
+  cudaError_t e = set_smem(k_tc_int4<TT, DU, MT, SA>, C::SMEM, configured);
   if (e != cudaSuccess) return e;
+  I4Items P;
+  int grid;
+  bool split;
+  plan_int4<MT>(J, njobs, ntt, K, num_sms, P, grid, split);
   return launch_pdl(k_tc_int4<TT, DU, MT, SA>, dim3(grid), dim3(C::THREADS), C::SMEM, st, 1, J, P,
                     (const uint8_t *)act, K, T);
+}
+
+// (token tile, quantisation units a k-tile, 128-row tiles an item, tensor-memory A slots)
+static cudaError_t dispatch_int4(const TcJobs &J, int njobs, int group, const void *act, int K, int T, int num_sms,
+                                 cudaStream_t st) {
+  const int TT = tt_int4(T);
+  const int ntt = (T + TT - 1) / TT;
+  const int DU = drain_units(group);
+  if (TT == 16) return DU == 1 ? launch_int4<16, 1, 2, 2>(J, njobs, act, K, T, ntt, num_sms, st)
+                               : launch_int4<16, 2, 2, 2>(J, njobs, act, K, T, ntt, num_sms, st);
+  return DU == 1 ? launch_int4<32, 1, 1, 2>(J, njobs, act, K, T, ntt, num_sms, st)
+                 : launch_int4<32, 2, 1, 2>(J, njobs, act, K, T, ntt, num_sms, st);
+}
+
+int tc_tile_rows(int T, bool int4) { return int4 ? tt_int4(T) : tt_f16(T); }
+
+bool tc_splits_int4(const TcJob *jobs, int njobs, int T, int K, int num_sms) {
+  TcJobs J;
+  int mtiles;
+  if (T > NARROW_MAX_T || fill_jobs(jobs, njobs, J, mtiles) != cudaSuccess) return false;
+  const int TT = tt_int4(T), ntt = (T + TT - 1) / TT;
+  I4Items P;
+  int grid;
+  bool split;
+  if (TT == 16) plan_int4<2>(J, njobs, ntt, K, num_sms, P, grid, split);
+  else plan_int4<1>(J, njobs, ntt, K, num_sms, P, grid, split);
+  return split;
+}
+
+bool tc_splits_f16(const TcJob *jobs, int njobs, int T, int K, int num_sms) {
+  TcJobs J;
+  int mtiles;
+  if (T > NARROW_MAX_T || fill_jobs(jobs, njobs, J, mtiles) != cudaSuccess) return false;
+  const int TT = tt_f16(T), ntt = (T + TT - 1) / TT;
+  int kc, splits;
+  plan(ntt, mtiles, K / 64, num_sms, 8, kc, splits);
+  return splits > 1;
+}
+
+cudaError_t tc_gemm_int4_packed(const TcJob *jobs, int njobs, int group, const void *act, int T, int K, int num_sms,
+                                cudaStream_t st) {
+  if (T > NARROW_MAX_T) return cudaErrorInvalidValue;
+  TcJobs J;
+  int mtiles;
+  cudaError_t e = fill_jobs(jobs, njobs, J, mtiles);
+  if (e != cudaSuccess) return e;
+  return dispatch_int4(J, njobs, group, act, K, T, num_sms, st);
 }
 
 cudaError_t tc_gemm_int4(const TcJob *jobs, int njobs, int group, const float *X, int ldx, int T, int K, void *act,
@@ -823,43 +874,45 @@ cudaError_t tc_gemm_int4(const TcJob *jobs, int njobs, int group, const float *X
   int mtiles;
   cudaError_t e = fill_jobs(jobs, njobs, J, mtiles);
   if (e != cudaSuccess) return e;
-  const int TT = tt_int4(T);
-  const int ntt = (T + TT - 1) / TT;
-  const int DU = drain_units(group);
-  // (token tile, quantisation units a k-tile, 128-row tiles an item, tensor-memory A slots)
-  if (TT == 16) return DU == 1 ? launch_int4<16, 1, 2, 2>(J, njobs, X, ldx, act, K, T, ntt, num_sms, jobs, st)
-                               : launch_int4<16, 2, 2, 2>(J, njobs, X, ldx, act, K, T, ntt, num_sms, jobs, st);
-  return DU == 1 ? launch_int4<32, 1, 1, 2>(J, njobs, X, ldx, act, K, T, ntt, num_sms, jobs, st)
-                 : launch_int4<32, 2, 1, 2>(J, njobs, X, ldx, act, K, T, ntt, num_sms, jobs, st);
+  e = launch_pack(X, ldx, T, K, tt_int4(T), 2, act, jobs, njobs, tc_splits_int4(jobs, njobs, T, K, num_sms), st);
+  if (e != cudaSuccess) return e;
+  return dispatch_int4(J, njobs, group, act, K, T, num_sms, st);
 }
 
+// ---- f16
 template <int TT>
-static cudaError_t launch_f16(const TcJobs &J, int mtiles, const float *X, int ldx, void *act, int K, int T, int ntt,
-                              int num_sms, const TcJob *jobs, int njobs, cudaStream_t st) {
+static cudaError_t launch_f16(const TcJobs &J, int mtiles, const void *act, int bstride, int K, int T, int ntt,
+                              int num_sms, cudaStream_t st) {
   using C = F16Cfg<TT>;
   static bool configured = false;
   cudaError_t e = set_smem(k_tc_f16<TT>, C::SMEM, configured);
   if (e != cudaSuccess) return e;
   int kc, splits;
   plan(ntt, mtiles, K / 64, num_sms, 8, kc, splits);
-  e = launch_pack(X, ldx, T, K, TT, 1, act, jobs, njobs, splits > 1, st);
-  if (e != cudaSuccess) return e;
   dim3 grid(ntt, mtiles, splits);
-  return launch_pdl(k_tc_f16<TT>, grid, dim3(TC_THREADS), C::SMEM, st, 1, J, (const uint8_t *)act, K, T, kc,
+  return launch_pdl(k_tc_f16<TT>, grid, dim3(TC_THREADS), C::SMEM, st, 1, J, (const uint8_t *)act, bstride, K, T, kc,
                     (int)(splits > 1));
+}
+
+cudaError_t tc_gemm_f16_packed(const TcJob *jobs, int njobs, const void *act, int bstride, int T, int K, int num_sms,
+                               cudaStream_t st) {
+  if (T > NARROW_MAX_T) return cudaErrorInvalidValue;
+  TcJobs J;
+  int mtiles;
+  cudaError_t e = fill_jobs(jobs, njobs, J, mtiles);
+  if (e != cudaSuccess) return e;
+  const int TT = tt_f16(T), ntt = (T + TT - 1) / TT;
+  return TT == 16 ? launch_f16<16>(J, mtiles, act, bstride, K, T, ntt, num_sms, st)
+                  : launch_f16<32>(J, mtiles, act, bstride, K, T, ntt, num_sms, st);
 }
 
 cudaError_t tc_gemm_f16(const TcJob *jobs, int njobs, const float *X, int ldx, int T, int K, void *act, int num_sms,
                         cudaStream_t st) {
   if (T > NARROW_MAX_T) return wide_jobs(jobs, njobs, false, 0, X, ldx, T, K, act, num_sms, st);
-  TcJobs J;
-  int mtiles;
-  cudaError_t e = fill_jobs(jobs, njobs, J, mtiles);
-  if (e != cudaSuccess) return e;
   const int TT = tt_f16(T);
-  const int ntt = (T + TT - 1) / TT;
-  return TT == 16 ? launch_f16<16>(J, mtiles, X, ldx, act, K, T, ntt, num_sms, jobs, njobs, st)
-                  : launch_f16<32>(J, mtiles, X, ldx, act, K, T, ntt, num_sms, jobs, njobs, st);
+  cudaError_t e = launch_pack(X, ldx, T, K, TT, 1, act, jobs, njobs, tc_splits_f16(jobs, njobs, T, K, num_sms), st);
+  if (e != cudaSuccess) return e;
+  return tc_gemm_f16_packed(jobs, njobs, act, TT * 128, T, K, num_sms, st);
 }
 
 cudaError_t read_device_error(unsigned *out, bool reset) {
