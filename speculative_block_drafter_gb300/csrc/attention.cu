@@ -345,8 +345,10 @@ __global__ void k_attn_merge(const float *__restrict__ part, int heads, int kv, 
 // The same merge written straight into the token tiles of the output
 // projection (hi/lo planes; a thread per 8 columns of a query row), with the
 // projection's outputs cleared by the blocks past the work grid when it splits.
+constexpr int MERGE_THREADS = 32;  // small CTAs: the work is a few thousand threads of dependent loads
+
 template <int HD>
-__global__ void __launch_bounds__(256) k_attn_merge_pack(const float *__restrict__ part, int heads, int kv, int R,
+__global__ void __launch_bounds__(MERGE_THREADS) k_attn_merge_pack(const float *__restrict__ part, int heads, int kv, int R,
                                                          int nsplit, int work_blocks, PackDst P, ZeroSet Z) {
   pdl_wait();
   pdl_trigger();  // the GEMM this feeds may fetch its weights meanwhile
@@ -357,7 +359,7 @@ __global__ void __launch_bounds__(256) k_attn_merge_pack(const float *__restrict
   constexpr int D8 = HD / 8;
   const int b = blockIdx.y;
   const int rep = heads / kv, Q = rep * R;
-  const int id = blockIdx.x * 256 + threadIdx.x;
+  const int id = blockIdx.x * MERGE_THREADS + threadIdx.x;
   if (id >= kv * Q * D8) return;
   const int qa = id / D8, d8 = id - qa * D8;
   const int g = qa / Q, qi = qa - g * Q;
@@ -400,12 +402,12 @@ static cudaError_t launch_attn(const float *q, const float *k, const float *v, c
   if (e != cudaSuccess) return e;
   const int Q = heads / kv * R;
   if (pack) {
-    const int work = (kv * Q * (HD / 8) + 255) / 256;
+    const int work = (kv * Q * (HD / 8) + MERGE_THREADS - 1) / MERGE_THREADS;
     int64_t most = 0;
     for (int j = 0; j < zero->count; ++j) most = std::max<int64_t>(most, zero->n[j]);
-    const int zb = zero->count ? (int)std::min<int64_t>((most + 1023) / 1024, 128) : 0;
-    return launch_pdl(k_attn_merge_pack<HD>, dim3(work + zb, batch), dim3(256), 0, st, 1, part, heads, kv, R, ns, work,
-                      *pack, *zero);
+    const int zb = zero->count ? (int)std::min<int64_t>((most + 4 * MERGE_THREADS - 1) / (4 * MERGE_THREADS), 256) : 0;
+    return launch_pdl(k_attn_merge_pack<HD>, dim3(work + zb, batch), dim3(MERGE_THREADS), 0, st, 1, part, heads, kv, R,
+                      ns, work, *pack, *zero);
   }
   dim3 g2(kv * Q, batch);
   return launch_pdl(k_attn_merge<HD>, g2, dim3(HD), 0, st, 1, part, heads, kv, R, ns, y);

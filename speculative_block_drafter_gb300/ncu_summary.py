@@ -1,12 +1,12 @@
 """Summarise an ncu launch list (``--metrics gpu__time_duration.sum --csv``) per kernel.
 
-    python -m speculative_block_drafter_gb300.ncu_summary launches.csv [--period-start NAME] [--step-launches N]
+    python -m speculative_block_drafter_gb300.ncu_summary launches.csv [--after NAME] [--step-launches N]
 
 Prints, per kernel name (template arguments kept, parameter list dropped), the
 number of launches, the total device time and its share of the total. With
-``--period-start`` and ``--step-launches`` it also cuts out one step: the last
-complete window of N launches that starts with a kernel whose name begins with
-NAME, and prints the same table for it. ncu serialises launches and runs each
+``--after`` and ``--step-launches`` it also cuts out one step: the last
+complete window of N of the library's launches that follows a launch whose
+name begins with NAME (the step's last kernel), and prints the same table. ncu serialises launches and runs each
 one cold, so the absolute times are longer than in a graph replay; the shares
 are what compare.
 """
@@ -55,16 +55,16 @@ def table(launches, title):
 def main():
     p = argparse.ArgumentParser()
     p.add_argument("csv")
-    p.add_argument("--period-start", default=None)
+    p.add_argument("--after", default=None)
     p.add_argument("--step-launches", type=int, default=0)
     a = p.parse_args()
     launches = read(a.csv)
     ours = [x for x in launches if not x[0].startswith("at::")]
     print(table(launches, "whole run"))
-    if a.period_start and a.step_launches:
-        starts = [i for i, x in enumerate(ours) if x[0].startswith(a.period_start)]
-        windows = [i for i in starts if i + a.step_launches <= len(ours)
-                   and all(ours[j][0].split("<")[0] != "k_tc_pack_int4" for j in range(i, i + a.step_launches))]
+    if a.after and a.step_launches:
+        ends = [i for i, x in enumerate(ours) if x[0].startswith(a.after)]
+        windows = [i + 1 for i in ends if i + 1 + a.step_launches <= len(ours)
+                   and ours[i + a.step_launches][0].startswith(a.after)]
         if windows:
             i = windows[-1]
             print()
