@@ -4,60 +4,90 @@
 // row) over the context and the block's rows, a row further on seeing less
 // far back when the layer has a window, a max-subtracted softmax).
 //
-// Split-K: the context rows of a sequence are cut into chunks, one CTA per
-// (chunk, KV head, sequence), plus one CTA per (KV head, sequence) for the
-// block's own rows. Each keeps a running maximum m, sum l and unnormalised
-// output o per query (the rep = heads/kv_heads query heads of the KV head times
-// the block rows) and a second kernel merges the chunks.
+// Split-K: the context rows of a sequence are cut into splits of whole 64-key
+// chunks, one CTA per (split, KV head, sequence); the last split of a sequence
+// also takes the block's own rows. Each keeps a running maximum m, sum l and
+// unnormalised output o per query (the rep = heads/kv_heads query heads of the
+// KV head times the block rows) and a second kernel merges the splits.
+#include <cudaTypedefs.h>
+
 #include <algorithm>
+#include <climits>
 
 #include "common.cuh"
 #include "kernels.h"
+#include "tc.cuh"
 
 namespace dfl {
 
 constexpr int ATT_THREADS = 256;
 constexpr int CH = 64;              // keys per chunk
 constexpr int QMAX = 64;            // queries per CTA (rep * block)
-// Split-K aims at one wave: a CTA (about 170 KB of shared memory) per SM.
 
 struct AttnArgs {
   AttnSeq seq[MAX_BATCH];
+  CUtensorMap own_k, own_v;
 };
 
-// Chunks a split takes: one wave of the context's CTAs over the SMs that the
-// block's own CTAs (one per sequence and KV head) leave free.
-static int chunks_per_split(int batch, int kv, int max_n, int num_sms) {
-  const int chunks = (max_n + CH - 1) / CH;
-  const int units = batch * kv * chunks;
-  const int ctas = std::max(num_sms - batch * kv, batch * kv);
-  return std::max(1, (units + ctas - 1) / ctas);
+// Splits per (sequence, KV head) and chunks per split: the split count whose
+// waves of CTAs (one an SM) finish first, counting a split's fixed cost (its
+// pipeline fill and merge) as two chunks; at most 1024 + 2 * pairs CTAs.
+static void plan_splits(int pairs, int max_n, int num_sms, int &ns, int &cps) {
+  const int chunks = std::max(1, (max_n + CH - 1) / CH);
+  int64_t best = INT64_MAX;
+  ns = 1;
+  cps = chunks;
+  for (int want = 1; want <= chunks && (int64_t)pairs * want <= 1024 + 2 * (int64_t)pairs; ++want) {
+    const int c = (chunks + want - 1) / want, n = (chunks + c - 1) / c;
+    const int64_t waves = ((int64_t)pairs * n + num_sms - 1) / num_sms;
+    const int64_t cost = waves * (c + 2);
+    if (cost < best) {
+      best = cost;
+      ns = n;
+      cps = c;
+    }
+  }
 }
 
 size_t attn_partial_bytes(int max_batch, int kv_heads, int heads, int block, int hd) {
   const int Q = heads / kv_heads * block;
-  // per (sequence, KV head): at most ceil(units / ctas) + 1 context splits (ctas >= batch * kv), plus
-  // the block's own; bounded for any SM count up to 1024
+  // one partial per CTA: at most 1024 + 2 * batch * kv of them (plan_splits)
   const size_t worst = (size_t)1024 + 3 * (size_t)max_batch * kv_heads;
   return worst * Q * (hd + 2) * sizeof(float);
 }
 
-// ---- fragments (mma.sync m16n8k16, f16 in, f32 accumulate)
-__device__ __forceinline__ void ldsm4(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-               : "r"(addr));
+// ---------------------------------------------------------------- tensor maps
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+    void *f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      f = nullptr;
+    return (PFN_cuTensorMapEncodeTiled_v12000)f;
+  }();
+  return fn;
 }
-__device__ __forceinline__ void ldsm4t(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-               : "r"(addr));
+
+bool attn_kv_map(CUtensorMap *m, const float *base, int64_t rows, int kv, int hd, int box_rows) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
+  if (!enc || rows < 1 || rows > INT32_MAX || box_rows < 1 || box_rows > 256 || hd % 32) return false;
+  const cuuint64_t dims[3] = {(cuuint64_t)hd, (cuuint64_t)kv, (cuuint64_t)rows};
+  const cuuint64_t strides[2] = {(cuuint64_t)hd * 4, (cuuint64_t)kv * hd * 4};
+  const cuuint32_t box[3] = {32, 1, (cuuint32_t)box_rows};
+  const cuuint32_t es[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, (void *)base, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
-__device__ __forceinline__ uint32_t cvta_smem(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, bool valid) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(valid ? 16 : 0));
+
+__device__ __forceinline__ void tma_load3(uint32_t dst, const CUtensorMap *m, int x, int y, int z, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
+      "[%5];" ::"r"(dst),
+      "l"((uint64_t)m), "r"(x), "r"(y), "r"(z), "r"(bar)
+      : "memory");
 }
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
 // Three-term product of f16 hi/lo pairs: acc += ah.bh + ah.bl + al.bh (about 22 bits).
 __device__ __forceinline__ void mma3(float (&acc)[4], const uint32_t (&ah)[4], const uint32_t (&al)[4], uint32_t bh0,
@@ -67,134 +97,145 @@ __device__ __forceinline__ void mma3(float (&acc)[4], const uint32_t (&ah)[4], c
   mma16816(acc, al, bh0, bh1);
 }
 
-template <int HD>
-struct AttnSmem {
-  static constexpr int LD = HD + 8;                       // halves per row (16-byte pad: no ldmatrix conflicts)
-  static constexpr int QPLANE = QMAX * LD;                // halves
-  static constexpr int KPLANE = CH * LD;
-  static constexpr int STAGE_F = 2 * CH * HD;             // f32 staging of K and V
-  static constexpr int MERGE_F = 8 * 16 * (HD + 2);       // per-warp partials for the in-CTA merge
-  static constexpr int SCRATCH_F = STAGE_F > MERGE_F ? STAGE_F : MERGE_F;
-  static constexpr size_t BYTES = (size_t)(2 * QPLANE + 4 * KPLANE) * 2 + (size_t)SCRATCH_F * 4;
+// ---------------------------------------------------------------- the split kernel
+//
+// One CTA per (split, KV head, sequence): the rep*R queries of the KV head over
+// the split's context keys in chunks of 64 (the last split also takes the
+// block's own R rows as a final chunk). Warp 0 loads each chunk's K and V with
+// 8 tensor copies (4 column quarters each, 128-byte swizzled) into a 3-stage
+// ring; the MMA fragments are built from the f32 rows with their hi/lo f16
+// split on the fly, the queries' hi/lo fragments stay in registers. Warp w
+// takes query block w % QW and key group w / QW of every chunk; each keeps a
+// running (m, l, o), merged in the CTA at the end.
+//
+// Within a k16 step the head dimensions are taken in the order that makes each
+// lane's four K values one 16-byte load: step ks, lane quad cq covers
+// dimensions 32 (ks / 2) + 4 (2 cq + ks % 2) + 0..3, the queries' fragments
+// follow the same order. Rows past a chunk's keys (the context's end, or the
+// block's own R rows) hold whatever the copy brought: their scores are masked
+// and their V values replaced by zero.
+struct AttnRing {
+  static constexpr int QUARTER = CH * 128;   // 64 rows x 32 floats
+  static constexpr int HALF = 4 * QUARTER;   // K or V of a chunk (hd = 128)
+  static constexpr int STAGE = 2 * HALF;
+  static constexpr int STAGES = 3;
+  static constexpr size_t BYTES = (size_t)STAGES * STAGE + 1024 + 64;  // + alignment, barriers
 };
 
-// One CTA per (split, KV head, sequence): the rep*R queries of the KV head over
-// the split's keys, in chunks of 64. Warp w takes query block w % QW and key
-// group w / QW (a quarter or half of each chunk); each keeps a running (m, l, o)
-// that the CTA merges at the end.
 template <int HD, int KG>
-__global__ void __launch_bounds__(ATT_THREADS) k_attn(const float *__restrict__ q, const float *__restrict__ k,
-                                                      const float *__restrict__ v, AttnArgs args, int heads, int kv,
-                                                      int R, int window, float scale, int nsplit, int cps,
-                                                      float *__restrict__ part) {
-  pdl_wait();
-  using SM = AttnSmem<HD>;
-  constexpr int KW = CH / KG;      // keys per warp per chunk
-  constexpr int NT = KW / 8;       // n8 tiles of scores
-  constexpr int KS = KW / 16;      // k16 steps of P . V
-  constexpr int OT = HD / 8;       // n8 tiles of the output
-  extern __shared__ __align__(16) uint8_t smb[];
-  __half *Qh = (__half *)smb, *Ql = Qh + SM::QPLANE;
-  __half *Kh = Ql + SM::QPLANE, *Kl = Kh + SM::KPLANE, *Vh = Kl + SM::KPLANE, *Vl = Vh + SM::KPLANE;
-  float *scr = (float *)(Vl + SM::KPLANE);
+__global__ void __launch_bounds__(ATT_THREADS, 1) k_attn(const float *__restrict__ q, const __grid_constant__ AttnArgs args,
+                                                         int heads, int kv, int R, int window, float scale, int nsplit,
+                                                         int cps, float *__restrict__ part) {
+  using RG = AttnRing;
+  constexpr int S = RG::STAGES;
+  constexpr int HQ = HD / 32;        // column quarters (boxes) of a row
+  constexpr int KW = CH / KG;        // keys per warp per chunk
+  constexpr int NT = KW / 8;         // n8 tiles of scores
+  constexpr int KS = KW / 16;        // k16 steps of P . V
+  constexpr int OT = HD / 8;         // n8 tiles of the output
+  extern __shared__ __align__(16) uint8_t smraw[];
+  uint8_t *sm = smraw + ((1024 - (smem_u32(smraw) & 1023)) & 1023);
+  const uint32_t ring = smem_u32(sm);
+  const uint32_t full0 = ring + S * RG::STAGE, empty0 = full0 + 8 * S;
 
   const int sp = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
   const int rep = heads / kv, Q = rep * R;
   const int QW = (Q + 15) / 16;
-  const AttnSeq S = args.seq[b];
-  const bool own = sp == nsplit;
-  const int kbeg = own ? 0 : sp * cps * CH;
-  const int kend = own ? R : min(S.n, kbeg + cps * CH);
-  const float *kbase = own ? k + (int64_t)b * R * kv * HD : S.ck;
-  const float *vbase = own ? v + (int64_t)b * R * kv * HD : S.cv;
+  const AttnSeq &Sq = args.seq[b];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, gq = lane >> 2, cq = lane & 3;
   const int qb = warp % QW, kgi = warp / QW;
   const bool busy = kgi < KG && warp < QW * KG;
+  const int nwarps = ATT_THREADS / 32;
 
-  // f32 rows of one chunk into the staging area
-  auto stage = [&](int kb) {
-    for (int i = tid; i < 2 * CH * (HD / 4); i += ATT_THREADS) {
-      const int which = i / (CH * (HD / 4)), rem = i % (CH * (HD / 4));
-      const int j = rem / (HD / 4), c4 = rem % (HD / 4);
-      const int key = kb + j;
-      const bool ok = key < kend;
-      const float *src = (which ? vbase : kbase) + ((int64_t)(ok ? key : kbeg) * kv + g) * HD + c4 * 4;
-      cp_async16(cvta_smem(scr + which * CH * HD + j * HD + c4 * 4), src, ok);
+  // this CTA's chunks: context chunks [c0, c1), then the block's own rows if last
+  const int n = Sq.n;
+  const int nctx = (n + CH - 1) / CH;
+  const int c0 = min(nctx, sp * cps), c1 = min(nctx, c0 + cps);
+  const bool own = sp == nsplit - 1;
+  const int nch = (c1 - c0) + (own ? 1 : 0);
+
+  if (tid == 0) {
+    for (int i = 0; i < S; ++i) {
+      mbar_init(full0 + 8 * i, 1);
+      mbar_init(empty0 + 8 * i, nwarps);
     }
-    asm volatile("cp.async.commit_group;");
+    mbar_fence_init();
+  }
+  pdl_wait();
+  __syncthreads();
+
+  // warp 0, lane 0: the 2 * HQ tensor copies of chunk j into stage st
+  auto fill = [&](int j, int st) {
+    if (lane != 0) return;
+    const bool is_own = own && j == nch - 1;
+    const CUtensorMap *km = is_own ? &args.own_k : &Sq.kmap;
+    const CUtensorMap *vm = is_own ? &args.own_v : &Sq.vmap;
+    const int z = is_own ? b * R : (int)(Sq.row0 + (int64_t)(c0 + j) * CH);
+    const uint32_t rows = is_own ? R : CH;
+    const uint32_t bar = full0 + 8 * st, kd = ring + st * RG::STAGE, vd = kd + RG::HALF;
+    mbar_expect_tx(bar, 2 * HQ * rows * 128);
+#pragma unroll
+    for (int h = 0; h < HQ; ++h) {
+      tma_load3(kd + h * RG::QUARTER, km, 32 * h, g, z, bar);
+      tma_load3(vd + h * RG::QUARTER, vm, 32 * h, g, z, bar);
+    }
   };
-  if (kbeg < kend) stage(kbeg);
+  int issued = 0;  // chunks warp 0 has filled
+  if (warp == 0)
+    for (; issued < S && issued < nch; ++issued) fill(issued, issued);
 
-  // the queries, hi/lo: every load of the thread first, then the conversions
+  // the queries' hi/lo A fragments (rows qb*16 + gq and + 8), dimensions in the load order
+  uint32_t qh[HD / 16][4], ql[HD / 16][4];
+  const int qi0 = qb * 16 + gq, qi1 = qi0 + 8;
   {
-    constexpr int PER = QMAX * HD / 4 / ATT_THREADS;  // float4 a thread
-    float4 xv[PER];
+    const float *q0 = nullptr, *q1 = nullptr;
+    if (qi0 < Q) q0 = q + ((int64_t)b * R + qi0 % R) * heads * HD + (g * rep + qi0 / R) * HD;
+    if (qi1 < Q) q1 = q + ((int64_t)b * R + qi1 % R) * heads * HD + (g * rep + qi1 / R) * HD;
 #pragma unroll
-    for (int m = 0; m < PER; ++m) {
-      const int i = tid + m * ATT_THREADS;
-      const int qi = i / (HD / 4), d4 = i % (HD / 4);
-      xv[m] = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (qi < Q) {
-        const int hrep = qi / R, r = qi - hrep * R;
-        xv[m] = *(const float4 *)(q + ((int64_t)b * R + r) * heads * HD + (g * rep + hrep) * HD + 4 * d4);
-      }
-    }
-#pragma unroll
-    for (int m = 0; m < PER; ++m) {
-      const int i = tid + m * ATT_THREADS;
-      const int qi = i / (HD / 4), d4 = i % (HD / 4);
-      uint32_t h0, l0, h1, l1;
-      split2(xv[m].x, xv[m].y, h0, l0);
-      split2(xv[m].z, xv[m].w, h1, l1);
-      *(uint2 *)(Qh + qi * SM::LD + 4 * d4) = make_uint2(h0, h1);
-      *(uint2 *)(Ql + qi * SM::LD + 4 * d4) = make_uint2(l0, l1);
+    for (int ks = 0; ks < HD / 16; ++ks) {
+      const int c = 32 * (ks >> 1) + 4 * (2 * cq + (ks & 1));
+      const float4 x0 = q0 ? *(const float4 *)(q0 + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+      const float4 x1 = q1 ? *(const float4 *)(q1 + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+      split2(x0.x, x0.y, qh[ks][0], ql[ks][0]);
+      split2(x1.x, x1.y, qh[ks][1], ql[ks][1]);
+      split2(x0.z, x0.w, qh[ks][2], ql[ks][2]);
+      split2(x1.z, x1.w, qh[ks][3], ql[ks][3]);
     }
   }
+  const int r0 = qi0 % R, r1 = qi1 % R;
 
   float o[OT][4];
 #pragma unroll
   for (int t = 0; t < OT; ++t) o[t][0] = o[t][1] = o[t][2] = o[t][3] = 0.f;
-  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;  // rows gq and gq + 8 of the warp's block
-  const int qi0 = qb * 16 + gq, qi1 = qi0 + 8;
-  const int r0 = qi0 % R, r1 = qi1 % R;
+  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+  bool ok = true;
 
-  for (int kb = kbeg; kb < kend; kb += CH) {
-    cp_async_wait_all();
-    __syncthreads();
-    // staging -> hi/lo planes
-    for (int i = tid; i < 2 * CH * HD / 2; i += ATT_THREADS) {
-      const int which = i / (CH * HD / 2), rem = i % (CH * HD / 2);
-      const int j = rem / (HD / 2), d2 = rem % (HD / 2);
-      const float2 x = *(const float2 *)(scr + which * CH * HD + j * HD + 2 * d2);
-      uint32_t hi, lo;
-      split2(x.x, x.y, hi, lo);
-      __half *ph = which ? Vh : Kh, *pl = which ? Vl : Kl;
-      *(uint32_t *)(ph + j * SM::LD + 2 * d2) = hi;
-      *(uint32_t *)(pl + j * SM::LD + 2 * d2) = lo;
-    }
-    __syncthreads();
-    if (kb + CH < kend) stage(kb + CH);
-
+  for (int j = 0; j < nch && ok; ++j) {
+    const int st = j % S;
+    ok = mbar_wait(full0 + 8 * st, (j / S) & 1);
+    ok = __all_sync(0xffffffffu, ok);
+    if (!ok) break;
+    const bool is_own = own && j == nch - 1;
+    const int kb = (c0 + j) * CH;
+    const int cnt = is_own ? R : min(CH, n - kb);
+    const uint8_t *Ks = sm + st * RG::STAGE, *Vs = Ks + RG::HALF;
     if (busy) {
-      // scores S = Q . K^T over the warp's keys
+      const int kk0 = kgi * KW;
       float sc[NT][4];
 #pragma unroll
       for (int t = 0; t < NT; ++t) sc[t][0] = sc[t][1] = sc[t][2] = sc[t][3] = 0.f;
-      const int kk0 = kgi * KW;
+      // S = Q . K^T over the warp's keys; row kk0 + 8t + gq has swizzle phase gq
 #pragma unroll
       for (int ks = 0; ks < HD / 16; ++ks) {
-        uint32_t ah[4], al[4];
-        const int qrow = qb * 16 + (lane & 7) + 8 * ((lane >> 3) & 1), qcol = ks * 16 + 8 * (lane >> 4);
-        ldsm4(cvta_smem(Qh + qrow * SM::LD + qcol), ah[0], ah[1], ah[2], ah[3]);
-        ldsm4(cvta_smem(Ql + qrow * SM::LD + qcol), al[0], al[1], al[2], al[3]);
 #pragma unroll
-        for (int np = 0; np < NT / 2; ++np) {
-          const int krow = kk0 + np * 16 + (lane & 7) + 8 * (lane >> 4), kcol = ks * 16 + 8 * ((lane >> 3) & 1);
-          uint32_t h0, h1, h2, h3, w0, w1, w2, w3;
-          ldsm4(cvta_smem(Kh + krow * SM::LD + kcol), h0, h1, h2, h3);
-          ldsm4(cvta_smem(Kl + krow * SM::LD + kcol), w0, w1, w2, w3);
-          mma3(sc[2 * np], ah, al, h0, h1, w0, w1);
-          mma3(sc[2 * np + 1], ah, al, h2, h3, w2, w3);
+        for (int t = 0; t < NT; ++t) {
+          const int row = kk0 + 8 * t + gq;
+          const float4 kx = *(const float4 *)(Ks + (ks >> 1) * RG::QUARTER + row * 128 +
+                                              (((2 * cq + (ks & 1)) ^ gq) << 4));
+          uint32_t bh0, bl0, bh1, bl1;
+          split2(kx.x, kx.y, bh0, bl0);
+          split2(kx.z, kx.w, bh1, bl1);
+          mma3(sc[t], qh[ks], ql[ks], bh0, bh1, bl0, bl1);
         }
       }
       // mask, scale, online softmax (rows gq, gq+8; the 4 lanes of a row hold its 2*NT keys)
@@ -203,12 +244,12 @@ __global__ void __launch_bounds__(ATT_THREADS) k_attn(const float *__restrict__ 
       for (int t = 0; t < NT; ++t) {
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          const int key = kb + kk0 + t * 8 + 2 * cq + (e & 1);
+          const int key = kk0 + t * 8 + 2 * cq + (e & 1);
           const int qi = (e < 2) ? qi0 : qi1;
           const int rr = (e < 2) ? r0 : r1;
-          bool ok = key < kend && qi < Q;
-          if (ok && !own && window > 0) ok = S.lo + key >= S.anchor + rr + 1 - window;
-          const float x = ok ? sc[t][e] * scale : -INFINITY;
+          bool vis = key < cnt && qi < Q;
+          if (vis && !is_own && window > 0) vis = Sq.lo + kb + key >= Sq.anchor + rr + 1 - window;
+          const float x = vis ? sc[t][e] * scale : -INFINITY;
           sc[t][e] = x;
           if (e < 2) mx0 = fmaxf(mx0, x);
           else mx1 = fmaxf(mx1, x);
@@ -242,7 +283,8 @@ __global__ void __launch_bounds__(ATT_THREADS) k_attn(const float *__restrict__ 
         o[t][2] *= a1;
         o[t][3] *= a1;
       }
-      // O += P . V, P as hi/lo A fragments straight from the score registers
+      // O += P . V: P as hi/lo A fragments from the scores; V rows kA, kA+1, kA+8,
+      // kA+9 (swizzle phases 2cq, 2cq+1) at dimension 8t + gq
 #pragma unroll
       for (int js = 0; js < KS; ++js) {
         uint32_t ph[4], pl[4];
@@ -250,23 +292,47 @@ __global__ void __launch_bounds__(ATT_THREADS) k_attn(const float *__restrict__ 
         split2(sc[2 * js][2], sc[2 * js][3], ph[1], pl[1]);
         split2(sc[2 * js + 1][0], sc[2 * js + 1][1], ph[2], pl[2]);
         split2(sc[2 * js + 1][2], sc[2 * js + 1][3], ph[3], pl[3]);
-        const int vrow = kk0 + js * 16 + (lane & 7) + 8 * ((lane >> 3) & 1);
+        const int kA = kk0 + 16 * js + 2 * cq;
+        const bool v0 = kA < cnt, v1 = kA + 1 < cnt, v2 = kA + 8 < cnt, v3 = kA + 9 < cnt;
+        const uint8_t *va = Vs + kA * 128 + ((gq & 3) << 2);
 #pragma unroll
-        for (int tp = 0; tp < OT / 2; ++tp) {
-          const int vcol = tp * 16 + 8 * (lane >> 4);
-          uint32_t h0, h1, h2, h3, w0, w1, w2, w3;
-          ldsm4t(cvta_smem(Vh + vrow * SM::LD + vcol), h0, h1, h2, h3);
-          ldsm4t(cvta_smem(Vl + vrow * SM::LD + vcol), w0, w1, w2, w3);
-          mma3(o[2 * tp], ph, pl, h0, h1, w0, w1);
-          mma3(o[2 * tp + 1], ph, pl, h2, h3, w2, w3);
+        for (int t = 0; t < OT; ++t) {
+          const int c = (2 * t + (gq >> 2)) & 7;
+          const uint8_t *vq = va + (t >> 2) * RG::QUARTER;
+          const float *e0 = (const float *)(vq + ((c ^ (2 * cq)) << 4));
+          const float *e1 = (const float *)(vq + 128 + ((c ^ (2 * cq + 1)) << 4));
+          float x0 = e0[0], x1 = e1[0], x2 = e0[256], x3 = e1[256];  // rows +8: 1024 bytes on
+          x0 = v0 ? x0 : 0.f;
+          x1 = v1 ? x1 : 0.f;
+          x2 = v2 ? x2 : 0.f;
+          x3 = v3 ? x3 : 0.f;
+          uint32_t bh0, bl0, bh1, bl1;
+          split2(x0, x1, bh0, bl0);
+          split2(x2, x3, bh1, bl1);
+          mma3(o[t], ph, pl, bh0, bh1, bl0, bl1);
         }
       }
     }
+    // release the stage; warp 0 refills it with the chunk S ahead
+    __syncwarp();
+    if (lane == 0) mbar_arrive(empty0 + 8 * st);
+    if (warp == 0 && j + S < nch) {
+      ok = mbar_wait(empty0 + 8 * st, (j / S) & 1);
+      ok = __all_sync(0xffffffffu, ok);
+      if (ok) {
+        fill(j + S, st);
+        ++issued;
+      }
+    }
   }
-  cp_async_wait_all();
+  // every copy issued has landed before the ring becomes the merge scratch (on
+  // the error path too: each stage's latest fill, a bounded wait each)
+  if (warp == 0)
+    for (int j = max(0, issued - S); j < issued; ++j) mbar_wait(full0 + 8 * (j % S), (j / S) & 1);
   __syncthreads();
 
   // in-CTA merge of the key groups: per warp 16 rows x (o, m, l) in the scratch
+  float *scr = (float *)sm;
   l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
   l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
   l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
@@ -288,7 +354,7 @@ __global__ void __launch_bounds__(ATT_THREADS) k_attn(const float *__restrict__ 
     }
   }
   __syncthreads();
-  float *out = part + ((int64_t)(b * kv + g) * (nsplit + 1) + sp) * Q * (HD + 2);
+  float *out = part + ((int64_t)(b * kv + g) * nsplit + sp) * Q * (HD + 2);
   // one warp per query row at a time: the key groups' weights once, then the row
   for (int qi = warp; qi < Q; qi += ATT_THREADS / 32) {
     const int qbk = qi / 16, rr = qi % 16;
@@ -384,21 +450,21 @@ __global__ void __launch_bounds__(MERGE_THREADS) k_attn_merge_pack(const float *
 }
 
 template <int HD, int KG>
-static cudaError_t launch_attn(const float *q, const float *k, const float *v, const AttnArgs &args, int batch,
-                               int max_n, int heads, int kv, int R, int window, float scale, float *part, float *y,
-                               int num_sms, const PackDst *pack, const ZeroSet *zero, cudaStream_t st) {
-  const size_t smem = AttnSmem<HD>::BYTES;
+static cudaError_t launch_attn(const float *q, const AttnArgs &args, int batch, int max_n, int heads, int kv, int R,
+                               int window, float scale, float *part, float *y, int num_sms, const PackDst *pack,
+                               const ZeroSet *zero, cudaStream_t st) {
+  const size_t smem = AttnRing::BYTES;
   static bool configured = false;
   if (!configured) {
     cudaError_t e = cudaFuncSetAttribute(k_attn<HD, KG>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  const int cps = chunks_per_split(batch, kv, max_n, num_sms);
-  const int ns = max_n > 0 ? ((max_n + CH - 1) / CH + cps - 1) / cps : 0;
-  dim3 grid(ns + 1, kv, batch);
-  cudaError_t e = launch_pdl(k_attn<HD, KG>, grid, dim3(ATT_THREADS), smem, st, 1, q, k, v, args, heads, kv, R, window,
-                             scale, ns, cps, part);
+  int ns, cps;
+  plan_splits(batch * kv, max_n, num_sms, ns, cps);
+  dim3 grid(ns, kv, batch);
+  cudaError_t e = launch_pdl(k_attn<HD, KG>, grid, dim3(ATT_THREADS), smem, st, 1, q, args, heads, kv, R, window, scale,
+                             ns, cps, part);
   if (e != cudaSuccess) return e;
   const int Q = heads / kv * R;
   if (pack) {
@@ -407,47 +473,52 @@ static cudaError_t launch_attn(const float *q, const float *k, const float *v, c
     for (int j = 0; j < zero->count; ++j) most = std::max<int64_t>(most, zero->n[j]);
     const int zb = zero->count ? (int)std::min<int64_t>((most + 4 * MERGE_THREADS - 1) / (4 * MERGE_THREADS), 256) : 0;
     return launch_pdl(k_attn_merge_pack<HD>, dim3(work + zb, batch), dim3(MERGE_THREADS), 0, st, 1, part, heads, kv, R,
-                      ns, work, *pack, *zero);
+                      ns - 1, work, *pack, *zero);
   }
   dim3 g2(kv * Q, batch);
-  return launch_pdl(k_attn_merge<HD>, g2, dim3(HD), 0, st, 1, part, heads, kv, R, ns, y);
+  return launch_pdl(k_attn_merge<HD>, g2, dim3(HD), 0, st, 1, part, heads, kv, R, ns - 1, y);
 }
 
 template <int HD>
-static cudaError_t launch_attn_hd(const float *q, const float *k, const float *v, const AttnArgs &args, int batch,
-                                  int max_n, int heads, int kv, int R, int window, float scale, float *part, float *y,
-                                  int num_sms, const PackDst *pack, const ZeroSet *zero, cudaStream_t st) {
+static cudaError_t launch_attn_hd(const float *q, const AttnArgs &args, int batch, int max_n, int heads, int kv, int R,
+                                  int window, float scale, float *part, float *y, int num_sms, const PackDst *pack,
+                                  const ZeroSet *zero, cudaStream_t st) {
   const int QW = (heads / kv * R + 15) / 16;
   if (QW >= 3)
-    return launch_attn<HD, 2>(q, k, v, args, batch, max_n, heads, kv, R, window, scale, part, y, num_sms, pack, zero,
-                              st);
-  return launch_attn<HD, 4>(q, k, v, args, batch, max_n, heads, kv, R, window, scale, part, y, num_sms, pack, zero,
-                            st);
+    return launch_attn<HD, 2>(q, args, batch, max_n, heads, kv, R, window, scale, part, y, num_sms, pack, zero, st);
+  return launch_attn<HD, 4>(q, args, batch, max_n, heads, kv, R, window, scale, part, y, num_sms, pack, zero, st);
 }
 
-cudaError_t attention(const float *q, const float *k, const float *v, const AttnSeq *seqs, int batch, int max_ctx,
-                      int heads, int kv_heads, int hd, int block, int window, float scale, float *partials, float *y,
-                      int num_sms, const PackDst *pack, const ZeroSet *zero, cudaStream_t st) {
-  (void)max_ctx;
-  if (batch > MAX_BATCH || heads / kv_heads * block > QMAX) return cudaErrorInvalidValue;
-  AttnArgs args;
+cudaError_t attention(const float *q, const CUtensorMap &own_k, const CUtensorMap &own_v, const AttnSeq *seqs,
+                      int batch, int heads, int kv_heads, int hd, int block, int window, float scale, float *partials,
+                      float *y, int num_sms, const PackDst *pack, const ZeroSet *zero, cudaStream_t st) {
+  if (batch < 1 || batch > MAX_BATCH || heads / kv_heads * block > QMAX) return cudaErrorInvalidValue;
+  AttnArgs args;  // entries past batch are not read
   int max_n = 0;
-  for (int i = 0; i < MAX_BATCH; ++i) {
-    if (i < batch) {
-      args.seq[i] = seqs[i];
-      max_n = std::max(max_n, seqs[i].n);
-    } else {
-      args.seq[i] = AttnSeq{nullptr, nullptr, 0, 0, 0};
-    }
+  for (int i = 0; i < batch; ++i) {
+    args.seq[i] = seqs[i];
+    max_n = std::max(max_n, seqs[i].n);
   }
+  args.own_k = own_k;
+  args.own_v = own_v;
   num_sms = std::max(1, std::min(num_sms, 1024));
   if (hd == 128)
-    return launch_attn_hd<128>(q, k, v, args, batch, max_n, heads, kv_heads, block, window, scale, partials, y, num_sms,
-                               pack, zero, st);
+    return launch_attn_hd<128>(q, args, batch, max_n, heads, kv_heads, block, window, scale, partials, y, num_sms, pack,
+                               zero, st);
   if (hd == 64)
-    return launch_attn_hd<64>(q, k, v, args, batch, max_n, heads, kv_heads, block, window, scale, partials, y, num_sms,
-                              pack, zero, st);
+    return launch_attn_hd<64>(q, args, batch, max_n, heads, kv_heads, block, window, scale, partials, y, num_sms, pack,
+                              zero, st);
   return cudaErrorInvalidValue;
+}
+
+// This file's device error word (a bounded wait that gave up).
+cudaError_t attn_read_error(unsigned *out, bool reset) {
+  cudaError_t e = cudaMemcpyFromSymbol(out, g_dev_error, sizeof(unsigned));
+  if (e == cudaSuccess && reset) {
+    const unsigned zero = 0;
+    e = cudaMemcpyToSymbol(g_dev_error, &zero, sizeof(unsigned));
+  }
+  return e;
 }
 
 }  // namespace dfl

@@ -139,7 +139,32 @@ struct dflash_t {
   std::vector<Seq> seqs;
   std::vector<float> inv;
   int num_sms = 148;
+  // tensor maps of the context caches [seq * layers + layer] and of the block's
+  // own K and V, encoded at the first block (host-only work)
+  std::vector<CUtensorMap> kmap, vmap;
+  CUtensorMap own_k, own_v;
+  bool maps = false;
 };
+
+namespace {
+bool encode_maps(dflash_t *d) {
+  if (d->maps) return true;
+  const dflash_geometry &g = d->g;
+  const size_t n = (size_t)d->max_batch * g.layers;
+  d->kmap.resize(n);
+  d->vmap.resize(n);
+  for (size_t i = 0; i < n; ++i)
+    if (!dfl::attn_kv_map(&d->kmap[i], d->ck[i], d->cap, g.kv_heads, g.head_dim, 64) ||
+        !dfl::attn_kv_map(&d->vmap[i], d->cv[i], d->cap, g.kv_heads, g.head_dim, 64))
+      return false;
+  const int64_t rows = (int64_t)d->max_batch * g.block;
+  if (!dfl::attn_kv_map(&d->own_k, d->k, rows, g.kv_heads, g.head_dim, g.block) ||
+      !dfl::attn_kv_map(&d->own_v, d->v, rows, g.kv_heads, g.head_dim, g.block))
+    return false;
+  d->maps = true;
+  return true;
+}
+}  // namespace
 
 extern "C" {
 
@@ -239,6 +264,7 @@ int dflash_create(dflash_t **out, const dflash_geometry *g, const dflash_weights
   if (!why.empty()) return fail(DFLASH_E_GEOMETRY, "unsupported DFlash geometry: " + why);
   if (max_batch < 1 || max_batch > dfl::MAX_BATCH) return fail(DFLASH_E_ARG, "create: max_batch must be 1..64");
   if (!ctx_k || !ctx_v || ctx_cap < 1) return fail(DFLASH_E_ARG, "create: context caches");
+  if (ctx_cap > INT32_MAX) return fail(DFLASH_E_ARG, "create: ctx_cap must be below 2^31");
   if (!workspace || !aligned16(workspace)) return fail(DFLASH_E_ARG, "create: null or misaligned workspace");
   const Carve c = carve_of(*g, max_batch);
   if (workspace_bytes < c.total) return fail(DFLASH_E_CAPACITY, "create: workspace smaller than dflash_workspace_bytes");
@@ -368,6 +394,7 @@ int dflash_block(dflash_t *d, int32_t batch, const int64_t *anchor_pos, const fl
   if (width < g.selector_top || width > g.vocab) return fail(DFLASH_E_ARG, "block: width must be selector_top..vocab");
   for (int b = 0; b < batch; ++b)
     if (anchor_pos[b] < 0) return fail(DFLASH_E_ARG, "block: a negative anchor position");
+  if (!encode_maps(d)) return fail(DFLASH_E_CUDA, "block: the driver could not encode the context caches' tensor maps");
   cudaStream_t st = (cudaStream_t)stream;
   const int T = batch * R;
   const int hs = g.hidden, nh = g.heads, kv = g.kv_heads, hd = g.head_dim, ffn = g.intermediate;
@@ -388,8 +415,9 @@ int dflash_block(dflash_t *d, int32_t batch, const int64_t *anchor_pos, const fl
       const int64_t hi = std::max(std::min(a, s.first + s.len), base);
       int64_t lo = base;
       if (W > 0) lo = std::min(std::max(std::max<int64_t>(a + 1 - W, 0), base), hi);
-      seqs[b].ck = d->ck[(size_t)b * g.layers + l] + (lo - s.first) * kvd;
-      seqs[b].cv = d->cv[(size_t)b * g.layers + l] + (lo - s.first) * kvd;
+      seqs[b].kmap = d->kmap[(size_t)b * g.layers + l];
+      seqs[b].vmap = d->vmap[(size_t)b * g.layers + l];
+      seqs[b].row0 = lo - s.first;
       seqs[b].n = (int)(hi - lo);
       seqs[b].lo = lo;
       seqs[b].anchor = a;
@@ -442,8 +470,8 @@ int dflash_block(dflash_t *d, int32_t batch, const int64_t *anchor_pos, const fl
       ranges(l, W);
       const dfl::PackDst po = pack_for(2, ti, qd);
       const dfl::ZeroSet zo = zero_for(&oj, 1, dfl::tc_splits_int4(&oj, 1, T, qd, sms), T);
-      DF_CUDA(dfl::attention(d->q, d->k, d->v, seqs.data(), batch, 0, nh, kv, hd, R, W, scale, d->part, d->y, sms, &po,
-                             &zo, st));
+      DF_CUDA(dfl::attention(d->q, d->own_k, d->own_v, seqs.data(), batch, nh, kv, hd, R, W, scale, d->part, d->y,
+                             sms, &po, &zo, st));
       DF_CUDA(dfl::tc_gemm_int4_packed(&oj, 1, grp, d->act, T, qd, sms, st));
       // h += conv_out(o, d); x = norm(h); the MLP the same way
       DF_CUDA(dfl::rms_pack(d->h, d->o, d->d, L.attn_base, kn, gs, L.post_norm, d->x, T, hs, eps, R, -1, -1,
@@ -494,7 +522,7 @@ int dflash_block(dflash_t *d, int32_t batch, const int64_t *anchor_pos, const fl
     DF_CUDA(dfl::qk_norm_rope(d->q, qd, L.q_norm, nh, d->k, kvd, L.k_norm, kv, d->inv.data(), T, hd, eps, rot,
                               anchor_pos, batch, R, st));
     ranges(l, W);
-    DF_CUDA(dfl::attention(d->q, d->k, d->v, seqs.data(), batch, 0, nh, kv, hd, R, W, scale, d->part, d->y, sms,
+    DF_CUDA(dfl::attention(d->q, d->own_k, d->own_v, seqs.data(), batch, nh, kv, hd, R, W, scale, d->part, d->y, sms,
                            nullptr, nullptr, st));
     const dfl::TcJob oj{L.o.data, L.o.scales, d->o, hs, hs};
     DF_CUDA(dfl::tc_gemm_int4(&oj, 1, grp, d->y, qd, T, qd, d->act, sms, st));

@@ -1,5 +1,6 @@
 // Host-side launchers of the drafter's kernels (internal to the library).
 #pragma once
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -122,8 +123,11 @@ cudaError_t tc_gemm_int4_packed(const TcJob *jobs, int njobs, int group, const v
 cudaError_t tc_gemm_f16_packed(const TcJob *jobs, int njobs, const void *act, int bstride, int T, int K, int num_sms,
                                cudaStream_t st);
 
-// The device error word (a bounded wait that gave up sets bit 0).
+// The device error word (a bounded wait that gave up sets bit 0): the union of
+// the words of the files whose kernels wait on mbarriers.
 cudaError_t read_device_error(unsigned *out, bool reset);
+cudaError_t wide_read_error(unsigned *out, bool reset);
+cudaError_t attn_read_error(unsigned *out, bool reset);
 
 // -------------------------------------------------------------- row kernels (rows.cu)
 // out[map(t)] = x[t] * rsqrt(mean(x[t]^2) + eps) * w for rows t < T. If
@@ -171,20 +175,26 @@ cudaError_t qk_norm_rope(float *q, int ldq, const float *wq, int hq, float *k, i
 cudaError_t silu_mul(const float *g, const float *u, float *m, int64_t n, cudaStream_t st);
 
 // -------------------------------------------------------------- attention (attention.cu)
-struct AttnSeq {        // per sequence and layer, on the device
-  const float *ck, *cv; // cache rows of positions lo.. (already offset)
-  int n;                // context rows read
-  int64_t lo;           // position of the first
-  int64_t anchor;       // position of block row 0
+// The kernel loads K and V rows with tensor copies: an f32 cache [rows][kv][hd]
+// is described by a map of boxes of 32 floats x 1 head x `box_rows` rows,
+// 128-byte swizzled. Encoding is host-only work; false if the driver cannot.
+bool attn_kv_map(CUtensorMap *m, const float *base, int64_t rows, int kv, int hd, int box_rows);
+struct AttnSeq {          // per sequence and layer
+  CUtensorMap kmap, vmap; // the layer's K and V cache of the sequence (box_rows 64)
+  int64_t row0;           // cache row of the first context row read
+  int64_t lo;             // its position
+  int64_t anchor;         // position of block row 0
+  int n;                  // context rows read
 };
 size_t attn_partial_bytes(int max_batch, int kv_heads, int heads, int block, int hd);
-// `seqs` is a host array of `batch` entries (passed by value).
-// With `pack` set, the merged rows go straight into those token tiles (for the
-// output projection; `zero` its outputs to clear) instead of y.
-cudaError_t attention(const float *q, const float *k, const float *v, const AttnSeq *seqs, int batch,
-                      int max_ctx, int heads, int kv_heads, int hd, int block, int window, float scale,
-                      float *partials, float *y, int num_sms, const PackDst *pack, const ZeroSet *zero,
-                      cudaStream_t st);
+// `seqs` is a host array of `batch` entries (passed by value). q is [batch *
+// block][heads][hd]; own_k / own_v map the block's own K and V [batch * block]
+// [kv][hd] (box_rows = block). With `pack` set, the merged rows go straight
+// into those token tiles (for the output projection; `zero` its outputs to
+// clear) instead of y.
+cudaError_t attention(const float *q, const CUtensorMap &own_k, const CUtensorMap &own_v, const AttnSeq *seqs,
+                      int batch, int heads, int kv_heads, int hd, int block, int window, float scale, float *partials,
+                      float *y, int num_sms, const PackDst *pack, const ZeroSet *zero, cudaStream_t st);
 
 // -------------------------------------------------------------- selector (select.cu)
 size_t select_scratch_bytes(int max_rows, int width, int top);

@@ -10,8 +10,8 @@
 namespace dfl {
 
 constexpr unsigned DFL_ERR_TIMEOUT = 1u;
-// The device error word of the translation unit that includes this header
-// (the tensor-core GEMMs); read with read_device_error().
+// The device error word of the translation unit that includes this header;
+// read_device_error() returns the union of all of them.
 static __device__ unsigned int g_dev_error = 0;
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }

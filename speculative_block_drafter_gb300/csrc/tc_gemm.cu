@@ -915,13 +915,24 @@ cudaError_t tc_gemm_f16(const TcJob *jobs, int njobs, const float *X, int ldx, i
   return tc_gemm_f16_packed(jobs, njobs, act, TT * 128, T, K, num_sms, st);
 }
 
-cudaError_t read_device_error(unsigned *out, bool reset) {
+// Each translation unit that waits on mbarriers has its own copy of the word
+// (tc.cuh); the library's is their union.
+static cudaError_t gemm_read_error(unsigned *out, bool reset) {
   cudaError_t e = cudaMemcpyFromSymbol(out, g_dev_error, sizeof(unsigned));
   if (e != cudaSuccess) return e;
   if (reset) {
     const unsigned zero = 0;
     e = cudaMemcpyToSymbol(g_dev_error, &zero, sizeof(unsigned));
   }
+  return e;
+}
+
+cudaError_t read_device_error(unsigned *out, bool reset) {
+  unsigned a = 0, b = 0, c = 0;
+  cudaError_t e = gemm_read_error(&a, reset);
+  if (e == cudaSuccess) e = wide_read_error(&b, reset);
+  if (e == cudaSuccess) e = attn_read_error(&c, reset);
+  *out = a | b | c;
   return e;
 }
 

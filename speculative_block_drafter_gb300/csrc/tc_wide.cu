@@ -585,4 +585,14 @@ cudaError_t wide_gemm(const WideJob *jobs, int njobs, int64_t y_off, bool int4, 
                      : launch_wide<W_KIND_I4, 2, W_CLUSTER>(A, X, ldx, act, num_sms, st);
 }
 
+// This file's device error word (a bounded wait that gave up).
+cudaError_t wide_read_error(unsigned *out, bool reset) {
+  cudaError_t e = cudaMemcpyFromSymbol(out, g_dev_error, sizeof(unsigned));
+  if (e == cudaSuccess && reset) {
+    const unsigned zero = 0;
+    e = cudaMemcpyToSymbol(g_dev_error, &zero, sizeof(unsigned));
+  }
+  return e;
+}
+
 }  // namespace dfl
