@@ -89,6 +89,21 @@ __device__ __forceinline__ void tma_load3(uint32_t dst, const CUtensorMap *m, in
       : "memory");
 }
 
+// f32 pair -> f16 hi/lo pairs without the conversion unit: hi keeps the top 11
+// significant bits (truncation, exact in f16 over its normal range), lo = x - hi
+// rounded to f16; hi + lo carries about 21 bits. Two packed conversions a pair.
+__device__ __forceinline__ uint32_t f16x2_rn(float first, float second) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(second), "f"(first));
+  return r;
+}
+__device__ __forceinline__ void split_hl(float x0, float x1, uint32_t &hi, uint32_t &lo) {
+  const float h0 = __uint_as_float(__float_as_uint(x0) & 0xFFFFE000u);
+  const float h1 = __uint_as_float(__float_as_uint(x1) & 0xFFFFE000u);
+  hi = f16x2_rn(h0, h1);
+  lo = f16x2_rn(x0 - h0, x1 - h1);
+}
+
 // Three-term product of f16 hi/lo pairs: acc += ah.bh + ah.bl + al.bh (about 22 bits).
 __device__ __forceinline__ void mma3(float (&acc)[4], const uint32_t (&ah)[4], const uint32_t (&al)[4], uint32_t bh0,
                                      uint32_t bh1, uint32_t bl0, uint32_t bl1) {
@@ -104,7 +119,8 @@ __device__ __forceinline__ void mma3(float (&acc)[4], const uint32_t (&ah)[4], c
 // block's own R rows as a final chunk). Warp 0 loads each chunk's K and V with
 // 8 tensor copies (4 column quarters each, 128-byte swizzled) into a 3-stage
 // ring; the MMA fragments are built from the f32 rows with their hi/lo f16
-// split on the fly, the queries' hi/lo fragments stay in registers. Warp w
+// split on the fly (bit masks and packed conversions, so that the split stays
+// off the conversion unit), the queries' hi/lo fragments stay in registers. Warp w
 // takes query block w % QW and key group w / QW of every chunk; each keeps a
 // running (m, l, o), merged in the CTA at the end.
 //
@@ -196,10 +212,10 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) k_attn(const float *__restrict
       const int c = 32 * (ks >> 1) + 4 * (2 * cq + (ks & 1));
       const float4 x0 = q0 ? *(const float4 *)(q0 + c) : make_float4(0.f, 0.f, 0.f, 0.f);
       const float4 x1 = q1 ? *(const float4 *)(q1 + c) : make_float4(0.f, 0.f, 0.f, 0.f);
-      split2(x0.x, x0.y, qh[ks][0], ql[ks][0]);
-      split2(x1.x, x1.y, qh[ks][1], ql[ks][1]);
-      split2(x0.z, x0.w, qh[ks][2], ql[ks][2]);
-      split2(x1.z, x1.w, qh[ks][3], ql[ks][3]);
+      split_hl(x0.x, x0.y, qh[ks][0], ql[ks][0]);
+      split_hl(x1.x, x1.y, qh[ks][1], ql[ks][1]);
+      split_hl(x0.z, x0.w, qh[ks][2], ql[ks][2]);
+      split_hl(x1.z, x1.w, qh[ks][3], ql[ks][3]);
     }
   }
   const int r0 = qi0 % R, r1 = qi1 % R;
@@ -233,8 +249,8 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) k_attn(const float *__restrict
           const float4 kx = *(const float4 *)(Ks + (ks >> 1) * RG::QUARTER + row * 128 +
                                               (((2 * cq + (ks & 1)) ^ gq) << 4));
           uint32_t bh0, bl0, bh1, bl1;
-          split2(kx.x, kx.y, bh0, bl0);
-          split2(kx.z, kx.w, bh1, bl1);
+          split_hl(kx.x, kx.y, bh0, bl0);
+          split_hl(kx.z, kx.w, bh1, bl1);
           mma3(sc[t], qh[ks], ql[ks], bh0, bh1, bl0, bl1);
         }
       }
@@ -288,10 +304,10 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) k_attn(const float *__restrict
 #pragma unroll
       for (int js = 0; js < KS; ++js) {
         uint32_t ph[4], pl[4];
-        split2(sc[2 * js][0], sc[2 * js][1], ph[0], pl[0]);
-        split2(sc[2 * js][2], sc[2 * js][3], ph[1], pl[1]);
-        split2(sc[2 * js + 1][0], sc[2 * js + 1][1], ph[2], pl[2]);
-        split2(sc[2 * js + 1][2], sc[2 * js + 1][3], ph[3], pl[3]);
+        split_hl(sc[2 * js][0], sc[2 * js][1], ph[0], pl[0]);
+        split_hl(sc[2 * js][2], sc[2 * js][3], ph[1], pl[1]);
+        split_hl(sc[2 * js + 1][0], sc[2 * js + 1][1], ph[2], pl[2]);
+        split_hl(sc[2 * js + 1][2], sc[2 * js + 1][3], ph[3], pl[3]);
         const int kA = kk0 + 16 * js + 2 * cq;
         const bool v0 = kA < cnt, v1 = kA + 1 < cnt, v2 = kA + 8 < cnt, v3 = kA + 9 < cnt;
         const uint8_t *va = Vs + kA * 128 + ((gq & 3) << 2);
@@ -307,8 +323,8 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) k_attn(const float *__restrict
           x2 = v2 ? x2 : 0.f;
           x3 = v3 ? x3 : 0.f;
           uint32_t bh0, bl0, bh1, bl1;
-          split2(x0, x1, bh0, bl0);
-          split2(x2, x3, bh1, bl1);
+          split_hl(x0, x1, bh0, bl0);
+          split_hl(x2, x3, bh1, bl1);
           mma3(o[t], ph, pl, bh0, bh1, bl0, bl1);
         }
       }
