@@ -13,6 +13,7 @@
 
 #include <algorithm>
 #include <climits>
+#include <type_traits>
 
 #include "common.cuh"
 #include "kernels.h"
@@ -292,42 +293,51 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) k_attn(const float *__restrict
       }
       l0 = l0 * a0 + s0;
       l1 = l1 * a1 + s1;
-#pragma unroll
-      for (int t = 0; t < OT; ++t) {
-        o[t][0] *= a0;
-        o[t][1] *= a0;
-        o[t][2] *= a1;
-        o[t][3] *= a1;
-      }
-      // O += P . V: P as hi/lo A fragments from the scores; V rows kA, kA+1, kA+8,
-      // kA+9 (swizzle phases 2cq, 2cq+1) at dimension 8t + gq
-#pragma unroll
-      for (int js = 0; js < KS; ++js) {
-        uint32_t ph[4], pl[4];
-        split_hl(sc[2 * js][0], sc[2 * js][1], ph[0], pl[0]);
-        split_hl(sc[2 * js][2], sc[2 * js][3], ph[1], pl[1]);
-        split_hl(sc[2 * js + 1][0], sc[2 * js + 1][1], ph[2], pl[2]);
-        split_hl(sc[2 * js + 1][2], sc[2 * js + 1][3], ph[3], pl[3]);
-        const int kA = kk0 + 16 * js + 2 * cq;
-        const bool v0 = kA < cnt, v1 = kA + 1 < cnt, v2 = kA + 8 < cnt, v3 = kA + 9 < cnt;
-        const uint8_t *va = Vs + kA * 128 + ((gq & 3) << 2);
+      if (__any_sync(0xffffffffu, a0 != 1.f || a1 != 1.f)) {  // a row's maximum moved
 #pragma unroll
         for (int t = 0; t < OT; ++t) {
-          const int c = (2 * t + (gq >> 2)) & 7;
-          const uint8_t *vq = va + (t >> 2) * RG::QUARTER;
-          const float *e0 = (const float *)(vq + ((c ^ (2 * cq)) << 4));
-          const float *e1 = (const float *)(vq + 128 + ((c ^ (2 * cq + 1)) << 4));
-          float x0 = e0[0], x1 = e1[0], x2 = e0[256], x3 = e1[256];  // rows +8: 1024 bytes on
-          x0 = v0 ? x0 : 0.f;
-          x1 = v1 ? x1 : 0.f;
-          x2 = v2 ? x2 : 0.f;
-          x3 = v3 ? x3 : 0.f;
-          uint32_t bh0, bl0, bh1, bl1;
-          split_hl(x0, x1, bh0, bl0);
-          split_hl(x2, x3, bh1, bl1);
-          mma3(o[t], ph, pl, bh0, bh1, bl0, bl1);
+          o[t][0] *= a0;
+          o[t][1] *= a0;
+          o[t][2] *= a1;
+          o[t][3] *= a1;
         }
       }
+      // O += P . V: P as hi/lo A fragments from the scores; V rows kA, kA+1, kA+8,
+      // kA+9 (swizzle phases 2cq, 2cq+1) at dimension 8t + gq. Rows past the
+      // chunk's keys (a partial chunk only) read as zero.
+      auto pv = [&](auto partial) {
+#pragma unroll
+        for (int js = 0; js < KS; ++js) {
+          uint32_t ph[4], pl[4];
+          split_hl(sc[2 * js][0], sc[2 * js][1], ph[0], pl[0]);
+          split_hl(sc[2 * js][2], sc[2 * js][3], ph[1], pl[1]);
+          split_hl(sc[2 * js + 1][0], sc[2 * js + 1][1], ph[2], pl[2]);
+          split_hl(sc[2 * js + 1][2], sc[2 * js + 1][3], ph[3], pl[3]);
+          const int kA = kk0 + 16 * js + 2 * cq;
+          const bool v0 = kA < cnt, v1 = kA + 1 < cnt, v2 = kA + 8 < cnt, v3 = kA + 9 < cnt;
+          const uint8_t *va = Vs + kA * 128 + ((gq & 3) << 2);
+#pragma unroll
+          for (int t = 0; t < OT; ++t) {
+            const int c = (2 * t + (gq >> 2)) & 7;
+            const uint8_t *vq = va + (t >> 2) * RG::QUARTER;
+            const float *e0 = (const float *)(vq + ((c ^ (2 * cq)) << 4));
+            const float *e1 = (const float *)(vq + 128 + ((c ^ (2 * cq + 1)) << 4));
+            float x0 = e0[0], x1 = e1[0], x2 = e0[256], x3 = e1[256];  // rows +8: 1024 bytes on
+            if (decltype(partial)::value) {
+              x0 = v0 ? x0 : 0.f;
+              x1 = v1 ? x1 : 0.f;
+              x2 = v2 ? x2 : 0.f;
+              x3 = v3 ? x3 : 0.f;
+            }
+            uint32_t bh0, bl0, bh1, bl1;
+            split_hl(x0, x1, bh0, bl0);
+            split_hl(x2, x3, bh1, bl1);
+            mma3(o[t], ph, pl, bh0, bh1, bl0, bl1);
+          }
+        }
+      };
+      if (cnt < CH) pv(std::true_type{});
+      else pv(std::false_type{});
     }
     // release the stage; warp 0 refills it with the chunk S ahead
     __syncwarp();
