@@ -2,7 +2,7 @@
 """Throughput of the DFlash 2 drafter pass on GB300.
 
 One step = one pass of the whole hot path over one batch of synthetic input:
-reset, settle of the workload's context (256-row calls), the block, and the
+reset, settle of the workload's context (1024-row calls), the block, and the
 selector (for the batched workload the contexts are settled once before the
 timed region and a step is one block per sequence plus the selector).
 

@@ -36,7 +36,7 @@ extern "C" {
 #endif
 
 #define DFLASH_MAX_LAYERS 64
-#define DFLASH_SETTLE_MAX 256     /* rows per settle call (gpu_cuda/hyb/dflash.rs, SETTLE_MAX) */
+#define DFLASH_SETTLE_MAX 1024    /* rows per settle call (gpu_cuda/hyb/dflash.rs, SETTLE_MAX, is 256 there) */
 #define DFLASH_MAX_BLOCK 16       /* rows of a block this build takes */
 
 enum {
@@ -154,7 +154,7 @@ int dflash_reset(dflash_t *d, int32_t seq, int64_t first);
 /* The settled context of `seq`: first position and row count. Host only. */
 int dflash_context(const dflash_t *d, int32_t seq, int64_t *first, int64_t *len);
 
-/* Settle `n` (1..256) tap rows of sequence `seq` at positions pos..pos+n-1
+/* Settle `n` (1..1024) tap rows of sequence `seq` at positions pos..pos+n-1
  * (gpu_cuda/hyb/dflash.rs `Dev::settle`; dflash.rs `settle_rows`). `taps` is a
  * device f32 [n][taps*hidden], joined in tap order. first <= pos <= first+len:
  * rows at held positions replace them and what follows (len = pos-first+n).

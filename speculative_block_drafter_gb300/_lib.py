@@ -13,7 +13,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "_build", "libdflash.so")
 
 MAX_LAYERS = 64
-SETTLE_MAX = 256
+SETTLE_MAX = 1024
 
 E_NAMES = {0: "OK", 1: "E_GEOMETRY", 2: "E_ARG", 3: "E_CAPACITY", 4: "E_CUDA", 5: "E_NOMEM"}
 

@@ -50,13 +50,14 @@ struct Carve {
 
 Carve carve_of(const dflash_geometry &g, int max_batch) {
   const int R = g.block;
-  const size_t T = (size_t)std::max(max_batch * R, DFLASH_SETTLE_MAX);
+  const size_t T = (size_t)max_batch * R;                           // block rows
+  const size_t Tx = std::max(T, (size_t)DFLASH_SETTLE_MAX);          // x also holds a settle's rows
   const size_t G = (size_t)g.hidden / g.conv_group;
   const size_t pr = 2 * (size_t)g.conv_kernel * G;
   const size_t f = sizeof(float);
   Carve c{};
   c.h = up(T * g.hidden * f);
-  c.x = up(T * g.hidden * f);
+  c.x = up(Tx * g.hidden * f);
   c.xc = up(T * g.hidden * f);
   c.d = up(T * pr * f);
   c.d2 = c.d;  // the MLP's kernel projection (the attention's d is still read when it is written)
@@ -349,7 +350,7 @@ int dflash_context(const dflash_t *d, int32_t seq, int64_t *first, int64_t *len)
 int dflash_settle(dflash_t *d, int32_t seq, int64_t pos, const float *taps, int32_t n, void *stream) {
   if (!d) return fail(DFLASH_E_ARG, "settle: null drafter");
   if (seq < 0 || seq >= d->max_batch) return fail(DFLASH_E_ARG, "settle: bad sequence");
-  if (n < 1 || n > DFLASH_SETTLE_MAX) return fail(DFLASH_E_ARG, "settle: a settle of 1 to 256 tap rows");
+  if (n < 1 || n > DFLASH_SETTLE_MAX) return fail(DFLASH_E_ARG, "settle: a settle of 1 to 1024 tap rows");
   if (!taps || ((uintptr_t)taps & 7)) return fail(DFLASH_E_ARG, "settle: null or misaligned taps");
   Seq &s = d->seqs[seq];
   if (pos < s.first || pos > s.first + s.len)

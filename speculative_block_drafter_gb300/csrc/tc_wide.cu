@@ -1,4 +1,4 @@
-// Weight GEMMs over many tokens (a settle chunk of up to 256 rows, a batch of
+// Weight GEMMs over many tokens (a settle chunk of up to 1024 rows, a batch of
 // blocks) on the tcgen05 tensor cores: Y[t][r] = sum_k X[t][k] W[r][k].
 //
 // At these sizes a 128-row weight tile meets up to 256 tokens in one MMA

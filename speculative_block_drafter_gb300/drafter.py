@@ -120,7 +120,7 @@ class Drafter:
         return L.dflash_context(self.h, seq)
 
     def settle(self, seq: int, pos: int, taps: torch.Tensor):
-        """Settle tap rows [n][tw] (device f32) at positions pos.., 256 rows a call."""
+        """Settle tap rows [n][tw] (device f32) at positions pos.., 1024 rows a call."""
         assert taps.dtype == torch.float32 and taps.is_cuda and taps.is_contiguous()
         n = taps.shape[0]
         st = _stream()

@@ -110,7 +110,7 @@ def test_create_and_host_state(L):
 def test_settle_and_block_argument_errors_before_any_launch(L):
     h, keep = _fake_create(L, max_batch=1, cap=64)
     taps = 1 << 24
-    for n in (0, 257):
+    for n in (0, L.SETTLE_MAX + 1):
         with pytest.raises(L.DflashError) as e:
             L.dflash_settle(h, 0, 0, taps, n, None)
         assert e.value.code == 2

@@ -158,11 +158,11 @@ def _tiny(**over):
 
 def test_settle_tiny_matches_oracle_with_ragged_chunks():
     g = _tiny()
-    p = Pair(g, ctx_cap=512)
-    taps = di.make_taps(g, 0, 301)
+    p = Pair(g, ctx_cap=1536)
+    taps = di.make_taps(g, 0, 1301)
     p.settle(0, 0, taps[:1])            # one row
-    p.settle(0, 1, taps[1:300])         # 256 + 43 rows, two calls
-    p.settle(0, 300, taps[300:301])
+    p.settle(0, 1, taps[1:1300])        # 1024 + 275 rows, two calls
+    p.settle(0, 1300, taps[1300:1301])
     assert p.check_cache() < 1e-4
     # rows at held positions replace them and what follows
     other = di.make_taps(g, 5, 40)
