@@ -2,10 +2,16 @@
 
     python -m speculative_block_drafter_gb300.microbench gemm --rows 151936 --cols 1024 --tokens 15 --kind 4
     python -m speculative_block_drafter_gb300.microbench gemm --rows 5120 --cols 25600 --tokens 256 --kind 16
+    python -m speculative_block_drafter_gb300.microbench block --workload batched --batch 8
 
-Random codes / values of the given shape; the L2 cache is flushed between
-launches; prints the mean time and the algorithmic bandwidth of one launch
-(weights, activations in, outputs out).
+gemm: random codes / values of the given shape; the L2 cache is flushed
+between launches; prints the mean time and the algorithmic bandwidth of one
+launch (weights, activations in, outputs out).
+
+block: the block pass of a workload's geometry at a chosen batch over its
+settled synthetic context (settled first, outside the timed and profiled
+range); the timed block passes sit between cudaProfilerStart and
+cudaProfilerStop, so `ncu --profile-from-start off` sees only them.
 """
 from __future__ import annotations
 
@@ -57,6 +63,40 @@ def gemm(args):
                       "TFLOP/s": round(2 * args.rows * args.cols * args.tokens / ms / 1e9, 1)}))
 
 
+def block(args):
+    import dataclasses
+    build.build()
+    from .drafter import Drafter
+    wl = di.workload(args.workload)
+    if args.batch:
+        wl = dataclasses.replace(wl, batch=args.batch)
+    g, B = wl.geometry, wl.batch
+    dev = torch.device("cuda", 0)
+    d = Drafter(g, di.make_weights(g, wl.seed), max_batch=B, ctx_cap=wl.context + g.block)
+    for s in range(B):
+        d.reset(s, 0)
+        d.settle(s, 0, torch.from_numpy(di.make_taps(g, wl.seed + s, wl.context)).to(dev))
+    h = torch.from_numpy(np.stack([di.block_rows(g, wl.seed + s, di.anchor_token(g, wl.seed + s))
+                                   for s in range(B)]).astype(np.float32)).to(dev).contiguous()
+    k = g.block - 1
+    logits = torch.empty(B, k, wl.head_width, device=dev)
+    hp = torch.empty(B, k, g.selector_rank, device=dev)
+    anchors = [wl.context] * B
+    for _ in range(3):
+        d.block(anchors, h, k, wl.head_width, out=(logits, hp))
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.profiler.start()
+    a.record()
+    for _ in range(args.iters):
+        d.block(anchors, h, k, wl.head_width, out=(logits, hp))
+    b.record()
+    torch.cuda.synchronize()
+    torch.cuda.profiler.stop()
+    print(json.dumps({"block": wl.name, "batch": B, "context": wl.context,
+                      "us_per_block": round(a.elapsed_time(b) / args.iters * 1e3, 1)}))
+
+
 def main():
     p = argparse.ArgumentParser()
     sub = p.add_subparsers(dest="cmd", required=True)
@@ -67,9 +107,15 @@ def main():
     g.add_argument("--kind", type=int, default=4, choices=[4, 16])
     g.add_argument("--group", type=int, default=64)
     g.add_argument("--iters", type=int, default=20)
+    k = sub.add_parser("block")
+    k.add_argument("--workload", default="batched", choices=sorted(di.WORKLOADS))
+    k.add_argument("--batch", type=int, default=0, help="sequences (default: the workload's)")
+    k.add_argument("--iters", type=int, default=5)
     args = p.parse_args()
     if args.cmd == "gemm":
         gemm(args)
+    else:
+        block(args)
 
 
 if __name__ == "__main__":
