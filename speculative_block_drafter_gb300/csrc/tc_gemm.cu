@@ -792,7 +792,8 @@ static void plan_int4(const TcJobs &J, int njobs, int ntt, int K, int num_sms, I
   P.ntt = ntt;
   const int KT = K / 64;
   P.units = (int)std::min<int64_t>((int64_t)ntt * P.groups * KT, INT32_MAX - 1);
-  // two CTAs an SM, each at least 8 units long; whole groups a CTA when there are enough of them
+  // two CTAs an SM, each at least 2 units long (a small GEMM is latency-bound: more CTAs, shorter
+  // chains); whole groups a CTA when there are enough of them
   const int ngroups = ntt * P.groups;
   split = false;
   if (ngroups >= 2 * num_sms) {
@@ -800,7 +801,7 @@ static void plan_int4(const TcJobs &J, int njobs, int ntt, int K, int num_sms, I
     grid = 2 * num_sms;
   } else {
     P.whole = 0;
-    grid = (int)std::max<int64_t>(1, std::min<int64_t>(2 * num_sms, P.units / 8));
+    grid = (int)std::max<int64_t>(1, std::min<int64_t>(2 * num_sms, P.units / 2));
     for (int b = 1; b < grid && !split; ++b) split = ((int64_t)b * P.units / grid) % KT != 0;
   }
 }
@@ -853,7 +854,7 @@ bool tc_splits_f16(const TcJob *jobs, int njobs, int T, int K, int num_sms) {
   if (T > NARROW_MAX_T || fill_jobs(jobs, njobs, J, mtiles) != cudaSuccess) return false;
   const int TT = tt_f16(T), ntt = (T + TT - 1) / TT;
   int kc, splits;
-  plan(ntt, mtiles, K / 64, num_sms, 8, kc, splits);
+  plan(ntt, mtiles, K / 64, num_sms, 2, kc, splits);
   return splits > 1;
 }
 
@@ -888,7 +889,7 @@ static cudaError_t launch_f16(const TcJobs &J, int mtiles, const void *act, int 
   cudaError_t e = set_smem(k_tc_f16<TT>, C::SMEM, configured);
   if (e != cudaSuccess) return e;
   int kc, splits;
-  plan(ntt, mtiles, K / 64, num_sms, 8, kc, splits);
+  plan(ntt, mtiles, K / 64, num_sms, 2, kc, splits);
   dim3 grid(ntt, mtiles, splits);
   return launch_pdl(k_tc_f16<TT>, grid, dim3(TC_THREADS), C::SMEM, st, 1, J, (const uint8_t *)act, bstride, K, T, kc,
                     (int)(splits > 1));
