@@ -256,3 +256,60 @@ def test_full_qwen3_0p6b_workload():
     # both sides round the kernel projections' inputs to f16, so a 1e-6 difference in the
     # cache can flip one of them by an ulp (~5e-4 of that element); the contract is LOGIT_REL
     assert r["logit_err"] < 5e-4, r
+
+
+def test_full_27b_workload():
+    """The 27b workload at full size: 4096 positions settled in 1024-row calls, windowed and
+    no-rope layers, one block over the whole head and the selector."""
+    wl = di.workload("27b")
+    g = wl.geometry
+    p = Pair(g, seed=wl.seed, ctx_cap=wl.context + 256)
+    p.settle(0, 0, di.make_taps(g, wl.seed, wl.context))
+    assert p.check_cache() < 1e-4
+    a = di.anchor_token(g, wl.seed)
+    r = p.draft([wl.context], [di.block_rows(g, wl.seed, a)], [a])[0]
+    assert r["logit_err"] < LOGIT_REL, r
+
+
+def test_full_batched_workload_sampled_sequences():
+    """The batched workload at full size (32 sequences of 8192 settled positions, one block of
+    512 rows through the wide GEMMs and the split attention); the oracle recomputes three of the
+    sequences from their own taps."""
+    wl = di.workload("batched")
+    g, B = wl.geometry, wl.batch
+    w = di.make_weights(g, wl.seed)
+    d = _drafter().Drafter(g, w, max_batch=B, ctx_cap=wl.context + g.block)
+    for s in range(B):
+        d.reset(s, 0)
+        d.settle(s, 0, torch.from_numpy(di.make_taps(g, wl.seed + s, wl.context)).cuda())
+    toks = [di.anchor_token(g, wl.seed + s) for s in range(B)]
+    rows = [di.block_rows(g, wl.seed + s, toks[s]) for s in range(B)]
+    h = torch.from_numpy(np.stack(rows).astype(np.float32)).cuda().contiguous()
+    k = g.block - 1
+    logits, hp = d.block([wl.context] * B, h, k, g.vocab)
+    chosen, plain = d.select(logits, hp, torch.tensor(toks, dtype=torch.int32, device="cuda"))
+    torch.cuda.synchronize()
+    for s in (0, 17, B - 1):
+        o = O.Oracle(g, w)
+        o.settle(0, di.make_taps(g, wl.seed + s, wl.context))
+        _, lo, hpo, _, _ = o.draft(wl.context, rows[s], toks[s], k, g.vocab)
+        check_close(f"logits seq {s}", logits[s].cpu().numpy(), lo)
+        check_close(f"hp seq {s}", hp[s].cpu().numpy(), hpo)
+        check_tokens(chosen[s].cpu().numpy(), plain[s].cpu().numpy(), hpo, lo, toks[s], w["pred_book"],
+                     w["succ_book"], g.selector_top)
+    d.close()
+
+
+def test_full_settle_heavy_workload():
+    """The settle-heavy workload at full size: 32,768 positions settled in 1024-row calls (the
+    oracle in 4096-row slices of the same taps), every layer over the whole context, one block
+    over the whole head and the selector."""
+    wl = di.workload("settle-heavy")
+    g = wl.geometry
+    p = Pair(g, seed=wl.seed, ctx_cap=wl.context + g.block)
+    for start in range(0, wl.context, 4096):
+        p.settle(0, start, di.make_taps(g, wl.seed, 4096, start))
+    assert p.check_cache() < 1e-4
+    a = di.anchor_token(g, wl.seed)
+    r = p.draft([wl.context], [di.block_rows(g, wl.seed, a)], [a])[0]
+    assert r["logit_err"] < LOGIT_REL, r
