@@ -24,6 +24,9 @@ namespace dfl {
 constexpr int ATT_THREADS = 256;
 constexpr int CH = 64;              // keys per chunk
 constexpr int QMAX = 64;            // queries per CTA (rep * block)
+// A split's partial row in global memory: o[hd], m, l, two floats of padding so
+// that every row starts on 16 bytes (the merge reads o with vector loads).
+__host__ __device__ constexpr int part_row(int hd) { return hd + 4; }
 
 struct AttnArgs {
   AttnSeq seq[MAX_BATCH];
@@ -54,7 +57,7 @@ size_t attn_partial_bytes(int max_batch, int kv_heads, int heads, int block, int
   const int Q = heads / kv_heads * block;
   // one partial per CTA: at most 1024 + 2 * batch * kv of them (plan_splits)
   const size_t worst = (size_t)1024 + 3 * (size_t)max_batch * kv_heads;
-  return worst * Q * (hd + 2) * sizeof(float);
+  return worst * Q * (hd + 4) * sizeof(float);
 }
 
 // ---------------------------------------------------------------- tensor maps
@@ -380,7 +383,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) k_attn(const float *__restrict
     }
   }
   __syncthreads();
-  float *out = part + ((int64_t)(b * kv + g) * nsplit + sp) * Q * (HD + 2);
+  float *out = part + ((int64_t)(b * kv + g) * nsplit + sp) * Q * part_row(HD);
   // one warp per query row at a time: the key groups' weights once, then the row
   for (int qi = warp; qi < Q; qi += ATT_THREADS / 32) {
     const int qbk = qi / 16, rr = qi % 16;
@@ -393,7 +396,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) k_attn(const float *__restrict
       const float mk = scr[(kg * QW + qbk) * 16 * (HD + 2) + rr * (HD + 2) + HD];
       wt[kg] = mk == -INFINITY ? 0.f : expf(mk - M);
     }
-    float *orow = out + (int64_t)qi * (HD + 2);
+    float *orow = out + (int64_t)qi * part_row(HD);
     for (int c = lane; c < HD + 2; c += 32) {
       float acc = 0.f;
       if (c == HD) {
@@ -408,71 +411,84 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) k_attn(const float *__restrict
   }
 }
 
-// y[b*R + r][h*HD + d] = sum_s o_s e^(m_s - M) / sum_s l_s e^(m_s - M)
-template <int HD>
-__global__ void k_attn_merge(const float *__restrict__ part, int heads, int kv, int R, int nsplit,
-                             float *__restrict__ y) {
-  pdl_wait();
-  const int qi_all = blockIdx.x;  // over kv * Q
-  const int b = blockIdx.y;
-  const int rep = heads / kv, Q = rep * R;
-  const int g = qi_all / Q, qi = qi_all % Q;
-  const int hrep = qi / R, r = qi % R;
-  const int d = threadIdx.x;
-  const float *base = part + (int64_t)(b * kv + g) * (nsplit + 1) * Q * (HD + 2) + (int64_t)qi * (HD + 2);
-  const int64_t sstride = (int64_t)Q * (HD + 2);
-  float M = -INFINITY;
-  for (int s = 0; s <= nsplit; ++s) M = fmaxf(M, base[s * sstride + HD]);
-  float L = 0.f, acc = 0.f;
-  for (int s = 0; s <= nsplit; ++s) {
-    const float m = base[s * sstride + HD];
-    if (m == -INFINITY) continue;
-    const float e = expf(m - M);
-    L = fmaf(base[s * sstride + HD + 1], e, L);
-    acc = fmaf(base[s * sstride + d], e, acc);
-  }
-  y[((int64_t)b * R + r) * heads * HD + (g * rep + hrep) * HD + d] = acc / L;
-}
+// y[b*R + r][h*HD + d] = sum_s o_s e^(m_s - M) / sum_s l_s e^(m_s - M), one warp a
+// query row: lane s reads split s's (m, l) (a loop past 32 splits), the warp
+// reduces M and L, then each lane sums 4 dimensions over the splits with the
+// splits' loads independent of one another (a few L2 round trips in all).
+// PACK writes the row into the output projection's token tiles (hi/lo planes;
+// even lanes take their neighbour's 4 values) and the blocks past the work
+// grid clear that GEMM's outputs when it splits; else the row goes to y.
+constexpr int MERGE_WARPS = 4;
 
-// The same merge written straight into the token tiles of the output
-// projection (hi/lo planes; a thread per 8 columns of a query row), with the
-// projection's outputs cleared by the blocks past the work grid when it splits.
-constexpr int MERGE_THREADS = 32;  // small CTAs: the work is a few thousand threads of dependent loads
-
-template <int HD>
-__global__ void __launch_bounds__(MERGE_THREADS) k_attn_merge_pack(const float *__restrict__ part, int heads, int kv, int R,
-                                                         int nsplit, int work_blocks, PackDst P, ZeroSet Z) {
+template <int HD, bool PACK>
+__global__ void __launch_bounds__(32 * MERGE_WARPS) k_attn_merge(const float *__restrict__ part, int heads, int kv,
+                                                                 int R, int ns, int work_blocks,
+                                                                 float *__restrict__ y, PackDst P, ZeroSet Z) {
+  static_assert(HD == 4 * 32 || HD == 2 * 32, "head dimension");
+  constexpr int DL = HD / 32;  // dimensions a lane
   pdl_wait();
-  pdl_trigger();  // the GEMM this feeds may fetch its weights meanwhile
+  if (PACK) pdl_trigger();  // the GEMM this feeds may fetch its weights meanwhile
   if ((int)blockIdx.x >= work_blocks) {
-    if (blockIdx.y == 0) zero_set_clear(Z, blockIdx.x - work_blocks, gridDim.x - work_blocks);
+    if (PACK && blockIdx.y == 0) zero_set_clear(Z, blockIdx.x - work_blocks, gridDim.x - work_blocks);
     return;
   }
-  constexpr int D8 = HD / 8;
-  const int b = blockIdx.y;
+  const int b = blockIdx.y, lane = threadIdx.x & 31;
   const int rep = heads / kv, Q = rep * R;
-  const int id = blockIdx.x * MERGE_THREADS + threadIdx.x;
-  if (id >= kv * Q * D8) return;
-  const int qa = id / D8, d8 = id - qa * D8;
-  const int g = qa / Q, qi = qa - g * Q;
+  const int row = blockIdx.x * MERGE_WARPS + (threadIdx.x >> 5);
+  if (row >= kv * Q) return;
+  const int g = row / Q, qi = row - g * Q;
   const int hrep = qi / R, r = qi - hrep * R;
-  const float *base = part + (int64_t)(b * kv + g) * (nsplit + 1) * Q * (HD + 2) + (int64_t)qi * (HD + 2);
-  const int64_t sstride = (int64_t)Q * (HD + 2);
+  const int64_t sstride = (int64_t)Q * part_row(HD);
+  const float *base = part + (int64_t)(b * kv + g) * ns * sstride + (int64_t)qi * part_row(HD);
+  // M and L over the splits
   float M = -INFINITY;
-  for (int s = 0; s <= nsplit; ++s) M = fmaxf(M, base[s * sstride + HD]);
-  float L = 0.f, acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-  for (int s = 0; s <= nsplit; ++s) {
+  for (int s = lane; s < ns; s += 32) M = fmaxf(M, base[s * sstride + HD]);
+  M = warp_max(M);
+  float L = 0.f;
+  for (int s = lane; s < ns; s += 32) {
+    const float m = base[s * sstride + HD];
+    if (m != -INFINITY) L = fmaf(base[s * sstride + HD + 1], expf(m - M), L);
+  }
+  L = warp_sum(L);
+  // the row: lane's DL dimensions over the splits
+  float acc[DL];
+#pragma unroll
+  for (int e = 0; e < DL; ++e) acc[e] = 0.f;
+#pragma unroll 4
+  for (int s = 0; s < ns; ++s) {
     const float *ps = base + s * sstride;
     const float m = ps[HD];
-    if (m == -INFINITY) continue;
-    const float e = expf(m - M);
-    L = fmaf(ps[HD + 1], e, L);
-#pragma unroll
-    for (int c = 0; c < 8; ++c) acc[c] = fmaf(ps[8 * d8 + c], e, acc[c]);
+    const float w = m == -INFINITY ? 0.f : expf(m - M);
+    if constexpr (DL == 4) {
+      const float4 o = *(const float4 *)(ps + 4 * lane);
+      acc[0] = fmaf(o.x, w, acc[0]);
+      acc[1] = fmaf(o.y, w, acc[1]);
+      acc[2] = fmaf(o.z, w, acc[2]);
+      acc[3] = fmaf(o.w, w, acc[3]);
+    } else {
+      const float2 o = *(const float2 *)(ps + 2 * lane);
+      acc[0] = fmaf(o.x, w, acc[0]);
+      acc[1] = fmaf(o.y, w, acc[1]);
+    }
   }
+  const float inv = 1.f / L;
 #pragma unroll
-  for (int c = 0; c < 8; ++c) acc[c] = acc[c] / L;
-  pack_store8(P, b * R + r, (g * rep + hrep) * HD + 8 * d8, acc);
+  for (int e = 0; e < DL; ++e) acc[e] *= inv;
+  const int col = (g * rep + hrep) * HD;
+  if constexpr (PACK) {
+    // 8 consecutive columns a store: lanes 8/DL apart hand theirs to the first
+    constexpr int LPC = 8 / DL;  // lanes a store
+    float x8[8];
+#pragma unroll
+    for (int j = 0; j < LPC; ++j)
+#pragma unroll
+      for (int e = 0; e < DL; ++e) x8[j * DL + e] = __shfl_sync(0xffffffffu, acc[e], (lane / LPC) * LPC + j);
+    if (lane % LPC == 0) pack_store8(P, b * R + r, col + DL * lane, x8);
+  } else {
+    float *out = y + ((int64_t)b * R + r) * heads * HD + col + DL * lane;
+    if constexpr (DL == 4) *(float4 *)out = make_float4(acc[0], acc[1], acc[2], acc[3]);
+    else *(float2 *)out = make_float2(acc[0], acc[1]);
+  }
 }
 
 template <int HD, int KG>
@@ -493,16 +509,17 @@ static cudaError_t launch_attn(const float *q, const AttnArgs &args, int batch, 
                              ns, cps, part);
   if (e != cudaSuccess) return e;
   const int Q = heads / kv * R;
+  const int work = (kv * Q + MERGE_WARPS - 1) / MERGE_WARPS;
   if (pack) {
-    const int work = (kv * Q * (HD / 8) + MERGE_THREADS - 1) / MERGE_THREADS;
     int64_t most = 0;
     for (int j = 0; j < zero->count; ++j) most = std::max<int64_t>(most, zero->n[j]);
-    const int zb = zero->count ? (int)std::min<int64_t>((most + 4 * MERGE_THREADS - 1) / (4 * MERGE_THREADS), 256) : 0;
-    return launch_pdl(k_attn_merge_pack<HD>, dim3(work + zb, batch), dim3(MERGE_THREADS), 0, st, 1, part, heads, kv, R,
-                      ns - 1, work, *pack, *zero);
+    const int zb =
+        zero->count ? (int)std::min<int64_t>((most + 4 * 32 * MERGE_WARPS - 1) / (4 * 32 * MERGE_WARPS), 256) : 0;
+    return launch_pdl(k_attn_merge<HD, true>, dim3(work + zb, batch), dim3(32 * MERGE_WARPS), 0, st, 1, part, heads,
+                      kv, R, ns, work, (float *)nullptr, *pack, *zero);
   }
-  dim3 g2(kv * Q, batch);
-  return launch_pdl(k_attn_merge<HD>, g2, dim3(HD), 0, st, 1, part, heads, kv, R, ns - 1, y);
+  return launch_pdl(k_attn_merge<HD, false>, dim3(work, batch), dim3(32 * MERGE_WARPS), 0, st, 1, part, heads, kv, R,
+                    ns, work, y, PackDst{}, ZeroSet{});
 }
 
 template <int HD>

@@ -265,7 +265,7 @@ cudaError_t silu_mul(const float *g, const float *u, float *m, int64_t n, cudaSt
 // consecutive columns of a row.
 
 constexpr int FP_THREADS = 256;
-constexpr int FP_KEEP = 4;  // 8-column groups a thread keeps between the two passes of a row (hs <= 8192)
+constexpr int FP_KEEP = 4;  // 8-column groups a thread keeps between the two passes of a row past 8192 columns
 
 __device__ __forceinline__ void load8(const float *p, float (&v)[8]) {
   const float4 a = ((const float4 *)p)[0], b = ((const float4 *)p)[1];
@@ -285,7 +285,8 @@ __device__ __forceinline__ void conv1_8(const float *__restrict__ x, const float
   const float *dr = d + (int64_t)t * (2 * kn * groups) + kn * groups;
   const float *br = base + (int64_t)kn * hs;
   const int nmax = min(kn, r + 1);
-  for (int o = 0; o < nmax; ++o) {
+#pragma unroll 4
+  for (int o = 0; o < nmax; ++o) {  // unrolled: the taps' loads go out together
     float xv[8], bv[8];
     load8(x + (int64_t)(t - o) * hs + i0, xv);
     load8(br + (int64_t)o * hs + i0, bv);
@@ -305,6 +306,7 @@ __device__ __forceinline__ void conv1_8(const float *__restrict__ x, const float
 // into xout (if set) and into the token tiles at the row's packed index
 // (rows outside [keep_from, keep_to] of their block are left out, packed per
 // sequence, when keep_from >= 0).
+template <int KEEP>
 __global__ void __launch_bounds__(1024) k_rms_pack(float *__restrict__ h, const float *__restrict__ cx,
                                                          const float *__restrict__ cd, const float *__restrict__ cbase,
                                                          int kn, int gs, const float *__restrict__ w,
@@ -318,11 +320,12 @@ __global__ void __launch_bounds__(1024) k_rms_pack(float *__restrict__ h, const 
   }
   const int t = blockIdx.x;
   const int ng = hs / 8, nt = blockDim.x;
-  float v[FP_KEEP][8];
+  float v[KEEP][8], w0[8];
   float ss = 0.f;
   float *hr = h + (int64_t)t * hs;
+  if ((int)threadIdx.x < ng) load8(w + 8 * threadIdx.x, w0);  // the first group's weights, fetched early
 #pragma unroll
-  for (int m = 0; m < FP_KEEP; ++m) {
+  for (int m = 0; m < KEEP; ++m) {
     const int gi = threadIdx.x + m * nt;
     if (gi < ng) {
       load8(hr + 8 * gi, v[m]);
@@ -354,11 +357,16 @@ __global__ void __launch_bounds__(1024) k_rms_pack(float *__restrict__ h, const 
   }
   if (!keep) return;
 #pragma unroll
-  for (int m = 0; m < FP_KEEP; ++m) {
+  for (int m = 0; m < KEEP; ++m) {
     const int gi = threadIdx.x + m * nt;
     if (gi < ng) {
-      float wv[8], o[8];
-      load8(w + 8 * gi, wv);
+      float o[8], wv[8];
+      if (m == 0) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) wv[e] = w0[e];
+      } else {
+        load8(w + 8 * gi, wv);
+      }
 #pragma unroll
       for (int e = 0; e < 8; ++e) o[e] = v[m][e] * sc * wv[e];
       if (xout) store8(xout + (int64_t)orow * hs + 8 * gi, o);
@@ -385,7 +393,8 @@ __global__ void __launch_bounds__(FP_THREADS) k_conv0_pack(const float *__restri
   const float *dr = d + (int64_t)t * (2 * kn * groups);
   const int nmax = min(kn, r + 1);
   float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-  for (int o = 0; o < nmax; ++o) {
+#pragma unroll 4
+  for (int o = 0; o < nmax; ++o) {  // unrolled: the taps' loads go out together
     float xv[8], bv[8];
     load8(x + (int64_t)(t - o) * hs + i0, xv);
     load8(base + (int64_t)o * hs + i0, bv);
@@ -453,8 +462,9 @@ cudaError_t rms_pack(float *h, const float *cx, const float *cd, const float *cb
   const int ng = hs / 8;
   const int nt = std::min(1024, std::max(32, (ng + 31) / 32 * 32));
   if (hs % 8 || ng > nt * FP_KEEP) return cudaErrorInvalidValue;
-  return launch_pdl(k_rms_pack, dim3(T + zero_blocks_for(Z)), dim3(nt), 0, st, 1, h, cx, cd, cbase, kn, gs, w, xout, T,
-                    hs, eps, block, keep_from, keep_to, P, Z);
+  // one 8-column group a thread up to 8192 columns (fewer live registers)
+  return launch_pdl(ng <= nt ? k_rms_pack<1> : k_rms_pack<FP_KEEP>, dim3(T + zero_blocks_for(Z)), dim3(nt), 0, st, 1,
+                    h, cx, cd, cbase, kn, gs, w, xout, T, hs, eps, block, keep_from, keep_to, P, Z);
 }
 
 cudaError_t conv0_pack(const float *x, const float *d, const float *base, int T, int hs, int kn, int gs, int block,
