@@ -126,6 +126,14 @@ size_t dflash_gemm_workspace_bytes(int32_t kind, int64_t cols, int32_t T);
 int dflash_gemm(const dflash_matrix *w, int32_t kind, int64_t rows, int64_t cols, int32_t group, const float *x,
                 int32_t T, float *y, void *workspace, size_t workspace_bytes, void *stream);
 
+/* The GEMM kernel of dflash_gemm alone, for T <= 32 rows: it reads the token
+ * tiles that a dflash_gemm call with the same kind, cols, T and workspace
+ * packed before (so that the kernel can be timed without its packing). When
+ * the launch splits its k-range, y is cleared first on the stream. Errors:
+ * ARG (T > 32 or a bad shape), CUDA. */
+int dflash_gemm_packed(const dflash_matrix *w, int32_t kind, int64_t rows, int64_t cols, int32_t group, int32_t T,
+                       float *y, const void *workspace, void *stream);
+
 /* The library's device error word: bit 0 is set when one of its kernels gave
  * up a bounded wait (the kernel then stopped early and its outputs are not to
  * be trusted). Reads it (synchronising the device) and clears it if `reset`. */

@@ -69,6 +69,8 @@ EXPORTS = {
     "dflash_dequant_int4": (C.c_int, [C.c_void_p, C.c_void_p, C.c_int64, C.c_int64, C.c_int32, C.c_void_p,
                                       C.c_void_p]),
     "dflash_gemm_workspace_bytes": (C.c_size_t, [C.c_int32, C.c_int64, C.c_int32]),
+    "dflash_gemm_packed": (C.c_int, [C.POINTER(Matrix), C.c_int32, C.c_int64, C.c_int64, C.c_int32, C.c_int32,
+                                     C.c_void_p, C.c_void_p, C.c_void_p]),
     "dflash_gemm": (C.c_int, [C.POINTER(Matrix), C.c_int32, C.c_int64, C.c_int64, C.c_int32, C.c_void_p, C.c_int32,
                               C.c_void_p, C.c_void_p, C.c_size_t, C.c_void_p]),
     "dflash_device_error": (C.c_int, [C.POINTER(C.c_uint32), C.c_int32]),
@@ -148,6 +150,10 @@ def dflash_gemm_workspace_bytes(kind, cols, T):
 
 def dflash_gemm(w: Matrix, kind, rows, cols, group, x, T, y, workspace, ws_bytes, stream):
     _check(lib().dflash_gemm(C.byref(w), kind, rows, cols, group, x, T, y, workspace, ws_bytes, stream))
+
+
+def dflash_gemm_packed(w: Matrix, kind, rows, cols, group, T, y, workspace, stream):
+    _check(lib().dflash_gemm_packed(C.byref(w), kind, rows, cols, group, T, y, workspace, stream))
 
 
 def dflash_device_error(reset: bool = True) -> int:

@@ -243,6 +243,31 @@ int dflash_gemm(const dflash_matrix *w, int32_t kind, int64_t rows, int64_t cols
   return DFLASH_OK;
 }
 
+int dflash_gemm_packed(const dflash_matrix *w, int32_t kind, int64_t rows, int64_t cols, int32_t group, int32_t T,
+                       float *y, const void *workspace, void *stream) {
+  if (!w || !y || !workspace || T < 1 || T > 32) return fail(DFLASH_E_ARG, "gemm_packed: null pointer or T not 1..32");
+  if (((uintptr_t)y & 3) || ((uintptr_t)workspace & 15)) return fail(DFLASH_E_ARG, "gemm_packed: misaligned y or workspace");
+  if (rows > INT32_MAX || cols > INT32_MAX || dflash_gemm_workspace_bytes(kind, cols, T) == 0)
+    return fail(DFLASH_E_ARG, "gemm_packed: kind must be 4 or 16, cols a multiple of 64");
+  int sms = 148, dev = 0;
+  if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  cudaStream_t st = (cudaStream_t)stream;
+  dfl::TcJob job{w->data, w->scales, y, (int)rows, (int)rows};
+  if (kind == 4) {
+    if (dflash_int4_packed_bytes(rows, cols, group) == 0) return fail(DFLASH_E_ARG, "gemm_packed: unsupported int4 shape");
+    if (!int4_ok(*w)) return fail(DFLASH_E_ARG, "gemm_packed: null or misaligned matrix");
+    if (dfl::tc_splits_int4(&job, 1, T, (int)cols, sms))
+      DF_CUDA(cudaMemsetAsync(y, 0, (size_t)T * rows * sizeof(float), st));
+    DF_CUDA(dfl::tc_gemm_int4_packed(&job, 1, group, workspace, T, (int)cols, sms, st));
+  } else {
+    if (!f16_ok(*w)) return fail(DFLASH_E_ARG, "gemm_packed: null or misaligned matrix");
+    if (dfl::tc_splits_f16(&job, 1, T, (int)cols, sms))
+      DF_CUDA(cudaMemsetAsync(y, 0, (size_t)T * rows * sizeof(float), st));
+    DF_CUDA(dfl::tc_gemm_f16_packed(&job, 1, workspace, dfl::tc_tile_rows(T, false) * 128, T, (int)cols, sms, st));
+  }
+  return DFLASH_OK;
+}
+
 int dflash_device_error(uint32_t *error, int32_t reset) {
   if (!error) return fail(DFLASH_E_ARG, "device_error: null pointer");
   unsigned v = 0;

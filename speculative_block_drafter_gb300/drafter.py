@@ -215,4 +215,13 @@ class PackedMatrix:
             self._ws = torch.empty(nb, dtype=torch.uint8, device=x.device)
         L.dflash_gemm(self.mat, self.kind, self.rows, self.cols, self.group, x.data_ptr(), x.shape[0], y.data_ptr(),
                       self._ws.data_ptr(), self._ws.numel(), _stream())
+        self._packed_T = x.shape[0]
+        return y
+
+    def matmul_packed(self, y: torch.Tensor) -> torch.Tensor:
+        """The GEMM kernel alone on the token tiles the last `matmul` packed (up to 32 rows), into y."""
+        T = self._packed_T
+        assert y.dtype == torch.float32 and y.is_cuda and y.is_contiguous() and y.shape == (T, self.rows)
+        L.dflash_gemm_packed(self.mat, self.kind, self.rows, self.cols, self.group, T, y.data_ptr(),
+                             self._ws.data_ptr(), _stream())
         return y

@@ -85,6 +85,24 @@ def test_gemm_int4_matches_oracle(rows, cols, group, T):
     assert err <= 2e-6 * _bound(wabs, x), (err, _bound(wabs, x))
 
 
+@pytest.mark.parametrize("kind,rows,cols,T", [(4, 4096, 1024, 16), (4, 151936, 1024, 15), (4, 256, 17408, 32),
+                                               (16, 1280, 5120, 16), (16, 512, 1024, 3)])
+def test_gemm_packed_repeats_gemm(kind, rows, cols, T):
+    """dflash_gemm_packed reruns dflash_gemm's kernel on the tiles it packed (whole and split k-ranges)."""
+    from speculative_block_drafter_gb300.drafter import PackedMatrix
+    rng = np.random.default_rng(rows + cols + T)
+    if kind == 4:
+        m = _rand_int4(rng, rows, cols, 64)
+    else:
+        m = (rng.standard_normal((rows, cols)) * 0.02).astype(np.float16)
+    pm = PackedMatrix(m)
+    x = torch.from_numpy(rng.standard_normal((T, cols)).astype(np.float32)).cuda()
+    y1 = pm.matmul(x).clone()
+    y2 = pm.matmul_packed(torch.full_like(y1, float("nan")))
+    torch.cuda.synchronize()
+    assert torch.allclose(y1, y2, rtol=1e-6, atol=1e-6 * float(y1.abs().max()))
+
+
 @pytest.mark.parametrize("rows,cols,T", [(16, 64, 1), (64, 512, 16), (1280, 5120, 16), (128, 3072, 256), (64, 256, 33),
                                          (1024, 3072, 256), (200, 1024, 300), (5120, 2560, 256)])
 def test_gemm_f16_matches_oracle(rows, cols, T):
