@@ -6,7 +6,7 @@
 //
 // Split-K: the context rows of a sequence are cut into splits of whole 64-key
 // chunks, one CTA per (split, KV head, sequence); the last split of a sequence
-// also takes the block's own rows. Each keeps a running maximum m, sum l and
+// takes the block's own rows (alone when the splits are short). Each keeps a running maximum m, sum l and
 // unnormalised output o per query (the rep = heads/kv_heads query heads of the
 // KV head times the block rows) and a second kernel merges the splits.
 #include <cudaTypedefs.h>
@@ -55,7 +55,8 @@ static void plan_splits(int pairs, int max_n, int num_sms, int &ns, int &cps) {
 
 size_t attn_partial_bytes(int max_batch, int kv_heads, int heads, int block, int hd) {
   const int Q = heads / kv_heads * block;
-  // one partial per CTA: at most 1024 + 2 * batch * kv of them (plan_splits)
+  // one partial per CTA: at most 1024 + 2 * batch * kv of them (plan_splits), plus the
+  // own rows' split
   const size_t worst = (size_t)1024 + 3 * (size_t)max_batch * kv_heads;
   return worst * Q * (hd + 4) * sizeof(float);
 }
@@ -119,7 +120,7 @@ __device__ __forceinline__ void mma3(float (&acc)[4], const uint32_t (&ah)[4], c
 // ---------------------------------------------------------------- the split kernel
 //
 // One CTA per (split, KV head, sequence): the rep*R queries of the KV head over
-// the split's context keys in chunks of 64 (the last split also takes the
+// the split's context keys in chunks of 64 (the last split takes the
 // block's own R rows as a final chunk). Warp 0 loads each chunk's K and V with
 // 8 tensor copies (4 column quarters each, 128-byte swizzled) into a 3-stage
 // ring; the MMA fragments are built from the f32 rows with their hi/lo f16
@@ -440,25 +441,41 @@ __global__ void __launch_bounds__(32 * MERGE_WARPS) k_attn_merge(const float *__
   const int hrep = qi / R, r = qi - hrep * R;
   const int64_t sstride = (int64_t)Q * part_row(HD);
   const float *base = part + (int64_t)(b * kv + g) * ns * sstride + (int64_t)qi * part_row(HD);
-  // M and L over the splits
-  float M = -INFINITY;
-  for (int s = lane; s < ns; s += 32) M = fmaxf(M, base[s * sstride + HD]);
-  M = warp_max(M);
-  float L = 0.f;
-  for (int s = lane; s < ns; s += 32) {
-    const float m = base[s * sstride + HD];
-    if (m != -INFINITY) L = fmaf(base[s * sstride + HD + 1], expf(m - M), L);
+  // M and L over the splits: lane s holds split s's (m, l) and weight e^(m - M)
+  // (more than 32 splits: a loop, the weights recomputed in the sum below)
+  float M = -INFINITY, L = 0.f, ws = 0.f;
+  if (ns <= 32) {
+    float ms = -INFINITY, ls = 0.f;
+    if (lane < ns) {
+      ms = base[lane * sstride + HD];
+      ls = base[lane * sstride + HD + 1];
+    }
+    M = warp_max(ms);
+    ws = ms == -INFINITY ? 0.f : expf(ms - M);
+    L = warp_sum(ls * ws);
+  } else {
+    for (int s = lane; s < ns; s += 32) M = fmaxf(M, base[s * sstride + HD]);
+    M = warp_max(M);
+    for (int s = lane; s < ns; s += 32) {
+      const float m = base[s * sstride + HD];
+      if (m != -INFINITY) L = fmaf(base[s * sstride + HD + 1], expf(m - M), L);
+    }
+    L = warp_sum(L);
   }
-  L = warp_sum(L);
-  // the row: lane's DL dimensions over the splits
+  // the row: lane's DL dimensions over the splits (independent vector loads)
   float acc[DL];
 #pragma unroll
   for (int e = 0; e < DL; ++e) acc[e] = 0.f;
-#pragma unroll 4
+#pragma unroll 8
   for (int s = 0; s < ns; ++s) {
     const float *ps = base + s * sstride;
-    const float m = ps[HD];
-    const float w = m == -INFINITY ? 0.f : expf(m - M);
+    float w;
+    if (ns <= 32) {
+      w = __shfl_sync(0xffffffffu, ws, s);
+    } else {
+      const float m = ps[HD];
+      w = m == -INFINITY ? 0.f : expf(m - M);
+    }
     if constexpr (DL == 4) {
       const float4 o = *(const float4 *)(ps + 4 * lane);
       acc[0] = fmaf(o.x, w, acc[0]);
@@ -504,6 +521,9 @@ static cudaError_t launch_attn(const float *q, const AttnArgs &args, int batch, 
   }
   int ns, cps;
   plan_splits(batch * kv, max_n, num_sms, ns, cps);
+  // With short splits the block's own rows get a split of their own (the last
+  // one, past every context chunk), so that no CTA does twice the others' work.
+  if (cps <= 4 && max_n > 0) ++ns;
   dim3 grid(ns, kv, batch);
   cudaError_t e = launch_pdl(k_attn<HD, KG>, grid, dim3(ATT_THREADS), smem, st, 1, q, args, heads, kv, R, window, scale,
                              ns, cps, part);
