@@ -157,3 +157,19 @@ def test_packed_sizes(L):
     assert L.dflash_gemm_workspace_bytes(16, 1024, 200) == 208 * 1024 * 2
     assert L.dflash_gemm_workspace_bytes(4, 1024, 480) == 2 * 240 * 1024 * 2 * 2
     assert L.dflash_gemm_workspace_bytes(5, 1024, 16) == 0
+
+
+def test_gemm_packed_argument_errors_before_any_launch(L):
+    """dflash_gemm_packed refuses more than 32 rows, null pointers, misalignment and bad shapes
+    on the host (no device work is enqueued)."""
+    m = L.Matrix(1 << 20, 1 << 20)
+    for args in ((4, 256, 1024, 64, 33, 1 << 24, 1 << 24),   # T > 32
+                 (4, 256, 1024, 64, 0, 1 << 24, 1 << 24),    # no rows
+                 (4, 256, 1000, 64, 16, 1 << 24, 1 << 24),   # cols not a multiple of 64
+                 (5, 256, 1024, 64, 16, 1 << 24, 1 << 24),   # kind
+                 (4, 256, 1024, 64, 16, 0, 1 << 24),         # y null
+                 (4, 256, 1024, 64, 16, 1 << 24, (1 << 24) + 4)):  # workspace misaligned
+        kind, rows, cols, group, T, y, ws = args
+        with pytest.raises(L.DflashError) as e:
+            L.dflash_gemm_packed(m, kind, rows, cols, group, T, y, ws, None)
+        assert e.value.code == 2, args
