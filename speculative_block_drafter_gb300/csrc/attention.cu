@@ -6,9 +6,10 @@
 //
 // Split-K: the context rows of a sequence are cut into splits of whole 64-key
 // chunks, one CTA per (split, KV head, sequence); the last split of a sequence
-// takes the block's own rows (alone when the splits are short). Each keeps a running maximum m, sum l and
-// unnormalised output o per query (the rep = heads/kv_heads query heads of the
-// KV head times the block rows) and a second kernel merges the splits.
+// takes the block's own rows (alone when the splits are short). Each keeps a
+// running maximum m, sum l and unnormalised output o per query (the rep =
+// heads/kv_heads query heads of the KV head times the block rows) and a second
+// kernel merges the splits.
 #include <cudaTypedefs.h>
 
 #include <algorithm>
