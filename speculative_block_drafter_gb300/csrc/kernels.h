@@ -142,13 +142,6 @@ cudaError_t conv_stage0(const float *x, const float *d, const float *base, float
 cudaError_t conv_stage1_residual(const float *x, const float *d, const float *base, float *h, int T, int hs,
                                  int kn, int gs, int block, cudaStream_t st);
 constexpr int MAX_BATCH = 64;
-// Per head rms norm (weight [hd]) and, if rotary, the half-split rotation of
-// row t to position pos0[t / block] + t % block (pos0: host array of `nseq`
-// positions, passed by value) or, when pos0 is null, to `pos_base + t`.
-// `inv_freq` is a host array of hd/2 f32 values, passed by value.
-cudaError_t head_norm_rope(float *x, int ld, const float *w, const float *inv_freq, int T, int heads, int hd,
-                           float eps, bool rotary, const int64_t *pos0, int nseq, int block, int64_t pos_base,
-                           cudaStream_t st);
 // The context K of every layer of one settle: the per-head norm and rotation of
 // rows [0, T) of k[l] (ld = heads * hd) to positions pos_base + t, with layer
 // l's norm weight w[l] and rotary flag (host arrays of `nlayers`, passed by value).

@@ -173,20 +173,6 @@ __device__ __forceinline__ void norm_rope_head(float *__restrict__ p, const floa
   }
 }
 
-// One warp per (row, head).
-template <int HD>
-__global__ void k_head_norm_rope(float *__restrict__ x, int ld, const float *__restrict__ w, int T, int heads,
-                                 float eps, int rotary, PosArgs pa,
-                                 int use_pos0, int block, int64_t pos_base) {
-  pdl_wait();
-  const int wid = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const int lane = threadIdx.x & 31;
-  if (wid >= T * heads) return;
-  const int t = wid / heads, h = wid % heads;
-  const int64_t pos = use_pos0 ? pa.pos0[t / block] + (t % block) : pos_base + t;
-  norm_rope_head<HD>(x + (int64_t)t * ld + h * HD, w, eps, rotary != 0, pos, pa.inv, lane);
-}
-
 struct CtxRope {
   float *k[64];
   const float *w[64];
@@ -224,25 +210,6 @@ cudaError_t ctx_norm_rope(float *const *k, const float *const *w, const int *rot
   return cudaErrorInvalidValue;
 }
 
-cudaError_t head_norm_rope(float *x, int ld, const float *w, const float *inv_freq, int T, int heads, int hd,
-                           float eps, bool rotary, const int64_t *pos0, int nseq, int block, int64_t pos_base,
-                           cudaStream_t st) {
-  if (T <= 0) return cudaSuccess;
-  if (hd > 128) return cudaErrorInvalidValue;
-  PosArgs pa;
-  for (int i = 0; i < MAX_BATCH; ++i) pa.pos0[i] = (pos0 && i < nseq) ? pos0[i] : 0;
-  for (int i = 0; i < 64; ++i) pa.inv[i] = i < hd / 2 ? inv_freq[i] : 0.f;
-  const int warps = T * heads;
-  const unsigned grid = (unsigned)((warps * 32 + 255) / 256);
-  const int up0 = pos0 != nullptr;
-  if (hd == 128)
-    return launch_pdl(k_head_norm_rope<128>, dim3(grid), dim3(256), 0, st, 1, x, ld, w, T, heads, eps, (int)rotary, pa,
-                      up0, block, pos_base);
-  if (hd == 64)
-    return launch_pdl(k_head_norm_rope<64>, dim3(grid), dim3(256), 0, st, 1, x, ld, w, T, heads, eps, (int)rotary, pa,
-                      up0, block, pos_base);
-  return cudaErrorInvalidValue;
-}
 
 // ---------------------------------------------------------------- SiLU gate
 __global__ void k_silu_mul(const float *__restrict__ g, const float *__restrict__ u, float *__restrict__ m, int64_t n) {
