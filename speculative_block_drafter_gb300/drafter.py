@@ -220,7 +220,9 @@ class PackedMatrix:
 
     def matmul_packed(self, y: torch.Tensor) -> torch.Tensor:
         """The GEMM kernel alone on the token tiles the last `matmul` packed (up to 32 rows), into y."""
-        T = self._packed_T
+        T = getattr(self, "_packed_T", None)
+        if T is None:
+            raise RuntimeError("matmul_packed needs a matmul call first (it packs the token tiles)")
         assert y.dtype == torch.float32 and y.is_cuda and y.is_contiguous() and y.shape == (T, self.rows)
         L.dflash_gemm_packed(self.mat, self.kind, self.rows, self.cols, self.group, T, y.data_ptr(),
                              self._ws.data_ptr(), _stream())
