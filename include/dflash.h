@@ -148,10 +148,15 @@ size_t dflash_workspace_bytes(const dflash_geometry *g, int32_t max_batch);
  * heads*head_dim % 64, intermediate % 64, head_dim in {64, 128}, block <= 16,
  * selector_top <= 32, vocab % 16) and bind the weights, the per-sequence
  * context caches and the workspace. `ctx_k` / `ctx_v` are host arrays of
- * max_batch*layers device pointers, indexed [seq*layers + layer], each an f32
- * cache [ctx_cap][kv_heads][head_dim] (the card arm's layout,
- * `[position - first][kv][hd]`). Every sequence starts empty at first = 0.
- * Nothing is enqueued. Errors: GEOMETRY, ARG, CAPACITY (workspace), NOMEM. */
+ * max_batch*layers device pointers, indexed [seq*layers + layer], each a
+ * cache of ctx_cap * kv_heads * head_dim * 4 bytes, 16-byte aligned: per
+ * (position - first, KV head), in the card arm's `[position - first][kv]`
+ * order, the row's f32 values as two f16 planes, hi[head_dim] then
+ * lo[head_dim], with hi = x with its low 13 mantissa bits cleared (exact in
+ * f16) and lo = f16(x - hi), so that hi + lo carries about 21 bits of x (the
+ * form the attention's tensor cores read). Every sequence starts empty at
+ * first = 0. Nothing is enqueued. Errors: GEOMETRY, ARG, CAPACITY (workspace),
+ * NOMEM. */
 int dflash_create(dflash_t **out, const dflash_geometry *g, const dflash_weights *w,
                   int32_t max_batch, float *const *ctx_k, float *const *ctx_v, int64_t ctx_cap,
                   void *workspace, size_t workspace_bytes);

@@ -75,24 +75,35 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-bool attn_kv_map(CUtensorMap *m, const float *base, int64_t rows, int kv, int hd, int box_rows) {
+bool attn_kv_map(CUtensorMap *m, const void *base, int64_t rows, int kv, int hd, int box_rows) {
   PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
-  if (!enc || rows < 1 || rows > INT32_MAX || box_rows < 1 || box_rows > 256 || hd % 32) return false;
-  const cuuint64_t dims[3] = {(cuuint64_t)hd, (cuuint64_t)kv, (cuuint64_t)rows};
-  const cuuint64_t strides[2] = {(cuuint64_t)hd * 4, (cuuint64_t)kv * hd * 4};
-  const cuuint32_t box[3] = {32, 1, (cuuint32_t)box_rows};
-  const cuuint32_t es[3] = {1, 1, 1};
-  return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, (void *)base, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+  if (!enc || rows < 1 || rows > INT32_MAX || box_rows < 1 || box_rows > 256 || hd % 64) return false;
+  // (dimension, plane, head, row) of halves; 64 halves (128 bytes) a box row
+  const cuuint64_t dims[4] = {(cuuint64_t)hd, 2, (cuuint64_t)kv, (cuuint64_t)rows};
+  const cuuint64_t strides[3] = {(cuuint64_t)hd * 2, (cuuint64_t)hd * 4, (cuuint64_t)kv * hd * 4};
+  const cuuint32_t box[4] = {64, 1, 1, (cuuint32_t)box_rows};
+  const cuuint32_t es[4] = {1, 1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4, (void *)base, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-__device__ __forceinline__ void tma_load3(uint32_t dst, const CUtensorMap *m, int x, int y, int z, uint32_t bar) {
+__device__ __forceinline__ void tma_load4(uint32_t dst, const CUtensorMap *m, int x, int p, int h, int z, uint32_t bar) {
   asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
-      "[%5];" ::"r"(dst),
-      "l"((uint64_t)m), "r"(x), "r"(y), "r"(z), "r"(bar)
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5}], "
+      "[%6];" ::"r"(dst),
+      "l"((uint64_t)m), "r"(x), "r"(p), "r"(h), "r"(z), "r"(bar)
       : "memory");
+}
+__device__ __forceinline__ void ldsm4(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm4t(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
 }
 
 // f32 pair -> f16 hi/lo pairs without the conversion unit: hi keeps the top 11
@@ -121,28 +132,31 @@ __device__ __forceinline__ void mma3(float (&acc)[4], const uint32_t (&ah)[4], c
 // ---------------------------------------------------------------- the split kernel
 //
 // One CTA per (split, KV head, sequence): the rep*R queries of the KV head over
-// the split's context keys in chunks of 64 (the last split takes the
-// block's own R rows as a final chunk). Warp 0 loads each chunk's K and V with
-// 8 tensor copies (4 column quarters each, 128-byte swizzled) into a 3-stage
-// ring; the MMA fragments are built from the f32 rows with their hi/lo f16
-// split on the fly (bit masks and packed conversions, so that the split stays
-// off the conversion unit), the queries' hi/lo fragments stay in registers. Warp w
-// takes query block w % QW and key group w / QW of every chunk; each keeps a
-// running (m, l, o), merged in the CTA at the end.
-//
-// Within a k16 step the head dimensions are taken in the order that makes each
-// lane's four K values one 16-byte load: step ks, lane quad cq covers
-// dimensions 32 (ks / 2) + 4 (2 cq + ks % 2) + 0..3, the queries' fragments
-// follow the same order. Rows past a chunk's keys (the context's end, or the
-// block's own R rows) hold whatever the copy brought: their scores are masked
-// and their V values replaced by zero.
+// the split's context keys in chunks of 64 (the last split takes the block's
+// own R rows as a final chunk). The context caches and the block's own K/V hold
+// f16 planes (hi, lo) per row and head, written once when the rows were
+// settled or projected. Warp 0 loads each chunk's K and V planes with tensor
+// copies (boxes of 64 rows x 64 halves, 128-byte swizzled) into a 3-stage
+// ring; the warps read their B fragments with ldmatrix (K as stored, V
+// transposed) and hold the queries' hi/lo fragments in registers. Warp w takes
+// query block w % QW and key group w / QW of every chunk; each keeps a running
+// (m, l, o), merged in the CTA at the end. Rows past a chunk's keys (the
+// context's end, or the block's own R rows) hold whatever the copy or an
+// earlier chunk left: their scores are masked and, before P.V, the warps whose
+// key range reaches them zero their V planes.
 struct AttnRing {
-  static constexpr int QUARTER = CH * 128;   // 64 rows x 32 floats
-  static constexpr int HALF = 4 * QUARTER;   // K or V of a chunk (hd = 128)
-  static constexpr int STAGE = 2 * HALF;
+  static constexpr int BOX = CH * 128;       // 64 rows x 64 halves
+  static constexpr int REGION = 2 * BOX;     // one plane of K or V of a chunk (hd <= 128)
+  static constexpr int STAGE = 4 * REGION;   // K hi, K lo, V hi, V lo
   static constexpr int STAGES = 3;
   static constexpr size_t BYTES = (size_t)STAGES * STAGE + 1024 + 64;  // + alignment, barriers
 };
+
+// Byte offset of 16-byte chunk j (8 halves: dimensions 8j..8j+7) of row r in a
+// plane region: box j / 8, swizzled within the row's 128 bytes.
+__device__ __forceinline__ uint32_t plane_off(int r, int j) {
+  return (uint32_t)((j >> 3) * AttnRing::BOX + r * 128 + (((j & 7) ^ (r & 7)) << 4));
+}
 
 template <int HD, int KG>
 __global__ void __launch_bounds__(ATT_THREADS, 1) k_attn(const float *__restrict__ q, const __grid_constant__ AttnArgs args,
@@ -150,11 +164,12 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) k_attn(const float *__restrict
                                                          int cps, float *__restrict__ part) {
   using RG = AttnRing;
   constexpr int S = RG::STAGES;
-  constexpr int HQ = HD / 32;        // column quarters (boxes) of a row
+  constexpr int H2 = HD / 64;        // boxes of a row
   constexpr int KW = CH / KG;        // keys per warp per chunk
   constexpr int NT = KW / 8;         // n8 tiles of scores
   constexpr int KS = KW / 16;        // k16 steps of P . V
   constexpr int OT = HD / 8;         // n8 tiles of the output
+  static_assert(NT % 2 == 0 && OT % 2 == 0 && KS >= 1, "fragments load in pairs of tiles");
   extern __shared__ __align__(16) uint8_t smraw[];
   uint8_t *sm = smraw + ((1024 - (smem_u32(smraw) & 1023)) & 1023);
   const uint32_t ring = smem_u32(sm);
@@ -186,7 +201,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) k_attn(const float *__restrict
   pdl_wait();
   __syncthreads();
 
-  // warp 0, lane 0: the 2 * HQ tensor copies of chunk j into stage st
+  // warp 0, lane 0: the 4 * H2 tensor copies of chunk j into stage st
   auto fill = [&](int j, int st) {
     if (lane != 0) return;
     const bool is_own = own && j == nch - 1;
@@ -194,19 +209,21 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) k_attn(const float *__restrict
     const CUtensorMap *vm = is_own ? &args.own_v : &Sq.vmap;
     const int z = is_own ? b * R : (int)(Sq.row0 + (int64_t)(c0 + j) * CH);
     const uint32_t rows = is_own ? R : CH;
-    const uint32_t bar = full0 + 8 * st, kd = ring + st * RG::STAGE, vd = kd + RG::HALF;
-    mbar_expect_tx(bar, 2 * HQ * rows * 128);
+    const uint32_t bar = full0 + 8 * st, base = ring + st * RG::STAGE;
+    mbar_expect_tx(bar, 4 * H2 * rows * 128);
 #pragma unroll
-    for (int h = 0; h < HQ; ++h) {
-      tma_load3(kd + h * RG::QUARTER, km, 32 * h, g, z, bar);
-      tma_load3(vd + h * RG::QUARTER, vm, 32 * h, g, z, bar);
+    for (int h = 0; h < H2; ++h) {
+      tma_load4(base + 0 * RG::REGION + h * RG::BOX, km, 64 * h, 0, g, z, bar);
+      tma_load4(base + 1 * RG::REGION + h * RG::BOX, km, 64 * h, 1, g, z, bar);
+      tma_load4(base + 2 * RG::REGION + h * RG::BOX, vm, 64 * h, 0, g, z, bar);
+      tma_load4(base + 3 * RG::REGION + h * RG::BOX, vm, 64 * h, 1, g, z, bar);
     }
   };
   int issued = 0;  // chunks warp 0 has filled
   if (warp == 0)
     for (; issued < S && issued < nch; ++issued) fill(issued, issued);
 
-  // the queries' hi/lo A fragments (rows qb*16 + gq and + 8), dimensions in the load order
+  // the queries' hi/lo A fragments (rows qb*16 + gq and + 8)
   uint32_t qh[HD / 16][4], ql[HD / 16][4];
   const int qi0 = qb * 16 + gq, qi1 = qi0 + 8;
   {
@@ -215,16 +232,20 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) k_attn(const float *__restrict
     if (qi1 < Q) q1 = q + ((int64_t)b * R + qi1 % R) * heads * HD + (g * rep + qi1 / R) * HD;
 #pragma unroll
     for (int ks = 0; ks < HD / 16; ++ks) {
-      const int c = 32 * (ks >> 1) + 4 * (2 * cq + (ks & 1));
-      const float4 x0 = q0 ? *(const float4 *)(q0 + c) : make_float4(0.f, 0.f, 0.f, 0.f);
-      const float4 x1 = q1 ? *(const float4 *)(q1 + c) : make_float4(0.f, 0.f, 0.f, 0.f);
-      split_hl(x0.x, x0.y, qh[ks][0], ql[ks][0]);
-      split_hl(x1.x, x1.y, qh[ks][1], ql[ks][1]);
-      split_hl(x0.z, x0.w, qh[ks][2], ql[ks][2]);
-      split_hl(x1.z, x1.w, qh[ks][3], ql[ks][3]);
+      const int c = ks * 16 + 2 * cq;
+      const float2 x00 = q0 ? *(const float2 *)(q0 + c) : make_float2(0.f, 0.f);
+      const float2 x10 = q1 ? *(const float2 *)(q1 + c) : make_float2(0.f, 0.f);
+      const float2 x01 = q0 ? *(const float2 *)(q0 + c + 8) : make_float2(0.f, 0.f);
+      const float2 x11 = q1 ? *(const float2 *)(q1 + c + 8) : make_float2(0.f, 0.f);
+      split_hl(x00.x, x00.y, qh[ks][0], ql[ks][0]);
+      split_hl(x10.x, x10.y, qh[ks][1], ql[ks][1]);
+      split_hl(x01.x, x01.y, qh[ks][2], ql[ks][2]);
+      split_hl(x11.x, x11.y, qh[ks][3], ql[ks][3]);
     }
   }
   const int r0 = qi0 % R, r1 = qi1 % R;
+  // ldmatrix lane roles: row within an 8x8 matrix and which of the four matrices
+  const int mr = lane & 7, mi = lane >> 3;
 
   float o[OT][4];
 #pragma unroll
@@ -240,26 +261,52 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) k_attn(const float *__restrict
     const bool is_own = own && j == nch - 1;
     const int kb = (c0 + j) * CH;
     const int cnt = is_own ? R : min(CH, n - kb);
-    const uint8_t *Ks = sm + st * RG::STAGE, *Vs = Ks + RG::HALF;
+    uint8_t *stp = sm + st * RG::STAGE;
+    const uint32_t khi = smem_u32(stp), klo = khi + RG::REGION, vhi = khi + 2 * RG::REGION, vlo = khi + 3 * RG::REGION;
+    const int kk0 = kgi * KW;
+    if (busy && cnt < kk0 + KW) {
+      // zero the V rows of this warp's keys past the chunk's (both planes, every box)
+      const int z0 = max(kk0, cnt), nz = kk0 + KW - z0;
+      for (int idx = lane; idx < nz * 2 * H2 * 8; idx += 32) {
+        const int row = z0 + idx / (2 * H2 * 8), rest = idx % (2 * H2 * 8);
+        const int pl = rest / (H2 * 8), bx = (rest / 8) % H2, ch = rest % 8;
+        *(uint4 *)(stp + (2 + pl) * RG::REGION + bx * RG::BOX + row * 128 + ch * 16) = make_uint4(0u, 0u, 0u, 0u);
+      }
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // before the stage's next tensor copy
+      __syncwarp();
+    }
     if (busy) {
-      const int kk0 = kgi * KW;
       float sc[NT][4];
+      // S = Q . K^T: per k16 step and pair of key tiles the four 8x8 matrices
+      // (tile t, dims 16ks..+8), (t, +8..+16), (t+1, ..), (t+1, ..) of each plane.
+      // The three products go to separate accumulators (two with four tiles),
+      // so that the MMAs of a step do not wait on one another.
+      constexpr int NA = NT == 2 ? 3 : 2;
+      float sa[NA][NT][4];
 #pragma unroll
-      for (int t = 0; t < NT; ++t) sc[t][0] = sc[t][1] = sc[t][2] = sc[t][3] = 0.f;
-      // S = Q . K^T over the warp's keys; row kk0 + 8t + gq has swizzle phase gq
+      for (int a = 0; a < NA; ++a)
+#pragma unroll
+        for (int t = 0; t < NT; ++t) sa[a][t][0] = sa[a][t][1] = sa[a][t][2] = sa[a][t][3] = 0.f;
 #pragma unroll
       for (int ks = 0; ks < HD / 16; ++ks) {
 #pragma unroll
-        for (int t = 0; t < NT; ++t) {
-          const int row = kk0 + 8 * t + gq;
-          const float4 kx = *(const float4 *)(Ks + (ks >> 1) * RG::QUARTER + row * 128 +
-                                              (((2 * cq + (ks & 1)) ^ gq) << 4));
-          uint32_t bh0, bl0, bh1, bl1;
-          split_hl(kx.x, kx.y, bh0, bl0);
-          split_hl(kx.z, kx.w, bh1, bl1);
-          mma3(sc[t], qh[ks], ql[ks], bh0, bh1, bl0, bl1);
+        for (int t = 0; t < NT; t += 2) {
+          const uint32_t off = plane_off(kk0 + 8 * (t + (mi >> 1)) + mr, 2 * ks + (mi & 1));
+          uint32_t h0, h1, h2, h3, w0, w1, w2, w3;
+          ldsm4(khi + off, h0, h1, h2, h3);
+          ldsm4(klo + off, w0, w1, w2, w3);
+          mma16816(sa[0][t], qh[ks], h0, h1);
+          mma16816(sa[0][t + 1], qh[ks], h2, h3);
+          mma16816(sa[1][t], qh[ks], w0, w1);
+          mma16816(sa[1][t + 1], qh[ks], w2, w3);
+          mma16816(sa[NA - 1][t], ql[ks], h0, h1);
+          mma16816(sa[NA - 1][t + 1], ql[ks], h2, h3);
         }
       }
+#pragma unroll
+      for (int t = 0; t < NT; ++t)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) sc[t][e] = sa[0][t][e] + (NA == 3 ? sa[1][t][e] + sa[2][t][e] : sa[1][t][e]);
       // mask, scale, online softmax (rows gq, gq+8; the 4 lanes of a row hold its 2*NT keys)
       float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
@@ -307,42 +354,26 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) k_attn(const float *__restrict
           o[t][3] *= a1;
         }
       }
-      // O += P . V: P as hi/lo A fragments from the scores; V rows kA, kA+1, kA+8,
-      // kA+9 (swizzle phases 2cq, 2cq+1) at dimension 8t + gq. Rows past the
-      // chunk's keys (a partial chunk only) read as zero.
-      auto pv = [&](auto partial) {
+      // O += P . V: P as hi/lo A fragments from the scores; V by transposed
+      // ldmatrix: (keys +0..8, dims tile t), (keys +8..16, t), (.., t+1), (.., t+1)
 #pragma unroll
-        for (int js = 0; js < KS; ++js) {
-          uint32_t ph[4], pl[4];
-          split_hl(sc[2 * js][0], sc[2 * js][1], ph[0], pl[0]);
-          split_hl(sc[2 * js][2], sc[2 * js][3], ph[1], pl[1]);
-          split_hl(sc[2 * js + 1][0], sc[2 * js + 1][1], ph[2], pl[2]);
-          split_hl(sc[2 * js + 1][2], sc[2 * js + 1][3], ph[3], pl[3]);
-          const int kA = kk0 + 16 * js + 2 * cq;
-          const bool v0 = kA < cnt, v1 = kA + 1 < cnt, v2 = kA + 8 < cnt, v3 = kA + 9 < cnt;
-          const uint8_t *va = Vs + kA * 128 + ((gq & 3) << 2);
+      for (int js = 0; js < KS; ++js) {
+        uint32_t ph[4], pl[4];
+        split_hl(sc[2 * js][0], sc[2 * js][1], ph[0], pl[0]);
+        split_hl(sc[2 * js][2], sc[2 * js][3], ph[1], pl[1]);
+        split_hl(sc[2 * js + 1][0], sc[2 * js + 1][1], ph[2], pl[2]);
+        split_hl(sc[2 * js + 1][2], sc[2 * js + 1][3], ph[3], pl[3]);
+        const int row = kk0 + 16 * js + 8 * (mi & 1) + mr;
 #pragma unroll
-          for (int t = 0; t < OT; ++t) {
-            const int c = (2 * t + (gq >> 2)) & 7;
-            const uint8_t *vq = va + (t >> 2) * RG::QUARTER;
-            const float *e0 = (const float *)(vq + ((c ^ (2 * cq)) << 4));
-            const float *e1 = (const float *)(vq + 128 + ((c ^ (2 * cq + 1)) << 4));
-            float x0 = e0[0], x1 = e1[0], x2 = e0[256], x3 = e1[256];  // rows +8: 1024 bytes on
-            if (decltype(partial)::value) {
-              x0 = v0 ? x0 : 0.f;
-              x1 = v1 ? x1 : 0.f;
-              x2 = v2 ? x2 : 0.f;
-              x3 = v3 ? x3 : 0.f;
-            }
-            uint32_t bh0, bl0, bh1, bl1;
-            split_hl(x0, x1, bh0, bl0);
-            split_hl(x2, x3, bh1, bl1);
-            mma3(o[t], ph, pl, bh0, bh1, bl0, bl1);
-          }
+        for (int t = 0; t < OT; t += 2) {
+          const uint32_t off = plane_off(row, t + (mi >> 1));
+          uint32_t h0, h1, h2, h3, w0, w1, w2, w3;
+          ldsm4t(vhi + off, h0, h1, h2, h3);
+          ldsm4t(vlo + off, w0, w1, w2, w3);
+          mma3(o[t], ph, pl, h0, h1, w0, w1);
+          mma3(o[t + 1], ph, pl, h2, h3, w2, w3);
         }
-      };
-      if (cnt < CH) pv(std::true_type{});
-      else pv(std::false_type{});
+      }
     }
     // release the stage; warp 0 refills it with the chunk S ahead
     __syncwarp();

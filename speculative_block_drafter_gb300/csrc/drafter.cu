@@ -45,7 +45,7 @@ struct Seq {
 
 // Workspace carve; sizes in bytes.
 struct Carve {
-  size_t h, x, xc, d, d2, q, k, v, y, o, gt, up, part, sel, act, total;
+  size_t h, x, xc, d, d2, q, k, v, y, o, gt, up, part, sel, act, kvs, kp, vp, total;
 };
 
 Carve carve_of(const dflash_geometry &g, int max_batch) {
@@ -69,6 +69,10 @@ Carve carve_of(const dflash_geometry &g, int max_batch) {
   c.gt = up(T * (size_t)g.intermediate * f);
   c.up = c.gt;
   c.part = up(dfl::attn_partial_bytes(max_batch, g.kv_heads, g.heads, R, g.head_dim));
+  const size_t kvd = (size_t)g.kv_heads * g.head_dim;
+  c.kvs = up((size_t)2 * g.layers * DFLASH_SETTLE_MAX * kvd * f);  // a settle's K and V before their planes
+  c.kp = up(T * kvd * 4);                                          // the block's own K and V as f16 planes
+  c.vp = c.kp;
   c.sel = up(dfl::select_scratch_bytes(max_batch * (R - 1), g.vocab, g.selector_top));
   // packed token tiles of the largest GEMM (block rows, a settle chunk, the fc's taps)
   const int Tb = max_batch * R;
@@ -76,7 +80,8 @@ Carve carve_of(const dflash_geometry &g, int max_batch) {
   c.act = up(std::max({dfl::tc_act_bytes(Tb, kmax, true), dfl::tc_act_bytes(DFLASH_SETTLE_MAX, g.hidden, true),
                        dfl::tc_act_bytes(DFLASH_SETTLE_MAX, g.taps * g.hidden, false),
                        dfl::tc_act_bytes(Tb, g.hidden, false)}));
-  c.total = c.h + c.x + c.xc + c.d + c.d2 + c.q + c.k + c.v + c.y + c.o + c.gt + c.up + c.part + c.sel + c.act;
+  c.total = c.h + c.x + c.xc + c.d + c.d2 + c.q + c.k + c.v + c.y + c.o + c.gt + c.up + c.part + c.sel + c.act +
+            c.kvs + c.kp + c.vp;
   return c;
 }
 
@@ -135,7 +140,8 @@ struct dflash_t {
   int64_t cap = 0;
   char *ws = nullptr;
   Carve c{};
-  float *h, *x, *xc, *d, *d2, *q, *k, *v, *y, *o, *gt, *up, *part;
+  float *h, *x, *xc, *d, *d2, *q, *k, *v, *y, *o, *gt, *up, *part, *kvs;
+  __half *kp, *vp;
   void *sel, *act;
   std::vector<Seq> seqs;
   std::vector<float> inv;
@@ -159,8 +165,8 @@ bool encode_maps(dflash_t *d) {
         !dfl::attn_kv_map(&d->vmap[i], d->cv[i], d->cap, g.kv_heads, g.head_dim, 64))
       return false;
   const int64_t rows = (int64_t)d->max_batch * g.block;
-  if (!dfl::attn_kv_map(&d->own_k, d->k, rows, g.kv_heads, g.head_dim, g.block) ||
-      !dfl::attn_kv_map(&d->own_v, d->v, rows, g.kv_heads, g.head_dim, g.block))
+  if (!dfl::attn_kv_map(&d->own_k, d->kp, rows, g.kv_heads, g.head_dim, g.block) ||
+      !dfl::attn_kv_map(&d->own_v, d->vp, rows, g.kv_heads, g.head_dim, g.block))
     return false;
   d->maps = true;
   return true;
@@ -340,6 +346,9 @@ int dflash_create(dflash_t **out, const dflash_geometry *g, const dflash_weights
   d->gt = (float *)take(c.gt);
   d->up = (float *)take(c.up);
   d->part = (float *)take(c.part);
+  d->kvs = (float *)take(c.kvs);
+  d->kp = (__half *)take(c.kp);
+  d->vp = (__half *)take(c.vp);
   d->sel = take(c.sel);
   d->act = take(c.act);
   d->seqs.assign(max_batch, Seq{});
@@ -389,22 +398,29 @@ int dflash_settle(dflash_t *d, int32_t seq, int64_t pos, const float *taps, int3
   const dfl::TcJob fc{d->w.fc.data, nullptr, d->x, hs, hs};
   DF_CUDA(dfl::tc_gemm_f16(&fc, 1, taps, tw, n, tw, d->act, d->num_sms, st));
   DF_CUDA(dfl::rmsnorm(d->x, d->w.hidden_norm, d->x, n, hs, (float)g.eps, 1, -1, -1, st));
-  // k = Wk t, v = Wv t of every layer in one GEMM, straight into the caches at rows at..at+n-1
+  // k = Wk t, v = Wv t of every layer in one GEMM (into the workspace), then
+  // k = rot(rms_head(k, k_norm)) at positions pos.. (rotary layers) and both as
+  // f16 planes into the caches at rows at..at+n-1
   dfl::WideJob kv[dfl::WIDE_MAX_JOBS];
-  float *kc[DFLASH_MAX_LAYERS];
+  const float *sk[DFLASH_MAX_LAYERS], *sv[DFLASH_MAX_LAYERS];
+  __half *ckp[DFLASH_MAX_LAYERS], *cvp[DFLASH_MAX_LAYERS];
   const float *kn[DFLASH_MAX_LAYERS];
   int rot[DFLASH_MAX_LAYERS];
   for (int l = 0; l < g.layers; ++l) {
     const dflash_layer_weights &L = d->layers[l];
-    kc[l] = d->ck[(size_t)seq * g.layers + l] + at * kvd;
+    float *yk = d->kvs + (size_t)(2 * l) * DFLASH_SETTLE_MAX * kvd, *yv = yk + (size_t)DFLASH_SETTLE_MAX * kvd;
+    sk[l] = yk;
+    sv[l] = yv;
+    ckp[l] = (__half *)(d->ck[(size_t)seq * g.layers + l] + at * kvd);
+    cvp[l] = (__half *)(d->cv[(size_t)seq * g.layers + l] + at * kvd);
     kn[l] = L.k_norm;
     rot[l] = g.no_rope[l] == 0;
-    kv[2 * l] = dfl::WideJob{L.k.data, L.k.scales, kc[l], kvd, kvd, 0};
-    kv[2 * l + 1] = dfl::WideJob{L.v.data, L.v.scales, d->cv[(size_t)seq * g.layers + l] + at * kvd, kvd, kvd, 0};
+    kv[2 * l] = dfl::WideJob{L.k.data, L.k.scales, yk, kvd, kvd, 0};
+    kv[2 * l + 1] = dfl::WideJob{L.v.data, L.v.scales, yv, kvd, kvd, 0};
   }
   DF_CUDA(dfl::wide_gemm(kv, 2 * g.layers, 0, true, g.quant_group, d->x, hs, n, hs, d->act, d->num_sms, st));
-  // k = rot(rms_head(k, k_norm)) at positions pos..pos+n-1 (rotary layers)
-  DF_CUDA(dfl::ctx_norm_rope(kc, kn, rot, g.layers, n, g.kv_heads, g.head_dim, (float)g.eps, d->inv.data(), pos, st));
+  DF_CUDA(dfl::ctx_planes(sk, sv, ckp, cvp, kn, rot, g.layers, n, g.kv_heads, g.head_dim, (float)g.eps, d->inv.data(),
+                          pos, st));
   s.len = at + n;
   return DFLASH_OK;
 }
@@ -491,8 +507,8 @@ int dflash_block(dflash_t *d, int32_t batch, const int64_t *anchor_pos, const fl
       DF_CUDA(dfl::conv0_pack(d->x, d->d, L.attn_base, T, hs, kn, gs, R, pack_for(2, ti, hs),
                               zero_for(qkv, 3, dfl::tc_splits_int4(qkv, 3, T, hs, sms), T), st));
       DF_CUDA(dfl::tc_gemm_int4_packed(qkv, 3, grp, d->act, T, hs, sms, st));
-      DF_CUDA(dfl::qk_norm_rope(d->q, qd, L.q_norm, nh, d->k, kvd, L.k_norm, kv, d->inv.data(), T, hd, eps, rot,
-                                anchor_pos, batch, R, st));
+      DF_CUDA(dfl::qk_norm_rope(d->q, qd, L.q_norm, nh, d->k, kvd, L.k_norm, d->v, kvd, kv, d->kp, d->vp,
+                                d->inv.data(), T, hd, eps, rot, anchor_pos, batch, R, st));
       ranges(l, W);
       const dfl::PackDst po = pack_for(2, ti, qd);
       const dfl::ZeroSet zo = zero_for(&oj, 1, dfl::tc_splits_int4(&oj, 1, T, qd, sms), T);
@@ -545,8 +561,8 @@ int dflash_block(dflash_t *d, int32_t batch, const int64_t *anchor_pos, const fl
     const dfl::TcJob qkv[3] = {{L.q.data, L.q.scales, d->q, qd, qd}, {L.k.data, L.k.scales, d->k, kvd, kvd},
                                {L.v.data, L.v.scales, d->v, kvd, kvd}};
     DF_CUDA(dfl::tc_gemm_int4(qkv, 3, grp, d->xc, hs, T, hs, d->act, sms, st));
-    DF_CUDA(dfl::qk_norm_rope(d->q, qd, L.q_norm, nh, d->k, kvd, L.k_norm, kv, d->inv.data(), T, hd, eps, rot,
-                              anchor_pos, batch, R, st));
+    DF_CUDA(dfl::qk_norm_rope(d->q, qd, L.q_norm, nh, d->k, kvd, L.k_norm, d->v, kvd, kv, d->kp, d->vp,
+                              d->inv.data(), T, hd, eps, rot, anchor_pos, batch, R, st));
     ranges(l, W);
     DF_CUDA(dfl::attention(d->q, d->own_k, d->own_v, seqs.data(), batch, nh, kv, hd, R, W, scale, d->part, d->y, sms,
                            nullptr, nullptr, st));

@@ -142,11 +142,14 @@ cudaError_t conv_stage0(const float *x, const float *d, const float *base, float
 cudaError_t conv_stage1_residual(const float *x, const float *d, const float *base, float *h, int T, int hs,
                                  int kn, int gs, int block, cudaStream_t st);
 constexpr int MAX_BATCH = 64;
-// The context K of every layer of one settle: the per-head norm and rotation of
-// rows [0, T) of k[l] (ld = heads * hd) to positions pos_base + t, with layer
-// l's norm weight w[l] and rotary flag (host arrays of `nlayers`, passed by value).
-cudaError_t ctx_norm_rope(float *const *k, const float *const *w, const int *rotary, int nlayers, int T, int heads,
-                          int hd, float eps, const float *inv_freq, int64_t pos_base, cudaStream_t st);
+// The settle's K and V of every layer into the context caches as f16 planes
+// (per row and head: hi[hd] then lo[hd], hi + lo carrying about 21 bits): K
+// normalised per head and, on rotary layers, rotated to pos_base + t. k/v[l]
+// are the settle's rows [T][heads][hd] f32, ck/cv[l] the cache rows they go
+// to; host arrays of `nlayers` (w: k norms, rotary flags), passed by value.
+cudaError_t ctx_planes(const float *const *k, const float *const *v, __half *const *ck, __half *const *cv,
+                       const float *const *w, const int *rotary, int nlayers, int T, int heads, int hd, float eps,
+                       const float *inv_freq, int64_t pos_base, cudaStream_t st);
 // Fused producers of a GEMM's packed token tiles (rows.cu). Each writes its
 // result into P (the following GEMM's token tiles) and clears Z (that GEMM's
 // outputs, when it splits its k-range).
@@ -160,18 +163,21 @@ cudaError_t conv0_pack(const float *x, const float *d, const float *base, int T,
                        const PackDst &P, const ZeroSet &Z, cudaStream_t st);
 cudaError_t silu_pack(const float *g, const float *u, int T, int n, const PackDst &P, const ZeroSet &Z,
                       cudaStream_t st);
-// q and k of the block: per head norm and rotation to pos0[t / block] + t % block, one launch.
-cudaError_t qk_norm_rope(float *q, int ldq, const float *wq, int hq, float *k, int ldk, const float *wk, int hk,
-                         const float *inv_freq, int T, int hd, float eps, bool rotary, const int64_t *pos0, int nseq,
-                         int block, cudaStream_t st);
+// The block's q, k and v, one launch: q normalised per head and rotated to
+// pos0[t / block] + t % block in place; k the same and v as it is, written as
+// f16 planes [T][hk][2][hd] to kp and vp (the attention's format).
+cudaError_t qk_norm_rope(float *q, int ldq, const float *wq, int hq, const float *k, int ldk, const float *wk,
+                         const float *v, int ldv, int hk, __half *kp, __half *vp, const float *inv_freq, int T, int hd,
+                         float eps, bool rotary, const int64_t *pos0, int nseq, int block, cudaStream_t st);
 // m = silu(g) * u, elementwise over n values.
 cudaError_t silu_mul(const float *g, const float *u, float *m, int64_t n, cudaStream_t st);
 
 // -------------------------------------------------------------- attention (attention.cu)
-// The kernel loads K and V rows with tensor copies: an f32 cache [rows][kv][hd]
-// is described by a map of boxes of 32 floats x 1 head x `box_rows` rows,
-// 128-byte swizzled. Encoding is host-only work; false if the driver cannot.
-bool attn_kv_map(CUtensorMap *m, const float *base, int64_t rows, int kv, int hd, int box_rows);
+// The kernel loads K and V with tensor copies: a cache of f16 planes
+// [rows][kv][2][hd] (per row and head: hi[hd], lo[hd]) is described by a map
+// of boxes of 64 halves x 1 plane x 1 head x `box_rows` rows, 128-byte
+// swizzled. Encoding is host-only work; false if the driver cannot.
+bool attn_kv_map(CUtensorMap *m, const void *base, int64_t rows, int kv, int hd, int box_rows);
 struct AttnSeq {          // per sequence and layer
   CUtensorMap kmap, vmap; // the layer's K and V cache of the sequence (box_rows 64)
   int64_t row0;           // cache row of the first context row read
@@ -181,8 +187,8 @@ struct AttnSeq {          // per sequence and layer
 };
 size_t attn_partial_bytes(int max_batch, int kv_heads, int heads, int block, int hd);
 // `seqs` is a host array of `batch` entries (passed by value). q is [batch *
-// block][heads][hd]; own_k / own_v map the block's own K and V [batch * block]
-// [kv][hd] (box_rows = block). With `pack` set, the merged rows go straight
+// block][heads][hd] f32 (normalised and rotated); own_k / own_v map the block's
+// own K and V planes [batch * block][kv][2][hd] (box_rows = block). With `pack` set, the merged rows go straight
 // into those token tiles (for the output projection; `zero` its outputs to
 // clear) instead of y.
 cudaError_t attention(const float *q, const CUtensorMap &own_k, const CUtensorMap &own_v, const AttnSeq *seqs,

@@ -135,15 +135,12 @@ struct PosArgs {
 // rotates it to `pos`. HD/32 values per lane: lane owns i = lane + 32m
 // (m < HD/64) of the low half and its partner i + HD/2.
 template <int HD>
-__device__ __forceinline__ void norm_rope_head(float *__restrict__ p, const float *__restrict__ w, float eps,
-                                               bool rotary, int64_t pos, const float *inv, int lane) {
+__device__ __forceinline__ void norm_rope_regs(float (&lo)[HD / 64], float (&hi)[HD / 64], const float *__restrict__ w,
+                                               float eps, bool rotary, int64_t pos, const float *inv, int lane) {
   constexpr int M = HD / 64;  // pairs per lane
-  float lo[M], hi[M];
   float ss = 0.f;
 #pragma unroll
   for (int m = 0; m < M; ++m) {
-    lo[m] = p[lane + 32 * m];
-    hi[m] = p[lane + 32 * m + HD / 2];
     ss = fmaf(lo[m], lo[m], ss);
     ss = fmaf(hi[m], hi[m], ss);
   }
@@ -166,6 +163,19 @@ __device__ __forceinline__ void norm_rope_head(float *__restrict__ p, const floa
       hi[m] = b * cs + a * sn;
     }
   }
+}
+
+template <int HD>
+__device__ __forceinline__ void norm_rope_head(float *__restrict__ p, const float *__restrict__ w, float eps,
+                                               bool rotary, int64_t pos, const float *inv, int lane) {
+  constexpr int M = HD / 64;
+  float lo[M], hi[M];
+#pragma unroll
+  for (int m = 0; m < M; ++m) {
+    lo[m] = p[lane + 32 * m];
+    hi[m] = p[lane + 32 * m + HD / 2];
+  }
+  norm_rope_regs<HD>(lo, hi, w, eps, rotary, pos, inv, lane);
 #pragma unroll
   for (int m = 0; m < M; ++m) {
     p[lane + 32 * m] = lo[m];
@@ -173,40 +183,80 @@ __device__ __forceinline__ void norm_rope_head(float *__restrict__ p, const floa
   }
 }
 
-struct CtxRope {
-  float *k[64];
-  const float *w[64];
+// A head row as f16 planes (the attention's K/V format): hi[i] = f16 of x with
+// its low 13 mantissa bits cleared (exact), lo[i] = f16(x - that); hi + lo
+// carries about 21 bits of x. dst holds hi[0..HD) then lo[0..HD).
+__device__ __forceinline__ void plane_pair(float x, __half &h, __half &l) {
+  const float t = __uint_as_float(__float_as_uint(x) & 0xFFFFE000u);
+  h = __float2half_rn(t);
+  l = __float2half_rn(x - t);
+}
+template <int HD>
+__device__ __forceinline__ void store_planes(__half *__restrict__ dst, const float (&lo)[HD / 64],
+                                             const float (&hi)[HD / 64], int lane) {
+#pragma unroll
+  for (int m = 0; m < HD / 64; ++m) {
+    __half h, l;
+    plane_pair(lo[m], h, l);
+    dst[lane + 32 * m] = h;
+    dst[HD + lane + 32 * m] = l;
+    plane_pair(hi[m], h, l);
+    dst[lane + 32 * m + HD / 2] = h;
+    dst[HD + lane + 32 * m + HD / 2] = l;
+  }
+}
+
+struct CtxPlanes {
+  const float *k[64], *v[64];   // the settle's K and V of each layer, f32 [T][heads][HD]
+  __half *ck[64], *cv[64];      // the cache rows they go to, planes [T][heads][2][HD]
+  const float *w[64];           // k norms
   int rotary[64];
   float inv[64];
 };
 
-// One warp per (row, head) of layer blockIdx.y's context K.
+// One warp per (K or V, row, head) of layer blockIdx.y: K normalised and
+// rotated to pos_base + t, both written to the cache as f16 planes.
 template <int HD>
-__global__ void k_ctx_norm_rope(CtxRope R, int T, int heads, float eps, int64_t pos_base) {
+__global__ void k_ctx_planes(CtxPlanes P, int T, int heads, float eps, int64_t pos_base) {
   pdl_wait();
   const int wid = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
-  if (wid >= T * heads) return;
+  if (wid >= 2 * T * heads) return;
   const int l = blockIdx.y;
-  const int t = wid / heads, h = wid % heads;
-  norm_rope_head<HD>(R.k[l] + ((int64_t)t * heads + h) * HD, R.w[l], eps, R.rotary[l] != 0, pos_base + t, R.inv, lane);
+  const bool isk = wid < T * heads;
+  const int w2 = isk ? wid : wid - T * heads;
+  const int t = w2 / heads, h = w2 % heads;
+  const float *src = (isk ? P.k[l] : P.v[l]) + ((int64_t)t * heads + h) * HD;
+  constexpr int M = HD / 64;
+  float lo[M], hi[M];
+#pragma unroll
+  for (int m = 0; m < M; ++m) {
+    lo[m] = src[lane + 32 * m];
+    hi[m] = src[lane + 32 * m + HD / 2];
+  }
+  if (isk) norm_rope_regs<HD>(lo, hi, P.w[l], eps, P.rotary[l] != 0, pos_base + t, P.inv, lane);
+  store_planes<HD>((isk ? P.ck[l] : P.cv[l]) + ((int64_t)t * heads + h) * 2 * HD, lo, hi, lane);
 }
 
-cudaError_t ctx_norm_rope(float *const *k, const float *const *w, const int *rotary, int nlayers, int T, int heads,
-                          int hd, float eps, const float *inv_freq, int64_t pos_base, cudaStream_t st) {
+cudaError_t ctx_planes(const float *const *k, const float *const *v, __half *const *ck, __half *const *cv,
+                       const float *const *w, const int *rotary, int nlayers, int T, int heads, int hd, float eps,
+                       const float *inv_freq, int64_t pos_base, cudaStream_t st) {
   if (T <= 0) return cudaSuccess;
   if (nlayers < 1 || nlayers > 64) return cudaErrorInvalidValue;
-  CtxRope R{};
+  CtxPlanes P{};
   for (int l = 0; l < nlayers; ++l) {
-    R.k[l] = k[l];
-    R.w[l] = w[l];
-    R.rotary[l] = rotary[l];
+    P.k[l] = k[l];
+    P.v[l] = v[l];
+    P.ck[l] = ck[l];
+    P.cv[l] = cv[l];
+    P.w[l] = w[l];
+    P.rotary[l] = rotary[l];
   }
-  for (int i = 0; i < 64; ++i) R.inv[i] = i < hd / 2 ? inv_freq[i] : 0.f;
-  const int warps = T * heads;
+  for (int i = 0; i < 64; ++i) P.inv[i] = i < hd / 2 ? inv_freq[i] : 0.f;
+  const int warps = 2 * T * heads;
   dim3 grid((unsigned)((warps * 32 + 255) / 256), nlayers);
-  if (hd == 128) return launch_pdl(k_ctx_norm_rope<128>, grid, dim3(256), 0, st, 1, R, T, heads, eps, pos_base);
-  if (hd == 64) return launch_pdl(k_ctx_norm_rope<64>, grid, dim3(256), 0, st, 1, R, T, heads, eps, pos_base);
+  if (hd == 128) return launch_pdl(k_ctx_planes<128>, grid, dim3(256), 0, st, 1, P, T, heads, eps, pos_base);
+  if (hd == 64) return launch_pdl(k_ctx_planes<64>, grid, dim3(256), 0, st, 1, P, T, heads, eps, pos_base);
   return cudaErrorInvalidValue;
 }
 
@@ -398,22 +448,38 @@ __global__ void __launch_bounds__(FP_THREADS) k_silu_pack(const float *__restric
   pack_store8(P, t, i0, m);
 }
 
-// The per-head norm and rotation of the block's q and k in one launch.
+// The block's q, k and v in one launch: q normalised and rotated in place; k
+// normalised and rotated, and v as it is, written as f16 planes [T][hk][2][HD]
+// (the attention's format) to kp and vp.
 template <int HD>
 __global__ void k_qk_norm_rope(float *__restrict__ q, int ldq, const float *__restrict__ wq, int hq,
-                               float *__restrict__ k, int ldk, const float *__restrict__ wk, int hk, int T, float eps,
-                               int rotary, PosArgs pa, int block) {
+                               const float *__restrict__ k, int ldk, const float *__restrict__ wk,
+                               const float *__restrict__ v, int ldv, int hk, __half *__restrict__ kp,
+                               __half *__restrict__ vp, int T, float eps, int rotary, PosArgs pa, int block) {
   pdl_wait();
   const int wid = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
-  const int nq = T * hq;
-  if (wid >= nq + T * hk) return;
-  const bool isq = wid < nq;
-  const int w2 = isq ? wid : wid - nq, heads = isq ? hq : hk;
+  const int nq = T * hq, nk = T * hk;
+  if (wid >= nq + 2 * nk) return;
+  const int kind = wid < nq ? 0 : wid < nq + nk ? 1 : 2;  // q, k, v
+  const int w2 = kind == 0 ? wid : kind == 1 ? wid - nq : wid - nq - nk;
+  const int heads = kind == 0 ? hq : hk;
   const int t = w2 / heads, h = w2 % heads;
   const int64_t pos = pa.pos0[t / block] + (t % block);
-  float *p = isq ? q + (int64_t)t * ldq + h * HD : k + (int64_t)t * ldk + h * HD;
-  norm_rope_head<HD>(p, isq ? wq : wk, eps, rotary != 0, pos, pa.inv, lane);
+  if (kind == 0) {
+    norm_rope_head<HD>(q + (int64_t)t * ldq + h * HD, wq, eps, rotary != 0, pos, pa.inv, lane);
+    return;
+  }
+  const float *src = kind == 1 ? k + (int64_t)t * ldk + h * HD : v + (int64_t)t * ldv + h * HD;
+  constexpr int M = HD / 64;
+  float lo[M], hi[M];
+#pragma unroll
+  for (int m = 0; m < M; ++m) {
+    lo[m] = src[lane + 32 * m];
+    hi[m] = src[lane + 32 * m + HD / 2];
+  }
+  if (kind == 1) norm_rope_regs<HD>(lo, hi, wk, eps, rotary != 0, pos, pa.inv, lane);
+  store_planes<HD>((kind == 1 ? kp : vp) + ((int64_t)t * hk + h) * 2 * HD, lo, hi, lane);
 }
 
 static unsigned zero_blocks_for(const ZeroSet &Z) {
@@ -449,21 +515,21 @@ cudaError_t silu_pack(const float *g, const float *u, int T, int n, const PackDs
   return launch_pdl(k_silu_pack, dim3(work + zero_blocks_for(Z)), dim3(FP_THREADS), 0, st, 1, g, u, T, n, work, P, Z);
 }
 
-cudaError_t qk_norm_rope(float *q, int ldq, const float *wq, int hq, float *k, int ldk, const float *wk, int hk,
-                         const float *inv_freq, int T, int hd, float eps, bool rotary, const int64_t *pos0, int nseq,
-                         int block, cudaStream_t st) {
+cudaError_t qk_norm_rope(float *q, int ldq, const float *wq, int hq, const float *k, int ldk, const float *wk,
+                         const float *v, int ldv, int hk, __half *kp, __half *vp, const float *inv_freq, int T, int hd,
+                         float eps, bool rotary, const int64_t *pos0, int nseq, int block, cudaStream_t st) {
   if (T <= 0) return cudaSuccess;
   PosArgs pa;
   for (int i = 0; i < MAX_BATCH; ++i) pa.pos0[i] = (pos0 && i < nseq) ? pos0[i] : 0;
   for (int i = 0; i < 64; ++i) pa.inv[i] = i < hd / 2 ? inv_freq[i] : 0.f;
-  const int warps = T * (hq + hk);
+  const int warps = T * (hq + 2 * hk);
   const unsigned grid = (unsigned)((warps * 32 + 255) / 256);
   if (hd == 128)
-    return launch_pdl(k_qk_norm_rope<128>, dim3(grid), dim3(256), 0, st, 1, q, ldq, wq, hq, k, ldk, wk, hk, T, eps,
-                      (int)rotary, pa, block);
+    return launch_pdl(k_qk_norm_rope<128>, dim3(grid), dim3(256), 0, st, 1, q, ldq, wq, hq, k, ldk, wk, v, ldv, hk,
+                      kp, vp, T, eps, (int)rotary, pa, block);
   if (hd == 64)
-    return launch_pdl(k_qk_norm_rope<64>, dim3(grid), dim3(256), 0, st, 1, q, ldq, wq, hq, k, ldk, wk, hk, T, eps,
-                      (int)rotary, pa, block);
+    return launch_pdl(k_qk_norm_rope<64>, dim3(grid), dim3(256), 0, st, 1, q, ldq, wq, hq, k, ldk, wk, v, ldv, hk, kp,
+                      vp, T, eps, (int)rotary, pa, block);
   return cudaErrorInvalidValue;
 }
 

@@ -96,10 +96,12 @@ class Drafter:
         w.layers = C.cast(layers, C.POINTER(L.LayerWeights))
         self._weights = w
 
+        # the caches: ctx_cap x kv x hd x 4 bytes each, holding per (position, head)
+        # the f16 planes hi[hd] then lo[hd] of the K/V values (context_kv decodes them)
         kv, hd = g.kv_heads, g.head_dim
-        self.ctx_k = [[torch.zeros(ctx_cap, kv, hd, dtype=torch.float32, device=self.dev) for _ in range(g.layers)]
+        self.ctx_k = [[torch.zeros(ctx_cap, kv, 2, hd, dtype=torch.float16, device=self.dev) for _ in range(g.layers)]
                       for _ in range(max_batch)]
-        self.ctx_v = [[torch.zeros(ctx_cap, kv, hd, dtype=torch.float32, device=self.dev) for _ in range(g.layers)]
+        self.ctx_v = [[torch.zeros(ctx_cap, kv, 2, hd, dtype=torch.float16, device=self.dev) for _ in range(g.layers)]
                       for _ in range(max_batch)]
         ks = [t.data_ptr() for row in self.ctx_k for t in row]
         vs = [t.data_ptr() for row in self.ctx_v for t in row]
@@ -118,6 +120,11 @@ class Drafter:
 
     def context(self, seq: int = 0):
         return L.dflash_context(self.h, seq)
+
+    def context_kv(self, seq: int, layer: int, n: int):
+        """The first n cached K and V rows of (seq, layer) as f32 [n][kv][hd]: hi + lo of the planes."""
+        k, v = self.ctx_k[seq][layer][:n].float(), self.ctx_v[seq][layer][:n].float()
+        return k[:, :, 0] + k[:, :, 1], v[:, :, 0] + v[:, :, 1]
 
     def settle(self, seq: int, pos: int, taps: torch.Tensor):
         """Settle tap rows [n][tw] (device f32) at positions pos.., 1024 rows a call."""

@@ -142,8 +142,7 @@ class Pair:
         assert (f, n) == (o.first, o.len)
         worst = 0.0
         for l in range(self.g.layers):
-            k = self.gpu.ctx_k[seq][l][:n].cpu().numpy()
-            v = self.gpu.ctx_v[seq][l][:n].cpu().numpy()
+            k, v = (t.cpu().numpy() for t in self.gpu.context_kv(seq, l, n))
             worst = max(worst, check_close(f"K layer {l}", k, o.ctx_k[l]), check_close(f"V layer {l}", v, o.ctx_v[l]))
         return worst
 
