@@ -153,12 +153,14 @@ size_t dflash_workspace_bytes(const dflash_geometry *g, int32_t max_batch);
  * (position - first, KV head), in the card arm's `[position - first][kv]`
  * order, the row's f32 values as two f16 planes, hi[head_dim] then
  * lo[head_dim], with hi = x with its low 13 mantissa bits cleared (exact in
- * f16) and lo = f16(x - hi), so that hi + lo carries about 21 bits of x (the
- * form the attention's tensor cores read). Every sequence starts empty at
+ * f16 for 2^-14 <= |x| < 65536; below that range hi + lo is off by at most
+ * 2^-24, at or above it the planes overflow to infinity) and lo = f16(x - hi),
+ * so that hi + lo carries about 21 bits of x (the form the attention's tensor
+ * cores read). Every sequence starts empty at
  * first = 0. Nothing is enqueued. Errors: GEOMETRY, ARG, CAPACITY (workspace),
  * NOMEM. */
 int dflash_create(dflash_t **out, const dflash_geometry *g, const dflash_weights *w,
-                  int32_t max_batch, float *const *ctx_k, float *const *ctx_v, int64_t ctx_cap,
+                  int32_t max_batch, void *const *ctx_k, void *const *ctx_v, int64_t ctx_cap,
                   void *workspace, size_t workspace_bytes);
 
 /* Context of sequence `seq` = empty, starting at position `first`. Host only. */

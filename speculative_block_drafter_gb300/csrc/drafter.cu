@@ -136,7 +136,7 @@ struct dflash_t {
   dflash_weights w;
   std::vector<dflash_layer_weights> layers;
   int max_batch = 0;
-  std::vector<float *> ck, cv;
+  std::vector<__half *> ck, cv;   // context caches, f16 planes [cap][kv][2][hd]
   int64_t cap = 0;
   char *ws = nullptr;
   Carve c{};
@@ -288,7 +288,7 @@ size_t dflash_workspace_bytes(const dflash_geometry *g, int32_t max_batch) {
 }
 
 int dflash_create(dflash_t **out, const dflash_geometry *g, const dflash_weights *w, int32_t max_batch,
-                  float *const *ctx_k, float *const *ctx_v, int64_t ctx_cap, void *workspace,
+                  void *const *ctx_k, void *const *ctx_v, int64_t ctx_cap, void *workspace,
                   size_t workspace_bytes) {
   if (!out || !g || !w) return fail(DFLASH_E_ARG, "create: null argument");
   *out = nullptr;
@@ -322,8 +322,10 @@ int dflash_create(dflash_t **out, const dflash_geometry *g, const dflash_weights
   d->layers.assign(w->layers, w->layers + g->layers);
   d->w.layers = d->layers.data();
   d->max_batch = max_batch;
-  d->ck.assign(ctx_k, ctx_k + (size_t)max_batch * g->layers);
-  d->cv.assign(ctx_v, ctx_v + (size_t)max_batch * g->layers);
+  for (int i = 0; i < max_batch * g->layers; ++i) {
+    d->ck.push_back((__half *)ctx_k[i]);
+    d->cv.push_back((__half *)ctx_v[i]);
+  }
   d->cap = ctx_cap;
   d->ws = (char *)workspace;
   d->c = c;
@@ -411,8 +413,8 @@ int dflash_settle(dflash_t *d, int32_t seq, int64_t pos, const float *taps, int3
     float *yk = d->kvs + (size_t)(2 * l) * DFLASH_SETTLE_MAX * kvd, *yv = yk + (size_t)DFLASH_SETTLE_MAX * kvd;
     sk[l] = yk;
     sv[l] = yv;
-    ckp[l] = (__half *)(d->ck[(size_t)seq * g.layers + l] + at * kvd);
-    cvp[l] = (__half *)(d->cv[(size_t)seq * g.layers + l] + at * kvd);
+    ckp[l] = d->ck[(size_t)seq * g.layers + l] + at * 2 * kvd;
+    cvp[l] = d->cv[(size_t)seq * g.layers + l] + at * 2 * kvd;
     kn[l] = L.k_norm;
     rot[l] = g.no_rope[l] == 0;
     kv[2 * l] = dfl::WideJob{L.k.data, L.k.scales, yk, kvd, kvd, 0};
