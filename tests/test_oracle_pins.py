@@ -94,6 +94,25 @@ def test_f16_matmul_rounds_activations_to_f16():
     assert np.allclose(O.f16_matmul(w, x), ref, rtol=0, atol=1e-12)
 
 
+def test_mlp_closed_form_on_scaled_identities():
+    """gate = 2I, up = I, down = the swap of the first two rows: the output is the
+    swapped vector of silu(2x) * x, with silu(a) = a / (1 + e^-a). Swapping gate and
+    up (silu(x) * 2x), applying silu to up, or reading down transposed each fail."""
+    n = 32
+    eye = np.eye(n, dtype=np.int64)
+    swap = eye.copy()
+    swap[[0, 1]] = swap[[1, 0]]
+    swap[0, 5] = 1                       # down row 0 also reads column 5: not symmetric
+    one = np.ones((n, 1), dtype=np.float16)
+    mat = lambda q, s: di.Int4(codes=_pack(q), scales=s, rows=n, cols=n, group=n)
+    L = {"gate": mat(2 * eye, one), "up": mat(eye, one), "down": mat(swap, np.full((n, 1), 0.5, np.float16))}
+    x = np.linspace(-3.0, 2.5, n)[None, :]
+    m = [2 * v / (1 + math.exp(-2 * v)) * v for v in x[0]]
+    want = [0.5 * m[i] for i in range(n)]
+    want[0], want[1] = 0.5 * (m[1] + m[5]), 0.5 * m[0]
+    assert np.allclose(O.mlp(L, x)[0], want, rtol=1e-13, atol=1e-15)
+
+
 # ------------------------------------------------------------------ norms and rotation
 
 def test_rms_constant_row_closed_form():
