@@ -433,6 +433,24 @@ def test_block_no_rope_layer_is_position_invariant():
     assert not np.allclose(c.block(24, h), d.block(1024, h), rtol=0, atol=1e-6)
 
 
+def test_block_with_zero_output_matrices_is_the_final_norm_of_its_input():
+    """With every layer's o and down matrices zero, both sub-layers add nothing to the
+    residual stream (the stage-1 convolution of a zero signal is zero), so the block
+    returns rms(h, norm) of its input rows; a nonzero o changes that."""
+    g, w = _tiny()
+    zero = lambda m: dataclasses.replace(m, codes=np.full_like(m.codes, 0x88))
+    wz = dict(w, layers=[dict(L, o=zero(L["o"]), down=zero(L["down"])) for L in w["layers"]])
+    o = O.Oracle(g, wz)
+    o.settle(0, di.make_taps(g, 0, 20))
+    h = di.block_rows(g, 0, 5)
+    want = [[hv * wv / math.sqrt(sum(t * t for t in row) / g.hidden + g.eps) for hv, wv in zip(row, w["norm"])]
+            for row in np.asarray(h, dtype=np.float64)]
+    assert np.allclose(o.block(20, h), want, rtol=1e-12, atol=0)
+    full = O.Oracle(g, dict(wz, layers=[dict(L, o=w["layers"][i]["o"]) for i, L in enumerate(wz["layers"])]))
+    full.settle(0, di.make_taps(g, 0, 20))
+    assert not np.allclose(full.block(20, h), want, rtol=1e-6, atol=0)
+
+
 def test_block_with_empty_context():
     g, w = _tiny()
     o = O.Oracle(g, w)
