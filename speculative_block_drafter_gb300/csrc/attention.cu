@@ -545,12 +545,8 @@ static cudaError_t launch_attn(const float *q, const AttnArgs &args, int batch, 
                                int window, float scale, float *part, float *y, int num_sms, const PackDst *pack,
                                const ZeroSet *zero, cudaStream_t st) {
   const size_t smem = AttnRing::BYTES;
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(k_attn<HD, KG>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  static PerDevice configured;
+  if (cudaError_t e = smem_limit(k_attn<HD, KG>, (int)smem, configured)) return e;
   int ns, cps;
   plan_splits(batch * kv, max_n, num_sms, ns, cps);
   // With short splits the block's own rows get a split of their own (the last

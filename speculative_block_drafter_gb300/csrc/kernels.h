@@ -48,6 +48,30 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 
+// One-time set-up of a kernel on each device (its dynamic shared-memory limit,
+// a cached occupancy figure), safe when several host threads launch at once:
+// one slot a device, 0 until set. Declare these `static` (zero-initialised).
+struct PerDevice {
+  std::atomic<int> slot[64];
+};
+// The calling thread's current device, within PerDevice's 64 slots.
+inline cudaError_t device_slot(int &dev) {
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  return dev >= 0 && dev < 64 ? cudaSuccess : cudaErrorInvalidDevice;
+}
+// Raise `kern`'s dynamic shared-memory limit to `bytes`, once per device.
+template <typename KERN>
+cudaError_t smem_limit(KERN kern, int bytes, PerDevice &done) {
+  int dev = 0;
+  cudaError_t e = device_slot(dev);
+  if (e != cudaSuccess) return e;
+  if (done.slot[dev].load(std::memory_order_acquire)) return cudaSuccess;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) done.slot[dev].store(1, std::memory_order_release);
+  return e;
+}
+
 // -------------------------------------------------------------- tensor-core GEMMs (tc_gemm.cu)
 // Packed layouts: four-bit codes in 4 KiB tiles of 128 rows x 64 columns plus
 // per-row f16 scales per 32-or-64-column unit; f16 matrices in 16 KiB tiles of

@@ -271,14 +271,10 @@ cudaError_t select_tokens(const float *logits, const float *hp, const uint32_t *
   int *cnt = (int *)(cands + (size_t)rows * CAND_CAP);
   uint32_t *ctok = (uint32_t *)(cnt + ((rows + 1) & ~1));
   float *score = (float *)(ctok + (size_t)rows * top);
-  static bool configured = false;
+  static PerDevice configured;
   const size_t smem = (size_t)k * top * top * 4 + (size_t)k * top * 4;
-  if (!configured) {
-    const size_t most = (size_t)KMAX * TOP_MAX * TOP_MAX * 4 + (size_t)KMAX * TOP_MAX * 4;
-    cudaError_t e = cudaFuncSetAttribute(k_chain, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)most);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  const size_t most = (size_t)KMAX * TOP_MAX * TOP_MAX * 4 + (size_t)KMAX * TOP_MAX * 4;
+  if (cudaError_t e = smem_limit(k_chain, (int)most, configured)) return e;
   // chunks a CTA so that stages 1 and 2 are about one wave (8 CTAs an SM)
   const int cpb = std::max(1, (int)(((int64_t)nchunks * rows + 8 * num_sms - 1) / (8 * num_sms)));
   const dim3 g12((nchunks + cpb - 1) / cpb, rows);

@@ -740,14 +740,6 @@ static cudaError_t wide_jobs(const TcJob *jobs, int njobs, bool int4, int group,
   return wide_gemm(w, njobs, 0, int4, group, X, ldx, T, K, act, num_sms, st);
 }
 
-template <typename KERN>
-static cudaError_t set_smem(KERN kern, int bytes, bool &done) {
-  if (done) return cudaSuccess;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-  if (e == cudaSuccess) done = true;
-  return e;
-}
-
 // Grid over (token tiles, row tiles of all jobs, k splits): splits fill the
 // GPU, but a CTA keeps at least `kc_min` k-tiles so that its set-up and its
 // output atomics stay small beside its stream.
@@ -810,8 +802,8 @@ template <int TT, int DU, int MT, int SA>
 static cudaError_t launch_int4(const TcJobs &J, int njobs, const void *act, int K, int T, int ntt, int num_sms,
                                cudaStream_t st) {
   using C = I4<TT, DU, MT, SA>;
-  static bool configured = false;
-  cudaError_t e = set_smem(k_tc_int4<TT, DU, MT, SA>, C::SMEM, configured);
+  static PerDevice configured;
+  cudaError_t e = smem_limit(k_tc_int4<TT, DU, MT, SA>, C::SMEM, configured);
   if (e != cudaSuccess) return e;
   I4Items P;
   int grid;
@@ -885,8 +877,8 @@ template <int TT>
 static cudaError_t launch_f16(const TcJobs &J, int mtiles, const void *act, int bstride, int K, int T, int ntt,
                               int num_sms, cudaStream_t st) {
   using C = F16Cfg<TT>;
-  static bool configured = false;
-  cudaError_t e = set_smem(k_tc_f16<TT>, C::SMEM, configured);
+  static PerDevice configured;
+  cudaError_t e = smem_limit(k_tc_f16<TT>, C::SMEM, configured);
   if (e != cudaSuccess) return e;
   int kc, splits;
   plan(ntt, mtiles, K / 64, num_sms, 2, kc, splits);

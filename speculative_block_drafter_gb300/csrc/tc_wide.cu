@@ -530,10 +530,13 @@ constexpr int W_CLUSTER = 2;
 template <int KIND, int DU, int CL>
 static cudaError_t launch_wide(WideArgs &A, const float *X, int ldx, void *act, int num_sms, cudaStream_t st) {
   using C = WCfg<KIND, DU>;
-  static int max_clusters = 0;
+  static PerDevice smem_set, clusters;   // per device: the limit raised; the resident clusters (0 = not yet)
   auto kern = k_wide<KIND, DU, CL>;
+  int dev = 0;
+  if (cudaError_t e = device_slot(dev)) return e;
+  int max_clusters = clusters.slot[dev].load(std::memory_order_acquire);
   if (max_clusters == 0) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    cudaError_t e = smem_limit(kern, C::SMEM, smem_set);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute at[1];
@@ -550,6 +553,7 @@ static cudaError_t launch_wide(WideArgs &A, const float *X, int ldx, void *act, 
     e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
     if (e != cudaSuccess) return e;
     max_clusters = std::max(1, n);
+    clusters.slot[dev].store(max_clusters, std::memory_order_release);
   }
   const int groups = (A.mtiles + CL - 1) / CL;
   A.units = (int64_t)A.ntt * groups * A.KT;
