@@ -169,6 +169,21 @@ def test_rotate_position_zero_identity_norms_and_relative_position():
     assert abs(d0 - d1) < 1e-5 * (np.abs(q).sum() * np.abs(k).sum()) ** 0.5
 
 
+def test_rotate_composes_by_adding_positions():
+    """Rotating by p2 and then by p1 is rotating by p1 + p2, up to the f32 rounding of
+    the angles; rotating by p then by -p returns the input."""
+    rng = np.random.default_rng(21)
+    inv = O.inv_freq(128, 1e6)
+    x = rng.standard_normal((3, 2 * 128))
+    p1, p2 = [5, 300, 4000], [17, 2, 123]
+    twice = O.rotate(O.rotate(x, 2, p2, inv), 2, p1, inv)
+    once = O.rotate(x, 2, [a + b for a, b in zip(p1, p2)], inv)
+    assert np.allclose(twice, once, rtol=0, atol=2e-3 * np.abs(x).max())
+    assert not np.allclose(twice, O.rotate(x, 2, p1, inv), rtol=0, atol=1e-3)
+    back = O.rotate(O.rotate(x, 2, p1, inv), 2, [-p for p in p1], inv)
+    assert np.allclose(back, x, rtol=0, atol=1e-12)
+
+
 # ------------------------------------------------------------------ row convolution
 
 def _base(kn, hs, rng):
