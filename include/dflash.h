@@ -24,6 +24,11 @@
  *    thread-local message in dflash_last_error(). On failure nothing is enqueued
  *    unless the code is DFLASH_E_CUDA (a launch failed after earlier launches).
  *  - The library fails loudly: there is no host fallback of any step.
+ *  - A drafter handle keeps host state (each sequence's settled range, the
+ *    caches' tensor maps): calls on one handle come from one thread at a time.
+ *    Separate handles may be driven from separate threads and devices; the
+ *    one-time set-up of each kernel is done once per device and is safe when
+ *    threads race to it.
  */
 #ifndef DFLASH_H
 #define DFLASH_H
