@@ -175,6 +175,40 @@ struct WCursor {
   }
 };
 
+// Four-bit: the power of two 2^p that row r of the CTA's row tile is scaled by
+// over the run [u, ue): smax * 2^p < 2^12 for the row's largest scale smax in
+// the run, so |q| * s * 2^p < 2^15. The run's DU * (ue - u) scales of the row
+// sit 128 halves apart; they are read eight at a time into separate maxima so
+// that the loads are in flight together.
+template <int CL, int DU>
+__device__ __forceinline__ int run_pow2(const WideArgs &A, int64_t u, int64_t ue, int rank, int r) {
+  const WUnit w0 = wunit<CL>(A, u, rank);
+  const WideJob J = wjob(A, wjob_of(A, w0.mt));
+  const int m = w0.mt - J.tile0;
+  const uint16_t *sc = (const uint16_t *)J.s + ((int64_t)m * A.KT + w0.kt) * DU * 128 + r;
+  const int n = (int)(ue - u) * DU;
+  float mx[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  int i = 0;
+  for (; i + 8 <= n; i += 8) {
+    uint16_t v[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) v[e] = __ldg(sc + (int64_t)(i + e) * 128);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) mx[e] = fmaxf(mx[e], fabsf(__half2float(__ushort_as_half(v[e]))));
+  }
+  for (; i < n; ++i) mx[0] = fmaxf(mx[0], fabsf(__half2float(__ushort_as_half(__ldg(sc + (int64_t)i * 128)))));
+  float smax = 0.f;
+#pragma unroll
+  for (int e = 0; e < 8; ++e) smax = fmaxf(smax, mx[e]);
+  int p = 0;
+  if (smax > 0.f) {
+    int e;
+    frexpf(smax, &e);                  // smax in [2^(e-1), 2^e)
+    p = max(-100, min(100, 12 - e));
+  }
+  return p;
+}
+
 template <int KIND, int DU, int CL>
 __global__ void __launch_bounds__(W_THREADS, 1) k_wide(WideArgs A) {
   using C = WCfg<KIND, DU>;
@@ -231,6 +265,10 @@ __global__ void __launch_bounds__(W_THREADS, 1) k_wide(WideArgs A) {
       cur.load_a<KIND, DU>(A, smem_u32(sm + npre * stage) + b_bytes, full0 + 8 * npre);
     }
   }
+  // Four-bit: the first run's row scaling, from the weights' scales (which do
+  // not depend on the kernels before this one either).
+  int p_next = 0;
+  if (KIND == W_KIND_I4 && warp < 4 && u0 < u1) p_next = run_pow2<CL, DU>(A, u0, wrun_end(A, u0, u1), rank, threadIdx.x);
   pdl_wait();
   if (warp == 0) tmem_alloc(smem_u32(tslot), 512);
   tc_fence_before();
@@ -323,21 +361,11 @@ __global__ void __launch_bounds__(W_THREADS, 1) k_wide(WideArgs A) {
       const WUnit w0 = wunit<CL>(A, u, rank);
       const WideJob J = wjob(A, wjob_of(A, w0.mt));
       const int m = w0.mt - J.tile0;
-      // four-bit: the row's power-of-two scaling for this run
+      // four-bit: the row's power-of-two scaling for this run (found before
+      // the run's first unit, see run_pow2)
       float unscale = 1.f;
       if (KIND == W_KIND_I4) {
-        const uint16_t *sc = (const uint16_t *)J.s + ((int64_t)m * A.KT) * DU * 128 + r;
-        float smax = 0.f;
-        for (int kt = w0.kt; kt < w0.kt + (int)(ue - u); ++kt)
-#pragma unroll
-          for (int du = 0; du < DU; ++du)
-            smax = fmaxf(smax, fabsf(__half2float(__ushort_as_half(sc[((int64_t)kt * DU + du) * 128]))));
-        int p = 0;
-        if (smax > 0.f) {
-          int e;
-          frexpf(smax, &e);          // smax in [2^(e-1), 2^e)
-          p = max(-100, min(100, 12 - e));  // smax * 2^p < 2^12: |q| * s * 2^p < 2^15
-        }
+        const int p = p_next;
         unscale = ldexpf(1.f, -p);
         for (int64_t v = u; v < ue && ok; ++v, ++i) {
           const int s = i % S, a = i % C::SA;
@@ -383,6 +411,8 @@ __global__ void __launch_bounds__(W_THREADS, 1) k_wide(WideArgs A) {
           mbar_arrive(afull0 + 8 * a);
         }
         if (!ok) break;
+        // the next run's scaling while the MMAs finish this run's last units
+        if (ue < u1) p_next = run_pow2<CL, DU>(A, ue, wrun_end(A, ue, u1), rank, r);
       }
       // the run's partial sums into Y
       const int d = run % C::NBUF;
