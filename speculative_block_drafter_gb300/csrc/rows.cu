@@ -214,28 +214,101 @@ struct CtxPlanes {
   float inv[64];
 };
 
-// One warp per (K or V, row, head) of layer blockIdx.y: K normalised and
-// rotated to pos_base + t, both written to the cache as f16 planes.
+// E consecutive floats (one vector load when E == 2).
+template <int E>
+__device__ __forceinline__ void load_e(const float *__restrict__ p, float (&v)[E]) {
+  if constexpr (E == 2) {
+    const float2 a = *(const float2 *)p;
+    v[0] = a.x;
+    v[1] = a.y;
+  } else {
+#pragma unroll
+    for (int j = 0; j < E; ++j) v[j] = p[j];
+  }
+}
+// E consecutive halves (one 4-byte store when E == 2).
+template <int E>
+__device__ __forceinline__ void store_e(__half *p, const __half (&v)[E]) {
+  if constexpr (E == 2) {
+    *(__half2 *)p = __halves2half2(v[0], v[1]);
+  } else {
+#pragma unroll
+    for (int j = 0; j < E; ++j) p[j] = v[j];
+  }
+}
+
+// One warp per (row, head) of layer blockIdx.y: the head's K normalised and
+// rotated to pos_base + t, then its K and V written to the cache as f16 planes
+// (plane_pair). A lane holds E = HD/64 consecutive elements of each half of
+// the head, i = E*lane + j and i + HD/2 (the rotation's pairs), so that its
+// loads and stores are vectors and both rows' loads are in flight together.
 template <int HD>
 __global__ void k_ctx_planes(CtxPlanes P, int T, int heads, float eps, int64_t pos_base) {
   pdl_wait();
+  constexpr int E = HD / 64;
   const int wid = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
-  if (wid >= 2 * T * heads) return;
+  if (wid >= T * heads) return;
   const int l = blockIdx.y;
-  const bool isk = wid < T * heads;
-  const int w2 = isk ? wid : wid - T * heads;
-  const int t = w2 / heads, h = w2 % heads;
-  const float *src = (isk ? P.k[l] : P.v[l]) + ((int64_t)t * heads + h) * HD;
-  constexpr int M = HD / 64;
-  float lo[M], hi[M];
+  const int t = wid / heads;
+  const int64_t off = (int64_t)wid * HD;  // (t * heads + h) * HD
+  const int i0 = E * lane;
+  float k0[E], k1[E], v0[E], v1[E];
+  load_e<E>(P.k[l] + off + i0, k0);
+  load_e<E>(P.k[l] + off + HD / 2 + i0, k1);
+  load_e<E>(P.v[l] + off + i0, v0);
+  load_e<E>(P.v[l] + off + HD / 2 + i0, v1);
+  float w0[E], w1[E];  // the norm's weights: plain loads (the caller's vector is only 4-byte aligned)
 #pragma unroll
-  for (int m = 0; m < M; ++m) {
-    lo[m] = src[lane + 32 * m];
-    hi[m] = src[lane + 32 * m + HD / 2];
+  for (int j = 0; j < E; ++j) {
+    w0[j] = P.w[l][i0 + j];
+    w1[j] = P.w[l][HD / 2 + i0 + j];
   }
-  if (isk) norm_rope_regs<HD>(lo, hi, P.w[l], eps, P.rotary[l] != 0, pos_base + t, P.inv, lane);
-  store_planes<HD>((isk ? P.ck[l] : P.cv[l]) + ((int64_t)t * heads + h) * 2 * HD, lo, hi, lane);
+  // K: the per-head RMS norm, then the rotation
+  float ss = 0.f;
+#pragma unroll
+  for (int j = 0; j < E; ++j) {
+    ss = fmaf(k0[j], k0[j], ss);
+    ss = fmaf(k1[j], k1[j], ss);
+  }
+  ss = warp_sum(ss);
+  const float s = 1.0f / sqrtf(ss / (float)HD + eps);
+#pragma unroll
+  for (int j = 0; j < E; ++j) {
+    k0[j] = k0[j] * s * w0[j];
+    k1[j] = k1[j] * s * w1[j];
+  }
+  if (P.rotary[l]) {
+    const float fp = (float)(pos_base + t);
+#pragma unroll
+    for (int j = 0; j < E; ++j) {
+      const float ang = __fmul_rn(fp, P.inv[i0 + j]);
+      float sn, cs;
+      sincosf(ang, &sn, &cs);
+      const float a = k0[j], b = k1[j];
+      k0[j] = a * cs - b * sn;
+      k1[j] = b * cs + a * sn;
+    }
+  }
+  // planes: dst[i] = hi of element i, dst[HD + i] = lo of element i
+  __half *ck = P.ck[l] + 2 * off, *cv = P.cv[l] + 2 * off;
+  __half h[E], lo[E];
+#pragma unroll
+  for (int j = 0; j < E; ++j) plane_pair(k0[j], h[j], lo[j]);
+  store_e<E>(ck + i0, h);
+  store_e<E>(ck + HD + i0, lo);
+#pragma unroll
+  for (int j = 0; j < E; ++j) plane_pair(k1[j], h[j], lo[j]);
+  store_e<E>(ck + HD / 2 + i0, h);
+  store_e<E>(ck + HD + HD / 2 + i0, lo);
+#pragma unroll
+  for (int j = 0; j < E; ++j) plane_pair(v0[j], h[j], lo[j]);
+  store_e<E>(cv + i0, h);
+  store_e<E>(cv + HD + i0, lo);
+#pragma unroll
+  for (int j = 0; j < E; ++j) plane_pair(v1[j], h[j], lo[j]);
+  store_e<E>(cv + HD / 2 + i0, h);
+  store_e<E>(cv + HD + HD / 2 + i0, lo);
 }
 
 cudaError_t ctx_planes(const float *const *k, const float *const *v, __half *const *ck, __half *const *cv,
@@ -253,7 +326,7 @@ cudaError_t ctx_planes(const float *const *k, const float *const *v, __half *con
     P.rotary[l] = rotary[l];
   }
   for (int i = 0; i < 64; ++i) P.inv[i] = i < hd / 2 ? inv_freq[i] : 0.f;
-  const int warps = 2 * T * heads;
+  const int warps = T * heads;
   dim3 grid((unsigned)((warps * 32 + 255) / 256), nlayers);
   if (hd == 128) return launch_pdl(k_ctx_planes<128>, grid, dim3(256), 0, st, 1, P, T, heads, eps, pos_base);
   if (hd == 64) return launch_pdl(k_ctx_planes<64>, grid, dim3(256), 0, st, 1, P, T, heads, eps, pos_base);
