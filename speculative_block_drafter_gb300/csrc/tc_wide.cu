@@ -587,10 +587,17 @@ static cudaError_t launch_wide(WideArgs &A, const float *X, int ldx, void *act, 
   }
   const int groups = (A.mtiles + CL - 1) / CL;
   A.units = (int64_t)A.ntt * groups * A.KT;
-  const int Q = (int)std::max<int64_t>(1, std::min<int64_t>(max_clusters, A.units / W_MIN_RUN));
+  // With at least 3/4 as many (token tile, row-tile group) tiles as resident
+  // clusters but no more, each cluster takes one tile over its whole k-range:
+  // at most 4/3 the units of an even split, but no split tile (no clearing of
+  // Y, no second read-back, plain stores instead of atomics).
+  const int64_t tiles = (int64_t)A.ntt * groups;
+  const bool whole = tiles <= max_clusters && 4 * tiles >= 3 * (int64_t)max_clusters;
+  const int Q = whole ? (int)tiles
+                      : (int)std::max<int64_t>(1, std::min<int64_t>(max_clusters, A.units / W_MIN_RUN));
   const int64_t chunks = (int64_t)A.ntt * A.KT * A.N * 8;
   const int pack_blocks = (int)((chunks + 255) / 256);
-  const int zero_blocks = (Q - 1) * CL * WZ_PARTS;
+  const int zero_blocks = whole ? 0 : (Q - 1) * CL * WZ_PARTS;
   cudaError_t e = launch_pdl(k_wide_pack<C::PLANES>, dim3(pack_blocks + zero_blocks), dim3(256), 0, st, 1, X, ldx, A, Q,
                              CL, (uint4 *)act, pack_blocks);
   if (e != cudaSuccess) return e;
