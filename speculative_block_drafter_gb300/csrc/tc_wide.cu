@@ -587,12 +587,15 @@ static cudaError_t launch_wide(WideArgs &A, const float *X, int ldx, void *act, 
   }
   const int groups = (A.mtiles + CL - 1) / CL;
   A.units = (int64_t)A.ntt * groups * A.KT;
-  // With at least 3/4 as many (token tile, row-tile group) tiles as resident
-  // clusters but no more, each cluster takes one tile over its whole k-range:
-  // at most 4/3 the units of an even split, but no split tile (no clearing of
-  // Y, no second read-back, plain stores instead of atomics).
+  // With no more (token tile, row-tile group) tiles than resident clusters but
+  // enough of them, each cluster takes one tile over its whole k-range: more
+  // units a cluster than an even split, but no split tile (no clearing of Y,
+  // no second read-back, plain stores instead of atomics). Measured: four-bit
+  // gains from 1/8 of the clusters on (a four-bit unit is three MMAs a
+  // k-step); f16 only from 3/4 on.
   const int64_t tiles = (int64_t)A.ntt * groups;
-  const bool whole = tiles <= max_clusters && 4 * tiles >= 3 * (int64_t)max_clusters;
+  const bool whole = tiles <= max_clusters && (KIND == W_KIND_I4 ? 8 * tiles >= (int64_t)max_clusters
+                                                                  : 4 * tiles >= 3 * (int64_t)max_clusters);
   const int Q = whole ? (int)tiles
                       : (int)std::max<int64_t>(1, std::min<int64_t>(max_clusters, A.units / W_MIN_RUN));
   const int64_t chunks = (int64_t)A.ntt * A.KT * A.N * 8;
