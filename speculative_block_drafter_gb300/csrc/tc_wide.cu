@@ -6,7 +6,9 @@
 // the work is split evenly over the SMs ("stream-K"). The (token tile, row
 // tile, 64-column k-tile) units of all matrices are laid end to end and each
 // CTA takes one contiguous run. Wherever the run crosses a row tile, the CTA
-// adds its partial sums into Y with atomics (Y is cleared first).
+// adds its partial sums into Y with atomics (Y is cleared first). When the
+// tiles about fill the clusters, each cluster takes one whole tile instead
+// (launch_wide), which splits none.
 //
 //   warp 4      bulk-copies each unit's operands into a shared-memory ring
 //   warp 5      issues the MMAs (one thread)
