@@ -173,3 +173,101 @@ def test_gemm_packed_argument_errors_before_any_launch(L):
         with pytest.raises(L.DflashError) as e:
             L.dflash_gemm_packed(m, kind, rows, cols, group, T, y, ws, None)
         assert e.value.code == 2, args
+
+
+def test_select_argument_errors_before_any_launch(L):
+    h, keep = _fake_create(L, max_batch=2)
+    g = keep[0]
+    p = 1 << 24
+    bad = [dict(batch=0), dict(batch=3), dict(k=0), dict(k=g.block), dict(width=g.selector_top - 1),
+           dict(width=g.vocab + 1), dict(logits=0), dict(hp=0), dict(anchor=0), dict(chosen=0), dict(plain=0)]
+    for over in bad:
+        a = dict(batch=1, logits=p, hp=p, anchor=p, k=g.block - 1, width=g.vocab, chosen=p, plain=p)
+        a.update(over)
+        with pytest.raises(L.DflashError) as e:
+            L.dflash_select(h, a["batch"], a["logits"], a["hp"], a["anchor"], a["k"], a["width"], a["chosen"],
+                            a["plain"], None)
+        assert e.value.code == 2, over
+    L.dflash_destroy(h)
+
+
+def test_select_static_argument_and_capacity_errors_before_any_launch(L):
+    """The fixed-scratch selector checks its sizes on the host; a call whose tables pass
+    the 8 MiB array gets CAPACITY before it looks the array up on any device."""
+    p = 1 << 24
+    base = dict(batch=1, k=15, width=151936, vocab=151936, rank=64, top=16)
+    bad = [dict(batch=0), dict(k=0), dict(k=16), dict(top=0), dict(top=33), dict(width=15), dict(width=151937),
+           dict(rank=8), dict(rank=24), dict(rank=272)]
+    for over in bad:
+        a = dict(base, **over)
+        with pytest.raises(L.DflashError) as e:
+            L.dflash_select_static(p, p, p, p, p, a["batch"], a["k"], a["width"], a["vocab"], a["rank"], a["top"],
+                                   p, p, None)
+        assert e.value.code == 2, over
+    for ptr in range(7):
+        ptrs = [p] * 7
+        ptrs[ptr] = 0
+        with pytest.raises(L.DflashError) as e:
+            L.dflash_select_static(ptrs[0], ptrs[1], ptrs[2], ptrs[3], ptrs[4], 1, 15, 151936, 151936, 64, 16,
+                                   ptrs[5], ptrs[6], None)
+        assert e.value.code == 2, ptr
+    # rows * (chunks * 8 + 8200 + top * 4 + top^2 * 4) + 256 bytes against 8 MiB: 56 sequences fit, 64 do not
+    with pytest.raises(L.DflashError) as e:
+        L.dflash_select_static(p, p, p, p, p, 64, 15, 151936, 151936, 64, 16, p, p, None)
+    assert e.value.code == 3
+
+
+def test_pack_and_dequant_argument_errors_before_any_launch(L):
+    p = 1 << 24
+    for rows, cols, group in ((32, 96, 32), (32, 128, 48), (0, 128, 64)):
+        with pytest.raises(L.DflashError) as e:
+            L.dflash_pack_int4(p, p, rows, cols, group, p, p, None)
+        assert e.value.code == 2
+        with pytest.raises(L.DflashError) as e:
+            L.dflash_dequant_int4(p, p, rows, cols, group, p, None)
+        assert e.value.code == 2
+    for args in ((0, p, p, p), (p, 0, p, p), (p, p, 0, p), (p, p, p, 0), (p, p, p + 8, p), (p, p, p, p + 4)):
+        with pytest.raises(L.DflashError) as e:
+            L.dflash_pack_int4(args[0], args[1], 256, 128, 64, args[2], args[3], None)
+        assert e.value.code == 2, args
+    for src, dst in ((0, p), (p, 0), (p, p + 8)):
+        with pytest.raises(L.DflashError) as e:
+            L.dflash_pack_f16(src, 256, 128, dst, None)
+        assert e.value.code == 2
+    with pytest.raises(L.DflashError) as e:
+        L.dflash_pack_f16(p, 256, 100, p, None)
+    assert e.value.code == 2
+    for codes, scales, out in ((0, p, p), (p, 0, p), (p, p, 0), (p + 4, p, p), (p, p + 4, p)):
+        with pytest.raises(L.DflashError) as e:
+            L.dflash_dequant_int4(codes, scales, 256, 128, 64, out, None)
+        assert e.value.code == 2
+
+
+def test_gemm_argument_errors_before_any_launch(L):
+    p = 1 << 24
+    m = L.Matrix(p, p)
+    ws = L.dflash_gemm_workspace_bytes(4, 1024, 16)
+    for kind, rows, cols, group, x, T, y, w, wb, code in (
+            (4, 256, 1024, 64, 0, 16, p, p, ws, 2),          # x null
+            (4, 256, 1024, 64, p, 0, p, p, ws, 2),           # no rows
+            (4, 256, 1024, 64, p + 2, 16, p, p, ws, 2),      # x misaligned
+            (4, 256, 1000, 64, p, 16, p, p, ws, 2),          # cols
+            (7, 256, 1024, 64, p, 16, p, p, ws, 2),          # kind
+            (4, 256, 1024, 64, p, 16, p, 0, ws, 2),          # workspace null
+            (4, 256, 1024, 64, p, 16, p, p + 8, ws, 2),      # workspace misaligned
+            (4, 256, 1024, 64, p, 16, p, p, ws - 16, 3)):    # workspace too small
+        with pytest.raises(L.DflashError) as e:
+            L.dflash_gemm(m, kind, rows, cols, group, x, T, y, w, wb, None)
+        assert e.value.code == code, (kind, rows, cols, x, T, w, wb)
+
+
+def test_context_and_reset_argument_errors(L):
+    h, keep = _fake_create(L, max_batch=1)
+    for seq in (-1, 1):
+        with pytest.raises(L.DflashError):
+            L.dflash_context(h, seq)
+        with pytest.raises(L.DflashError):
+            L.dflash_reset(h, seq, 0)
+    with pytest.raises(L.DflashError):
+        L.dflash_reset(h, 0, -1)
+    L.dflash_destroy(h)
