@@ -44,7 +44,7 @@ def _rank_main(rank, world, port, out):
 
 def test_two_gloo_replicas_report_the_slowest_rank():
     world = 2
-    mgr = mp.Manager()
+    mgr = mp.get_context("spawn").Manager()   # no fork of a multi-threaded process
     out = mgr.dict()
     mp.spawn(_rank_main, args=(world, _free_port(), out), nprocs=world, join=True)
     for r in range(world):
