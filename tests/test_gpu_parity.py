@@ -72,7 +72,10 @@ def _bound(wabs: np.ndarray, x: np.ndarray) -> float:
                                                (96, 1024, 64, 17), (32, 2048, 64, 40), (2048, 5120, 64, 16),
                                                # many tokens: the split-weight kernel, one and two token tiles
                                                (300, 1024, 64, 256), (130, 512, 32, 100), (256, 768, 64, 480),
-                                               (1024, 5120, 64, 256)])
+                                               (1024, 5120, 64, 256),
+                                               # 19 row tiles: 10 tile pairs, each over its whole k-range,
+                                               # the last pair's second CTA past the matrix
+                                               (2432, 1024, 64, 256)])
 def test_gemm_int4_matches_oracle(rows, cols, group, T):
     rng = np.random.default_rng(rows * 7 + T)
     m = _rand_int4(rng, rows, cols, group)
