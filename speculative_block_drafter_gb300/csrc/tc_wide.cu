@@ -7,8 +7,8 @@
 // tile, 64-column k-tile) units of all matrices are laid end to end and each
 // CTA takes one contiguous run. Wherever the run crosses a row tile, the CTA
 // adds its partial sums into Y with atomics (Y is cleared first). When the
-// tiles about fill the clusters, each cluster takes one whole tile instead
-// (launch_wide), which splits none.
+// tiles about fill the resident CTAs, each CTA takes one whole tile instead
+// (launch_wide), which splits none. Every CTA bulk-copies its own operands.
 //
 //   warp 4      bulk-copies each unit's operands into a shared-memory ring
 //   warp 5      issues the MMAs (one thread)
@@ -81,53 +81,21 @@ __device__ __forceinline__ int wjob_of(const WideArgs &A, int mt) {
   return lo;
 }
 
-__device__ __forceinline__ uint32_t cluster_rank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-__device__ __forceinline__ void cluster_sync() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-// Bulk copy into the same offset of the shared memory of every CTA in `mask`,
-// signalling each one's barrier at offset `bar`.
-__device__ __forceinline__ void bulk_g2s_mc(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar,
-                                            uint16_t mask) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster [%0], [%1], %2, [%3], %4;" ::
-          "r"(dst),
-      "l"(src), "r"(bytes), "r"(bar), "h"(mask)
-      : "memory");
-}
-// Arrive on the barrier at offset `bar` of every CTA in `mask` once this thread's MMAs so far are done.
-__device__ __forceinline__ void mma_commit_mc(uint32_t bar, uint16_t mask) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::
-                   "r"(bar),
-               "h"(mask)
-               : "memory");
-}
-
-// A unit: token tile, group of CL row tiles (this CTA's tile = group * CL + rank), k-tile.
+// A unit: token tile, row tile, k-tile.
 struct WUnit {
   int tt, mt, kt;
-  bool ghost;  // past the last row tile: the CTA only helps its cluster load B
 };
-template <int CL>
-__device__ __forceinline__ WUnit wunit(const WideArgs &A, int64_t u, int rank) {
-  const int groups = (A.mtiles + CL - 1) / CL;
-  const int64_t per_tt = (int64_t)groups * A.KT;
+__device__ __forceinline__ WUnit wunit(const WideArgs &A, int64_t u) {
+  const int64_t per_tt = (int64_t)A.mtiles * A.KT;
   WUnit r;
   r.tt = (int)(u / per_tt);
   const int64_t rest = u - (int64_t)r.tt * per_tt;
-  const int g = (int)(rest / A.KT);
-  r.kt = (int)(rest - (int64_t)g * A.KT);
-  r.mt = g * CL + rank;
-  r.ghost = r.mt >= A.mtiles;
-  if (r.ghost) r.mt = A.mtiles - 1;
+  r.mt = (int)(rest / A.KT);
+  r.kt = (int)(rest - (int64_t)r.mt * A.KT);
   return r;
 }
 
-// the end (exclusive) of the run that starts at unit u: the end of its k-range or of the cluster's range
+// the end (exclusive) of the run that starts at unit u: the end of its k-range or of the CTA's range
 __device__ __forceinline__ int64_t wrun_end(const WideArgs &A, int64_t u, int64_t u1) {
   const int64_t tile_end = (u / A.KT + 1) * A.KT;
   return tile_end < u1 ? tile_end : u1;
@@ -135,35 +103,31 @@ __device__ __forceinline__ int64_t wrun_end(const WideArgs &A, int64_t u, int64_
 
 // A walk over consecutive units of one CTA: the token tile, the k-tile and the
 // address of the CTA's weight tile, advanced without divisions.
-template <int CL>
 struct WCursor {
-  int tt, g, kt, groups;
+  int tt, mt, kt;
   int64_t tile0;              // the row tile's first k-tile in its matrix's packed tiles
   const uint8_t *w, *s;       // the matrix's codes (or f16 tiles) and scales
-  __device__ __forceinline__ void locate(const WideArgs &A, int rank) {
-    int mt = g * CL + rank;
-    if (mt >= A.mtiles) mt = A.mtiles - 1;  // a ghost CTA loads a real tile it will not write
+  __device__ __forceinline__ void locate(const WideArgs &A) {
     const WideJob J = wjob(A, wjob_of(A, mt));
     tile0 = (int64_t)(mt - J.tile0) * A.KT;
     w = (const uint8_t *)J.w;
     s = (const uint8_t *)J.s;
   }
-  __device__ __forceinline__ void start(const WideArgs &A, int64_t u, int rank) {
-    groups = (A.mtiles + CL - 1) / CL;
+  __device__ __forceinline__ void start(const WideArgs &A, int64_t u) {
     const int64_t tg = u / A.KT;
     kt = (int)(u - tg * A.KT);
-    g = (int)(tg % groups);
-    tt = (int)(tg / groups);
-    locate(A, rank);
+    mt = (int)(tg % A.mtiles);
+    tt = (int)(tg / A.mtiles);
+    locate(A);
   }
-  __device__ __forceinline__ void next(const WideArgs &A, int rank) {
+  __device__ __forceinline__ void next(const WideArgs &A) {
     if (++kt == A.KT) {
       kt = 0;
-      if (++g == groups) {
-        g = 0;
+      if (++mt == A.mtiles) {
+        mt = 0;
         ++tt;
       }
-      locate(A, rank);
+      locate(A);
     }
   }
   template <int KIND, int DU>
@@ -182,9 +146,9 @@ struct WCursor {
 // the run, so |q| * s * 2^p < 2^15. The run's DU * (ue - u) scales of the row
 // sit 128 halves apart; they are read eight at a time into separate maxima so
 // that the loads are in flight together.
-template <int CL, int DU>
-__device__ __forceinline__ int run_pow2(const WideArgs &A, int64_t u, int64_t ue, int rank, int r) {
-  const WUnit w0 = wunit<CL>(A, u, rank);
+template <int DU>
+__device__ __forceinline__ int run_pow2(const WideArgs &A, int64_t u, int64_t ue, int r) {
+  const WUnit w0 = wunit(A, u);
   const WideJob J = wjob(A, wjob_of(A, w0.mt));
   const int m = w0.mt - J.tile0;
   const uint16_t *sc = (const uint16_t *)J.s + ((int64_t)m * A.KT + w0.kt) * DU * 128 + r;
@@ -211,7 +175,7 @@ __device__ __forceinline__ int run_pow2(const WideArgs &A, int64_t u, int64_t ue
   return p;
 }
 
-template <int KIND, int DU, int CL>
+template <int KIND, int DU>
 __global__ void __launch_bounds__(W_THREADS, 1) k_wide(WideArgs A) {
   using C = WCfg<KIND, DU>;
   constexpr int S = C::STAGES;
@@ -227,19 +191,17 @@ __global__ void __launch_bounds__(W_THREADS, 1) k_wide(WideArgs A) {
   const uint32_t afree0 = afull0 + 8 * C::SA, dfull0 = afree0 + 8 * C::SA, dfree0 = dfull0 + 8 * C::NBUF;
   const uint32_t ebar = dfree0 + 8 * C::NBUF;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int rank = CL > 1 ? (int)cluster_rank() : 0;
-  const uint16_t everyone = (uint16_t)((1u << CL) - 1);
 
-  // this cluster's units
-  const int64_t q = blockIdx.x / CL, Q = gridDim.x / CL;
+  // this CTA's units
+  const int64_t q = blockIdx.x, Q = gridDim.x;
   const int64_t u0 = q * A.units / Q;
   const int64_t u1 = (q + 1) * A.units / Q;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < S; ++i) {
       mbar_init(full0 + 8 * i, 1);
-      // released by every cluster CTA's MMAs (their B) and, four-bit, this CTA's dequantisers (codes)
-      mbar_init(empty0 + 8 * i, KIND == W_KIND_F16 ? CL : CL + 128);
+      // released by the MMAs (B) and, four-bit, the dequantisers (codes)
+      mbar_init(empty0 + 8 * i, KIND == W_KIND_F16 ? 1 : 1 + 128);
     }
     for (int i = 0; i < C::SA; ++i) {
       mbar_init(afull0 + 8 * i, 128);
@@ -253,16 +215,15 @@ __global__ void __launch_bounds__(W_THREADS, 1) k_wide(WideArgs A) {
     mbar_fence_init();
   }
   __syncthreads();
-  if (CL > 1) cluster_sync();  // every barrier of the cluster exists before the first multicast
   // The weights do not depend on the kernels before this one: the first stages'
   // weight tiles are fetched before waiting for them. The producer walks its
   // units with counters (a division per unit would slow the one thread that
   // feeds the pipeline).
-  WCursor<CL> cur;
+  WCursor cur;
   int npre = 0;
   if (warp == W_PRODUCER && lane == 0) {
-    cur.start(A, u0, rank);
-    for (; npre < S && u0 + npre < u1; ++npre, cur.next(A, rank)) {
+    cur.start(A, u0);
+    for (; npre < S && u0 + npre < u1; ++npre, cur.next(A)) {
       mbar_expect_tx(full0 + 8 * npre, b_bytes + C::A_BYTES);
       cur.load_a<KIND, DU>(A, smem_u32(sm + npre * stage) + b_bytes, full0 + 8 * npre);
     }
@@ -270,7 +231,7 @@ __global__ void __launch_bounds__(W_THREADS, 1) k_wide(WideArgs A) {
   // Four-bit: the first run's row scaling, from the weights' scales (which do
   // not depend on the kernels before this one either).
   int p_next = 0;
-  if (KIND == W_KIND_I4 && warp < 4 && u0 < u1) p_next = run_pow2<CL, DU>(A, u0, wrun_end(A, u0, u1), rank, threadIdx.x);
+  if (KIND == W_KIND_I4 && warp < 4 && u0 < u1) p_next = run_pow2<DU>(A, u0, wrun_end(A, u0, u1), threadIdx.x);
   pdl_wait();
   if (warp == 0) tmem_alloc(smem_u32(tslot), 512);
   tc_fence_before();
@@ -280,12 +241,11 @@ __global__ void __launch_bounds__(W_THREADS, 1) k_wide(WideArgs A) {
 
   if (warp == W_PRODUCER) {
     if (lane == 0) {
-      const int slice = b_bytes / CL;
-      WCursor<CL> bc;  // the units' token tiles
-      bc.start(A, u0, rank);
+      WCursor bc;  // the units' token tiles
+      bc.start(A, u0);
       int i = 0;
       bool ok = true;
-      for (int64_t u = u0; u < u1; ++u, ++i, bc.next(A, rank)) {
+      for (int64_t u = u0; u < u1; ++u, ++i, bc.next(A)) {
         const int s = i % S;
         const uint32_t st = smem_u32(sm + s * stage);
         if (i >= npre) {
@@ -295,13 +255,12 @@ __global__ void __launch_bounds__(W_THREADS, 1) k_wide(WideArgs A) {
           }
           mbar_expect_tx(full0 + 8 * s, b_bytes + C::A_BYTES);
           cur.load_a<KIND, DU>(A, st + b_bytes, full0 + 8 * s);
-          cur.next(A, rank);
+          cur.next(A);
         }
         const uint8_t *bp = A.bpack + ((int64_t)bc.tt * A.KT + bc.kt) * b_bytes;
-        if (CL > 1) bulk_g2s_mc(st + rank * slice, bp + rank * slice, slice, full0 + 8 * s, everyone);
-        else bulk_g2s(st, bp, b_bytes, full0 + 8 * s);
+        bulk_g2s(st, bp, b_bytes, full0 + 8 * s);
       }
-      // every stage released by every consumer (no copy or remote arrive still bound for this CTA)
+      // every stage released by every consumer (no copy still bound for this CTA)
       if (ok)
         for (int k = (i > S ? i - S : 0); k < i; ++k)
           if (!mbar_wait(empty0 + 8 * (k % S), (k / S) & 1)) break;
@@ -346,8 +305,7 @@ __global__ void __launch_bounds__(W_THREADS, 1) k_wide(WideArgs A) {
             }
             mma_commit(afree0 + 8 * a);
           }
-          if (CL > 1) mma_commit_mc(empty0 + 8 * s, everyone);
-          else mma_commit(empty0 + 8 * s);
+          mma_commit(empty0 + 8 * s);
         }
         mma_commit(dfull0 + 8 * d);
         u = ue;
@@ -360,7 +318,7 @@ __global__ void __launch_bounds__(W_THREADS, 1) k_wide(WideArgs A) {
     bool ok = true;
     for (int64_t u = u0; u < u1 && ok; ++run) {
       const int64_t ue = wrun_end(A, u, u1);
-      const WUnit w0 = wunit<CL>(A, u, rank);
+      const WUnit w0 = wunit(A, u);
       const WideJob J = wjob(A, wjob_of(A, w0.mt));
       const int m = w0.mt - J.tile0;
       // four-bit: the row's power-of-two scaling for this run (found before
@@ -414,7 +372,7 @@ __global__ void __launch_bounds__(W_THREADS, 1) k_wide(WideArgs A) {
         }
         if (!ok) break;
         // the next run's scaling while the MMAs finish this run's last units
-        if (ue < u1) p_next = run_pow2<CL, DU>(A, ue, wrun_end(A, ue, u1), rank, r);
+        if (ue < u1) p_next = run_pow2<DU>(A, ue, wrun_end(A, ue, u1), r);
       }
       // the run's partial sums into Y
       const int d = run % C::NBUF;
@@ -428,9 +386,7 @@ __global__ void __launch_bounds__(W_THREADS, 1) k_wide(WideArgs A) {
       const int tok0 = w0.tt * N;
       const int ntok = min(N, A.T - tok0);
       const bool bulk = (rows & 3) == 0 && (J.ldy & 3) == 0 && (((uintptr_t)ybase) & 15) == 0;
-      if (w0.ghost) {
-        // nothing to write
-      } else if (bulk) {
+      if (bulk) {
         // 16 tokens at a time: TMEM -> registers -> a [token][row] slice in shared
         // memory; then each warp writes 4 whole token rows, 16 bytes a lane
         // (vector stores, or vector atomic adds for a split tile)
@@ -483,7 +439,6 @@ __global__ void __launch_bounds__(W_THREADS, 1) k_wide(WideArgs A) {
     tc_fence_after();
     tmem_dealloc(tbase, 512);
   }
-  if (CL > 1) cluster_sync();  // no CTA leaves while its peers may still reach its shared memory
 }
 
 // ---------------------------------------------------------------- launch
@@ -502,14 +457,13 @@ size_t wide_act_bytes(int T, int K, bool int4) {
 }
 
 // The token tiles (blocks < pack_blocks) and the clearing of the row tiles
-// that a boundary between two clusters' ranges splits (their runs add into the
+// that a boundary between two CTAs' ranges splits (their runs add into the
 // outputs; runs over a whole k-range store). Clearing block b takes boundary
-// b / (CL * WZ_PARTS), row tile (b / WZ_PARTS) % CL of its group and a part
-// of the tile's token rows.
+// b / WZ_PARTS and a part of that tile's token rows.
 constexpr int WZ_PARTS = 8;
 
 template <int PLANES>
-__global__ void k_wide_pack(const float *__restrict__ X, int ldx, WideArgs A, int Q, int CL, uint4 *__restrict__ dst,
+__global__ void k_wide_pack(const float *__restrict__ X, int ldx, WideArgs A, int Q, uint4 *__restrict__ dst,
                             int pack_blocks) {
   pdl_wait();
   pdl_trigger();
@@ -520,17 +474,14 @@ __global__ void k_wide_pack(const float *__restrict__ X, int ldx, WideArgs A, in
     return;
   }
   const int zb = blockIdx.x - pack_blocks;
-  const int part = zb % WZ_PARTS, c = (zb / WZ_PARTS) % CL, q = zb / (WZ_PARTS * CL) + 1;
+  const int part = zb % WZ_PARTS, q = zb / WZ_PARTS + 1;
   const int64_t u = (int64_t)q * A.units / Q;
   if (u % A.KT == 0) return;
-  // the tile group was cleared for the boundary before if that one split it too
+  // the tile was cleared for the boundary before if that one split it too
   const int64_t up = (int64_t)(q - 1) * A.units / Q;
   if (q > 1 && up % A.KT != 0 && up / A.KT == u / A.KT) return;
-  const int groups = (A.mtiles + CL - 1) / CL;
   const int64_t tg = u / A.KT;
-  const int tt = (int)(tg / groups), g = (int)(tg % groups);
-  const int mt = g * CL + c;
-  if (mt >= A.mtiles) return;
+  const int tt = (int)(tg / A.mtiles), mt = (int)(tg % A.mtiles);
   int lo = 0, hi = A.njobs - 1;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
@@ -556,57 +507,42 @@ __global__ void k_wide_pack(const float *__restrict__ X, int ldx, WideArgs A, in
 
 // Runs of at least this many units: a run ends with a read-back of its accumulator.
 constexpr int W_MIN_RUN = 4;
-// CTAs sharing each token tile (multicast).
-constexpr int W_CLUSTER = 2;
 
-template <int KIND, int DU, int CL>
+template <int KIND, int DU>
 static cudaError_t launch_wide(WideArgs &A, const float *X, int ldx, void *act, int num_sms, cudaStream_t st) {
   using C = WCfg<KIND, DU>;
-  static PerDevice smem_set, clusters;   // per device: the limit raised; the resident clusters (0 = not yet)
-  auto kern = k_wide<KIND, DU, CL>;
+  static PerDevice smem_set, resident;   // per device: the limit raised; the resident CTAs (0 = not yet)
+  auto kern = k_wide<KIND, DU>;
   int dev = 0;
   if (cudaError_t e = device_slot(dev)) return e;
-  int max_clusters = clusters.slot[dev].load(std::memory_order_acquire);
-  if (max_clusters == 0) {
+  int max_ctas = resident.slot[dev].load(std::memory_order_acquire);
+  if (max_ctas == 0) {
     cudaError_t e = smem_limit(kern, C::SMEM, smem_set);
     if (e != cudaSuccess) return e;
-    cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute at[1];
-    at[0].id = cudaLaunchAttributeClusterDimension;
-    at[0].val.clusterDim.x = CL;
-    at[0].val.clusterDim.y = 1;
-    at[0].val.clusterDim.z = 1;
-    cfg.gridDim = dim3(CL * num_sms);
-    cfg.blockDim = dim3(W_THREADS);
-    cfg.dynamicSmemBytes = C::SMEM;
-    cfg.attrs = at;
-    cfg.numAttrs = 1;
-    int n = 0;
-    e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
+    int per_sm = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, W_THREADS, C::SMEM);
     if (e != cudaSuccess) return e;
-    max_clusters = std::max(1, n);
-    clusters.slot[dev].store(max_clusters, std::memory_order_release);
+    max_ctas = std::max(1, per_sm) * num_sms;
+    resident.slot[dev].store(max_ctas, std::memory_order_release);
   }
-  const int groups = (A.mtiles + CL - 1) / CL;
-  A.units = (int64_t)A.ntt * groups * A.KT;
-  // With no more (token tile, row-tile group) tiles than resident clusters but
-  // enough of them, each cluster takes one tile over its whole k-range: more
-  // units a cluster than an even split, but no split tile (no clearing of Y,
-  // no second read-back, plain stores instead of atomics). Measured: four-bit
-  // gains from 1/8 of the clusters on (a four-bit unit is three MMAs a
-  // k-step); f16 only from 3/4 on.
-  const int64_t tiles = (int64_t)A.ntt * groups;
-  const bool whole = tiles <= max_clusters && (KIND == W_KIND_I4 ? 8 * tiles >= (int64_t)max_clusters
-                                                                  : 4 * tiles >= 3 * (int64_t)max_clusters);
-  const int Q = whole ? (int)tiles
-                      : (int)std::max<int64_t>(1, std::min<int64_t>(max_clusters, A.units / W_MIN_RUN));
+  A.units = (int64_t)A.ntt * A.mtiles * A.KT;
+  // With no more (token tile, row tile) tiles than resident CTAs but enough of
+  // them, each CTA takes one tile over its whole k-range: more units a CTA
+  // than an even split, but no split tile (no clearing of Y, no second
+  // read-back, plain stores instead of atomics). Measured: four-bit gains from
+  // 1/8 of the resident CTAs on (a four-bit unit is three MMAs a k-step); f16
+  // only from 3/4 on.
+  const int64_t tiles = (int64_t)A.ntt * A.mtiles;
+  const bool whole = tiles <= max_ctas && (KIND == W_KIND_I4 ? 8 * tiles >= (int64_t)max_ctas
+                                                              : 4 * tiles >= 3 * (int64_t)max_ctas);
+  const int Q = whole ? (int)tiles : (int)std::max<int64_t>(1, std::min<int64_t>(max_ctas, A.units / W_MIN_RUN));
   const int64_t chunks = (int64_t)A.ntt * A.KT * A.N * 8;
   const int pack_blocks = (int)((chunks + 255) / 256);
-  const int zero_blocks = whole ? 0 : (Q - 1) * CL * WZ_PARTS;
+  const int zero_blocks = whole ? 0 : (Q - 1) * WZ_PARTS;
   cudaError_t e = launch_pdl(k_wide_pack<C::PLANES>, dim3(pack_blocks + zero_blocks), dim3(256), 0, st, 1, X, ldx, A, Q,
-                             CL, (uint4 *)act, pack_blocks);
+                             (uint4 *)act, pack_blocks);
   if (e != cudaSuccess) return e;
-  return launch_pdl(kern, dim3((unsigned)(Q * CL)), dim3(W_THREADS), C::SMEM, st, CL, A);
+  return launch_pdl(kern, dim3((unsigned)Q), dim3(W_THREADS), C::SMEM, st, 1, A);
 }
 
 cudaError_t wide_gemm(const WideJob *jobs, int njobs, int64_t y_off, bool int4, int group, const float *X, int ldx,
@@ -626,9 +562,9 @@ cudaError_t wide_gemm(const WideJob *jobs, int njobs, int64_t y_off, bool int4, 
   A.KT = K / 64;
   A.T = T;
   wide_tiles(T, A.ntt, A.N);
-  if (!int4) return launch_wide<W_KIND_F16, 1, W_CLUSTER>(A, X, ldx, act, num_sms, st);
-  return group >= 64 ? launch_wide<W_KIND_I4, 1, W_CLUSTER>(A, X, ldx, act, num_sms, st)
-                     : launch_wide<W_KIND_I4, 2, W_CLUSTER>(A, X, ldx, act, num_sms, st);
+  if (!int4) return launch_wide<W_KIND_F16, 1>(A, X, ldx, act, num_sms, st);
+  return group >= 64 ? launch_wide<W_KIND_I4, 1>(A, X, ldx, act, num_sms, st)
+                     : launch_wide<W_KIND_I4, 2>(A, X, ldx, act, num_sms, st);
 }
 
 // This file's device error word (a bounded wait that gave up).
