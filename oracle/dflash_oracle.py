@@ -32,9 +32,13 @@ embeddings). Readings fixed where the pages leave a step open:
 
 Parity pins: every function here is pinned by a ``-m "not gpu"`` test against
 a closed form, the page's worked example, a brute-force evaluation or an
-invariant (tests/test_oracle_pins.py). The end-to-end composition (``block``,
-``settle``) is pinned only through its parts and the invariants listed there;
-no printed end-to-end value exists on the pages.
+invariant (tests/test_oracle_pins.py). The composition is pinned too: the
+block rows the head and the selector's projection read (a closed form on
+one-hot matrices), the settle's order (a closed form: the norm after the fc,
+the key norm before the rotation), which kernel each stage-1 convolution uses
+(linearity in its signal and which projection rows reach it), and the
+checker's scores against ``select_with``. No printed end-to-end value exists
+on the pages, so the whole pass is otherwise pinned through these parts.
 """
 from __future__ import annotations
 

@@ -506,3 +506,169 @@ def test_inputs_are_seeded():
     g = di.workload("tiny").geometry
     assert np.array_equal(di.make_taps(g, 3, 70)[64:], di.make_taps(g, 3, 6, start=64))
     assert not np.array_equal(di.make_taps(g, 3, 4), di.make_taps(g, 4, 4))
+
+
+# ------------------------------------------------------------------ composition of the pass
+# The primitives above are pinned on their own; these pin how the pass wires
+# them: which block rows reach the head, the order of the settle's steps and
+# which convolution kernel each residual add uses.
+
+def _one_hot_int4(rows: int, cols: int, group: int, col_of, scale: float) -> "di.Int4":
+    """A four-bit matrix with the single code +1 at (r, col_of(r)) of every row, scale `scale`."""
+    q = np.zeros((rows, cols), dtype=np.int64)
+    for r in range(rows):
+        q[r, col_of(r)] = 1
+    scales = np.full((rows, cols // group), scale, dtype=np.float16)
+    return di.Int4(codes=_pack(q), scales=scales, rows=rows, cols=cols, group=group)
+
+
+def test_head_and_selector_read_block_rows_one_to_k():
+    """gpu dflash.rs ``Dev::block``: the head and the selector's projection take the
+    final-normed rows 1..=k of the block (the anchor row 0 gets no logits), the head
+    over its first ``width`` rows. With a head whose row v is the unit vector e_v and
+    distinct rows hn[r][c] = 100 r + c, logit[j][v] must be hn[j + 1][v]."""
+    g, w = _tiny()
+    hs = g.hidden
+    hn = np.array([[100.0 * r + c for c in range(hs)] for r in range(g.block)])
+    rows = 48
+    head = _one_hot_int4(rows, hs, g.quant_group, lambda r: r, 1.0)
+    sel = np.zeros((g.selector_rank, hs), dtype=np.float16)
+    for i in range(g.selector_rank):
+        sel[i, 3 * i] = 1.0                      # hp[j][i] = f16(hn[j + 1][3 i]): exact integers < 2048
+    o = O.Oracle(g, dict(w, head=head, sel=sel))
+    for k, width in ((g.block - 1, rows), (4, 17)):
+        lg = o.head_logits(hn, k, width)
+        assert lg.shape == (k, width)
+        assert np.array_equal(lg, [[100.0 * (j + 1) + v for v in range(width)] for j in range(k)])
+        hp = o.selector_projection(hn, k)
+        assert np.array_equal(hp, [[100.0 * (j + 1) + 3 * i for i in range(g.selector_rank)] for j in range(k)])
+
+
+def test_settle_rows_closed_form_norm_then_rotation():
+    """dflash.rs ``Drafter::settle_rows`` / gpu dflash.rs ``Dev::settle`` on matrices with a
+    closed form: fc the identity on the first tap, so t = rms(f16(tap0), hidden_norm) (the
+    norm after the fc, over its hidden outputs); Wk and Wv single codes, so k = s_k t and
+    v = s_v t on the first kv_heads*head_dim channels; K = the head's RMS norm times k_norm
+    (non-uniform), THEN the half-split rotation to pos + r. Normalising after the rotation,
+    or norming the raw taps, or leaving out hidden_norm, each breaks an equality here."""
+    g, w = _tiny()
+    hs, hd, kvd, tw = g.hidden, g.head_dim, g.kv_heads * g.head_dim, g.tap_width
+    fc = np.zeros((hs, tw), dtype=np.float16)
+    fc[np.arange(hs), np.arange(hs)] = 1.0
+    hidden_norm = (1.0 + np.arange(hs) / 64.0).astype(np.float32)
+    L = dict(w["layers"][0])
+    L["k_norm"] = (0.5 + np.arange(hd) / 16.0).astype(np.float32)
+    L["k"] = _one_hot_int4(kvd, hs, g.quant_group, lambda r: r, 0.5)
+    L["v"] = _one_hot_int4(kvd, hs, g.quant_group, lambda r: (r + 7) % hs, 0.25)
+    o = O.Oracle(g, dict(w, fc=fc, hidden_norm=hidden_norm, layers=[L]))
+    n, pos = 5, 37
+    taps = di.make_taps(g, 4, n)
+    _, kv = o.settle_rows(pos, taps)
+    K, V = kv[0]
+    eps = g.eps
+    inv = [np.float32(g.rope_theta ** (-(2.0 * i) / hd)) for i in range(hd // 2)]
+    for r in range(n):
+        t0 = [float(np.float16(x)) for x in taps[r, :hs]]
+        s = 1.0 / math.sqrt(sum(x * x for x in t0) / hs + eps)
+        t = [t0[i] * s * float(hidden_norm[i]) for i in range(hs)]
+        for h in range(g.kv_heads):
+            for i in range(hd):
+                assert abs(V[r, h, i] - 0.25 * t[(h * hd + i + 7) % hs]) <= 1e-12 * abs(t[(h * hd + i + 7) % hs]) + 1e-15
+            k = [0.5 * t[h * hd + i] for i in range(hd)]
+            sk = 1.0 / math.sqrt(sum(x * x for x in k) / hd + eps)
+            kn = [k[i] * sk * float(L["k_norm"][i]) for i in range(hd)]
+            for i in range(hd // 2):
+                ang = float(np.float32(np.float32(pos + r) * inv[i]))
+                c, sn = math.cos(ang), math.sin(ang)
+                a, b = kn[i], kn[i + hd // 2]
+                assert abs(K[r, h, i] - (a * c - b * sn)) <= 1e-12
+                assert abs(K[r, h, i + hd // 2] - (b * c + a * sn)) <= 1e-12
+
+
+def _scaled(m, factor: float):
+    """The same codes with every scale multiplied by a power of two (exact in f16)."""
+    return dataclasses.replace(m, scales=(m.scales.astype(np.float32) * factor).astype(np.float16))
+
+
+def _layer_delta(g, w, layers):
+    """The residual stream's change over the (single) layer: h after the layer minus h before."""
+    o = O.Oracle(g, dict(w, layers=layers))
+    o.settle(0, di.make_taps(g, 0, 20))
+    h = di.block_rows(g, 0, 5)
+    tr = {}
+    o.block(20, h, tr)
+    return tr["layers"][0]["h"] - np.asarray(h, np.float64), tr["layers"][0]
+
+
+def test_attention_conv_out_uses_the_stage0_kernel_and_is_linear_in_o():
+    """dflash.rs ``Drafter::block``: the attention's stage-1 convolution (conv_out) applies the
+    kernel d computed from the sub-layer's input x (conv_in's d), not one computed from its
+    own signal o. So with the MLP silenced (down = 0), doubling Wo doubles the residual
+    change exactly, and changing only the stage-1 rows of attn_proj leaves q, k, v, y and
+    o untouched while the residual change moves."""
+    g, w = _tiny()
+    zero = lambda m: dataclasses.replace(m, codes=np.full_like(m.codes, 0x88))
+    L = dict(w["layers"][0], down=zero(w["layers"][0]["down"]))
+    d1, t1 = _layer_delta(g, w, [L])
+    d2, _ = _layer_delta(g, w, [dict(L, o=_scaled(L["o"], 2.0))])
+    assert np.abs(d1).max() > 1e-3
+    assert np.allclose(d2, 2.0 * d1, rtol=1e-12, atol=1e-12)
+    stage1 = g.conv_kernel * g.groups                      # rows [stage 1][offset][group] of the projection
+    ap = L["attn_proj"].copy()
+    ap[stage1:] = (ap[stage1:].astype(np.float32) * 2.0).astype(np.float16)
+    d3, t3 = _layer_delta(g, w, [dict(L, attn_proj=ap)])
+    for name in ("x", "xc", "q", "k", "v", "y", "o"):
+        assert np.array_equal(t1[name], t3[name]), name
+    assert not np.allclose(d3, d1, rtol=1e-6, atol=0)
+
+
+def test_mlp_conv_out_uses_the_mlp_kernel_not_the_attention_one():
+    """dflash.rs ``Drafter::block``: the MLP's stage-1 convolution reuses md, the kernel of the
+    MLP's own stage-0 input, not the attention's ad. With the attention silenced (o = 0), the
+    stage-1 rows of attn_proj reach nothing; those of mlp_proj do; and doubling down doubles
+    the residual change."""
+    g, w = _tiny()
+    zero = lambda m: dataclasses.replace(m, codes=np.full_like(m.codes, 0x88))
+    L = dict(w["layers"][0], o=zero(w["layers"][0]["o"]))
+    stage1 = g.conv_kernel * g.groups
+    d1, t1 = _layer_delta(g, w, [L])
+    assert np.abs(d1).max() > 1e-3
+    ap = L["attn_proj"].copy()
+    ap[stage1:] = 0
+    d2, _ = _layer_delta(g, w, [dict(L, attn_proj=ap)])
+    assert np.array_equal(d2, d1)
+    mp = L["mlp_proj"].copy()
+    mp[stage1:] = 0
+    d3, t3 = _layer_delta(g, w, [dict(L, mlp_proj=mp)])
+    assert np.array_equal(t1["dn"], t3["dn"]) and not np.allclose(d3, d1, rtol=1e-6, atol=0)
+    d4, _ = _layer_delta(g, w, [dict(L, down=_scaled(L["down"], 2.0))])
+    assert np.allclose(d4, 2.0 * d1, rtol=1e-12, atol=1e-12)
+
+
+def test_select_scores_agree_with_select_with():
+    """The per-candidate scores the token checker uses (``select_scores``) give, row by row
+    along select_with's own chain, the token select_with chose (first strictly greater
+    score in candidate order), and each score is the brute-force sum
+    logit + sum_i P[prev][i] hp[i] C[cand][i]."""
+    rng = np.random.default_rng(11)
+    V, rank, top, k = 50, 4, 6, 7
+    for trial in range(20):
+        logits = rng.standard_normal((k, V))
+        if trial % 4 == 0:
+            logits[:, 3] = logits[:, 9] = logits.max() + 1.0          # an exact tie at the top
+        hp = rng.standard_normal((k, rank))
+        P = rng.standard_normal((V, rank)).astype(np.float16)
+        Cb = rng.standard_normal((V, rank)).astype(np.float16)
+        anchor = int(rng.integers(0, V))
+        chosen, plain = O.select_with(hp, logits, anchor, P, Cb, top)
+        prevs = [anchor] + chosen[:-1]
+        scores = O.select_scores(hp, logits, prevs, P, Cb, top)
+        for j in range(k):
+            best_t, best_s = None, -np.inf
+            for tok, s in scores[j]:
+                want = logits[j, tok] + sum(float(P[prevs[j], i]) * hp[j, i] * float(Cb[tok, i]) for i in range(rank))
+                assert abs(s - want) <= 1e-12 * max(1.0, abs(want))
+                if s > best_s:
+                    best_t, best_s = tok, s
+            assert best_t == chosen[j]
+            assert scores[j][0][0] == plain[j]
