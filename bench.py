@@ -2,18 +2,28 @@
 """Throughput of the DFlash 2 drafter pass on GB300.
 
 One step = one pass of the whole hot path over one batch of synthetic input:
-reset, settle of the workload's context (1024-row calls), the block, and the
-selector (for the batched workload the contexts are settled once before the
-timed region and a step is one block per sequence plus the selector).
+reset, settle of the workload's context in 256-row calls (the settle chunk of
+the pages' CUDA arm), the block, and the selector. For the batched workload
+the 32 contexts are settled once before the timed region and a step is one
+block per sequence plus the selector.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl gb300|reference]
 
+The default workload is settle-heavy (the 27B-shaped drafter settling 32,768
+positions, then one block at that context), the largest single-GPU one.
 Prints one JSON line (rank 0). Under torchrun every rank runs its own replica
 on its own GPU (no data-path collective); the value is the sum over ranks.
+
+Roofline: the block pass (every kernel of one block, replayed from a CUDA
+graph, the L2 flushed before each replay) against the measured HBM copy peak,
+with the algorithmic bytes of the block (every weight once, the K/V rows the
+windows admit); the settle at 256-row calls against the sustained tensor peak
+and the HBM peak; the head GEMM kernel alone as a sub-entry.
 """
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import json
 import os
 import subprocess
@@ -30,7 +40,8 @@ if ROOT not in sys.path:
 import dflash_inputs as di  # noqa: E402
 
 METRIC = "DFlash2 draft blocks/s and settle rows/s on 1 GB300; % of HBM roofline"
-DEFAULT_WORKLOAD = "qwen3-0.6b"
+DEFAULT_WORKLOAD = "settle-heavy"
+SETTLE_CHUNK = 256          # rows a settle call in the step (gpu_cuda/hyb/dflash.rs, SETTLE_MAX)
 L2_FLUSH_BYTES = 256 << 20
 REJECT = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown")
 
@@ -38,8 +49,8 @@ REJECT = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown")
 def parse(argv=None):
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=100)
-    p.add_argument("--warmup", type=int, default=10)
+    p.add_argument("--steps", type=int, default=50)
+    p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(di.WORKLOADS))
     p.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     p.add_argument("--no-graph", action="store_true", help="direct calls instead of a CUDA graph replay")
@@ -48,12 +59,63 @@ def parse(argv=None):
 
 
 def peaks():
+    """(HBM GB/s, bf16 TFLOP/s burst, bf16 TFLOP/s sustained, kind)."""
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
             m = json.load(f)
-        return float(m["hbm_gbs"]), float(m["bf16_tflops"]), "measured"
+        return float(m["hbm_gbs"]), float(m["bf16_tflops"]), float(m["bf16_tflops_sustained"]), "measured"
     except Exception:
-        return 6800.0, 1900.0, "fallback"
+        return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+# ------------------------------------------------------------------ algorithmic bytes and flops
+
+def int4_bytes(rows: int, cols: int, group: int) -> int:
+    """Codes (half a byte a weight) and f16 scales of a four-bit matrix."""
+    return rows * cols // 2 + rows * (cols // group) * 2
+
+
+def context_rows(g, context: int, anchor: int) -> list:
+    """Context rows each layer's block reads (dflash.rs ``Drafter::block``'s range, first = 0)."""
+    out = []
+    for l in range(g.layers):
+        hi = min(anchor, context)
+        lo = 0 if g.windows[l] == 0 else min(max(anchor + 1 - g.windows[l], 0), hi)
+        out.append(hi - lo)
+    return out
+
+
+def block_cost(g, width: int, ctx_rows: list, batch: int):
+    """Algorithmic bytes and flops of one block step of `batch` sequences: every weight once
+    (the layers' four-bit and f16 matrices, the head's first `width` rows, the selector's
+    projection), each sequence's admitted K/V rows (4 bytes an element), and the selector's
+    codebook rows; flops: two a weight per token row plus the attention's products."""
+    hs, R, k = g.hidden, g.block, g.block - 1
+    kvd = g.kv_heads * g.head_dim
+    layer = sum(int4_bytes(r, c, g.quant_group) for r, c in di.weight_shapes(g).values())
+    proj = 2 * g.proj_rows * hs * 2
+    head = int4_bytes(width, hs, g.quant_group)
+    sel = g.selector_rank * hs * 2 + batch * k * g.selector_top * 2 * g.selector_rank * 2
+    kv = batch * sum(ctx_rows) * kvd * 4 * 2
+    nbytes = g.layers * (layer + proj) + head + sel + kv
+    params = sum(r * c for r, c in di.weight_shapes(g).values()) + 2 * g.proj_rows * hs
+    flops = 2.0 * batch * R * g.layers * params + 2.0 * batch * k * (width + g.selector_rank) * hs
+    flops += sum(4.0 * batch * R * g.heads * g.head_dim * (n + R) for n in ctx_rows)
+    parts = {"layer_weights": g.layers * layer, "kernel_projections": g.layers * proj, "head": head,
+             "selector": sel, "kv": kv}
+    return nbytes, flops, parts
+
+
+def settle_cost_per_row(g, chunk: int):
+    """Algorithmic bytes and flops of one settled row in calls of `chunk` rows: the fc and every
+    layer's Wk, Wv once a call, the row's taps in (f32) and its K/V out (4 bytes an element)."""
+    hs, tw = g.hidden, g.tap_width
+    kvd = g.kv_heads * g.head_dim
+    fc = hs * tw * 2
+    kvw = g.layers * 2 * int4_bytes(kvd, hs, g.quant_group)
+    nbytes = (fc + kvw) / chunk + tw * 4 + g.layers * 2 * kvd * 4
+    flops = 2.0 * (hs * tw + g.layers * 2 * kvd * hs)
+    return nbytes, flops
 
 
 # ------------------------------------------------------------------ clocks
@@ -110,7 +172,8 @@ class Clocks:
                     reasons.add(n)
         loaded = [s for s, p in zip(sm, power) if p > 0.3 * max(power)] if power else []
         return {"sm_mhz": float(np.median(loaded or sm)) if sm else None,
-                "sm_max_mhz": max(smax) if smax else None, "reasons": sorted(reasons), "samples": len(sm)}
+                "sm_max_mhz": max(smax) if smax else None, "reasons": sorted(reasons), "samples": len(sm),
+                "samples_under_load": len(loaded)}
 
 
 def max_over_ranks(x: float, device=None) -> float:
@@ -149,6 +212,28 @@ def head_traffic(workload: str):
         return None
 
 
+def block_traffic(workload: str):
+    """DRAM bytes of one block pass (every kernel of it) from the committed ncu capture, or
+    None when there is none for this workload or any kernel source changed since."""
+    import hashlib
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            doc = json.load(f)
+        entry = doc.get(f"block@{workload}")
+        if not entry:
+            return None
+        h = hashlib.sha256()
+        csrc = os.path.join(ROOT, "speculative_block_drafter_gb300", "csrc")
+        for s in sorted(os.listdir(csrc)):
+            with open(os.path.join(csrc, s), "rb") as f:
+                h.update(f.read())
+        if h.hexdigest()[:16] != entry.get("sources_sha256_16"):
+            return None
+        return int(entry["bytes"])
+    except (OSError, ValueError, KeyError):
+        return None
+
+
 # ------------------------------------------------------------------ the GB300 arm
 class Bench:
     def __init__(self, wl, device):
@@ -179,19 +264,25 @@ class Bench:
         self.flush_buf = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
         self.settle_in_step = wl.batch == 1
         if not self.settle_in_step:
-            self._settle_all()
+            self.settle_all(SETTLE_CHUNK)
         self.head = PackedMatrix(self.w["head"], device=str(device))
 
-    def _settle_all(self):
+    def settle_all(self, chunk):
         for s in range(self.wl.batch):
             self.d.reset(s, 0)
-            self.d.settle(s, 0, self.taps[s])
+            self.d.settle(s, 0, self.taps[s], chunk=chunk)
+
+    def block(self):
+        self.d.block(self.anchors, self.h, self.k, self.width, out=(self.logits, self.hp))
+
+    def select(self):
+        self.d.select(self.logits, self.hp, self.at, out=(self.chosen, self.plain))
 
     def step(self):
         if self.settle_in_step:
-            self._settle_all()
-        self.d.block(self.anchors, self.h, self.k, self.width, out=(self.logits, self.hp))
-        self.d.select(self.logits, self.hp, self.at, out=(self.chosen, self.plain))
+            self.settle_all(SETTLE_CHUNK)
+        self.block()
+        self.select()
 
     def flush(self):
         self.flush_buf.zero_()
@@ -210,32 +301,36 @@ class Bench:
         torch.cuda.synchronize()
         return [a.elapsed_time(b) for a, b in evs]
 
-    def capture(self):
+    def capture(self, fn):
+        """(CUDA graph of `fn`, the library's launches in one call of it); the graph is None
+        where capture fails (then `fn` is timed by direct calls)."""
         torch = self.torch
         c0 = self.L.dflash_launch_count()
-        self.step()
+        fn()
         torch.cuda.synchronize()
-        per_step = self.L.dflash_launch_count() - c0
+        launches = self.L.dflash_launch_count() - c0
         try:
             graph = torch.cuda.CUDAGraph()
             s = torch.cuda.Stream()
             s.wait_stream(torch.cuda.current_stream())
             with torch.cuda.stream(s):
                 with torch.cuda.graph(graph, stream=s):
-                    self.step()
+                    fn()
             torch.cuda.current_stream().wait_stream(s)
             torch.cuda.synchronize()
-            return graph, per_step
+            graph.replay()
+            torch.cuda.synchronize()
+            return graph, launches
         except Exception as e:  # capture unsupported: time direct calls
             sys.stderr.write(f"graph capture failed ({e}); timing direct calls\n")
-            return None, per_step
+            return None, launches
 
-    def roofline(self, steps, hbm_peak, tc_peak):
-        """The head GEMM (the int4 weight-streaming kernel at its largest shape), timed alone: up
-        to 32 rows the GEMM kernel on token tiles packed once (as the block's producers pack
-        them), against the HBM peak; more rows the packing and the wide kernel, which is
-        bound by its f16 tensor-core products (three MMAs per product for the exact int4 and
-        f32 operands), against the tensor peak with one product's 2 flops counted."""
+    def head_roofline(self, steps, hbm_peak, tc_peak):
+        """The head GEMM (the four-bit weight-streaming kernel at its largest shape), timed alone:
+        up to 32 rows the GEMM kernel on token tiles packed once (as the block's producers pack
+        them), against the HBM peak; more rows the packing and the wide kernel, bound by its
+        f16 tensor-core products (three MMAs a product for the exact four-bit and f32
+        operands), against the tensor peak with one product's 2 flops counted."""
         torch = self.torch
         g = self.g
         x = torch.randn(self.wl.batch * self.k, g.hidden, device=self.dev, dtype=torch.float32)
@@ -249,9 +344,7 @@ class Bench:
             name = "k_wide<int4> + packing (head, %d x %d, %d rows)"
         t = float(np.mean(ms)) * 1e-3
         rows = self.width
-        nbytes = (rows * g.hidden // 2 + rows * (g.hidden // g.quant_group) * 2
-                  + x.numel() * 4 + x.shape[0] * rows * 4)
-        traffic = head_traffic(self.wl.name)
+        nbytes = int4_bytes(rows, g.hidden, g.quant_group) + x.numel() * 4 + x.shape[0] * rows * 4
         out = {"kernel": name % (rows, g.hidden, x.shape[0])}
         if x.shape[0] <= 32:
             achieved = nbytes / t / 1e9
@@ -262,90 +355,69 @@ class Bench:
             achieved = flops / t / 1e12
             out.update(bound="tensor", achieved=round(achieved, 1), peak=tc_peak, unit="TFLOP/s",
                        frac=round(achieved / tc_peak, 4), algorithmic_flops=int(flops))
-        out.update(traffic=traffic, algorithmic_bytes=int(nbytes), ms_per_launch=round(t * 1e3, 5))
+        out.update(traffic=head_traffic(self.wl.name), algorithmic_bytes=int(nbytes), ms_per_launch=round(t * 1e3, 5))
         return out
 
-    def phases(self, steps):
-        torch = self.torch
-        out = {}
-        if self.settle_in_step:
-            ms = self.timed(self._settle_all, steps)
-            out["settle_rows_per_s"] = self.wl.context * self.wl.batch / (np.mean(ms) * 1e-3)
-            out["settle_ms"] = float(np.mean(ms))
-        ms = self.timed(lambda: self.d.block(self.anchors, self.h, self.k, self.width, out=(self.logits, self.hp)),
-                        steps)
-        out["block_ms"] = float(np.mean(ms))
-        out["blocks_per_s_block_only"] = self.wl.batch / (np.mean(ms) * 1e-3)
-        ms = self.timed(lambda: self.d.select(self.logits, self.hp, self.at, out=(self.chosen, self.plain)), steps)
-        out["select_ms"] = float(np.mean(ms))
-        return {k: (round(v, 4) if isinstance(v, float) else v) for k, v in out.items()}
 
-    def e2e(self, steps):
-        """Through the public API from pinned host memory: inputs in, tokens out, every step."""
-        torch = self.torch
-        taps_pin = [torch.from_numpy(t).pin_memory() for t in self.taps_host]
-        h_pin = torch.from_numpy(self.h_host).pin_memory()
-        at_pin = torch.tensor(self.anchor_tok, dtype=torch.int32).pin_memory()
-        out_pin = torch.empty(self.wl.batch, self.k, dtype=torch.int32).pin_memory()
-        taps_dev = [torch.empty_like(t, device=self.dev) for t in taps_pin]
-        h_dev = torch.empty_like(h_pin, device=self.dev)
-        at_dev = torch.empty_like(at_pin, device=self.dev)
-        h2d = (sum(t.numel() * 4 for t in taps_pin) if self.settle_in_step else 0) + h_pin.numel() * 4 + at_pin.numel() * 4
-        d2h = out_pin.numel() * 4
-
-        def one():
-            if self.settle_in_step:
-                for s in range(self.wl.batch):
-                    taps_dev[s].copy_(taps_pin[s], non_blocking=True)
-                    self.d.reset(s, 0)
-                    self.d.settle(s, 0, taps_dev[s])
-            h_dev.copy_(h_pin, non_blocking=True)
-            at_dev.copy_(at_pin, non_blocking=True)
-            self.d.block(self.anchors, h_dev, self.k, self.width, out=(self.logits, self.hp))
-            self.d.select(self.logits, self.hp, at_dev, out=(self.chosen, self.plain))
-            out_pin.copy_(self.chosen, non_blocking=True)
-            torch.cuda.current_stream().synchronize()
-
-        one()
-        times = []
-        for _ in range(steps):
-            self.flush()
-            torch.cuda.synchronize()
-            t0 = time.perf_counter()
-            one()
-            times.append(time.perf_counter() - t0)
-        return float(np.mean(times)), h2d, d2h
-
-
-def cpu_baseline(wl):
-    """The oracle as it stands on this host's cores, on a bounded sample of the workload."""
+def cpu_sample(wl, w=None, rounds=1):
+    """The oracle as it stands, timed on this host's cores on a bounded sample of one step of the
+    workload, scaled to the whole step. Returns (seconds a step, description, threads)."""
     from oracle import dflash_oracle as O
     g = wl.geometry
-    w = di.make_weights(g, wl.seed)
-    orc = O.Oracle(g, w)
+    w = di.make_weights(g, wl.seed) if w is None else w
+    big = g.hidden >= 4096
+    n_settle = min(wl.context, 16 if big else 256)         # settled rows sampled
+    n_layers = 1 if big else g.layers                      # block layers sampled (a sub-model of layer 0)
+    head_part = 32 if big else 1                           # 1 / the head rows sampled
+    sub_g = dataclasses.replace(g, layers=n_layers, windows=g.windows[:n_layers],
+                                no_rope=tuple(l for l in g.no_rope if l < n_layers))
+    sub_w = dict(w, layers=w["layers"][:n_layers])
+    taps = di.make_taps(g, wl.seed, n_settle)
     a = di.anchor_token(g, wl.seed)
     h = di.block_rows(g, wl.seed, a)
-    chunk = min(wl.context, 256)
-    taps = di.make_taps(g, wl.seed, chunk)
-    t0 = time.perf_counter()
-    orc.settle(0, taps)
-    t_chunk = time.perf_counter() - t0
-    # the block over a context of `chunk` rows stands in for the full context's (the
-    # context's attention is a small part of the oracle's block time)
-    t0 = time.perf_counter()
-    orc.draft(chunk, h, a)
-    t_block = time.perf_counter() - t0
-    nchunks = (wl.context + 255) // 256 if wl.batch == 1 else 0
-    step = nchunks * t_chunk + t_block * wl.batch
+    width = wl.head_width // head_part
+    times = []
+    for _ in range(rounds):
+        full = O.Oracle(g, w)
+        t0 = time.perf_counter()
+        full.settle(0, taps)
+        t_settle = time.perf_counter() - t0
+        sub = O.Oracle(sub_g, sub_w)
+        # the sub-model's context: the sampled rows repeated up to the workload's context (the
+        # block's cost does not depend on the cached values)
+        reps = -(-wl.context // n_settle)
+        for l in range(n_layers):
+            sub.ctx_k[l] = np.tile(full.ctx_k[l], (reps, 1, 1))[:wl.context]
+            sub.ctx_v[l] = np.tile(full.ctx_v[l], (reps, 1, 1))[:wl.context]
+        sub.len = wl.context
+        t0 = time.perf_counter()
+        hn = sub.block(wl.context, h)
+        t1 = time.perf_counter()
+        lg = O.int4_matmul(w["head"], hn[1:g.block], 0, width)
+        t2 = time.perf_counter()
+        hp = sub.selector_projection(hn, g.block - 1)
+        sub.select(hp, lg, a)
+        t3 = time.perf_counter()
+        settles = (wl.context / n_settle) if wl.batch == 1 else 0.0
+        step = (settles * t_settle + wl.batch * ((t1 - t0) * g.layers / n_layers
+                                                 + (t2 - t1) * head_part + (t3 - t2)))
+        times.append(step)
+    desc = (f"per step: the oracle's settle of {n_settle} tap rows scaled to {wl.context if wl.batch == 1 else 0} "
+            f"settled rows; a block of {n_layers} of the {g.layers} layers (layer 0's weights, its context the "
+            f"sampled rows repeated to {wl.context} positions) scaled by {g.layers}/{n_layers}; the head over "
+            f"{width} of {wl.head_width} rows scaled by {head_part}; the selector; times {wl.batch} sequence(s)")
     threads = os.cpu_count()
     try:
         from threadpoolctl import threadpool_info
         threads = max([i.get("num_threads", 0) for i in threadpool_info()] + [1])
     except Exception:
         pass
-    sample = (f"one {chunk}-row settle chunk ({t_chunk:.2f} s) and one block + selector over {chunk} context rows "
-              f"({t_block:.2f} s), scaled to {nchunks} chunks + {wl.batch} block(s) per step")
-    return {"value": wl.batch / step, "unit": "blocks/s", "cores": threads, "kind": "oracle", "sample": sample}
+    return times, desc, threads
+
+
+def cpu_baseline(wl, w):
+    times, desc, threads = cpu_sample(wl, w)
+    return {"value": wl.batch / times[0], "unit": "blocks/s", "cores": threads, "kind": "oracle", "sample": desc}
 
 
 def run_gb300(args):
@@ -367,19 +439,20 @@ def run_gb300(args):
     _lib.lib()
     dev = torch.device("cuda", torch.cuda.current_device())
     wl = di.workload(args.workload)
-    hbm_peak, tc_peak, peak_kind = peaks()
+    g = wl.geometry
+    hbm_peak, tc_burst, tc_sust, peak_kind = peaks()
     b = Bench(wl, dev)
     for _ in range(args.warmup):
         b.step()
     torch.cuda.synchronize()
-    graph, launches = (None, None)
     if args.no_graph:
+        graph = None
         c0 = _lib.dflash_launch_count()
         b.step()
         torch.cuda.synchronize()
         launches = _lib.dflash_launch_count() - c0
     else:
-        graph, launches = b.capture()
+        graph, launches = b.capture(b.step)
         for _ in range(2):
             graph.replay() if graph is not None else b.step()
         torch.cuda.synchronize()
@@ -403,75 +476,136 @@ def run_gb300(args):
         clocks["remeasured"] = True
     step_ms = max_over_ranks(float(np.mean(ms)), dev)
     value = whole_job_rate(wl.batch, world, step_ms * 1e-3)
-    roof = b.roofline(max(5, min(args.steps, 50)), hbm_peak, tc_peak)
-    what = "HBM copy" if roof["bound"] == "hbm" else "cuBLAS bf16 burst; f16 MMAs run at the bf16 rate"
-    roof["peak_kind"] = f"{peak_kind} ({what}, MEASURED_PEAKS.json)" if peak_kind == "measured" else "fallback"
-    phases = b.phases(max(5, min(args.steps, 50)))
-    e2e_s, h2d, d2h = b.e2e(max(3, min(args.steps, 30)))
+    reps = max(5, min(args.steps, 50))
+
+    # phases, each replayed from its own graph (L2 flushed before each replay)
+    phases = {}
+    if b.settle_in_step:
+        for chunk, key in ((SETTLE_CHUNK, ""), (1024, "_1024")):
+            gr, n_l = b.capture(lambda: b.settle_all(chunk))
+            t = float(np.mean(b.timed(lambda: b.settle_all(chunk), reps, gr))) * 1e-3
+            phases["settle%s_ms" % key] = round(t * 1e3, 4)
+            phases["settle%s_rows_per_s" % key] = round(wl.context * wl.batch / t, 1)
+            phases["settle%s_launches" % key] = int(n_l)
+    gb, n_block = b.capture(b.block)
+    block_s = float(np.mean(b.timed(b.block, reps, gb))) * 1e-3
+    gs, n_sel = b.capture(b.select)
+    sel_s = float(np.mean(b.timed(b.select, reps, gs))) * 1e-3
+    phases.update(block_ms=round(block_s * 1e3, 4), block_launches=int(n_block),
+                  blocks_per_s_block_only=round(wl.batch / block_s, 2), select_ms=round(sel_s * 1e3, 4),
+                  select_launches=int(n_sel))
+
+    ctx = context_rows(g, wl.context, wl.context)
+    bbytes, bflops, parts = block_cost(g, wl.head_width, ctx, wl.batch)
+    achieved = bbytes / block_s / 1e9
+    roof = {
+        "what": "block pass: every kernel of one block (%d launches) replayed from a CUDA graph, the L2 "
+                "flushed before each replay; bytes = every weight once + the admitted K/V rows" % n_block,
+        "bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
+        "frac": round(achieved / hbm_peak, 4), "traffic": block_traffic(wl.name),
+        "algorithmic_bytes": int(bbytes), "bytes_parts": {k: int(v) for k, v in parts.items()},
+        "ms_per_launch": round(block_s * 1e3, 5),
+        "peak_kind": f"{peak_kind} (HBM copy, MEASURED_PEAKS.json)" if peak_kind == "measured" else "fallback",
+        "tensor_frac": round(bflops / block_s / 1e12 / tc_sust, 4),
+    }
+    if b.settle_in_step:
+        rps = phases["settle_rows_per_s"]
+        sb, sf = settle_cost_per_row(g, SETTLE_CHUNK)
+        roof["settle"] = {
+            "what": f"settle in {SETTLE_CHUNK}-row calls (fc GEMM, norm, every layer's K/V GEMM, key norm and "
+                    "rotation, cache write), replayed from a CUDA graph",
+            "bound": "tensor" if sf / (tc_sust * 1e12) > sb / (hbm_peak * 1e9) else "hbm",
+            "rows_per_s": rps, "flops_per_row": int(sf), "bytes_per_row": int(sb),
+            "achieved_tflops": round(rps * sf / 1e12, 1), "peak_tflops": tc_sust,
+            "frac_tensor": round(rps * sf / 1e12 / tc_sust, 4),
+            "achieved_gbs": round(rps * sb / 1e9, 1), "frac_hbm": round(rps * sb / 1e9 / hbm_peak, 4),
+            "peak_kind": "measured sustained bf16 (f16 MMAs run at the bf16 rate) and HBM copy",
+        }
+    roof["head_gemm"] = b.head_roofline(reps, hbm_peak, tc_burst)
+
+    e2e_s, h2d, d2h = e2e(b, max(3, min(args.steps, 10)))
     e2e_value = whole_job_rate(wl.batch, world, max_over_ranks(e2e_s, dev))
     out = {
-        "metric": METRIC, "value": round(value, 2), "unit": "blocks/s", "n_gpus": world, "steps": args.steps,
+        "metric": METRIC, "value": round(value, 3), "unit": "blocks/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(step_ms, 5), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {"workload": wl.name, "description": wl.description, "context": wl.context, "batch": wl.batch,
-                   "block": wl.geometry.block, "head_width": wl.head_width,
-                   "step": ("reset + settle(%d rows) + block + select" % wl.context) if b.settle_in_step
-                   else "one block per sequence + select (contexts settled before)",
+                   "block": g.block, "head_width": wl.head_width,
+                   "step": ("reset + settle(%d rows in %d-row calls) + block + select" % (wl.context, SETTLE_CHUNK))
+                   if b.settle_in_step else "one block per sequence + select (contexts settled before)",
                    "l2": "flushed between steps (256 MiB write)", "graph": graph is not None,
                    "parallelism": "replicas" if world > 1 else "single"},
+        "settle_rows_per_s": phases.get("settle_rows_per_s"),
         "roofline": roof,
         "phases": phases,
-        "e2e": {"value": round(e2e_value, 2), "unit": "blocks/s", "h2d_bytes_per_step": int(h2d),
+        "e2e": {"value": round(e2e_value, 3), "unit": "blocks/s", "h2d_bytes_per_step": int(h2d),
                 "d2h_bytes_per_step": int(d2h)},
         "gpu_launches": int(launches) * args.steps if launches is not None else None,
         "clocks": clocks,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        out["cpu_baseline"] = cpu_baseline(wl)
+        out["cpu_baseline"] = cpu_baseline(wl, b.w)
     if rank == 0:
         print(json.dumps(out), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()
 
 
+def e2e(b, steps):
+    """Through the public API from pinned host memory: inputs in, tokens out, every step."""
+    torch = b.torch
+    wl = b.wl
+    taps_pin = [torch.from_numpy(t).pin_memory() for t in b.taps_host] if b.settle_in_step else []
+    h_pin = torch.from_numpy(b.h_host).pin_memory()
+    at_pin = torch.tensor(b.anchor_tok, dtype=torch.int32).pin_memory()
+    out_pin = torch.empty(wl.batch, b.k, dtype=torch.int32).pin_memory()
+    taps_dev = [torch.empty_like(t, device=b.dev) for t in taps_pin]
+    h_dev = torch.empty_like(h_pin, device=b.dev)
+    at_dev = torch.empty_like(at_pin, device=b.dev)
+    h2d = sum(t.numel() * 4 for t in taps_pin) + h_pin.numel() * 4 + at_pin.numel() * 4
+    d2h = out_pin.numel() * 4
+
+    def one():
+        for s in range(len(taps_pin)):
+            taps_dev[s].copy_(taps_pin[s], non_blocking=True)
+            b.d.reset(s, 0)
+            b.d.settle(s, 0, taps_dev[s], chunk=SETTLE_CHUNK)
+        h_dev.copy_(h_pin, non_blocking=True)
+        at_dev.copy_(at_pin, non_blocking=True)
+        b.d.block(b.anchors, h_dev, b.k, b.width, out=(b.logits, b.hp))
+        b.d.select(b.logits, b.hp, at_dev, out=(b.chosen, b.plain))
+        out_pin.copy_(b.chosen, non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+
+    one()
+    times = []
+    for _ in range(steps):
+        b.flush()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        one()
+        times.append(time.perf_counter() - t0)
+    return float(np.mean(times)), h2d, d2h
+
+
 def run_reference(args):
-    """The oracle as it stands, timed on the host cores on the same workload and unit."""
+    """The oracle as it stands, timed on the host cores on bounded samples of the same workload."""
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
     wl = di.workload(args.workload)
-    from oracle import dflash_oracle as O
-    g = wl.geometry
-    w = di.make_weights(g, wl.seed)
-    a = di.anchor_token(g, wl.seed)
-    h = di.block_rows(g, wl.seed, a)
-    chunk = min(wl.context, 256)
-    taps = di.make_taps(g, wl.seed, chunk)
-    nchunks = (wl.context + 255) // 256 if wl.batch == 1 else 0
-
-    def sample():
-        orc = O.Oracle(g, w)
-        t0 = time.perf_counter()
-        orc.settle(0, taps)
-        t1 = time.perf_counter()
-        orc.draft(chunk, h, a)
-        t2 = time.perf_counter()
-        return nchunks * (t1 - t0) + wl.batch * (t2 - t1)
-
+    w = di.make_weights(wl.geometry, wl.seed)
     for _ in range(args.warmup):
-        sample()
-    times = [sample() for _ in range(args.steps)]
+        cpu_sample(wl, w)
+    times, desc, threads = cpu_sample(wl, w, rounds=args.steps)
     step = float(np.mean(times))
     value = wl.batch / step
-    threads = os.cpu_count()
-    s = (f"per step: one {chunk}-row settle chunk scaled to {nchunks} chunks and {wl.batch} block(s) + selector "
-         f"over {chunk} context rows")
     print(json.dumps({
         "impl": "reference", "metric": METRIC, "value": value, "unit": "blocks/s", "n_gpus": 1, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": step * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": wl.name, "description": wl.description, "context": wl.context, "batch": wl.batch},
-        "cpu_baseline": {"value": value, "unit": "blocks/s", "cores": threads, "kind": "oracle", "sample": s},
+        "cpu_baseline": {"value": value, "unit": "blocks/s", "cores": threads, "kind": "oracle", "sample": desc},
         "e2e": {"value": value, "unit": "blocks/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }), flush=True)
 

@@ -139,9 +139,12 @@ int dflash_gemm(const dflash_matrix *w, int32_t kind, int64_t rows, int64_t cols
 int dflash_gemm_packed(const dflash_matrix *w, int32_t kind, int64_t rows, int64_t cols, int32_t group, int32_t T,
                        float *y, const void *workspace, void *stream);
 
-/* The library's device error word: bit 0 is set when one of its kernels gave
- * up a bounded wait (the kernel then stopped early and its outputs are not to
- * be trusted). Reads it (synchronising the device) and clears it if `reset`. */
+/* The library's device error word: bit 0 (value 1) is set when one of its
+ * kernels gave up a bounded wait (the kernel then stopped early and its outputs
+ * are not to be trusted); bit 1 (value 2) when a settle or a block wrote a K or
+ * V value that is not finite or at least 65,536 in magnitude, beyond the range
+ * of the cache's hi plane (that element then reads as infinity). Reads the word
+ * (synchronising the device) and clears it if `reset`. */
 int dflash_device_error(uint32_t *error, int32_t reset);
 
 /* ---- the drafter ----------------------------------------------------------- */
@@ -161,7 +164,8 @@ size_t dflash_workspace_bytes(const dflash_geometry *g, int32_t max_batch);
  * f16 for 2^-14 <= |x| < 65536; below that range hi + lo is off by at most
  * 2^-24, at or above it the planes overflow to infinity) and lo = f16(x - hi),
  * so that hi + lo carries about 21 bits of x (the form the attention's tensor
- * cores read). Every sequence starts empty at
+ * cores read); a value out of that range sets bit 1 of the device error word
+ * (dflash_device_error). Every sequence starts empty at
  * first = 0. Nothing is enqueued. Errors: GEOMETRY, ARG, CAPACITY (workspace),
  * NOMEM. */
 int dflash_create(dflash_t **out, const dflash_geometry *g, const dflash_weights *w,
@@ -218,7 +222,7 @@ int dflash_select(dflash_t *d, int32_t batch, const float *logits, const float *
  * (cudaGetSymbolAddress); make that first call before any stream capture.
  * Every call on a device shares the one array, so calls that overlap on the
  * GPU (other streams, other threads) race; serialise them. The one part that
- * must start at zero (a per-sequence counter) is cleared by each call itself;
+ * must start at zero (a per-row candidate counter) is cleared by each call itself;
  * everything else a call reads it wrote itself.
  * It calls no cudaMalloc, cudaFree or allocating library routine.
  * Errors: ARG, CAPACITY, CUDA. */

@@ -1,8 +1,8 @@
 """Time one of the drafter's kernels alone through the C ABI (for tuning and profiling).
 
-    python -m speculative_block_drafter_gb300.microbench gemm --rows 151936 --cols 1024 --tokens 15 --kind 4
-    python -m speculative_block_drafter_gb300.microbench gemm --rows 5120 --cols 25600 --tokens 256 --kind 16
-    python -m speculative_block_drafter_gb300.microbench block --workload batched --batch 8
+    python microbench.py gemm --rows 151936 --cols 1024 --tokens 15 --kind 4
+    python microbench.py gemm --rows 5120 --cols 25600 --tokens 256 --kind 16
+    python microbench.py block --workload batched --batch 8
 
 gemm: random codes / values of the given shape; the L2 cache is flushed
 between launches; prints the mean time and the algorithmic bandwidth of one
@@ -17,13 +17,19 @@ from __future__ import annotations
 
 import argparse
 import json
+import os
+import sys
 
 import numpy as np
 import torch
 
-import dflash_inputs as di
-from . import build
-from .drafter import PackedMatrix
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import dflash_inputs as di  # noqa: E402
+from speculative_block_drafter_gb300 import build  # noqa: E402
+from speculative_block_drafter_gb300.drafter import Drafter, PackedMatrix  # noqa: E402
 
 
 def _int4(rows, cols, group, seed=0):
@@ -66,7 +72,6 @@ def gemm(args):
 def block(args):
     import dataclasses
     build.build()
-    from .drafter import Drafter
     wl = di.workload(args.workload)
     if args.batch:
         wl = dataclasses.replace(wl, batch=args.batch)

@@ -6,6 +6,10 @@
 
 namespace dfl {
 
+// Bits of the library's device error word (dflash_device_error).
+constexpr unsigned DFL_ERR_TIMEOUT = 1u;  // a kernel gave up a bounded wait
+constexpr unsigned DFL_ERR_RANGE = 2u;    // a K/V value out of the cache planes' range
+
 // ---------------------------------------------------------------- programmatic dependent launch
 // Every kernel of the pass is launched so that it may start while the kernel
 // before it in the stream finishes (launch_pdl). Such a kernel calls pdl_wait()

@@ -147,11 +147,12 @@ cudaError_t tc_gemm_int4_packed(const TcJob *jobs, int njobs, int group, const v
 cudaError_t tc_gemm_f16_packed(const TcJob *jobs, int njobs, const void *act, int bstride, int T, int K, int num_sms,
                                cudaStream_t st);
 
-// The device error word (a bounded wait that gave up sets bit 0): the union of
-// the words of the files whose kernels wait on mbarriers.
+// The device error word (DFL_ERR_* bits, common.cuh): the union of the words of
+// the files whose kernels wait on mbarriers or write the cache planes.
 cudaError_t read_device_error(unsigned *out, bool reset);
 cudaError_t wide_read_error(unsigned *out, bool reset);
 cudaError_t attn_read_error(unsigned *out, bool reset);
+cudaError_t rows_read_error(unsigned *out, bool reset);
 
 // -------------------------------------------------------------- row kernels (rows.cu)
 // out[map(t)] = x[t] * rsqrt(mean(x[t]^2) + eps) * w for rows t < T. If

@@ -183,27 +183,39 @@ __device__ __forceinline__ void norm_rope_head(float *__restrict__ p, const floa
   }
 }
 
+// This file's device error word: DFL_ERR_RANGE when a K or V value written to
+// a cache's planes was not finite or at least 65,536 in magnitude (its hi
+// plane then holds infinity).
+static __device__ unsigned int g_rows_error = 0;
+
 // A head row as f16 planes (the attention's K/V format): hi[i] = f16 of x with
-// its low 13 mantissa bits cleared (exact), lo[i] = f16(x - that); hi + lo
-// carries about 21 bits of x. dst holds hi[0..HD) then lo[0..HD).
-__device__ __forceinline__ void plane_pair(float x, __half &h, __half &l) {
+// its low 13 mantissa bits cleared (exact below 65,536 in magnitude), lo[i] =
+// f16(x - that); hi + lo carries about 21 bits of x. dst holds hi[0..HD) then
+// lo[0..HD). `bad` is set where x is out of the planes' range.
+__device__ __forceinline__ void plane_pair(float x, __half &h, __half &l, bool &bad) {
   const float t = __uint_as_float(__float_as_uint(x) & 0xFFFFE000u);
   h = __float2half_rn(t);
   l = __float2half_rn(x - t);
+  bad |= !(fabsf(x) < 65536.f);
+}
+__device__ __forceinline__ void flag_range(bool bad) {
+  if (bad) atomicOr(&g_rows_error, DFL_ERR_RANGE);
 }
 template <int HD>
 __device__ __forceinline__ void store_planes(__half *__restrict__ dst, const float (&lo)[HD / 64],
                                              const float (&hi)[HD / 64], int lane) {
+  bool bad = false;
 #pragma unroll
   for (int m = 0; m < HD / 64; ++m) {
     __half h, l;
-    plane_pair(lo[m], h, l);
+    plane_pair(lo[m], h, l, bad);
     dst[lane + 32 * m] = h;
     dst[HD + lane + 32 * m] = l;
-    plane_pair(hi[m], h, l);
+    plane_pair(hi[m], h, l, bad);
     dst[lane + 32 * m + HD / 2] = h;
     dst[HD + lane + 32 * m + HD / 2] = l;
   }
+  flag_range(bad);
 }
 
 struct CtxPlanes {
@@ -293,22 +305,24 @@ __global__ void k_ctx_planes(CtxPlanes P, int T, int heads, float eps, int64_t p
   // planes: dst[i] = hi of element i, dst[HD + i] = lo of element i
   __half *ck = P.ck[l] + 2 * off, *cv = P.cv[l] + 2 * off;
   __half h[E], lo[E];
+  bool bad = false;
 #pragma unroll
-  for (int j = 0; j < E; ++j) plane_pair(k0[j], h[j], lo[j]);
+  for (int j = 0; j < E; ++j) plane_pair(k0[j], h[j], lo[j], bad);
   store_e<E>(ck + i0, h);
   store_e<E>(ck + HD + i0, lo);
 #pragma unroll
-  for (int j = 0; j < E; ++j) plane_pair(k1[j], h[j], lo[j]);
+  for (int j = 0; j < E; ++j) plane_pair(k1[j], h[j], lo[j], bad);
   store_e<E>(ck + HD / 2 + i0, h);
   store_e<E>(ck + HD + HD / 2 + i0, lo);
 #pragma unroll
-  for (int j = 0; j < E; ++j) plane_pair(v0[j], h[j], lo[j]);
+  for (int j = 0; j < E; ++j) plane_pair(v0[j], h[j], lo[j], bad);
   store_e<E>(cv + i0, h);
   store_e<E>(cv + HD + i0, lo);
 #pragma unroll
-  for (int j = 0; j < E; ++j) plane_pair(v1[j], h[j], lo[j]);
+  for (int j = 0; j < E; ++j) plane_pair(v1[j], h[j], lo[j], bad);
   store_e<E>(cv + HD / 2 + i0, h);
   store_e<E>(cv + HD + HD / 2 + i0, lo);
+  flag_range(bad);
 }
 
 cudaError_t ctx_planes(const float *const *k, const float *const *v, __half *const *ck, __half *const *cv,
@@ -604,6 +618,16 @@ cudaError_t qk_norm_rope(float *q, int ldq, const float *wq, int hq, const float
     return launch_pdl(k_qk_norm_rope<64>, dim3(grid), dim3(256), 0, st, 1, q, ldq, wq, hq, k, ldk, wk, v, ldv, hk, kp,
                       vp, T, eps, (int)rotary, pa, block);
   return cudaErrorInvalidValue;
+}
+
+// This file's device error word (a value out of the cache planes' range).
+cudaError_t rows_read_error(unsigned *out, bool reset) {
+  cudaError_t e = cudaMemcpyFromSymbol(out, g_rows_error, sizeof(unsigned));
+  if (e == cudaSuccess && reset) {
+    const unsigned zero = 0;
+    e = cudaMemcpyToSymbol(g_rows_error, &zero, sizeof(unsigned));
+  }
+  return e;
 }
 
 }  // namespace dfl

@@ -9,7 +9,6 @@
 
 namespace dfl {
 
-constexpr unsigned DFL_ERR_TIMEOUT = 1u;
 // The device error word of the translation unit that includes this header;
 // read_device_error() returns the union of all of them.
 static __device__ unsigned int g_dev_error = 0;

@@ -921,11 +921,12 @@ static cudaError_t gemm_read_error(unsigned *out, bool reset) {
 }
 
 cudaError_t read_device_error(unsigned *out, bool reset) {
-  unsigned a = 0, b = 0, c = 0;
+  unsigned a = 0, b = 0, c = 0, r = 0;
   cudaError_t e = gemm_read_error(&a, reset);
   if (e == cudaSuccess) e = wide_read_error(&b, reset);
   if (e == cudaSuccess) e = attn_read_error(&c, reset);
-  *out = a | b | c;
+  if (e == cudaSuccess) e = rows_read_error(&r, reset);
+  *out = a | b | c | r;
   return e;
 }
 

@@ -126,13 +126,14 @@ class Drafter:
         k, v = self.ctx_k[seq][layer][:n].float(), self.ctx_v[seq][layer][:n].float()
         return k[:, :, 0] + k[:, :, 1], v[:, :, 0] + v[:, :, 1]
 
-    def settle(self, seq: int, pos: int, taps: torch.Tensor):
-        """Settle tap rows [n][tw] (device f32) at positions pos.., 1024 rows a call."""
+    def settle(self, seq: int, pos: int, taps: torch.Tensor, chunk: int = L.SETTLE_MAX):
+        """Settle tap rows [n][tw] (device f32) at positions pos.., `chunk` (1..1024) rows a call."""
         assert taps.dtype == torch.float32 and taps.is_cuda and taps.is_contiguous()
+        assert 1 <= chunk <= L.SETTLE_MAX
         n = taps.shape[0]
         st = _stream()
-        for i in range(0, n, L.SETTLE_MAX):
-            m = min(L.SETTLE_MAX, n - i)
+        for i in range(0, n, chunk):
+            m = min(chunk, n - i)
             L.dflash_settle(self.h, seq, pos + i, taps[i:i + m].data_ptr(), m, st)
 
     def block(self, anchor_pos: Sequence[int], h: torch.Tensor, k: Optional[int] = None, width: Optional[int] = None,

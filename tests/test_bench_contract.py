@@ -65,3 +65,26 @@ def test_binding_raises_when_the_library_is_missing(monkeypatch):
     monkeypatch.setattr(L, "LIB_PATH", os.path.join(ROOT, "no-such-dir", "libdflash.so"))
     with pytest.raises(RuntimeError, match="missing"):
         L.lib()
+
+
+def test_algorithmic_bytes_of_each_workload():
+    """The roofline's per-unit bytes: every weight once per block (or per settle call), the K/V
+    rows the windows admit at 4 bytes an element, taps in and K/V out for the settle. The
+    figures of the five workloads: 0.6B block 120.5 MB, 27b block 1,495 MB, settle-heavy block
+    2,737 MB, batched step 4,399 MB, a 27B settle row 1.276 MB at 256-row calls."""
+    sys.path.insert(0, ROOT)
+    import bench
+    import dflash_inputs as di
+    want = {"qwen3-0.6b": 120.5e6, "27b": 1495e6, "settle-heavy": 2737e6, "batched": 4399e6}
+    for name, mb in want.items():
+        wl = di.workload(name)
+        g = wl.geometry
+        ctx = bench.context_rows(g, wl.context, wl.context)
+        nbytes, flops, parts = bench.block_cost(g, wl.head_width, ctx, wl.batch)
+        assert nbytes == pytest.approx(mb, rel=2e-3), (name, nbytes)
+        assert sum(parts.values()) == nbytes and flops > 0
+    g27 = di.workload("27b").geometry
+    assert bench.context_rows(g27, 4096, 4096) == [2047, 2047, 4096, 2047, 2047]
+    per_row, flops = bench.settle_cost_per_row(g27, 256)
+    assert per_row == pytest.approx(326.7e6 / 256, rel=2e-3)
+    assert flops * 256 == pytest.approx(94.0e9, rel=2e-3)

@@ -73,8 +73,7 @@ def _bound(wabs: np.ndarray, x: np.ndarray) -> float:
                                                # many tokens: the split-weight kernel, one and two token tiles
                                                (300, 1024, 64, 256), (130, 512, 32, 100), (256, 768, 64, 480),
                                                (1024, 5120, 64, 256),
-                                               # 19 row tiles: 10 tile pairs, each over its whole k-range,
-                                               # the last pair's second CTA past the matrix
+                                               # 19 row tiles, each one CTA's over its whole k-range
                                                (2432, 1024, 64, 256)])
 def test_gemm_int4_matches_oracle(rows, cols, group, T):
     rng = np.random.default_rng(rows * 7 + T)
@@ -130,8 +129,8 @@ class Pair:
         self.gpu = _drafter().Drafter(g, self.w, max_batch=max_batch, ctx_cap=ctx_cap)
         self.orc = [O.Oracle(g, self.w) for _ in range(max_batch)]
 
-    def settle(self, seq, pos, taps):
-        self.gpu.settle(seq, pos, torch.from_numpy(taps).cuda())
+    def settle(self, seq, pos, taps, chunk=1024):
+        self.gpu.settle(seq, pos, torch.from_numpy(taps).cuda(), chunk=chunk)
         self.orc[seq].settle(pos, taps)
 
     def reset(self, seq, first):
@@ -201,6 +200,30 @@ def test_block_tiny_matches_oracle():
     assert r["logit_err"] < 1e-4 and r["hp_err"] < 5e-4
 
 
+def test_cache_value_out_of_range_sets_the_error_word():
+    """A K/V value of magnitude 65,536 or more does not fit the cache's hi plane: the settle
+    writes infinity there and sets bit 1 (value 2) of the device error word. An ordinary
+    settle of the same rows leaves the word clear."""
+    from speculative_block_drafter_gb300 import _lib as L
+    g = _tiny()
+    w = di.make_weights(g, 0)
+    taps = torch.from_numpy(di.make_taps(g, 0, 8)).cuda()
+    d = _drafter().Drafter(g, w, max_batch=1, ctx_cap=64)
+    d.settle(0, 0, taps)
+    torch.cuda.synchronize()
+    assert L.dflash_device_error(reset=True) == 0
+    d.close()
+    L0 = w["layers"][0]
+    big = dataclasses.replace(L0["v"], scales=np.full_like(L0["v"].scales, 60000.0))
+    d = _drafter().Drafter(g, dict(w, layers=[dict(L0, v=big)]), max_batch=1, ctx_cap=64)
+    d.settle(0, 0, taps)
+    torch.cuda.synchronize()
+    assert L.dflash_device_error(reset=True) == 2
+    k, v = d.context_kv(0, 0, 8)
+    assert torch.isinf(v).any() and torch.isfinite(k).all()
+    d.close()
+
+
 @pytest.mark.parametrize("vocab", [4096, 151936])
 def test_select_alone_on_identical_inputs(vocab):
     """The selector on the oracle's own logits and hp (f32): isolates it from the block.
@@ -265,11 +288,12 @@ def test_block_edge_cases(case):
 
 
 def test_full_qwen3_0p6b_workload():
-    """The bench's workload: 1024 positions settled in four chunks, then one block and the selector."""
+    """The qwen3-0.6b workload: 1024 positions settled in 256-row calls (as the bench settles),
+    then one block and the selector."""
     wl = di.workload("qwen3-0.6b")
     g = wl.geometry
     p = Pair(g, ctx_cap=wl.context + 256)
-    p.settle(0, 0, di.make_taps(g, 0, wl.context))
+    p.settle(0, 0, di.make_taps(g, 0, wl.context), chunk=256)
     assert p.check_cache() < 1e-4
     a = di.anchor_token(g, 0)
     r = p.draft([wl.context], [di.block_rows(g, 0, a)], [a])[0]
@@ -279,12 +303,12 @@ def test_full_qwen3_0p6b_workload():
 
 
 def test_full_27b_workload():
-    """The 27b workload at full size: 4096 positions settled in 1024-row calls, windowed and
-    no-rope layers, one block over the whole head and the selector."""
+    """The 27b workload at full size: 4096 positions settled in 256-row calls (as the bench
+    settles), windowed and no-rope layers, one block over the whole head and the selector."""
     wl = di.workload("27b")
     g = wl.geometry
     p = Pair(g, seed=wl.seed, ctx_cap=wl.context + 256)
-    p.settle(0, 0, di.make_taps(g, wl.seed, wl.context))
+    p.settle(0, 0, di.make_taps(g, wl.seed, wl.context), chunk=256)
     assert p.check_cache() < 1e-4
     a = di.anchor_token(g, wl.seed)
     r = p.draft([wl.context], [di.block_rows(g, wl.seed, a)], [a])[0]
@@ -321,14 +345,14 @@ def test_full_batched_workload_sampled_sequences():
 
 
 def test_full_settle_heavy_workload():
-    """The settle-heavy workload at full size: 32,768 positions settled in 1024-row calls (the
-    oracle in 4096-row slices of the same taps), every layer over the whole context, one block
-    over the whole head and the selector."""
+    """The settle-heavy workload at full size, in the bench's launch configuration: 32,768
+    positions settled in 256-row calls (the oracle in 4096-row slices of the same taps), every
+    layer over the whole context, one block over the whole head and the selector."""
     wl = di.workload("settle-heavy")
     g = wl.geometry
     p = Pair(g, seed=wl.seed, ctx_cap=wl.context + g.block)
     for start in range(0, wl.context, 4096):
-        p.settle(0, start, di.make_taps(g, wl.seed, 4096, start))
+        p.settle(0, start, di.make_taps(g, wl.seed, 4096, start), chunk=256)
     assert p.check_cache() < 1e-4
     a = di.anchor_token(g, wl.seed)
     r = p.draft([wl.context], [di.block_rows(g, wl.seed, a)], [a])[0]
