@@ -94,6 +94,32 @@ typedef struct dflash_weights {
 
 typedef struct dflash_t dflash_t;
 
+/* ---- context caches --------------------------------------------------------- */
+
+#define DFLASH_KV_PLANES 0  /* two f16 planes an element (hi, lo): 4 bytes, about 21 bits (dflash_create) */
+#define DFLASH_KV_F16 1     /* one f16 an element: 2 bytes, 11 bits */
+
+/* How the K and V caches of every (sequence, layer) are laid out. `format` is
+ * DFLASH_KV_PLANES or DFLASH_KV_F16 (the element's form, per row and KV head:
+ * hi[head_dim] then lo[head_dim], or one f16[head_dim]). ring[l] = 0: a linear
+ * cache of ctx_cap rows, row = position - first. ring[l] = C > 0, only for a
+ * layer with a window w (C >= 2 * w): a ring of C rows, row = (position -
+ * first) % C, followed by w more rows that repeat its first w rows, so that
+ * every range a block reads (fewer than w rows) is contiguous. A ring holds
+ * every row the layer keeps: after each settle the window trim of dflash.rs
+ * `Drafter::settle_rows` leaves a layer at most 2 * w rows (the ring of
+ * dory.rs `struct Slot` holds a sliding layer's rows the same way). */
+typedef struct dflash_cache_config {
+  int32_t format;
+  int32_t ring[DFLASH_MAX_LAYERS];
+} dflash_cache_config;
+
+/* Rows, and bytes, of layer `layer`'s K cache (the V cache is the same) of one
+ * sequence under `cache` (NULL: DFLASH_KV_PLANES, no rings); 0 for a bad
+ * argument or a ring the layer cannot take. */
+int64_t dflash_cache_rows(const dflash_geometry *g, const dflash_cache_config *cache, int32_t layer, int64_t ctx_cap);
+size_t dflash_cache_bytes(const dflash_geometry *g, const dflash_cache_config *cache, int32_t layer, int64_t ctx_cap);
+
 /* ---- packing (the library's matrix layouts) -------------------------------- */
 
 /* Bytes of the packed codes and of the packed scales of a four-bit matrix
@@ -172,18 +198,78 @@ int dflash_create(dflash_t **out, const dflash_geometry *g, const dflash_weights
                   int32_t max_batch, void *const *ctx_k, void *const *ctx_v, int64_t ctx_cap,
                   void *workspace, size_t workspace_bytes);
 
+/* dflash_create with the caches laid out by `cache` (dflash_cache_config):
+ * ctx_k / ctx_v[seq * layers + l] hold dflash_cache_bytes(g, cache, l, ctx_cap)
+ * bytes each. Errors as dflash_create. */
+int dflash_create_ex(dflash_t **out, const dflash_geometry *g, const dflash_weights *w, int32_t max_batch,
+                     const dflash_cache_config *cache, void *const *ctx_k, void *const *ctx_v, int64_t ctx_cap,
+                     void *workspace, size_t workspace_bytes);
+
+/* ---- the context of a sequence (dflash.rs `Drafter`: first, len, pending,
+ * and per layer `Ctx::dropped`). The context covers positions first ..
+ * first + len; `pending` rows of positions first + len .. wait to be settled;
+ * layer l holds positions first + dropped[l] .. first + len. */
+
 /* Context of sequence `seq` = empty, starting at position `first`. Host only. */
 int dflash_reset(dflash_t *d, int32_t seq, int64_t first);
 
 /* The settled context of `seq`: first position and row count. Host only. */
 int dflash_context(const dflash_t *d, int32_t seq, int64_t *first, int64_t *len);
 
-/* Settle `n` (1..1024) tap rows of sequence `seq` at positions pos..pos+n-1
- * (gpu_cuda/hyb/dflash.rs `Dev::settle`; dflash.rs `settle_rows`). `taps` is a
- * device f32 [n][taps*hidden], joined in tap order. first <= pos <= first+len:
- * rows at held positions replace them and what follows (len = pos-first+n).
- * Errors: ARG (n, pos), CAPACITY (pos-first+n > ctx_cap), CUDA. */
+/* dflash_context plus the rows waiting to be settled and, per layer, the rows
+ * the window trim let go (`dropped`: a host array of `layers`, or NULL). */
+int dflash_context_ex(const dflash_t *d, int32_t seq, int64_t *first, int64_t *len, int64_t *pending,
+                      int64_t *dropped);
+
+/* Add `n` (1..1024) tap rows of sequence `seq` at positions pos..pos+n-1 to the
+ * context (dflash.rs `Drafter::push_context`: `queue_context`, then `settle`;
+ * the rows computed as gpu_cuda/hyb/dflash.rs `Dev::settle` does). `taps` is a
+ * device f32 [n][taps*hidden], joined in tap order. A position already held
+ * (first <= pos <= the next position) drops what follows it first
+ * (`Drafter::truncate`); any other pos (a gap) starts the context over at
+ * pos. Rows that waited settle with these; when they and these are more than
+ * dflash_pending_limit, the oldest (a multiple of 64 rows) settle first, in a
+ * settle of their own. After each settle a windowed layer holding more than
+ * twice its window rows lets go of all but its last `window` rows
+ * (`Drafter::settle_rows`). Errors: ARG (n), CAPACITY (a linear cache past
+ * ctx_cap), CUDA. */
 int dflash_settle(dflash_t *d, int32_t seq, int64_t pos, const float *taps, int32_t n, void *stream);
+
+/* Rows that may wait unsettled in a sequence (dflash.rs `Drafter::queue_context`,
+ * the limit of its CUDA arm): max(512, widest window + 256) when every layer
+ * has a window, else 512. */
+int64_t dflash_pending_limit(const dflash_geometry *g);
+
+/* Give sequence `seq` the device buffer its waiting tap rows are kept in:
+ * 16-byte aligned, `rows` * taps * hidden * 4 bytes, rows >= the pending limit
+ * (NULL: none; then dflash_queue fails). The buffer stays the caller's; rows
+ * waiting in an earlier buffer are dropped. Host only. Errors: ARG, CAPACITY. */
+int dflash_bind_pending(dflash_t *d, int32_t seq, void *buf, int64_t rows);
+
+/* Queue `n` (1..1024) tap rows at pos.. (dflash.rs `Drafter::queue_context`):
+ * the position rule of dflash_settle; the rows are copied into the pending
+ * buffer and wait, except that past the pending limit the oldest (a multiple
+ * of 64 rows) settle at once. A block reads no waiting rows: settle them first.
+ * Errors: ARG (n, no pending buffer), CAPACITY, CUDA. */
+int dflash_queue(dflash_t *d, int32_t seq, int64_t pos, const float *taps, int32_t n, void *stream);
+
+/* Every waiting row of `seq` becomes context, in one settle (dflash.rs
+ * `Drafter::settle`). Errors: CAPACITY, CUDA. */
+int dflash_settle_pending(dflash_t *d, int32_t seq, void *stream);
+
+/* Forget the context of `seq` from position `pos` on (dflash.rs
+ * `Drafter::truncate`, a rewind of the target): waiting rows past pos,
+ * settled rows at or past it; nothing is enqueued. Host only. */
+int dflash_truncate(dflash_t *d, int32_t seq, int64_t pos);
+
+/* Keys and values made elsewhere as the context rows of positions
+ * pos..pos+n-1 (n 1..1024) of every layer (gpu_cuda/hyb/dflash.rs
+ * `Dev::push_rows`, here for every layer at once): k[l], v[l] are device f32
+ * [n][kv_heads][head_dim], keys already normalised and rotated. The position
+ * rule, the waiting rows and the window trim are dflash_settle's; the rows are
+ * written in the cache format. Errors: ARG, CAPACITY, CUDA. */
+int dflash_push_rows(dflash_t *d, int32_t seq, int64_t pos, int32_t n, const float *const *k, const float *const *v,
+                     void *stream);
 
 /* One block of `batch` sequences 0..batch-1 (dflash.rs `Drafter::block` +
  * the head and selector GEMMs of `Dev::block`). `anchor_pos` is a host array
@@ -191,7 +277,8 @@ int dflash_settle(dflash_t *d, int32_t seq, int64_t pos, const float *taps, int3
  * (read only). Writes logits f32 [batch][k][width] (rows 1..k over the head's
  * first `width` rows) and hp f32 [batch][k][selector_rank]. 0 < k < block,
  * selector_top <= width <= vocab. Layer l of sequence s reads its context
- * range by `Drafter::block`'s rule. Errors: ARG, CUDA. */
+ * range by `Drafter::block`'s rule, from first + dropped[l] on. Errors: ARG
+ * (also: rows of a sequence wait to be settled), CUDA. */
 int dflash_block(dflash_t *d, int32_t batch, const int64_t *anchor_pos, const float *h, int32_t k,
                  int32_t width, float *logits, float *hp, void *stream);
 

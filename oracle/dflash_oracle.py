@@ -27,8 +27,14 @@ embeddings). Readings fixed where the pages leave a step open:
 * rotary angle: ``f32(f32(pos) * inv_freq_f32)`` as in ``Drafter::rotate``;
   its cosine and sine are taken in f64;
 * the attention scale is the f32 value of ``head_dim^-1/2`` (``Drafter::block``);
-* the device keeps every settled row since ``first`` (``dropped = 0``); the
-  context range of a layer is ``Drafter::block``'s rule with that base.
+* context bookkeeping follows the host drafter: ``Drafter::truncate``,
+  ``Drafter::queue_context`` (a gap starts the context over; past the pending
+  limit the oldest rows settle in multiples of ``CONTEXT_CHUNK``), ``settle``
+  and the window trim at the end of ``Drafter::settle_rows`` (a layer holding
+  more than twice its window keeps its last ``window`` rows, ``dropped`` grows
+  by the rest); the pending limit is the one the page gives when CUDA is
+  active; a layer's context range is ``Drafter::block``'s rule with the base
+  ``first + dropped``.
 
 Parity pins: every function here is pinned by a ``-m "not gpu"`` test against
 a closed form, the page's worked example, a brute-force evaluation or an
@@ -49,8 +55,13 @@ import numpy as np
 
 __all__ = [
     "dequant_int4", "int4_matmul", "f16_matmul", "rms", "inv_freq", "rotate", "conv",
-    "context_range", "attention", "mlp", "top_k", "select_with", "Oracle",
+    "context_range", "attention", "mlp", "top_k", "select_with", "pending_limit", "Oracle",
 ]
+
+# Context bookkeeping constants of the host drafter (dflash.rs, module constants).
+BLOCK_SLACK = 256       # positions past a layer's window still kept for the next anchors
+CONTEXT_CHUNK = 64      # the over-limit settle takes a multiple of this many rows
+PENDING_ROWS = 512      # rows that may wait unsettled
 
 
 # ---------------------------------------------------------------- matrices
@@ -155,9 +166,19 @@ def conv(base: np.ndarray, d: np.ndarray, x: np.ndarray, stage: int, kn: int, gs
 
 # ---------------------------------------------------------------- attention
 
-def context_range(first: int, length: int, anchor_pos: int, window: int):
-    """Context positions ``[lo, hi)`` a layer's block reads (dflash.rs ``Drafter::block``), no rows dropped."""
-    base = first
+def pending_limit(g) -> int:
+    """Rows that may wait unsettled (dflash.rs ``Drafter::queue_context``, the CUDA arm's limit):
+    as many as the widest window reads plus ``BLOCK_SLACK`` when every layer is windowed, else
+    ``PENDING_ROWS``; never fewer than ``PENDING_ROWS``."""
+    if all(g.window_of(l) > 0 for l in range(g.layers)):
+        return max(PENDING_ROWS, max(g.window_of(l) for l in range(g.layers)) + BLOCK_SLACK)
+    return PENDING_ROWS
+
+
+def context_range(first: int, length: int, anchor_pos: int, window: int, dropped: int = 0):
+    """Context positions ``[lo, hi)`` a layer's block reads (dflash.rs ``Drafter::block``): the
+    layer holds ``first + dropped .. first + length``."""
+    base = first + dropped
     hi = max(min(anchor_pos, first + length), base)
     if window > 0:
         lo = min(max(max(anchor_pos + 1 - window, 0), base), hi)
@@ -269,13 +290,18 @@ class Oracle:
         self.inv = inv_freq(g.head_dim, g.rope_theta)
         self.first = 0
         self.len = 0
+        self.dropped = [0] * g.layers           # per layer: rows let go by the window trim
+        self.pending: List[np.ndarray] = []     # tap rows waiting to be settled, from first + len on
         kvd = (0, g.kv_heads, g.head_dim)
         self.ctx_k: List[np.ndarray] = [np.zeros(kvd) for _ in range(g.layers)]
         self.ctx_v: List[np.ndarray] = [np.zeros(kvd) for _ in range(g.layers)]
 
     # -- context
     def reset(self, first: int = 0):
+        """The context empty, starting at ``first`` (dflash.rs ``Drafter::reset`` starts at 0)."""
         self.first, self.len = first, 0
+        self.dropped = [0] * self.g.layers
+        self.pending = []
         for i in range(self.g.layers):
             self.ctx_k[i] = self.ctx_k[i][:0]
             self.ctx_v[i] = self.ctx_v[i][:0]
@@ -301,15 +327,89 @@ class Oracle:
             out.append((k.reshape(-1, g.kv_heads, g.head_dim), v.reshape(-1, g.kv_heads, g.head_dim)))
         return t, out
 
-    def settle(self, pos: int, taps: np.ndarray):
-        """Append tap rows at ``pos`` (``first <= pos <= first + len``); rows from ``pos`` on are replaced."""
-        assert self.first <= pos <= self.first + self.len
-        keep = pos - self.first
-        _, kv = self.settle_rows(pos, taps)
+    def next_position(self) -> int:
+        """The position the next context row belongs to (dflash.rs ``Drafter::next_position``)."""
+        return self.first + self.len + len(self.pending)
+
+    def truncate(self, pos: int):
+        """Forget the context from position ``pos`` on (dflash.rs ``Drafter::truncate``): waiting rows
+        past it, settled rows at or past it; a layer that let rows go keeps ``dropped <= len``."""
+        held = self.first + self.len
+        self.pending = self.pending[:max(pos - held, 0)]
+        keep = min(max(pos - self.first, 0), self.len)
+        for li in range(self.g.layers):
+            rows = max(keep - self.dropped[li], 0)
+            self.ctx_k[li] = self.ctx_k[li][:rows]
+            self.ctx_v[li] = self.ctx_v[li][:rows]
+            self.dropped[li] = min(self.dropped[li], keep)
+        self.len = keep
+
+    def _append(self, pos: int, rows):
+        """Rows of positions ``pos ..`` (= first + len) into every layer's context, then the window
+        trim (the end of dflash.rs ``Drafter::settle_rows``). ``rows`` is tap rows ``[n][tw]`` or,
+        for imported rows, a list of per-layer ``(k, v)`` ``[n][kv_heads][head_dim]``."""
+        if isinstance(rows, np.ndarray):
+            if len(rows) == 0:
+                return
+            _, kv = self.settle_rows(pos, rows)
+        else:
+            kv = rows
+        n = len(kv[0][0])
         for li, (k, v) in enumerate(kv):
-            self.ctx_k[li] = np.concatenate([self.ctx_k[li][:keep], k], axis=0)
-            self.ctx_v[li] = np.concatenate([self.ctx_v[li][:keep], v], axis=0)
-        self.len = keep + len(taps)
+            self.ctx_k[li] = np.concatenate([self.ctx_k[li], np.asarray(k, np.float64)], axis=0)
+            self.ctx_v[li] = np.concatenate([self.ctx_v[li], np.asarray(v, np.float64)], axis=0)
+        self.len += n
+        for li in range(self.g.layers):
+            w, held = self.g.window_of(li), self.len - self.dropped[li]
+            if w > 0 and held > 2 * w:
+                cut = held - w
+                self.ctx_k[li] = self.ctx_k[li][cut:]
+                self.ctx_v[li] = self.ctx_v[li][cut:]
+                self.dropped[li] += cut
+
+    def _restart_or_truncate(self, pos: int):
+        # a gap starts the context over; a held position replaces what follows
+        if pos > self.next_position() or pos < self.first:
+            self.truncate(0)
+            self.first = pos
+        else:
+            self.truncate(pos)
+
+    def queue(self, pos: int, taps: np.ndarray):
+        """Tap rows of positions ``pos ..`` wait to become context (dflash.rs ``Drafter::queue_context``);
+        past ``pending_limit`` the oldest settle at once, a multiple of ``CONTEXT_CHUNK`` rows."""
+        self._restart_or_truncate(pos)
+        self.pending.extend(np.asarray(taps))
+        held = len(self.pending)
+        limit = pending_limit(self.g)
+        if held > limit:
+            over = min(-(-(held - limit) // CONTEXT_CHUNK) * CONTEXT_CHUNK, held)
+            rows = np.stack(self.pending[:over])
+            self.pending = self.pending[over:]
+            self._append(self.first + self.len, rows)
+
+    def settle_pending(self):
+        """Every waiting row becomes context (dflash.rs ``Drafter::settle``)."""
+        if self.pending:
+            rows = np.stack(self.pending)
+            self.pending = []
+            self._append(self.first + self.len, rows)
+
+    def settle(self, pos: int, taps: np.ndarray):
+        """Add tap rows of positions ``pos ..`` to the context (dflash.rs ``Drafter::push_context``):
+        queue them, then settle every waiting row. Rows at held positions replace them and what
+        follows; a gap starts the context over."""
+        self.queue(pos, taps)
+        self.settle_pending()
+
+    def push_rows(self, pos: int, kv):
+        """Keys and values made elsewhere (per layer ``(k, v)`` ``[n][kv_heads][head_dim]``, keys
+        already normed and rotated) as the context rows of positions ``pos ..``: the bookkeeping
+        of a settle at ``pos`` (gap, truncate, window trim), the rows taken as given (the
+        card arm's ``Dev::push_rows`` import, for every layer at once)."""
+        self._restart_or_truncate(pos)
+        self.settle_pending()
+        self._append(self.first + self.len, kv)
 
     # -- block
     def block(self, anchor_pos: int, h: np.ndarray, trace: Optional[Dict] = None) -> np.ndarray:
@@ -325,9 +425,11 @@ class Oracle:
         pos = [anchor_pos + r for r in range(R)]
         for li, L in enumerate(w["layers"]):
             win = g.window_of(li)
-            lo, hi = context_range(self.first, self.len, anchor_pos, win)
-            ck = self.ctx_k[li][lo - self.first:hi - self.first]
-            cv = self.ctx_v[li][lo - self.first:hi - self.first]
+            assert not self.pending, "rows wait to become context (settle_pending)"
+            base = self.first + self.dropped[li]
+            lo, hi = context_range(self.first, self.len, anchor_pos, win, self.dropped[li])
+            ck = self.ctx_k[li][lo - base:hi - base]
+            cv = self.ctx_v[li][lo - base:hi - base]
             # attention sub-layer: x = norm(h); x, d = conv_in(x); q, k, v
             x = rms(h, L["in_norm"], g.eps)
             ad = f16_matmul(L["attn_proj"], x)

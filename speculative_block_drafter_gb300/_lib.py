@@ -36,6 +36,14 @@ class Geometry(C.Structure):
     ]
 
 
+KV_PLANES = 0   # two f16 planes an element (4 bytes, about 21 bits)
+KV_F16 = 1      # one f16 an element (2 bytes)
+
+
+class CacheConfig(C.Structure):
+    _fields_ = [("format", C.c_int32), ("ring", C.c_int32 * MAX_LAYERS)]
+
+
 class Matrix(C.Structure):
     _fields_ = [("data", C.c_void_p), ("scales", C.c_void_p)]
 
@@ -77,9 +85,23 @@ EXPORTS = {
     "dflash_workspace_bytes": (C.c_size_t, [C.POINTER(Geometry), C.c_int32]),
     "dflash_create": (C.c_int, [C.POINTER(C.c_void_p), C.POINTER(Geometry), C.POINTER(Weights), C.c_int32,
                                 C.POINTER(C.c_void_p), C.POINTER(C.c_void_p), C.c_int64, C.c_void_p, C.c_size_t]),
+    "dflash_cache_rows": (C.c_int64, [C.POINTER(Geometry), C.POINTER(CacheConfig), C.c_int32, C.c_int64]),
+    "dflash_cache_bytes": (C.c_size_t, [C.POINTER(Geometry), C.POINTER(CacheConfig), C.c_int32, C.c_int64]),
+    "dflash_create_ex": (C.c_int, [C.POINTER(C.c_void_p), C.POINTER(Geometry), C.POINTER(Weights), C.c_int32,
+                                   C.POINTER(CacheConfig), C.POINTER(C.c_void_p), C.POINTER(C.c_void_p), C.c_int64,
+                                   C.c_void_p, C.c_size_t]),
     "dflash_reset": (C.c_int, [C.c_void_p, C.c_int32, C.c_int64]),
     "dflash_context": (C.c_int, [C.c_void_p, C.c_int32, C.POINTER(C.c_int64), C.POINTER(C.c_int64)]),
+    "dflash_context_ex": (C.c_int, [C.c_void_p, C.c_int32, C.POINTER(C.c_int64), C.POINTER(C.c_int64),
+                                    C.POINTER(C.c_int64), C.POINTER(C.c_int64)]),
     "dflash_settle": (C.c_int, [C.c_void_p, C.c_int32, C.c_int64, C.c_void_p, C.c_int32, C.c_void_p]),
+    "dflash_pending_limit": (C.c_int64, [C.POINTER(Geometry)]),
+    "dflash_bind_pending": (C.c_int, [C.c_void_p, C.c_int32, C.c_void_p, C.c_int64]),
+    "dflash_queue": (C.c_int, [C.c_void_p, C.c_int32, C.c_int64, C.c_void_p, C.c_int32, C.c_void_p]),
+    "dflash_settle_pending": (C.c_int, [C.c_void_p, C.c_int32, C.c_void_p]),
+    "dflash_truncate": (C.c_int, [C.c_void_p, C.c_int32, C.c_int64]),
+    "dflash_push_rows": (C.c_int, [C.c_void_p, C.c_int32, C.c_int64, C.c_int32, C.POINTER(C.c_void_p),
+                                   C.POINTER(C.c_void_p), C.c_void_p]),
     "dflash_block": (C.c_int, [C.c_void_p, C.c_int32, C.POINTER(C.c_int64), C.c_void_p, C.c_int32, C.c_int32,
                                C.c_void_p, C.c_void_p, C.c_void_p]),
     "dflash_select": (C.c_int, [C.c_void_p, C.c_int32, C.c_void_p, C.c_void_p, C.c_void_p, C.c_int32, C.c_int32,
@@ -175,8 +197,60 @@ def dflash_create(geom: Geometry, weights: Weights, max_batch, ctx_k, ctx_v, ctx
     return h
 
 
+def dflash_cache_rows(geom: Geometry, cache: CacheConfig, layer, ctx_cap) -> int:
+    return lib().dflash_cache_rows(C.byref(geom), C.byref(cache) if cache is not None else None, layer, ctx_cap)
+
+
+def dflash_cache_bytes(geom: Geometry, cache: CacheConfig, layer, ctx_cap) -> int:
+    return lib().dflash_cache_bytes(C.byref(geom), C.byref(cache) if cache is not None else None, layer, ctx_cap)
+
+
+def dflash_create_ex(geom: Geometry, weights: Weights, max_batch, cache: CacheConfig, ctx_k, ctx_v, ctx_cap, workspace,
+                     ws_bytes):
+    h = C.c_void_p()
+    ks = (C.c_void_p * len(ctx_k))(*ctx_k)
+    vs = (C.c_void_p * len(ctx_v))(*ctx_v)
+    _check(lib().dflash_create_ex(C.byref(h), C.byref(geom), C.byref(weights), max_batch, C.byref(cache), ks, vs,
+                                  ctx_cap, workspace, ws_bytes))
+    return h
+
+
 def dflash_reset(h, seq, first):
     _check(lib().dflash_reset(h, seq, first))
+
+
+def dflash_context_ex(h, seq, layers):
+    """(first, len, pending, dropped per layer)."""
+    f, n, p = C.c_int64(), C.c_int64(), C.c_int64()
+    dr = (C.c_int64 * max(1, layers))()
+    _check(lib().dflash_context_ex(h, seq, C.byref(f), C.byref(n), C.byref(p), dr))
+    return f.value, n.value, p.value, [dr[i] for i in range(layers)]
+
+
+def dflash_pending_limit(geom: Geometry) -> int:
+    return lib().dflash_pending_limit(C.byref(geom))
+
+
+def dflash_bind_pending(h, seq, buf, rows):
+    _check(lib().dflash_bind_pending(h, seq, buf, rows))
+
+
+def dflash_queue(h, seq, pos, taps, n, stream):
+    _check(lib().dflash_queue(h, seq, pos, taps, n, stream))
+
+
+def dflash_settle_pending(h, seq, stream):
+    _check(lib().dflash_settle_pending(h, seq, stream))
+
+
+def dflash_truncate(h, seq, pos):
+    _check(lib().dflash_truncate(h, seq, pos))
+
+
+def dflash_push_rows(h, seq, pos, n, k_ptrs, v_ptrs, stream):
+    ks = (C.c_void_p * len(k_ptrs))(*k_ptrs)
+    vs = (C.c_void_p * len(v_ptrs))(*v_ptrs)
+    _check(lib().dflash_push_rows(h, seq, pos, n, ks, vs, stream))
 
 
 def dflash_context(h, seq):

@@ -75,12 +75,13 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-bool attn_kv_map(CUtensorMap *m, const void *base, int64_t rows, int kv, int hd, int box_rows) {
+bool attn_kv_map(CUtensorMap *m, const void *base, int64_t rows, int kv, int hd, int planes, int box_rows) {
   PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
-  if (!enc || rows < 1 || rows > INT32_MAX || box_rows < 1 || box_rows > 256 || hd % 64) return false;
+  if (!enc || rows < 1 || rows > INT32_MAX || box_rows < 1 || box_rows > 256 || hd % 64 || (planes != 1 && planes != 2))
+    return false;
   // (dimension, plane, head, row) of halves; 64 halves (128 bytes) a box row
-  const cuuint64_t dims[4] = {(cuuint64_t)hd, 2, (cuuint64_t)kv, (cuuint64_t)rows};
-  const cuuint64_t strides[3] = {(cuuint64_t)hd * 2, (cuuint64_t)hd * 4, (cuuint64_t)kv * hd * 4};
+  const cuuint64_t dims[4] = {(cuuint64_t)hd, (cuuint64_t)planes, (cuuint64_t)kv, (cuuint64_t)rows};
+  const cuuint64_t strides[3] = {(cuuint64_t)hd * 2, (cuuint64_t)hd * 2 * planes, (cuuint64_t)kv * hd * 2 * planes};
   const cuuint32_t box[4] = {64, 1, 1, (cuuint32_t)box_rows};
   const cuuint32_t es[4] = {1, 1, 1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4, (void *)base, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -134,35 +135,38 @@ __device__ __forceinline__ void mma3(float (&acc)[4], const uint32_t (&ah)[4], c
 // One CTA per (split, KV head, sequence): the rep*R queries of the KV head over
 // the split's context keys in chunks of 64 (the last split takes the block's
 // own R rows as a final chunk). The context caches and the block's own K/V hold
-// f16 planes (hi, lo) per row and head, written once when the rows were
-// settled or projected. Warp 0 loads each chunk's K and V planes with tensor
-// copies (boxes of 64 rows x 64 halves, 128-byte swizzled) into a 3-stage
-// ring; the warps read their B fragments with ldmatrix (K as stored, V
-// transposed) and hold the queries' hi/lo fragments in registers. Warp w takes
-// query block w % QW and key group w / QW of every chunk; each keeps a running
-// (m, l, o), merged in the CTA at the end. Rows past a chunk's keys (the
-// context's end, or the block's own R rows) hold whatever the copy or an
+// f16 values per row and head in PL planes (PL = 2: hi, lo; PL = 1: one f16),
+// written once when the rows were settled or projected. Warp 0 loads each
+// chunk's K and V planes with tensor copies (boxes of 64 rows x 64 halves,
+// 128-byte swizzled) into a ring of stages; the warps read their B fragments
+// with ldmatrix (K as stored, V transposed) and hold the queries' hi/lo
+// fragments in registers. The products: q.k as qh.kh + qh.kl + ql.kh (PL = 2)
+// or qh.k + ql.k (PL = 1), p.v likewise with p split into hi and lo. Warp w
+// takes query block w % QW and key group w / QW of every chunk; each keeps a
+// running (m, l, o), merged in the CTA at the end. Rows past a chunk's keys
+// (the context's end, or the block's own R rows) hold whatever the copy or an
 // earlier chunk left: their scores are masked and, before P.V, the warps whose
 // key range reaches them zero their V planes.
+template <int PL>
 struct AttnRing {
   static constexpr int BOX = CH * 128;       // 64 rows x 64 halves
   static constexpr int REGION = 2 * BOX;     // one plane of K or V of a chunk (hd <= 128)
-  static constexpr int STAGE = 4 * REGION;   // K hi, K lo, V hi, V lo
-  static constexpr int STAGES = 3;
-  static constexpr size_t BYTES = (size_t)STAGES * STAGE + 1024 + 64;  // + alignment, barriers
+  static constexpr int STAGE = 2 * PL * REGION;  // K planes, then V planes
+  static constexpr int STAGES = PL == 2 ? 3 : 5;
+  static constexpr size_t BYTES = (size_t)STAGES * STAGE + 1024 + 16 * STAGES;  // + alignment, barriers
 };
 
 // Byte offset of 16-byte chunk j (8 halves: dimensions 8j..8j+7) of row r in a
 // plane region: box j / 8, swizzled within the row's 128 bytes.
 __device__ __forceinline__ uint32_t plane_off(int r, int j) {
-  return (uint32_t)((j >> 3) * AttnRing::BOX + r * 128 + (((j & 7) ^ (r & 7)) << 4));
+  return (uint32_t)((j >> 3) * (CH * 128) + r * 128 + (((j & 7) ^ (r & 7)) << 4));
 }
 
-template <int HD, int KG>
+template <int HD, int KG, int PL>
 __global__ void __launch_bounds__(ATT_THREADS, 1) k_attn(const float *__restrict__ q, const __grid_constant__ AttnArgs args,
                                                          int heads, int kv, int R, int window, float scale, int nsplit,
                                                          int cps, float *__restrict__ part) {
-  using RG = AttnRing;
+  using RG = AttnRing<PL>;
   constexpr int S = RG::STAGES;
   constexpr int H2 = HD / 64;        // boxes of a row
   constexpr int KW = CH / KG;        // keys per warp per chunk
@@ -210,14 +214,14 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) k_attn(const float *__restrict
     const int z = is_own ? b * R : (int)(Sq.row0 + (int64_t)(c0 + j) * CH);
     const uint32_t rows = is_own ? R : CH;
     const uint32_t bar = full0 + 8 * st, base = ring + st * RG::STAGE;
-    mbar_expect_tx(bar, 4 * H2 * rows * 128);
+    mbar_expect_tx(bar, 2 * PL * H2 * rows * 128);
 #pragma unroll
-    for (int h = 0; h < H2; ++h) {
-      tma_load4(base + 0 * RG::REGION + h * RG::BOX, km, 64 * h, 0, g, z, bar);
-      tma_load4(base + 1 * RG::REGION + h * RG::BOX, km, 64 * h, 1, g, z, bar);
-      tma_load4(base + 2 * RG::REGION + h * RG::BOX, vm, 64 * h, 0, g, z, bar);
-      tma_load4(base + 3 * RG::REGION + h * RG::BOX, vm, 64 * h, 1, g, z, bar);
-    }
+    for (int h = 0; h < H2; ++h)
+#pragma unroll
+      for (int p = 0; p < PL; ++p) {
+        tma_load4(base + p * RG::REGION + h * RG::BOX, km, 64 * h, p, g, z, bar);
+        tma_load4(base + (PL + p) * RG::REGION + h * RG::BOX, vm, 64 * h, p, g, z, bar);
+      }
   };
   int issued = 0;  // chunks warp 0 has filled
   if (warp == 0)
@@ -262,15 +266,16 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) k_attn(const float *__restrict
     const int kb = (c0 + j) * CH;
     const int cnt = is_own ? R : min(CH, n - kb);
     uint8_t *stp = sm + st * RG::STAGE;
-    const uint32_t khi = smem_u32(stp), klo = khi + RG::REGION, vhi = khi + 2 * RG::REGION, vlo = khi + 3 * RG::REGION;
+    // K planes at regions 0..PL-1, V planes at PL..2PL-1 (klo, vlo unused with one plane)
+    const uint32_t khi = smem_u32(stp), klo = khi + RG::REGION, vhi = khi + PL * RG::REGION, vlo = vhi + RG::REGION;
     const int kk0 = kgi * KW;
     if (busy && cnt < kk0 + KW) {
       // zero the V rows of this warp's keys past the chunk's (both planes, every box)
       const int z0 = max(kk0, cnt), nz = kk0 + KW - z0;
-      for (int idx = lane; idx < nz * 2 * H2 * 8; idx += 32) {
-        const int row = z0 + idx / (2 * H2 * 8), rest = idx % (2 * H2 * 8);
+      for (int idx = lane; idx < nz * PL * H2 * 8; idx += 32) {
+        const int row = z0 + idx / (PL * H2 * 8), rest = idx % (PL * H2 * 8);
         const int pl = rest / (H2 * 8), bx = (rest / 8) % H2, ch = rest % 8;
-        *(uint4 *)(stp + (2 + pl) * RG::REGION + bx * RG::BOX + row * 128 + ch * 16) = make_uint4(0u, 0u, 0u, 0u);
+        *(uint4 *)(stp + (PL + pl) * RG::REGION + bx * RG::BOX + row * 128 + ch * 16) = make_uint4(0u, 0u, 0u, 0u);
       }
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // before the stage's next tensor copy
       __syncwarp();
@@ -281,7 +286,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) k_attn(const float *__restrict
       // (tile t, dims 16ks..+8), (t, +8..+16), (t+1, ..), (t+1, ..) of each plane.
       // The three products go to separate accumulators (two with four tiles),
       // so that the MMAs of a step do not wait on one another.
-      constexpr int NA = NT == 2 ? 3 : 2;
+      constexpr int NA = (PL == 2 && NT == 2) ? 3 : 2;
       float sa[NA][NT][4];
 #pragma unroll
       for (int a = 0; a < NA; ++a)
@@ -292,13 +297,16 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) k_attn(const float *__restrict
 #pragma unroll
         for (int t = 0; t < NT; t += 2) {
           const uint32_t off = plane_off(kk0 + 8 * (t + (mi >> 1)) + mr, 2 * ks + (mi & 1));
-          uint32_t h0, h1, h2, h3, w0, w1, w2, w3;
+          uint32_t h0, h1, h2, h3;
           ldsm4(khi + off, h0, h1, h2, h3);
-          ldsm4(klo + off, w0, w1, w2, w3);
           mma16816(sa[0][t], qh[ks], h0, h1);
           mma16816(sa[0][t + 1], qh[ks], h2, h3);
-          mma16816(sa[1][t], qh[ks], w0, w1);
-          mma16816(sa[1][t + 1], qh[ks], w2, w3);
+          if constexpr (PL == 2) {
+            uint32_t w0, w1, w2, w3;
+            ldsm4(klo + off, w0, w1, w2, w3);
+            mma16816(sa[1][t], qh[ks], w0, w1);
+            mma16816(sa[1][t + 1], qh[ks], w2, w3);
+          }
           mma16816(sa[NA - 1][t], ql[ks], h0, h1);
           mma16816(sa[NA - 1][t + 1], ql[ks], h2, h3);
         }
@@ -367,11 +375,19 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) k_attn(const float *__restrict
 #pragma unroll
         for (int t = 0; t < OT; t += 2) {
           const uint32_t off = plane_off(row, t + (mi >> 1));
-          uint32_t h0, h1, h2, h3, w0, w1, w2, w3;
+          uint32_t h0, h1, h2, h3;
           ldsm4t(vhi + off, h0, h1, h2, h3);
-          ldsm4t(vlo + off, w0, w1, w2, w3);
-          mma3(o[t], ph, pl, h0, h1, w0, w1);
-          mma3(o[t + 1], ph, pl, h2, h3, w2, w3);
+          if constexpr (PL == 2) {
+            uint32_t w0, w1, w2, w3;
+            ldsm4t(vlo + off, w0, w1, w2, w3);
+            mma3(o[t], ph, pl, h0, h1, w0, w1);
+            mma3(o[t + 1], ph, pl, h2, h3, w2, w3);
+          } else {
+            mma16816(o[t], ph, h0, h1);
+            mma16816(o[t + 1], ph, h2, h3);
+            mma16816(o[t], pl, h0, h1);
+            mma16816(o[t + 1], pl, h2, h3);
+          }
         }
       }
     }
@@ -540,21 +556,21 @@ __global__ void __launch_bounds__(32 * MERGE_WARPS) k_attn_merge(const float *__
   }
 }
 
-template <int HD, int KG>
+template <int HD, int KG, int PL>
 static cudaError_t launch_attn(const float *q, const AttnArgs &args, int batch, int max_n, int heads, int kv, int R,
                                int window, float scale, float *part, float *y, int num_sms, const PackDst *pack,
                                const ZeroSet *zero, cudaStream_t st) {
-  const size_t smem = AttnRing::BYTES;
+  const size_t smem = AttnRing<PL>::BYTES;
   static PerDevice configured;
-  if (cudaError_t e = smem_limit(k_attn<HD, KG>, (int)smem, configured)) return e;
+  if (cudaError_t e = smem_limit(k_attn<HD, KG, PL>, (int)smem, configured)) return e;
   int ns, cps;
   plan_splits(batch * kv, max_n, num_sms, ns, cps);
   // With short splits the block's own rows get a split of their own (the last
   // one, past every context chunk), so that no CTA does twice the others' work.
   if (cps <= 4 && max_n > 0) ++ns;
   dim3 grid(ns, kv, batch);
-  cudaError_t e = launch_pdl(k_attn<HD, KG>, grid, dim3(ATT_THREADS), smem, st, 1, q, args, heads, kv, R, window, scale,
-                             ns, cps, part);
+  cudaError_t e = launch_pdl(k_attn<HD, KG, PL>, grid, dim3(ATT_THREADS), smem, st, 1, q, args, heads, kv, R, window,
+                             scale, ns, cps, part);
   if (e != cudaSuccess) return e;
   const int Q = heads / kv * R;
   const int work = (kv * Q + MERGE_WARPS - 1) / MERGE_WARPS;
@@ -570,20 +586,22 @@ static cudaError_t launch_attn(const float *q, const AttnArgs &args, int batch, 
                     ns, work, y, PackDst{}, ZeroSet{});
 }
 
-template <int HD>
+template <int HD, int PL>
 static cudaError_t launch_attn_hd(const float *q, const AttnArgs &args, int batch, int max_n, int heads, int kv, int R,
                                   int window, float scale, float *part, float *y, int num_sms, const PackDst *pack,
                                   const ZeroSet *zero, cudaStream_t st) {
   const int QW = (heads / kv * R + 15) / 16;
   if (QW >= 3)
-    return launch_attn<HD, 2>(q, args, batch, max_n, heads, kv, R, window, scale, part, y, num_sms, pack, zero, st);
-  return launch_attn<HD, 4>(q, args, batch, max_n, heads, kv, R, window, scale, part, y, num_sms, pack, zero, st);
+    return launch_attn<HD, 2, PL>(q, args, batch, max_n, heads, kv, R, window, scale, part, y, num_sms, pack, zero, st);
+  return launch_attn<HD, 4, PL>(q, args, batch, max_n, heads, kv, R, window, scale, part, y, num_sms, pack, zero, st);
 }
 
 cudaError_t attention(const float *q, const CUtensorMap &own_k, const CUtensorMap &own_v, const AttnSeq *seqs,
-                      int batch, int heads, int kv_heads, int hd, int block, int window, float scale, float *partials,
-                      float *y, int num_sms, const PackDst *pack, const ZeroSet *zero, cudaStream_t st) {
-  if (batch < 1 || batch > MAX_BATCH || heads / kv_heads * block > QMAX) return cudaErrorInvalidValue;
+                      int batch, int heads, int kv_heads, int hd, int planes, int block, int window, float scale,
+                      float *partials, float *y, int num_sms, const PackDst *pack, const ZeroSet *zero,
+                      cudaStream_t st) {
+  if (batch < 1 || batch > MAX_BATCH || heads / kv_heads * block > QMAX || (planes != 1 && planes != 2))
+    return cudaErrorInvalidValue;
   AttnArgs args;  // entries past batch are not read
   int max_n = 0;
   for (int i = 0; i < batch; ++i) {
@@ -593,12 +611,18 @@ cudaError_t attention(const float *q, const CUtensorMap &own_k, const CUtensorMa
   args.own_k = own_k;
   args.own_v = own_v;
   num_sms = std::max(1, std::min(num_sms, 1024));
+  if (hd == 128 && planes == 2)
+    return launch_attn_hd<128, 2>(q, args, batch, max_n, heads, kv_heads, block, window, scale, partials, y, num_sms,
+                                  pack, zero, st);
   if (hd == 128)
-    return launch_attn_hd<128>(q, args, batch, max_n, heads, kv_heads, block, window, scale, partials, y, num_sms, pack,
-                               zero, st);
+    return launch_attn_hd<128, 1>(q, args, batch, max_n, heads, kv_heads, block, window, scale, partials, y, num_sms,
+                                  pack, zero, st);
+  if (hd == 64 && planes == 2)
+    return launch_attn_hd<64, 2>(q, args, batch, max_n, heads, kv_heads, block, window, scale, partials, y, num_sms,
+                                 pack, zero, st);
   if (hd == 64)
-    return launch_attn_hd<64>(q, args, batch, max_n, heads, kv_heads, block, window, scale, partials, y, num_sms, pack,
-                              zero, st);
+    return launch_attn_hd<64, 1>(q, args, batch, max_n, heads, kv_heads, block, window, scale, partials, y, num_sms,
+                                 pack, zero, st);
   return cudaErrorInvalidValue;
 }
 

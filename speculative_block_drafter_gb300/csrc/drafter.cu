@@ -1,9 +1,11 @@
 // The C ABI of the drafter (include/dflash.h) and the host driver that
 // enqueues a settle, a block and a selection. The pass follows cortiq-engine
 // src/gpu_cuda/hyb/dflash.rs (`Dev::settle`, `Dev::block`) and
-// src/cortiq_engine/dflash.rs (`Drafter::block`, `Drafter::select_with`).
-// The host keeps only each sequence's (first, len); the device memory is the
-// caller's.
+// src/cortiq_engine/dflash.rs (`Drafter::block`, `Drafter::select_with`); the
+// context bookkeeping follows the host drafter (`Drafter::queue_context`,
+// `settle`, `truncate`, the window trim of `settle_rows`). The host keeps each
+// sequence's (first, len, dropped per layer, waiting rows); the device memory
+// is the caller's.
 #include <algorithm>
 #include <cmath>
 #include <climits>
@@ -39,9 +41,21 @@ size_t up(size_t n) { return (n + ALIGN - 1) / ALIGN * ALIGN; }
 
 bool aligned16(const void *p) { return ((uintptr_t)p & 15) == 0; }
 
+// A sequence's context (dflash.rs `Drafter`: first, len, `Ctx::dropped` per
+// layer, the pending rows). The pending rows live in the caller's buffer as a
+// ring of `pcap` rows: `pcount` rows from slot `phead` on, of positions
+// first + len ...
 struct Seq {
   int64_t first = 0, len = 0;
+  int64_t dropped[DFLASH_MAX_LAYERS] = {};
+  float *pbuf = nullptr;
+  int64_t pcap = 0, phead = 0, pcount = 0;
 };
+
+// Rows of the host drafter's bookkeeping (dflash.rs, module constants).
+constexpr int64_t PENDING_ROWS = 512;
+constexpr int64_t BLOCK_SLACK = 256;
+constexpr int64_t CONTEXT_CHUNK = 64;
 
 // Workspace carve; sizes in bytes.
 struct Carve {
@@ -136,8 +150,11 @@ struct dflash_t {
   dflash_weights w;
   std::vector<dflash_layer_weights> layers;
   int max_batch = 0;
-  std::vector<__half *> ck, cv;   // context caches, f16 planes [cap][kv][2][hd]
-  int64_t cap = 0;
+  std::vector<__half *> ck, cv;   // context caches [seq * layers + l], [rows][kv][planes][hd]
+  int64_t cap = 0;                // rows of a linear cache
+  int planes = 2;                 // 2: DFLASH_KV_PLANES, 1: DFLASH_KV_F16
+  int ring[DFLASH_MAX_LAYERS] = {};    // a layer's ring rows C (0: linear)
+  int mirror[DFLASH_MAX_LAYERS] = {};  // rows past the ring repeating its first ones (the window)
   char *ws = nullptr;
   Carve c{};
   float *h, *x, *xc, *d, *d2, *q, *k, *v, *y, *o, *gt, *up, *part, *kvs;
@@ -154,22 +171,196 @@ struct dflash_t {
 };
 
 namespace {
+// Rows of layer l's cache: a linear cache's ctx_cap, or a ring and its mirror.
+int64_t layer_rows(const dflash_t *d, int l) { return d->ring[l] ? (int64_t)d->ring[l] + d->mirror[l] : d->cap; }
+
 bool encode_maps(dflash_t *d) {
   if (d->maps) return true;
   const dflash_geometry &g = d->g;
   const size_t n = (size_t)d->max_batch * g.layers;
   d->kmap.resize(n);
   d->vmap.resize(n);
-  for (size_t i = 0; i < n; ++i)
-    if (!dfl::attn_kv_map(&d->kmap[i], d->ck[i], d->cap, g.kv_heads, g.head_dim, 64) ||
-        !dfl::attn_kv_map(&d->vmap[i], d->cv[i], d->cap, g.kv_heads, g.head_dim, 64))
+  for (size_t i = 0; i < n; ++i) {
+    const int64_t rows = layer_rows(d, (int)(i % g.layers));
+    if (!dfl::attn_kv_map(&d->kmap[i], d->ck[i], rows, g.kv_heads, g.head_dim, d->planes, 64) ||
+        !dfl::attn_kv_map(&d->vmap[i], d->cv[i], rows, g.kv_heads, g.head_dim, d->planes, 64))
       return false;
+  }
   const int64_t rows = (int64_t)d->max_batch * g.block;
-  if (!dfl::attn_kv_map(&d->own_k, d->kp, rows, g.kv_heads, g.head_dim, g.block) ||
-      !dfl::attn_kv_map(&d->own_v, d->vp, rows, g.kv_heads, g.head_dim, g.block))
+  if (!dfl::attn_kv_map(&d->own_k, d->kp, rows, g.kv_heads, g.head_dim, d->planes, g.block) ||
+      !dfl::attn_kv_map(&d->own_v, d->vp, rows, g.kv_heads, g.head_dim, d->planes, g.block))
     return false;
   d->maps = true;
   return true;
+}
+
+int64_t pending_limit(const dflash_geometry &g) {
+  int64_t widest = 0;
+  bool all = true;
+  for (int l = 0; l < g.layers; ++l) {
+    all = all && g.windows[l] > 0;
+    widest = std::max<int64_t>(widest, g.windows[l]);
+  }
+  return all ? std::max(PENDING_ROWS, widest + BLOCK_SLACK) : PENDING_ROWS;
+}
+
+// dflash.rs `Drafter::truncate`: waiting rows past pos, settled rows at or past it.
+void truncate_seq(dflash_t *d, Seq &s, int64_t pos) {
+  const int64_t held = s.first + s.len;
+  s.pcount = std::min(s.pcount, std::max<int64_t>(pos - held, 0));
+  const int64_t keep = std::min(std::max<int64_t>(pos - s.first, 0), s.len);
+  for (int l = 0; l < d->g.layers; ++l) s.dropped[l] = std::min(s.dropped[l], keep);
+  s.len = keep;
+}
+
+// The position rule of `Drafter::queue_context`: a gap starts the context over at
+// pos; a held position (first <= pos <= the next position) truncates there.
+void restart_or_truncate(dflash_t *d, Seq &s, int64_t pos) {
+  if (pos > s.first + s.len + s.pcount || pos < s.first) {
+    truncate_seq(d, s, 0);
+    s.pcount = 0;
+    s.phead = 0;
+    s.first = pos;
+  } else {
+    truncate_seq(d, s, pos);
+  }
+}
+
+// The end of `Drafter::settle_rows`: a windowed layer holding more than twice its
+// window lets go of all but its last `window` rows.
+void window_trim(dflash_t *d, Seq &s) {
+  for (int l = 0; l < d->g.layers; ++l) {
+    const int64_t w = d->g.windows[l], held = s.len - s.dropped[l];
+    if (w > 0 && held > 2 * w) s.dropped[l] += held - w;
+  }
+}
+
+// Whether the linear caches take rows up to (not including) cache row `end`.
+bool fits(const dflash_t *d, int64_t end) {
+  for (int l = 0; l < d->g.layers; ++l)
+    if (!d->ring[l] && end > d->cap) return false;
+  return true;
+}
+
+// Cache rows of every layer of `seq`, for ctx_planes.
+void cache_rows(const dflash_t *d, int seq, dfl::CtxWrite &W) {
+  const dflash_geometry &g = d->g;
+  for (int l = 0; l < g.layers; ++l) {
+    W.ck[l] = d->ck[(size_t)seq * g.layers + l];
+    W.cv[l] = d->cv[(size_t)seq * g.layers + l];
+    W.ring[l] = d->ring[l];
+    W.mirror[l] = d->mirror[l];
+    W.w[l] = d->layers[l].k_norm;
+    W.rotary[l] = g.no_rope[l] == 0;
+  }
+}
+}  // namespace
+
+namespace {
+// gpu_cuda/hyb/dflash.rs `Dev::settle`: n (<= 1024) tap rows of positions
+// first + len .. into every layer's cache at row index len: t = rms(fc .
+// f16(taps), hidden_norm); per layer K = rot(rms_head(Wk t, k_norm)), V = Wv t.
+int settle_call(dflash_t *d, int seq, const float *taps, int n, cudaStream_t st) {
+  Seq &s = d->seqs[seq];
+  const dflash_geometry &g = d->g;
+  const int hs = g.hidden, tw = g.taps * g.hidden, kvd = g.kv_heads * g.head_dim;
+  const dfl::TcJob fc{d->w.fc.data, nullptr, d->x, hs, hs};
+  DF_CUDA(dfl::tc_gemm_f16(&fc, 1, taps, tw, n, tw, d->act, d->num_sms, st));
+  DF_CUDA(dfl::rmsnorm(d->x, d->w.hidden_norm, d->x, n, hs, (float)g.eps, 1, -1, -1, st));
+  // k = Wk t, v = Wv t of every layer in one GEMM (into the workspace), then
+  // k normed and rotated and both written into the caches
+  dfl::WideJob kv[dfl::WIDE_MAX_JOBS];
+  dfl::CtxWrite W{};
+  cache_rows(d, seq, W);
+  for (int l = 0; l < g.layers; ++l) {
+    const dflash_layer_weights &L = d->layers[l];
+    float *yk = d->kvs + (size_t)(2 * l) * DFLASH_SETTLE_MAX * kvd, *yv = yk + (size_t)DFLASH_SETTLE_MAX * kvd;
+    W.k[l] = yk;
+    W.v[l] = yv;
+    kv[2 * l] = dfl::WideJob{L.k.data, L.k.scales, yk, kvd, kvd, 0};
+    kv[2 * l + 1] = dfl::WideJob{L.v.data, L.v.scales, yv, kvd, kvd, 0};
+  }
+  DF_CUDA(dfl::wide_gemm(kv, 2 * g.layers, 0, true, g.quant_group, d->x, hs, n, hs, d->act, d->num_sms, st));
+  DF_CUDA(dfl::ctx_planes(W, g.layers, n, g.kv_heads, g.head_dim, d->planes, (float)g.eps, d->inv.data(),
+                           s.first + s.len, s.len, true, st));
+  s.len += n;
+  return DFLASH_OK;
+}
+
+// A run of rows for one settle (`Drafter::settle_rows`): device tap rows.
+struct Seg {
+  const float *taps;
+  int64_t n;
+};
+
+// `Drafter::settle_rows` over the rows of `segs` in order (positions first + len ..),
+// in calls of at most DFLASH_SETTLE_MAX rows, then the window trim.
+int settle_rows(dflash_t *d, int seq, const Seg *segs, int nseg, cudaStream_t st) {
+  const size_t tw = (size_t)d->g.taps * d->g.hidden;
+  for (int i = 0; i < nseg; ++i)
+    for (int64_t r = 0; r < segs[i].n; r += DFLASH_SETTLE_MAX) {
+      const int n = (int)std::min<int64_t>(DFLASH_SETTLE_MAX, segs[i].n - r);
+      if (int e = settle_call(d, seq, segs[i].taps + (size_t)r * tw, n, st)) return e;
+    }
+  window_trim(d, d->seqs[seq]);
+  return DFLASH_OK;
+}
+
+// The `take` oldest waiting rows as up to two runs of the pending ring.
+int pending_segs(const Seq &s, int64_t take, size_t tw, Seg *out) {
+  if (take <= 0) return 0;
+  const int64_t first = std::min(take, s.pcap - s.phead);
+  out[0] = Seg{s.pbuf + (size_t)s.phead * tw, first};
+  if (first == take) return 1;
+  out[1] = Seg{s.pbuf, take - first};
+  return 2;
+}
+
+// `Drafter::queue_context` (queue = true: the rows left under the limit wait in
+// the pending buffer) or `push_context` (queue = false: they settle now).
+int add_context(dflash_t *d, int seq, int64_t pos, const float *taps, int n, bool queue, cudaStream_t st) {
+  Seq &s = d->seqs[seq];
+  const size_t tw = (size_t)d->g.taps * d->g.hidden;
+  const int64_t limit = pending_limit(d->g);
+  Seq after = s;
+  restart_or_truncate(d, after, pos);
+  // rows up to the end of these must fit the linear caches
+  if (!fits(d, pos - after.first + n)) return fail(DFLASH_E_CAPACITY, "context rows do not fit the cache");
+  if (queue && !s.pbuf) return fail(DFLASH_E_ARG, "queue: no pending buffer (dflash_bind_pending)");
+  s = after;
+  int64_t total = s.pcount + n;
+  int64_t used = 0;  // of the new rows
+  if (total > limit) {
+    const int64_t over = std::min((total - limit + CONTEXT_CHUNK - 1) / CONTEXT_CHUNK * CONTEXT_CHUNK, total);
+    Seg segs[3];
+    const int64_t from_pending = std::min(over, s.pcount);
+    int ns = pending_segs(s, from_pending, tw, segs);
+    used = over - from_pending;
+    if (used > 0) segs[ns++] = Seg{taps, used};
+    s.phead = s.pcap ? (s.phead + from_pending) % s.pcap : 0;
+    s.pcount -= from_pending;
+    if (int e = settle_rows(d, seq, segs, ns, st)) return e;
+  }
+  const int64_t rest = n - used;
+  if (!queue) {
+    Seg segs[3];
+    int ns = pending_segs(s, s.pcount, tw, segs);
+    if (rest > 0) segs[ns++] = Seg{taps + (size_t)used * tw, rest};
+    s.pcount = 0;
+    s.phead = 0;
+    return ns ? settle_rows(d, seq, segs, ns, st) : DFLASH_OK;
+  }
+  // the rest wait: copied behind the pending rows (up to two runs of the ring)
+  int64_t done = 0;
+  while (done < rest) {
+    const int64_t slot = (s.phead + s.pcount) % s.pcap;
+    const int64_t m = std::min(rest - done, s.pcap - slot);
+    DF_CUDA(cudaMemcpyAsync(s.pbuf + (size_t)slot * tw, taps + (size_t)(used + done) * tw, (size_t)m * tw * 4,
+                             cudaMemcpyDeviceToDevice, st));
+    s.pcount += m;
+    done += m;
+  }
+  return DFLASH_OK;
 }
 }  // namespace
 
@@ -287,16 +478,47 @@ size_t dflash_workspace_bytes(const dflash_geometry *g, int32_t max_batch) {
   return carve_of(*g, max_batch).total;
 }
 
+int64_t dflash_cache_rows(const dflash_geometry *g, const dflash_cache_config *cache, int32_t layer, int64_t ctx_cap) {
+  if (!g || layer < 0 || layer >= g->layers || layer >= DFLASH_MAX_LAYERS || ctx_cap < 1) return 0;
+  const int64_t C = cache ? cache->ring[layer] : 0;
+  if (C == 0) return ctx_cap;
+  const int64_t w = g->windows[layer];
+  if (w <= 0 || C < 2 * w || C > INT32_MAX / 2) return 0;
+  return C + w;
+}
+
+size_t dflash_cache_bytes(const dflash_geometry *g, const dflash_cache_config *cache, int32_t layer, int64_t ctx_cap) {
+  const int64_t rows = dflash_cache_rows(g, cache, layer, ctx_cap);
+  if (rows == 0) return 0;
+  const int fmt = cache ? cache->format : DFLASH_KV_PLANES;
+  if (fmt != DFLASH_KV_PLANES && fmt != DFLASH_KV_F16) return 0;
+  return (size_t)rows * g->kv_heads * g->head_dim * (fmt == DFLASH_KV_PLANES ? 4 : 2);
+}
+
 int dflash_create(dflash_t **out, const dflash_geometry *g, const dflash_weights *w, int32_t max_batch,
                   void *const *ctx_k, void *const *ctx_v, int64_t ctx_cap, void *workspace,
                   size_t workspace_bytes) {
-  if (!out || !g || !w) return fail(DFLASH_E_ARG, "create: null argument");
+  dflash_cache_config cache{};
+  cache.format = DFLASH_KV_PLANES;
+  return dflash_create_ex(out, g, w, max_batch, &cache, ctx_k, ctx_v, ctx_cap, workspace, workspace_bytes);
+}
+
+int dflash_create_ex(dflash_t **out, const dflash_geometry *g, const dflash_weights *w, int32_t max_batch,
+                     const dflash_cache_config *cache, void *const *ctx_k, void *const *ctx_v, int64_t ctx_cap,
+                     void *workspace, size_t workspace_bytes) {
+  if (!out || !g || !w || !cache) return fail(DFLASH_E_ARG, "create: null argument");
   *out = nullptr;
   const std::string why = check_geometry(*g);
   if (!why.empty()) return fail(DFLASH_E_GEOMETRY, "unsupported DFlash geometry: " + why);
   if (max_batch < 1 || max_batch > dfl::MAX_BATCH) return fail(DFLASH_E_ARG, "create: max_batch must be 1..64");
   if (!ctx_k || !ctx_v || ctx_cap < 1) return fail(DFLASH_E_ARG, "create: context caches");
   if (ctx_cap > INT32_MAX) return fail(DFLASH_E_ARG, "create: ctx_cap must be below 2^31");
+  if (cache->format != DFLASH_KV_PLANES && cache->format != DFLASH_KV_F16)
+    return fail(DFLASH_E_ARG, "create: cache format must be DFLASH_KV_PLANES or DFLASH_KV_F16");
+  for (int l = 0; l < g->layers; ++l)
+    if (dflash_cache_rows(g, cache, l, ctx_cap) == 0)
+      return fail(DFLASH_E_ARG, "create: a ring needs a windowed layer and at least twice its window rows (layer " +
+                                    std::to_string(l) + ")");
   if (!workspace || !aligned16(workspace)) return fail(DFLASH_E_ARG, "create: null or misaligned workspace");
   const Carve c = carve_of(*g, max_batch);
   if (workspace_bytes < c.total) return fail(DFLASH_E_CAPACITY, "create: workspace smaller than dflash_workspace_bytes");
@@ -327,6 +549,11 @@ int dflash_create(dflash_t **out, const dflash_geometry *g, const dflash_weights
     d->cv.push_back((__half *)ctx_v[i]);
   }
   d->cap = ctx_cap;
+  d->planes = cache->format == DFLASH_KV_PLANES ? 2 : 1;
+  for (int l = 0; l < g->layers; ++l) {
+    d->ring[l] = cache->ring[l];
+    d->mirror[l] = cache->ring[l] ? g->windows[l] : 0;
+  }
   d->ws = (char *)workspace;
   d->c = c;
   char *p = d->ws;
@@ -371,59 +598,111 @@ void dflash_destroy(dflash_t *d) { delete d; }
 
 int dflash_reset(dflash_t *d, int32_t seq, int64_t first) {
   if (!d || seq < 0 || seq >= d->max_batch || first < 0) return fail(DFLASH_E_ARG, "reset: bad sequence or position");
-  d->seqs[seq].first = first;
-  d->seqs[seq].len = 0;
+  Seq &s = d->seqs[seq];
+  float *buf = s.pbuf;
+  const int64_t cap = s.pcap;
+  s = Seq{};
+  s.pbuf = buf;
+  s.pcap = cap;
+  s.first = first;
   return DFLASH_OK;
 }
 
 int dflash_context(const dflash_t *d, int32_t seq, int64_t *first, int64_t *len) {
+  return dflash_context_ex(d, seq, first, len, nullptr, nullptr);
+}
+
+int dflash_context_ex(const dflash_t *d, int32_t seq, int64_t *first, int64_t *len, int64_t *pending,
+                      int64_t *dropped) {
   if (!d || seq < 0 || seq >= d->max_batch) return fail(DFLASH_E_ARG, "context: bad sequence");
-  if (first) *first = d->seqs[seq].first;
-  if (len) *len = d->seqs[seq].len;
+  const Seq &s = d->seqs[seq];
+  if (first) *first = s.first;
+  if (len) *len = s.len;
+  if (pending) *pending = s.pcount;
+  if (dropped)
+    for (int l = 0; l < d->g.layers; ++l) dropped[l] = s.dropped[l];
+  return DFLASH_OK;
+}
+
+int64_t dflash_pending_limit(const dflash_geometry *g) {
+  if (!g || g->layers < 1 || g->layers > DFLASH_MAX_LAYERS) return 0;
+  return pending_limit(*g);
+}
+
+int dflash_bind_pending(dflash_t *d, int32_t seq, void *buf, int64_t rows) {
+  if (!d || seq < 0 || seq >= d->max_batch) return fail(DFLASH_E_ARG, "bind_pending: bad sequence");
+  Seq &s = d->seqs[seq];
+  if (buf && (!aligned16(buf) || rows < 1)) return fail(DFLASH_E_ARG, "bind_pending: misaligned buffer or no rows");
+  if (buf && rows < pending_limit(d->g))
+    return fail(DFLASH_E_CAPACITY, "bind_pending: fewer rows than dflash_pending_limit");
+  s.pbuf = (float *)buf;
+  s.pcap = buf ? rows : 0;
+  s.phead = s.pcount = 0;
+  return DFLASH_OK;
+}
+
+static int context_call_checks(dflash_t *d, int32_t seq, int64_t pos, const void *rows, int32_t n, const char *who) {
+  if (!d) return fail(DFLASH_E_ARG, std::string(who) + ": null drafter");
+  if (seq < 0 || seq >= d->max_batch) return fail(DFLASH_E_ARG, std::string(who) + ": bad sequence");
+  if (n < 1 || n > DFLASH_SETTLE_MAX) return fail(DFLASH_E_ARG, std::string(who) + ": 1 to 1024 rows a call");
+  if (pos < 0) return fail(DFLASH_E_ARG, std::string(who) + ": a negative position");
+  if (!rows || ((uintptr_t)rows & 7)) return fail(DFLASH_E_ARG, std::string(who) + ": null or misaligned rows");
   return DFLASH_OK;
 }
 
 int dflash_settle(dflash_t *d, int32_t seq, int64_t pos, const float *taps, int32_t n, void *stream) {
-  if (!d) return fail(DFLASH_E_ARG, "settle: null drafter");
-  if (seq < 0 || seq >= d->max_batch) return fail(DFLASH_E_ARG, "settle: bad sequence");
-  if (n < 1 || n > DFLASH_SETTLE_MAX) return fail(DFLASH_E_ARG, "settle: a settle of 1 to 1024 tap rows");
-  if (!taps || ((uintptr_t)taps & 7)) return fail(DFLASH_E_ARG, "settle: null or misaligned taps");
+  if (int e = context_call_checks(d, seq, pos, taps, n, "settle")) return e;
+  return add_context(d, seq, pos, taps, n, false, (cudaStream_t)stream);
+}
+
+int dflash_queue(dflash_t *d, int32_t seq, int64_t pos, const float *taps, int32_t n, void *stream) {
+  if (int e = context_call_checks(d, seq, pos, taps, n, "queue")) return e;
+  return add_context(d, seq, pos, taps, n, true, (cudaStream_t)stream);
+}
+
+int dflash_settle_pending(dflash_t *d, int32_t seq, void *stream) {
+  if (!d || seq < 0 || seq >= d->max_batch) return fail(DFLASH_E_ARG, "settle_pending: bad sequence");
   Seq &s = d->seqs[seq];
-  if (pos < s.first || pos > s.first + s.len)
-    return fail(DFLASH_E_ARG, "settle: pos must lie in [first, first + len] (reset the sequence for a gap)");
-  const int64_t at = pos - s.first;
-  if (at + n > d->cap) return fail(DFLASH_E_CAPACITY, "settle: context rows do not fit the cache");
+  if (s.pcount == 0) return DFLASH_OK;
+  Seg segs[2];
+  const int ns = pending_segs(s, s.pcount, (size_t)d->g.taps * d->g.hidden, segs);
+  s.pcount = 0;
+  s.phead = 0;
+  return settle_rows(d, seq, segs, ns, (cudaStream_t)stream);
+}
+
+int dflash_truncate(dflash_t *d, int32_t seq, int64_t pos) {
+  if (!d || seq < 0 || seq >= d->max_batch || pos < 0) return fail(DFLASH_E_ARG, "truncate: bad sequence or position");
+  truncate_seq(d, d->seqs[seq], pos);
+  return DFLASH_OK;
+}
+
+int dflash_push_rows(dflash_t *d, int32_t seq, int64_t pos, int32_t n, const float *const *k, const float *const *v,
+                     void *stream) {
+  if (int e = context_call_checks(d, seq, pos, k, n, "push_rows")) return e;
   const dflash_geometry &g = d->g;
+  if (!v) return fail(DFLASH_E_ARG, "push_rows: null rows");
+  for (int l = 0; l < g.layers; ++l)
+    if (!k[l] || !v[l] || ((uintptr_t)k[l] & 7) || ((uintptr_t)v[l] & 7))
+      return fail(DFLASH_E_ARG, "push_rows: a null or misaligned layer's rows");
   cudaStream_t st = (cudaStream_t)stream;
-  const int hs = g.hidden, tw = g.taps * g.hidden, kvd = g.kv_heads * g.head_dim;
-  // t = rms(fc . f16(taps), hidden_norm)
-  const dfl::TcJob fc{d->w.fc.data, nullptr, d->x, hs, hs};
-  DF_CUDA(dfl::tc_gemm_f16(&fc, 1, taps, tw, n, tw, d->act, d->num_sms, st));
-  DF_CUDA(dfl::rmsnorm(d->x, d->w.hidden_norm, d->x, n, hs, (float)g.eps, 1, -1, -1, st));
-  // k = Wk t, v = Wv t of every layer in one GEMM (into the workspace), then
-  // k = rot(rms_head(k, k_norm)) at positions pos.. (rotary layers) and both as
-  // f16 planes into the caches at rows at..at+n-1
-  dfl::WideJob kv[dfl::WIDE_MAX_JOBS];
-  const float *sk[DFLASH_MAX_LAYERS], *sv[DFLASH_MAX_LAYERS];
-  __half *ckp[DFLASH_MAX_LAYERS], *cvp[DFLASH_MAX_LAYERS];
-  const float *kn[DFLASH_MAX_LAYERS];
-  int rot[DFLASH_MAX_LAYERS];
+  Seq &s = d->seqs[seq];
+  Seq after = s;
+  restart_or_truncate(d, after, pos);
+  if (!fits(d, pos - after.first + n)) return fail(DFLASH_E_CAPACITY, "push_rows: context rows do not fit the cache");
+  s = after;
+  // the waiting rows before pos settle first, then the rows are the context's next ones
+  if (int e = dflash_settle_pending(d, seq, stream)) return e;
+  dfl::CtxWrite W{};
+  cache_rows(d, seq, W);
   for (int l = 0; l < g.layers; ++l) {
-    const dflash_layer_weights &L = d->layers[l];
-    float *yk = d->kvs + (size_t)(2 * l) * DFLASH_SETTLE_MAX * kvd, *yv = yk + (size_t)DFLASH_SETTLE_MAX * kvd;
-    sk[l] = yk;
-    sv[l] = yv;
-    ckp[l] = d->ck[(size_t)seq * g.layers + l] + at * 2 * kvd;
-    cvp[l] = d->cv[(size_t)seq * g.layers + l] + at * 2 * kvd;
-    kn[l] = L.k_norm;
-    rot[l] = g.no_rope[l] == 0;
-    kv[2 * l] = dfl::WideJob{L.k.data, L.k.scales, yk, kvd, kvd, 0};
-    kv[2 * l + 1] = dfl::WideJob{L.v.data, L.v.scales, yv, kvd, kvd, 0};
+    W.k[l] = k[l];
+    W.v[l] = v[l];
   }
-  DF_CUDA(dfl::wide_gemm(kv, 2 * g.layers, 0, true, g.quant_group, d->x, hs, n, hs, d->act, d->num_sms, st));
-  DF_CUDA(dfl::ctx_planes(sk, sv, ckp, cvp, kn, rot, g.layers, n, g.kv_heads, g.head_dim, (float)g.eps, d->inv.data(),
-                          pos, st));
-  s.len = at + n;
+  DF_CUDA(dfl::ctx_planes(W, g.layers, n, g.kv_heads, g.head_dim, d->planes, (float)g.eps, d->inv.data(),
+                          s.first + s.len, s.len, false, st));
+  s.len += n;
+  window_trim(d, s);
   return DFLASH_OK;
 }
 
@@ -436,8 +715,11 @@ int dflash_block(dflash_t *d, int32_t batch, const int64_t *anchor_pos, const fl
   if (!anchor_pos || !h || !logits || !hp || ((uintptr_t)h & 15)) return fail(DFLASH_E_ARG, "block: null or misaligned pointer");
   if (k < 1 || k >= R) return fail(DFLASH_E_ARG, "block: k must be 1..block-1");
   if (width < g.selector_top || width > g.vocab) return fail(DFLASH_E_ARG, "block: width must be selector_top..vocab");
-  for (int b = 0; b < batch; ++b)
+  for (int b = 0; b < batch; ++b) {
     if (anchor_pos[b] < 0) return fail(DFLASH_E_ARG, "block: a negative anchor position");
+    if (d->seqs[b].pcount > 0)
+      return fail(DFLASH_E_ARG, "block: rows of sequence " + std::to_string(b) + " wait to be settled");
+  }
   if (!encode_maps(d)) return fail(DFLASH_E_CUDA, "block: the driver could not encode the context caches' tensor maps");
   cudaStream_t st = (cudaStream_t)stream;
   const int T = batch * R;
@@ -451,17 +733,20 @@ int dflash_block(dflash_t *d, int32_t batch, const int64_t *anchor_pos, const fl
   DF_CUDA(cudaMemcpyAsync(d->h, h, (size_t)T * hs * sizeof(float), cudaMemcpyDeviceToDevice, st));
   std::vector<dfl::AttnSeq> seqs(batch);
   auto ranges = [&](int l, int W) {
-    // the layer's context range (src/cortiq_engine/dflash.rs, Drafter::block; no rows dropped)
+    // the layer's context range (src/cortiq_engine/dflash.rs, Drafter::block): the
+    // layer holds positions first + dropped .. first + len; a ring's rows start
+    // at (position - first) % C, and a range (fewer than W rows) runs on into the
+    // rows past the ring that repeat its first ones
     for (int b = 0; b < batch; ++b) {
       const Seq &s = d->seqs[b];
       const int64_t a = anchor_pos[b];
-      const int64_t base = s.first;
+      const int64_t base = s.first + s.dropped[l];
       const int64_t hi = std::max(std::min(a, s.first + s.len), base);
       int64_t lo = base;
       if (W > 0) lo = std::min(std::max(std::max<int64_t>(a + 1 - W, 0), base), hi);
       seqs[b].kmap = d->kmap[(size_t)b * g.layers + l];
       seqs[b].vmap = d->vmap[(size_t)b * g.layers + l];
-      seqs[b].row0 = lo - s.first;
+      seqs[b].row0 = d->ring[l] ? (lo - s.first) % d->ring[l] : lo - s.first;
       seqs[b].n = (int)(hi - lo);
       seqs[b].lo = lo;
       seqs[b].anchor = a;
@@ -510,12 +795,12 @@ int dflash_block(dflash_t *d, int32_t batch, const int64_t *anchor_pos, const fl
                               zero_for(qkv, 3, dfl::tc_splits_int4(qkv, 3, T, hs, sms), T), st));
       DF_CUDA(dfl::tc_gemm_int4_packed(qkv, 3, grp, d->act, T, hs, sms, st));
       DF_CUDA(dfl::qk_norm_rope(d->q, qd, L.q_norm, nh, d->k, kvd, L.k_norm, d->v, kvd, kv, d->kp, d->vp,
-                                d->inv.data(), T, hd, eps, rot, anchor_pos, batch, R, st));
+                                d->inv.data(), T, hd, eps, rot, anchor_pos, batch, R, d->planes, st));
       ranges(l, W);
       const dfl::PackDst po = pack_for(2, ti, qd);
       const dfl::ZeroSet zo = zero_for(&oj, 1, dfl::tc_splits_int4(&oj, 1, T, qd, sms), T);
-      DF_CUDA(dfl::attention(d->q, d->own_k, d->own_v, seqs.data(), batch, nh, kv, hd, R, W, scale, d->part, d->y,
-                             sms, &po, &zo, st));
+      DF_CUDA(dfl::attention(d->q, d->own_k, d->own_v, seqs.data(), batch, nh, kv, hd, d->planes, R, W, scale,
+                             d->part, d->y, sms, &po, &zo, st));
       DF_CUDA(dfl::tc_gemm_int4_packed(&oj, 1, grp, d->act, T, qd, sms, st));
       // h += conv_out(o, d); x = norm(h); the MLP the same way
       DF_CUDA(dfl::rms_pack(d->h, d->o, d->d, L.attn_base, kn, gs, L.post_norm, d->x, T, hs, eps, R, -1, -1,
@@ -564,10 +849,10 @@ int dflash_block(dflash_t *d, int32_t batch, const int64_t *anchor_pos, const fl
                                {L.v.data, L.v.scales, d->v, kvd, kvd}};
     DF_CUDA(dfl::tc_gemm_int4(qkv, 3, grp, d->xc, hs, T, hs, d->act, sms, st));
     DF_CUDA(dfl::qk_norm_rope(d->q, qd, L.q_norm, nh, d->k, kvd, L.k_norm, d->v, kvd, kv, d->kp, d->vp,
-                              d->inv.data(), T, hd, eps, rot, anchor_pos, batch, R, st));
+                              d->inv.data(), T, hd, eps, rot, anchor_pos, batch, R, d->planes, st));
     ranges(l, W);
-    DF_CUDA(dfl::attention(d->q, d->own_k, d->own_v, seqs.data(), batch, nh, kv, hd, R, W, scale, d->part, d->y, sms,
-                           nullptr, nullptr, st));
+    DF_CUDA(dfl::attention(d->q, d->own_k, d->own_v, seqs.data(), batch, nh, kv, hd, d->planes, R, W, scale, d->part,
+                           d->y, sms, nullptr, nullptr, st));
     const dfl::TcJob oj{L.o.data, L.o.scales, d->o, hs, hs};
     DF_CUDA(dfl::tc_gemm_int4(&oj, 1, grp, d->y, qd, T, qd, d->act, sms, st));
     DF_CUDA(dfl::conv_stage1_residual(d->o, d->d, L.attn_base, d->h, T, hs, kn, gs, R, st));

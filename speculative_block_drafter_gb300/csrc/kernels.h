@@ -167,14 +167,21 @@ cudaError_t conv_stage0(const float *x, const float *d, const float *base, float
 cudaError_t conv_stage1_residual(const float *x, const float *d, const float *base, float *h, int T, int hs,
                                  int kn, int gs, int block, cudaStream_t st);
 constexpr int MAX_BATCH = 64;
-// The settle's K and V of every layer into the context caches as f16 planes
-// (per row and head: hi[hd] then lo[hd], hi + lo carrying about 21 bits): K
-// normalised per head and, on rotary layers, rotated to pos_base + t. k/v[l]
-// are the settle's rows [T][heads][hd] f32, ck/cv[l] the cache rows they go
-// to; host arrays of `nlayers` (w: k norms, rotary flags), passed by value.
-cudaError_t ctx_planes(const float *const *k, const float *const *v, __half *const *ck, __half *const *cv,
-                       const float *const *w, const int *rotary, int nlayers, int T, int heads, int hd, float eps,
-                       const float *inv_freq, int64_t pos_base, cudaStream_t st);
+// K and V rows of every layer into the context caches, in the cache format
+// (planes = 2: per row and head hi[hd] then lo[hd], hi + lo carrying about 21
+// bits; planes = 1: one f16 per element). With `norm`, K is normalised per head
+// and, on rotary layers, rotated to pos_base + t (a settle); without, the rows
+// are taken as they are (imported rows). Row t goes to cache row at + t, or for
+// a ring of C rows to (at + t) % C (also C rows further on when below the
+// layer's mirror); k/v[l] are f32 [T][heads][hd].
+struct CtxWrite {
+  const float *k[64], *v[64];
+  __half *ck[64], *cv[64];
+  const float *w[64];
+  int rotary[64], ring[64], mirror[64];
+};
+cudaError_t ctx_planes(const CtxWrite &W, int nlayers, int T, int heads, int hd, int planes, float eps,
+                       const float *inv_freq, int64_t pos_base, int64_t at, bool norm, cudaStream_t st);
 // Fused producers of a GEMM's packed token tiles (rows.cu). Each writes its
 // result into P (the following GEMM's token tiles) and clears Z (that GEMM's
 // outputs, when it splits its k-range).
@@ -189,20 +196,21 @@ cudaError_t conv0_pack(const float *x, const float *d, const float *base, int T,
 cudaError_t silu_pack(const float *g, const float *u, int T, int n, const PackDst &P, const ZeroSet &Z,
                       cudaStream_t st);
 // The block's q, k and v, one launch: q normalised per head and rotated to
-// pos0[t / block] + t % block in place; k the same and v as it is, written as
-// f16 planes [T][hk][2][hd] to kp and vp (the attention's format).
+// pos0[t / block] + t % block in place; k the same and v as it is, written in
+// the cache format [T][hk][planes][hd] to kp and vp (the attention's format).
 cudaError_t qk_norm_rope(float *q, int ldq, const float *wq, int hq, const float *k, int ldk, const float *wk,
                          const float *v, int ldv, int hk, __half *kp, __half *vp, const float *inv_freq, int T, int hd,
-                         float eps, bool rotary, const int64_t *pos0, int nseq, int block, cudaStream_t st);
+                         float eps, bool rotary, const int64_t *pos0, int nseq, int block, int planes,
+                         cudaStream_t st);
 // m = silu(g) * u, elementwise over n values.
 cudaError_t silu_mul(const float *g, const float *u, float *m, int64_t n, cudaStream_t st);
 
 // -------------------------------------------------------------- attention (attention.cu)
-// The kernel loads K and V with tensor copies: a cache of f16 planes
-// [rows][kv][2][hd] (per row and head: hi[hd], lo[hd]) is described by a map
-// of boxes of 64 halves x 1 plane x 1 head x `box_rows` rows, 128-byte
-// swizzled. Encoding is host-only work; false if the driver cannot.
-bool attn_kv_map(CUtensorMap *m, const void *base, int64_t rows, int kv, int hd, int box_rows);
+// The kernel loads K and V with tensor copies: a cache of f16 values
+// [rows][kv][planes][hd] (per row and head: hi[hd], lo[hd] for two planes) is
+// described by a map of boxes of 64 halves x 1 plane x 1 head x `box_rows`
+// rows, 128-byte swizzled. Encoding is host-only work; false if the driver cannot.
+bool attn_kv_map(CUtensorMap *m, const void *base, int64_t rows, int kv, int hd, int planes, int box_rows);
 struct AttnSeq {          // per sequence and layer
   CUtensorMap kmap, vmap; // the layer's K and V cache of the sequence (box_rows 64)
   int64_t row0;           // cache row of the first context row read
@@ -217,8 +225,9 @@ size_t attn_partial_bytes(int max_batch, int kv_heads, int heads, int block, int
 // into those token tiles (for the output projection; `zero` its outputs to
 // clear) instead of y.
 cudaError_t attention(const float *q, const CUtensorMap &own_k, const CUtensorMap &own_v, const AttnSeq *seqs,
-                      int batch, int heads, int kv_heads, int hd, int block, int window, float scale, float *partials,
-                      float *y, int num_sms, const PackDst *pack, const ZeroSet *zero, cudaStream_t st);
+                      int batch, int heads, int kv_heads, int hd, int planes, int block, int window, float scale,
+                      float *partials, float *y, int num_sms, const PackDst *pack, const ZeroSet *zero,
+                      cudaStream_t st);
 
 // -------------------------------------------------------------- selector (select.cu)
 size_t select_scratch_bytes(int max_rows, int width, int top);

@@ -184,45 +184,54 @@ __device__ __forceinline__ void norm_rope_head(float *__restrict__ p, const floa
 }
 
 // This file's device error word: DFL_ERR_RANGE when a K or V value written to
-// a cache's planes was not finite or at least 65,536 in magnitude (its hi
-// plane then holds infinity).
+// a cache was not finite or beyond the range of the cache's f16 values (it
+// then reads as infinity).
 static __device__ unsigned int g_rows_error = 0;
 
-// A head row as f16 planes (the attention's K/V format): hi[i] = f16 of x with
-// its low 13 mantissa bits cleared (exact below 65,536 in magnitude), lo[i] =
-// f16(x - that); hi + lo carries about 21 bits of x. dst holds hi[0..HD) then
-// lo[0..HD). `bad` is set where x is out of the planes' range.
-__device__ __forceinline__ void plane_pair(float x, __half &h, __half &l, bool &bad) {
-  const float t = __uint_as_float(__float_as_uint(x) & 0xFFFFE000u);
-  h = __float2half_rn(t);
-  l = __float2half_rn(x - t);
-  bad |= !(fabsf(x) < 65536.f);
+// The cache formats (per row and KV head). PL = 2: two f16 planes, hi[HD] then
+// lo[HD], hi = x with its low 13 mantissa bits cleared (exact below 65,536 in
+// magnitude), lo = f16(x - hi); hi + lo carries about 21 bits of x. PL = 1:
+// one f16 plane, f16(x) rounded to nearest (11 bits; infinite from 65,520).
+template <int PL>
+__device__ __forceinline__ void kv_pair(float x, __half &h, __half &l, bool &bad) {
+  if constexpr (PL == 2) {
+    const float t = __uint_as_float(__float_as_uint(x) & 0xFFFFE000u);
+    h = __float2half_rn(t);
+    l = __float2half_rn(x - t);
+    bad |= !(fabsf(x) < 65536.f);
+  } else {
+    h = __float2half_rn(x);
+    bad |= !(fabsf(x) < 65520.f);
+  }
 }
 __device__ __forceinline__ void flag_range(bool bad) {
   if (bad) atomicOr(&g_rows_error, DFL_ERR_RANGE);
 }
-template <int HD>
-__device__ __forceinline__ void store_planes(__half *__restrict__ dst, const float (&lo)[HD / 64],
-                                             const float (&hi)[HD / 64], int lane) {
+// A head row into the cache format at dst (lane owns i = lane + 32m and i + HD/2).
+template <int HD, int PL>
+__device__ __forceinline__ void store_kv(__half *__restrict__ dst, const float (&lo)[HD / 64],
+                                         const float (&hi)[HD / 64], int lane) {
   bool bad = false;
 #pragma unroll
   for (int m = 0; m < HD / 64; ++m) {
     __half h, l;
-    plane_pair(lo[m], h, l, bad);
+    kv_pair<PL>(lo[m], h, l, bad);
     dst[lane + 32 * m] = h;
-    dst[HD + lane + 32 * m] = l;
-    plane_pair(hi[m], h, l, bad);
+    if (PL == 2) dst[HD + lane + 32 * m] = l;
+    kv_pair<PL>(hi[m], h, l, bad);
     dst[lane + 32 * m + HD / 2] = h;
-    dst[HD + lane + 32 * m + HD / 2] = l;
+    if (PL == 2) dst[HD + lane + 32 * m + HD / 2] = l;
   }
   flag_range(bad);
 }
 
 struct CtxPlanes {
-  const float *k[64], *v[64];   // the settle's K and V of each layer, f32 [T][heads][HD]
-  __half *ck[64], *cv[64];      // the cache rows they go to, planes [T][heads][2][HD]
+  const float *k[64], *v[64];   // per layer f32 [T][heads][HD]: the settle's K and V, or imported rows
+  __half *ck[64], *cv[64];      // per layer: the cache (row r at ck + r * heads * PL * HD)
   const float *w[64];           // k norms
   int rotary[64];
+  int ring[64];                 // 0: a linear cache (row = at + t); else the ring's rows C
+  int mirror[64];               // ring rows below this are also written C rows further on
   float inv[64];
 };
 
@@ -249,20 +258,45 @@ __device__ __forceinline__ void store_e(__half *p, const __half (&v)[E]) {
   }
 }
 
-// One warp per (row, head) of layer blockIdx.y: the head's K normalised and
-// rotated to pos_base + t, then its K and V written to the cache as f16 planes
-// (plane_pair). A lane holds E = HD/64 consecutive elements of each half of
-// the head, i = E*lane + j and i + HD/2 (the rotation's pairs), so that its
-// loads and stores are vectors and both rows' loads are in flight together.
-template <int HD>
-__global__ void k_ctx_planes(CtxPlanes P, int T, int heads, float eps, int64_t pos_base) {
+// E consecutive elements of each half of a head into the cache format at dst.
+template <int HD, int PL, int E>
+__device__ __forceinline__ void store_kv_e(__half *__restrict__ dst, const float (&x0)[E], const float (&x1)[E], int i0,
+                                           bool &bad) {
+  __half h[E], l[E];
+#pragma unroll
+  for (int j = 0; j < E; ++j) kv_pair<PL>(x0[j], h[j], l[j], bad);
+  store_e<E>(dst + i0, h);
+  if (PL == 2) store_e<E>(dst + HD + i0, l);
+#pragma unroll
+  for (int j = 0; j < E; ++j) kv_pair<PL>(x1[j], h[j], l[j], bad);
+  store_e<E>(dst + HD / 2 + i0, h);
+  if (PL == 2) store_e<E>(dst + HD + HD / 2 + i0, l);
+}
+
+// One warp per (row t, head) of layer blockIdx.y: with `norm`, the head's K
+// normalised and rotated to pos_base + t (a settle); without, K taken as given
+// (imported rows); then K and V into the cache row at + t, or, for a ring of C
+// rows, into row (at + t) % C (and C rows further on when that is below the
+// layer's mirror). In a ring, rows that a later row of the same call replaces
+// (t < T - C) are not written, so that no two warps write one row. A lane
+// holds E = HD/64 consecutive elements of each half of the head, i = E*lane + j
+// and i + HD/2 (the rotation's pairs), so that its loads and stores are vectors
+// and both rows' loads are in flight together.
+template <int HD, int PL>
+__global__ void k_ctx_planes(CtxPlanes P, int T, int heads, float eps, int64_t pos_base, int64_t at, int norm) {
   pdl_wait();
   constexpr int E = HD / 64;
   const int wid = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (wid >= T * heads) return;
   const int l = blockIdx.y;
-  const int t = wid / heads;
+  const int t = wid / heads, hh = wid - t * heads;
+  const int C = P.ring[l];
+  int64_t row = at + t;
+  if (C > 0) {
+    if (t < T - C) return;
+    row %= C;
+  }
   const int64_t off = (int64_t)wid * HD;  // (t * heads + h) * HD
   const int i0 = E * lane;
   float k0[E], k1[E], v0[E], v1[E];
@@ -270,80 +304,78 @@ __global__ void k_ctx_planes(CtxPlanes P, int T, int heads, float eps, int64_t p
   load_e<E>(P.k[l] + off + HD / 2 + i0, k1);
   load_e<E>(P.v[l] + off + i0, v0);
   load_e<E>(P.v[l] + off + HD / 2 + i0, v1);
-  float w0[E], w1[E];  // the norm's weights: plain loads (the caller's vector is only 4-byte aligned)
-#pragma unroll
-  for (int j = 0; j < E; ++j) {
-    w0[j] = P.w[l][i0 + j];
-    w1[j] = P.w[l][HD / 2 + i0 + j];
-  }
-  // K: the per-head RMS norm, then the rotation
-  float ss = 0.f;
-#pragma unroll
-  for (int j = 0; j < E; ++j) {
-    ss = fmaf(k0[j], k0[j], ss);
-    ss = fmaf(k1[j], k1[j], ss);
-  }
-  ss = warp_sum(ss);
-  const float s = 1.0f / sqrtf(ss / (float)HD + eps);
-#pragma unroll
-  for (int j = 0; j < E; ++j) {
-    k0[j] = k0[j] * s * w0[j];
-    k1[j] = k1[j] * s * w1[j];
-  }
-  if (P.rotary[l]) {
-    const float fp = (float)(pos_base + t);
+  if (norm) {
+    float w0[E], w1[E];  // the norm's weights: plain loads (the caller's vector is only 4-byte aligned)
 #pragma unroll
     for (int j = 0; j < E; ++j) {
-      const float ang = __fmul_rn(fp, P.inv[i0 + j]);
-      float sn, cs;
-      sincosf(ang, &sn, &cs);
-      const float a = k0[j], b = k1[j];
-      k0[j] = a * cs - b * sn;
-      k1[j] = b * cs + a * sn;
+      w0[j] = P.w[l][i0 + j];
+      w1[j] = P.w[l][HD / 2 + i0 + j];
+    }
+    // K: the per-head RMS norm, then the rotation
+    float ss = 0.f;
+#pragma unroll
+    for (int j = 0; j < E; ++j) {
+      ss = fmaf(k0[j], k0[j], ss);
+      ss = fmaf(k1[j], k1[j], ss);
+    }
+    ss = warp_sum(ss);
+    const float s = 1.0f / sqrtf(ss / (float)HD + eps);
+#pragma unroll
+    for (int j = 0; j < E; ++j) {
+      k0[j] = k0[j] * s * w0[j];
+      k1[j] = k1[j] * s * w1[j];
+    }
+    if (P.rotary[l]) {
+      const float fp = (float)(pos_base + t);
+#pragma unroll
+      for (int j = 0; j < E; ++j) {
+        const float ang = __fmul_rn(fp, P.inv[i0 + j]);
+        float sn, cs;
+        sincosf(ang, &sn, &cs);
+        const float a = k0[j], b = k1[j];
+        k0[j] = a * cs - b * sn;
+        k1[j] = b * cs + a * sn;
+      }
     }
   }
-  // planes: dst[i] = hi of element i, dst[HD + i] = lo of element i
-  __half *ck = P.ck[l] + 2 * off, *cv = P.cv[l] + 2 * off;
-  __half h[E], lo[E];
   bool bad = false;
-#pragma unroll
-  for (int j = 0; j < E; ++j) plane_pair(k0[j], h[j], lo[j], bad);
-  store_e<E>(ck + i0, h);
-  store_e<E>(ck + HD + i0, lo);
-#pragma unroll
-  for (int j = 0; j < E; ++j) plane_pair(k1[j], h[j], lo[j], bad);
-  store_e<E>(ck + HD / 2 + i0, h);
-  store_e<E>(ck + HD + HD / 2 + i0, lo);
-#pragma unroll
-  for (int j = 0; j < E; ++j) plane_pair(v0[j], h[j], lo[j], bad);
-  store_e<E>(cv + i0, h);
-  store_e<E>(cv + HD + i0, lo);
-#pragma unroll
-  for (int j = 0; j < E; ++j) plane_pair(v1[j], h[j], lo[j], bad);
-  store_e<E>(cv + HD / 2 + i0, h);
-  store_e<E>(cv + HD + HD / 2 + i0, lo);
+  for (int copy = 0; copy < 2; ++copy) {
+    const int64_t r = row + (int64_t)copy * C;
+    const int64_t dst = (r * heads + hh) * PL * HD;
+    store_kv_e<HD, PL, E>(P.ck[l] + dst, k0, k1, i0, bad);
+    store_kv_e<HD, PL, E>(P.cv[l] + dst, v0, v1, i0, bad);
+    if (C == 0 || row >= P.mirror[l]) break;
+  }
   flag_range(bad);
 }
 
-cudaError_t ctx_planes(const float *const *k, const float *const *v, __half *const *ck, __half *const *cv,
-                       const float *const *w, const int *rotary, int nlayers, int T, int heads, int hd, float eps,
-                       const float *inv_freq, int64_t pos_base, cudaStream_t st) {
+cudaError_t ctx_planes(const CtxWrite &W, int nlayers, int T, int heads, int hd, int planes, float eps,
+                       const float *inv_freq, int64_t pos_base, int64_t at, bool norm, cudaStream_t st) {
   if (T <= 0) return cudaSuccess;
-  if (nlayers < 1 || nlayers > 64) return cudaErrorInvalidValue;
+  if (nlayers < 1 || nlayers > 64 || (planes != 1 && planes != 2)) return cudaErrorInvalidValue;
   CtxPlanes P{};
   for (int l = 0; l < nlayers; ++l) {
-    P.k[l] = k[l];
-    P.v[l] = v[l];
-    P.ck[l] = ck[l];
-    P.cv[l] = cv[l];
-    P.w[l] = w[l];
-    P.rotary[l] = rotary[l];
+    P.k[l] = W.k[l];
+    P.v[l] = W.v[l];
+    P.ck[l] = W.ck[l];
+    P.cv[l] = W.cv[l];
+    P.w[l] = W.w[l];
+    P.rotary[l] = W.rotary[l];
+    P.ring[l] = W.ring[l];
+    P.mirror[l] = W.mirror[l];
   }
   for (int i = 0; i < 64; ++i) P.inv[i] = i < hd / 2 ? inv_freq[i] : 0.f;
   const int warps = T * heads;
   dim3 grid((unsigned)((warps * 32 + 255) / 256), nlayers);
-  if (hd == 128) return launch_pdl(k_ctx_planes<128>, grid, dim3(256), 0, st, 1, P, T, heads, eps, pos_base);
-  if (hd == 64) return launch_pdl(k_ctx_planes<64>, grid, dim3(256), 0, st, 1, P, T, heads, eps, pos_base);
+  const int nm = norm ? 1 : 0;
+  if (hd == 128 && planes == 2)
+    return launch_pdl(k_ctx_planes<128, 2>, grid, dim3(256), 0, st, 1, P, T, heads, eps, pos_base, at, nm);
+  if (hd == 128)
+    return launch_pdl(k_ctx_planes<128, 1>, grid, dim3(256), 0, st, 1, P, T, heads, eps, pos_base, at, nm);
+  if (hd == 64 && planes == 2)
+    return launch_pdl(k_ctx_planes<64, 2>, grid, dim3(256), 0, st, 1, P, T, heads, eps, pos_base, at, nm);
+  if (hd == 64)
+    return launch_pdl(k_ctx_planes<64, 1>, grid, dim3(256), 0, st, 1, P, T, heads, eps, pos_base, at, nm);
   return cudaErrorInvalidValue;
 }
 
@@ -536,9 +568,9 @@ __global__ void __launch_bounds__(FP_THREADS) k_silu_pack(const float *__restric
 }
 
 // The block's q, k and v in one launch: q normalised and rotated in place; k
-// normalised and rotated, and v as it is, written as f16 planes [T][hk][2][HD]
-// (the attention's format) to kp and vp.
-template <int HD>
+// normalised and rotated, and v as it is, written in the cache format
+// [T][hk][PL][HD] (the attention's format) to kp and vp.
+template <int HD, int PL>
 __global__ void k_qk_norm_rope(float *__restrict__ q, int ldq, const float *__restrict__ wq, int hq,
                                const float *__restrict__ k, int ldk, const float *__restrict__ wk,
                                const float *__restrict__ v, int ldv, int hk, __half *__restrict__ kp,
@@ -566,7 +598,7 @@ __global__ void k_qk_norm_rope(float *__restrict__ q, int ldq, const float *__re
     hi[m] = src[lane + 32 * m + HD / 2];
   }
   if (kind == 1) norm_rope_regs<HD>(lo, hi, wk, eps, rotary != 0, pos, pa.inv, lane);
-  store_planes<HD>((kind == 1 ? kp : vp) + ((int64_t)t * hk + h) * 2 * HD, lo, hi, lane);
+  store_kv<HD, PL>((kind == 1 ? kp : vp) + ((int64_t)t * hk + h) * PL * HD, lo, hi, lane);
 }
 
 static unsigned zero_blocks_for(const ZeroSet &Z) {
@@ -604,19 +636,20 @@ cudaError_t silu_pack(const float *g, const float *u, int T, int n, const PackDs
 
 cudaError_t qk_norm_rope(float *q, int ldq, const float *wq, int hq, const float *k, int ldk, const float *wk,
                          const float *v, int ldv, int hk, __half *kp, __half *vp, const float *inv_freq, int T, int hd,
-                         float eps, bool rotary, const int64_t *pos0, int nseq, int block, cudaStream_t st) {
+                         float eps, bool rotary, const int64_t *pos0, int nseq, int block, int planes,
+                         cudaStream_t st) {
   if (T <= 0) return cudaSuccess;
+  if (planes != 1 && planes != 2) return cudaErrorInvalidValue;
   PosArgs pa;
   for (int i = 0; i < MAX_BATCH; ++i) pa.pos0[i] = (pos0 && i < nseq) ? pos0[i] : 0;
   for (int i = 0; i < 64; ++i) pa.inv[i] = i < hd / 2 ? inv_freq[i] : 0.f;
   const int warps = T * (hq + 2 * hk);
   const unsigned grid = (unsigned)((warps * 32 + 255) / 256);
-  if (hd == 128)
-    return launch_pdl(k_qk_norm_rope<128>, dim3(grid), dim3(256), 0, st, 1, q, ldq, wq, hq, k, ldk, wk, v, ldv, hk,
-                      kp, vp, T, eps, (int)rotary, pa, block);
-  if (hd == 64)
-    return launch_pdl(k_qk_norm_rope<64>, dim3(grid), dim3(256), 0, st, 1, q, ldq, wq, hq, k, ldk, wk, v, ldv, hk, kp,
-                      vp, T, eps, (int)rotary, pa, block);
+  auto kern = hd == 128 ? (planes == 2 ? k_qk_norm_rope<128, 2> : k_qk_norm_rope<128, 1>)
+                        : (planes == 2 ? k_qk_norm_rope<64, 2> : k_qk_norm_rope<64, 1>);
+  if (hd == 128 || hd == 64)
+    return launch_pdl(kern, dim3(grid), dim3(256), 0, st, 1, q, ldq, wq, hq, k, ldk, wk, v, ldv, hk, kp, vp, T, eps,
+                      (int)rotary, pa, block);
   return cudaErrorInvalidValue;
 }
 

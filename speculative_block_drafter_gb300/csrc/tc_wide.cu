@@ -507,6 +507,8 @@ __global__ void k_wide_pack(const float *__restrict__ X, int ldx, WideArgs A, in
 
 // Runs of at least this many units: a run ends with a read-back of its accumulator.
 constexpr int W_MIN_RUN = 4;
+// What a run's read-back and atomic add of its partial sums cost, in units.
+constexpr int W_RUN_COST = 6;
 
 template <int KIND, int DU>
 static cudaError_t launch_wide(WideArgs &A, const float *X, int ldx, void *act, int num_sms, cudaStream_t st) {
@@ -526,16 +528,20 @@ static cudaError_t launch_wide(WideArgs &A, const float *X, int ldx, void *act, 
     resident.slot[dev].store(max_ctas, std::memory_order_release);
   }
   A.units = (int64_t)A.ntt * A.mtiles * A.KT;
-  // With no more (token tile, row tile) tiles than resident CTAs but enough of
-  // them, each CTA takes one tile over its whole k-range: more units a CTA
-  // than an even split, but no split tile (no clearing of Y, no second
-  // read-back, plain stores instead of atomics). Measured: four-bit gains from
-  // 1/8 of the resident CTAs on (a four-bit unit is three MMAs a k-step); f16
-  // only from 3/4 on.
+  // With no more (token tile, row tile) tiles than resident CTAs, each CTA may
+  // take one tile over its whole k-range: no split tile (no clearing of Y, no
+  // second read-back, plain stores instead of atomics), but KT units a CTA.
+  // An even split costs units / Q a CTA plus, for each run it holds, a
+  // read-back and atomic add of the run's partial sums, worth about W_RUN_COST
+  // units. The cheaper one is taken (measured: whole tiles for the 0.6B K/V
+  // and the batched projections, k-ranges of 16; split for the FCs and the
+  // 27B K/V, k-ranges of 80 to 400).
   const int64_t tiles = (int64_t)A.ntt * A.mtiles;
-  const bool whole = tiles <= max_ctas && (KIND == W_KIND_I4 ? 8 * tiles >= (int64_t)max_ctas
-                                                              : 4 * tiles >= 3 * (int64_t)max_ctas);
-  const int Q = whole ? (int)tiles : (int)std::max<int64_t>(1, std::min<int64_t>(max_ctas, A.units / W_MIN_RUN));
+  const int64_t q_split = std::max<int64_t>(1, std::min<int64_t>(max_ctas, A.units / W_MIN_RUN));
+  const int64_t per = (A.units + q_split - 1) / q_split;
+  const int64_t split_cost = per + W_RUN_COST * (1 + (per + A.KT - 1) / A.KT);
+  const bool whole = tiles <= max_ctas && A.KT <= split_cost;
+  const int Q = whole ? (int)tiles : (int)q_split;
   const int64_t chunks = (int64_t)A.ntt * A.KT * A.N * 8;
   const int pack_blocks = (int)((chunks + 255) / 256);
   const int zero_blocks = whole ? 0 : (Q - 1) * WZ_PARTS;

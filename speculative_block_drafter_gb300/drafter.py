@@ -34,11 +34,25 @@ def _stream() -> int:
 
 
 class Drafter:
-    def __init__(self, g, weights: dict, max_batch: int = 1, ctx_cap: int = 4096, device: str = "cuda"):
+    """``cache_format``: "planes" (two f16 planes an element, about 21 bits) or "f16" (one f16).
+    ``rings``: None (linear caches of ``ctx_cap`` rows), "window" (every windowed layer a ring
+    of twice its window rows) or a list of ring rows per layer (0 = linear)."""
+
+    def __init__(self, g, weights: dict, max_batch: int = 1, ctx_cap: int = 4096, device: str = "cuda",
+                 cache_format: str = "planes", rings=None):
         self.g = g
         self.dev = torch.device(device)
         self.max_batch = max_batch
         self.ctx_cap = ctx_cap
+        self.cache = L.CacheConfig()
+        self.cache.format = {"planes": L.KV_PLANES, "f16": L.KV_F16}[cache_format]
+        self.planes = 2 if cache_format == "planes" else 1
+        if rings == "window":
+            rings = [2 * g.windows[l] for l in range(g.layers)]
+        for l, r in enumerate(rings or []):
+            self.cache.ring[l] = int(r)
+        self.rings = [int(self.cache.ring[l]) for l in range(g.layers)]
+        self._pending = {}
         self._keep: List[torch.Tensor] = []
         self.geom = geometry_struct(g)
         st = _stream()
@@ -96,13 +110,16 @@ class Drafter:
         w.layers = C.cast(layers, C.POINTER(L.LayerWeights))
         self._weights = w
 
-        # the caches: ctx_cap x kv x hd x 4 bytes each, holding per (position, head)
-        # the f16 planes hi[hd] then lo[hd] of the K/V values (context_kv decodes them)
+        # the caches: per (position, head) the f16 planes hi[hd] then lo[hd], or one
+        # f16[hd] (held_kv decodes them); a ring layer's rows past the ring repeat its first ones
         kv, hd = g.kv_heads, g.head_dim
-        self.ctx_k = [[torch.zeros(ctx_cap, kv, 2, hd, dtype=torch.float16, device=self.dev) for _ in range(g.layers)]
-                      for _ in range(max_batch)]
-        self.ctx_v = [[torch.zeros(ctx_cap, kv, 2, hd, dtype=torch.float16, device=self.dev) for _ in range(g.layers)]
-                      for _ in range(max_batch)]
+        rows = [L.dflash_cache_rows(self.geom, self.cache, l, ctx_cap) for l in range(g.layers)]
+        if not all(rows):
+            raise ValueError("a ring needs a windowed layer and at least twice its window rows")
+        self.ctx_k = [[torch.zeros(rows[l], kv, self.planes, hd, dtype=torch.float16, device=self.dev)
+                       for l in range(g.layers)] for _ in range(max_batch)]
+        self.ctx_v = [[torch.zeros(rows[l], kv, self.planes, hd, dtype=torch.float16, device=self.dev)
+                       for l in range(g.layers)] for _ in range(max_batch)]
         ks = [t.data_ptr() for row in self.ctx_k for t in row]
         vs = [t.data_ptr() for row in self.ctx_v for t in row]
         self.ws_bytes = L.dflash_workspace_bytes(self.geom, max_batch)
@@ -111,8 +128,8 @@ class Drafter:
         self.workspace = torch.empty(self.ws_bytes, dtype=torch.uint8, device=self.dev)
         torch.cuda.synchronize()
         del tmp
-        self.h = L.dflash_create(self.geom, self._weights, max_batch, ks, vs, ctx_cap, self.workspace.data_ptr(),
-                                 self.ws_bytes)
+        self.h = L.dflash_create_ex(self.geom, self._weights, max_batch, self.cache, ks, vs, ctx_cap,
+                                    self.workspace.data_ptr(), self.ws_bytes)
 
     # ------------------------------------------------------------------ calls
     def reset(self, seq: int = 0, first: int = 0):
@@ -121,10 +138,52 @@ class Drafter:
     def context(self, seq: int = 0):
         return L.dflash_context(self.h, seq)
 
+    def context_ex(self, seq: int = 0):
+        """(first, len, pending rows, dropped rows per layer)."""
+        return L.dflash_context_ex(self.h, seq, self.g.layers)
+
+    def held_kv(self, seq: int, layer: int):
+        """The K and V rows layer `layer` of `seq` holds (positions first + dropped .. first + len),
+        decoded to f32 [rows][kv][hd] (hi + lo of the planes, or the f16 values)."""
+        _, n, _, dropped = self.context_ex(seq)
+        idx = torch.arange(dropped[layer], n, device=self.dev)
+        if self.rings[layer]:
+            idx = idx % self.rings[layer]
+        k, v = self.ctx_k[seq][layer][idx].float(), self.ctx_v[seq][layer][idx].float()
+        return k.sum(dim=2), v.sum(dim=2)
+
     def context_kv(self, seq: int, layer: int, n: int):
-        """The first n cached K and V rows of (seq, layer) as f32 [n][kv][hd]: hi + lo of the planes."""
+        """The first n cached K and V rows of (seq, layer) of a linear cache with nothing dropped."""
         k, v = self.ctx_k[seq][layer][:n].float(), self.ctx_v[seq][layer][:n].float()
-        return k[:, :, 0] + k[:, :, 1], v[:, :, 0] + v[:, :, 1]
+        return k.sum(dim=2), v.sum(dim=2)
+
+    def bind_pending(self, seq: int, rows: Optional[int] = None):
+        """A pending buffer for `seq` of `rows` tap rows (default: the pending limit)."""
+        rows = L.dflash_pending_limit(self.geom) if rows is None else rows
+        buf = torch.empty(rows, self.g.taps * self.g.hidden, dtype=torch.float32, device=self.dev)
+        L.dflash_bind_pending(self.h, seq, buf.data_ptr(), rows)
+        self._pending[seq] = buf
+
+    def queue(self, seq: int, pos: int, taps: torch.Tensor, chunk: int = L.SETTLE_MAX):
+        """Queue tap rows [n][tw] (device f32) at positions pos.., `chunk` rows a call."""
+        assert taps.dtype == torch.float32 and taps.is_cuda and taps.is_contiguous()
+        st = _stream()
+        for i in range(0, taps.shape[0], chunk):
+            m = min(chunk, taps.shape[0] - i)
+            L.dflash_queue(self.h, seq, pos + i, taps[i:i + m].data_ptr(), m, st)
+
+    def settle_pending(self, seq: int):
+        L.dflash_settle_pending(self.h, seq, _stream())
+
+    def truncate(self, seq: int, pos: int):
+        L.dflash_truncate(self.h, seq, pos)
+
+    def push_rows(self, seq: int, pos: int, k: Sequence[torch.Tensor], v: Sequence[torch.Tensor]):
+        """Every layer's K and V rows of positions pos.. (device f32 [n][kv][hd], keys normed and rotated)."""
+        n = k[0].shape[0]
+        for t in list(k) + list(v):
+            assert t.dtype == torch.float32 and t.is_cuda and t.is_contiguous() and t.shape[0] == n
+        L.dflash_push_rows(self.h, seq, pos, n, [t.data_ptr() for t in k], [t.data_ptr() for t in v], _stream())
 
     def settle(self, seq: int, pos: int, taps: torch.Tensor, chunk: int = L.SETTLE_MAX):
         """Settle tap rows [n][tw] (device f32) at positions pos.., `chunk` (1..1024) rows a call."""

@@ -114,12 +114,17 @@ def test_settle_and_block_argument_errors_before_any_launch(L):
         with pytest.raises(L.DflashError) as e:
             L.dflash_settle(h, 0, 0, taps, n, None)
         assert e.value.code == 2
-    with pytest.raises(L.DflashError) as e:               # a gap: the caller resets the sequence
-        L.dflash_settle(h, 0, 5, taps, 1, None)
-    assert e.value.code == 2
     with pytest.raises(L.DflashError) as e:               # the cache holds 64 rows
         L.dflash_settle(h, 0, 0, taps, 65, None)
     assert e.value.code == 3
+    with pytest.raises(L.DflashError) as e:               # a gap starts over at 1000: 65 rows still do not fit
+        L.dflash_settle(h, 0, 1000, taps, 65, None)
+    assert e.value.code == 3
+    assert L.dflash_context(h, 0) == (0, 0)               # a refused call leaves the context as it was
+    for pos in (-1,):
+        with pytest.raises(L.DflashError) as e:
+            L.dflash_settle(h, 0, pos, taps, 1, None)
+        assert e.value.code == 2
     out = 1 << 25
     for k, width in ((0, 4096), (16, 4096), (15, 7), (15, 4097)):
         with pytest.raises(L.DflashError) as e:
@@ -271,3 +276,80 @@ def test_context_and_reset_argument_errors(L):
     with pytest.raises(L.DflashError):
         L.dflash_reset(h, 0, -1)
     L.dflash_destroy(h)
+
+
+def test_cache_layouts(L):
+    """Linear caches hold ctx_cap rows; a ring needs a windowed layer and at least twice its
+    window, and holds its ring plus `window` rows repeating its first ones; planes take 4
+    bytes an element, one f16 two."""
+    g = _geom(L, windows=(100,))
+    lin = L.CacheConfig()
+    assert L.dflash_cache_rows(g, lin, 0, 4096) == 4096
+    assert L.dflash_cache_bytes(g, lin, 0, 4096) == 4096 * 2 * 64 * 4
+    assert L.dflash_cache_rows(g, None, 0, 4096) == 4096
+    ring = L.CacheConfig()
+    ring.ring[0] = 200
+    assert L.dflash_cache_rows(g, ring, 0, 4096) == 300
+    ring.format = L.KV_F16
+    assert L.dflash_cache_bytes(g, ring, 0, 4096) == 300 * 2 * 64 * 2
+    ring.ring[0] = 199                                     # less than twice the window
+    assert L.dflash_cache_rows(g, ring, 0, 4096) == 0
+    ring.ring[0] = 200
+    assert L.dflash_cache_rows(_geom(L), ring, 0, 4096) == 0   # window 0: no ring
+    bad = L.CacheConfig()
+    bad.format = 7
+    assert L.dflash_cache_bytes(g, bad, 0, 4096) == 0
+    assert L.dflash_cache_rows(g, lin, 1, 4096) == 0           # no such layer
+
+
+def test_pending_limit_follows_the_widest_window(L):
+    # dflash.rs Drafter::queue_context (CUDA arm): 512, or the widest window + 256 when every layer has one
+    assert L.dflash_pending_limit(_geom(L)) == 512
+    assert L.dflash_pending_limit(_geom(L, windows=(100,))) == 512
+    assert L.dflash_pending_limit(_geom(L, windows=(600,))) == 856
+
+
+def test_bookkeeping_argument_errors_before_any_launch(L):
+    h, keep = _fake_create(L, max_batch=1, cap=64)
+    taps = 1 << 24
+    assert L.dflash_context_ex(h, 0, 1) == (0, 0, 0, [0])
+    with pytest.raises(L.DflashError) as e:                   # no pending buffer bound
+        L.dflash_queue(h, 0, 0, taps, 1, None)
+    assert e.value.code == 2
+    with pytest.raises(L.DflashError) as e:                   # fewer rows than the pending limit
+        L.dflash_bind_pending(h, 0, 1 << 26, 511)
+    assert e.value.code == 3
+    with pytest.raises(L.DflashError) as e:
+        L.dflash_bind_pending(h, 0, (1 << 26) + 8, 512)
+    assert e.value.code == 2
+    L.dflash_bind_pending(h, 0, None, 0)
+    L.dflash_settle_pending(h, 0, None)                      # nothing waits: nothing to do
+    L.dflash_truncate(h, 0, 10)
+    assert L.dflash_context_ex(h, 0, 1) == (0, 0, 0, [0])
+    with pytest.raises(L.DflashError):
+        L.dflash_truncate(h, 1, 0)
+    with pytest.raises(L.DflashError) as e:                   # rows past the 64-row cache
+        L.dflash_push_rows(h, 0, 0, 65, [taps], [taps], None)
+    assert e.value.code == 3
+    with pytest.raises(L.DflashError) as e:                   # a layer's rows missing
+        L.dflash_push_rows(h, 0, 0, 4, [taps], [None], None)
+    assert e.value.code == 2
+    L.dflash_destroy(h)
+
+
+def test_create_ex_rejects_bad_cache_layouts(L):
+    from speculative_block_drafter_gb300.drafter import geometry_struct
+    g = geometry_struct(dataclasses.replace(di.workload("tiny").geometry, windows=(100,)))
+    h = C.c_void_p()
+    w = L.Weights()
+    one = (C.c_void_p * 1)(C.c_void_p(4096))
+    cache = L.CacheConfig()
+    cache.ring[0] = 150
+    code = L.lib().dflash_create_ex(C.byref(h), C.byref(g), C.byref(w), 1, C.byref(cache), one, one, 16,
+                                    C.c_void_p(4096), 1 << 30)
+    assert code == 2 and "ring" in L.last_error()
+    cache.ring[0] = 0
+    cache.format = 3
+    code = L.lib().dflash_create_ex(C.byref(h), C.byref(g), C.byref(w), 1, C.byref(cache), one, one, 16,
+                                    C.c_void_p(4096), 1 << 30)
+    assert code == 2 and "format" in L.last_error()

@@ -121,31 +121,61 @@ def test_gemm_f16_matches_oracle(rows, cols, T):
 # ------------------------------------------------------------------ the pass
 
 class Pair:
-    """The GPU drafter and the oracle on the same weights."""
+    """The GPU drafter and the oracle on the same weights, driven through the same calls."""
 
-    def __init__(self, g, seed=0, max_batch=1, ctx_cap=4096):
+    def __init__(self, g, seed=0, max_batch=1, ctx_cap=4096, cache_format="planes", rings=None):
         self.g = g
         self.w = di.make_weights(g, seed)
-        self.gpu = _drafter().Drafter(g, self.w, max_batch=max_batch, ctx_cap=ctx_cap)
+        self.gpu = _drafter().Drafter(g, self.w, max_batch=max_batch, ctx_cap=ctx_cap, cache_format=cache_format,
+                                      rings=rings)
         self.orc = [O.Oracle(g, self.w) for _ in range(max_batch)]
+        # one f16 per element: the cache rounds each K/V value to 11 bits
+        self.cache_rel = 1e-3 if cache_format == "f16" else 1e-4
 
     def settle(self, seq, pos, taps, chunk=1024):
+        # each library call is one `push_context`: the oracle takes the same calls
         self.gpu.settle(seq, pos, torch.from_numpy(taps).cuda(), chunk=chunk)
-        self.orc[seq].settle(pos, taps)
+        for i in range(0, len(taps), chunk):
+            self.orc[seq].settle(pos + i, taps[i:i + chunk])
+
+    def queue(self, seq, pos, taps, chunk=1024):
+        self.gpu.queue(seq, pos, torch.from_numpy(taps).cuda(), chunk=chunk)
+        for i in range(0, len(taps), chunk):
+            self.orc[seq].queue(pos + i, taps[i:i + chunk])
+
+    def settle_pending(self, seq):
+        self.gpu.settle_pending(seq)
+        self.orc[seq].settle_pending()
+
+    def truncate(self, seq, pos):
+        self.gpu.truncate(seq, pos)
+        self.orc[seq].truncate(pos)
+
+    def push_rows(self, seq, pos, kv):
+        """kv: per layer (k, v) f64 [n][kv][hd] (the oracle's own rows), sent as f32."""
+        k = [torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).cuda() for a, _ in kv]
+        v = [torch.from_numpy(np.ascontiguousarray(b, dtype=np.float32)).cuda() for _, b in kv]
+        self.gpu.push_rows(seq, pos, k, v)
+        self.orc[seq].push_rows(pos, [(a.astype(np.float32).astype(np.float64), b.astype(np.float32).astype(np.float64))
+                                      for a, b in kv])
 
     def reset(self, seq, first):
         self.gpu.reset(seq, first)
         self.orc[seq].reset(first)
 
     def check_cache(self, seq=0):
+        """The context's state and every layer's held rows against the oracle's."""
         torch.cuda.synchronize()
         o = self.orc[seq]
-        f, n = self.gpu.context(seq)
-        assert (f, n) == (o.first, o.len)
+        f, n, pend, dropped = self.gpu.context_ex(seq)
+        assert (f, n, pend, dropped) == (o.first, o.len, len(o.pending), o.dropped)
         worst = 0.0
         for l in range(self.g.layers):
-            k, v = (t.cpu().numpy() for t in self.gpu.context_kv(seq, l, n))
-            worst = max(worst, check_close(f"K layer {l}", k, o.ctx_k[l]), check_close(f"V layer {l}", v, o.ctx_v[l]))
+            k, v = (t.cpu().numpy() for t in self.gpu.held_kv(seq, l))
+            assert k.shape[0] == o.ctx_k[l].shape[0], (l, k.shape, o.ctx_k[l].shape)
+            if k.shape[0]:
+                worst = max(worst, check_close(f"K layer {l}", k, o.ctx_k[l], self.cache_rel),
+                            check_close(f"V layer {l}", v, o.ctx_v[l], self.cache_rel))
         return worst
 
     def draft(self, anchors, hs_rows, anchor_toks, k=None, width=None):
@@ -356,4 +386,79 @@ def test_full_settle_heavy_workload():
     assert p.check_cache() < 1e-4
     a = di.anchor_token(g, wl.seed)
     r = p.draft([wl.context], [di.block_rows(g, wl.seed, a)], [a])[0]
+    assert r["logit_err"] < LOGIT_REL, r
+
+
+# ------------------------------------------------------------------ context bookkeeping, rings, f16 caches
+
+@pytest.mark.parametrize("fmt,rings", [("planes", None), ("planes", "window"), ("f16", None), ("f16", "window")])
+def test_bookkeeping_against_oracle(fmt, rings):
+    """dflash.rs `Drafter`: settles that trim a windowed layer, queued rows past the pending
+    limit, truncation below the held rows, a gap, imported rows; the caches linear or rings
+    of twice the window (the rows wrap many times), two planes or one f16; each state and
+    the blocks (anchored at the end and inside the context) against the oracle."""
+    g = _tiny(windows=(40,))
+    p = Pair(g, ctx_cap=4096, cache_format=fmt, rings=rings)
+    p.gpu.bind_pending(0)
+    taps = di.make_taps(g, 7, 1600)
+    a = di.anchor_token(g, 3)
+    rows = di.block_rows(g, 3, a)
+
+    def draft(anchor):
+        r = p.draft([anchor], [rows], [a])[0]
+        assert r["logit_err"] < (5e-4 if fmt == "f16" else 1e-4), r
+
+    p.settle(0, 0, taps[:100], chunk=37)            # trims after the third call
+    assert p.check_cache() < p.cache_rel
+    draft(100)
+    p.queue(0, 100, taps[100:160])
+    p.truncate(0, 130)                               # waiting rows past 130 go
+    p.settle_pending(0)
+    assert p.check_cache() < p.cache_rel
+    p.truncate(0, 70)                                # below the rows the layer holds
+    p.settle(0, 70, taps[160:170])
+    assert p.check_cache() < p.cache_rel
+    draft(80)
+    p.queue(0, 80, taps[170:770], chunk=300)          # past the 512-row limit: the oldest 128 settle
+    assert p.gpu.context_ex(0)[2] == p.orc[0].pending.__len__() == 472
+    p.settle_pending(0)
+    assert p.check_cache() < p.cache_rel
+    draft(680)
+    draft(650)                                       # anchored inside the context
+    kv = p.orc[0].settle_rows(680, taps[800:830])[1]
+    p.push_rows(0, 680, kv)
+    assert p.check_cache() < p.cache_rel
+    draft(710)
+    p.settle(0, 5000, taps[900:1000], chunk=64)       # a gap: the context starts over at 5000
+    assert p.check_cache() < p.cache_rel
+    draft(5100)
+
+
+def test_block_refuses_waiting_rows():
+    from speculative_block_drafter_gb300 import _lib as L
+    g = _tiny()
+    p = Pair(g, ctx_cap=256)
+    p.gpu.bind_pending(0)
+    p.queue(0, 0, di.make_taps(g, 1, 20))
+    with pytest.raises(L.DflashError) as e:
+        p.gpu.block([20], torch.from_numpy(di.block_rows(g, 0, 1)[None]).cuda().contiguous())
+    assert e.value.code == 2 and "wait" in str(e.value)
+    p.settle_pending(0)
+    assert p.check_cache() < 1e-4
+
+
+def test_full_27b_windows_f16_rings():
+    """The 27b geometry with one-f16 caches and rings of twice the window for its four
+    windowed layers (the no-rope layer 2 keeps a linear cache): 6,144 positions settled in
+    256-row calls, so that the rings wrap and the window trim lets rows go; then one block
+    over the whole head and the selector, against the oracle."""
+    wl = di.workload("27b")
+    g = wl.geometry
+    n = 6144
+    p = Pair(g, seed=wl.seed, ctx_cap=n + 256, cache_format="f16", rings="window")
+    taps = di.make_taps(g, wl.seed, n)
+    p.settle(0, 0, taps, chunk=256)
+    assert p.check_cache() < 1e-3
+    a = di.anchor_token(g, wl.seed)
+    r = p.draft([n], [di.block_rows(g, wl.seed, a)], [a])[0]
     assert r["logit_err"] < LOGIT_REL, r

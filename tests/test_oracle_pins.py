@@ -672,3 +672,93 @@ def test_select_scores_agree_with_select_with():
                     best_t, best_s = tok, s
             assert best_t == chosen[j]
             assert scores[j][0][0] == plain[j]
+
+
+# ------------------------------------------------------------------ context bookkeeping
+# Sequences worked by hand from dflash.rs: `Drafter::queue_context` (a gap starts over, a
+# held position truncates, past the pending limit the oldest rows settle in multiples of
+# CONTEXT_CHUNK), `settle`, `truncate` and the window trim at the end of `settle_rows`
+# (a layer holding more than twice its window keeps its last `window` rows).
+
+def _kv_of(o, pos, taps):
+    return o.settle_rows(pos, taps)[1]
+
+
+def test_window_trim_and_truncate_worked_sequence():
+    g, w = _tiny(windows=(8,))
+    taps = di.make_taps(g, 2, 40)
+    o = O.Oracle(g, w)
+    o.settle(0, taps[:20])                 # held 20 > 16: keeps 8, dropped 12
+    assert (o.len, o.dropped) == (20, [12])
+    k, v = _kv_of(o, 12, taps[12:20])[0]
+    assert np.allclose(o.ctx_k[0], k, rtol=0, atol=1e-13) and np.allclose(o.ctx_v[0], v, rtol=0, atol=1e-13)
+    o.settle(20, taps[20:25])              # held 13: nothing let go
+    assert (o.len, o.dropped, len(o.ctx_k[0])) == (25, [12], 13)
+    o.settle(25, taps[25:29])              # held 17 > 16: keeps 8, dropped 21
+    assert (o.len, o.dropped, len(o.ctx_k[0])) == (29, [21], 8)
+    o.truncate(27)                         # keeps positions 21..26
+    assert (o.len, o.dropped, len(o.ctx_k[0])) == (27, [21], 6)
+    o.truncate(10)                         # below what the layer holds: it holds nothing from 10 on
+    assert (o.len, o.dropped, len(o.ctx_k[0])) == (10, [10], 0)
+    o.settle(10, taps[30:33])              # new rows at 10..12
+    assert (o.len, o.dropped, len(o.ctx_k[0])) == (13, [10], 3)
+    k, v = _kv_of(o, 10, taps[30:33])[0]
+    assert np.allclose(o.ctx_k[0], k, rtol=0, atol=1e-13)
+    assert O.context_range(o.first, o.len, 13, 8, o.dropped[0]) == (10, 13)
+
+
+def test_queue_pending_limit_gap_and_truncate_worked_sequence():
+    g, w = _tiny()                          # window 0: the pending limit is 512
+    assert O.pending_limit(g) == 512
+    assert O.pending_limit(dataclasses.replace(g, windows=(600,))) == 856
+    assert O.pending_limit(dataclasses.replace(g, windows=(100,))) == 512
+    taps = di.make_taps(g, 3, 620)
+    o = O.Oracle(g, w)
+    o.queue(0, taps[:600])                 # 600 > 512: the oldest 128 settle (88 rounded up to 64s)
+    assert (o.len, len(o.pending), o.next_position()) == (128, 472, 600)
+    o.queue(600, taps[600:610])
+    assert (o.len, len(o.pending)) == (128, 482)
+    o.queue(300, taps[610:615])            # a held position: waiting rows from 300 on go
+    assert (o.len, len(o.pending), o.next_position()) == (128, 177, 305)
+    o.truncate(100)
+    assert (o.len, len(o.pending)) == (100, 0)
+    ref = O.Oracle(g, w)
+    ref.settle(0, taps[:100])
+    assert np.allclose(o.ctx_k[0], ref.ctx_k[0], rtol=0, atol=1e-13)
+    o.queue(2000, taps[:3])                # a gap: the context starts over at 2000
+    assert (o.first, o.len, len(o.pending)) == (2000, 0, 3)
+    o.settle_pending()
+    assert (o.first, o.len) == (2000, 3)
+    k, _ = _kv_of(o, 2000, taps[:3])[0]
+    assert np.allclose(o.ctx_k[0], k, rtol=0, atol=1e-13)
+    o.queue(1500, taps[3:4])               # before first: a gap as well
+    assert (o.first, o.len, len(o.pending)) == (1500, 0, 1)
+
+
+def test_queued_rows_equal_settled_rows_and_blocks_wait_for_them():
+    g, w = _tiny()
+    taps = di.make_taps(g, 4, 90)
+    a, b = O.Oracle(g, w), O.Oracle(g, w)
+    a.settle(0, taps)
+    for i in range(0, 90, 30):
+        b.queue(i, taps[i:i + 30])
+    with pytest.raises(AssertionError):
+        b.block(90, di.block_rows(g, 0, 1))
+    b.settle_pending()
+    assert b.len == 90 and np.allclose(a.ctx_k[0], b.ctx_k[0], rtol=0, atol=1e-13)
+    assert np.array_equal(a.block(90, di.block_rows(g, 0, 1)), b.block(90, di.block_rows(g, 0, 1)))
+
+
+def test_pushed_rows_equal_settled_rows():
+    """Rows imported with their keys and values (`Dev::push_rows`) are the context a settle of
+    the same taps makes, the bookkeeping (trim included) the same."""
+    g, w = _tiny(windows=(8,))
+    taps = di.make_taps(g, 5, 30)
+    a, b = O.Oracle(g, w), O.Oracle(g, w)
+    a.settle(0, taps[:20])
+    a.settle(20, taps[20:30])
+    b.push_rows(0, _kv_of(b, 0, taps[:20]))
+    b.push_rows(20, _kv_of(b, 20, taps[20:30]))
+    assert (a.len, a.dropped) == (b.len, b.dropped) == (30, [22])   # 20 held: 8 kept; then 18: 8 kept
+    assert np.allclose(a.ctx_k[0], b.ctx_k[0], rtol=0, atol=1e-13)
+    assert np.allclose(a.block(30, di.block_rows(g, 0, 3)), b.block(30, di.block_rows(g, 0, 3)), rtol=0, atol=1e-12)

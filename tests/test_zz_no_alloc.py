@@ -97,9 +97,10 @@ def test_select_static_leaves_device_memory_as_it_found_it():
 
     call()
     torch.cuda.synchronize()
+    first = chosen.clone()
+    torch.cuda.synchronize()
     free0, _ = torch.cuda.mem_get_info()
     alloc0 = torch.cuda.memory_allocated()
-    first = chosen.clone()
     for _ in range(5):
         call()
     torch.cuda.synchronize()
