@@ -318,6 +318,28 @@ int dflash_select_static(const float *logits, const float *hp, const uint32_t *a
                          int32_t width, int32_t vocab, int32_t rank, int32_t top, uint32_t *chosen,
                          uint32_t *plain, void *stream);
 
+/* ---- the router ------------------------------------------------------------ */
+
+/* A sidecar's router (dflash.rs `RouteFit` / `Route`): for the rounds the block
+ * drafter won and for those the target's own chain won, a fitted subspace of
+ * the target's rows, its mean f16 [hidden] and basis rows f16 [rank][hidden]
+ * (orthonormal as fitted); device pointers, the caller's. */
+typedef struct dflash_route {
+  const uint16_t *block_mean, *block_basis;
+  const uint16_t *chain_mean, *chain_basis;
+  int32_t block_rank, chain_rank;   /* 0..256; a basis may be NULL at rank 0 */
+} dflash_route;
+
+/* `Route::margin` of `n` rows (device f32 [n][hidden], the target's rows at the
+ * tip) into margin (device f32 [n]): each row scaled to unit length (its norm
+ * at least 1e-12), then the chain subspace's reconstruction error minus the
+ * block subspace's, an error being the squared length of d - B^T (B d) with
+ * d = unit - mean (the pages call `router::recon_error` without printing it;
+ * this is its plain reading). Above zero the round is the block drafter's.
+ * Enqueued on `stream`. Errors: ARG (hidden 1..16384, ranks 0..256), CUDA. */
+int dflash_route_margin(const dflash_route *r, int32_t hidden, const float *rows, int32_t n, float *margin,
+                        void *stream);
+
 void dflash_destroy(dflash_t *d);
 
 /* The message of the calling thread's last failure ("" if none). */

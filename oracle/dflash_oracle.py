@@ -55,7 +55,8 @@ import numpy as np
 
 __all__ = [
     "dequant_int4", "int4_matmul", "f16_matmul", "rms", "inv_freq", "rotate", "conv",
-    "context_range", "attention", "mlp", "top_k", "select_with", "pending_limit", "Oracle",
+    "context_range", "attention", "mlp", "top_k", "select_with", "pending_limit", "recon_error",
+    "route_margin", "Oracle",
 ]
 
 # Context bookkeeping constants of the host drafter (dflash.rs, module constants).
@@ -264,6 +265,28 @@ def select_with(hp: np.ndarray, logits: np.ndarray, anchor: int, pred_book: np.n
         prev = best_t
         chosen.append(prev)
     return chosen, plain
+
+
+# ---------------------------------------------------------------- router
+
+def recon_error(unit: np.ndarray, mean: np.ndarray, basis: np.ndarray) -> float:
+    """How badly a subspace holds a row: the squared length of what is left of ``unit - mean``
+    after taking away its projection on the basis rows, ``d - B^T (B d)`` (the basis rows of a
+    fitted descriptor are orthonormal). The pages call ``router::recon_error`` without
+    printing it; this is the plain reading of a reconstruction error."""
+    d = np.asarray(unit, np.float64) - np.asarray(mean, np.float64)
+    B = np.asarray(basis, np.float64).reshape(-1, d.shape[0])
+    r = d - B.T @ (B @ d)
+    return float(r @ r)
+
+
+def route_margin(row: np.ndarray, block_mean, block_basis, chain_mean, chain_basis) -> float:
+    """``Route::margin`` (dflash.rs): the row scaled to unit length (its norm at least 1e-12),
+    then the chain subspace's reconstruction error minus the block subspace's; above zero
+    the round is the block's. Means and bases are f16 ``[hidden]``, ``[rank][hidden]``."""
+    row = np.asarray(row, np.float64)
+    unit = row / max(float(np.sqrt(row @ row)), 1e-12)
+    return recon_error(unit, chain_mean, chain_basis) - recon_error(unit, block_mean, block_basis)
 
 
 def select_scores(hp: np.ndarray, logits: np.ndarray, prev_tokens: Sequence[int], pred_book, succ_book, top: int):

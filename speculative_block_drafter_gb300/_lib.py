@@ -44,6 +44,11 @@ class CacheConfig(C.Structure):
     _fields_ = [("format", C.c_int32), ("ring", C.c_int32 * MAX_LAYERS)]
 
 
+class Route(C.Structure):
+    _fields_ = [("block_mean", C.c_void_p), ("block_basis", C.c_void_p), ("chain_mean", C.c_void_p),
+                ("chain_basis", C.c_void_p), ("block_rank", C.c_int32), ("chain_rank", C.c_int32)]
+
+
 class Matrix(C.Structure):
     _fields_ = [("data", C.c_void_p), ("scales", C.c_void_p)]
 
@@ -109,6 +114,7 @@ EXPORTS = {
     "dflash_select_static": (C.c_int, [C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_int32,
                                        C.c_int32, C.c_int32, C.c_int32, C.c_int32, C.c_int32, C.c_void_p,
                                        C.c_void_p, C.c_void_p]),
+    "dflash_route_margin": (C.c_int, [C.POINTER(Route), C.c_int32, C.c_void_p, C.c_int32, C.c_void_p, C.c_void_p]),
     "dflash_destroy": (None, [C.c_void_p]),
     "dflash_last_error": (C.c_char_p, []),
     "dflash_launch_count": (C.c_uint64, []),
@@ -277,6 +283,10 @@ def dflash_select_static(logits, hp, anchor_tok, pred_book, succ_book, batch, k,
     """The selector with its scratch inside the library (for callers that cannot allocate device memory)."""
     _check(lib().dflash_select_static(logits, hp, anchor_tok, pred_book, succ_book, batch, k, width, vocab, rank,
                                       top, chosen, plain, stream))
+
+
+def dflash_route_margin(route: Route, hidden, rows, n, margin, stream):
+    _check(lib().dflash_route_margin(C.byref(route), hidden, rows, n, margin, stream))
 
 
 def dflash_destroy(h):

@@ -294,3 +294,27 @@ class PackedMatrix:
         L.dflash_gemm_packed(self.mat, self.kind, self.rows, self.cols, self.group, T, y.data_ptr(),
                              self._ws.data_ptr(), _stream())
         return y
+
+
+class Router:
+    """A router's two fitted subspaces (means f16 [hidden], bases f16 [rank][hidden]) on the GPU;
+    ``margin(rows)`` is `Route::margin` of each row (device f32 [n][hidden])."""
+
+    def __init__(self, block_mean, block_basis, chain_mean, chain_basis, device="cuda"):
+        dev = torch.device(device)
+
+        def up(a):
+            return torch.from_numpy(np.ascontiguousarray(a, dtype=np.float16).view(np.int16)).to(dev)
+
+        self._t = [up(block_mean), up(block_basis), up(chain_mean), up(chain_basis)]
+        self.hidden = int(np.asarray(block_mean).shape[0])
+        self.r = L.Route(self._t[0].data_ptr(), self._t[1].data_ptr() if self._t[1].numel() else None,
+                         self._t[2].data_ptr(), self._t[3].data_ptr() if self._t[3].numel() else None,
+                         int(np.asarray(block_basis).reshape(-1, self.hidden).shape[0]),
+                         int(np.asarray(chain_basis).reshape(-1, self.hidden).shape[0]))
+
+    def margin(self, rows: torch.Tensor) -> torch.Tensor:
+        assert rows.dtype == torch.float32 and rows.is_cuda and rows.is_contiguous() and rows.shape[1] == self.hidden
+        out = torch.empty(rows.shape[0], dtype=torch.float32, device=rows.device)
+        L.dflash_route_margin(self.r, self.hidden, rows.data_ptr(), rows.shape[0], out.data_ptr(), _stream())
+        return out

@@ -353,3 +353,15 @@ def test_create_ex_rejects_bad_cache_layouts(L):
     code = L.lib().dflash_create_ex(C.byref(h), C.byref(g), C.byref(w), 1, C.byref(cache), one, one, 16,
                                     C.c_void_p(4096), 1 << 30)
     assert code == 2 and "format" in L.last_error()
+
+
+def test_route_margin_argument_errors_before_any_launch(L):
+    p = 1 << 20
+    for r, hidden, n, code in ((L.Route(p, p, p, p, 257, 4), 64, 1, 2),   # rank past 256
+                               (L.Route(None, p, p, p, 4, 4), 64, 1, 2),  # no block mean
+                               (L.Route(p, None, p, p, 4, 4), 64, 1, 2),  # a basis missing at rank 4
+                               (L.Route(p, p, p, p, 4, 4), 0, 1, 2),      # hidden
+                               (L.Route(p, p, p, p, 4, 4), 64, 0, 2)):    # no rows
+        with pytest.raises(L.DflashError) as e:
+            L.dflash_route_margin(r, hidden, p, n, p, None)
+        assert e.value.code == code

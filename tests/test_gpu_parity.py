@@ -462,3 +462,27 @@ def test_full_27b_windows_f16_rings():
     a = di.anchor_token(g, wl.seed)
     r = p.draft([n], [di.block_rows(g, wl.seed, a)], [a])[0]
     assert r["logit_err"] < LOGIT_REL, r
+
+
+# ------------------------------------------------------------------ router margin
+
+def test_route_margin_matches_oracle():
+    """`Route::margin` on the 27B hidden size: rank-64 block and rank-48 chain subspaces with
+    near-orthonormal f16 bases and small means; random rows, a row inside the block subspace
+    (margin well above zero), one inside the chain's (below zero) and a zero row."""
+    from speculative_block_drafter_gb300.drafter import Router
+    rng = np.random.default_rng(31)
+    hs = 5120
+    qb, _ = np.linalg.qr(rng.standard_normal((hs, 64)))
+    qc, _ = np.linalg.qr(rng.standard_normal((hs, 48)))
+    Bb, Bc = qb.T.astype(np.float16), qc.T.astype(np.float16)
+    mb = (rng.standard_normal(hs) * 0.002).astype(np.float16)
+    mc = (rng.standard_normal(hs) * 0.002).astype(np.float16)
+    rows = rng.standard_normal((37, hs)).astype(np.float32)
+    rows[3] = (Bb.astype(np.float64).T @ rng.standard_normal(64)).astype(np.float32)
+    rows[4] = (Bc.astype(np.float64).T @ rng.standard_normal(48)).astype(np.float32)
+    rows[5] = 0.0
+    got = Router(mb, Bb, mc, Bc).margin(torch.from_numpy(rows).cuda()).cpu().numpy()
+    ref = np.array([O.route_margin(r, mb, Bb, mc, Bc) for r in rows])
+    assert np.abs(got - ref).max() <= 2e-5 * max(1.0, np.abs(ref).max()), np.abs(got - ref).max()
+    assert ref[3] > 0.5 and ref[4] < -0.5 and got[3] > 0.5 and got[4] < -0.5

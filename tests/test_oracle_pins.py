@@ -762,3 +762,51 @@ def test_pushed_rows_equal_settled_rows():
     assert (a.len, a.dropped) == (b.len, b.dropped) == (30, [22])   # 20 held: 8 kept; then 18: 8 kept
     assert np.allclose(a.ctx_k[0], b.ctx_k[0], rtol=0, atol=1e-13)
     assert np.allclose(a.block(30, di.block_rows(g, 0, 3)), b.block(30, di.block_rows(g, 0, 3)), rtol=0, atol=1e-12)
+
+
+# ------------------------------------------------------------------ router margin
+
+def _orthonormal_rows(rng, rank, hidden):
+    """`rank` distinct rows of the Sylvester-Hadamard matrix over sqrt(hidden) (hidden a power of
+    4): entries +-1/8 at 64, exact in f16, so the rows are exactly orthonormal."""
+    H = np.array([[1.0]])
+    while H.shape[0] < hidden:
+        H = np.block([[H, H], [H, -H]])
+    rows = rng.choice(hidden, size=rank, replace=False)
+    return (H[rows] / np.sqrt(hidden)).astype(np.float16)
+
+
+def test_recon_error_closed_forms():
+    rng = np.random.default_rng(21)
+    hs, rank = 64, 5
+    B = _orthonormal_rows(rng, rank, hs)
+    m = (rng.standard_normal(hs) * 0.1).astype(np.float16)
+    Bf, mf = B.astype(np.float64), m.astype(np.float64)
+    # a row inside the affine subspace is held exactly
+    inside = mf + Bf.T @ rng.standard_normal(rank)
+    assert O.recon_error(inside, m, B) < 1e-20
+    # rank 0: the whole offset from the mean
+    x = rng.standard_normal(hs)
+    assert O.recon_error(x, m, np.zeros((0, hs), np.float16)) == pytest.approx(float((x - mf) @ (x - mf)), rel=1e-12)
+    # against least squares (the distance to the span, by another route)
+    coef, *_ = np.linalg.lstsq(Bf.T, x - mf, rcond=None)
+    res = (x - mf) - Bf.T @ coef
+    assert O.recon_error(x, m, B) == pytest.approx(float(res @ res), rel=1e-9)
+
+
+def test_route_margin_closed_forms():
+    rng = np.random.default_rng(22)
+    hs = 64
+    Bb, Bc = _orthonormal_rows(rng, 4, hs), _orthonormal_rows(rng, 6, hs)
+    mb, mc = np.zeros(hs, np.float16), np.zeros(hs, np.float16)
+    # a row along the block's first basis row: the block holds it, the chain does not
+    row = 3.0 * Bb[0].astype(np.float64)
+    m = O.route_margin(row, mb, Bb, mc, Bc)
+    u = Bb[0].astype(np.float64) / np.linalg.norm(Bb[0].astype(np.float64))
+    assert m == pytest.approx(O.recon_error(u, mc, Bc), abs=1e-9) and m > 0
+    # scale-free, antisymmetric in the two subspaces, zero row guarded
+    x = rng.standard_normal(hs)
+    assert O.route_margin(x, mb, Bb, mc, Bc) == pytest.approx(O.route_margin(7.5 * x, mb, Bb, mc, Bc), rel=1e-12)
+    assert O.route_margin(x, mb, Bb, mc, Bc) == pytest.approx(-O.route_margin(x, mc, Bc, mb, Bb), rel=1e-12)
+    zero = O.route_margin(np.zeros(hs), mb, Bb, mc, Bc)
+    assert zero == pytest.approx(0.0, abs=1e-12)        # both errors are |0 - mean|^2 = 0
