@@ -55,6 +55,9 @@ def parse(argv=None):
     p.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     p.add_argument("--no-graph", action="store_true", help="direct calls instead of a CUDA graph replay")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cache", default="planes", choices=["planes", "f16", "f16-rings"],
+                   help="K/V caches: two f16 planes (the f32 contract), one f16, or one f16 with rings of twice "
+                        "the window for windowed layers")
     return p.parse_args(argv)
 
 
@@ -85,18 +88,19 @@ def context_rows(g, context: int, anchor: int) -> list:
     return out
 
 
-def block_cost(g, width: int, ctx_rows: list, batch: int):
+def block_cost(g, width: int, ctx_rows: list, batch: int, kv_bytes: int = 4):
     """Algorithmic bytes and flops of one block step of `batch` sequences: every weight once
     (the layers' four-bit and f16 matrices, the head's first `width` rows, the selector's
-    projection), each sequence's admitted K/V rows (4 bytes an element), and the selector's
-    codebook rows; flops: two a weight per token row plus the attention's products."""
+    projection), each sequence's admitted K/V rows (`kv_bytes` an element: 4 for the f32
+    contract, 2 for one-f16 caches), and the selector's codebook rows; flops: two a weight
+    per token row plus the attention's products."""
     hs, R, k = g.hidden, g.block, g.block - 1
     kvd = g.kv_heads * g.head_dim
     layer = sum(int4_bytes(r, c, g.quant_group) for r, c in di.weight_shapes(g).values())
     proj = 2 * g.proj_rows * hs * 2
     head = int4_bytes(width, hs, g.quant_group)
     sel = g.selector_rank * hs * 2 + batch * k * g.selector_top * 2 * g.selector_rank * 2
-    kv = batch * sum(ctx_rows) * kvd * 4 * 2
+    kv = batch * sum(ctx_rows) * kvd * kv_bytes * 2
     nbytes = g.layers * (layer + proj) + head + sel + kv
     params = sum(r * c for r, c in di.weight_shapes(g).values()) + 2 * g.proj_rows * hs
     flops = 2.0 * batch * R * g.layers * params + 2.0 * batch * k * (width + g.selector_rank) * hs
@@ -106,14 +110,14 @@ def block_cost(g, width: int, ctx_rows: list, batch: int):
     return nbytes, flops, parts
 
 
-def settle_cost_per_row(g, chunk: int):
+def settle_cost_per_row(g, chunk: int, kv_bytes: int = 4):
     """Algorithmic bytes and flops of one settled row in calls of `chunk` rows: the fc and every
-    layer's Wk, Wv once a call, the row's taps in (f32) and its K/V out (4 bytes an element)."""
+    layer's Wk, Wv once a call, the row's taps in (f32) and its K/V out (`kv_bytes` an element)."""
     hs, tw = g.hidden, g.tap_width
     kvd = g.kv_heads * g.head_dim
     fc = hs * tw * 2
     kvw = g.layers * 2 * int4_bytes(kvd, hs, g.quant_group)
-    nbytes = (fc + kvw) / chunk + tw * 4 + g.layers * 2 * kvd * 4
+    nbytes = (fc + kvw) / chunk + tw * 4 + g.layers * 2 * kvd * kv_bytes
     flops = 2.0 * (hs * tw + g.layers * 2 * kvd * hs)
     return nbytes, flops
 
@@ -236,7 +240,7 @@ def block_traffic(workload: str):
 
 # ------------------------------------------------------------------ the GB300 arm
 class Bench:
-    def __init__(self, wl, device):
+    def __init__(self, wl, device, cache="planes"):
         import torch
         from speculative_block_drafter_gb300 import _lib
         from speculative_block_drafter_gb300.drafter import Drafter, PackedMatrix
@@ -248,7 +252,10 @@ class Bench:
         self.k = g.block - 1
         self.width = wl.head_width
         self.w = di.make_weights(g, wl.seed)
-        self.d = Drafter(g, self.w, max_batch=wl.batch, ctx_cap=wl.context + g.block)
+        self.d = Drafter(g, self.w, max_batch=wl.batch, ctx_cap=wl.context + g.block,
+                         cache_format="planes" if cache == "planes" else "f16",
+                         rings="window" if cache == "f16-rings" else None)
+        self.cache = cache
         B = wl.batch
         self.taps_host = [di.make_taps(g, wl.seed + s, wl.context) for s in range(B)]
         self.anchor_tok = [di.anchor_token(g, wl.seed + s) for s in range(B)]
@@ -441,7 +448,7 @@ def run_gb300(args):
     wl = di.workload(args.workload)
     g = wl.geometry
     hbm_peak, tc_burst, tc_sust, peak_kind = peaks()
-    b = Bench(wl, dev)
+    b = Bench(wl, dev, args.cache)
     for _ in range(args.warmup):
         b.step()
     torch.cuda.synchronize()
@@ -496,7 +503,7 @@ def run_gb300(args):
                   select_launches=int(n_sel))
 
     ctx = context_rows(g, wl.context, wl.context)
-    bbytes, bflops, parts = block_cost(g, wl.head_width, ctx, wl.batch)
+    bbytes, bflops, parts = block_cost(g, wl.head_width, ctx, wl.batch, 4 if args.cache == "planes" else 2)
     achieved = bbytes / block_s / 1e9
     roof = {
         "what": "block pass: every kernel of one block (%d launches) replayed from a CUDA graph, the L2 "
@@ -510,7 +517,7 @@ def run_gb300(args):
     }
     if b.settle_in_step:
         rps = phases["settle_rows_per_s"]
-        sb, sf = settle_cost_per_row(g, SETTLE_CHUNK)
+        sb, sf = settle_cost_per_row(g, SETTLE_CHUNK, 4 if args.cache == "planes" else 2)
         roof["settle"] = {
             "what": f"settle in {SETTLE_CHUNK}-row calls (fc GEMM, norm, every layer's K/V GEMM, key norm and "
                     "rotation, cache write), replayed from a CUDA graph",
@@ -530,7 +537,7 @@ def run_gb300(args):
         "warmup": args.warmup, "ms_per_step": round(step_ms, 5), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {"workload": wl.name, "description": wl.description, "context": wl.context, "batch": wl.batch,
-                   "block": g.block, "head_width": wl.head_width,
+                   "block": g.block, "head_width": wl.head_width, "kv_cache": args.cache,
                    "step": ("reset + settle(%d rows in %d-row calls) + block + select" % (wl.context, SETTLE_CHUNK))
                    if b.settle_in_step else "one block per sequence + select (contexts settled before)",
                    "l2": "flushed between steps (256 MiB write)", "graph": graph is not None,

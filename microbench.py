@@ -3,6 +3,7 @@
     python microbench.py gemm --rows 151936 --cols 1024 --tokens 15 --kind 4
     python microbench.py gemm --rows 5120 --cols 25600 --tokens 256 --kind 16
     python microbench.py block --workload batched --batch 8
+    python microbench.py settle --workload 27b --rows 256 --calls 4
 
 gemm: random codes / values of the given shape; the L2 cache is flushed
 between launches; prints the mean time and the algorithmic bandwidth of one
@@ -102,6 +103,34 @@ def block(args):
                       "us_per_block": round(a.elapsed_time(b) / args.iters * 1e3, 1)}))
 
 
+def settle(args):
+    """`calls` settles of `rows` tap rows each (positions 0.., one sequence), between
+    cudaProfilerStart and cudaProfilerStop after two untimed ones."""
+    build.build()
+    wl = di.workload(args.workload)
+    g = wl.geometry
+    dev = torch.device("cuda", 0)
+    n = args.rows * args.calls
+    d = Drafter(g, di.make_weights(g, wl.seed), max_batch=1, ctx_cap=n + g.block, cache_format=args.cache,
+                rings="window" if args.rings else None)
+    taps = torch.from_numpy(di.make_taps(g, wl.seed, n)).to(dev)
+    for _ in range(2):
+        d.reset(0, 0)
+        d.settle(0, 0, taps, chunk=args.rows)
+    torch.cuda.synchronize()
+    d.reset(0, 0)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.profiler.start()
+    a.record()
+    d.settle(0, 0, taps, chunk=args.rows)
+    b.record()
+    torch.cuda.synchronize()
+    torch.cuda.profiler.stop()
+    ms = a.elapsed_time(b)
+    print(json.dumps({"settle": wl.name, "rows_per_call": args.rows, "calls": args.calls,
+                      "us_per_call": round(ms / args.calls * 1e3, 1), "rows_per_s": round(n / ms * 1e3, 1)}))
+
+
 def main():
     p = argparse.ArgumentParser()
     sub = p.add_subparsers(dest="cmd", required=True)
@@ -116,9 +145,17 @@ def main():
     k.add_argument("--workload", default="batched", choices=sorted(di.WORKLOADS))
     k.add_argument("--batch", type=int, default=0, help="sequences (default: the workload's)")
     k.add_argument("--iters", type=int, default=5)
+    s = sub.add_parser("settle")
+    s.add_argument("--workload", default="27b", choices=sorted(di.WORKLOADS))
+    s.add_argument("--rows", type=int, default=256)
+    s.add_argument("--calls", type=int, default=4)
+    s.add_argument("--cache", default="planes", choices=["planes", "f16"])
+    s.add_argument("--rings", action="store_true")
     args = p.parse_args()
     if args.cmd == "gemm":
         gemm(args)
+    elif args.cmd == "settle":
+        settle(args)
     else:
         block(args)
 

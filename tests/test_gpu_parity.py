@@ -405,8 +405,10 @@ def test_bookkeeping_against_oracle(fmt, rings):
     rows = di.block_rows(g, 3, a)
 
     def draft(anchor):
+        # planes: an f16 rounding flip of a kernel-projection input (both sides round) moves an
+        # element by about 5e-4 of its value; one f16 per cache element: the contract's bound
         r = p.draft([anchor], [rows], [a])[0]
-        assert r["logit_err"] < (5e-4 if fmt == "f16" else 1e-4), r
+        assert r["logit_err"] < (LOGIT_REL if fmt == "f16" else 5e-4), r
 
     p.settle(0, 0, taps[:100], chunk=37)            # trims after the third call
     assert p.check_cache() < p.cache_rel
