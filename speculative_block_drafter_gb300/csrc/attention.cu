@@ -22,7 +22,6 @@
 
 namespace dfl {
 
-constexpr int ATT_THREADS = 256;
 constexpr int CH = 64;              // keys per chunk
 constexpr int QMAX = 64;            // queries per CTA (rep * block)
 // A split's partial row in global memory: o[hd], m, l, two floats of padding so
@@ -96,15 +95,74 @@ __device__ __forceinline__ void tma_load4(uint32_t dst, const CUtensorMap *m, in
       "l"((uint64_t)m), "r"(x), "r"(p), "r"(h), "r"(z), "r"(bar)
       : "memory");
 }
-__device__ __forceinline__ void ldsm4(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-               : "r"(addr));
-}
-__device__ __forceinline__ void ldsm4t(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-               : "r"(addr));
+
+// ---------------------------------------------------------------- the split kernel
+//
+// One CTA per (split, KV head, sequence): the Q = rep * R queries of the KV
+// head over the split's context keys in chunks of 64 (the last split takes the
+// block's own R rows as a final chunk of 16), on the 5th-generation tensor
+// cores with everything the products need in tensor memory (512 columns, one
+// CTA an SM; lanes = query rows, the Q real ones first, the rest zero):
+//   QH, QL   the queries as f16 hi/lo planes (the A operand of S = Q K^T)
+//   S0, S1   two score buffers (64 columns each)
+//   P0, P1   two probability buffers, hi and lo planes (A of O += P V)
+//   O        the output accumulator (HD columns)
+// The context caches and the block's own K/V hold f16 values in PL planes per
+// row and head (PL = 2: hi, lo; PL = 1: one f16), written once when the rows
+// were settled or projected.
+//   warp 8    tensor copies of each chunk's K and V planes (boxes of 64 rows x
+//             64 halves, 128-byte swizzled) into a ring of stages
+//   warp 9    the MMAs, one thread: S = Qh Kh + Qh Kl + Ql Kh (PL = 2) or
+//             Qh K + Ql K (PL = 1), K read K-major from the stage; then, once
+//             the chunk's P is written, O += Ph Vh + Ph Vl + Pl Vh (or Ph V +
+//             Pl V), V read MN-major from the same stage. QK of chunk j+1 is
+//             issued before PV of chunk j, so the softmax of one chunk runs
+//             while the tensor cores take the next.
+//   warps 0-7 two threads a query row, each with half of a chunk's keys (warp w
+//             takes the rows of tensor-memory lanes 32 (w % 4).. and key half
+//             w / 4): the scores from tensor memory, the window mask, the row's
+//             largest score exchanged with the partner through shared memory,
+//             an online softmax, P as hi/lo planes into tensor memory; at the
+//             end the row's (o, m, l) to the partials. Warps whose rows are all
+//             past the Q queries skip the arithmetic.
+// Online softmax in the base-2 domain with a lazy reference: P = 2^(x - m) with
+// m the largest score seen when it last moved by more than TAU, so that P <=
+// 2^TAU stays in f16's range and O (in tensor memory) is rescaled only when m
+// moves that far; O and l always share m, so the result is exact. Keys past a
+// chunk's end are masked and their V rows zeroed in the stage before the P.V
+// products read them. The softmax warps meet at a named barrier with an AND
+// of their wait results, so that a wait that gave up ends all of them together.
+template <int HD, int PL>
+struct AttnTc {
+  static constexpr int QH = 0, QL = HD / 2;          // HD/2 columns a plane (f16 pairs)
+  static constexpr int S0 = HD;                      // + 64 * buffer
+  static constexpr int P0 = HD + 128;                // + 64 * buffer: hi 32 columns, lo 32 columns
+  static constexpr int OC = HD + 256;                // HD columns
+  static_assert(OC + HD <= 512, "tensor memory");
+  static constexpr int BOX = CH * 128;               // 64 rows x 64 halves
+  static constexpr int REGION = (HD / 64) * BOX;     // one plane of K or V of a chunk
+  static constexpr int STAGE = 2 * PL * REGION;      // K planes, then V planes
+  static constexpr int STAGES = (192 * 1024) / STAGE < 6 ? (192 * 1024) / STAGE : 6;
+  // kvfull, kvempty (a stage each), qfull, sfull[2], sfree[2], pfull[2], pfree[2], obar, fin
+  static constexpr int NBAR = 2 * STAGES + 11;
+  // + alignment, barriers, the tensor-memory address; and 20 KB past them that no
+  // operand descriptor of the last stage can reach beyond
+  static constexpr size_t BYTES = (size_t)STAGES * STAGE + 1024 + 8 * NBAR + 16 + 20 * 1024;
+};
+constexpr int ATT_TC_THREADS = 320;
+constexpr int ATT_SM_THREADS = 256;  // the softmax warps 0-7
+constexpr float ATT_TAU = 11.f;      // P <= 2^11 between rescales
+
+// bar.red.and over the softmax warps (named barrier 1): every thread waits for
+// all ATT_SM_THREADS and gets the AND of their `p`.
+__device__ __forceinline__ bool sm_and(bool p) {
+  uint32_t r;
+  asm volatile(
+      "{\n .reg .pred a, b;\n setp.ne.u32 a, %1, 0;\n bar.red.and.pred b, 1, %2, a;\n selp.u32 %0, 1, 0, b;\n}\n"
+      : "=r"(r)
+      : "r"((uint32_t)p), "n"(ATT_SM_THREADS)
+      : "memory");
+  return r != 0;
 }
 
 // f32 pair -> f16 hi/lo pairs without the conversion unit: hi keeps the top 11
@@ -122,72 +180,26 @@ __device__ __forceinline__ void split_hl(float x0, float x1, uint32_t &hi, uint3
   lo = f16x2_rn(x0 - h0, x1 - h1);
 }
 
-// Three-term product of f16 hi/lo pairs: acc += ah.bh + ah.bl + al.bh (about 22 bits).
-__device__ __forceinline__ void mma3(float (&acc)[4], const uint32_t (&ah)[4], const uint32_t (&al)[4], uint32_t bh0,
-                                     uint32_t bh1, uint32_t bl0, uint32_t bl1) {
-  mma16816(acc, ah, bh0, bh1);
-  mma16816(acc, ah, bl0, bl1);
-  mma16816(acc, al, bh0, bh1);
-}
-
-// ---------------------------------------------------------------- the split kernel
-//
-// One CTA per (split, KV head, sequence): the rep*R queries of the KV head over
-// the split's context keys in chunks of 64 (the last split takes the block's
-// own R rows as a final chunk). The context caches and the block's own K/V hold
-// f16 values per row and head in PL planes (PL = 2: hi, lo; PL = 1: one f16),
-// written once when the rows were settled or projected. Warp 0 loads each
-// chunk's K and V planes with tensor copies (boxes of 64 rows x 64 halves,
-// 128-byte swizzled) into a ring of stages; the warps read their B fragments
-// with ldmatrix (K as stored, V transposed) and hold the queries' hi/lo
-// fragments in registers. The products: q.k as qh.kh + qh.kl + ql.kh (PL = 2)
-// or qh.k + ql.k (PL = 1), p.v likewise with p split into hi and lo. Warp w
-// takes query block w % QW and key group w / QW of every chunk; each keeps a
-// running (m, l, o), merged in the CTA at the end. Rows past a chunk's keys
-// (the context's end, or the block's own R rows) hold whatever the copy or an
-// earlier chunk left: their scores are masked and, before P.V, the warps whose
-// key range reaches them zero their V planes.
-template <int PL>
-struct AttnRing {
-  static constexpr int BOX = CH * 128;       // 64 rows x 64 halves
-  static constexpr int REGION = 2 * BOX;     // one plane of K or V of a chunk (hd <= 128)
-  static constexpr int STAGE = 2 * PL * REGION;  // K planes, then V planes
-  static constexpr int STAGES = PL == 2 ? 3 : 5;
-  static constexpr size_t BYTES = (size_t)STAGES * STAGE + 1024 + 16 * STAGES;  // + alignment, barriers
-};
-
-// Byte offset of 16-byte chunk j (8 halves: dimensions 8j..8j+7) of row r in a
-// plane region: box j / 8, swizzled within the row's 128 bytes.
-__device__ __forceinline__ uint32_t plane_off(int r, int j) {
-  return (uint32_t)((j >> 3) * (CH * 128) + r * 128 + (((j & 7) ^ (r & 7)) << 4));
-}
-
-template <int HD, int KG, int PL>
-__global__ void __launch_bounds__(ATT_THREADS, 1) k_attn(const float *__restrict__ q, const __grid_constant__ AttnArgs args,
-                                                         int heads, int kv, int R, int window, float scale, int nsplit,
-                                                         int cps, float *__restrict__ part) {
-  using RG = AttnRing<PL>;
-  constexpr int S = RG::STAGES;
-  constexpr int H2 = HD / 64;        // boxes of a row
-  constexpr int KW = CH / KG;        // keys per warp per chunk
-  constexpr int NT = KW / 8;         // n8 tiles of scores
-  constexpr int KS = KW / 16;        // k16 steps of P . V
-  constexpr int OT = HD / 8;         // n8 tiles of the output
-  static_assert(NT % 2 == 0 && OT % 2 == 0 && KS >= 1, "fragments load in pairs of tiles");
-  extern __shared__ __align__(16) uint8_t smraw[];
+template <int HD, int PL>
+__global__ void __launch_bounds__(ATT_TC_THREADS, 1)
+    k_attn_tc(const float *__restrict__ q, const __grid_constant__ AttnArgs args, int heads, int kv, int R, int window,
+              float scale, int nsplit, int cps, float *__restrict__ part) {
+  using C = AttnTc<HD, PL>;
+  constexpr int S = C::STAGES;
+  constexpr int H2 = HD / 64;
+  extern __shared__ __align__(1024) uint8_t smraw[];
   uint8_t *sm = smraw + ((1024 - (smem_u32(smraw) & 1023)) & 1023);
   const uint32_t ring = smem_u32(sm);
-  const uint32_t full0 = ring + S * RG::STAGE, empty0 = full0 + 8 * S;
+  uint64_t *bars = (uint64_t *)(sm + S * C::STAGE);
+  uint32_t *tslot = (uint32_t *)(bars + C::NBAR);
+  const uint32_t kvfull = smem_u32(bars), kvempty = kvfull + 8 * S, qfull = kvempty + 8 * S;
+  const uint32_t sfull = qfull + 8, sfree = sfull + 16, pfull = sfree + 16, pfree = pfull + 16, obar = pfree + 16;
+  const uint32_t fin = obar + 8;
 
   const int sp = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
   const int rep = heads / kv, Q = rep * R;
-  const int QW = (Q + 15) / 16;
   const AttnSeq &Sq = args.seq[b];
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, gq = lane >> 2, cq = lane & 3;
-  const int qb = warp % QW, kgi = warp / QW;
-  const bool busy = kgi < KG && warp < QW * KG;
-  const int nwarps = ATT_THREADS / 32;
-
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // this CTA's chunks: context chunks [c0, c1), then the block's own rows if last
   const int n = Sq.n;
   const int nctx = (n + CH - 1) / CH;
@@ -195,268 +207,266 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) k_attn(const float *__restrict
   const bool own = sp == nsplit - 1;
   const int nch = (c1 - c0) + (own ? 1 : 0);
 
-  if (tid == 0) {
+  if (threadIdx.x == 0) {
     for (int i = 0; i < S; ++i) {
-      mbar_init(full0 + 8 * i, 1);
-      mbar_init(empty0 + 8 * i, nwarps);
+      mbar_init(kvfull + 8 * i, 1);
+      mbar_init(kvempty + 8 * i, 1);
     }
+    mbar_init(qfull, 128);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(sfull + 8 * i, 1);
+      mbar_init(sfree + 8 * i, ATT_SM_THREADS);
+      mbar_init(pfull + 8 * i, ATT_SM_THREADS);
+      mbar_init(pfree + 8 * i, 1);
+    }
+    mbar_init(obar, 1);
+    mbar_init(fin, 1);
     mbar_fence_init();
   }
   pdl_wait();
+  if (warp == 0) tmem_alloc(smem_u32(tslot), 512);
+  tc_fence_before();
   __syncthreads();
+  tc_fence_after();
+  const uint32_t tb = *tslot;
 
-  // warp 0, lane 0: the 4 * H2 tensor copies of chunk j into stage st
-  auto fill = [&](int j, int st) {
-    if (lane != 0) return;
-    const bool is_own = own && j == nch - 1;
-    const CUtensorMap *km = is_own ? &args.own_k : &Sq.kmap;
-    const CUtensorMap *vm = is_own ? &args.own_v : &Sq.vmap;
-    const int z = is_own ? b * R : (int)(Sq.row0 + (int64_t)(c0 + j) * CH);
-    const uint32_t rows = is_own ? R : CH;
-    const uint32_t bar = full0 + 8 * st, base = ring + st * RG::STAGE;
-    mbar_expect_tx(bar, 2 * PL * H2 * rows * 128);
+  if (warp == 8) {
+    // the K and V planes of chunk j into stage j % S
+    if (lane == 0) {
+      int issued = 0;
+      for (int j = 0; j < nch; ++j, ++issued) {
+        const int st = j % S;
+        if (j >= S && !mbar_wait(kvempty + 8 * st, ((j / S) - 1) & 1)) break;
+        const bool is_own = own && j == nch - 1;
+        const CUtensorMap *km = is_own ? &args.own_k : &Sq.kmap;
+        const CUtensorMap *vm = is_own ? &args.own_v : &Sq.vmap;
+        const int z = is_own ? b * R : (int)(Sq.row0 + (int64_t)(c0 + j) * CH);
+        const uint32_t rows = is_own ? R : CH;
+        const uint32_t bar = kvfull + 8 * st, base = ring + st * C::STAGE;
+        mbar_expect_tx(bar, 2 * PL * H2 * rows * 128);
 #pragma unroll
-    for (int h = 0; h < H2; ++h)
+        for (int h = 0; h < H2; ++h)
 #pragma unroll
-      for (int p = 0; p < PL; ++p) {
-        tma_load4(base + p * RG::REGION + h * RG::BOX, km, 64 * h, p, g, z, bar);
-        tma_load4(base + (PL + p) * RG::REGION + h * RG::BOX, vm, 64 * h, p, g, z, bar);
-      }
-  };
-  int issued = 0;  // chunks warp 0 has filled
-  if (warp == 0)
-    for (; issued < S && issued < nch; ++issued) fill(issued, issued);
-
-  // the queries' hi/lo A fragments (rows qb*16 + gq and + 8)
-  uint32_t qh[HD / 16][4], ql[HD / 16][4];
-  const int qi0 = qb * 16 + gq, qi1 = qi0 + 8;
-  {
-    const float *q0 = nullptr, *q1 = nullptr;
-    if (qi0 < Q) q0 = q + ((int64_t)b * R + qi0 % R) * heads * HD + (g * rep + qi0 / R) * HD;
-    if (qi1 < Q) q1 = q + ((int64_t)b * R + qi1 % R) * heads * HD + (g * rep + qi1 / R) * HD;
-#pragma unroll
-    for (int ks = 0; ks < HD / 16; ++ks) {
-      const int c = ks * 16 + 2 * cq;
-      const float2 x00 = q0 ? *(const float2 *)(q0 + c) : make_float2(0.f, 0.f);
-      const float2 x10 = q1 ? *(const float2 *)(q1 + c) : make_float2(0.f, 0.f);
-      const float2 x01 = q0 ? *(const float2 *)(q0 + c + 8) : make_float2(0.f, 0.f);
-      const float2 x11 = q1 ? *(const float2 *)(q1 + c + 8) : make_float2(0.f, 0.f);
-      split_hl(x00.x, x00.y, qh[ks][0], ql[ks][0]);
-      split_hl(x10.x, x10.y, qh[ks][1], ql[ks][1]);
-      split_hl(x01.x, x01.y, qh[ks][2], ql[ks][2]);
-      split_hl(x11.x, x11.y, qh[ks][3], ql[ks][3]);
-    }
-  }
-  const int r0 = qi0 % R, r1 = qi1 % R;
-  // ldmatrix lane roles: row within an 8x8 matrix and which of the four matrices
-  const int mr = lane & 7, mi = lane >> 3;
-
-  float o[OT][4];
-#pragma unroll
-  for (int t = 0; t < OT; ++t) o[t][0] = o[t][1] = o[t][2] = o[t][3] = 0.f;
-  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-  bool ok = true;
-
-  for (int j = 0; j < nch && ok; ++j) {
-    const int st = j % S;
-    ok = mbar_wait(full0 + 8 * st, (j / S) & 1);
-    ok = __all_sync(0xffffffffu, ok);
-    if (!ok) break;
-    const bool is_own = own && j == nch - 1;
-    const int kb = (c0 + j) * CH;
-    const int cnt = is_own ? R : min(CH, n - kb);
-    uint8_t *stp = sm + st * RG::STAGE;
-    // K planes at regions 0..PL-1, V planes at PL..2PL-1 (klo, vlo unused with one plane)
-    const uint32_t khi = smem_u32(stp), klo = khi + RG::REGION, vhi = khi + PL * RG::REGION, vlo = vhi + RG::REGION;
-    const int kk0 = kgi * KW;
-    if (busy && cnt < kk0 + KW) {
-      // zero the V rows of this warp's keys past the chunk's (both planes, every box)
-      const int z0 = max(kk0, cnt), nz = kk0 + KW - z0;
-      for (int idx = lane; idx < nz * PL * H2 * 8; idx += 32) {
-        const int row = z0 + idx / (PL * H2 * 8), rest = idx % (PL * H2 * 8);
-        const int pl = rest / (H2 * 8), bx = (rest / 8) % H2, ch = rest % 8;
-        *(uint4 *)(stp + (PL + pl) * RG::REGION + bx * RG::BOX + row * 128 + ch * 16) = make_uint4(0u, 0u, 0u, 0u);
-      }
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // before the stage's next tensor copy
-      __syncwarp();
-    }
-    if (busy) {
-      float sc[NT][4];
-      // S = Q . K^T: per k16 step and pair of key tiles the four 8x8 matrices
-      // (tile t, dims 16ks..+8), (t, +8..+16), (t+1, ..), (t+1, ..) of each plane.
-      // The three products go to separate accumulators (two with four tiles),
-      // so that the MMAs of a step do not wait on one another.
-      constexpr int NA = (PL == 2 && NT == 2) ? 3 : 2;
-      float sa[NA][NT][4];
-#pragma unroll
-      for (int a = 0; a < NA; ++a)
-#pragma unroll
-        for (int t = 0; t < NT; ++t) sa[a][t][0] = sa[a][t][1] = sa[a][t][2] = sa[a][t][3] = 0.f;
-#pragma unroll
-      for (int ks = 0; ks < HD / 16; ++ks) {
-#pragma unroll
-        for (int t = 0; t < NT; t += 2) {
-          const uint32_t off = plane_off(kk0 + 8 * (t + (mi >> 1)) + mr, 2 * ks + (mi & 1));
-          uint32_t h0, h1, h2, h3;
-          ldsm4(khi + off, h0, h1, h2, h3);
-          mma16816(sa[0][t], qh[ks], h0, h1);
-          mma16816(sa[0][t + 1], qh[ks], h2, h3);
-          if constexpr (PL == 2) {
-            uint32_t w0, w1, w2, w3;
-            ldsm4(klo + off, w0, w1, w2, w3);
-            mma16816(sa[1][t], qh[ks], w0, w1);
-            mma16816(sa[1][t + 1], qh[ks], w2, w3);
+          for (int p = 0; p < PL; ++p) {
+            tma_load4(base + p * C::REGION + h * C::BOX, km, 64 * h, p, g, z, bar);
+            tma_load4(base + (PL + p) * C::REGION + h * C::BOX, vm, 64 * h, p, g, z, bar);
           }
-          mma16816(sa[NA - 1][t], ql[ks], h0, h1);
-          mma16816(sa[NA - 1][t + 1], ql[ks], h2, h3);
+      }
+      // no copy still bound for this CTA's shared memory when it leaves (the
+      // copies of the last stages issued; a bounded wait each)
+      for (int j = (issued > S ? issued - S : 0); j < issued; ++j) mbar_wait(kvfull + 8 * (j % S), (j / S) & 1);
+    }
+  } else if (warp == 9) {
+    if (lane == 0 && nch > 0) {
+      bool ok = mbar_wait(qfull, 0);
+      tc_fence_after();
+      for (int j = 0; j <= nch && ok; ++j) {
+        if (j < nch) {
+          // S = Q K^T of chunk j into score buffer j & 1
+          const int st = j % S, sb = j & 1;
+          if (!mbar_wait(kvfull + 8 * st, (j / S) & 1)) break;
+          if (j >= 2 && !mbar_wait(sfree + 8 * sb, ((j >> 1) - 1) & 1)) break;
+          tc_fence_after();
+          const bool is_own = own && j == nch - 1;
+          const uint32_t idesc = f16_idesc(128, is_own ? 16 : CH);
+          const uint32_t kh = ring + st * C::STAGE, kl = kh + C::REGION;
+          const uint32_t dS = tb + C::S0 + sb * 64;
+#pragma unroll
+          for (int ks = 0; ks < HD / 16; ++ks) {
+            const uint32_t off = (ks >> 2) * C::BOX + (ks & 3) * 32;
+            mma_ts(dS, tb + C::QH + ks * 8, sw128_desc(kh + off), idesc, ks > 0);
+            if (PL == 2) mma_ts(dS, tb + C::QH + ks * 8, sw128_desc(kl + off), idesc, 1);
+            mma_ts(dS, tb + C::QL + ks * 8, sw128_desc(kh + off), idesc, 1);
+          }
+          mma_commit(sfull + 8 * sb);
+        }
+        if (j >= 1) {
+          // O += P V of chunk j - 1, once its P is written
+          const int jj = j - 1, st = jj % S, pb = jj & 1;
+          if (!mbar_wait(pfull + 8 * pb, (jj >> 1) & 1)) break;
+          tc_fence_after();
+          const bool is_own = own && jj == nch - 1;
+          const int ksteps = is_own ? 1 : CH / 16;
+          const uint32_t idesc = f16_idesc_bmn(128, HD);
+          const uint32_t vh = ring + st * C::STAGE + PL * C::REGION, vl = vh + C::REGION;
+          const uint32_t ph = tb + C::P0 + pb * 64, pl = ph + 32;
+          for (int kk = 0; kk < ksteps; ++kk) {
+            const uint64_t bh = sw128_mn_desc(vh + kk * 2048, C::BOX), bl = sw128_mn_desc(vl + kk * 2048, C::BOX);
+            mma_ts(tb + C::OC, ph + kk * 8, bh, idesc, (jj > 0 || kk > 0));
+            if (PL == 2) mma_ts(tb + C::OC, ph + kk * 8, bl, idesc, 1);
+            mma_ts(tb + C::OC, pl + kk * 8, bh, idesc, 1);
+          }
+          mma_commit(obar);
+          mma_commit(pfree + 8 * pb);
+          mma_commit(kvempty + 8 * st);
         }
       }
+      // every MMA issued has completed before the tensor memory is freed
+      mma_commit(fin);
+      mbar_wait(fin, 0);
+    }
+  } else {
+    // warps 0-7: query row `row` (tensor-memory lane), key half `kh` of each chunk
+    // the rows' largest scores per key half, by chunk parity (a slot is written
+    // again two chunks later, after both halves passed the barrier between); the sums
+    __shared__ float xch[2][2][128], lsum[2][128];
+    const int row = threadIdx.x & 127, kh = warp >> 2;
+    const uint32_t lrow = (uint32_t)((warp & 3) * 32) << 16;
+    const bool live = row < Q;
+    const bool dead = (warp & 3) * 32 >= Q;  // every row of this warp past the queries
+    const int rr = row % R;
+    const float sl2 = scale * 1.4426950408889634f;  // scores to the base-2 domain
+    if (kh == 0) {
+      // the row's query (normalised, rotated) as hi/lo planes into tensor memory
+      const float *qr = live ? q + ((int64_t)b * R + rr) * heads * HD + (g * rep + row / R) * HD : nullptr;
 #pragma unroll
-      for (int t = 0; t < NT; ++t)
+      for (int half = 0; half < H2; ++half) {
+        uint32_t vh[32], vl[32];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) sc[t][e] = sa[0][t][e] + (NA == 3 ? sa[1][t][e] + sa[2][t][e] : sa[1][t][e]);
-      // mask, scale, online softmax (rows gq, gq+8; the 4 lanes of a row hold its 2*NT keys)
-      float mx0 = -INFINITY, mx1 = -INFINITY;
+        for (int e = 0; e < 32; ++e) {
+          float2 x = make_float2(0.f, 0.f);
+          if (live) x = *(const float2 *)(qr + half * 64 + 2 * e);
+          split_hl(x.x, x.y, vh[e], vl[e]);
+        }
+        tmem_st32(tb + lrow + C::QH + half * 32, vh);
+        tmem_st32(tb + lrow + C::QL + half * 32, vl);
+      }
+      tc_wait_st();
+      tc_fence_before();
+      mbar_arrive(qfull);
+    }
+    float mref = -INFINITY, l = 0.f;
+    bool ok = true;
+    for (int j = 0; j < nch; ++j) {
+      const int sb = j & 1, st = j % S;
+      const bool is_own = own && j == nch - 1;
+      const int kb = (c0 + j) * CH;
+      const int cnt = is_own ? R : min(CH, n - kb);
+      const int N = is_own ? 16 : CH;
+      const int k0 = kh * 32;  // this thread's keys k0 .. k0 + 31 of the chunk
+      bool w_ok = __all_sync(0xffffffffu, mbar_wait(sfull + 8 * sb, (j >> 1) & 1));
+      tc_fence_after();
+      float x[32];
+      float mh = -INFINITY;
+      if (!dead && w_ok) {
+        uint32_t r0[32];
+        tmem_ld32(tb + lrow + C::S0 + sb * 64 + k0, r0);
+        tc_wait_ld();
 #pragma unroll
-      for (int t = 0; t < NT; ++t) {
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int key = kk0 + t * 8 + 2 * cq + (e & 1);
-          const int qi = (e < 2) ? qi0 : qi1;
-          const int rr = (e < 2) ? r0 : r1;
-          bool vis = key < cnt && qi < Q;
-          if (vis && !is_own && window > 0) vis = Sq.lo + kb + key >= Sq.anchor + rr + 1 - window;
-          const float x = vis ? sc[t][e] * scale : -INFINITY;
-          sc[t][e] = x;
-          if (e < 2) mx0 = fmaxf(mx0, x);
-          else mx1 = fmaxf(mx1, x);
+        for (int e = 0; e < 32; ++e) {
+          const int k = k0 + e;
+          bool vis = live && k < cnt;
+          if (vis && !is_own && window > 0) vis = Sq.lo + kb + k >= Sq.anchor + rr + 1 - window;
+          x[e] = vis ? __uint_as_float(r0[e]) * sl2 : -INFINITY;
+          mh = fmaxf(mh, x[e]);
         }
       }
-      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
-      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
-      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
-      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-      const float n0 = fmaxf(m0, mx0), n1 = fmaxf(m1, mx1);
-      const float a0 = n0 == -INFINITY ? 1.f : expf(m0 - n0);
-      const float a1 = n1 == -INFINITY ? 1.f : expf(m1 - n1);
-      m0 = n0;
-      m1 = n1;
-      float s0 = 0.f, s1 = 0.f;
-#pragma unroll
-      for (int t = 0; t < NT; ++t) {
-        sc[t][0] = sc[t][0] == -INFINITY ? 0.f : expf(sc[t][0] - n0);
-        sc[t][1] = sc[t][1] == -INFINITY ? 0.f : expf(sc[t][1] - n0);
-        sc[t][2] = sc[t][2] == -INFINITY ? 0.f : expf(sc[t][2] - n1);
-        sc[t][3] = sc[t][3] == -INFINITY ? 0.f : expf(sc[t][3] - n1);
-        s0 += sc[t][0] + sc[t][1];
-        s1 += sc[t][2] + sc[t][3];
-      }
-      l0 = l0 * a0 + s0;
-      l1 = l1 * a1 + s1;
-      if (__any_sync(0xffffffffu, a0 != 1.f || a1 != 1.f)) {  // a row's maximum moved
-#pragma unroll
-        for (int t = 0; t < OT; ++t) {
-          o[t][0] *= a0;
-          o[t][1] *= a0;
-          o[t][2] *= a1;
-          o[t][3] *= a1;
+      tc_fence_before();
+      mbar_arrive(sfree + 8 * sb);
+      // keys past the chunk's end: their V rows zeroed before the P.V products read them
+      if (cnt < N && w_ok) {
+        const int nz = N - cnt;
+        uint8_t *vst = sm + st * C::STAGE + PL * C::REGION;
+        for (int idx = threadIdx.x; idx < nz * PL * H2 * 8; idx += ATT_SM_THREADS) {
+          const int r = cnt + idx / (PL * H2 * 8), rest = idx % (PL * H2 * 8);
+          const int pl = rest / (H2 * 8), bx = (rest / 8) % H2, ch = rest % 8;
+          *(uint4 *)(vst + pl * C::REGION + bx * C::BOX + r * 128 + ch * 16) = make_uint4(0u, 0u, 0u, 0u);
         }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       }
-      // O += P . V: P as hi/lo A fragments from the scores; V by transposed
-      // ldmatrix: (keys +0..8, dims tile t), (keys +8..16, t), (.., t+1), (.., t+1)
+      xch[sb][kh][row] = mh;
+      ok = sm_and(ok && w_ok);
+      if (!ok) break;
+      const float mx = fmaxf(xch[sb][0][row], xch[sb][1][row]);
+      // the reference moves (both halves of a row decide alike); O's half `kh` of
+      // the columns is rescaled once the products of the chunks before are done
+      const bool up = mx > mref + ATT_TAU;
+      if (__any_sync(0xffffffffu, up)) {
+        float alpha = 1.f;
+        if (up) {
+          alpha = mref == -INFINITY ? 0.f : exp2f(mref - mx);
+          l *= alpha;
+          mref = mx;
+        }
+        if (j > 0 && !dead) {
+          ok = __all_sync(0xffffffffu, mbar_wait(obar, (j - 1) & 1));
+          tc_fence_after();
+          if (ok) {
 #pragma unroll
-      for (int js = 0; js < KS; ++js) {
-        uint32_t ph[4], pl[4];
-        split_hl(sc[2 * js][0], sc[2 * js][1], ph[0], pl[0]);
-        split_hl(sc[2 * js][2], sc[2 * js][3], ph[1], pl[1]);
-        split_hl(sc[2 * js + 1][0], sc[2 * js + 1][1], ph[2], pl[2]);
-        split_hl(sc[2 * js + 1][2], sc[2 * js + 1][3], ph[3], pl[3]);
-        const int row = kk0 + 16 * js + 8 * (mi & 1) + mr;
+            for (int c = 0; c < HD / 64; ++c) {
+              uint32_t o[32];
+              const uint32_t col = tb + lrow + C::OC + kh * (HD / 2) + c * 32;
+              tmem_ld32(col, o);
+              tc_wait_ld();
 #pragma unroll
-        for (int t = 0; t < OT; t += 2) {
-          const uint32_t off = plane_off(row, t + (mi >> 1));
-          uint32_t h0, h1, h2, h3;
-          ldsm4t(vhi + off, h0, h1, h2, h3);
-          if constexpr (PL == 2) {
-            uint32_t w0, w1, w2, w3;
-            ldsm4t(vlo + off, w0, w1, w2, w3);
-            mma3(o[t], ph, pl, h0, h1, w0, w1);
-            mma3(o[t + 1], ph, pl, h2, h3, w2, w3);
-          } else {
-            mma16816(o[t], ph, h0, h1);
-            mma16816(o[t + 1], ph, h2, h3);
-            mma16816(o[t], pl, h0, h1);
-            mma16816(o[t + 1], pl, h2, h3);
+              for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+              tmem_st32(col, o);
+            }
+            tc_wait_st();
           }
         }
       }
-    }
-    // release the stage; warp 0 refills it with the chunk S ahead
-    __syncwarp();
-    if (lane == 0) mbar_arrive(empty0 + 8 * st);
-    if (warp == 0 && j + S < nch) {
-      ok = mbar_wait(empty0 + 8 * st, (j / S) & 1);
-      ok = __all_sync(0xffffffffu, ok);
-      if (ok) {
-        fill(j + S, st);
-        ++issued;
+      // P = 2^(x - m) of this thread's keys, as hi/lo planes (16 columns each)
+      uint32_t ph[16], pw[16];
+      if (!dead) {
+        float sum = 0.f;
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const float p0 = x[2 * e] == -INFINITY ? 0.f : exp2f(x[2 * e] - mref);
+          const float p1 = x[2 * e + 1] == -INFINITY ? 0.f : exp2f(x[2 * e + 1] - mref);
+          sum += p0 + p1;
+          split_hl(p0, p1, ph[e], pw[e]);
+        }
+        l += sum;
       }
+      if (j >= 2) {
+        ok = ok && __all_sync(0xffffffffu, mbar_wait(pfree + 8 * sb, ((j >> 1) - 1) & 1));
+        tc_fence_after();
+      }
+      if (!dead && ok) {
+        tmem_st16(tb + lrow + C::P0 + sb * 64 + kh * 16, ph);
+        tmem_st16(tb + lrow + C::P0 + sb * 64 + 32 + kh * 16, pw);
+        tc_wait_st();
+      }
+      tc_fence_before();
+      mbar_arrive(pfull + 8 * sb);
+    }
+    // the row's partial: o (unnormalised, against m), m (natural base), l; key
+    // half kh writes o's columns kh * HD/2 ..
+    lsum[kh][row] = l;
+    const bool all_ok = sm_and(ok);
+    l = lsum[0][row] + lsum[1][row];
+    float *out = part + ((int64_t)(b * kv + g) * nsplit + sp) * Q * part_row(HD) + (int64_t)row * part_row(HD);
+    const bool have = all_ok && nch > 0 && !dead && __all_sync(0xffffffffu, mbar_wait(obar, (nch - 1) & 1));
+    if (have) {
+      tc_fence_after();
+#pragma unroll
+      for (int c = 0; c < HD / 64; ++c) {
+        uint32_t o[32];
+        tmem_ld32(tb + lrow + C::OC + kh * (HD / 2) + c * 32, o);
+        tc_wait_ld();
+        if (live)
+#pragma unroll
+          for (int e = 0; e < 32; e += 4)
+            *(float4 *)(out + kh * (HD / 2) + c * 32 + e) = make_float4(
+                __uint_as_float(o[e]), __uint_as_float(o[e + 1]), __uint_as_float(o[e + 2]), __uint_as_float(o[e + 3]));
+      }
+    } else if (live) {
+      for (int c = 0; c < HD / 2; ++c) out[kh * (HD / 2) + c] = 0.f;
+      mref = -INFINITY;
+      l = 0.f;
+    }
+    if (live && kh == 0) {
+      out[HD] = mref == -INFINITY ? -INFINITY : mref * 0.6931471805599453f;
+      out[HD + 1] = l;
     }
   }
-  // every copy issued has landed before the ring becomes the merge scratch (on
-  // the error path too: each stage's latest fill, a bounded wait each)
-  if (warp == 0)
-    for (int j = max(0, issued - S); j < issued; ++j) mbar_wait(full0 + 8 * (j % S), (j / S) & 1);
+  pdl_trigger();  // this CTA's work is done
+  tc_fence_before();
   __syncthreads();
-
-  // in-CTA merge of the key groups: per warp 16 rows x (o, m, l) in the scratch
-  float *scr = (float *)sm;
-  l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
-  l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
-  l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
-  l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
-  if (busy) {
-    float *w = scr + warp * 16 * (HD + 2);
-#pragma unroll
-    for (int t = 0; t < OT; ++t) {
-      w[gq * (HD + 2) + t * 8 + 2 * cq] = o[t][0];
-      w[gq * (HD + 2) + t * 8 + 2 * cq + 1] = o[t][1];
-      w[(gq + 8) * (HD + 2) + t * 8 + 2 * cq] = o[t][2];
-      w[(gq + 8) * (HD + 2) + t * 8 + 2 * cq + 1] = o[t][3];
-    }
-    if (cq == 0) {
-      w[gq * (HD + 2) + HD] = m0;
-      w[gq * (HD + 2) + HD + 1] = l0;
-      w[(gq + 8) * (HD + 2) + HD] = m1;
-      w[(gq + 8) * (HD + 2) + HD + 1] = l1;
-    }
-  }
-  __syncthreads();
-  float *out = part + ((int64_t)(b * kv + g) * nsplit + sp) * Q * part_row(HD);
-  // one warp per query row at a time: the key groups' weights once, then the row
-  for (int qi = warp; qi < Q; qi += ATT_THREADS / 32) {
-    const int qbk = qi / 16, rr = qi % 16;
-    float M = -INFINITY;
-#pragma unroll
-    for (int kg = 0; kg < KG; ++kg) M = fmaxf(M, scr[(kg * QW + qbk) * 16 * (HD + 2) + rr * (HD + 2) + HD]);
-    float wt[KG];
-#pragma unroll
-    for (int kg = 0; kg < KG; ++kg) {
-      const float mk = scr[(kg * QW + qbk) * 16 * (HD + 2) + rr * (HD + 2) + HD];
-      wt[kg] = mk == -INFINITY ? 0.f : expf(mk - M);
-    }
-    float *orow = out + (int64_t)qi * part_row(HD);
-    for (int c = lane; c < HD + 2; c += 32) {
-      float acc = 0.f;
-      if (c == HD) {
-        acc = M;
-      } else {
-#pragma unroll
-        for (int kg = 0; kg < KG; ++kg)
-          acc = fmaf(scr[(kg * QW + qbk) * 16 * (HD + 2) + rr * (HD + 2) + c], wt[kg], acc);  // o, or l at HD + 1
-      }
-      orow[c] = acc;
-    }
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tb, 512);
   }
 }
 
@@ -556,21 +566,21 @@ __global__ void __launch_bounds__(32 * MERGE_WARPS) k_attn_merge(const float *__
   }
 }
 
-template <int HD, int KG, int PL>
+template <int HD, int PL>
 static cudaError_t launch_attn(const float *q, const AttnArgs &args, int batch, int max_n, int heads, int kv, int R,
                                int window, float scale, float *part, float *y, int num_sms, const PackDst *pack,
                                const ZeroSet *zero, cudaStream_t st) {
-  const size_t smem = AttnRing<PL>::BYTES;
+  const size_t smem = AttnTc<HD, PL>::BYTES;
   static PerDevice configured;
-  if (cudaError_t e = smem_limit(k_attn<HD, KG, PL>, (int)smem, configured)) return e;
+  if (cudaError_t e = smem_limit(k_attn_tc<HD, PL>, (int)smem, configured)) return e;
   int ns, cps;
   plan_splits(batch * kv, max_n, num_sms, ns, cps);
   // With short splits the block's own rows get a split of their own (the last
   // one, past every context chunk), so that no CTA does twice the others' work.
   if (cps <= 4 && max_n > 0) ++ns;
   dim3 grid(ns, kv, batch);
-  cudaError_t e = launch_pdl(k_attn<HD, KG, PL>, grid, dim3(ATT_THREADS), smem, st, 1, q, args, heads, kv, R, window,
-                             scale, ns, cps, part);
+  cudaError_t e = launch_pdl(k_attn_tc<HD, PL>, grid, dim3(ATT_TC_THREADS), smem, st, 1, q, args, heads, kv, R,
+                             window, scale, ns, cps, part);
   if (e != cudaSuccess) return e;
   const int Q = heads / kv * R;
   const int work = (kv * Q + MERGE_WARPS - 1) / MERGE_WARPS;
@@ -590,10 +600,7 @@ template <int HD, int PL>
 static cudaError_t launch_attn_hd(const float *q, const AttnArgs &args, int batch, int max_n, int heads, int kv, int R,
                                   int window, float scale, float *part, float *y, int num_sms, const PackDst *pack,
                                   const ZeroSet *zero, cudaStream_t st) {
-  const int QW = (heads / kv * R + 15) / 16;
-  if (QW >= 3)
-    return launch_attn<HD, 2, PL>(q, args, batch, max_n, heads, kv, R, window, scale, part, y, num_sms, pack, zero, st);
-  return launch_attn<HD, 4, PL>(q, args, batch, max_n, heads, kv, R, window, scale, part, y, num_sms, pack, zero, st);
+  return launch_attn<HD, PL>(q, args, batch, max_n, heads, kv, R, window, scale, part, y, num_sms, pack, zero, st);
 }
 
 cudaError_t attention(const float *q, const CUtensorMap &own_k, const CUtensorMap &own_v, const AttnSeq *seqs,

@@ -266,9 +266,9 @@ int settle_call(dflash_t *d, int seq, const float *taps, int n, cudaStream_t st)
   const int hs = g.hidden, tw = g.taps * g.hidden, kvd = g.kv_heads * g.head_dim;
   const dfl::TcJob fc{d->w.fc.data, nullptr, d->x, hs, hs};
   DF_CUDA(dfl::tc_gemm_f16(&fc, 1, taps, tw, n, tw, d->act, d->num_sms, st));
-  DF_CUDA(dfl::rmsnorm(d->x, d->w.hidden_norm, d->x, n, hs, (float)g.eps, 1, -1, -1, st));
-  // k = Wk t, v = Wv t of every layer in one GEMM (into the workspace), then
-  // k normed and rotated and both written into the caches
+  // the hidden norm is taken by the K/V GEMM's packing of t (below)
+  // k = Wk rms(t), v = Wv rms(t) of every layer in one GEMM (into the
+  // workspace), then k normed and rotated and both written into the caches
   dfl::WideJob kv[dfl::WIDE_MAX_JOBS];
   dfl::CtxWrite W{};
   cache_rows(d, seq, W);
@@ -280,7 +280,8 @@ int settle_call(dflash_t *d, int seq, const float *taps, int n, cudaStream_t st)
     kv[2 * l] = dfl::WideJob{L.k.data, L.k.scales, yk, kvd, kvd, 0};
     kv[2 * l + 1] = dfl::WideJob{L.v.data, L.v.scales, yv, kvd, kvd, 0};
   }
-  DF_CUDA(dfl::wide_gemm(kv, 2 * g.layers, 0, true, g.quant_group, d->x, hs, n, hs, d->act, d->num_sms, st));
+  DF_CUDA(dfl::wide_gemm(kv, 2 * g.layers, 0, true, g.quant_group, d->x, hs, n, hs, d->act, d->num_sms, st,
+                          d->w.hidden_norm, (float)g.eps));
   DF_CUDA(dfl::ctx_planes(W, g.layers, n, g.kv_heads, g.head_dim, d->planes, (float)g.eps, d->inv.data(),
                            s.first + s.len, s.len, true, st));
   s.len += n;

@@ -505,13 +505,86 @@ __global__ void k_wide_pack(const float *__restrict__ X, int ldx, WideArgs A, in
   }
 }
 
+// The token tiles of rows that still need their RMS norm (the settle's t before
+// the K/V GEMM): block b < ntt * N takes token row b, x * (mean(x^2) + eps)^-1/2
+// * w into its packed chunks (zeros past T); the blocks past them clear split
+// tiles as k_wide_pack does. One launch and one round trip of the rows fewer
+// than a norm kernel before the packing.
+constexpr int WR_THREADS = 256;
+template <int PLANES>
+__global__ void __launch_bounds__(WR_THREADS) k_wide_rms_pack(const float *__restrict__ X, int ldx,
+                                                              const float *__restrict__ w, float eps, WideArgs A, int Q,
+                                                              uint4 *__restrict__ dst, int pack_blocks) {
+  pdl_wait();
+  pdl_trigger();
+  if ((int)blockIdx.x >= pack_blocks) {
+    // the split tiles' outputs: the clearing blocks of k_wide_pack
+    const int zb = blockIdx.x - pack_blocks;
+    const int part = zb % WZ_PARTS, q = zb / WZ_PARTS + 1;
+    const int64_t u = (int64_t)q * A.units / Q;
+    if (u % A.KT == 0) return;
+    const int64_t up = (int64_t)(q - 1) * A.units / Q;
+    if (q > 1 && up % A.KT != 0 && up / A.KT == u / A.KT) return;
+    const int64_t tg = u / A.KT;
+    const int tt = (int)(tg / A.mtiles), mt = (int)(tg % A.mtiles);
+    int lo = 0, hi = A.njobs - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (A.job[mid].tile0 <= mt) lo = mid;
+      else hi = mid - 1;
+    }
+    const WideJob J = A.job[lo];
+    const int row0 = (mt - J.tile0) * 128;
+    const int rows = min(128, J.n - row0);
+    const int toks = min(A.N, A.T - tt * A.N);
+    const int per = (toks + WZ_PARTS - 1) / WZ_PARTS;
+    const int t0 = part * per, t1 = min(toks, t0 + per);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+    float *base = J.y + A.y_off + (int64_t)(tt * A.N) * J.ldy + row0;
+    const bool v4 = rows == 128 && (J.ldy & 3) == 0 && (((uintptr_t)base) & 15) == 0;
+    for (int t = t0 + warp; t < t1; t += nw) {
+      float *y = base + (int64_t)t * J.ldy;
+      if (v4) ((float4 *)y)[lane] = make_float4(0.f, 0.f, 0.f, 0.f);
+      else
+        for (int r = lane; r < rows; r += 32) y[r] = 0.f;
+    }
+    return;
+  }
+  const int tok = blockIdx.x;
+  const PackDst P{dst, A.N, PLANES, A.KT};
+  const int nc = A.K / 8;  // 8-column chunks of a row
+  if (tok >= A.T) {
+    const float z[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    for (int c = threadIdx.x; c < nc; c += WR_THREADS) pack_store8(P, tok, 8 * c, z);
+    return;
+  }
+  const float *xr = X + (int64_t)tok * ldx;
+  float ss = 0.f;
+  for (int i = threadIdx.x; i < A.K; i += WR_THREADS) ss = fmaf(xr[i], xr[i], ss);
+  __shared__ float red[WR_THREADS / 32];
+  ss = warp_sum(ss);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
+  __syncthreads();
+  float tot = 0.f;
+#pragma unroll
+  for (int i = 0; i < WR_THREADS / 32; ++i) tot += red[i];
+  const float sc = 1.0f / sqrtf(tot / (float)A.K + eps);
+  for (int c = threadIdx.x; c < nc; c += WR_THREADS) {
+    float v[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) v[e] = xr[8 * c + e] * sc * w[8 * c + e];
+    pack_store8(P, tok, 8 * c, v);
+  }
+}
+
 // Runs of at least this many units: a run ends with a read-back of its accumulator.
 constexpr int W_MIN_RUN = 4;
 // What a run's read-back and atomic add of its partial sums cost, in units.
 constexpr int W_RUN_COST = 6;
 
 template <int KIND, int DU>
-static cudaError_t launch_wide(WideArgs &A, const float *X, int ldx, void *act, int num_sms, cudaStream_t st) {
+static cudaError_t launch_wide(WideArgs &A, const float *X, int ldx, const float *norm_w, float eps, void *act,
+                               int num_sms, cudaStream_t st) {
   using C = WCfg<KIND, DU>;
   static PerDevice smem_set, resident;   // per device: the limit raised; the resident CTAs (0 = not yet)
   auto kern = k_wide<KIND, DU>;
@@ -543,16 +616,23 @@ static cudaError_t launch_wide(WideArgs &A, const float *X, int ldx, void *act, 
   const bool whole = tiles <= max_ctas && A.KT <= split_cost;
   const int Q = whole ? (int)tiles : (int)q_split;
   const int64_t chunks = (int64_t)A.ntt * A.KT * A.N * 8;
-  const int pack_blocks = (int)((chunks + 255) / 256);
   const int zero_blocks = whole ? 0 : (Q - 1) * WZ_PARTS;
-  cudaError_t e = launch_pdl(k_wide_pack<C::PLANES>, dim3(pack_blocks + zero_blocks), dim3(256), 0, st, 1, X, ldx, A, Q,
-                             (uint4 *)act, pack_blocks);
+  cudaError_t e;
+  if (norm_w) {
+    const int pack_blocks = A.ntt * A.N;  // one block a token row
+    e = launch_pdl(k_wide_rms_pack<C::PLANES>, dim3(pack_blocks + zero_blocks), dim3(WR_THREADS), 0, st, 1, X, ldx,
+                   norm_w, eps, A, Q, (uint4 *)act, pack_blocks);
+  } else {
+    const int pack_blocks = (int)((chunks + 255) / 256);
+    e = launch_pdl(k_wide_pack<C::PLANES>, dim3(pack_blocks + zero_blocks), dim3(256), 0, st, 1, X, ldx, A, Q,
+                   (uint4 *)act, pack_blocks);
+  }
   if (e != cudaSuccess) return e;
   return launch_pdl(kern, dim3((unsigned)Q), dim3(W_THREADS), C::SMEM, st, 1, A);
 }
 
 cudaError_t wide_gemm(const WideJob *jobs, int njobs, int64_t y_off, bool int4, int group, const float *X, int ldx,
-                      int T, int K, void *act, int num_sms, cudaStream_t st) {
+                      int T, int K, void *act, int num_sms, cudaStream_t st, const float *norm_w, float eps) {
   if (njobs < 1 || njobs > WIDE_MAX_JOBS || T < 1 || K % 64) return cudaErrorInvalidValue;
   WideArgs A{};
   A.njobs = njobs;
@@ -568,9 +648,9 @@ cudaError_t wide_gemm(const WideJob *jobs, int njobs, int64_t y_off, bool int4, 
   A.KT = K / 64;
   A.T = T;
   wide_tiles(T, A.ntt, A.N);
-  if (!int4) return launch_wide<W_KIND_F16, 1>(A, X, ldx, act, num_sms, st);
-  return group >= 64 ? launch_wide<W_KIND_I4, 1>(A, X, ldx, act, num_sms, st)
-                     : launch_wide<W_KIND_I4, 2>(A, X, ldx, act, num_sms, st);
+  if (!int4) return launch_wide<W_KIND_F16, 1>(A, X, ldx, norm_w, eps, act, num_sms, st);
+  return group >= 64 ? launch_wide<W_KIND_I4, 1>(A, X, ldx, norm_w, eps, act, num_sms, st)
+                     : launch_wide<W_KIND_I4, 2>(A, X, ldx, norm_w, eps, act, num_sms, st);
 }
 
 // This file's device error word (a bounded wait that gave up).
