@@ -559,30 +559,48 @@ def run_gb300(args):
 
 
 def e2e(b, steps):
-    """Through the public API from pinned host memory: inputs in, tokens out, every step."""
+    """Through the public API from pinned host memory: inputs in, tokens out, every step. The
+    taps go up in settle-sized chunks on a copy stream into two device buffers, each chunk's
+    settle waiting for its own copy only, so that the copies overlap the settles."""
     torch = b.torch
     wl = b.wl
     taps_pin = [torch.from_numpy(t).pin_memory() for t in b.taps_host] if b.settle_in_step else []
     h_pin = torch.from_numpy(b.h_host).pin_memory()
     at_pin = torch.tensor(b.anchor_tok, dtype=torch.int32).pin_memory()
     out_pin = torch.empty(wl.batch, b.k, dtype=torch.int32).pin_memory()
-    taps_dev = [torch.empty_like(t, device=b.dev) for t in taps_pin]
+    tw = b.g.tap_width
+    bufs = [torch.empty(SETTLE_CHUNK, tw, dtype=torch.float32, device=b.dev) for _ in range(2)]
     h_dev = torch.empty_like(h_pin, device=b.dev)
     at_dev = torch.empty_like(at_pin, device=b.dev)
     h2d = sum(t.numel() * 4 for t in taps_pin) + h_pin.numel() * 4 + at_pin.numel() * 4
     d2h = out_pin.numel() * 4
+    comp = torch.cuda.current_stream()
+    copy = torch.cuda.Stream()
+    copied = [torch.cuda.Event() for _ in range(2)]
+    freed = [torch.cuda.Event() for _ in range(2)]
 
     def one():
-        for s in range(len(taps_pin)):
-            taps_dev[s].copy_(taps_pin[s], non_blocking=True)
+        i = 0
+        for s, tp in enumerate(taps_pin):
             b.d.reset(s, 0)
-            b.d.settle(s, 0, taps_dev[s], chunk=SETTLE_CHUNK)
+            for r in range(0, tp.shape[0], SETTLE_CHUNK):
+                m = min(SETTLE_CHUNK, tp.shape[0] - r)
+                k = i % 2
+                with torch.cuda.stream(copy):
+                    if i >= 2:
+                        copy.wait_event(freed[k])
+                    bufs[k][:m].copy_(tp[r:r + m], non_blocking=True)
+                    copied[k].record(copy)
+                comp.wait_event(copied[k])
+                b.d.settle(s, r, bufs[k][:m], chunk=SETTLE_CHUNK)
+                freed[k].record(comp)
+                i += 1
         h_dev.copy_(h_pin, non_blocking=True)
         at_dev.copy_(at_pin, non_blocking=True)
         b.d.block(b.anchors, h_dev, b.k, b.width, out=(b.logits, b.hp))
         b.d.select(b.logits, b.hp, at_dev, out=(b.chosen, b.plain))
         out_pin.copy_(b.chosen, non_blocking=True)
-        torch.cuda.current_stream().synchronize()
+        comp.synchronize()
 
     one()
     times = []

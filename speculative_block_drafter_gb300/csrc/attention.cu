@@ -165,6 +165,13 @@ __device__ __forceinline__ bool sm_and(bool p) {
   return r != 0;
 }
 
+// 2^x, the hardware's approximation (relative error about 2^-22; 2^-inf = 0).
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // f32 pair -> f16 hi/lo pairs without the conversion unit: hi keeps the top 11
 // significant bits (truncation, exact in f16 over its normal range), lo = x - hi
 // rounded to f16; hi + lo carries about 21 bits. Two packed conversions a pair.
@@ -264,8 +271,8 @@ __global__ void __launch_bounds__(ATT_TC_THREADS, 1)
         if (j < nch) {
           // S = Q K^T of chunk j into score buffer j & 1
           const int st = j % S, sb = j & 1;
-          if (!mbar_wait(kvfull + 8 * st, (j / S) & 1)) break;
-          if (j >= 2 && !mbar_wait(sfree + 8 * sb, ((j >> 1) - 1) & 1)) break;
+          if (!mbar_wait_spin(kvfull + 8 * st, (j / S) & 1)) break;
+          if (j >= 2 && !mbar_wait_spin(sfree + 8 * sb, ((j >> 1) - 1) & 1)) break;
           tc_fence_after();
           const bool is_own = own && j == nch - 1;
           const uint32_t idesc = f16_idesc(128, is_own ? 16 : CH);
@@ -283,7 +290,7 @@ __global__ void __launch_bounds__(ATT_TC_THREADS, 1)
         if (j >= 1) {
           // O += P V of chunk j - 1, once its P is written
           const int jj = j - 1, st = jj % S, pb = jj & 1;
-          if (!mbar_wait(pfull + 8 * pb, (jj >> 1) & 1)) break;
+          if (!mbar_wait_spin(pfull + 8 * pb, (jj >> 1) & 1)) break;
           tc_fence_after();
           const bool is_own = own && jj == nch - 1;
           const int ksteps = is_own ? 1 : CH / 16;
@@ -344,21 +351,34 @@ __global__ void __launch_bounds__(ATT_TC_THREADS, 1)
       const int cnt = is_own ? R : min(CH, n - kb);
       const int N = is_own ? 16 : CH;
       const int k0 = kh * 32;  // this thread's keys k0 .. k0 + 31 of the chunk
-      bool w_ok = __all_sync(0xffffffffu, mbar_wait(sfull + 8 * sb, (j >> 1) & 1));
+      bool w_ok = __all_sync(0xffffffffu, mbar_wait_spin(sfull + 8 * sb, (j >> 1) & 1));
       tc_fence_after();
+      // raw scores of the visible keys [kmin, kmax) of the chunk, -inf elsewhere
       float x[32];
       float mh = -INFINITY;
       if (!dead && w_ok) {
         uint32_t r0[32];
         tmem_ld32(tb + lrow + C::S0 + sb * 64 + k0, r0);
         tc_wait_ld();
+        const int kmax = live ? cnt : 0;
+        int kmin = 0;
+        if (!is_own && window > 0) {
+          const int64_t first_vis = Sq.anchor + rr + 1 - window - (Sq.lo + kb);  // as a key of this chunk
+          kmin = first_vis <= 0 ? 0 : (first_vis >= CH ? CH : (int)first_vis);
+        }
+        if (kmin <= k0 && kmax >= k0 + 32) {
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const int k = k0 + e;
-          bool vis = live && k < cnt;
-          if (vis && !is_own && window > 0) vis = Sq.lo + kb + k >= Sq.anchor + rr + 1 - window;
-          x[e] = vis ? __uint_as_float(r0[e]) * sl2 : -INFINITY;
-          mh = fmaxf(mh, x[e]);
+          for (int e = 0; e < 32; ++e) {
+            x[e] = __uint_as_float(r0[e]);
+            mh = fmaxf(mh, x[e]);
+          }
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            const int k = k0 + e;
+            x[e] = (k >= kmin && k < kmax) ? __uint_as_float(r0[e]) : -INFINITY;
+            mh = fmaxf(mh, x[e]);
+          }
         }
       }
       tc_fence_before();
@@ -377,14 +397,14 @@ __global__ void __launch_bounds__(ATT_TC_THREADS, 1)
       xch[sb][kh][row] = mh;
       ok = sm_and(ok && w_ok);
       if (!ok) break;
-      const float mx = fmaxf(xch[sb][0][row], xch[sb][1][row]);
+      const float mx = fmaxf(xch[sb][0][row], xch[sb][1][row]) * sl2;  // the base-2 domain
       // the reference moves (both halves of a row decide alike); O's half `kh` of
       // the columns is rescaled once the products of the chunks before are done
       const bool up = mx > mref + ATT_TAU;
       if (__any_sync(0xffffffffu, up)) {
         float alpha = 1.f;
         if (up) {
-          alpha = mref == -INFINITY ? 0.f : exp2f(mref - mx);
+          alpha = mref == -INFINITY ? 0.f : ex2(mref - mx);
           l *= alpha;
           mref = mx;
         }
@@ -409,11 +429,14 @@ __global__ void __launch_bounds__(ATT_TC_THREADS, 1)
       // P = 2^(x - m) of this thread's keys, as hi/lo planes (16 columns each)
       uint32_t ph[16], pw[16];
       if (!dead) {
+        // 2^(x sl2 - m): a masked key's -inf gives 0 (and no row has a visible
+        // key while m is still -inf)
+        const float negm = mref == -INFINITY ? 0.f : -mref;
         float sum = 0.f;
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
-          const float p0 = x[2 * e] == -INFINITY ? 0.f : exp2f(x[2 * e] - mref);
-          const float p1 = x[2 * e + 1] == -INFINITY ? 0.f : exp2f(x[2 * e + 1] - mref);
+          const float p0 = ex2(fmaf(x[2 * e], sl2, negm));
+          const float p1 = ex2(fmaf(x[2 * e + 1], sl2, negm));
           sum += p0 + p1;
           split_hl(p0, p1, ph[e], pw[e]);
         }
@@ -437,7 +460,10 @@ __global__ void __launch_bounds__(ATT_TC_THREADS, 1)
     const bool all_ok = sm_and(ok);
     l = lsum[0][row] + lsum[1][row];
     float *out = part + ((int64_t)(b * kv + g) * nsplit + sp) * Q * part_row(HD) + (int64_t)row * part_row(HD);
-    const bool have = all_ok && nch > 0 && !dead && __all_sync(0xffffffffu, mbar_wait(obar, (nch - 1) & 1));
+    // O is final once every MMA has completed (`fin`, committed after the last
+    // P V): obar may still be two phases behind here, where a wait on the
+    // parity of its last phase would pass at once
+    const bool have = all_ok && nch > 0 && !dead && __all_sync(0xffffffffu, mbar_wait(fin, 0));
     if (have) {
       tc_fence_after();
 #pragma unroll

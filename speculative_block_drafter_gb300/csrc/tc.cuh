@@ -56,11 +56,26 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
   return false;
 }
 
+// The same without the suspend hint, for the waits on a pipeline's critical
+// path (a suspended thread may resume later than the phase completes); false
+// after 2^22 polls.
+__device__ __forceinline__ bool mbar_wait_spin(uint32_t bar, uint32_t parity) {
+  for (int i = 0; i < (1 << 22); ++i)
+    if (mbar_try(bar, parity)) return true;
+  atomicOr(&g_dev_error, DFL_ERR_TIMEOUT);
+  return false;
+}
+
 // ---------------------------------------------------------------- bulk copy (no tensor map)
 __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar) {
   asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
                "l"(src), "r"(bytes), "r"(bar)
                : "memory");
+}
+
+// Ask for `bytes` (a multiple of 16) at src in L2, ahead of their bulk copy.
+__device__ __forceinline__ void bulk_prefetch_l2(const void *src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
 
 // ---------------------------------------------------------------- tensor memory

@@ -189,6 +189,7 @@ __device__ __forceinline__ int job_of(const TcJobs &J, int mt) {
 // carries both planes. The drain warps release a shared-memory stage (they read
 // its scales last).
 constexpr int I4_PRODUCER = 8;
+constexpr int I4_PREFETCH = 8;  // k-tiles ahead of the ring's copies asked for in L2
 constexpr int I4_MMA0 = 9;
 constexpr int I4_MAX_THREADS = 32 * (I4_MMA0 + 2);
 
@@ -317,6 +318,14 @@ __global__ void __launch_bounds__(I4_MAX_THREADS, 2) k_tc_int4(TcJobs J, I4Items
         for (int kt = kt0; kt < kt1; ++kt, ++i) {
           const int s = i % C::S;
           const uint32_t st = smem_u32(sm + s * C::STAGE);
+          // the run's codes and scales I4_PREFETCH k-tiles on asked for in L2, so
+          // that the ring's later copies (a stage frees once its tile is drained)
+          // do not wait on DRAM
+          if (kt + I4_PREFETCH < kt1)
+            for (int jj = 0; jj < mtv; ++jj) {
+              bulk_prefetch_l2(wc + ((int64_t)jj * KT + kt + I4_PREFETCH) * 4096, 4096);
+              bulk_prefetch_l2(ws + ((int64_t)jj * KT + kt + I4_PREFETCH) * DU * 256, DU * 256);
+            }
           if (i >= npre) {
             if (i >= C::S && !mbar_wait(empty0 + 8 * s, ((i / C::S) - 1) & 1)) {
               ok = false;
