@@ -214,6 +214,11 @@ cudaError_t silu_mul(const float *g, const float *u, float *m, int64_t n, cudaSt
 // described by a map of boxes of 64 halves x 1 plane x 1 head x `box_rows`
 // rows, 128-byte swizzled. Encoding is host-only work; false if the driver cannot.
 bool attn_kv_map(CUtensorMap *m, const void *base, int64_t rows, int kv, int hd, int planes, int box_rows);
+// A map over bytes of `rank` (<= 5) dimensions (dims[0] innermost, strides in
+// bytes for dims 1..), boxes of `box`, no swizzle, zero fill outside; false if
+// the driver cannot encode it (unaligned base or strides, a box over 256).
+bool byte_map(CUtensorMap *m, const void *base, int rank, const uint64_t *dims, const uint64_t *strides,
+              const uint32_t *box);
 struct AttnSeq {          // per sequence and layer
   CUtensorMap kmap, vmap; // the layer's K and V cache of the sequence (box_rows 64)
   int64_t row0;           // cache row of the first context row read

@@ -2,6 +2,7 @@
 // Every wait is bounded: a wait that gives up records DFL_ERR_TIMEOUT in the
 // library's device error word and returns false, and the caller unwinds.
 #pragma once
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -73,9 +74,13 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t
                : "memory");
 }
 
-// Ask for `bytes` (a multiple of 16) at src in L2, ahead of their bulk copy.
-__device__ __forceinline__ void bulk_prefetch_l2(const void *src, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+// A tensor copy of the box at coordinates (x, p, h, z) of map m (x innermost).
+__device__ __forceinline__ void tma_load4(uint32_t dst, const CUtensorMap *m, int x, int p, int h, int z, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5}], "
+      "[%6];" ::"r"(dst),
+      "l"((uint64_t)m), "r"(x), "r"(p), "r"(h), "r"(z), "r"(bar)
+      : "memory");
 }
 
 // ---------------------------------------------------------------- tensor memory

@@ -22,6 +22,9 @@
 // arm's `to_half`); one accumulator spans the CTA's k-range.
 #include <algorithm>
 #include <climits>
+#include <map>
+#include <mutex>
+#include <tuple>
 
 #include "common.cuh"
 #include "kernels.h"
@@ -175,37 +178,54 @@ __device__ __forceinline__ int job_of(const TcJobs &J, int mt) {
 }
 
 // ---------------------------------------------------------------- four-bit kernel
+// The shape used: two CTAs an SM (256 tensor-memory columns each), stages of
+// two k-tiles, four dequantising warps, two issuing warps a row tile, both
+// activation planes into one accumulator. Measured on the head (151,936 x
+// 5,120, 15 rows): one CTA an SM with 512 columns, eight dequantising warps or
+// four-k-tile stages were each slower; see the kernel comment for why the
+// issuing warps matter.
+constexpr int I4_CPS = 2, I4_KS = 2, I4_NDQ = 4, I4_P = 2, I4_FOLD = 1;
 //
 // Persistent CTAs walk a list of items (MT row tiles of one matrix, a token
 // tile, a k-range); the k-tiles of consecutive items flow through one pipeline:
-//   warp 8        bulk-copies each k-tile (tokens hi/lo, the MT tiles' codes and scales)
-//   warps 0-3     dequantise their row of each tile into a tensor-memory A slot
-//   warps 9..     one per row tile: the MMAs of each quantisation unit, N = 2 TT
-//                 (the hi and lo planes are one 2TT-row B operand)
-//   warps 4-7     read each accumulator back (hi + lo halves), scale it and add
-//                 it up; at the end of an item they write the item's rows
-// A small-N MMA is cheap to run but not to issue (about 50 cycles from one
-// thread), so each row tile has its own issuing warp and each instruction
-// carries both planes. The drain warps release a shared-memory stage (they read
-// its scales last).
-constexpr int I4_PRODUCER = 8;
-constexpr int I4_PREFETCH = 8;  // k-tiles ahead of the ring's copies asked for in L2
-constexpr int I4_MMA0 = 9;
-constexpr int I4_MAX_THREADS = 32 * (I4_MMA0 + 2);
-
-template <int TT, int DU, int MT, int SA_>
+//   producer      copies a stage of KS k-tiles: one tensor copy of the MT row
+//                 tiles' codes, one of their scales (boxes of MT tiles x KS
+//                 k-tiles; past a matrix's last tile or k-tile they read zeros),
+//                 one bulk copy of the tokens' hi/lo planes
+//   NDQ warps     dequantise each k-tile's codes into a tensor-memory A slot
+//                 (8 warps: two a lane quarter, one half of the columns each)
+//   MT x P warps  issue the MMAs: P warps a row tile, taking its k-tiles in
+//                 turn; with FOLD the hi and the lo plane go into the same
+//                 accumulator (two MMAs of N = TT), else one MMA of N = 2 TT
+//   4 warps       read each accumulator back, scale it and add it up; at the
+//                 end of an item they write the item's rows, and they free a
+//                 stage once its last k-tile is drained
+// Measured on this GPU: an MMA of M = 128, K = 16 holds its issuing thread for
+// about 150 cycles whatever its N, while MMAs issued from different warps
+// overlap; so the issue is spread over several warps. A CTA's bulk copies are
+// served nearly one after another at a cost that hardly depends on their size
+// up to 16 KiB, so a stage is a few large copies; A slots and accumulators still
+// turn over per k-tile.
+template <int TT, int DU, int MT, int KS, int CPS, int NDQ, int P, int FOLD>
 struct I4 {
-  static constexpr int THREADS = 32 * (I4_MMA0 + MT);
-  static constexpr int B_BYTES = 2 * TT * 128;                 // hi + lo planes of a k-tile
-  static constexpr int CODE_OFF = B_BYTES;                     // MT x 4 KiB
-  static constexpr int SCALE_OFF = B_BYTES + MT * 4096;        // MT x DU x 256 B
-  static constexpr int STAGE = ((SCALE_OFF + MT * DU * 256) + 1023) / 1024 * 1024;
-  static constexpr int S = (96 * 1024 / STAGE) < 12 ? (96 * 1024 / STAGE) : 12;  // shared-memory stages
-  static constexpr int SA = SA_;                               // tensor-memory A slots
+  static constexpr int DRAIN0 = NDQ;                           // 4 drain warps
+  static constexpr int PRODUCER = NDQ + 4;
+  static constexpr int MMA0 = NDQ + 5;                         // MT x P issuing warps
+  static constexpr int THREADS = 32 * (MMA0 + MT * P);
+  static constexpr uint32_t TMEM_COLS = CPS == 1 ? 512 : 256;  // CPS CTAs an SM share its 512 columns
+  static constexpr int B1 = 2 * TT * 128;                      // hi + lo planes of one k-tile
+  static constexpr int CODE_OFF = KS * B1;                     // MT x KS x 4 KiB
+  static constexpr int SCALE_OFF = CODE_OFF + MT * KS * 4096;  // MT x KS x DU x 256 B
+  static constexpr int STAGE = ((SCALE_OFF + MT * KS * DU * 256) + 1023) / 1024 * 1024;
+  static constexpr int S_FIT = (CPS == 1 ? 196 : 108) * 1024 / STAGE;
+  static constexpr int S = S_FIT < 16 ? S_FIT : 16;            // shared-memory stages
+  static_assert(S >= 2, "shared memory");
   static constexpr int AW = MT * 32;                           // A columns of a slot
-  static constexpr int DW = MT * 2 * TT;                       // accumulator columns of a unit
+  static constexpr int SA = CPS == 1 ? 4 : 2;                  // tensor-memory A slots
+  static constexpr int DW = MT * TT * (FOLD ? 1 : 2);          // accumulator columns of a unit
   static constexpr int DCOL = SA * AW;
-  static constexpr int NDU = ((int)TC_TMEM_COLS - DCOL) / DW;  // accumulators in flight
+  static constexpr int NDU_FIT = ((int)TMEM_COLS - DCOL) / DW;
+  static constexpr int NDU = NDU_FIT < 8 ? NDU_FIT : 8;        // accumulators in flight
   static_assert(NDU >= 2, "tensor memory");
   static constexpr int NBAR = 2 * S + 2 * SA + 2 * NDU;
   static constexpr int SMEM = S * STAGE + 1024 + 512;
@@ -215,6 +235,18 @@ struct I4 {
 // to end; CTA b takes units [b U / grid, (b + 1) U / grid) ("stream-K"), as runs
 // that each stay inside one group's k-range. A run over the whole k-range
 // stores its rows; a shorter one adds them into outputs cleared beforehand.
+// Per job: the codes as bytes (256, 16, k-tile, row tile), boxes (256, 16, KS,
+// MT), and the scales as bytes (256, DU, k-tile, row tile), boxes (256, DU, KS,
+// MT), so that one copy brings a stage's codes (or scales) of all MT tiles.
+// A box spans min(KS, k-tiles) k-tiles and min(MT, row tiles) tiles of its
+// matrix; wbox is the bytes of the two boxes, ksb the k-tiles of a box (the
+// stride of a tile's codes in the stage).
+struct I4Maps {
+  CUtensorMap code[MAX_JOBS], scale[MAX_JOBS];
+  int wbox[MAX_JOBS];
+  int ksb;
+};
+
 struct I4Items {
   int groups;       // row-tile groups over all jobs
   int gtile0[MAX_JOBS + 1];
@@ -240,10 +272,10 @@ __device__ __forceinline__ void i4_run(const TcJobs &J, const I4Items &P, int MT
   mtv = min(MT, tiles - m0);
 }
 
-template <int TT, int DU, int MT, int SA>
-__global__ void __launch_bounds__(I4_MAX_THREADS, 2) k_tc_int4(TcJobs J, I4Items P, const uint8_t *__restrict__ bpack,
-                                                               int K, int T) {
-  using C = I4<TT, DU, MT, SA>;
+template <int TT, int DU, int MT, int KS, int CPS, int NDQ, int NP, int FOLD>
+__global__ void __launch_bounds__(32 * (NDQ + 5 + MT * NP), CPS)
+    k_tc_int4(const __grid_constant__ I4Maps M, TcJobs J, I4Items P, const uint8_t *__restrict__ bpack, int K, int T) {
+  using C = I4<TT, DU, MT, KS, CPS, NDQ, NP, FOLD>;
   extern __shared__ __align__(1024) uint8_t smraw[];
   uint8_t *sm = smraw + ((1024 - (smem_u32(smraw) & 1023)) & 1023);
   uint64_t *bars = (uint64_t *)(sm + C::S * C::STAGE);
@@ -265,15 +297,15 @@ __global__ void __launch_bounds__(I4_MAX_THREADS, 2) k_tc_int4(TcJobs J, I4Items
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::S; ++i) {
       mbar_init(full0 + 8 * i, 1);
-      mbar_init(empty0 + 8 * i, 128);
+      mbar_init(empty0 + 8 * i, 4);  // one arrive per drain warp
     }
     for (int i = 0; i < C::SA; ++i) {
-      mbar_init(afull0 + 8 * i, 128);
+      mbar_init(afull0 + 8 * i, NDQ);  // one arrive per dequantising warp
       mbar_init(afree0 + 8 * i, MT);
     }
     for (int i = 0; i < C::NDU; ++i) {
       mbar_init(dfull0 + 8 * i, MT);
-      mbar_init(dfree0 + 8 * i, 128);
+      mbar_init(dfree0 + 8 * i, 4);
     }
     mbar_fence_init();
   }
@@ -281,185 +313,131 @@ __global__ void __launch_bounds__(I4_MAX_THREADS, 2) k_tc_int4(TcJobs J, I4Items
   // The weights do not depend on the kernels before this one: the first stages'
   // codes and scales are fetched before waiting for them.
   int npre = 0;
-  if (warp == I4_PRODUCER && lane == 0) {
+  if (warp == C::PRODUCER && lane == 0) {
     int job, m0, mtv, tt, kt0, kt1;
     for (int pu = ru0; pu < ru1 && npre < C::S; pu += kt1 - kt0) {
       i4_run(J, P, MT, KT, pu, ru1, job, m0, mtv, tt, kt0, kt1);
-      const uint8_t *wc = (const uint8_t *)J.w[job] + (int64_t)m0 * KT * 4096;
-      const uint8_t *ws = (const uint8_t *)J.s[job] + (int64_t)m0 * KT * DU * 256;
-      for (int kt = kt0; kt < kt1 && npre < C::S; ++kt, ++npre) {
-        const uint32_t st = smem_u32(sm + npre * C::STAGE);
-        mbar_expect_tx(full0 + 8 * npre, C::B_BYTES + mtv * (4096 + DU * 256));
-        for (int jj = 0; jj < mtv; ++jj) {
-          bulk_g2s(st + C::CODE_OFF + jj * 4096, wc + ((int64_t)jj * KT + kt) * 4096, 4096, full0 + 8 * npre);
-          bulk_g2s(st + C::SCALE_OFF + jj * DU * 256, ws + ((int64_t)jj * KT + kt) * DU * 256, DU * 256,
-                   full0 + 8 * npre);
-        }
+      for (int kt = kt0; kt < kt1 && npre < C::S; kt += KS, ++npre) {
+        const int n = min(KS, kt1 - kt);
+        const uint32_t st = smem_u32(sm + npre * C::STAGE), fb = full0 + 8 * npre;
+        mbar_expect_tx(fb, n * C::B1 + M.wbox[job]);
+        tma_load4(st + C::CODE_OFF, &M.code[job], 0, 0, kt, m0, fb);
+        tma_load4(st + C::SCALE_OFF, &M.scale[job], 0, 0, kt, m0, fb);
       }
     }
   }
   pdl_wait();
-  if (warp == 0) tmem_alloc(smem_u32(tslot), TC_TMEM_COLS);
+  if (warp == 0) tmem_alloc(smem_u32(tslot), C::TMEM_COLS);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = *tslot;
 
-  if (warp == I4_PRODUCER) {
+  if (warp == C::PRODUCER) {
     if (lane == 0) {
-      int i = 0;
+      int g = 0;
       bool ok = true;
       int job, m0, mtv, tt, kt0, kt1;
       for (int pu = ru0; pu < ru1 && ok; pu += kt1 - kt0) {
         i4_run(J, P, MT, KT, pu, ru1, job, m0, mtv, tt, kt0, kt1);
-        const uint8_t *wc = (const uint8_t *)J.w[job] + (int64_t)m0 * KT * 4096;
-        const uint8_t *ws = (const uint8_t *)J.s[job] + (int64_t)m0 * KT * DU * 256;
-        const uint8_t *bp = bpack + (int64_t)tt * KT * C::B_BYTES;
-        for (int kt = kt0; kt < kt1; ++kt, ++i) {
-          const int s = i % C::S;
-          const uint32_t st = smem_u32(sm + s * C::STAGE);
-          // the run's codes and scales I4_PREFETCH k-tiles on asked for in L2, so
-          // that the ring's later copies (a stage frees once its tile is drained)
-          // do not wait on DRAM
-          if (kt + I4_PREFETCH < kt1)
-            for (int jj = 0; jj < mtv; ++jj) {
-              bulk_prefetch_l2(wc + ((int64_t)jj * KT + kt + I4_PREFETCH) * 4096, 4096);
-              bulk_prefetch_l2(ws + ((int64_t)jj * KT + kt + I4_PREFETCH) * DU * 256, DU * 256);
-            }
-          if (i >= npre) {
-            if (i >= C::S && !mbar_wait(empty0 + 8 * s, ((i / C::S) - 1) & 1)) {
+        const uint8_t *bp = bpack + (int64_t)tt * KT * C::B1;
+        for (int kt = kt0; kt < kt1; kt += KS, ++g) {
+          const int n = min(KS, kt1 - kt), s = g % C::S;
+          const uint32_t st = smem_u32(sm + s * C::STAGE), fb = full0 + 8 * s;
+          if (g >= npre) {
+            if (g >= C::S && !mbar_wait(empty0 + 8 * s, ((g / C::S) - 1) & 1)) {
               ok = false;
               break;
             }
-            mbar_expect_tx(full0 + 8 * s, C::B_BYTES + mtv * (4096 + DU * 256));
-            for (int jj = 0; jj < mtv; ++jj) {
-              bulk_g2s(st + C::CODE_OFF + jj * 4096, wc + ((int64_t)jj * KT + kt) * 4096, 4096, full0 + 8 * s);
-              bulk_g2s(st + C::SCALE_OFF + jj * DU * 256, ws + ((int64_t)jj * KT + kt) * DU * 256, DU * 256,
-                       full0 + 8 * s);
-            }
+            mbar_expect_tx(fb, n * C::B1 + M.wbox[job]);
+            tma_load4(st + C::CODE_OFF, &M.code[job], 0, 0, kt, m0, fb);
+            tma_load4(st + C::SCALE_OFF, &M.scale[job], 0, 0, kt, m0, fb);
           }
-          bulk_g2s(st, bp + (int64_t)kt * C::B_BYTES, C::B_BYTES, full0 + 8 * s);
+          bulk_g2s(st, bp + (int64_t)kt * C::B1, n * C::B1, fb);
         }
       }
     }
-  } else if (warp >= I4_MMA0 && warp < I4_MMA0 + MT) {
+  } else if (warp >= C::MMA0) {
     if (lane == 0) {
-      const int jj = warp - I4_MMA0;  // this warp's row tile of the item
-      constexpr uint32_t idesc = f16_idesc(128, 2 * TT);
+      // this warp's row tile of the item, and its share of the k-tiles (those
+      // with i % NP == pw): an MMA holds its issuing thread for about 150
+      // cycles whatever its N, so several warps issue side by side
+      const int jj = (warp - C::MMA0) % MT, pw = (warp - C::MMA0) / MT;
+      constexpr uint32_t idesc = f16_idesc(128, FOLD ? TT : 2 * TT);
       constexpr int KSU = 4 / DU;
-      int i = 0, u = 0;
+      int g = 0, i = 0, u = 0;
       bool ok = true;
       int job, m0, mtv, tt, kt0, kt1;
       for (int pu = ru0; pu < ru1 && ok; pu += kt1 - kt0) {
         i4_run(J, P, MT, KT, pu, ru1, job, m0, mtv, tt, kt0, kt1);
         const bool live = jj < mtv;
-        for (int kt = kt0; kt < kt1 && ok; ++kt, ++i) {
-          const int s = i % C::S, a = i % C::SA;
-          if (!mbar_wait(full0 + 8 * s, (i / C::S) & 1) || !mbar_wait(afull0 + 8 * a, (i / C::SA) & 1)) {
+        for (int kt = kt0; kt < kt1 && ok; kt += KS, ++g) {
+          const int n = min(KS, kt1 - kt), s = g % C::S;
+          if (!mbar_wait(full0 + 8 * s, (g / C::S) & 1)) {
             ok = false;
             break;
           }
-          tc_fence_after();
           const uint32_t st = smem_u32(sm + s * C::STAGE);
-          for (int du = 0; du < DU; ++du, ++u) {
-            const int d = u % C::NDU;
-            if (u >= C::NDU && !mbar_wait(dfree0 + 8 * d, ((u / C::NDU) - 1) & 1)) {
+          for (int sub = 0; sub < n && ok; ++sub, ++i) {
+            if (NP > 1 && i % NP != pw) {
+              u += DU;
+              continue;
+            }
+            const int a = i % C::SA;
+            if (!mbar_wait(afull0 + 8 * a, (i / C::SA) & 1)) {
               ok = false;
               break;
             }
             tc_fence_after();
-            if (live) {
-              const uint32_t dcol = tbase + C::DCOL + d * C::DW + jj * 2 * TT;
-#pragma unroll
-              for (int ks = 0; ks < KSU; ++ks) {
-                const int kstep = du * KSU + ks;
-                mma_ts(dcol, tbase + a * C::AW + jj * 32 + kstep * 8, sw128_desc(st + kstep * 32), idesc, ks > 0);
+            const uint32_t bsub = st + sub * C::B1;
+            for (int du = 0; du < DU; ++du, ++u) {
+              const int d = u % C::NDU;
+              if (u >= C::NDU && !mbar_wait(dfree0 + 8 * d, ((u / C::NDU) - 1) & 1)) {
+                ok = false;
+                break;
               }
+              tc_fence_after();
+              if (live) {
+                // both activation planes into one accumulator: the hi rows of the
+                // B tile, then its lo rows (TT rows = TT * 128 bytes further on)
+                const uint32_t dcol = tbase + C::DCOL + d * C::DW + jj * (C::DW / MT);
+#pragma unroll
+                for (int ks = 0; ks < KSU; ++ks) {
+                  const int kstep = du * KSU + ks;
+                  const uint32_t acol = tbase + a * C::AW + jj * 32 + kstep * 8;
+                  mma_ts(dcol, acol, sw128_desc(bsub + kstep * 32), idesc, ks > 0);
+                  if (FOLD) mma_ts(dcol, acol, sw128_desc(bsub + TT * 128 + kstep * 32), idesc, 1);
+                }
+              }
+              mma_commit(dfull0 + 8 * d);
             }
-            mma_commit(dfull0 + 8 * d);
+            mma_commit(afree0 + 8 * a);
           }
-          mma_commit(afree0 + 8 * a);
         }
       }
     }
-  } else if (warp < 4) {
-    // dequantise: thread r owns row r of each of the item's tiles
-    const int r = warp * 32 + lane;
-    const uint32_t lrow = (uint32_t)(warp * 32) << 16;
-    int i = 0;
+  } else if (warp < NDQ) {
+    // dequantise: thread r of lane quarter warp % 4 owns row r of each of the
+    // item's tiles; with 8 warps, warp / 4 picks the half of the 64 columns
+    const int r = (warp & 3) * 32 + lane;
+    const uint32_t lrow = (uint32_t)((warp & 3) * 32) << 16;
+    constexpr int HALVES = NDQ == 8 ? 1 : 2;  // column halves a thread dequantises
+    const int h0 = NDQ == 8 ? warp >> 2 : 0;
+    int g = 0, i = 0;
     bool ok = true;
     int job, m0, mtv, tt, kt0, kt1;
     for (int pu = ru0; pu < ru1 && ok; pu += kt1 - kt0) {
       i4_run(J, P, MT, KT, pu, ru1, job, m0, mtv, tt, kt0, kt1);
-      for (int kt = kt0; kt < kt1; ++kt, ++i) {
-        const int s = i % C::S, a = i % C::SA;
-        if (!__all_sync(0xffffffffu, mbar_wait(full0 + 8 * s, (i / C::S) & 1))) {
+      for (int kt = kt0; kt < kt1 && ok; kt += KS, ++g) {
+        const int n = min(KS, kt1 - kt), s = g % C::S;
+        if (!__all_sync(0xffffffffu, mbar_wait(full0 + 8 * s, (g / C::S) & 1))) {
           ok = false;
           break;
         }
         const uint8_t *st = sm + s * C::STAGE;
-        if (i >= C::SA && !__all_sync(0xffffffffu, mbar_wait(afree0 + 8 * a, ((i / C::SA) - 1) & 1))) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-#pragma unroll
-        for (int jj = 0; jj < MT; ++jj) {
-          if (jj < mtv) {
-            const uint4 c0 = *(const uint4 *)(st + C::CODE_OFF + jj * 4096 + r * 16);
-            const uint4 c1 = *(const uint4 *)(st + C::CODE_OFF + jj * 4096 + 2048 + r * 16);
-            const uint32_t words[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-            uint32_t v[32];
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              uint32_t a4[4];
-              dequant8(words[j], a4);
-              v[4 * j + 0] = a4[0];
-              v[4 * j + 1] = a4[1];
-              v[4 * j + 2] = a4[2];
-              v[4 * j + 3] = a4[3];
-            }
-            tmem_st32(tbase + lrow + a * C::AW + jj * 32, v);
-          }
-        }
-        tc_wait_st();
-        tc_fence_before();
-        mbar_arrive(afull0 + 8 * a);
-      }
-    }
-  } else if (warp < 8) {
-    // drain: warps 4-7 read the accumulators of their lanes (rows 32(warp-4) ..)
-    const int r = (warp - 4) * 32 + lane;
-    const uint32_t lrow = (uint32_t)((warp - 4) * 32) << 16;
-    float acc[MT][TT];
-#pragma unroll
-    for (int jj = 0; jj < MT; ++jj)
-#pragma unroll
-      for (int t = 0; t < TT; ++t) acc[jj][t] = 0.f;
-    int i = 0, u = 0;
-    bool ok = true;
-    int job, m0, mtv, tt, kt0, kt1;
-    for (int pu = ru0; pu < ru1 && ok; pu += kt1 - kt0) {
-      i4_run(J, P, MT, KT, pu, ru1, job, m0, mtv, tt, kt0, kt1);
-      for (int kt = kt0; kt < kt1 && ok; ++kt, ++i) {
-        const int s = i % C::S;
-        if (!__all_sync(0xffffffffu, mbar_wait(full0 + 8 * s, (i / C::S) & 1))) {
-          ok = false;
-          break;
-        }
-        const uint8_t *st = sm + s * C::STAGE;
-        float sc[MT][DU];
-#pragma unroll
-        for (int jj = 0; jj < MT; ++jj)
-#pragma unroll
-          for (int du = 0; du < DU; ++du)
-            sc[jj][du] = jj < mtv ? __half2float(__ushort_as_half(
-                                        *(const uint16_t *)(st + C::SCALE_OFF + (jj * DU + du) * 256 + r * 2)))
-                                  : 0.f;
-#pragma unroll
-        for (int du = 0; du < DU; ++du, ++u) {
-          const int d = u % C::NDU;
-          if (!__all_sync(0xffffffffu, mbar_wait(dfull0 + 8 * d, (u / C::NDU) & 1))) {
+        for (int sub = 0; sub < n; ++sub, ++i) {
+          const int a = i % C::SA;
+          if (i >= C::SA && !__all_sync(0xffffffffu, mbar_wait(afree0 + 8 * a, ((i / C::SA) - 1) & 1))) {
             ok = false;
             break;
           }
@@ -467,24 +445,104 @@ __global__ void __launch_bounds__(I4_MAX_THREADS, 2) k_tc_int4(TcJobs J, I4Items
 #pragma unroll
           for (int jj = 0; jj < MT; ++jj) {
             if (jj < mtv) {
+              const uint8_t *cp = st + C::CODE_OFF + (jj * M.ksb + sub) * 4096 + r * 16;
 #pragma unroll
-              for (int c0 = 0; c0 < TT; c0 += 16) {
-                uint32_t wh[16], wl[16];
-                const uint32_t col = tbase + lrow + C::DCOL + d * C::DW + jj * 2 * TT + c0;
-                tmem_ld16(col, wh);
-                tmem_ld16(col + TT, wl);
-                tc_wait_ld();
+              for (int hh = 0; hh < HALVES; ++hh) {
+                const int h = h0 + hh;
+                const uint4 c = *(const uint4 *)(cp + h * 2048);
+                const uint32_t words[4] = {c.x, c.y, c.z, c.w};
+                uint32_t v[16];
 #pragma unroll
-                for (int e = 0; e < 16; ++e)
-                  acc[jj][c0 + e] =
-                      fmaf(sc[jj][du], __uint_as_float(wh[e]) + __uint_as_float(wl[e]), acc[jj][c0 + e]);
+                for (int j = 0; j < 4; ++j) {
+                  uint32_t a4[4];
+                  dequant8(words[j], a4);
+                  v[4 * j + 0] = a4[0];
+                  v[4 * j + 1] = a4[1];
+                  v[4 * j + 2] = a4[2];
+                  v[4 * j + 3] = a4[3];
+                }
+                tmem_st16(tbase + lrow + a * C::AW + jj * 32 + h * 16, v);
               }
             }
           }
+          tc_wait_st();
           tc_fence_before();
-          mbar_arrive(dfree0 + 8 * d);
+          __syncwarp();
+          if (lane == 0) mbar_arrive(afull0 + 8 * a);
         }
-        mbar_arrive(empty0 + 8 * s);
+      }
+    }
+  } else if (warp < C::DRAIN0 + 4) {
+    // drain: 4 warps read the accumulators of their lane quarter
+    const int r = (warp & 3) * 32 + lane;
+    const uint32_t lrow = (uint32_t)((warp & 3) * 32) << 16;
+    float acc[MT][TT];
+#pragma unroll
+    for (int jj = 0; jj < MT; ++jj)
+#pragma unroll
+      for (int t = 0; t < TT; ++t) acc[jj][t] = 0.f;
+    int g = 0, i = 0, u = 0;
+    bool ok = true;
+    int job, m0, mtv, tt, kt0, kt1;
+    for (int pu = ru0; pu < ru1 && ok; pu += kt1 - kt0) {
+      i4_run(J, P, MT, KT, pu, ru1, job, m0, mtv, tt, kt0, kt1);
+      for (int kt = kt0; kt < kt1 && ok; kt += KS, ++g) {
+        const int n = min(KS, kt1 - kt), s = g % C::S;
+        if (!__all_sync(0xffffffffu, mbar_wait(full0 + 8 * s, (g / C::S) & 1))) {
+          ok = false;
+          break;
+        }
+        const uint8_t *st = sm + s * C::STAGE;
+        for (int sub = 0; sub < n && ok; ++sub, ++i) {
+          float sc[MT][DU];
+#pragma unroll
+          for (int jj = 0; jj < MT; ++jj)
+#pragma unroll
+            for (int du = 0; du < DU; ++du)
+              sc[jj][du] = jj < mtv ? __half2float(__ushort_as_half(*(const uint16_t *)(
+                                          st + C::SCALE_OFF + ((jj * M.ksb + sub) * DU + du) * 256 + r * 2)))
+                                    : 0.f;
+#pragma unroll
+          for (int du = 0; du < DU; ++du, ++u) {
+            const int d = u % C::NDU;
+            if (!__all_sync(0xffffffffu, mbar_wait(dfull0 + 8 * d, (u / C::NDU) & 1))) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+#pragma unroll
+            for (int jj = 0; jj < MT; ++jj) {
+              if (jj < mtv) {
+#pragma unroll
+                for (int c0 = 0; c0 < TT; c0 += 16) {
+                  const uint32_t col = tbase + lrow + C::DCOL + d * C::DW + jj * (C::DW / MT) + c0;
+                  uint32_t w[16];
+                  tmem_ld16(col, w);
+                  if (FOLD) {
+                    tc_wait_ld();
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) acc[jj][c0 + e] = fmaf(sc[jj][du], __uint_as_float(w[e]), acc[jj][c0 + e]);
+                  } else {
+                    uint32_t wl[16];
+                    tmem_ld16(col + TT, wl);
+                    tc_wait_ld();
+#pragma unroll
+                    for (int e = 0; e < 16; ++e)
+                      acc[jj][c0 + e] =
+                          fmaf(sc[jj][du], __uint_as_float(w[e]) + __uint_as_float(wl[e]), acc[jj][c0 + e]);
+                  }
+                }
+              }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(dfree0 + 8 * d);
+          }
+        }
+        // the stage's codes, scales and tokens are no longer read (its MMAs
+        // completed before their accumulators were drained)
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty0 + 8 * s);
       }
       if (!ok) break;
       // the item's rows
@@ -513,7 +571,7 @@ __global__ void __launch_bounds__(I4_MAX_THREADS, 2) k_tc_int4(TcJobs J, I4Items
   __syncthreads();
   if (warp == 0) {
     tc_fence_after();
-    tmem_dealloc(tbase, TC_TMEM_COLS);
+    tmem_dealloc(tbase, C::TMEM_COLS);
   }
 }
 
@@ -781,7 +839,7 @@ static cudaError_t fill_jobs(const TcJob *jobs, int njobs, TcJobs &J, int &mtile
 }
 
 // ---- four-bit: the partition of a launch
-template <int MT>
+template <int MT, int CPS>
 static void plan_int4(const TcJobs &J, int njobs, int ntt, int K, int num_sms, I4Items &P, int &grid, bool &split) {
   P = I4Items{};
   P.groups = 0;
@@ -797,28 +855,63 @@ static void plan_int4(const TcJobs &J, int njobs, int ntt, int K, int num_sms, I
   // chains); whole groups a CTA when there are enough of them
   const int ngroups = ntt * P.groups;
   split = false;
-  if (ngroups >= 2 * num_sms) {
+  if (ngroups >= CPS * num_sms) {
     P.whole = 1;
-    grid = 2 * num_sms;
+    grid = CPS * num_sms;
   } else {
     P.whole = 0;
-    grid = (int)std::max<int64_t>(1, std::min<int64_t>(2 * num_sms, P.units / 2));
+    grid = (int)std::max<int64_t>(1, std::min<int64_t>(CPS * num_sms, P.units / 2));
     for (int b = 1; b < grid && !split; ++b) split = ((int64_t)b * P.units / grid) % KT != 0;
   }
 }
 
-template <int TT, int DU, int MT, int SA>
+// The jobs' tensor maps, encoded once per (matrix, box shape) and kept: the
+// weights of a drafter stay where they are between calls.
+static bool i4_maps(const TcJobs &J, int njobs, int KT, int KS, int MT, int DU, I4Maps &M) {
+  using Key = std::tuple<const void *, const void *, int, int, int, int, int>;
+  static std::mutex mu;
+  static std::map<Key, std::pair<CUtensorMap, CUtensorMap>> cache;
+  std::lock_guard<std::mutex> lock(mu);
+  M.ksb = std::min(KS, KT);
+  for (int j = 0; j < njobs; ++j) {
+    const int mt = J.tile0[j + 1] - J.tile0[j];
+    const int mtb = std::min(MT, mt);
+    M.wbox[j] = mtb * M.ksb * (4096 + DU * 256);
+    const Key key{J.w[j], J.s[j], mt, KT, M.ksb, mtb, DU};
+    auto it = cache.find(key);
+    if (it == cache.end()) {
+      if (cache.size() > 4096) cache.clear();
+      std::pair<CUtensorMap, CUtensorMap> maps;
+      const uint64_t cd[4] = {256, 16, (uint64_t)KT, (uint64_t)mt};
+      const uint64_t cs[3] = {256, 4096, (uint64_t)KT * 4096};
+      const uint32_t cb[4] = {256, 16, (uint32_t)M.ksb, (uint32_t)mtb};
+      const uint64_t sd[4] = {256, (uint64_t)DU, (uint64_t)KT, (uint64_t)mt};
+      const uint64_t ss[3] = {256, (uint64_t)DU * 256, (uint64_t)KT * DU * 256};
+      const uint32_t sb[4] = {256, (uint32_t)DU, (uint32_t)M.ksb, (uint32_t)mtb};
+      if (!byte_map(&maps.first, J.w[j], 4, cd, cs, cb) || !byte_map(&maps.second, J.s[j], 4, sd, ss, sb))
+        return false;
+      it = cache.emplace(key, maps).first;
+    }
+    M.code[j] = it->second.first;
+    M.scale[j] = it->second.second;
+  }
+  return true;
+}
+
+template <int TT, int DU, int MT>
 static cudaError_t launch_int4(const TcJobs &J, int njobs, const void *act, int K, int T, int ntt, int num_sms,
                                cudaStream_t st) {
-  using C = I4<TT, DU, MT, SA>;
+  using C = I4<TT, DU, MT, I4_KS, I4_CPS, I4_NDQ, I4_P, I4_FOLD>;
   static PerDevice configured;
-  cudaError_t e = smem_limit(k_tc_int4<TT, DU, MT, SA>, C::SMEM, configured);
+  cudaError_t e = smem_limit(k_tc_int4<TT, DU, MT, I4_KS, I4_CPS, I4_NDQ, I4_P, I4_FOLD>, C::SMEM, configured);
   if (e != cudaSuccess) return e;
+  I4Maps M{};
+  if (!i4_maps(J, njobs, K / 64, I4_KS, MT, DU, M)) return cudaErrorInvalidValue;
   I4Items P;
   int grid;
   bool split;
-  plan_int4<MT>(J, njobs, ntt, K, num_sms, P, grid, split);
-  return launch_pdl(k_tc_int4<TT, DU, MT, SA>, dim3(grid), dim3(C::THREADS), C::SMEM, st, 1, J, P,
+  plan_int4<MT, I4_CPS>(J, njobs, ntt, K, num_sms, P, grid, split);
+  return launch_pdl(k_tc_int4<TT, DU, MT, I4_KS, I4_CPS, I4_NDQ, I4_P, I4_FOLD>, dim3(grid), dim3(C::THREADS), C::SMEM, st, 1, M, J, P,
                     (const uint8_t *)act, K, T);
 }
 
@@ -828,10 +921,10 @@ static cudaError_t dispatch_int4(const TcJobs &J, int njobs, int group, const vo
   const int TT = tt_int4(T);
   const int ntt = (T + TT - 1) / TT;
   const int DU = drain_units(group);
-  if (TT == 16) return DU == 1 ? launch_int4<16, 1, 2, 2>(J, njobs, act, K, T, ntt, num_sms, st)
-                               : launch_int4<16, 2, 2, 2>(J, njobs, act, K, T, ntt, num_sms, st);
-  return DU == 1 ? launch_int4<32, 1, 1, 2>(J, njobs, act, K, T, ntt, num_sms, st)
-                 : launch_int4<32, 2, 1, 2>(J, njobs, act, K, T, ntt, num_sms, st);
+  if (TT == 16) return DU == 1 ? launch_int4<16, 1, 2>(J, njobs, act, K, T, ntt, num_sms, st)
+                               : launch_int4<16, 2, 2>(J, njobs, act, K, T, ntt, num_sms, st);
+  return DU == 1 ? launch_int4<32, 1, 1>(J, njobs, act, K, T, ntt, num_sms, st)
+                 : launch_int4<32, 2, 1>(J, njobs, act, K, T, ntt, num_sms, st);
 }
 
 int tc_tile_rows(int T, bool int4) { return int4 ? tt_int4(T) : tt_f16(T); }
@@ -844,8 +937,8 @@ bool tc_splits_int4(const TcJob *jobs, int njobs, int T, int K, int num_sms) {
   I4Items P;
   int grid;
   bool split;
-  if (TT == 16) plan_int4<2>(J, njobs, ntt, K, num_sms, P, grid, split);
-  else plan_int4<1>(J, njobs, ntt, K, num_sms, P, grid, split);
+  if (TT == 16) plan_int4<2, I4_CPS>(J, njobs, ntt, K, num_sms, P, grid, split);
+  else plan_int4<1, I4_CPS>(J, njobs, ntt, K, num_sms, P, grid, split);
   return split;
 }
 
