@@ -130,13 +130,14 @@ struct WCursor {
       locate(A);
     }
   }
+  // the weights are read once: evict them from L2 first
   template <int KIND, int DU>
-  __device__ __forceinline__ void load_a(const WideArgs &A, uint32_t dst, uint32_t bar) const {
+  __device__ __forceinline__ void load_a(const WideArgs &A, uint32_t dst, uint32_t bar, uint64_t pol) const {
     if (KIND == W_KIND_F16) {
-      bulk_g2s(dst, w + (tile0 + kt) * 16384, 16384, bar);
+      bulk_g2s_hint(dst, w + (tile0 + kt) * 16384, 16384, bar, pol);
     } else {
-      bulk_g2s(dst, w + (tile0 + kt) * 4096, 4096, bar);
-      bulk_g2s(dst + 4096, s + (tile0 + kt) * DU * 256, DU * 256, bar);
+      bulk_g2s_hint(dst, w + (tile0 + kt) * 4096, 4096, bar, pol);
+      bulk_g2s_hint(dst + 4096, s + (tile0 + kt) * DU * 256, DU * 256, bar, pol);
     }
   }
 };
@@ -222,10 +223,11 @@ __global__ void __launch_bounds__(W_THREADS, 1) k_wide(WideArgs A) {
   WCursor cur;
   int npre = 0;
   if (warp == W_PRODUCER && lane == 0) {
+    const uint64_t wpol = l2_evict_first();
     cur.start(A, u0);
     for (; npre < S && u0 + npre < u1; ++npre, cur.next(A)) {
       mbar_expect_tx(full0 + 8 * npre, b_bytes + C::A_BYTES);
-      cur.load_a<KIND, DU>(A, smem_u32(sm + npre * stage) + b_bytes, full0 + 8 * npre);
+      cur.load_a<KIND, DU>(A, smem_u32(sm + npre * stage) + b_bytes, full0 + 8 * npre, wpol);
     }
   }
   // Four-bit: the first run's row scaling, from the weights' scales (which do
@@ -243,6 +245,8 @@ __global__ void __launch_bounds__(W_THREADS, 1) k_wide(WideArgs A) {
     if (lane == 0) {
       WCursor bc;  // the units' token tiles
       bc.start(A, u0);
+      // the token tiles are read by every row tile: keep them in L2
+      const uint64_t wpol = l2_evict_first(), bpol = l2_evict_last();
       int i = 0;
       bool ok = true;
       for (int64_t u = u0; u < u1; ++u, ++i, bc.next(A)) {
@@ -254,11 +258,11 @@ __global__ void __launch_bounds__(W_THREADS, 1) k_wide(WideArgs A) {
             break;
           }
           mbar_expect_tx(full0 + 8 * s, b_bytes + C::A_BYTES);
-          cur.load_a<KIND, DU>(A, st + b_bytes, full0 + 8 * s);
+          cur.load_a<KIND, DU>(A, st + b_bytes, full0 + 8 * s, wpol);
           cur.next(A);
         }
         const uint8_t *bp = A.bpack + ((int64_t)bc.tt * A.KT + bc.kt) * b_bytes;
-        bulk_g2s(st, bp, b_bytes, full0 + 8 * s);
+        bulk_g2s_hint(st, bp, b_bytes, full0 + 8 * s, bpol);
       }
       // every stage released by every consumer (no copy still bound for this CTA)
       if (ok)
