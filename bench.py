@@ -285,11 +285,16 @@ class Bench:
     def select(self):
         self.d.select(self.logits, self.hp, self.at, out=(self.chosen, self.plain))
 
+    def draft(self):
+        """The block and the selector in one call (dflash_draft: the head GEMM also takes the
+        selector's first stage when it can)."""
+        self.d.draft(self.anchors, self.h, self.at, self.k, self.width,
+                     out=(self.logits, self.hp, self.chosen, self.plain))
+
     def step(self):
         if self.settle_in_step:
             self.settle_all(SETTLE_CHUNK)
-        self.block()
-        self.select()
+        self.draft()
 
     def flush(self):
         self.flush_buf.zero_()
@@ -498,9 +503,11 @@ def run_gb300(args):
     block_s = float(np.mean(b.timed(b.block, reps, gb))) * 1e-3
     gs, n_sel = b.capture(b.select)
     sel_s = float(np.mean(b.timed(b.select, reps, gs))) * 1e-3
+    gd, n_draft = b.capture(b.draft)
+    draft_s = float(np.mean(b.timed(b.draft, reps, gd))) * 1e-3
     phases.update(block_ms=round(block_s * 1e3, 4), block_launches=int(n_block),
                   blocks_per_s_block_only=round(wl.batch / block_s, 2), select_ms=round(sel_s * 1e3, 4),
-                  select_launches=int(n_sel))
+                  select_launches=int(n_sel), draft_ms=round(draft_s * 1e3, 4), draft_launches=int(n_draft))
 
     ctx = context_rows(g, wl.context, wl.context)
     bbytes, bflops, parts = block_cost(g, wl.head_width, ctx, wl.batch, 4 if args.cache == "planes" else 2)
@@ -538,8 +545,8 @@ def run_gb300(args):
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {"workload": wl.name, "description": wl.description, "context": wl.context, "batch": wl.batch,
                    "block": g.block, "head_width": wl.head_width, "kv_cache": args.cache,
-                   "step": ("reset + settle(%d rows in %d-row calls) + block + select" % (wl.context, SETTLE_CHUNK))
-                   if b.settle_in_step else "one block per sequence + select (contexts settled before)",
+                   "step": ("reset + settle(%d rows in %d-row calls) + draft (block + select)" % (wl.context, SETTLE_CHUNK))
+                   if b.settle_in_step else "draft: one block per sequence + select (contexts settled before)",
                    "l2": "flushed between steps (256 MiB write)", "graph": graph is not None,
                    "parallelism": "replicas" if world > 1 else "single"},
         "settle_rows_per_s": phases.get("settle_rows_per_s"),
@@ -597,8 +604,7 @@ def e2e(b, steps):
                 i += 1
         h_dev.copy_(h_pin, non_blocking=True)
         at_dev.copy_(at_pin, non_blocking=True)
-        b.d.block(b.anchors, h_dev, b.k, b.width, out=(b.logits, b.hp))
-        b.d.select(b.logits, b.hp, at_dev, out=(b.chosen, b.plain))
+        b.d.draft(b.anchors, h_dev, at_dev, b.k, b.width, out=(b.logits, b.hp, b.chosen, b.plain))
         out_pin.copy_(b.chosen, non_blocking=True)
         comp.synchronize()
 

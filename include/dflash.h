@@ -292,6 +292,19 @@ int dflash_select(dflash_t *d, int32_t batch, const float *logits, const float *
                   const uint32_t *anchor_tok, int32_t k, int32_t width, uint32_t *chosen,
                   uint32_t *plain, void *stream);
 
+/* dflash_block then dflash_select in one call, with the same arguments and
+ * results (logits and hp are written as dflash_block writes them; chosen and
+ * plain are the tokens dflash_select would return for them). When the head's
+ * GEMM gives every CTA whole row tiles over the full hidden width (at most 32
+ * draft rows, and at least two row-tile pairs a CTA, as with a full
+ * vocabulary), the GEMM also finds each row's largest key (logit, then lower
+ * index) of every 2048 logits, the selector's first stage, from the values it
+ * writes, so that the logits are not read back for it; otherwise the selector
+ * runs its own first stage. Errors: those of dflash_block and dflash_select. */
+int dflash_draft(dflash_t *d, int32_t batch, const int64_t *anchor_pos, const float *h, int32_t k,
+                 int32_t width, const uint32_t *anchor_tok, float *logits, float *hp, uint32_t *chosen,
+                 uint32_t *plain, void *stream);
+
 /* The selector for callers that cannot allocate device memory: code running
  * under another framework's memory pool (which owns the device heap and does
  * not let a plug-in call cudaMalloc), decode loops that must not take

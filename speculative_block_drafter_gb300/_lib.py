@@ -111,6 +111,8 @@ EXPORTS = {
                                C.c_void_p, C.c_void_p, C.c_void_p]),
     "dflash_select": (C.c_int, [C.c_void_p, C.c_int32, C.c_void_p, C.c_void_p, C.c_void_p, C.c_int32, C.c_int32,
                                 C.c_void_p, C.c_void_p, C.c_void_p]),
+    "dflash_draft": (C.c_int, [C.c_void_p, C.c_int32, C.POINTER(C.c_int64), C.c_void_p, C.c_int32, C.c_int32,
+                               C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p]),
     "dflash_select_static": (C.c_int, [C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_int32,
                                        C.c_int32, C.c_int32, C.c_int32, C.c_int32, C.c_int32, C.c_void_p,
                                        C.c_void_p, C.c_void_p]),
@@ -276,6 +278,11 @@ def dflash_block(h, batch, anchor_pos, hrows, k, width, logits, hp, stream):
 
 def dflash_select(h, batch, logits, hp, anchor_tok, k, width, chosen, plain, stream):
     _check(lib().dflash_select(h, batch, logits, hp, anchor_tok, k, width, chosen, plain, stream))
+
+
+def dflash_draft(h, batch, anchor_pos, hrows, k, width, anchor_tok, logits, hp, chosen, plain, stream):
+    ap = (C.c_int64 * batch)(*[int(a) for a in anchor_pos])
+    _check(lib().dflash_draft(h, batch, ap, hrows, k, width, anchor_tok, logits, hp, chosen, plain, stream))
 
 
 def dflash_select_static(logits, hp, anchor_tok, pred_book, succ_book, batch, k, width, vocab, rank, top, chosen,

@@ -107,6 +107,7 @@ __device__ __forceinline__ unsigned long long cand_key(float v, uint32_t idx) {
 }
 __device__ __forceinline__ uint32_t cand_index(unsigned long long k) { return 0xFFFFFFFFu - (uint32_t)k; }
 
+__device__ __forceinline__ unsigned long long umax64(unsigned long long a, unsigned long long b) { return a > b ? a : b; }
 __device__ __forceinline__ unsigned long long warp_max_u64(unsigned long long v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
@@ -127,9 +128,10 @@ __host__ __device__ __forceinline__ uint32_t sw128_off(int r, int c) {
 // per (token tile tt, k-tile kt, plane p) TT rows x 64 columns f16, K-major
 // with the 128-byte swizzle. Plane 0 = f16(x); plane 1 = f16(x - f16(x)).
 // Chunk t < ceil(T/TT) * (K/64) * TT * 8; rows past T are zero.
-template <int PLANES>
-__device__ __forceinline__ void pack_act_chunk(const float *__restrict__ X, int ldx, int T, int K, int TT,
-                                               uint4 *__restrict__ dst, int64_t t) {
+// Its two halves, so that a caller can have several chunks' loads in flight
+// before the stores: the 8 values of chunk t (zeros past T), then their store.
+__device__ __forceinline__ void pack_chunk_load(const float *__restrict__ X, int ldx, int T, int K, int TT, int64_t t,
+                                                float (&x)[8]) {
   const int KT = K / 64;
   const int c = (int)(t & 7);
   const int r = (int)((t >> 3) % TT);
@@ -137,11 +139,10 @@ __device__ __forceinline__ void pack_act_chunk(const float *__restrict__ X, int 
   const int kt = (int)(rest % KT);
   const int tt = (int)(rest / KT);
   const int tok = tt * TT + r;
-  float x[8];
   if (tok < T) {
     const float *src = X + (int64_t)tok * ldx + kt * 64 + c * 8;
     if ((((uintptr_t)src) & 15) == 0) {
-      const float4 a = ((const float4 *)src)[0], b = ((const float4 *)src)[1];
+      const float4 a = __ldg((const float4 *)src), b = __ldg((const float4 *)src + 1);
       x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
       x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
     } else {
@@ -152,6 +153,16 @@ __device__ __forceinline__ void pack_act_chunk(const float *__restrict__ X, int 
 #pragma unroll
     for (int i = 0; i < 8; ++i) x[i] = 0.f;
   }
+}
+template <int PLANES>
+__device__ __forceinline__ void pack_chunk_store(int K, int TT, int64_t t, const float (&x)[8],
+                                                 uint4 *__restrict__ dst) {
+  const int KT = K / 64;
+  const int c = (int)(t & 7);
+  const int r = (int)((t >> 3) % TT);
+  const int64_t rest = (t >> 3) / TT;
+  const int kt = (int)(rest % KT);
+  const int tt = (int)(rest / KT);
   uint32_t hi[4], lo[4];
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
@@ -164,6 +175,13 @@ __device__ __forceinline__ void pack_act_chunk(const float *__restrict__ X, int 
   const int64_t base = (((int64_t)tt * KT + kt) * PLANES) * TT * 8;  // in 16-byte chunks
   dst[base + sw128_off(r, c) / 16] = make_uint4(hi[0], hi[1], hi[2], hi[3]);
   if (PLANES == 2) dst[base + TT * 8 + sw128_off(r, c) / 16] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+}
+template <int PLANES>
+__device__ __forceinline__ void pack_act_chunk(const float *__restrict__ X, int ldx, int T, int K, int TT,
+                                               uint4 *__restrict__ dst, int64_t t) {
+  float x[8];
+  pack_chunk_load(X, ldx, T, K, TT, t, x);
+  pack_chunk_store<PLANES>(K, TT, t, x, dst);
 }
 
 // A GEMM's packed token tiles as a producer kernel writes them: 8 consecutive

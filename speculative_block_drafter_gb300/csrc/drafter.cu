@@ -707,8 +707,16 @@ int dflash_push_rows(dflash_t *d, int32_t seq, int64_t pos, int32_t n, const flo
   return DFLASH_OK;
 }
 
-int dflash_block(dflash_t *d, int32_t batch, const int64_t *anchor_pos, const float *h, int32_t k, int32_t width,
-                 float *logits, float *hp, void *stream) {
+}  // extern "C"
+
+// The block pass. With `stage1` set, and when the head GEMM takes whole k-ranges
+// (the narrow path over the full head), the head also writes the selector's
+// chunk maxima into the drafter's selector scratch, cleared by the pass's last
+// norm: *stage1 is then left true, else false.
+static int block_pass(dflash_t *d, int32_t batch, const int64_t *anchor_pos, const float *h, int32_t k, int32_t width,
+                      float *logits, float *hp, void *stream, bool *stage1) {
+  const bool want_stage1 = stage1 && *stage1;
+  if (stage1) *stage1 = false;
   if (!d) return fail(DFLASH_E_ARG, "block: null drafter");
   const dflash_geometry &g = d->g;
   const int R = g.block;
@@ -754,6 +762,9 @@ int dflash_block(dflash_t *d, int32_t batch, const int64_t *anchor_pos, const fl
     }
   };
   const int Tk = batch * k;
+  bool fuse = false;
+  unsigned long long *cmax = nullptr;
+  int nchunks = 0;
 
   if (T <= 32) {
     // Up to 32 rows: every GEMM reads token tiles that the kernel before it
@@ -824,14 +835,29 @@ int dflash_block(dflash_t *d, int32_t batch, const int64_t *anchor_pos, const fl
         const dfl::TcJob ends[2] = {{d->w.head.data, d->w.head.scales, logits, width, width},
                                     {d->w.sel.data, nullptr, hp, g.selector_rank, g.selector_rank}};
         const bool split = dfl::tc_splits_int4(&ends[0], 1, Tk, hs, sms) || dfl::tc_splits_f16(&ends[1], 1, Tk, hs, sms);
+        dfl::ZeroSet z = zero_for(ends, 2, split, Tk);
+        // the selector's chunk maxima and candidate counts, when the head computes the former
+        fuse = want_stage1 && dfl::tc_int4_whole(&ends[0], 1, Tk, hs, sms);
+        if (fuse) {
+          int *cnt;
+          dfl::select_stage1(d->sel, Tk, width, &cmax, &cnt, &nchunks);
+          z.T = Tk;
+          z.y[z.count] = (float *)cmax;
+          z.ldy[z.count] = 2 * nchunks;
+          z.n[z.count++] = 2 * nchunks;
+          z.y[z.count] = (float *)cnt;
+          z.ldy[z.count] = 1;
+          z.n[z.count++] = 1;
+        }
         DF_CUDA(dfl::rms_pack(d->h, d->o, d->d2, L.mlp_base, kn, gs, d->w.norm, nullptr, T, hs, eps, R, 1, k,
-                              pack_for(2, dfl::tc_tile_rows(Tk, true), hs), zero_for(ends, 2, split, Tk), st));
+                              pack_for(2, dfl::tc_tile_rows(Tk, true), hs), z, st));
       }
     }
     // the head and the selector's projection over rows 1..k (the selector reads the hi plane)
     const int th = dfl::tc_tile_rows(Tk, true);
     const dfl::TcJob hj{d->w.head.data, d->w.head.scales, logits, width, width};
-    DF_CUDA(dfl::tc_gemm_int4_packed(&hj, 1, grp, d->act, Tk, hs, sms, st));
+    DF_CUDA(dfl::tc_gemm_int4_packed(&hj, 1, grp, d->act, Tk, hs, sms, st, fuse ? cmax : nullptr, nchunks));
+    if (stage1) *stage1 = fuse;
     const dfl::TcJob sj{d->w.sel.data, nullptr, hp, g.selector_rank, g.selector_rank};
     DF_CUDA(dfl::tc_gemm_f16_packed(&sj, 1, d->act, 2 * th * 128, Tk, hs, sms, st));
     return DFLASH_OK;
@@ -875,6 +901,28 @@ int dflash_block(dflash_t *d, int32_t batch, const int64_t *anchor_pos, const fl
   DF_CUDA(dfl::tc_gemm_int4(&hj, 1, grp, d->x, hs, Tk, hs, d->act, sms, st));
   const dfl::TcJob sj{d->w.sel.data, nullptr, hp, g.selector_rank, g.selector_rank};
   DF_CUDA(dfl::tc_gemm_f16(&sj, 1, d->x, hs, Tk, hs, d->act, sms, st));
+  return DFLASH_OK;
+}
+
+extern "C" {
+
+int dflash_block(dflash_t *d, int32_t batch, const int64_t *anchor_pos, const float *h, int32_t k, int32_t width,
+                 float *logits, float *hp, void *stream) {
+  return block_pass(d, batch, anchor_pos, h, k, width, logits, hp, stream, nullptr);
+}
+
+int dflash_draft(dflash_t *d, int32_t batch, const int64_t *anchor_pos, const float *h, int32_t k, int32_t width,
+                 const uint32_t *anchor_tok, float *logits, float *hp, uint32_t *chosen, uint32_t *plain,
+                 void *stream) {
+  if (!d) return fail(DFLASH_E_ARG, "draft: null drafter");
+  if (!anchor_tok || !chosen || !plain) return fail(DFLASH_E_ARG, "draft: null pointer");
+  bool stage1 = true;
+  int rc = block_pass(d, batch, anchor_pos, h, k, width, logits, hp, stream, &stage1);
+  if (rc != DFLASH_OK) return rc;
+  const dflash_geometry &g = d->g;
+  DF_CUDA(dfl::select_tokens(logits, hp, anchor_tok, d->w.pred_book, d->w.succ_book, batch, k, width, g.selector_rank,
+                             g.selector_top, g.vocab, d->sel, chosen, plain, d->num_sms, (cudaStream_t)stream,
+                             stage1));
   return DFLASH_OK;
 }
 

@@ -111,6 +111,7 @@ cudaError_t tc_gemm_f16(const TcJob *jobs, int njobs, const float *X, int ldx, i
 // cleared first and accumulated with atomics. Jobs share K; `tile0` (set
 // here) is a job's first row tile in the concatenation of all jobs' 128-row
 // tiles. The jobs travel by value in the launch (K and V of up to 64 layers).
+constexpr int SELECT_CHUNK = 2048;   // logits per chunk of the selector's first stage
 constexpr int WIDE_MAX_N = 256;      // token rows of one MMA
 constexpr int WIDE_MAX_JOBS = 128;
 struct WideJob {
@@ -145,8 +146,13 @@ cudaError_t wide_gemm(const WideJob *jobs, int njobs, int64_t y_off, bool int4, 
 int tc_tile_rows(int T, bool int4);
 bool tc_splits_int4(const TcJob *jobs, int njobs, int T, int K, int num_sms);
 bool tc_splits_f16(const TcJob *jobs, int njobs, int T, int K, int num_sms);
+// With `cmax` (one job whose launch takes whole k-ranges: tc_int4_whole), the
+// kernel also adds each token's largest key of every SELECT_CHUNK rows into
+// cmax[token * nchunks + chunk] (atomicMax; cleared beforehand): the
+// selector's first stage, from the values it stores.
+bool tc_int4_whole(const TcJob *jobs, int njobs, int T, int K, int num_sms);
 cudaError_t tc_gemm_int4_packed(const TcJob *jobs, int njobs, int group, const void *act, int T, int K, int num_sms,
-                                cudaStream_t st);
+                                cudaStream_t st, unsigned long long *cmax = nullptr, int nchunks = 0);
 cudaError_t tc_gemm_f16_packed(const TcJob *jobs, int njobs, const void *act, int bstride, int T, int K, int num_sms,
                                cudaStream_t st);
 
@@ -239,9 +245,14 @@ cudaError_t attention(const float *q, const CUtensorMap &own_k, const CUtensorMa
 
 // -------------------------------------------------------------- selector (select.cu)
 size_t select_scratch_bytes(int max_rows, int width, int top);
+// `stage1_done`: the chunk maxima (and the cleared candidate counts) are
+// already in the scratch (the head GEMM wrote them): the first stage is skipped.
 cudaError_t select_tokens(const float *logits, const float *hp, const uint32_t *anchor_tok,
                           const uint16_t *pred, const uint16_t *succ, int batch, int k, int width, int rank,
                           int top, int vocab, void *scratch, uint32_t *chosen, uint32_t *plain, int num_sms,
-                          cudaStream_t st);
+                          cudaStream_t st, bool stage1_done = false);
+// Where a call over `rows` rows of `width` logits keeps its chunk maxima
+// ([rows][nchunks] keys) and candidate counts ([rows] ints) in `scratch`.
+void select_stage1(void *scratch, int rows, int width, unsigned long long **cmax, int **cnt, int *nchunks);
 
 }  // namespace dfl

@@ -28,7 +28,7 @@
 namespace dfl {
 
 constexpr int SEL_THREADS = 256;
-constexpr int SEL_CHUNK = 2048;                    // logits per chunk of stage 1
+constexpr int SEL_CHUNK = SELECT_CHUNK;            // logits per chunk of stage 1
 constexpr int ROW_THREADS = 512;
 constexpr int CAND_CAP = 1024;                     // candidates (and chunk maxima) a row CTA holds
 constexpr int MAX_CHUNKS = CAND_CAP;               // width <= 2 M
@@ -46,7 +46,6 @@ static size_t row_scratch(int width, int top) {
 }
 size_t select_scratch_bytes(int max_rows, int width, int top) { return (size_t)max_rows * row_scratch(width, top) + 256; }
 
-__device__ __forceinline__ unsigned long long umax64(unsigned long long a, unsigned long long b) { return a > b ? a : b; }
 
 // Stage 1: a CTA per (group of cpb chunks, row), eight logits a thread per chunk.
 __global__ void __launch_bounds__(SEL_THREADS) k_chunk_max(const float *__restrict__ logits, int width, int nchunks,
@@ -259,9 +258,16 @@ __global__ void __launch_bounds__(CHAIN_THREADS) k_chain(const uint32_t *__restr
   }
 }
 
+void select_stage1(void *scratch, int rows, int width, unsigned long long **cmax, int **cnt, int *nchunks) {
+  *nchunks = sel_chunks(width);
+  *cmax = (unsigned long long *)scratch;
+  unsigned long long *cands = *cmax + (size_t)rows * *nchunks;
+  *cnt = (int *)(cands + (size_t)rows * CAND_CAP);
+}
+
 cudaError_t select_tokens(const float *logits, const float *hp, const uint32_t *anchor_tok, const uint16_t *pred,
                           const uint16_t *succ, int batch, int k, int width, int rank, int top, int vocab, void *scratch,
-                          uint32_t *chosen, uint32_t *plain, int num_sms, cudaStream_t st) {
+                          uint32_t *chosen, uint32_t *plain, int num_sms, cudaStream_t st, bool stage1_done) {
   if (top > TOP_MAX || rank > RANK_MAX || top < 1 || k > KMAX || rank % 2) return cudaErrorInvalidValue;
   const int nchunks = sel_chunks(width);
   if (nchunks > MAX_CHUNKS) return cudaErrorInvalidValue;
@@ -278,8 +284,11 @@ cudaError_t select_tokens(const float *logits, const float *hp, const uint32_t *
   // chunks a CTA so that stages 1 and 2 are about one wave (8 CTAs an SM)
   const int cpb = std::max(1, (int)(((int64_t)nchunks * rows + 8 * num_sms - 1) / (8 * num_sms)));
   const dim3 g12((nchunks + cpb - 1) / cpb, rows);
-  cudaError_t e = launch_pdl(k_chunk_max, g12, dim3(SEL_THREADS), 0, st, 1, logits, width, nchunks, cpb, cmax, cnt);
-  if (e != cudaSuccess) return e;
+  cudaError_t e = cudaSuccess;
+  if (!stage1_done) {
+    e = launch_pdl(k_chunk_max, g12, dim3(SEL_THREADS), 0, st, 1, logits, width, nchunks, cpb, cmax, cnt);
+    if (e != cudaSuccess) return e;
+  }
   e = launch_pdl(k_chunk_filter, g12, dim3(SEL_THREADS), 0, st, 1, logits, width, top, nchunks, cpb, cmax, cnt,
                  cands);
   if (e != cudaSuccess) return e;

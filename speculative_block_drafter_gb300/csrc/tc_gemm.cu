@@ -253,7 +253,14 @@ struct I4Items {
   int ntt;
   int units;        // < 2^31 (checked at launch)
   int whole;        // CTA ranges at group boundaries (when there are as many groups as CTAs)
+  // With whole runs and one job (the head): the selector's first stage, the
+  // largest key (value, then lower row) of each chunk of I4_KEY_CHUNK rows per
+  // token, added with atomicMax into cmax[token * nchunks + chunk] (cleared
+  // by the producer before); null: none.
+  unsigned long long *cmax;
+  int nchunks;
 };
+constexpr int I4_KEY_CHUNK = 2048;
 
 // The run that starts at unit u and ends at the group's last k-tile or at u1.
 __device__ __forceinline__ void i4_run(const TcJobs &J, const I4Items &P, int MT, int KT, int u, int u1, int &job,
@@ -548,6 +555,24 @@ __global__ void __launch_bounds__(32 * (NDQ + 5 + MT * NP), CPS)
       // the item's rows
       float *y = J.y[job];
       const int ldy = J.ldy[job], n = J.n[job];
+      if (P.cmax && kt1 - kt0 == KT) {
+        // the chunk maxima of the values stored below: the item's MT tiles
+        // start on an even tile, so they lie in one chunk of 2048 rows
+        const int chunk = (m0 * 128) / I4_KEY_CHUNK;
+#pragma unroll
+        for (int t = 0; t < TT; ++t) {
+          const int tok = tt * TT + t;
+          if (tok >= T) break;
+          unsigned long long key = 0ull;
+#pragma unroll
+          for (int jj = 0; jj < MT; ++jj) {
+            const int row = (m0 + jj) * 128 + r;
+            if (jj < mtv && row < n) key = umax64(key, cand_key(acc[jj][t], (uint32_t)row));
+          }
+          key = warp_max_u64(key);
+          if (lane == 0 && key) atomicMax(P.cmax + (int64_t)tok * P.nchunks + chunk, key);
+        }
+      }
 #pragma unroll
       for (int jj = 0; jj < MT; ++jj) {
         const int row = (m0 + jj) * 128 + r;
@@ -900,7 +925,7 @@ static bool i4_maps(const TcJobs &J, int njobs, int KT, int KS, int MT, int DU, 
 
 template <int TT, int DU, int MT>
 static cudaError_t launch_int4(const TcJobs &J, int njobs, const void *act, int K, int T, int ntt, int num_sms,
-                               cudaStream_t st) {
+                               cudaStream_t st, unsigned long long *cmax, int nchunks) {
   using C = I4<TT, DU, MT, I4_KS, I4_CPS, I4_NDQ, I4_P, I4_FOLD>;
   static PerDevice configured;
   cudaError_t e = smem_limit(k_tc_int4<TT, DU, MT, I4_KS, I4_CPS, I4_NDQ, I4_P, I4_FOLD>, C::SMEM, configured);
@@ -911,20 +936,23 @@ static cudaError_t launch_int4(const TcJobs &J, int njobs, const void *act, int 
   int grid;
   bool split;
   plan_int4<MT, I4_CPS>(J, njobs, ntt, K, num_sms, P, grid, split);
+  if (cmax && (!P.whole || njobs != 1)) return cudaErrorInvalidValue;  // the caller asks tc_int4_whole first
+  P.cmax = cmax;
+  P.nchunks = nchunks;
   return launch_pdl(k_tc_int4<TT, DU, MT, I4_KS, I4_CPS, I4_NDQ, I4_P, I4_FOLD>, dim3(grid), dim3(C::THREADS), C::SMEM, st, 1, M, J, P,
                     (const uint8_t *)act, K, T);
 }
 
 // (token tile, quantisation units a k-tile, 128-row tiles an item, tensor-memory A slots)
 static cudaError_t dispatch_int4(const TcJobs &J, int njobs, int group, const void *act, int K, int T, int num_sms,
-                                 cudaStream_t st) {
+                                 cudaStream_t st, unsigned long long *cmax = nullptr, int nchunks = 0) {
   const int TT = tt_int4(T);
   const int ntt = (T + TT - 1) / TT;
   const int DU = drain_units(group);
-  if (TT == 16) return DU == 1 ? launch_int4<16, 1, 2>(J, njobs, act, K, T, ntt, num_sms, st)
-                               : launch_int4<16, 2, 2>(J, njobs, act, K, T, ntt, num_sms, st);
-  return DU == 1 ? launch_int4<32, 1, 1>(J, njobs, act, K, T, ntt, num_sms, st)
-                 : launch_int4<32, 2, 1>(J, njobs, act, K, T, ntt, num_sms, st);
+  if (TT == 16) return DU == 1 ? launch_int4<16, 1, 2>(J, njobs, act, K, T, ntt, num_sms, st, cmax, nchunks)
+                               : launch_int4<16, 2, 2>(J, njobs, act, K, T, ntt, num_sms, st, cmax, nchunks);
+  return DU == 1 ? launch_int4<32, 1, 1>(J, njobs, act, K, T, ntt, num_sms, st, cmax, nchunks)
+                 : launch_int4<32, 2, 1>(J, njobs, act, K, T, ntt, num_sms, st, cmax, nchunks);
 }
 
 int tc_tile_rows(int T, bool int4) { return int4 ? tt_int4(T) : tt_f16(T); }
@@ -942,6 +970,19 @@ bool tc_splits_int4(const TcJob *jobs, int njobs, int T, int K, int num_sms) {
   return split;
 }
 
+bool tc_int4_whole(const TcJob *jobs, int njobs, int T, int K, int num_sms) {
+  TcJobs J;
+  int mtiles;
+  if (T > NARROW_MAX_T || fill_jobs(jobs, njobs, J, mtiles) != cudaSuccess) return false;
+  const int TT = tt_int4(T), ntt = (T + TT - 1) / TT;
+  I4Items P;
+  int grid;
+  bool split;
+  if (TT == 16) plan_int4<2, I4_CPS>(J, njobs, ntt, K, num_sms, P, grid, split);
+  else plan_int4<1, I4_CPS>(J, njobs, ntt, K, num_sms, P, grid, split);
+  return P.whole != 0;
+}
+
 bool tc_splits_f16(const TcJob *jobs, int njobs, int T, int K, int num_sms) {
   TcJobs J;
   int mtiles;
@@ -953,13 +994,13 @@ bool tc_splits_f16(const TcJob *jobs, int njobs, int T, int K, int num_sms) {
 }
 
 cudaError_t tc_gemm_int4_packed(const TcJob *jobs, int njobs, int group, const void *act, int T, int K, int num_sms,
-                                cudaStream_t st) {
+                                cudaStream_t st, unsigned long long *cmax, int nchunks) {
   if (T > NARROW_MAX_T) return cudaErrorInvalidValue;
   TcJobs J;
   int mtiles;
   cudaError_t e = fill_jobs(jobs, njobs, J, mtiles);
   if (e != cudaSuccess) return e;
-  return dispatch_int4(J, njobs, group, act, K, T, num_sms, st);
+  return dispatch_int4(J, njobs, group, act, K, T, num_sms, st, cmax, nchunks);
 }
 
 cudaError_t tc_gemm_int4(const TcJob *jobs, int njobs, int group, const float *X, int ldx, int T, int K, void *act,

@@ -466,18 +466,10 @@ size_t wide_act_bytes(int T, int K, bool int4) {
 // b / WZ_PARTS and a part of that tile's token rows.
 constexpr int WZ_PARTS = 8;
 
-template <int PLANES>
-__global__ void k_wide_pack(const float *__restrict__ X, int ldx, WideArgs A, int Q, uint4 *__restrict__ dst,
-                            int pack_blocks) {
-  pdl_wait();
-  pdl_trigger();
-  if ((int)blockIdx.x < pack_blocks) {
-    const int64_t total = (int64_t)A.ntt * A.KT * A.N * 8;
-    const int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (t < total) pack_act_chunk<PLANES>(X, ldx, A.T, A.K, A.N, dst, t);
-    return;
-  }
-  const int zb = blockIdx.x - pack_blocks;
+// Clearing block zb: boundary q = zb / WZ_PARTS + 1 between two CTAs' ranges,
+// when it falls inside a row tile's k-range, and part zb % WZ_PARTS of that
+// tile's token rows (the runs on either side add into them).
+__device__ void wide_clear(const WideArgs &A, int Q, int zb) {
   const int part = zb % WZ_PARTS, q = zb / WZ_PARTS + 1;
   const int64_t u = (int64_t)q * A.units / Q;
   if (u % A.KT == 0) return;
@@ -486,13 +478,7 @@ __global__ void k_wide_pack(const float *__restrict__ X, int ldx, WideArgs A, in
   if (q > 1 && up % A.KT != 0 && up / A.KT == u / A.KT) return;
   const int64_t tg = u / A.KT;
   const int tt = (int)(tg / A.mtiles), mt = (int)(tg % A.mtiles);
-  int lo = 0, hi = A.njobs - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (A.job[mid].tile0 <= mt) lo = mid;
-    else hi = mid - 1;
-  }
-  const WideJob J = A.job[lo];
+  const WideJob J = A.job[wjob_of(A, mt)];
   const int row0 = (mt - J.tile0) * 128;
   const int rows = min(128, J.n - row0);
   const int toks = min(A.N, A.T - tt * A.N);
@@ -509,12 +495,27 @@ __global__ void k_wide_pack(const float *__restrict__ X, int ldx, WideArgs A, in
   }
 }
 
+template <int PLANES>
+__global__ void k_wide_pack(const float *__restrict__ X, int ldx, WideArgs A, int Q, uint4 *__restrict__ dst,
+                            int pack_blocks) {
+  pdl_wait();
+  pdl_trigger();
+  if ((int)blockIdx.x < pack_blocks) {
+    const int64_t total = (int64_t)A.ntt * A.KT * A.N * 8;
+    const int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (t < total) pack_act_chunk<PLANES>(X, ldx, A.T, A.K, A.N, dst, t);
+    return;
+  }
+  wide_clear(A, Q, blockIdx.x - pack_blocks);
+}
+
 // The token tiles of rows that still need their RMS norm (the settle's t before
 // the K/V GEMM): block b < ntt * N takes token row b, x * (mean(x^2) + eps)^-1/2
 // * w into its packed chunks (zeros past T); the blocks past them clear split
 // tiles as k_wide_pack does. One launch and one round trip of the rows fewer
 // than a norm kernel before the packing.
 constexpr int WR_THREADS = 256;
+constexpr int WR_CHUNKS = 3;  // 8-column chunks a thread holds: rows of up to 6,144 columns in registers
 template <int PLANES>
 __global__ void __launch_bounds__(WR_THREADS) k_wide_rms_pack(const float *__restrict__ X, int ldx,
                                                               const float *__restrict__ w, float eps, WideArgs A, int Q,
@@ -523,35 +524,7 @@ __global__ void __launch_bounds__(WR_THREADS) k_wide_rms_pack(const float *__res
   pdl_trigger();
   if ((int)blockIdx.x >= pack_blocks) {
     // the split tiles' outputs: the clearing blocks of k_wide_pack
-    const int zb = blockIdx.x - pack_blocks;
-    const int part = zb % WZ_PARTS, q = zb / WZ_PARTS + 1;
-    const int64_t u = (int64_t)q * A.units / Q;
-    if (u % A.KT == 0) return;
-    const int64_t up = (int64_t)(q - 1) * A.units / Q;
-    if (q > 1 && up % A.KT != 0 && up / A.KT == u / A.KT) return;
-    const int64_t tg = u / A.KT;
-    const int tt = (int)(tg / A.mtiles), mt = (int)(tg % A.mtiles);
-    int lo = 0, hi = A.njobs - 1;
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (A.job[mid].tile0 <= mt) lo = mid;
-      else hi = mid - 1;
-    }
-    const WideJob J = A.job[lo];
-    const int row0 = (mt - J.tile0) * 128;
-    const int rows = min(128, J.n - row0);
-    const int toks = min(A.N, A.T - tt * A.N);
-    const int per = (toks + WZ_PARTS - 1) / WZ_PARTS;
-    const int t0 = part * per, t1 = min(toks, t0 + per);
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
-    float *base = J.y + A.y_off + (int64_t)(tt * A.N) * J.ldy + row0;
-    const bool v4 = rows == 128 && (J.ldy & 3) == 0 && (((uintptr_t)base) & 15) == 0;
-    for (int t = t0 + warp; t < t1; t += nw) {
-      float *y = base + (int64_t)t * J.ldy;
-      if (v4) ((float4 *)y)[lane] = make_float4(0.f, 0.f, 0.f, 0.f);
-      else
-        for (int r = lane; r < rows; r += 32) y[r] = 0.f;
-    }
+    wide_clear(A, Q, blockIdx.x - pack_blocks);
     return;
   }
   const int tok = blockIdx.x;
@@ -563,9 +536,48 @@ __global__ void __launch_bounds__(WR_THREADS) k_wide_rms_pack(const float *__res
     return;
   }
   const float *xr = X + (int64_t)tok * ldx;
+  __shared__ float red[WR_THREADS / 32];
+  const bool aligned = (((uintptr_t)xr) & 15) == 0;
+  if (nc <= WR_CHUNKS * WR_THREADS && aligned) {
+    // the row stays in registers between its sum of squares and its packing
+    // (chunk c = threadIdx.x + j * WR_THREADS, all loads in flight together)
+    float v[WR_CHUNKS][8];
+    float ss = 0.f;
+#pragma unroll
+    for (int j = 0; j < WR_CHUNKS; ++j) {
+      const int c = threadIdx.x + j * WR_THREADS;
+      if (c < nc) {
+        const float4 a = __ldg((const float4 *)(xr + 8 * c)), b = __ldg((const float4 *)(xr + 8 * c) + 1);
+        v[j][0] = a.x; v[j][1] = a.y; v[j][2] = a.z; v[j][3] = a.w;
+        v[j][4] = b.x; v[j][5] = b.y; v[j][6] = b.z; v[j][7] = b.w;
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < WR_CHUNKS; ++j)
+      if (threadIdx.x + j * WR_THREADS < nc)
+#pragma unroll
+        for (int e = 0; e < 8; ++e) ss = fmaf(v[j][e], v[j][e], ss);
+    ss = warp_sum(ss);
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
+    __syncthreads();
+    float tot = 0.f;
+#pragma unroll
+    for (int i = 0; i < WR_THREADS / 32; ++i) tot += red[i];
+    const float sc = 1.0f / sqrtf(tot / (float)A.K + eps);
+#pragma unroll
+    for (int j = 0; j < WR_CHUNKS; ++j) {
+      const int c = threadIdx.x + j * WR_THREADS;
+      if (c < nc) {
+        float o[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) o[e] = v[j][e] * sc * __ldg(w + 8 * c + e);
+        pack_store8(P, tok, 8 * c, o);
+      }
+    }
+    return;
+  }
   float ss = 0.f;
   for (int i = threadIdx.x; i < A.K; i += WR_THREADS) ss = fmaf(xr[i], xr[i], ss);
-  __shared__ float red[WR_THREADS / 32];
   ss = warp_sum(ss);
   if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
   __syncthreads();

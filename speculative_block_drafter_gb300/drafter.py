@@ -222,6 +222,26 @@ class Drafter:
                         chosen.data_ptr(), plain.data_ptr(), _stream())
         return chosen, plain
 
+    def draft(self, anchor_pos: Sequence[int], h: torch.Tensor, anchor_tok: torch.Tensor, k: Optional[int] = None,
+              width: Optional[int] = None, out: Optional[tuple] = None):
+        """block() then select() in one call (dflash_draft): (logits, hp, chosen, plain)."""
+        g = self.g
+        batch = len(anchor_pos)
+        k = g.block - 1 if k is None else k
+        width = g.vocab if width is None else width
+        assert h.dtype == torch.float32 and h.is_cuda and h.is_contiguous() and h.numel() == batch * g.block * g.hidden
+        assert anchor_tok.dtype == torch.int32 and anchor_tok.is_cuda and anchor_tok.numel() == batch
+        if out is None:
+            logits = torch.empty(batch, k, width, dtype=torch.float32, device=self.dev)
+            hp = torch.empty(batch, k, g.selector_rank, dtype=torch.float32, device=self.dev)
+            chosen = torch.empty(batch, k, dtype=torch.int32, device=self.dev)
+            plain = torch.empty(batch, k, dtype=torch.int32, device=self.dev)
+        else:
+            logits, hp, chosen, plain = out
+        L.dflash_draft(self.h, batch, anchor_pos, h.data_ptr(), k, width, anchor_tok.data_ptr(), logits.data_ptr(),
+                       hp.data_ptr(), chosen.data_ptr(), plain.data_ptr(), _stream())
+        return logits, hp, chosen, plain
+
     def close(self):
         if getattr(self, "h", None):
             L.dflash_destroy(self.h)

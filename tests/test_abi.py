@@ -136,6 +136,27 @@ def test_settle_and_block_argument_errors_before_any_launch(L):
     L.dflash_destroy(h)
 
 
+def test_draft_argument_errors_before_any_launch(L):
+    """dflash_draft refuses what dflash_block or dflash_select would refuse, and null
+    token pointers, on the host."""
+    h, keep = _fake_create(L, max_batch=1, cap=64)
+    rows, p = 1 << 24, 1 << 25
+    for k, width in ((0, 4096), (16, 4096), (15, 7), (15, 4097)):
+        with pytest.raises(L.DflashError) as e:
+            L.dflash_draft(h, 1, [0], rows, k, width, p, p, p, p, p, None)
+        assert e.value.code == 2
+    with pytest.raises(L.DflashError) as e:               # batch above max_batch
+        L.dflash_draft(h, 2, [0, 0], rows, 15, 4096, p, p, p, p, p, None)
+    assert e.value.code == 2
+    for null in range(3):                                 # anchor tokens, chosen, plain
+        ptrs = [p, p, p]
+        ptrs[null] = 0
+        with pytest.raises(L.DflashError) as e:
+            L.dflash_draft(h, 1, [0], rows, 15, 4096, ptrs[0], p, p, ptrs[1], ptrs[2], None)
+        assert e.value.code == 2
+    L.dflash_destroy(h)
+
+
 def test_create_rejects_small_workspace_and_null_weights(L):
     g = _geom(L)
     h = C.c_void_p()

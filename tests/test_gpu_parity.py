@@ -178,14 +178,18 @@ class Pair:
                             check_close(f"V layer {l}", v, o.ctx_v[l], self.cache_rel))
         return worst
 
-    def draft(self, anchors, hs_rows, anchor_toks, k=None, width=None):
+    def draft(self, anchors, hs_rows, anchor_toks, k=None, width=None, fused=False):
+        """block + select (or, fused, dflash_draft) against the oracle's draft."""
         g = self.g
         k = g.block - 1 if k is None else k
         width = g.vocab if width is None else width
         h = torch.from_numpy(np.stack(hs_rows).astype(np.float32)).cuda().contiguous()
-        logits, hp = self.gpu.block(anchors, h, k, width)
         at = torch.tensor(anchor_toks, dtype=torch.int32, device="cuda")
-        chosen, plain = self.gpu.select(logits, hp, at)
+        if fused:
+            logits, hp, chosen, plain = self.gpu.draft(anchors, h, at, k, width)
+        else:
+            logits, hp = self.gpu.block(anchors, h, k, width)
+            chosen, plain = self.gpu.select(logits, hp, at)
         torch.cuda.synchronize()
         res = []
         for b in range(len(anchors)):
@@ -342,6 +346,39 @@ def test_full_27b_workload():
     assert p.check_cache() < 1e-4
     a = di.anchor_token(g, wl.seed)
     r = p.draft([wl.context], [di.block_rows(g, wl.seed, a)], [a])[0]
+    assert r["logit_err"] < LOGIT_REL, r
+    # dflash_draft: the head's GEMM finds the selector's chunk maxima itself
+    r = p.draft([wl.context], [di.block_rows(g, wl.seed, a)], [a], fused=True)[0]
+    assert r["logit_err"] < LOGIT_REL, r
+
+
+@pytest.mark.parametrize("name,k,width", [("qwen3-0.6b", 15, None), ("qwen3-0.6b", 7, 100000), ("tiny", 15, None)])
+def test_draft_equals_block_then_select(name, k, width):
+    """dflash_draft gives the logits, hp and tokens of dflash_block then dflash_select
+    (the head's chunk maxima in the GEMM when it takes whole k-ranges, the selector's
+    own first stage otherwise: tiny's 4096-row head); the tokens also against the oracle."""
+    wl = di.workload(name)
+    g = wl.geometry
+    p = Pair(g, seed=wl.seed, ctx_cap=wl.context + 256)
+    p.settle(0, 0, di.make_taps(g, wl.seed, wl.context), chunk=256)
+    a = di.anchor_token(g, wl.seed)
+    rows = di.block_rows(g, wl.seed, a)
+    width = g.vocab if width is None else width
+    h = torch.from_numpy(rows[None].astype(np.float32)).cuda().contiguous()
+    at = torch.tensor([a], dtype=torch.int32, device="cuda")
+    lb, hb = p.gpu.block([wl.context], h, k, width)
+    cb, pb = p.gpu.select(lb, hb, at)
+    lb, hb, cb, pb = lb.clone(), hb.clone(), cb.clone(), pb.clone()
+    ld, hd, cd, pd = p.gpu.draft([wl.context], h, at, k, width)
+    torch.cuda.synchronize()
+    # the block pass is the same launch sequence, but split GEMMs add with atomics: two
+    # passes agree to rounding, which an f16 rounding of a kernel projection's input can
+    # turn into about 5e-4 of a logit (the bar of the 0.6B workload's logits)
+    assert float((ld - lb).abs().max()) <= 5e-4 * float(lb.abs().max())
+    assert float((hd - hb).abs().max()) <= 5e-4 * float(hb.abs().max())
+    if torch.equal(ld, lb) and torch.equal(hd, hb):
+        assert torch.equal(cd, cb) and torch.equal(pd, pb)
+    r = p.draft([wl.context], [rows], [a], k, width, fused=True)[0]
     assert r["logit_err"] < LOGIT_REL, r
 
 
