@@ -122,12 +122,14 @@ bool byte_map(CUtensorMap *m, const void *base, int rank, const uint64_t *dims, 
 // were settled or projected.
 //   warp 8    tensor copies of each chunk's K and V planes (boxes of 64 rows x
 //             64 halves, 128-byte swizzled) into a ring of stages
-//   warp 9    the MMAs, one thread: S = Qh Kh + Qh Kl + Ql Kh (PL = 2) or
-//             Qh K + Ql K (PL = 1), K read K-major from the stage; then, once
-//             the chunk's P is written, O += Ph Vh + Ph Vl + Pl Vh (or Ph V +
-//             Pl V), V read MN-major from the same stage. QK of chunk j+1 is
-//             issued before PV of chunk j, so the softmax of one chunk runs
-//             while the tensor cores take the next.
+//   warp 9    the score MMAs, one thread: S = Qh Kh + Qh Kl + Ql Kh (PL = 2)
+//             or Qh K + Ql K (PL = 1), K read K-major from the stage
+//   warp 10   the output MMAs, one thread: once the chunk's P is written,
+//             O += Ph Vh + Ph Vl + Pl Vh (or Ph V + Pl V), V read MN-major from
+//             the same stage. An MMA holds its issuing thread for about 150
+//             cycles whatever its N, so the two kinds are issued side by side;
+//             the softmax of one chunk runs while the next chunk's scores are
+//             taken. A stage is released by both threads' commits.
 //   warps 0-7 two threads a query row, each with half of a chunk's keys (warp w
 //             takes the rows of tensor-memory lanes 32 (w % 4).. and key half
 //             w / 4): the scores from tensor memory, the window mask, the row's
@@ -159,7 +161,7 @@ struct AttnTc {
   // operand descriptor of the last stage can reach beyond
   static constexpr size_t BYTES = (size_t)STAGES * STAGE + 1024 + 8 * NBAR + 16 + 20 * 1024;
 };
-constexpr int ATT_TC_THREADS = 320;
+constexpr int ATT_TC_THREADS = 352;
 constexpr int ATT_SM_THREADS = 256;  // the softmax warps 0-7
 constexpr float ATT_TAU = 11.f;      // P <= 2^11 between rescales
 
@@ -227,7 +229,7 @@ __global__ void __launch_bounds__(ATT_TC_THREADS, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < S; ++i) {
       mbar_init(kvfull + 8 * i, 1);
-      mbar_init(kvempty + 8 * i, 1);
+      mbar_init(kvempty + 8 * i, 2);  // released by the Q K and the P V products
     }
     mbar_init(qfull, 128);
     for (int i = 0; i < 2; ++i) {
@@ -237,7 +239,7 @@ __global__ void __launch_bounds__(ATT_TC_THREADS, 1)
       mbar_init(pfree + 8 * i, 1);
     }
     mbar_init(obar, 1);
-    mbar_init(fin, 1);
+    mbar_init(fin, 2);  // the two issuing threads' last commits
     mbar_fence_init();
   }
   pdl_wait();
@@ -274,51 +276,58 @@ __global__ void __launch_bounds__(ATT_TC_THREADS, 1)
       for (int j = (issued > S ? issued - S : 0); j < issued; ++j) mbar_wait(kvfull + 8 * (j % S), (j / S) & 1);
     }
   } else if (warp == 9) {
+    // S = Q K^T of each chunk into score buffer j & 1. An MMA holds its issuing
+    // thread for about 150 cycles whatever its N, so the P V products have a
+    // warp of their own (warp 10).
     if (lane == 0 && nch > 0) {
       bool ok = mbar_wait(qfull, 0);
       tc_fence_after();
-      for (int j = 0; j <= nch && ok; ++j) {
-        if (j < nch) {
-          // S = Q K^T of chunk j into score buffer j & 1
-          const int st = j % S, sb = j & 1;
-          if (!mbar_wait_spin(kvfull + 8 * st, (j / S) & 1)) break;
-          if (j >= 2 && !mbar_wait_spin(sfree + 8 * sb, ((j >> 1) - 1) & 1)) break;
-          tc_fence_after();
-          const bool is_own = own && j == nch - 1;
-          const uint32_t idesc = f16_idesc(128, is_own ? 16 : CH);
-          const uint32_t kh = ring + st * C::STAGE, kl = kh + C::REGION;
-          const uint32_t dS = tb + C::S0 + sb * 64;
+      for (int j = 0; j < nch && ok; ++j) {
+        const int st = j % S, sb = j & 1;
+        if (!mbar_wait_spin(kvfull + 8 * st, (j / S) & 1)) break;
+        if (j >= 2 && !mbar_wait_spin(sfree + 8 * sb, ((j >> 1) - 1) & 1)) break;
+        tc_fence_after();
+        const bool is_own = own && j == nch - 1;
+        const uint32_t idesc = f16_idesc(128, is_own ? 16 : CH);
+        const uint32_t kh = ring + st * C::STAGE, kl = kh + C::REGION;
+        const uint32_t dS = tb + C::S0 + sb * 64;
 #pragma unroll
-          for (int ks = 0; ks < HD / 16; ++ks) {
-            const uint32_t off = (ks >> 2) * C::BOX + (ks & 3) * 32;
-            mma_ts(dS, tb + C::QH + ks * 8, sw128_desc(kh + off), idesc, ks > 0);
-            if (PL == 2) mma_ts(dS, tb + C::QH + ks * 8, sw128_desc(kl + off), idesc, 1);
-            mma_ts(dS, tb + C::QL + ks * 8, sw128_desc(kh + off), idesc, 1);
-          }
-          mma_commit(sfull + 8 * sb);
+        for (int ks = 0; ks < HD / 16; ++ks) {
+          const uint32_t off = (ks >> 2) * C::BOX + (ks & 3) * 32;
+          mma_ts(dS, tb + C::QH + ks * 8, sw128_desc(kh + off), idesc, ks > 0);
+          if (PL == 2) mma_ts(dS, tb + C::QH + ks * 8, sw128_desc(kl + off), idesc, 1);
+          mma_ts(dS, tb + C::QL + ks * 8, sw128_desc(kh + off), idesc, 1);
         }
-        if (j >= 1) {
-          // O += P V of chunk j - 1, once its P is written
-          const int jj = j - 1, st = jj % S, pb = jj & 1;
-          if (!mbar_wait_spin(pfull + 8 * pb, (jj >> 1) & 1)) break;
-          tc_fence_after();
-          const bool is_own = own && jj == nch - 1;
-          const int ksteps = is_own ? 1 : CH / 16;
-          const uint32_t idesc = f16_idesc_bmn(128, HD);
-          const uint32_t vh = ring + st * C::STAGE + PL * C::REGION, vl = vh + C::REGION;
-          const uint32_t ph = tb + C::P0 + pb * 64, pl = ph + 32;
-          for (int kk = 0; kk < ksteps; ++kk) {
-            const uint64_t bh = sw128_mn_desc(vh + kk * 2048, C::BOX), bl = sw128_mn_desc(vl + kk * 2048, C::BOX);
-            mma_ts(tb + C::OC, ph + kk * 8, bh, idesc, (jj > 0 || kk > 0));
-            if (PL == 2) mma_ts(tb + C::OC, ph + kk * 8, bl, idesc, 1);
-            mma_ts(tb + C::OC, pl + kk * 8, bh, idesc, 1);
-          }
-          mma_commit(obar);
-          mma_commit(pfree + 8 * pb);
-          mma_commit(kvempty + 8 * st);
-        }
+        mma_commit(sfull + 8 * sb);
+        mma_commit(kvempty + 8 * st);  // K read (the stage's other release: P V)
       }
-      // every MMA issued has completed before the tensor memory is freed
+      // every MMA of this thread completed before the tensor memory is freed
+      mma_commit(fin);
+      mbar_wait(fin, 0);
+    }
+  } else if (warp == 10) {
+    // O += P V of each chunk, once its P is written
+    if (lane == 0 && nch > 0) {
+      for (int jj = 0; jj < nch; ++jj) {
+        const int st = jj % S, pb = jj & 1;
+        if (!mbar_wait_spin(kvfull + 8 * st, (jj / S) & 1)) break;
+        if (!mbar_wait_spin(pfull + 8 * pb, (jj >> 1) & 1)) break;
+        tc_fence_after();
+        const bool is_own = own && jj == nch - 1;
+        const int ksteps = is_own ? 1 : CH / 16;
+        const uint32_t idesc = f16_idesc_bmn(128, HD);
+        const uint32_t vh = ring + st * C::STAGE + PL * C::REGION, vl = vh + C::REGION;
+        const uint32_t ph = tb + C::P0 + pb * 64, pl = ph + 32;
+        for (int kk = 0; kk < ksteps; ++kk) {
+          const uint64_t bh = sw128_mn_desc(vh + kk * 2048, C::BOX), bl = sw128_mn_desc(vl + kk * 2048, C::BOX);
+          mma_ts(tb + C::OC, ph + kk * 8, bh, idesc, (jj > 0 || kk > 0));
+          if (PL == 2) mma_ts(tb + C::OC, ph + kk * 8, bl, idesc, 1);
+          mma_ts(tb + C::OC, pl + kk * 8, bh, idesc, 1);
+        }
+        mma_commit(obar);
+        mma_commit(pfree + 8 * pb);
+        mma_commit(kvempty + 8 * st);
+      }
       mma_commit(fin);
       mbar_wait(fin, 0);
     }
@@ -419,7 +428,12 @@ __global__ void __launch_bounds__(ATT_TC_THREADS, 1)
           mref = mx;
         }
         if (j > 0 && !dead) {
-          ok = __all_sync(0xffffffffu, mbar_wait(obar, (j - 1) & 1));
+          // O holds the products of chunks 0 .. j-1 once obar completed its phase
+          // j-1. The P V products have their own issuing thread, so first make
+          // sure that chunk j-2's completed (it frees P buffer j & 1): obar is
+          // then at most one phase behind and the parity wait cannot pass early
+          if (j >= 2) ok = __all_sync(0xffffffffu, mbar_wait(pfree + 8 * sb, ((j >> 1) - 1) & 1));
+          ok = ok && __all_sync(0xffffffffu, mbar_wait(obar, (j - 1) & 1));
           tc_fence_after();
           if (ok) {
 #pragma unroll

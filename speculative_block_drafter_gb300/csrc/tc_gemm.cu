@@ -408,12 +408,14 @@ __global__ void __launch_bounds__(32 * (NDQ + 5 + MT * NP), CPS)
                 // both activation planes into one accumulator: the hi rows of the
                 // B tile, then its lo rows (TT rows = TT * 128 bytes further on)
                 const uint32_t dcol = tbase + C::DCOL + d * C::DW + jj * (C::DW / MT);
+                // the descriptor's start address counts 16-byte units: a k-step
+                // (32 bytes) is +2, the lo plane (TT rows of 128 bytes) + TT * 8
+                const uint64_t bdesc = sw128_desc(bsub + du * KSU * 32);
+                const uint32_t acol0 = tbase + a * C::AW + jj * 32 + du * KSU * 8;
 #pragma unroll
                 for (int ks = 0; ks < KSU; ++ks) {
-                  const int kstep = du * KSU + ks;
-                  const uint32_t acol = tbase + a * C::AW + jj * 32 + kstep * 8;
-                  mma_ts(dcol, acol, sw128_desc(bsub + kstep * 32), idesc, ks > 0);
-                  if (FOLD) mma_ts(dcol, acol, sw128_desc(bsub + TT * 128 + kstep * 32), idesc, 1);
+                  mma_ts(dcol, acol0 + ks * 8, bdesc + 2 * ks, idesc, ks > 0);
+                  if (FOLD) mma_ts(dcol, acol0 + ks * 8, bdesc + 2 * ks + TT * 8, idesc, 1);
                 }
               }
               mma_commit(dfull0 + 8 * d);
