@@ -59,7 +59,7 @@ constexpr int64_t CONTEXT_CHUNK = 64;
 
 // Workspace carve; sizes in bytes.
 struct Carve {
-  size_t h, x, xc, d, d2, q, k, v, y, o, gt, up, part, sel, act, kvs, kp, vp, total;
+  size_t h, x, xc, d, d2, q, k, v, y, o, gt, up, part, sel, act, act_fc, kvs, kp, vp, total;
 };
 
 Carve carve_of(const dflash_geometry &g, int max_batch) {
@@ -92,10 +92,12 @@ Carve carve_of(const dflash_geometry &g, int max_batch) {
   const int Tb = max_batch * R;
   const int kmax = std::max(std::max(g.hidden, g.intermediate), g.heads * g.head_dim);
   c.act = up(std::max({dfl::tc_act_bytes(Tb, kmax, true), dfl::tc_act_bytes(DFLASH_SETTLE_MAX, g.hidden, true),
-                       dfl::tc_act_bytes(DFLASH_SETTLE_MAX, g.taps * g.hidden, false),
                        dfl::tc_act_bytes(Tb, g.hidden, false)}));
+  // the settle's fc has token tiles of its own, which it packs from the taps while
+  // the previous settle's last kernel runs
+  c.act_fc = up(dfl::tc_act_bytes(DFLASH_SETTLE_MAX, g.taps * g.hidden, false));
   c.total = c.h + c.x + c.xc + c.d + c.d2 + c.q + c.k + c.v + c.y + c.o + c.gt + c.up + c.part + c.sel + c.act +
-            c.kvs + c.kp + c.vp;
+            c.act_fc + c.kvs + c.kp + c.vp;
   return c;
 }
 
@@ -159,7 +161,7 @@ struct dflash_t {
   Carve c{};
   float *h, *x, *xc, *d, *d2, *q, *k, *v, *y, *o, *gt, *up, *part, *kvs;
   __half *kp, *vp;
-  void *sel, *act;
+  void *sel, *act, *act_fc;
   std::vector<Seq> seqs;
   std::vector<float> inv;
   int num_sms = 148;
@@ -265,7 +267,13 @@ int settle_call(dflash_t *d, int seq, const float *taps, int n, cudaStream_t st)
   const dflash_geometry &g = d->g;
   const int hs = g.hidden, tw = g.taps * g.hidden, kvd = g.kv_heads * g.head_dim;
   const dfl::TcJob fc{d->w.fc.data, nullptr, d->x, hs, hs};
-  DF_CUDA(dfl::tc_gemm_f16(&fc, 1, taps, tw, n, tw, d->act, d->num_sms, st));
+  if (n > 32) {
+    // the taps come from the caller: their packing needs no kernel before it
+    const dfl::WideJob fj{d->w.fc.data, nullptr, d->x, hs, hs, 0};
+    DF_CUDA(dfl::wide_gemm(&fj, 1, 0, false, 0, taps, tw, n, tw, d->act_fc, d->num_sms, st, nullptr, 0.f, true));
+  } else {
+    DF_CUDA(dfl::tc_gemm_f16(&fc, 1, taps, tw, n, tw, d->act, d->num_sms, st));
+  }
   // the hidden norm is taken by the K/V GEMM's packing of t (below)
   // k = Wk rms(t), v = Wv rms(t) of every layer in one GEMM (into the
   // workspace), then k normed and rotated and both written into the caches
@@ -581,6 +589,7 @@ int dflash_create_ex(dflash_t **out, const dflash_geometry *g, const dflash_weig
   d->vp = (__half *)take(c.vp);
   d->sel = take(c.sel);
   d->act = take(c.act);
+  d->act_fc = take(c.act_fc);
   d->seqs.assign(max_batch, Seq{});
   // inv_freq = f32(theta^(-2i/hd)) (src/cortiq_engine/dflash.rs, Drafter::new)
   d->inv.resize(g->head_dim / 2);

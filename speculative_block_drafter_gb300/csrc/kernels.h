@@ -134,9 +134,12 @@ void wide_tiles(int T, int &ntt, int &N);
 size_t wide_act_bytes(int T, int K, bool int4);
 // With `norm_w`, the rows of X enter as rms(X[t], norm_w) (eps), the norm taken
 // by the kernel that packs them.
+// With `x_ready` (X does not come from a kernel before this one in the stream,
+// and `act` and the outputs are this GEMM's alone), the packing runs before its
+// dependency wait, overlapping the kernels before it.
 cudaError_t wide_gemm(const WideJob *jobs, int njobs, int64_t y_off, bool int4, int group, const float *X, int ldx,
                       int T, int K, void *act, int num_sms, cudaStream_t st, const float *norm_w = nullptr,
-                      float eps = 0.f);
+                      float eps = 0.f, bool x_ready = false);
 
 // Narrow GEMMs (T <= 32) on token tiles a producer kernel has packed: the
 // tiles' rows, whether the launch will split its k-range (its outputs must then

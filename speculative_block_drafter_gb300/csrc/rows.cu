@@ -285,6 +285,9 @@ __device__ __forceinline__ void store_kv_e(__half *__restrict__ dst, const float
 template <int HD, int PL>
 __global__ void k_ctx_planes(CtxPlanes P, int T, int heads, float eps, int64_t pos_base, int64_t at, int norm) {
   pdl_wait();
+  // the next settle's packing of its taps (which needs nothing of this) may run
+  // meanwhile; every kernel after this one waits for it before touching its data
+  pdl_trigger();
   constexpr int E = HD / 64;
   const int wid = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;

@@ -495,17 +495,23 @@ __device__ void wide_clear(const WideArgs &A, int Q, int zb) {
   }
 }
 
+// With x_ready (X and dst depend on no kernel before this one), the packing
+// blocks do their work before the dependency wait and wait at the end, so that
+// the kernel still completes only after the one before it; the clearing blocks
+// always wait first (the outputs may still be read before).
 template <int PLANES>
 __global__ void k_wide_pack(const float *__restrict__ X, int ldx, WideArgs A, int Q, uint4 *__restrict__ dst,
-                            int pack_blocks) {
-  pdl_wait();
+                            int pack_blocks, int x_ready) {
+  if (!x_ready) pdl_wait();
   pdl_trigger();
   if ((int)blockIdx.x < pack_blocks) {
     const int64_t total = (int64_t)A.ntt * A.KT * A.N * 8;
     const int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (t < total) pack_act_chunk<PLANES>(X, ldx, A.T, A.K, A.N, dst, t);
+    if (x_ready) pdl_wait();
     return;
   }
+  if (x_ready) pdl_wait();
   wide_clear(A, Q, blockIdx.x - pack_blocks);
 }
 
@@ -600,7 +606,7 @@ constexpr int W_RUN_COST = 6;
 
 template <int KIND, int DU>
 static cudaError_t launch_wide(WideArgs &A, const float *X, int ldx, const float *norm_w, float eps, void *act,
-                               int num_sms, cudaStream_t st) {
+                               int num_sms, cudaStream_t st, bool x_ready) {
   using C = WCfg<KIND, DU>;
   static PerDevice smem_set, resident;   // per device: the limit raised; the resident CTAs (0 = not yet)
   auto kern = k_wide<KIND, DU>;
@@ -641,14 +647,16 @@ static cudaError_t launch_wide(WideArgs &A, const float *X, int ldx, const float
   } else {
     const int pack_blocks = (int)((chunks + 255) / 256);
     e = launch_pdl(k_wide_pack<C::PLANES>, dim3(pack_blocks + zero_blocks), dim3(256), 0, st, 1, X, ldx, A, Q,
-                   (uint4 *)act, pack_blocks);
+                   (uint4 *)act, pack_blocks, (int)x_ready);
   }
   if (e != cudaSuccess) return e;
   return launch_pdl(kern, dim3((unsigned)Q), dim3(W_THREADS), C::SMEM, st, 1, A);
 }
 
 cudaError_t wide_gemm(const WideJob *jobs, int njobs, int64_t y_off, bool int4, int group, const float *X, int ldx,
-                      int T, int K, void *act, int num_sms, cudaStream_t st, const float *norm_w, float eps) {
+                      int T, int K, void *act, int num_sms, cudaStream_t st, const float *norm_w, float eps,
+                      bool x_ready) {
+  if (x_ready && norm_w) return cudaErrorInvalidValue;  // the norm's packing waits first
   if (njobs < 1 || njobs > WIDE_MAX_JOBS || T < 1 || K % 64) return cudaErrorInvalidValue;
   WideArgs A{};
   A.njobs = njobs;
@@ -664,9 +672,9 @@ cudaError_t wide_gemm(const WideJob *jobs, int njobs, int64_t y_off, bool int4, 
   A.KT = K / 64;
   A.T = T;
   wide_tiles(T, A.ntt, A.N);
-  if (!int4) return launch_wide<W_KIND_F16, 1>(A, X, ldx, norm_w, eps, act, num_sms, st);
-  return group >= 64 ? launch_wide<W_KIND_I4, 1>(A, X, ldx, norm_w, eps, act, num_sms, st)
-                     : launch_wide<W_KIND_I4, 2>(A, X, ldx, norm_w, eps, act, num_sms, st);
+  if (!int4) return launch_wide<W_KIND_F16, 1>(A, X, ldx, norm_w, eps, act, num_sms, st, x_ready);
+  return group >= 64 ? launch_wide<W_KIND_I4, 1>(A, X, ldx, norm_w, eps, act, num_sms, st, x_ready)
+                     : launch_wide<W_KIND_I4, 2>(A, X, ldx, norm_w, eps, act, num_sms, st, x_ready);
 }
 
 // This file's device error word (a bounded wait that gave up).
