@@ -318,7 +318,11 @@ __global__ void __launch_bounds__(W_THREADS, 1) k_wide(WideArgs A) {
   } else if (warp < 4) {
     const int r = warp * 32 + lane;
     const uint32_t lrow = (uint32_t)(warp * 32) << 16;
-    int i = 0, run = 0, ephase = 0;
+    // slice: the epilogue's 16-token slices so far; the two staging buffers
+    // alternate across runs too, so that a slice is never written while the
+    // one before it in the same buffer may still be read (a run's slices can be
+    // odd in number)
+    int i = 0, run = 0, ephase = 0, slice = 0;
     bool ok = true;
     for (int64_t u = u0; u < u1 && ok; ++run) {
       const int64_t ue = wrun_end(A, u, u1);
@@ -394,8 +398,8 @@ __global__ void __launch_bounds__(W_THREADS, 1) k_wide(WideArgs A) {
         // 16 tokens at a time: TMEM -> registers -> a [token][row] slice in shared
         // memory; then each warp writes 4 whole token rows, 16 bytes a lane
         // (vector stores, or vector atomic adds for a split tile)
-        for (int c0 = 0, ci = 0; c0 < N && ok; c0 += 16, ++ci) {
-          float *stg = staging + (ci & 1) * 16 * 128;
+        for (int c0 = 0; c0 < N && ok; c0 += 16, ++slice) {
+          float *stg = staging + (slice & 1) * 16 * 128;
           uint32_t v16[16];
           tmem_ld16(tbase + lrow + d * 256 + c0, v16);
           tc_wait_ld();
