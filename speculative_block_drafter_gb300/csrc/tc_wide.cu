@@ -52,21 +52,10 @@ struct WCfg {
   static constexpr int SA = 2;                     // tensor-memory A slots (four-bit)
   static constexpr int NBUF = KIND == W_KIND_F16 ? 2 : 1;
   static constexpr int A_COL = 256;                // A slots after the accumulator (four-bit)
-  static constexpr int NBAR = 2 * STAGES + 2 * SA + 2 * NBUF + 1;  // + the epilogue's 128-thread barrier
-  static constexpr int STAGING = 2 * 16 * 128 * 4;  // two slices of 16 tokens x 128 rows f32 (the epilogue)
+  static constexpr int NBAR = 2 * STAGES + 2 * SA + 2 * NBUF;
+  static constexpr int STAGING = 4 * 16 * 32 * 4;  // a slice of 16 tokens x 32 rows f32 a warp (the epilogue)
   static constexpr int SMEM = STAGES * STAGE_MAX + STAGING + 1024 + 8 * NBAR + 64;
 };
-
-// ---------------------------------------------------------------- epilogue helpers
-// The epilogue's warps 0-3 meet on an mbarrier of count 128 (a bounded wait, so
-// that a warp that gave up elsewhere cannot stall the others for ever).
-__device__ __forceinline__ bool drain_bar(uint32_t bar, int &phase) {
-  mbar_arrive(bar);
-  const bool ok = mbar_wait(bar, (uint32_t)phase);
-  phase ^= 1;
-  return ok;
-}
-
 
 __device__ __forceinline__ WideJob wjob(const WideArgs &A, int j) { return A.job[j]; }
 
@@ -190,7 +179,6 @@ __global__ void __launch_bounds__(W_THREADS, 1) k_wide(WideArgs A) {
   uint32_t *tslot = (uint32_t *)(bars + C::NBAR);
   const uint32_t full0 = smem_u32(bars), empty0 = full0 + 8 * S, afull0 = empty0 + 8 * S;
   const uint32_t afree0 = afull0 + 8 * C::SA, dfull0 = afree0 + 8 * C::SA, dfree0 = dfull0 + 8 * C::NBUF;
-  const uint32_t ebar = dfree0 + 8 * C::NBUF;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   // this CTA's units
@@ -212,7 +200,6 @@ __global__ void __launch_bounds__(W_THREADS, 1) k_wide(WideArgs A) {
       mbar_init(dfull0 + 8 * i, 1);
       mbar_init(dfree0 + 8 * i, 128);
     }
-    mbar_init(ebar, 128);
     mbar_fence_init();
   }
   __syncthreads();
@@ -318,11 +305,7 @@ __global__ void __launch_bounds__(W_THREADS, 1) k_wide(WideArgs A) {
   } else if (warp < 4) {
     const int r = warp * 32 + lane;
     const uint32_t lrow = (uint32_t)(warp * 32) << 16;
-    // slice: the epilogue's 16-token slices so far; the two staging buffers
-    // alternate across runs too, so that a slice is never written while the
-    // one before it in the same buffer may still be read (a run's slices can be
-    // odd in number)
-    int i = 0, run = 0, ephase = 0, slice = 0;
+    int i = 0, run = 0;
     bool ok = true;
     for (int64_t u = u0; u < u1 && ok; ++run) {
       const int64_t ue = wrun_end(A, u, u1);
@@ -395,31 +378,32 @@ __global__ void __launch_bounds__(W_THREADS, 1) k_wide(WideArgs A) {
       const int ntok = min(N, A.T - tok0);
       const bool bulk = (rows & 3) == 0 && (J.ldy & 3) == 0 && (((uintptr_t)ybase) & 15) == 0;
       if (bulk) {
-        // 16 tokens at a time: TMEM -> registers -> a [token][row] slice in shared
-        // memory; then each warp writes 4 whole token rows, 16 bytes a lane
-        // (vector stores, or vector atomic adds for a split tile)
-        for (int c0 = 0; c0 < N && ok; c0 += 16, ++slice) {
-          float *stg = staging + (slice & 1) * 16 * 128;
+        // 16 tokens at a time: TMEM -> registers -> this warp's [token][32 rows]
+        // slice in shared memory -> 16 bytes a lane, four tokens an instruction
+        // (vector stores, or vector atomic adds for a split tile). Each warp
+        // turns its own rows around, so the warps never wait for one another.
+        float *stg = staging + warp * 16 * 32;
+        const int rq = 4 * (lane & 7), eq = lane >> 3;  // a lane's 4 rows, and its token of each 4
+        const bool rlive = warp * 32 + rq < rows;
+        for (int c0 = 0; c0 < N; c0 += 16) {
           uint32_t v16[16];
           tmem_ld16(tbase + lrow + d * 256 + c0, v16);
           tc_wait_ld();
 #pragma unroll
-          for (int e = 0; e < 16; ++e) stg[e * 128 + r] = __uint_as_float(v16[e]) * unscale;
-          ok = drain_bar(ebar, ephase);
-          if (4 * lane < rows) {
+          for (int e = 0; e < 16; ++e) stg[e * 32 + lane] = __uint_as_float(v16[e]) * unscale;
+          __syncwarp();
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              const int e = warp * 4 + q;
-              if (c0 + e < ntok) {
-                const float4 v = *(const float4 *)(stg + e * 128 + 4 * lane);
-                float4 *dst = (float4 *)(ybase + (int64_t)(tok0 + c0 + e) * J.ldy) + lane;
-                if (whole) *dst = v;
-                else atomicAdd(dst, v);
-              }
+          for (int q = 0; q < 4; ++q) {
+            const int e = 4 * q + eq;
+            if (rlive && c0 + e < ntok) {
+              const float4 v = *(const float4 *)(stg + e * 32 + rq);
+              float4 *dst = (float4 *)(ybase + (int64_t)(tok0 + c0 + e) * J.ldy + warp * 32 + rq);
+              if (whole) *dst = v;
+              else atomicAdd(dst, v);
             }
           }
+          __syncwarp();
         }
-        ok = __all_sync(0xffffffffu, ok);
       } else {
         const bool live = r < rows;
         float *y = ybase + r;
