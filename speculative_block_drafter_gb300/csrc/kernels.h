@@ -114,6 +114,7 @@ cudaError_t tc_gemm_f16(const TcJob *jobs, int njobs, const float *X, int ldx, i
 constexpr int SELECT_CHUNK = 2048;   // logits per chunk of the selector's first stage
 constexpr int WIDE_MAX_N = 256;      // token rows of one MMA
 constexpr int WIDE_MAX_JOBS = 128;
+constexpr int WIDE_MAX_CTAS = 320;   // CTAs a launch may list its ranges for (WideArgs::bnd)
 struct WideJob {
   const void *w;   // packed codes or f16 tiles
   const void *s;   // packed scales (four-bit), else null
@@ -128,6 +129,9 @@ struct WideArgs {
   const uint8_t *bpack;
   int K, KT, T, N, ntt;
   int64_t units;
+  // CTA q's units are [bnd[q], bnd[q + 1]) when nbnd > 0, else [q U / Q, (q + 1) U / Q)
+  int nbnd;
+  int bnd[WIDE_MAX_CTAS + 1];
   WideJob job[WIDE_MAX_JOBS];
 };
 void wide_tiles(int T, int &ntt, int &N);

@@ -28,6 +28,11 @@
 //   D = Wh xh + Wh xl + Wl xh   (three MMAs a k-step; Wl xl is below 2^-22)
 // and the run's partial sums are multiplied by 2^-p when added to Y.
 #include <algorithm>
+#include <climits>
+#include <map>
+#include <mutex>
+#include <tuple>
+#include <vector>
 
 #include "common.cuh"
 #include "kernels.h"
@@ -68,6 +73,17 @@ __device__ __forceinline__ int wjob_of(const WideArgs &A, int mt) {
     else hi = mid - 1;
   }
   return lo;
+}
+
+// The units [u0, u1) of CTA q of Q.
+__device__ __forceinline__ void wrange(const WideArgs &A, int64_t q, int64_t Q, int64_t &u0, int64_t &u1) {
+  if (A.nbnd > 0) {
+    u0 = A.bnd[q];
+    u1 = A.bnd[q + 1];
+  } else {
+    u0 = q * A.units / Q;
+    u1 = (q + 1) * A.units / Q;
+  }
 }
 
 // A unit: token tile, row tile, k-tile.
@@ -182,9 +198,8 @@ __global__ void __launch_bounds__(W_THREADS, 1) k_wide(WideArgs A) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   // this CTA's units
-  const int64_t q = blockIdx.x, Q = gridDim.x;
-  const int64_t u0 = q * A.units / Q;
-  const int64_t u1 = (q + 1) * A.units / Q;
+  int64_t u0, u1;
+  wrange(A, blockIdx.x, gridDim.x, u0, u1);
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < S; ++i) {
@@ -459,10 +474,11 @@ constexpr int WZ_PARTS = 8;
 // tile's token rows (the runs on either side add into them).
 __device__ void wide_clear(const WideArgs &A, int Q, int zb) {
   const int part = zb % WZ_PARTS, q = zb / WZ_PARTS + 1;
-  const int64_t u = (int64_t)q * A.units / Q;
-  if (u % A.KT == 0) return;
+  int64_t u, up, un;
+  wrange(A, q, Q, u, un);
+  if (u % A.KT == 0 || u >= A.units) return;
   // the tile was cleared for the boundary before if that one split it too
-  const int64_t up = (int64_t)(q - 1) * A.units / Q;
+  wrange(A, q - 1, Q, up, un);
   if (q > 1 && up % A.KT != 0 && up / A.KT == u / A.KT) return;
   const int64_t tg = u / A.KT;
   const int tt = (int)(tg / A.mtiles), mt = (int)(tg % A.mtiles);
@@ -592,6 +608,61 @@ constexpr int W_MIN_RUN = 4;
 // What a run's read-back and atomic add of its partial sums cost, in units.
 constexpr int W_RUN_COST = 6;
 
+// Ranges of equal cost: a CTA's units plus `run_cost` units for each run it
+// holds (a run ends with a read-back of its accumulator, which, with one
+// accumulator, the next run's MMAs wait for). The smallest cost C for which
+// CTAs that each take as many units as C allows cover them all; the CTAs past
+// the last units get none. A CTA's range is walked a tile at a time, and the
+// ranges of a shape are kept (the settle asks for the same few shapes again
+// and again).
+static bool wide_cover(int64_t U, int64_t KT, int Q, int run_cost, int64_t C, int *bnd) {
+  int64_t u = 0;
+  for (int q = 0; q < Q; ++q) {
+    if (bnd) bnd[q] = (int)u;
+    int64_t budget = C;
+    while (u < U && budget > run_cost) {
+      if (u % KT == 0) {  // whole tiles at once, each a run
+        const int64_t whole = std::min(budget / (KT + run_cost), (U - u) / KT);
+        if (whole > 0) {
+          u += whole * KT;
+          budget -= whole * (KT + run_cost);
+          continue;
+        }
+      }
+      budget -= run_cost;  // a run begins at u
+      const int64_t take = std::min(std::min(budget, (u / KT + 1) * KT - u), U - u);
+      u += take;
+      budget -= take;
+      if (u % KT != 0) break;  // the budget ended inside the tile
+    }
+  }
+  if (bnd) bnd[Q] = (int)U;
+  return u >= U;
+}
+
+static void wide_bounds(WideArgs &A, int Q, int run_cost) {
+  static std::mutex mu;
+  static std::map<std::tuple<int64_t, int, int, int>, std::vector<int>> cache;
+  const auto key = std::make_tuple(A.units, A.KT, Q, run_cost);
+  std::lock_guard<std::mutex> lock(mu);
+  auto it = cache.find(key);
+  if (it == cache.end()) {
+    const int64_t U = A.units, KT = A.KT;
+    int64_t lo = (U + Q - 1) / Q, hi = U + (int64_t)run_cost * (U / KT + Q + 1);
+    while (lo < hi) {
+      const int64_t mid = (lo + hi) / 2;
+      if (wide_cover(U, KT, Q, run_cost, mid, nullptr)) hi = mid;
+      else lo = mid + 1;
+    }
+    std::vector<int> b(Q + 1);
+    wide_cover(U, KT, Q, run_cost, lo, b.data());
+    if (cache.size() > 256) cache.clear();
+    it = cache.emplace(key, std::move(b)).first;
+  }
+  std::copy(it->second.begin(), it->second.end(), A.bnd);
+  A.nbnd = Q + 1;
+}
+
 template <int KIND, int DU>
 static cudaError_t launch_wide(WideArgs &A, const float *X, int ldx, const float *norm_w, float eps, void *act,
                                int num_sms, cudaStream_t st, bool x_ready) {
@@ -625,6 +696,10 @@ static cudaError_t launch_wide(WideArgs &A, const float *X, int ldx, const float
   const int64_t split_cost = per + W_RUN_COST * (1 + (per + A.KT - 1) / A.KT);
   const bool whole = tiles <= max_ctas && A.KT <= split_cost;
   const int Q = whole ? (int)tiles : (int)q_split;
+  // four-bit split runs: ranges balanced by cost (a run's read-back blocks the
+  // next run's MMAs; the f16 kernel drains one accumulator while it fills the other)
+  A.nbnd = 0;
+  if (KIND == W_KIND_I4 && !whole && Q <= WIDE_MAX_CTAS && A.units < INT32_MAX) wide_bounds(A, Q, W_RUN_COST);
   const int64_t chunks = (int64_t)A.ntt * A.KT * A.N * 8;
   const int zero_blocks = whole ? 0 : (Q - 1) * WZ_PARTS;
   cudaError_t e;
