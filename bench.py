@@ -42,6 +42,8 @@ import dflash_inputs as di  # noqa: E402
 METRIC = "DFlash2 draft blocks/s and settle rows/s on 1 GB300; % of HBM roofline"
 DEFAULT_WORKLOAD = "settle-heavy"
 SETTLE_CHUNK = 256          # rows a settle call in the step (gpu_cuda/hyb/dflash.rs, SETTLE_MAX)
+COPY_ROWS = 1024            # tap rows a host-to-device copy in the e2e leg (four settle calls)
+E2E_BUFS = 3                # device buffers the e2e leg's copies rotate through
 L2_FLUSH_BYTES = 256 << 20
 REJECT = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown")
 
@@ -567,8 +569,10 @@ def run_gb300(args):
 
 def e2e(b, steps):
     """Through the public API from pinned host memory: inputs in, tokens out, every step. The
-    taps go up in settle-sized chunks on a copy stream into two device buffers, each chunk's
-    settle waiting for its own copy only, so that the copies overlap the settles."""
+    taps go up in pieces of COPY_ROWS rows (the first SETTLE_CHUNK rows alone) on a copy stream
+    into E2E_BUFS device buffers, each piece settled in SETTLE_CHUNK-row calls that wait for its
+    own copy only, so that the copies run ahead of the settles (the host link and the settle
+    take about as long)."""
     torch = b.torch
     wl = b.wl
     taps_pin = [torch.from_numpy(t).pin_memory() for t in b.taps_host] if b.settle_in_step else []
@@ -576,25 +580,27 @@ def e2e(b, steps):
     at_pin = torch.tensor(b.anchor_tok, dtype=torch.int32).pin_memory()
     out_pin = torch.empty(wl.batch, b.k, dtype=torch.int32).pin_memory()
     tw = b.g.tap_width
-    bufs = [torch.empty(SETTLE_CHUNK, tw, dtype=torch.float32, device=b.dev) for _ in range(2)]
+    bufs = [torch.empty(COPY_ROWS, tw, dtype=torch.float32, device=b.dev) for _ in range(E2E_BUFS)]
     h_dev = torch.empty_like(h_pin, device=b.dev)
     at_dev = torch.empty_like(at_pin, device=b.dev)
     h2d = sum(t.numel() * 4 for t in taps_pin) + h_pin.numel() * 4 + at_pin.numel() * 4
     d2h = out_pin.numel() * 4
     comp = torch.cuda.current_stream()
     copy = torch.cuda.Stream()
-    copied = [torch.cuda.Event() for _ in range(2)]
-    freed = [torch.cuda.Event() for _ in range(2)]
+    copied = [torch.cuda.Event() for _ in range(E2E_BUFS)]
+    freed = [torch.cuda.Event() for _ in range(E2E_BUFS)]
 
     def one():
         i = 0
         for s, tp in enumerate(taps_pin):
             b.d.reset(s, 0)
-            for r in range(0, tp.shape[0], SETTLE_CHUNK):
-                m = min(SETTLE_CHUNK, tp.shape[0] - r)
-                k = i % 2
+            r = 0
+            while r < tp.shape[0]:
+                # the first piece small, so that the settles start early
+                m = min(SETTLE_CHUNK if r == 0 else COPY_ROWS, tp.shape[0] - r)
+                k = i % E2E_BUFS
                 with torch.cuda.stream(copy):
-                    if i >= 2:
+                    if i >= E2E_BUFS:
                         copy.wait_event(freed[k])
                     bufs[k][:m].copy_(tp[r:r + m], non_blocking=True)
                     copied[k].record(copy)
@@ -602,6 +608,7 @@ def e2e(b, steps):
                 b.d.settle(s, r, bufs[k][:m], chunk=SETTLE_CHUNK)
                 freed[k].record(comp)
                 i += 1
+                r += m
         h_dev.copy_(h_pin, non_blocking=True)
         at_dev.copy_(at_pin, non_blocking=True)
         b.d.draft(b.anchors, h_dev, at_dev, b.k, b.width, out=(b.logits, b.hp, b.chosen, b.plain))

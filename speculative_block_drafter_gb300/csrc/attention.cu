@@ -114,7 +114,8 @@ bool byte_map(CUtensorMap *m, const void *base, int rank, const uint64_t *dims, 
 // cores with everything the products need in tensor memory (512 columns, one
 // CTA an SM; lanes = query rows, the Q real ones first, the rest zero):
 //   QH, QL   the queries as f16 hi/lo planes (the A operand of S = Q K^T)
-//   S0, S1   two score buffers (64 columns each)
+//   SA, SB   the scores' two partial sums (64 columns each): the products
+//            over the first and over the second half of the head dimension
 //   P0, P1   two probability buffers, hi and lo planes (A of O += P V)
 //   O        the output accumulator (HD columns)
 // The context caches and the block's own K/V hold f16 values in PL planes per
@@ -122,17 +123,22 @@ bool byte_map(CUtensorMap *m, const void *base, int rank, const uint64_t *dims, 
 // were settled or projected.
 //   warp 8    tensor copies of each chunk's K and V planes (boxes of 64 rows x
 //             64 halves, 128-byte swizzled) into a ring of stages
-//   warp 9    the score MMAs, one thread: S = Qh Kh + Qh Kl + Ql Kh (PL = 2)
-//             or Qh K + Ql K (PL = 1), K read K-major from the stage
+//   warps 9, 11  the score MMAs, one thread each, one half of the head
+//             dimension each into its partial sum: S = Qh Kh + Qh Kl + Ql Kh
+//             (PL = 2) or Qh K + Ql K (PL = 1), K read K-major from the stage.
+//             A chunk's partials are taken once the softmax has read the
+//             previous chunk's
 //   warp 10   the output MMAs, one thread: once the chunk's P is written,
 //             O += Ph Vh + Ph Vl + Pl Vh (or Ph V + Pl V), V read MN-major from
 //             the same stage. An MMA holds its issuing thread for about 150
-//             cycles whatever its N, so the two kinds are issued side by side;
-//             the softmax of one chunk runs while the next chunk's scores are
-//             taken. A stage is released by both threads' commits.
+//             cycles whatever its N, so the MMAs are spread over three
+//             threads; the softmax of one chunk runs while the next chunk's
+//             scores are taken. A stage is released by the three threads'
+//             commits.
 //   warps 0-7 two threads a query row, each with half of a chunk's keys (warp w
 //             takes the rows of tensor-memory lanes 32 (w % 4).. and key half
-//             w / 4): the scores from tensor memory, the window mask, the row's
+//             w / 4): the scores from tensor memory (the two partials added),
+//             the window mask, the row's
 //             largest score exchanged with the partner through shared memory,
 //             an online softmax, P as hi/lo planes into tensor memory; at the
 //             end the row's (o, m, l) to the partials. Warps whose rows are all
@@ -147,7 +153,7 @@ bool byte_map(CUtensorMap *m, const void *base, int rank, const uint64_t *dims, 
 template <int HD, int PL>
 struct AttnTc {
   static constexpr int QH = 0, QL = HD / 2;          // HD/2 columns a plane (f16 pairs)
-  static constexpr int S0 = HD;                      // + 64 * buffer
+  static constexpr int S0 = HD;                      // + 64 * partial
   static constexpr int P0 = HD + 128;                // + 64 * buffer: hi 32 columns, lo 32 columns
   static constexpr int OC = HD + 256;                // HD columns
   static_assert(OC + HD <= 512, "tensor memory");
@@ -155,13 +161,13 @@ struct AttnTc {
   static constexpr int REGION = (HD / 64) * BOX;     // one plane of K or V of a chunk
   static constexpr int STAGE = 2 * PL * REGION;      // K planes, then V planes
   static constexpr int STAGES = (192 * 1024) / STAGE < 6 ? (192 * 1024) / STAGE : 6;
-  // kvfull, kvempty (a stage each), qfull, sfull[2], sfree[2], pfull[2], pfree[2], obar, fin
+  // kvfull, kvempty (a stage each), qfull, sfull, sfree (+1 unused each), pfull[2], pfree[2], obar, fin
   static constexpr int NBAR = 2 * STAGES + 11;
   // + alignment, barriers, the tensor-memory address; and 20 KB past them that no
   // operand descriptor of the last stage can reach beyond
   static constexpr size_t BYTES = (size_t)STAGES * STAGE + 1024 + 8 * NBAR + 16 + 20 * 1024;
 };
-constexpr int ATT_TC_THREADS = 352;
+constexpr int ATT_TC_THREADS = 384;
 constexpr int ATT_SM_THREADS = 256;  // the softmax warps 0-7
 constexpr float ATT_TAU = 11.f;      // P <= 2^11 between rescales
 
@@ -229,17 +235,17 @@ __global__ void __launch_bounds__(ATT_TC_THREADS, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < S; ++i) {
       mbar_init(kvfull + 8 * i, 1);
-      mbar_init(kvempty + 8 * i, 2);  // released by the Q K and the P V products
+      mbar_init(kvempty + 8 * i, 3);  // released by the two halves' Q K and the P V products
     }
     mbar_init(qfull, 128);
+    mbar_init(sfull, 2);               // both partials of a chunk's scores
+    mbar_init(sfree, ATT_SM_THREADS);  // read by the softmax
     for (int i = 0; i < 2; ++i) {
-      mbar_init(sfull + 8 * i, 1);
-      mbar_init(sfree + 8 * i, ATT_SM_THREADS);
       mbar_init(pfull + 8 * i, ATT_SM_THREADS);
       mbar_init(pfree + 8 * i, 1);
     }
     mbar_init(obar, 1);
-    mbar_init(fin, 2);  // the two issuing threads' last commits
+    mbar_init(fin, 3);  // the three issuing threads' last commits
     mbar_fence_init();
   }
   pdl_wait();
@@ -275,31 +281,35 @@ __global__ void __launch_bounds__(ATT_TC_THREADS, 1)
       // copies of the last stages issued; a bounded wait each)
       for (int j = (issued > S ? issued - S : 0); j < issued; ++j) mbar_wait(kvfull + 8 * (j % S), (j / S) & 1);
     }
-  } else if (warp == 9) {
-    // S = Q K^T of each chunk into score buffer j & 1. An MMA holds its issuing
-    // thread for about 150 cycles whatever its N, so the P V products have a
-    // warp of their own (warp 10).
+  } else if (warp == 9 || warp == 11) {
+    // the partial S_h = Q K^T over half h of the head dimension into its 64
+    // columns. An MMA holds its issuing thread for about 150 cycles whatever
+    // its N, so the scores have two warps and the P V products a third.
     if (lane == 0 && nch > 0) {
+      const int h = warp == 9 ? 0 : 1;
+      constexpr int KS = HD / 32;  // k-steps of a half
       bool ok = mbar_wait(qfull, 0);
       tc_fence_after();
+      const uint32_t dS = tb + C::S0 + h * 64;
       for (int j = 0; j < nch && ok; ++j) {
-        const int st = j % S, sb = j & 1;
+        const int st = j % S;
         if (!mbar_wait_spin(kvfull + 8 * st, (j / S) & 1)) break;
-        if (j >= 2 && !mbar_wait_spin(sfree + 8 * sb, ((j >> 1) - 1) & 1)) break;
+        // the softmax has read the previous chunk's partials
+        if (j >= 1 && !mbar_wait_spin(sfree, (j - 1) & 1)) break;
         tc_fence_after();
         const bool is_own = own && j == nch - 1;
         const uint32_t idesc = f16_idesc(128, is_own ? 16 : CH);
         const uint32_t kh = ring + st * C::STAGE, kl = kh + C::REGION;
-        const uint32_t dS = tb + C::S0 + sb * 64;
 #pragma unroll
-        for (int ks = 0; ks < HD / 16; ++ks) {
+        for (int kk = 0; kk < KS; ++kk) {
+          const int ks = h * KS + kk;
           const uint32_t off = (ks >> 2) * C::BOX + (ks & 3) * 32;
-          mma_ts(dS, tb + C::QH + ks * 8, sw128_desc(kh + off), idesc, ks > 0);
+          mma_ts(dS, tb + C::QH + ks * 8, sw128_desc(kh + off), idesc, kk > 0);
           if (PL == 2) mma_ts(dS, tb + C::QH + ks * 8, sw128_desc(kl + off), idesc, 1);
           mma_ts(dS, tb + C::QL + ks * 8, sw128_desc(kh + off), idesc, 1);
         }
-        mma_commit(sfull + 8 * sb);
-        mma_commit(kvempty + 8 * st);  // K read (the stage's other release: P V)
+        mma_commit(sfull);
+        mma_commit(kvempty + 8 * st);  // K read (the stage's other releases: the other half, P V)
       }
       // every MMA of this thread completed before the tensor memory is freed
       mma_commit(fin);
@@ -370,15 +380,22 @@ __global__ void __launch_bounds__(ATT_TC_THREADS, 1)
       const int cnt = is_own ? R : min(CH, n - kb);
       const int N = is_own ? 16 : CH;
       const int k0 = kh * 32;  // this thread's keys k0 .. k0 + 31 of the chunk
-      bool w_ok = __all_sync(0xffffffffu, mbar_wait_spin(sfull + 8 * sb, (j >> 1) & 1));
+      bool w_ok = __all_sync(0xffffffffu, mbar_wait_spin(sfull, j & 1));
       tc_fence_after();
       // raw scores of the visible keys [kmin, kmax) of the chunk, -inf elsewhere
       float x[32];
       float mh = -INFINITY;
       if (!dead && w_ok) {
+        // the two partial sums of the scores
         uint32_t r0[32];
-        tmem_ld32(tb + lrow + C::S0 + sb * 64 + k0, r0);
+        tmem_ld32(tb + lrow + C::S0 + k0, r0);
         tc_wait_ld();
+#pragma unroll
+        for (int e = 0; e < 32; ++e) x[e] = __uint_as_float(r0[e]);
+        tmem_ld32(tb + lrow + C::S0 + 64 + k0, r0);
+        tc_wait_ld();
+#pragma unroll
+        for (int e = 0; e < 32; ++e) r0[e] = __float_as_uint(x[e] + __uint_as_float(r0[e]));
         const int kmax = live ? cnt : 0;
         int kmin = 0;
         if (!is_own && window > 0) {
@@ -401,7 +418,7 @@ __global__ void __launch_bounds__(ATT_TC_THREADS, 1)
         }
       }
       tc_fence_before();
-      mbar_arrive(sfree + 8 * sb);
+      mbar_arrive(sfree);
       // keys past the chunk's end: their V rows zeroed before the P.V products read them
       if (cnt < N && w_ok) {
         const int nz = N - cnt;
