@@ -3,12 +3,15 @@
 //
 // At these sizes a 128-row weight tile meets up to 256 tokens in one MMA
 // (M = 128, N = tokens, K = 16), so the weights are no longer the whole cost:
-// the work is split evenly over the SMs ("stream-K"). The (token tile, row
-// tile, 64-column k-tile) units of all matrices are laid end to end and each
-// CTA takes one contiguous run. Wherever the run crosses a row tile, the CTA
-// adds its partial sums into Y with atomics (Y is cleared first). When the
-// tiles about fill the resident CTAs, each CTA takes one whole tile instead
-// (launch_wide), which splits none. Every CTA bulk-copies its own operands.
+// the work is split over the SMs ("stream-K"). The (token tile, row tile,
+// 64-column k-tile) units of all matrices are laid end to end and each CTA
+// takes one contiguous range of them, in runs that each stay inside one tile.
+// A run over part of a tile adds its partial sums into Y with atomics (Y is
+// cleared first). The f16 kernel's ranges are equal; the four-bit kernel's
+// are equal in cost, a run's read-back of its one accumulator counted as a
+// few units (wide_bounds). When the tiles about fill the resident CTAs, each
+// CTA takes one whole tile instead (launch_wide), which splits none. Every
+// CTA bulk-copies its own operands.
 //
 //   warp 4      bulk-copies each unit's operands into a shared-memory ring
 //   warp 5      issues the MMAs (one thread)
